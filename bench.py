@@ -1,0 +1,589 @@
+#!/usr/bin/env python
+"""Benchmark of the CPR Gated DeltaNet hot path on one GB300 (or N independent GPUs).
+
+One step = the whole hot path over the prefill workload (4 sequences x 4096 tokens,
+16 query/key heads shared by 32 value heads, d = 128, C = 64, bf16 inputs):
+    1. rollout prefill with a decode cache          (work list, boundary pass, chunks)
+    2. 64 decode steps continuing those 4 sequences (one resynchronisation each),
+       replayed from a CUDA graph
+    3. trainer forward + backward on the same 16384 tokens
+Tokens per step = 16384 (prefill) + 4 x 64 (decode) + 16384 (trainer).  `value` is
+tokens/s over the whole step with inputs resident in HBM.  Per-stage times, a
+256-slot decode measurement (the decode workload's shape: 256 x 32 heads of d = 128
+states, 64 steps with one resync), per-kernel rooflines from CUDA events recorded by the
+library on its launching stream, the end-to-end number through host buffers and the fp64
+oracle timed on the host cores are reported in the same JSON line.
+
+--impl reference times the fp64 CPU oracle (the only reference this operator has) on a
+bounded sample of the same workload per step.
+
+Multi-GPU: one process per GPU (torchrun).  Every rank runs its own copy of the workload
+(independent sequences, no collective on the data path: weak scaling); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CPR GDN prefill & fwd+bwd tokens/s, decode µs/step; % HBM/TC roofline"
+UNIT = "tokens/s"
+WORKLOAD = "prefill"
+DECODE_STEPS = 64
+DECODE_SLOTS_BIG = 256
+PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
+
+
+# ------------------------------------------------------------------ utilities ----
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(PEAK_FALLBACK), "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def shard_seed(rank: int) -> int:
+    """Weak scaling: every rank draws its own independent copy of the workload."""
+    return 1000 * rank
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max over ranks (the slowest rank defines the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+        return False
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append(parts)
+        if self.bus_id:
+            mine = [r for r in rows if r[1].lower().endswith(self.bus_id[-12:])]
+            rows = mine or rows
+        if rows:
+            idx0 = rows[0][0]
+            rows = [r for r in rows if r[0] == idx0]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        mx = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max((num(r[4]) or 0.0) for r in rows)}
+
+
+# ------------------------------------------------------------- CPU baseline ----
+def oracle_rates(x, hv, fwd_tokens: int, bwd_tokens: int, threads: int):
+    """Time the fp64 oracle (as it stands) on the first `fwd_tokens` / `bwd_tokens` tokens
+    of the first sequence, all value heads.  Returns token-heads/s for forward and for
+    backward (the backward recomputes its own forward)."""
+    import oracle
+    from gated_deltanet_cpr_gb300.synth import as_f64 as f
+
+    def sl(n, L):
+        return f(x[n][:L])
+
+    t0 = time.perf_counter()
+    oracle.fwd(sl("q", fwd_tokens), sl("k", fwd_tokens), sl("v", fwd_tokens), sl("g", fwd_tokens),
+               sl("beta", fwd_tokens), [0, fwd_tokens], n_threads=threads)
+    t_fwd = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.bwd(sl("q", bwd_tokens), sl("k", bwd_tokens), sl("v", bwd_tokens), sl("g", bwd_tokens),
+               sl("beta", bwd_tokens), [0, bwd_tokens], sl("dout", bwd_tokens), n_threads=threads)
+    t_bwd = time.perf_counter() - t0
+    return fwd_tokens * hv / t_fwd, bwd_tokens * hv / t_bwd, t_fwd + t_bwd
+
+
+def step_tokens(w):
+    T = w.total_tokens
+    n_seq = len(w.lengths)
+    return {"prefill": T, "decode": n_seq * DECODE_STEPS, "trainer": T}
+
+
+def oracle_step_estimate(w, rate_fwd, rate_bwd):
+    """Seconds the oracle would take for one whole step (linear in token-heads)."""
+    tk = step_tokens(w)
+    hv = w.h_v
+    return ((tk["prefill"] + tk["decode"]) * hv / rate_fwd
+            + tk["trainer"] * hv * (1.0 / rate_fwd + 1.0 / rate_bwd))
+
+
+def threads_available():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference ----
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from gated_deltanet_cpr_gb300 import synth
+
+    w = synth.workloads()[WORKLOAD]
+    x = synth.make_inputs(w.lengths[:1], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0, dout=True)
+    threads = threads_available()
+    fwd_tok, bwd_tok = 512, 256
+    times = []
+    for i in range(args.warmup + args.steps):
+        rf, rb, dt = oracle_rates(x, w.h_v, fwd_tok, bwd_tok, threads)
+        if i >= args.warmup:
+            times.append((rf, rb, dt))
+    rf = statistics.median(t[0] for t in times)
+    rb = statistics.median(t[1] for t in times)
+    est = oracle_step_estimate(w, rf, rb)
+    tk = sum(step_tokens(w).values())
+    value = tk / est
+    sample = (f"per step: oracle fwd on {fwd_tok} tokens x {w.h_v} heads and oracle bwd on "
+              f"{bwd_tok} tokens x {w.h_v} heads of sequence 0; whole-step time extrapolated "
+              f"linearly in token-heads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "tokens_per_step": tk},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- CUDA arm ----
+def run_cuda(args):
+    import torch
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from gated_deltanet_cpr_gb300 import api, synth
+
+    api.load()
+    P, peak_kind = peaks()
+    w = synth.workloads()[WORKLOAD]
+    C, d, hqk, hv = w.chunk, w.d, w.h_qk, w.h_v
+    nseq = len(w.lengths)
+    seed = shard_seed(rank)
+    x = synth.make_inputs(w.lengths, hqk, hv, d, dtype=w.dtype, seed=seed, dout=True)
+    # decode tokens (one per sequence per step)
+    xd = synth.make_inputs([DECODE_STEPS * nseq], hqk, hv, d, dtype=w.dtype, seed=seed + 7)
+    host = {n: x[n].pin_memory() for n in ("q", "k", "v", "g", "beta", "dout", "cu_seqlens")}
+    t = {n: host[n].to(dev) for n in host}
+    dq_in = {n: xd[n].view(DECODE_STEPS, nseq, *xd[n].shape[1:]).contiguous().to(dev)
+             for n in ("q", "k", "v", "g", "beta")}
+    cu_host = x["cu_seqlens"]
+    T = w.total_tokens
+    stream = torch.cuda.current_stream(dev)
+
+    # resident buffers
+    shp = api.make_shape(nseq, T, hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
+    ws_pre = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_PREFILL, cu_host), dev)
+    ws_fwd = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_FWD, cu_host), dev)
+    have_bwd = True
+    try:
+        ws_bwd = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_BWD, cu_host), dev)
+    except api.GdnError:
+        have_bwd = False
+        ws_bwd = None
+    dshp = api.make_shape(nseq, nseq, hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
+    ws_dec = api.alloc_workspace(api.workspace_bytes(dshp, api.MODE_DECODE), dev)
+    cache = api.Cache(nseq, hqk, hv, d, C, dtype=torch.bfloat16, device=dev)
+    o_pre = torch.empty((T, hv, d), dtype=torch.bfloat16, device=dev)
+    st_pre = torch.empty((nseq, hv, d, d), dtype=torch.float32, device=dev)
+    o_fwd = torch.empty_like(o_pre)
+    st_fwd = torch.empty_like(st_pre)
+    n_chunks = sum((L + C - 1) // C for L in w.lengths)
+    saved = torch.empty((n_chunks, hv, d, d), dtype=torch.float32, device=dev)
+    o_dec = torch.empty((DECODE_STEPS, nseq, hv, d), dtype=torch.bfloat16, device=dev)
+    slots = torch.arange(nseq, dtype=torch.int32, device=dev)
+    grads = None
+
+    def prefill_call():
+        api.prefill(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], chunk=C,
+                    cache=cache, cu_seqlens_host=cu_host, ws=ws_pre, o=o_pre, state_out=st_pre)
+
+    def decode_call(i):
+        api.decode_step(dq_in["q"][i], dq_in["k"][i], dq_in["v"][i], dq_in["g"][i],
+                        dq_in["beta"][i], slots, cache, ws=ws_dec, o=o_dec[i])
+
+    def trainer_call():
+        nonlocal grads
+        api.fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], chunk=C,
+                cu_seqlens_host=cu_host, ws=ws_fwd, o=o_fwd, state_out=st_fwd, saved_bnd=saved)
+        if have_bwd:
+            grads = api.bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], saved,
+                            t["dout"], chunk=C, cu_seqlens_host=cu_host, ws=ws_bwd,
+                            want_dstate_in=False)
+
+    # the 64 decode steps as one CUDA graph (fixed pointers, device-side resync decision)
+    prefill_call()
+    for i in range(2):
+        decode_call(i)
+    torch.cuda.synchronize(dev)
+    with api.Profiler(2) as cap_prof:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(DECODE_STEPS):
+                decode_call(i)
+    decode_kernels_per_replay = cap_prof.kernels
+
+    tokens = step_tokens(w)
+    step_tok = sum(tokens.values()) if have_bwd else tokens["prefill"] + tokens["decode"] + tokens["trainer"]
+
+    def one_step(prof_pre, prof_fwd, ev):
+        ev[0].record(stream)
+        with prof_pre:
+            prefill_call()
+        ev[1].record(stream)
+        graph.replay()
+        ev[2].record(stream)
+        with prof_fwd:
+            trainer_call()
+        ev[3].record(stream)
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        one_step(api.Profiler(6), api.Profiler(12), [mk() for _ in range(4)])
+    torch.cuda.synchronize(dev)
+
+    profs = [(api.Profiler(6), api.Profiler(12), [mk() for _ in range(4)]) for _ in range(args.steps)]
+    start, end = mk(), mk()
+    bus = getattr(torch.cuda.get_device_properties(dev), "pci_bus_id", None)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(None if bus is None else str(bus)) as clk:
+        start.record(stream)
+        for pp, pf, ev in profs:
+            one_step(pp, pf, ev)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = reduce_max(ms_local, world)
+    value = world * step_tok / (ms * 1e-3)
+    launches = sum(pp.kernels + pf.kernels for pp, pf, _ in profs) + args.steps * decode_kernels_per_replay
+
+    stage_ms = {"prefill": statistics.mean(ev[0].elapsed_time(ev[1]) for _, _, ev in profs),
+                "decode_64_steps": statistics.mean(ev[1].elapsed_time(ev[2]) for _, _, ev in profs),
+                "trainer_fwd_bwd": statistics.mean(ev[2].elapsed_time(ev[3]) for _, _, ev in profs)}
+    pre_k = [pp.stage_ms() for pp, _, _ in profs]
+    names = ["worklist", "boundary_prepass", "boundary_chain", "intra_chunk", "cache_tail"]
+    kern = {n: statistics.mean(s[i] for s in pre_k) for i, n in enumerate(names) if all(len(s) > i for s in pre_k)}
+
+    # dominant kernel: intra-chunk recurrence (FP32 ALU bound)
+    intra_ms = kern["intra_chunk"]
+    flops_intra = T * hv * 7 * d * d  # per token-head: d^2 MUL + 3 d^2 FMA (FMA = 2 FLOP)
+    alu_peak = 2 * SMS * FP32_LANES * SM_MAX_MHZ * 1e6 / 1e12
+    ach_intra = flops_intra / (intra_ms * 1e-3) / 1e12
+    roofline = {"bound": "alu", "kernel": "k_intra (intra-chunk recurrence)", "achieved": ach_intra,
+                "peak": alu_peak, "unit": "TFLOP/s", "frac": ach_intra / alu_peak, "traffic": None,
+                "peak_note": "FP32 FMA peak 2 x 152 SMs x 128 lanes x 2070 MHz; this op mix "
+                             "(1 MUL + 3 FMA per state element) caps frac at 7/8"}
+    chunk_heads_full = sum(L // C for L in w.lengths) * hv
+    flops_bnd = chunk_heads_full * (6 * C * C * d + 4 * C * d * d)
+    bnd_ms = kern["boundary_prepass"] + kern["boundary_chain"]
+    tc_peak = float(P.get("bf16_tflops", PEAK_FALLBACK["bf16_tflops"]))
+    boundary = {"bound": "tensor", "achieved": flops_bnd / (bnd_ms * 1e-3) / 1e12, "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": flops_bnd / (bnd_ms * 1e-3) / 1e12 / tc_peak,
+                "note": "boundary pass (pre-pass + chain) runs on FP32 SIMT in this build"}
+
+    # 256-slot decode (the decode workload's state shape), graph-replayed and per kernel
+    dec = bench_decode_big(api, synth, torch, dev, w, P, seed)
+
+    # end to end through host buffers: H2D inputs each step, D2H results each step
+    e2e = bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call,
+                    t, dq_in, o_pre, o_dec, lambda: grads, step_tok, world)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) inputs, q/k L2-normalised, beta=sigmoid, g=-softplus)",
+            "config": {"workload": w.name, "tokens_per_step": step_tok, "stages": tokens,
+                       "l2": "inputs larger than L2 (step working set > 2 GB of HBM traffic)",
+                       "bwd_included": have_bwd},
+            "stage_ms": stage_ms, "kernel_ms": kern, "roofline": roofline,
+            "boundary_roofline": boundary, "decode": dec, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk.summary(),
+            "peaks_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = threads_available()
+        rf, rb, dt = oracle_rates(x, hv, 4096, 1024, threads)
+        est = oracle_step_estimate(w, rf, rb)
+        line["cpu_baseline"] = {
+            "value": step_tok / est, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": (f"oracle fwd on 4096 tokens x {hv} heads and oracle bwd on 1024 tokens x "
+                       f"{hv} heads of sequence 0 ({dt:.1f} s wall); whole-step time "
+                       f"extrapolated linearly in token-heads")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_decode_big(api, synth, torch, dev, w, P, seed):
+    """256 slots x 32 heads of 128x128 fp32 states, positions at 2048 (so 64 steps contain one
+    resync at step 63), random resident states and tails."""
+    N, C, d, hqk, hv = DECODE_SLOTS_BIG, w.chunk, w.d, w.h_qk, w.h_v
+    cache = api.Cache(N, hqk, hv, d, C, dtype=torch.bfloat16, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(seed + 11)
+    cache.s_run.normal_(generator=gen).mul_(0.05)
+    cache.s_bnd.copy_(cache.s_run)
+    cache.tail_k.normal_(generator=gen).mul_(0.09)
+    cache.tail_v.normal_(generator=gen)
+    cache.tail_g.uniform_(-1.5, -0.1, generator=gen)
+    cache.tail_beta.uniform_(0.2, 0.8, generator=gen)
+    cache.pos.fill_(2048)
+    xd = synth.make_inputs([DECODE_STEPS * N], hqk, hv, d, dtype=w.dtype, seed=seed + 13)
+    din = {n: xd[n].view(DECODE_STEPS, N, *xd[n].shape[1:]).contiguous().to(dev)
+           for n in ("q", "k", "v", "g", "beta")}
+    slots = torch.arange(N, dtype=torch.int32, device=dev)
+    shp = api.make_shape(N, N, hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
+    ws = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_DECODE), dev)
+    o = torch.empty((DECODE_STEPS, N, hv, d), dtype=torch.bfloat16, device=dev)
+    saved = {n: getattr(cache, n).clone() for n in api.Cache.TENSORS}
+
+    def call(i):
+        api.decode_step(din["q"][i], din["k"][i], din["v"][i], din["g"][i], din["beta"][i],
+                        slots, cache, ws=ws, o=o[i])
+
+    def reset():
+        for n in api.Cache.TENSORS:
+            getattr(cache, n).copy_(saved[n])
+
+    # per-kernel times from the library's stage events (direct launches)
+    reset()
+    per = []
+    for i in range(DECODE_STEPS):
+        prof = api.Profiler(5)
+        with prof:
+            call(i)
+        per.append(prof)
+    torch.cuda.synchronize(dev)
+    stages = [p.stage_ms() for p in per]
+    normal = [s for i, s in enumerate(stages) if i != DECODE_STEPS - 1]
+    step_k3 = statistics.median(s[0] for s in normal)
+    resync_step_ms = sum(stages[-1])
+    # graph replay of all 64 steps
+    reset()
+    call(0)
+    reset()
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(DECODE_STEPS):
+            call(i)
+    times = []
+    for _ in range(3):
+        reset()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    us_per_step = statistics.median(times) * 1e3 / DECODE_STEPS
+    # K3 algorithmic bytes: state read+write, q,k per qk head, v, o, tail appends, g, beta
+    bpe = 2
+    bytes_k3 = (N * hv * d * d * 4 * 2 + N * hqk * d * bpe * 2 + N * hv * d * bpe
+                + N * hv * d * bpe + N * hqk * d * bpe + N * hv * d * bpe + N * hv * 4 * 4)
+    hbm = float(P.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
+    ach = bytes_k3 / (step_k3 * 1e-3) / 1e9
+    return {"slots": N, "heads": hv, "d": d, "steps": DECODE_STEPS,
+            "us_per_step_mean": us_per_step, "us_token_step_kernel_median": step_k3 * 1e3,
+            "us_resync_step": resync_step_ms * 1e3, "tokens_per_s": N / (us_per_step * 1e-6),
+            "roofline": {"bound": "hbm", "kernel": "k_decode (token step)", "achieved": ach,
+                         "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_k3}}
+
+
+def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call, t, dq_in,
+              o_pre, o_dec, get_grads, step_tok, world):
+    """Same step through the public API with host buffers: every step copies its inputs from
+    pinned host memory and reads its results back."""
+    nseq = len(w.lengths)
+    dhost = {n: xd[n].view(DECODE_STEPS, nseq, *xd[n].shape[1:]).contiguous().pin_memory()
+             for n in ("q", "k", "v", "g", "beta")}
+    outs = {"o_prefill": o_pre, "o_decode": o_dec}
+    h2d = sum(v.numel() * v.element_size() for v in host.values()) + \
+        sum(v.numel() * v.element_size() for v in dhost.values())
+
+    def result_tensors():
+        r = dict(outs)
+        gr = get_grads()
+        if gr is not None:
+            for n in ("dq", "dk", "dv", "dg", "dbeta"):
+                r[n] = gr[n]
+        return r
+
+    res_host = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for n, v in result_tensors().items()}
+    d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+
+    def step():
+        for n in host:
+            t[n].copy_(host[n], non_blocking=True)
+        for n in dhost:
+            dq_in[n].copy_(dhost[n], non_blocking=True)
+        prefill_call()
+        graph.replay()
+        trainer_call()
+        for n, v in result_tensors().items():
+            res_host[n].copy_(v, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    return {"value": world * step_tok / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_ncu_case(args):
+    """Small, fixed cases for ncu captures (a few hundred MB on the device):
+    prefill   one 4096-token sequence, 16/32 heads, d=128, C=64, bf16: three prefills
+    decode    64 slots x 32 heads of 128x128 states: three decode steps (no resync)
+    """
+    import torch
+
+    from gated_deltanet_cpr_gb300 import api, synth
+
+    dev = torch.device("cuda", 0)
+    w = synth.workloads()[WORKLOAD]
+    if args.ncu_case == "prefill":
+        x = synth.make_inputs([4096], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0)
+        t = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+        for _ in range(3):
+            api.prefill(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], chunk=w.chunk,
+                        cu_seqlens_host=x["cu_seqlens"])
+    else:
+        N = 64
+        cache = api.Cache(N, w.h_qk, w.h_v, w.d, w.chunk, dtype=torch.bfloat16, device=dev)
+        cache.s_run.normal_()
+        cache.pos.fill_(2048)
+        x = synth.make_inputs([N], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0)
+        t = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+        slots = torch.arange(N, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            cache.pos.fill_(2048)
+            api.decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], slots, cache)
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"ncu_case": args.ncu_case, "ok": True}))
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", choices=["prefill", "decode"], default=None,
+                    help="run a small fixed case for an ncu capture and exit")
+    args = ap.parse_args(argv)
+    if args.ncu_case:
+        return run_ncu_case(args)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_cuda(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

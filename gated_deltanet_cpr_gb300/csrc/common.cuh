@@ -1,0 +1,142 @@
+// common.cuh -- device definitions shared by every CPR kernel.
+//
+// Bit-exactness across prefill, trainer forward and decode rests on two routines that
+// every mode calls with the same operands in the same order:
+//   * token_step  -- one step of the gated delta rule on a state row (the recurrence that
+//                    CPR keeps as its main computation; IsoExec page, section
+//                    "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet");
+//   * the boundary routines (prep_* and chain_*) -- the chunk (WY/UT) form that advances
+//                    a boundary state over one full chunk, used by the prefill boundary
+//                    pass and by the decode resynchronisation every C tokens.
+// All floating-point arithmetic in them is written with explicit round-to-nearest
+// intrinsics (__fmaf_rn, __fmul_rn, __fadd_rn, __fsub_rn), which the compiler never fuses
+// or reorders, and every reduction has one fixed order that depends only on (C, D).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kMaxChunk = 64;
+constexpr int kRowsPerChain = 16;   // state rows per boundary-chain CTA
+constexpr int kPrepThreads = 256;   // boundary pre-pass CTA size
+constexpr int kChainThreads = 256;  // boundary chain CTA size
+
+// ---------------------------------------------------------------- workspace ----
+struct WsHeader {
+  int32_t err;    // gdn_device_error, first error wins
+  int32_t valid;  // 1 once the work list is built and consistent with the host's copy
+  int32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+struct ChunkRec {  // one chunk of one sequence
+  int32_t seq, tok0, len, jloc;
+};
+struct SeqRec {  // one sequence
+  int32_t tok0, len, chunk0, nchunks;
+};
+
+__device__ __forceinline__ void set_error(WsHeader* h, int code) { atomicCAS(&h->err, 0, code); }
+
+// ---------------------------------------------------------------- conversions ----
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 8 consecutive elements -> fp32 (16-byte aligned source)
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* o) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void load8(const float* p, float* o) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+__device__ __forceinline__ void store_out(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// ---------------------------------------------------------------- fixed dot ----
+// Canonical dot product of length D (multiple of 4) over fp32 arrays in shared memory:
+// four partial sums, partial e takes elements 4m+e in ascending m, combined as
+// (p0 + p1) + (p2 + p3).  Every boundary-pass dot uses exactly this order.
+template <int D>
+__device__ __forceinline__ float dot_canon(const float* __restrict__ a, const float* __restrict__ b) {
+  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < D / 4; ++m) {
+    const float4 x = reinterpret_cast<const float4*>(a)[m];
+    const float4 y = reinterpret_cast<const float4*>(b)[m];
+    p0 = __fmaf_rn(x.x, y.x, p0);
+    p1 = __fmaf_rn(x.y, y.y, p1);
+    p2 = __fmaf_rn(x.z, y.z, p2);
+    p3 = __fmaf_rn(x.w, y.w, p3);
+  }
+  return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+}
+
+// ---------------------------------------------------------------- token step ----
+// One gated delta-rule step on row i of the state, held by a pair of adjacent lanes
+// (half = lane & 1).  The pair splits the D columns into float4 groups: register group m
+// holds columns [8m + 4*half, 8m + 4*half + 4).  Order of operations (the recurrence's
+// own order):
+//     S <- a S;   p = S k;   u = beta (v_i - p);   S <- S + u k^T;   o_i = S q
+// Each dot is four partial sums over the lane's columns in ascending m, combined as
+// (p0 + p1) + (p2 + p3), then added to the partner lane's partial with one xor-shuffle;
+// fp32 addition is commutative, so both lanes hold identical bits.  k and q are fp32
+// copies in shared memory (exact widenings of the inputs).  All 32 lanes of the warp must
+// call this together.
+template <int D>
+__device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __restrict__ k_sh,
+                                            const float* __restrict__ q_sh, float a, float beta,
+                                            float v_i, int half) {
+  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < D / 8; ++m) {
+    const float4 kk = *reinterpret_cast<const float4*>(k_sh + 8 * m + 4 * half);
+    S[m].x = __fmul_rn(a, S[m].x);
+    S[m].y = __fmul_rn(a, S[m].y);
+    S[m].z = __fmul_rn(a, S[m].z);
+    S[m].w = __fmul_rn(a, S[m].w);
+    p0 = __fmaf_rn(S[m].x, kk.x, p0);
+    p1 = __fmaf_rn(S[m].y, kk.y, p1);
+    p2 = __fmaf_rn(S[m].z, kk.z, p2);
+    p3 = __fmaf_rn(S[m].w, kk.w, p3);
+  }
+  float part = __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+  const float p = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
+  const float u = __fmul_rn(beta, __fsub_rn(v_i, p));
+  p0 = p1 = p2 = p3 = 0.f;
+#pragma unroll
+  for (int m = 0; m < D / 8; ++m) {
+    const float4 kk = *reinterpret_cast<const float4*>(k_sh + 8 * m + 4 * half);
+    const float4 qq = *reinterpret_cast<const float4*>(q_sh + 8 * m + 4 * half);
+    S[m].x = __fmaf_rn(u, kk.x, S[m].x);
+    S[m].y = __fmaf_rn(u, kk.y, S[m].y);
+    S[m].z = __fmaf_rn(u, kk.z, S[m].z);
+    S[m].w = __fmaf_rn(u, kk.w, S[m].w);
+    p0 = __fmaf_rn(S[m].x, qq.x, p0);
+    p1 = __fmaf_rn(S[m].y, qq.y, p1);
+    p2 = __fmaf_rn(S[m].z, qq.z, p2);
+    p3 = __fmaf_rn(S[m].w, qq.w, p3);
+  }
+  part = __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+  return __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
+}
+
+// State row i, half h: global float offset of register group m.
+template <int D>
+__device__ __forceinline__ int state_col(int m, int half) {
+  return 8 * m + 4 * half;
+}
+
+}  // namespace gdn

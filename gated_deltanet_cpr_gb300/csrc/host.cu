@@ -1,0 +1,379 @@
+// host.cu -- the C ABI of include/gdn_cpr.h: argument checks, workspace layout and the
+// launch sequence of every mode.  The host never touches tensor data; it only reads the
+// caller's host copy of cu_seqlens to size grids and the workspace.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/gdn_cpr.h"
+#include "launch.h"
+
+#define GDN_VERSION_NUM 100  // 0.1.0
+
+namespace {
+using namespace gdn;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline bool ok_ptr(const void* p, size_t a) { return p != nullptr && aligned(p, a); }
+
+gdn_status check_shape(const gdn_cpr_shape* s) {
+  if (!s) return GDN_ERR_INVALID_ARG;
+  if (s->num_seqs < 0 || s->total_tokens < 0 || s->h_qk <= 0 || s->h_v <= 0 || s->d_k <= 0 ||
+      s->d_v <= 0 || s->chunk <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (s->h_v % s->h_qk != 0) return GDN_ERR_UNSUPPORTED;
+  if (s->d_k != s->d_v) return GDN_ERR_UNSUPPORTED;
+  if (s->d_k != 32 && s->d_k != 64 && s->d_k != 128) return GDN_ERR_UNSUPPORTED;
+  if (s->chunk != 16 && s->chunk != 32 && s->chunk != 64) return GDN_ERR_UNSUPPORTED;
+  if ((s->in_dtype != GDN_F32 && s->in_dtype != GDN_BF16) ||
+      (s->out_dtype != GDN_F32 && s->out_dtype != GDN_BF16))
+    return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+// Host copy of cu_seqlens: checks it and returns the chunk count and the hash the
+// work-list kernel compares the device copy against.
+gdn_status scan_cu(const gdn_cpr_shape* s, const int32_t* cu, int64_t* n_chunks, uint32_t* hash) {
+  const int N = s->num_seqs;
+  if (!cu) return GDN_ERR_INVALID_ARG;
+  if (cu[0] != 0 || cu[N] != s->total_tokens) return GDN_ERR_INVALID_ARG;
+  int64_t nc = 0;
+  uint32_t h = 0;
+  for (int i = 0; i <= N; ++i) {
+    if (i < N && cu[i + 1] < cu[i]) return GDN_ERR_INVALID_ARG;
+    h += (uint32_t)cu[i] * (uint32_t)(2 * i + 1);
+    if (i < N) nc += (cu[i + 1] - cu[i] + s->chunk - 1) / s->chunk;
+  }
+  *n_chunks = nc;
+  *hash = h;
+  return GDN_OK;
+}
+
+Dims dims_of(const gdn_cpr_shape* s) {
+  Dims d;
+  d.hqk = s->h_qk;
+  d.hv = s->h_v;
+  d.D = s->d_k;
+  d.C = s->chunk;
+  d.in_bf16 = s->in_dtype == GDN_BF16;
+  d.out_bf16 = s->out_dtype == GDN_BF16;
+  return d;
+}
+
+// ------------------------------------------------------------- layouts ----
+struct FwdLayout {
+  size_t chunks, seqs, W, U, gamma, bnd, total;
+};
+
+FwdLayout fwd_layout(const gdn_cpr_shape* s, int64_t n_chunks, bool own_bnd) {
+  const size_t D = s->d_k, C = s->chunk, hv = s->h_v;
+  FwdLayout L;
+  size_t off = align_up(sizeof(WsHeader));
+  L.chunks = off; off = align_up(off + sizeof(ChunkRec) * (size_t)n_chunks);
+  L.seqs = off;   off = align_up(off + sizeof(SeqRec) * (size_t)s->num_seqs);
+  L.W = off;      off = align_up(off + sizeof(float) * (size_t)n_chunks * hv * C * D);
+  L.U = off;      off = align_up(off + sizeof(float) * (size_t)n_chunks * hv * C * D);
+  L.gamma = off;  off = align_up(off + sizeof(float) * (size_t)n_chunks * hv);
+  L.bnd = off;
+  if (own_bnd) off = align_up(off + sizeof(float) * (size_t)n_chunks * hv * D * D);
+  L.total = off;
+  return L;
+}
+
+struct DecLayout {
+  size_t W, U, gamma, total;
+};
+
+DecLayout dec_layout(const gdn_cpr_shape* s) {
+  const size_t D = s->d_k, C = s->chunk, hv = s->h_v, N = s->num_seqs;
+  DecLayout L;
+  size_t off = align_up(sizeof(WsHeader));
+  L.W = off;     off = align_up(off + sizeof(float) * N * hv * C * D);
+  L.U = off;     off = align_up(off + sizeof(float) * N * hv * C * D);
+  L.gamma = off; off = align_up(off + sizeof(float) * N * hv);
+  L.total = off;
+  return L;
+}
+
+inline char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
+
+gdn_status check_cache(const gdn_cpr_cache* c) {
+  if (!c) return GDN_ERR_INVALID_ARG;
+  if (c->slots <= 0) return GDN_ERR_INVALID_ARG;
+  if (!ok_ptr(c->s_run, 16) || !ok_ptr(c->s_bnd, 16) || !ok_ptr(c->tail_k, 16) ||
+      !ok_ptr(c->tail_v, 16) || !ok_ptr(c->tail_g, 4) || !ok_ptr(c->tail_beta, 4) ||
+      !ok_ptr(c->pos, 4))
+    return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+thread_local gdn_cpr_profile* t_profile = nullptr;
+
+// Stage marker of the profiling hook: event `stage` after the stage's kernels, and the
+// count of kernels those stages launched.
+struct Stages {
+  cudaStream_t st;
+  int next = 0;
+  explicit Stages(cudaStream_t s) : st(s) {
+    if (t_profile) t_profile->stages = 0;
+    mark(0);
+  }
+  void mark(int kernels) {
+    if (!t_profile) return;
+    t_profile->kernels += kernels;
+    if (next < t_profile->n_events && next < 16 && t_profile->events[next]) {
+      cudaEventRecord(static_cast<cudaEvent_t>(t_profile->events[next]), st);
+      t_profile->stages = next + 1;
+    }
+    ++next;
+  }
+};
+
+gdn_status finish(cudaStream_t st) {
+  (void)st;
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+// Forward path shared by prefill and the trainer forward (same kernels, same order).
+gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* state_in,
+                       const int32_t* cu_dev, const int32_t* cu_host, void* o, float* state_out,
+                       const gdn_cpr_cache* cache, const int32_t* slot_of_seq, float* saved_bnd,
+                       void* ws, size_t ws_bytes, cudaStream_t st) {
+  gdn_status rc = check_shape(shape);
+  if (rc != GDN_OK) return rc;
+  int64_t n_chunks = 0;
+  uint32_t hash = 0;
+  rc = scan_cu(shape, cu_host, &n_chunks, &hash);
+  if (rc != GDN_OK) return rc;
+  const int N = shape->num_seqs;
+  const int64_t T = shape->total_tokens;
+  if (T > 0 && (!ok_ptr(q, 16) || !ok_ptr(k, 16) || !ok_ptr(v, 16) || !ok_ptr(g, 4) ||
+                !ok_ptr(beta, 4) || !ok_ptr(o, 16)))
+    return GDN_ERR_INVALID_ARG;
+  if (N > 0 && !ok_ptr(cu_dev, 4)) return GDN_ERR_INVALID_ARG;
+  if (state_in && !aligned(state_in, 16)) return GDN_ERR_INVALID_ARG;
+  if (state_out && !aligned(state_out, 16)) return GDN_ERR_INVALID_ARG;
+  if (saved_bnd && !aligned(saved_bnd, 16)) return GDN_ERR_INVALID_ARG;
+  if (cache) {
+    rc = check_cache(cache);
+    if (rc != GDN_OK) return rc;
+    if (slot_of_seq && !aligned(slot_of_seq, 4)) return GDN_ERR_INVALID_ARG;
+    if (!slot_of_seq && N > cache->slots) return GDN_ERR_INVALID_ARG;
+  }
+  const FwdLayout L = fwd_layout(shape, n_chunks, saved_bnd == nullptr);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if (N == 0) return GDN_OK;
+
+  const Dims d = dims_of(shape);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  ChunkRec* chunks = reinterpret_cast<ChunkRec*>(at(ws, L.chunks));
+  SeqRec* seqs = reinterpret_cast<SeqRec*>(at(ws, L.seqs));
+  float* W = reinterpret_cast<float*>(at(ws, L.W));
+  float* U = reinterpret_cast<float*>(at(ws, L.U));
+  float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
+  float* bnd = saved_bnd ? saved_bnd : reinterpret_cast<float*>(at(ws, L.bnd));
+  TokenArrays in{q, k, v, g, beta};
+
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
+  Stages stg(st);
+  launch_worklist(cu_dev, N, (int)T, d.C, n_chunks, hash, chunks, seqs, hdr, st);
+  stg.mark(1);
+
+  PrepWork pw{};
+  pw.chunks = chunks;
+  pw.n_items = n_chunks;
+  launch_prep(d, in, pw, W, U, gamma, hdr, st);
+  stg.mark(n_chunks > 0 ? 1 : 0);
+
+  ChainWork cw{};
+  cw.seqs = seqs;
+  cw.N = N;
+  cw.state_in = state_in;
+  cw.bnd = bnd;
+  cw.state_out = state_out;
+  if (cache) {
+    cw.cache_bnd = cache->s_bnd;
+    cw.cache_run = cache->s_run;
+    cw.cache_slots = cache->slots;
+    cw.slot_of_seq = slot_of_seq;
+  }
+  launch_chain(d, k, W, U, gamma, cw, hdr, st);
+  stg.mark(1);
+
+  IntraWork iw{};
+  iw.chunks = chunks;
+  iw.seqs = seqs;
+  iw.n_chunks = n_chunks;
+  iw.bnd = bnd;
+  iw.o = o;
+  iw.state_out = state_out;
+  if (cache) {
+    iw.cache_run = cache->s_run;
+    iw.cache_slots = cache->slots;
+    iw.slot_of_seq = slot_of_seq;
+  }
+  launch_intra(d, in, iw, hdr, st);
+  stg.mark(n_chunks > 0 ? 1 : 0);
+
+  if (cache) {
+    launch_tail_fill(d, in, seqs, N, slot_of_seq, cache->slots, cache->tail_k, cache->tail_v,
+                     cache->tail_g, cache->tail_beta, cache->pos, hdr, st);
+    stg.mark(1);
+  }
+  return finish(st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_cpr_version(void) { return GDN_VERSION_NUM; }
+
+const char* gdn_cpr_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GDN_ERR_CUDA: return "CUDA error";
+    case GDN_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case GDN_ERR_DEVICE: return "device-side error recorded";
+  }
+  return "unknown status";
+}
+
+gdn_status gdn_cpr_workspace_size(const gdn_cpr_shape* shape, gdn_mode mode,
+                                  const int32_t* cu_seqlens_host, size_t* bytes) {
+  if (!bytes) return GDN_ERR_INVALID_ARG;
+  gdn_status rc = check_shape(shape);
+  if (rc != GDN_OK) return rc;
+  if (mode == GDN_MODE_DECODE) {
+    *bytes = dec_layout(shape).total;
+    return GDN_OK;
+  }
+  int64_t n_chunks = 0;
+  uint32_t hash = 0;
+  rc = scan_cu(shape, cu_seqlens_host, &n_chunks, &hash);
+  if (rc != GDN_OK) return rc;
+  switch (mode) {
+    case GDN_MODE_PREFILL: *bytes = fwd_layout(shape, n_chunks, true).total; return GDN_OK;
+    case GDN_MODE_FWD: *bytes = fwd_layout(shape, n_chunks, false).total; return GDN_OK;
+    case GDN_MODE_BWD: return GDN_ERR_UNSUPPORTED;
+    default: return GDN_ERR_INVALID_ARG;
+  }
+}
+
+gdn_status gdn_cpr_prefill(const gdn_cpr_shape* shape, const void* q, const void* k,
+                           const void* v, const float* g, const float* beta,
+                           const float* state_in, const int32_t* cu_seqlens_dev,
+                           const int32_t* cu_seqlens_host, void* o, float* state_out,
+                           const gdn_cpr_cache* cache_out, const int32_t* slot_of_seq, void* ws,
+                           size_t ws_bytes, gdn_stream_t stream) {
+  return run_forward(shape, q, k, v, g, beta, state_in, cu_seqlens_dev, cu_seqlens_host, o,
+                     state_out, cache_out, slot_of_seq, nullptr, ws, ws_bytes, stream);
+}
+
+gdn_status gdn_cpr_fwd(const gdn_cpr_shape* shape, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* state_in,
+                       const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, void* o,
+                       float* state_out, float* saved_bnd, void* ws, size_t ws_bytes,
+                       gdn_stream_t stream) {
+  if (!saved_bnd) return GDN_ERR_INVALID_ARG;
+  return run_forward(shape, q, k, v, g, beta, state_in, cu_seqlens_dev, cu_seqlens_host, o,
+                     state_out, nullptr, nullptr, saved_bnd, ws, ws_bytes, stream);
+}
+
+gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const void* k,
+                               const void* v, const float* g, const float* beta,
+                               const int32_t* slot, const gdn_cpr_cache* cache, void* o,
+                               void* ws, size_t ws_bytes, gdn_stream_t stream) {
+  gdn_status rc = check_shape(shape);
+  if (rc != GDN_OK) return rc;
+  const int N = shape->num_seqs;
+  if (shape->total_tokens != N) return GDN_ERR_INVALID_ARG;
+  rc = check_cache(cache);
+  if (rc != GDN_OK) return rc;
+  if (N > 0 && (!ok_ptr(q, 16) || !ok_ptr(k, 16) || !ok_ptr(v, 16) || !ok_ptr(g, 4) ||
+                !ok_ptr(beta, 4) || !ok_ptr(o, 16) || !ok_ptr(slot, 4)))
+    return GDN_ERR_INVALID_ARG;
+  const DecLayout L = dec_layout(shape);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if (N == 0) return GDN_OK;
+  const Dims d = dims_of(shape);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* W = reinterpret_cast<float*>(at(ws, L.W));
+  float* U = reinterpret_cast<float*>(at(ws, L.U));
+  float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
+  TokenArrays in{q, k, v, g, beta};
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
+  Stages stg(stream);
+
+  DecodeWork dw{};
+  dw.N = N;
+  dw.slot = slot;
+  dw.slots = cache->slots;
+  dw.s_run = cache->s_run;
+  dw.tail_k = cache->tail_k;
+  dw.tail_v = cache->tail_v;
+  dw.tail_g = cache->tail_g;
+  dw.tail_beta = cache->tail_beta;
+  dw.pos = cache->pos;
+  dw.o = o;
+  launch_decode(d, in, dw, hdr, stream);
+  stg.mark(1);
+
+  // resynchronisation: the same boundary pre-pass and chain step as prefill, on the tail
+  TokenArrays tail{nullptr, cache->tail_k, cache->tail_v, cache->tail_g, cache->tail_beta};
+  PrepWork pw{};
+  pw.chunks = nullptr;
+  pw.n_items = N;
+  pw.slot = slot;
+  pw.pos = cache->pos;
+  pw.slots = cache->slots;
+  launch_prep(d, tail, pw, W, U, gamma, hdr, stream);
+  stg.mark(1);
+
+  ChainWork cw{};
+  cw.seqs = nullptr;
+  cw.N = N;
+  cw.slot = slot;
+  cw.pos = cache->pos;
+  cw.s_bnd = cache->s_bnd;
+  cw.s_run = cache->s_run;
+  cw.slots = cache->slots;
+  launch_chain(d, cache->tail_k, W, U, gamma, cw, hdr, stream);
+  stg.mark(1);
+
+  launch_advance(N, slot, cache->slots, cache->pos, stream);
+  stg.mark(1);
+  return finish(stream);
+}
+
+gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* state_in,
+                       const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host,
+                       const float* saved_bnd, const void* dO, const float* dstate_out,
+                       float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                       float* dstate_in, void* ws, size_t ws_bytes, gdn_stream_t stream) {
+  (void)shape; (void)q; (void)k; (void)v; (void)g; (void)beta; (void)state_in;
+  (void)cu_seqlens_dev; (void)cu_seqlens_host; (void)saved_bnd; (void)dO; (void)dstate_out;
+  (void)dq; (void)dk; (void)dv; (void)dg; (void)dbeta; (void)dstate_in; (void)ws;
+  (void)ws_bytes; (void)stream;
+  return GDN_ERR_UNSUPPORTED;
+}
+
+void gdn_cpr_set_profile(gdn_cpr_profile* profile) { t_profile = profile; }
+
+gdn_status gdn_cpr_get_device_error(const void* ws, gdn_stream_t stream, int32_t* code) {
+  if (!ws || !code) return GDN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
+  int32_t c = 0;
+  if (cudaMemcpy(&c, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  *code = c;
+  return c == 0 ? GDN_OK : GDN_ERR_DEVICE;
+}
+
+}  // extern "C"

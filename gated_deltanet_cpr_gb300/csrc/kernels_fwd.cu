@@ -1,0 +1,676 @@
+// kernels_fwd.cu -- forward-path kernels of CPR Gated DeltaNet for sm_103a.
+//
+// CPR (IsoExec page, section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet") keeps
+// the gated delta-rule recurrence as the main computation and evaluates it in parallel
+// across chunks; decode resynchronises its state every C tokens.  Here:
+//   K0 k_worklist  chunk/sequence records from cu_seqlens (device-checked)
+//   K1a k_prep     chunk pre-pass, parallel over (chunk, head):
+//                    G = cumsum g, A_is = beta_i e^{G_i-G_s} k_i.k_s (i>s), T = (I+A)^-1,
+//                    Wd = diag(e^{G_C-G}) T diag(beta e^G) K,  Ud = diag(e^{G_C-G}) T diag(beta) V
+//   K1b k_chain    boundary chain, sequential over chunks per (sequence, head, row block):
+//                    Vd = Ud - Wd S^T,   S <- e^{G_C} S + Vd^T K
+//   K2 k_intra     token recurrence inside every chunk from its boundary state
+//   K3 k_decode    one token step per decode slot, appended to the slot's chunk tail
+// Prefill and decode resync run the very same k_prep/k_chain code on the same values, and
+// K2 and K3 call the same token_step, which is what makes every mode bit-identical.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "../../include/gdn_cpr.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace gdn {
+
+// Opt a kernel into more than 48 KB of dynamic shared memory, once per (kernel, device):
+// later calls (including ones made while a CUDA graph is being captured) skip the runtime
+// call entirely.
+template <typename F>
+static void ensure_smem(F* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.insert({reinterpret_cast<const void*>(fn), dev}).second)
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// =====================================================================  K0  ====
+__global__ void __launch_bounds__(1024) k_worklist(const int32_t* __restrict__ cu, int N, int T,
+                                                   int C, int64_t n_chunks, uint32_t cu_hash,
+                                                   ChunkRec* __restrict__ chunks,
+                                                   SeqRec* __restrict__ seqs,
+                                                   WsHeader* __restrict__ hdr) {
+  __shared__ int64_t scan[1024];
+  __shared__ int bad;
+  __shared__ uint32_t hsum;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    bad = 0;
+    hsum = 0;
+  }
+  __syncthreads();
+  int64_t carry = 0;
+  for (int base = 0; base <= N; base += 1024) {
+    const int s = base + t;
+    int64_t nc = 0;
+    int32_t tok0 = 0, L = 0;
+    if (s <= N) {
+      const int32_t c = cu[s];
+      atomicAdd(&hsum, (uint32_t)c * (uint32_t)(2 * s + 1));
+      if (s == 0 && c != 0) bad = 1;
+      if (s == N && c != T) bad = 1;
+    }
+    if (s < N) {
+      tok0 = cu[s];
+      L = cu[s + 1] - tok0;
+      if (L < 0 || tok0 < 0) bad = 1;
+      nc = (L > 0) ? (L + C - 1) / C : 0;
+    }
+    scan[t] = nc;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      const int64_t x = (t >= off) ? scan[t - off] : 0;
+      __syncthreads();
+      scan[t] += x;
+      __syncthreads();
+    }
+    const int64_t first = carry + scan[t] - nc;
+    if (s < N && L >= 0) {
+      seqs[s] = SeqRec{tok0, L, (int32_t)first, (int32_t)nc};
+      for (int64_t j = 0; j < nc; ++j) {
+        const int64_t c = first + j;
+        if (c < n_chunks) {
+          const int32_t rem = L - (int32_t)(j * C);
+          chunks[c] = ChunkRec{s, tok0 + (int32_t)(j * C), rem < C ? rem : C, (int32_t)j};
+        }
+      }
+    }
+    carry += scan[1023];
+    __syncthreads();
+  }
+  if (t == 0) {
+    if (bad || carry != n_chunks || hsum != cu_hash) {
+      set_error(hdr, GDN_DEVERR_CU_SEQLENS);
+      hdr->valid = 0;
+    } else {
+      hdr->valid = 1;
+    }
+  }
+}
+
+void launch_worklist(const int32_t* cu, int N, int T, int C, int64_t n_chunks, uint32_t cu_hash,
+                     ChunkRec* chunks, SeqRec* seqs, WsHeader* hdr, cudaStream_t st) {
+  k_worklist<<<1, 1024, 0, st>>>(cu, N, T, C, n_chunks, cu_hash, chunks, seqs, hdr);
+}
+
+// =====================================================================  K1a  ===
+// Shared-memory plan (floats): Ks[64][D+4] Vs[64][D+4] A[64][65] T[64][65] + 5 vectors.
+template <int D>
+constexpr size_t prep_smem_bytes() {
+  return sizeof(float) * (2 * kMaxChunk * (D + 4) + 2 * kMaxChunk * (kMaxChunk + 1) + 5 * kMaxChunk + 4);
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, PrepWork w,
+                                                       float* __restrict__ Wout,
+                                                       float* __restrict__ Uout,
+                                                       float* __restrict__ gamma_out,
+                                                       WsHeader* __restrict__ hdr) {
+  constexpr int DP = D + 4;
+  constexpr int CP = kMaxChunk + 1;
+  extern __shared__ __align__(16) float sm[];
+  float* Ks = sm;
+  float* Vs = Ks + kMaxChunk * DP;
+  float* A = Vs + kMaxChunk * DP;
+  float* Tm = A + kMaxChunk * CP;
+  float* gs = Tm + kMaxChunk * CP;
+  float* Gs = gs + kMaxChunk;
+  float* bs = Gs + kMaxChunk;
+  float* bk = bs + kMaxChunk;
+  float* dec = bk + kMaxChunk;
+
+  const int t = threadIdx.x;
+  const int C = dm.C;
+  const int h = blockIdx.y;
+  const int hq = h / (dm.hv / dm.hqk);
+  const int64_t item = blockIdx.x;
+  int64_t tok0;
+  if (w.chunks) {  // prefill: chunk record
+    if (!hdr->valid) return;
+    const ChunkRec rec = w.chunks[item];
+    if (rec.len != C) return;  // only full chunks advance a boundary state
+    tok0 = rec.tok0;
+  } else {  // decode: the slot's tail, when this token completes it
+    const int sl = w.slot[item];
+    if (sl < 0 || sl >= w.slots) {
+      if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_SLOT);
+      return;
+    }
+    const int p = w.pos[sl];
+    if (p < 0) {
+      if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_POS);
+      return;
+    }
+    if ((p + 1) % C != 0) return;
+    tok0 = (int64_t)sl * C;
+  }
+  const Tin* kin = static_cast<const Tin*>(in.k);
+  const Tin* vin = static_cast<const Tin*>(in.v);
+
+  // 1. chunk inputs -> fp32 shared memory
+  for (int idx = t; idx < C * (D / 8); idx += kPrepThreads) {
+    const int r = idx / (D / 8), c8 = idx % (D / 8);
+    float tmp[8];
+    load8(kin + ((tok0 + r) * dm.hqk + hq) * D + 8 * c8, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) Ks[r * DP + 8 * c8 + e] = tmp[e];
+    load8(vin + ((tok0 + r) * dm.hv + h) * D + 8 * c8, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) Vs[r * DP + 8 * c8 + e] = tmp[e];
+  }
+  if (t < C) {
+    gs[t] = in.g[(tok0 + t) * dm.hv + h];
+    bs[t] = in.beta[(tok0 + t) * dm.hv + h];
+  }
+  __syncthreads();
+  // 2. G_i = g_0 + ... + g_i, left to right
+  if (t == 0) {
+    float run = gs[0];
+    Gs[0] = run;
+    for (int i = 1; i < C; ++i) {
+      run = __fadd_rn(run, gs[i]);
+      Gs[i] = run;
+    }
+  }
+  __syncthreads();
+  // 3. decay factors and A (strictly lower)
+  if (t < C) {
+    bk[t] = __fmul_rn(bs[t], expf(Gs[t]));
+    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
+  }
+  for (int o = t; o < C * C; o += kPrepThreads) {
+    const int i = o / C, s = o % C;
+    if (i > s) {
+      const float e = expf(__fsub_rn(Gs[i], Gs[s]));
+      A[i * CP + s] = __fmul_rn(__fmul_rn(bs[i], e), dot_canon<D>(Ks + i * DP, Ks + s * DP));
+    }
+  }
+  __syncthreads();
+  // 4. T = (I + A)^{-1} by forward substitution, one column per thread:
+  //    T[r][r] = 1,  T[i][r] = -sum_{m=r}^{i-1} A[i][m] T[m][r]  (m ascending)
+  if (t < C) {
+    const int r = t;
+    Tm[r * CP + r] = 1.f;
+    for (int i = r + 1; i < C; ++i) {
+      float acc = 0.f;
+      for (int m = r; m < i; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
+      Tm[i * CP + r] = -acc;
+    }
+  }
+  __syncthreads();
+  // 5. TK = T diag(beta e^G) (into A), TV = T diag(beta) (in place)
+  for (int o = t; o < C * C; o += kPrepThreads) {
+    const int i = o / C, r = o % C;
+    if (r <= i) {
+      const float x = Tm[i * CP + r];
+      A[i * CP + r] = __fmul_rn(x, bk[r]);
+      Tm[i * CP + r] = __fmul_rn(x, bs[r]);
+    }
+  }
+  __syncthreads();
+  // 6. Wd[i][c] = dec_i * sum_{r<=i} TK[i][r] K[r][c];  Ud[i][c] = dec_i * sum_{r<=i} TV[i][r] V[r][c]
+  constexpr int RG = kPrepThreads / D;  // row groups
+  const int c = t % D;
+  float* Wo = Wout + ((item * dm.hv + h) * C) * (int64_t)D;
+  float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
+  for (int i = t / D; i < C; i += RG) {
+    float aw = 0.f, au = 0.f;
+    for (int r = 0; r <= i; ++r) {
+      aw = __fmaf_rn(A[i * CP + r], Ks[r * DP + c], aw);
+      au = __fmaf_rn(Tm[i * CP + r], Vs[r * DP + c], au);
+    }
+    Wo[i * D + c] = __fmul_rn(dec[i], aw);
+    Uo[i * D + c] = __fmul_rn(dec[i], au);
+  }
+  if (t == 0) gamma_out[item * dm.hv + h] = expf(Gs[C - 1]);
+}
+
+template <int D, typename Tin>
+static void launch_prep_t(const Dims& d, const TokenArrays& in, const PrepWork& w, float* W,
+                          float* U, float* gamma, WsHeader* hdr, cudaStream_t st) {
+  constexpr size_t smem = prep_smem_bytes<D>();
+  ensure_smem(k_prep<D, Tin>, smem);
+  dim3 grid((unsigned)w.n_items, d.hv);
+  k_prep<D, Tin><<<grid, kPrepThreads, smem, st>>>(d, in, w, W, U, gamma, hdr);
+}
+
+// =====================================================================  K1b  ===
+// Shared-memory plan (floats): Ws[64][D+4] Ks[64][D+4] Ss[16][D+4] Us[64][16] Vd[64][16].
+template <int D>
+constexpr size_t chain_smem_bytes() {
+  return sizeof(float) * (2 * kMaxChunk * (D + 4) + kRowsPerChain * (D + 4) + 2 * kMaxChunk * kRowsPerChain);
+}
+
+// One boundary step on rows [r0, r0+16) of S (in Ss):  Vd = Ud - Wd S^T,  S <- gamma S + Vd^T K.
+// Vd[s][i] = Ud[s][i] - dot_canon(Wd[s], S[i]);  S[i][c] = gamma S[i][c] + sum_s Vd[s][i] K[s][c]
+// with s ascending after the gamma term.
+template <int D, typename Tin>
+__device__ __forceinline__ void chain_step(float* Ss, float* Ws, float* Ks, float* Us, float* Vd,
+                                           const float* __restrict__ Wg, const float* __restrict__ Ug,
+                                           float gamma, const Tin* __restrict__ keys, int64_t tok0,
+                                           int hqk, int hq, int C, int r0) {
+  constexpr int DP = D + 4;
+  constexpr int R = kRowsPerChain;
+  const int t = threadIdx.x;
+  for (int idx = t; idx < C * (D / 4); idx += kChainThreads) {
+    const int s = idx / (D / 4), c4 = idx % (D / 4);
+    *reinterpret_cast<float4*>(Ws + s * DP + 4 * c4) = reinterpret_cast<const float4*>(Wg + s * D)[c4];
+  }
+  for (int idx = t; idx < C * (D / 8); idx += kChainThreads) {
+    const int s = idx / (D / 8), c8 = idx % (D / 8);
+    float tmp[8];
+    load8(keys + ((tok0 + s) * hqk + hq) * D + 8 * c8, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) Ks[s * DP + 8 * c8 + e] = tmp[e];
+  }
+  for (int idx = t; idx < C * (R / 4); idx += kChainThreads) {
+    const int s = idx / (R / 4), i4 = idx % (R / 4);
+    *reinterpret_cast<float4*>(Us + s * R + 4 * i4) = *reinterpret_cast<const float4*>(Ug + s * D + r0 + 4 * i4);
+  }
+  __syncthreads();
+  for (int o = t; o < C * R; o += kChainThreads) {
+    const int s = o % C, i = o / C;
+    Vd[s * R + i] = __fsub_rn(Us[s * R + i], dot_canon<D>(Ws + s * DP, Ss + i * DP));
+  }
+  __syncthreads();
+  for (int o = t; o < R * D; o += kChainThreads) {
+    const int i = o / D, c = o % D;
+    float acc = __fmul_rn(gamma, Ss[i * DP + c]);
+    for (int s = 0; s < C; ++s) acc = __fmaf_rn(Vd[s * R + i], Ks[s * DP + c], acc);
+    Ss[i * DP + c] = acc;
+  }
+  __syncthreads();
+}
+
+template <int D>
+__device__ __forceinline__ void rows_to_global(const float* Ss, float* dst /* row r0 of a state */) {
+  constexpr int DP = D + 4;
+  for (int idx = threadIdx.x; idx < kRowsPerChain * (D / 4); idx += kChainThreads) {
+    const int i = idx / (D / 4), c4 = idx % (D / 4);
+    reinterpret_cast<float4*>(dst + i * D)[c4] = *reinterpret_cast<const float4*>(Ss + i * DP + 4 * c4);
+  }
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* keys_v,
+                                                         const float* __restrict__ W,
+                                                         const float* __restrict__ U,
+                                                         const float* __restrict__ gamma,
+                                                         ChainWork w, WsHeader* __restrict__ hdr) {
+  constexpr int DP = D + 4;
+  constexpr int R = kRowsPerChain;
+  extern __shared__ __align__(16) float sm[];
+  float* Ws = sm;
+  float* Ks = Ws + kMaxChunk * DP;
+  float* Ss = Ks + kMaxChunk * DP;
+  float* Us = Ss + R * DP;
+  float* Vd = Us + kMaxChunk * R;
+  const int t = threadIdx.x;
+  const int C = dm.C;
+  const int n = blockIdx.x, h = blockIdx.y, r0 = blockIdx.z * R;
+  const int hq = h / (dm.hv / dm.hqk);
+  const Tin* keys = static_cast<const Tin*>(keys_v);
+  const int64_t SZ = (int64_t)D * D;
+
+  if (w.seqs) {  // ------------------------------------------------ prefill chain
+    if (!hdr->valid) return;
+    const SeqRec rec = w.seqs[n];
+    const int nfull = rec.len / C;
+    // S <- state_in rows (or 0)
+    for (int idx = t; idx < R * (D / 4); idx += kChainThreads) {
+      const int i = idx / (D / 4), c4 = idx % (D / 4);
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (w.state_in) x = reinterpret_cast<const float4*>(w.state_in + ((int64_t)n * dm.hv + h) * SZ + (int64_t)(r0 + i) * D)[c4];
+      *reinterpret_cast<float4*>(Ss + i * DP + 4 * c4) = x;
+    }
+    __syncthreads();
+    for (int j = 0; j < nfull; ++j) {
+      const int64_t c = (int64_t)rec.chunk0 + j;
+      rows_to_global<D>(Ss, w.bnd + (c * dm.hv + h) * SZ + (int64_t)r0 * D);
+      const int64_t wo = (c * dm.hv + h) * (int64_t)C * D;
+      chain_step<D, Tin>(Ss, Ws, Ks, Us, Vd, W + wo, U + wo, gamma[c * dm.hv + h], keys,
+                         (int64_t)rec.tok0 + (int64_t)j * C, dm.hqk, hq, C, r0);
+    }
+    if (rec.len % C != 0) {
+      const int64_t c = (int64_t)rec.chunk0 + nfull;  // start state of the partial chunk
+      rows_to_global<D>(Ss, w.bnd + (c * dm.hv + h) * SZ + (int64_t)r0 * D);
+    } else if (w.state_out) {
+      rows_to_global<D>(Ss, w.state_out + ((int64_t)n * dm.hv + h) * SZ + (int64_t)r0 * D);
+    }
+    if (w.cache_bnd) {
+      const int sl = w.slot_of_seq ? w.slot_of_seq[n] : n;
+      if (sl < 0 || sl >= w.cache_slots) {
+        if (t == 0) set_error(hdr, GDN_DEVERR_SLOT);
+        return;
+      }
+      rows_to_global<D>(Ss, w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)r0 * D);
+      if (rec.len % C == 0)
+        rows_to_global<D>(Ss, w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)r0 * D);
+    }
+  } else {  // ---------------------------------------------------- decode resync
+    const int sl = w.slot[n];
+    if (sl < 0 || sl >= w.slots) return;  // reported by k_decode
+    const int p = w.pos[sl];
+    if (p < 0 || (p + 1) % C != 0) return;
+    const int64_t so = ((int64_t)sl * dm.hv + h) * SZ + (int64_t)r0 * D;
+    for (int idx = t; idx < R * (D / 4); idx += kChainThreads) {
+      const int i = idx / (D / 4), c4 = idx % (D / 4);
+      *reinterpret_cast<float4*>(Ss + i * DP + 4 * c4) = reinterpret_cast<const float4*>(w.s_bnd + so + (int64_t)i * D)[c4];
+    }
+    __syncthreads();
+    const int64_t wo = ((int64_t)n * dm.hv + h) * (int64_t)C * D;
+    chain_step<D, Tin>(Ss, Ws, Ks, Us, Vd, W + wo, U + wo, gamma[(int64_t)n * dm.hv + h], keys,
+                       (int64_t)sl * C, dm.hqk, hq, C, r0);
+    rows_to_global<D>(Ss, w.s_bnd + so);
+    rows_to_global<D>(Ss, w.s_run + so);
+  }
+}
+
+template <int D, typename Tin>
+static void launch_chain_t(const Dims& d, const void* keys, const float* W, const float* U,
+                           const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st) {
+  constexpr size_t smem = chain_smem_bytes<D>();
+  ensure_smem(k_chain<D, Tin>, smem);
+  dim3 grid((unsigned)w.N, d.hv, D / kRowsPerChain);
+  k_chain<D, Tin><<<grid, kChainThreads, smem, st>>>(d, keys, W, U, gamma, w, hdr);
+}
+
+// =====================================================================  K2  ====
+template <int D>
+constexpr size_t intra_smem_bytes() {
+  return sizeof(float) * (3 * kMaxChunk * D + 2 * kMaxChunk);
+}
+
+template <int D, typename Tin, typename Tout>
+__global__ void __launch_bounds__(2 * D) k_intra(Dims dm, TokenArrays in, IntraWork w,
+                                                 WsHeader* __restrict__ hdr) {
+  extern __shared__ __align__(16) float sm[];
+  float* ks = sm;
+  float* qs = ks + kMaxChunk * D;
+  float* vs = qs + kMaxChunk * D;  // v, then o (staged)
+  float* as = vs + kMaxChunk * D;
+  float* bs = as + kMaxChunk;
+  if (!hdr->valid) return;
+  const int t = threadIdx.x;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y;
+  const int hq = h / (dm.hv / dm.hqk);
+  const ChunkRec rec = w.chunks[c];
+  const int len = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t SZ = (int64_t)D * D;
+  const Tin* qin = static_cast<const Tin*>(in.q);
+  const Tin* kin = static_cast<const Tin*>(in.k);
+  const Tin* vin = static_cast<const Tin*>(in.v);
+
+  for (int idx = t; idx < len * (D / 8); idx += 2 * D) {
+    const int r = idx / (D / 8), c8 = idx % (D / 8);
+    float tmp[8];
+    load8(kin + ((tok0 + r) * dm.hqk + hq) * D + 8 * c8, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ks[r * D + 8 * c8 + e] = tmp[e];
+    load8(qin + ((tok0 + r) * dm.hqk + hq) * D + 8 * c8, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qs[r * D + 8 * c8 + e] = tmp[e];
+    load8(vin + ((tok0 + r) * dm.hv + h) * D + 8 * c8, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vs[r * D + 8 * c8 + e] = tmp[e];
+  }
+  for (int r = t; r < len; r += 2 * D) {
+    as[r] = expf(in.g[(tok0 + r) * dm.hv + h]);
+    bs[r] = in.beta[(tok0 + r) * dm.hv + h];
+  }
+  const int i = t >> 1, half = t & 1;
+  float4 S[D / 8];
+  const float* src = w.bnd + (c * dm.hv + h) * SZ + (int64_t)i * D;
+#pragma unroll
+  for (int m = 0; m < D / 8; ++m) S[m] = *reinterpret_cast<const float4*>(src + state_col<D>(m, half));
+  __syncthreads();
+
+  for (int tt = 0; tt < len; ++tt) {
+    const float o = token_step<D>(S, ks + tt * D, qs + tt * D, as[tt], bs[tt], vs[tt * D + i], half);
+    __syncwarp();
+    if (half == 0) vs[tt * D + i] = o;
+  }
+  __syncthreads();
+  Tout* out = static_cast<Tout*>(w.o);
+  for (int idx = t; idx < len * D; idx += 2 * D) {
+    const int r = idx / D, e = idx % D;
+    store_out(out + ((tok0 + r) * dm.hv + h) * D + e, vs[idx]);
+  }
+  // state decode continues from: the token recurrence through a final partial chunk
+  const SeqRec sr = w.seqs[rec.seq];
+  if (rec.jloc == sr.nchunks - 1 && (sr.len % dm.C) != 0) {
+    if (w.state_out) {
+      float* dst = w.state_out + ((int64_t)rec.seq * dm.hv + h) * SZ + (int64_t)i * D;
+#pragma unroll
+      for (int m = 0; m < D / 8; ++m) *reinterpret_cast<float4*>(dst + state_col<D>(m, half)) = S[m];
+    }
+    if (w.cache_run) {
+      const int sl = w.slot_of_seq ? w.slot_of_seq[rec.seq] : rec.seq;
+      if (sl >= 0 && sl < w.cache_slots) {
+        float* dst = w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)i * D;
+#pragma unroll
+        for (int m = 0; m < D / 8; ++m) *reinterpret_cast<float4*>(dst + state_col<D>(m, half)) = S[m];
+      }
+    }
+  }
+}
+
+template <int D, typename Tin, typename Tout>
+static void launch_intra_t(const Dims& d, const TokenArrays& in, const IntraWork& w, WsHeader* hdr,
+                           cudaStream_t st) {
+  constexpr size_t smem = intra_smem_bytes<D>();
+  ensure_smem(k_intra<D, Tin, Tout>, smem);
+  dim3 grid((unsigned)w.n_chunks, d.hv);
+  k_intra<D, Tin, Tout><<<grid, 2 * D, smem, st>>>(d, in, w, hdr);
+}
+
+// =====================================================================  K3  ====
+template <int D, typename Tin, typename Tout>
+__global__ void __launch_bounds__(2 * D) k_decode(Dims dm, TokenArrays in, DecodeWork w,
+                                                  WsHeader* __restrict__ hdr) {
+  __shared__ __align__(16) float ks[D];
+  __shared__ __align__(16) float qs[D];
+  const int t = threadIdx.x;
+  const int n = blockIdx.x, h = blockIdx.y;
+  const int grp = dm.hv / dm.hqk;
+  const int hq = h / grp;
+  const int C = dm.C;
+  const int sl = w.slot[n];
+  if (sl < 0 || sl >= w.slots) {
+    if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_SLOT);
+    return;
+  }
+  const int p = w.pos[sl];
+  if (p < 0) {
+    if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_POS);
+    return;
+  }
+  const Tin* qin = static_cast<const Tin*>(in.q);
+  const Tin* kin = static_cast<const Tin*>(in.k);
+  const Tin* vin = static_cast<const Tin*>(in.v);
+  const int64_t SZ = (int64_t)D * D;
+  if (t < D / 8) {
+    float tmp[8];
+    load8(kin + ((int64_t)n * dm.hqk + hq) * D + 8 * t, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ks[8 * t + e] = tmp[e];
+    load8(qin + ((int64_t)n * dm.hqk + hq) * D + 8 * t, tmp);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) qs[8 * t + e] = tmp[e];
+  }
+  const int i = t >> 1, half = t & 1;
+  float4 S[D / 8];
+  float* srow = w.s_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)i * D;
+#pragma unroll
+  for (int m = 0; m < D / 8; ++m) S[m] = *reinterpret_cast<const float4*>(srow + state_col<D>(m, half));
+  const float a = expf(in.g[(int64_t)n * dm.hv + h]);
+  const float b = in.beta[(int64_t)n * dm.hv + h];
+  const Tin vraw = vin[((int64_t)n * dm.hv + h) * D + i];
+  __syncthreads();
+  const float o = token_step<D>(S, ks, qs, a, b, to_f32(vraw), half);
+#pragma unroll
+  for (int m = 0; m < D / 8; ++m) *reinterpret_cast<float4*>(srow + state_col<D>(m, half)) = S[m];
+  const int ti = p % C;
+  if (half == 0) {
+    store_out(static_cast<Tout*>(w.o) + ((int64_t)n * dm.hv + h) * D + i, o);
+    static_cast<Tin*>(w.tail_v)[(((int64_t)sl * C + ti) * dm.hv + h) * D + i] = vraw;
+  }
+  if (t == 0) {
+    w.tail_g[((int64_t)sl * C + ti) * dm.hv + h] = in.g[(int64_t)n * dm.hv + h];
+    w.tail_beta[((int64_t)sl * C + ti) * dm.hv + h] = b;
+  }
+  if (h % grp == 0 && t < D) {
+    static_cast<Tin*>(w.tail_k)[(((int64_t)sl * C + ti) * dm.hqk + hq) * D + t] =
+        kin[((int64_t)n * dm.hqk + hq) * D + t];
+  }
+}
+
+template <int D, typename Tin, typename Tout>
+static void launch_decode_t(const Dims& d, const TokenArrays& in, const DecodeWork& w,
+                            WsHeader* hdr, cudaStream_t st) {
+  dim3 grid((unsigned)w.N, d.hv);
+  k_decode<D, Tin, Tout><<<grid, 2 * D, 0, st>>>(d, in, w, hdr);
+}
+
+// ============================================================ small helpers ====
+__global__ void k_advance(int N, const int32_t* __restrict__ slot, int slots, int32_t* pos) {
+  for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
+    const int sl = slot[n];
+    if (sl >= 0 && sl < slots && pos[sl] >= 0) pos[sl] += 1;
+  }
+}
+
+void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st) {
+  k_advance<<<(N + 255) / 256, 256, 0, st>>>(N, slot, slots, pos);
+}
+
+template <typename Tin>
+__global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ seqs,
+                            const int32_t* __restrict__ slot_of_seq, int slots, Tin* tail_k,
+                            Tin* tail_v, float* tail_g, float* tail_beta, int32_t* pos,
+                            WsHeader* __restrict__ hdr) {
+  if (!hdr->valid) return;
+  const int n = blockIdx.x;
+  const SeqRec rec = seqs[n];
+  const int sl = slot_of_seq ? slot_of_seq[n] : n;
+  if (sl < 0 || sl >= slots) {
+    if (threadIdx.x == 0) set_error(hdr, GDN_DEVERR_SLOT);
+    return;
+  }
+  const int C = dm.C, D = dm.D;
+  const int nt = rec.len % C;
+  const int64_t base = (int64_t)rec.tok0 + rec.len - nt;
+  const Tin* kin = static_cast<const Tin*>(in.k);
+  const Tin* vin = static_cast<const Tin*>(in.v);
+  const int64_t nk = (int64_t)nt * dm.hqk * D, nv = (int64_t)nt * dm.hv * D, ng = (int64_t)nt * dm.hv;
+  for (int64_t e = threadIdx.x; e < nk; e += blockDim.x)
+    tail_k[(int64_t)sl * C * dm.hqk * D + e] = kin[base * dm.hqk * D + e];
+  for (int64_t e = threadIdx.x; e < nv; e += blockDim.x)
+    tail_v[(int64_t)sl * C * dm.hv * D + e] = vin[base * dm.hv * D + e];
+  for (int64_t e = threadIdx.x; e < ng; e += blockDim.x) {
+    tail_g[(int64_t)sl * C * dm.hv + e] = in.g[base * dm.hv + e];
+    tail_beta[(int64_t)sl * C * dm.hv + e] = in.beta[base * dm.hv + e];
+  }
+  if (threadIdx.x == 0) pos[sl] = rec.len;
+}
+
+void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, int N,
+                      const int32_t* slot_of_seq, int slots, void* tail_k, void* tail_v,
+                      float* tail_g, float* tail_beta, int32_t* pos, WsHeader* hdr,
+                      cudaStream_t st) {
+  if (N <= 0) return;
+  if (d.in_bf16)
+    k_tail_fill<__nv_bfloat16><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
+                                                  static_cast<__nv_bfloat16*>(tail_k),
+                                                  static_cast<__nv_bfloat16*>(tail_v), tail_g,
+                                                  tail_beta, pos, hdr);
+  else
+    k_tail_fill<float><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
+                                          static_cast<float*>(tail_k), static_cast<float*>(tail_v),
+                                          tail_g, tail_beta, pos, hdr);
+}
+
+// ================================================================= dispatch ====
+#define GDN_DISPATCH_D(D_, ...)         \
+  switch (D_) {                         \
+    case 32: { constexpr int DD = 32; __VA_ARGS__; } break; \
+    case 64: { constexpr int DD = 64; __VA_ARGS__; } break; \
+    default: { constexpr int DD = 128; __VA_ARGS__; } break; \
+  }
+
+void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float* W, float* U,
+                 float* gamma, WsHeader* hdr, cudaStream_t st) {
+  if (w.n_items <= 0) return;
+  if (d.in_bf16) {
+    GDN_DISPATCH_D(d.D, launch_prep_t<DD, __nv_bfloat16>(d, in, w, W, U, gamma, hdr, st))
+  } else {
+    GDN_DISPATCH_D(d.D, launch_prep_t<DD, float>(d, in, w, W, U, gamma, hdr, st))
+  }
+}
+
+void launch_chain(const Dims& d, const void* keys, const float* W, const float* U,
+                  const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st) {
+  if (w.N <= 0) return;
+  if (d.in_bf16) {
+    GDN_DISPATCH_D(d.D, launch_chain_t<DD, __nv_bfloat16>(d, keys, W, U, gamma, w, hdr, st))
+  } else {
+    GDN_DISPATCH_D(d.D, launch_chain_t<DD, float>(d, keys, W, U, gamma, w, hdr, st))
+  }
+}
+
+void launch_intra(const Dims& d, const TokenArrays& in, const IntraWork& w, WsHeader* hdr,
+                  cudaStream_t st) {
+  if (w.n_chunks <= 0) return;
+  if (d.in_bf16) {
+    if (d.out_bf16) {
+      GDN_DISPATCH_D(d.D, (launch_intra_t<DD, __nv_bfloat16, __nv_bfloat16>(d, in, w, hdr, st)))
+    } else {
+      GDN_DISPATCH_D(d.D, (launch_intra_t<DD, __nv_bfloat16, float>(d, in, w, hdr, st)))
+    }
+  } else {
+    if (d.out_bf16) {
+      GDN_DISPATCH_D(d.D, (launch_intra_t<DD, float, __nv_bfloat16>(d, in, w, hdr, st)))
+    } else {
+      GDN_DISPATCH_D(d.D, (launch_intra_t<DD, float, float>(d, in, w, hdr, st)))
+    }
+  }
+}
+
+void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, WsHeader* hdr,
+                   cudaStream_t st) {
+  if (w.N <= 0) return;
+  if (d.in_bf16) {
+    if (d.out_bf16) {
+      GDN_DISPATCH_D(d.D, (launch_decode_t<DD, __nv_bfloat16, __nv_bfloat16>(d, in, w, hdr, st)))
+    } else {
+      GDN_DISPATCH_D(d.D, (launch_decode_t<DD, __nv_bfloat16, float>(d, in, w, hdr, st)))
+    }
+  } else {
+    if (d.out_bf16) {
+      GDN_DISPATCH_D(d.D, (launch_decode_t<DD, float, __nv_bfloat16>(d, in, w, hdr, st)))
+    } else {
+      GDN_DISPATCH_D(d.D, (launch_decode_t<DD, float, float>(d, in, w, hdr, st)))
+    }
+  }
+}
+
+}  // namespace gdn

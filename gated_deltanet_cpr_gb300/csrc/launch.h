@@ -1,0 +1,112 @@
+// launch.h -- internal interface between the C-ABI host code and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace gdn {
+
+// Pointers to a run of tokens laid out as the packed inputs ([tok, H, D] / [tok, H]);
+// the decode tail of slot s is such a run starting at token s * C.
+struct TokenArrays {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+};
+
+struct Dims {
+  int hqk, hv, D, C;
+  bool in_bf16, out_bf16;
+};
+
+// K0: chunk and sequence records from the device cu_seqlens, checked against the host's
+// chunk count and a hash of the host copy.
+void launch_worklist(const int32_t* cu, int N, int T, int C, int64_t n_chunks, uint32_t cu_hash,
+                     ChunkRec* chunks, SeqRec* seqs, WsHeader* hdr, cudaStream_t st);
+
+// K1a: boundary pre-pass over full chunks.  Prefill: one CTA per (chunk record, head),
+// partial chunks skip.  Decode: one CTA per (step token n, head) whose slot completes a
+// chunk with this token; the chunk is read from the slot's tail.
+struct PrepWork {
+  // prefill
+  const ChunkRec* chunks;  // NULL in decode mode
+  int64_t n_items;
+  // decode
+  const int32_t* slot;
+  const int32_t* pos;
+  int slots;
+};
+void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float* W, float* U,
+                 float* gamma, WsHeader* hdr, cudaStream_t st);
+
+// K1b: boundary chain.  Prefill: one CTA per (sequence, head, 16-row block), sequential
+// over the sequence's full chunks; writes the start state of every chunk to bnd and the
+// final boundary state to state_out (if L % C == 0) and to the cache.  Decode: one step per
+// resynchronising (token n, head, row block): s_bnd <- F(s_bnd, tail), s_run <- s_bnd.
+struct ChainWork {
+  // prefill
+  const SeqRec* seqs;  // NULL in decode mode
+  int N;
+  const float* state_in;
+  float* bnd;
+  float* state_out;
+  float* cache_bnd;  // cache s_bnd (prefill with cache) or NULL
+  float* cache_run;  // cache s_run (prefill with cache, written when L % C == 0) or NULL
+  const int32_t* slot_of_seq;
+  int cache_slots;
+  // decode
+  const int32_t* slot;
+  const int32_t* pos;
+  float* s_bnd;
+  float* s_run;
+  int slots;
+};
+void launch_chain(const Dims& d, const void* keys, const float* W, const float* U,
+                  const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st);
+
+// K2: token recurrence inside every chunk from its boundary state, all chunks at once.
+struct IntraWork {
+  const ChunkRec* chunks;
+  const SeqRec* seqs;
+  int64_t n_chunks;
+  const float* bnd;
+  void* o;
+  float* state_out;
+  float* cache_run;
+  const int32_t* slot_of_seq;
+  int cache_slots;
+};
+void launch_intra(const Dims& d, const TokenArrays& in, const IntraWork& w, WsHeader* hdr,
+                  cudaStream_t st);
+
+// K3: one decode token per slot: token step on s_run, output, append to the tail.
+struct DecodeWork {
+  int N;
+  const int32_t* slot;
+  int slots;
+  float* s_run;
+  void* tail_k;
+  void* tail_v;
+  float* tail_g;
+  float* tail_beta;
+  const int32_t* pos;
+  void* o;
+};
+void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, WsHeader* hdr,
+                   cudaStream_t st);
+
+// pos[slot[n]] += 1 for every valid n (last kernel of a decode step).
+void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st);
+
+// Prefill with a cache: copy the last L % C tokens of every sequence to its slot's tail and
+// set pos = L.
+void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, int N,
+                      const int32_t* slot_of_seq, int slots, void* tail_k, void* tail_v,
+                      float* tail_g, float* tail_beta, int32_t* pos, WsHeader* hdr,
+                      cudaStream_t st);
+
+}  // namespace gdn

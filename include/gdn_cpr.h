@@ -1,0 +1,236 @@
+/*
+ * gdn_cpr.h -- C ABI of the CPR Gated DeltaNet library (sm_103a, one GPU).
+ *
+ * The operator (Gated DeltaNet; IsoExec page "IsoExec: SkyRLにおけるトレーナーと推論の
+ * ミスマッチを解消する", section "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet"), per
+ * (sequence, value head) with an fp32 state S of d_v x d_k:
+ *
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,      o_t = S_t q_t.
+ *
+ * CPR, as that section describes it, keeps this recurrence as the main computation but
+ * evaluates it in parallel across chunks of C tokens, and resynchronises the decode
+ * state every C tokens.  Concretely, in this library:
+ *   - a boundary pass computes the state S^(j) before every chunk j (chunks aligned to
+ *     each sequence's own first token) with the chunk (WY/UT) form, sequentially in j;
+ *   - every chunk then runs the token recurrence from its own S^(j), all chunks at once;
+ *   - decode runs the same token step on a running state and, whenever a chunk's C-th
+ *     token has been appended, replaces that running state by the next boundary state,
+ *     computed by the same boundary code on the cached chunk.
+ * Every mode uses one token-step routine and one boundary routine with fixed reduction
+ * orders, so prefill, trainer forward and decode give bit-identical o and states, for any
+ * batch size, packing or slot assignment.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts (row-major, densely packed; T = total tokens, N = sequences or decode slots):
+ *     q, k        [T, H_qk, d_k]   in_dtype
+ *     v           [T, H_v,  d_v]   in_dtype
+ *     g, beta     [T, H_v]         fp32 (g is the log decay: the step multiplies S by exp(g))
+ *     o           [T, H_v,  d_v]   out_dtype
+ *     states      [N, H_v, d_v, d_k] fp32 (row i of S is value dim i; o = S q)
+ *     cu_seqlens  [N + 1] int32, cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T
+ * Grouped heads: value head h reads query/key head h / (H_v / H_qk).  No scale is applied
+ * to q.  Sequences of length 0 are allowed (state_out = state_in, bit for bit).
+ *
+ * Supported configurations ("claims"; anything else returns GDN_ERR_UNSUPPORTED before any
+ * work is queued, in the spirit of the IsoExec contract's topology claims on the
+ * hegai.media page, section "Что именно объединяет IsoExec"):
+ *     d_k == d_v in {32, 64, 128};  chunk C in {16, 32, 64};  H_v % H_qk == 0;
+ *     in_dtype in {GDN_F32, GDN_BF16};  out_dtype in {GDN_F32, GDN_BF16};
+ *     every tensor pointer 16-byte aligned (g, beta: 4-byte).
+ *
+ * Ownership: the caller allocates and owns every buffer, including the workspace.  The
+ * library allocates no device memory and keeps no mutable global state apart from the
+ * optional per-thread profiling hook (gdn_cpr_set_profile).
+ *
+ * Execution: every call only queues work on `stream` and returns; nothing synchronises
+ * except gdn_cpr_get_device_error.  Inputs must stay valid until the stream reaches the
+ * queued work.  cu_seqlens_host must describe the same values as cu_seqlens_dev; it is
+ * read on the host during the call (grid and workspace sizing) and not kept.
+ *
+ * Errors: argument errors are returned synchronously and nothing is queued.  Errors that
+ * only the device can see (device cu_seqlens disagreeing with the host copy, a decode
+ * slot out of range, a bounded wait that gave up) are recorded in an error word inside the
+ * workspace; the affected kernels then skip their work (they never read or write out of
+ * bounds), and gdn_cpr_get_device_error reports the code.  Each call clears the word
+ * when it starts.  No kernel traps or asserts.
+ */
+#ifndef GDN_CPR_H
+#define GDN_CPR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gdn_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad sizes, bad cu_seqlens_host */
+    GDN_ERR_UNSUPPORTED = 2, /* outside the supported configurations listed above */
+    GDN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed */
+    GDN_ERR_WORKSPACE = 4,   /* workspace NULL, misaligned or smaller than required */
+    GDN_ERR_DEVICE = 5       /* returned by gdn_cpr_get_device_error when the word is set */
+} gdn_status;
+
+/* Codes stored in the device error word (read back by gdn_cpr_get_device_error). */
+typedef enum {
+    GDN_DEVERR_NONE = 0,
+    GDN_DEVERR_CU_SEQLENS = 1, /* device cu_seqlens disagree with cu_seqlens_host */
+    GDN_DEVERR_SLOT = 2,       /* decode slot index outside [0, cache.slots) */
+    GDN_DEVERR_POS = 3,        /* negative cache position */
+    GDN_DEVERR_TIMEOUT = 4     /* a bounded on-device wait gave up */
+} gdn_device_error;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef enum {
+    GDN_MODE_PREFILL = 0, /* gdn_cpr_prefill */
+    GDN_MODE_DECODE = 1,  /* gdn_cpr_decode_step */
+    GDN_MODE_FWD = 2,     /* gdn_cpr_fwd */
+    GDN_MODE_BWD = 3      /* gdn_cpr_bwd */
+} gdn_mode;
+
+typedef struct {
+    int32_t num_seqs;     /* N: sequences (prefill/fwd/bwd) or tokens this step (decode) */
+    int32_t total_tokens; /* T: cu_seqlens[N] (prefill/fwd/bwd); N for decode */
+    int32_t h_qk;         /* query/key heads */
+    int32_t h_v;          /* value heads (state heads) */
+    int32_t d_k;          /* key dim */
+    int32_t d_v;          /* value dim */
+    int32_t chunk;        /* C */
+    gdn_dtype in_dtype;   /* q, k, v */
+    gdn_dtype out_dtype;  /* o */
+} gdn_cpr_shape;
+
+/* Decode cache: everything needed to continue a sequence bit-exactly (also the full
+ * checkpoint of a decoding sequence: copy it out and back to resume).  All arrays are
+ * caller-owned device memory, indexed by slot.
+ *   s_run     [slots, H_v, d_v, d_k] fp32   running state (recurrent since the last boundary)
+ *   s_bnd     [slots, H_v, d_v, d_k] fp32   boundary state before the current chunk
+ *   tail_k    [slots, C, H_qk, d_k]  in_dtype  keys of the current, unfinished chunk
+ *   tail_v    [slots, C, H_v,  d_v]  in_dtype  values of the current chunk
+ *   tail_g    [slots, C, H_v]        fp32
+ *   tail_beta [slots, C, H_v]        fp32
+ *   pos       [slots] int32          tokens consumed so far by the slot's sequence          */
+typedef struct {
+    float *s_run;
+    float *s_bnd;
+    void *tail_k;
+    void *tail_v;
+    float *tail_g;
+    float *tail_beta;
+    int32_t *pos;
+    int32_t slots;
+} gdn_cpr_cache;
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int gdn_cpr_version(void);
+
+/* Static, human-readable name of a status code. */
+const char *gdn_cpr_status_string(gdn_status s);
+
+/* Bytes of workspace the given mode needs for this shape.  cu_seqlens_host [N+1] is
+ * required for PREFILL, FWD and BWD (the size depends on the number of chunks,
+ * sum over sequences of ceil(L/C)) and ignored for DECODE.  The workspace must be
+ * 256-byte aligned.  Returns GDN_ERR_INVALID_ARG / GDN_ERR_UNSUPPORTED like the calls. */
+gdn_status gdn_cpr_workspace_size(const gdn_cpr_shape *shape, gdn_mode mode,
+                                  const int32_t *cu_seqlens_host, size_t *bytes);
+
+/* Prefill (rollout prefill; IsoExec page section "Chunkwise-Parallel Recurrent (CPR)
+ * Gated DeltaNet": the recurrence evaluated in parallel across chunks).
+ *   q, k, v, g, beta    inputs, layouts above (device)
+ *   state_in            [N, H_v, d_v, d_k] fp32 or NULL for zero (device)
+ *   cu_seqlens_dev/host the same N+1 offsets, on the device and on the host
+ *   o                   output [T, H_v, d_v] in out_dtype (device)
+ *   state_out           NULL or [N, H_v, d_v, d_k]: the state decode continues from --
+ *                       the boundary state S^(L/C) if L % C == 0, else the token
+ *                       recurrence from S^(floor(L/C)) through the last L % C tokens
+ *   cache_out           NULL or a decode cache to initialise for these sequences:
+ *                       s_run = state_out, s_bnd = S^(floor(L/C)), tail = the last L % C
+ *                       tokens, pos = L, at slot slot_of_seq[n] (NULL: slot n)
+ *   slot_of_seq         NULL or [N] int32 device array of distinct slots
+ *   ws, ws_bytes        workspace of gdn_cpr_workspace_size(GDN_MODE_PREFILL) bytes  */
+gdn_status gdn_cpr_prefill(const gdn_cpr_shape *shape, const void *q, const void *k,
+                           const void *v, const float *g, const float *beta,
+                           const float *state_in, const int32_t *cu_seqlens_dev,
+                           const int32_t *cu_seqlens_host, void *o, float *state_out,
+                           const gdn_cpr_cache *cache_out, const int32_t *slot_of_seq, void *ws,
+                           size_t ws_bytes, gdn_stream_t stream);
+
+/* One decode token for each of N slots (rollout decode; IsoExec page section
+ * "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet": the hidden state is resynchronised
+ * every C tokens).  shape->num_seqs = shape->total_tokens = N.
+ *   q, k [N, H_qk, d_k], v [N, H_v, d_v], g, beta [N, H_v]: this step's token per slot
+ *   slot [N] int32 device: distinct cache slots (out of range -> device error, skipped)
+ *   cache               updated in place: s_run stepped, token appended to the tail, pos+1;
+ *                       when pos+1 is a multiple of C the boundary state is advanced over
+ *                       the completed chunk and s_run is replaced by it
+ *   o [N, H_v, d_v]     output
+ * The launch configuration depends only on N and the shape, and the resync decision is
+ * taken on the device from pos, so a step can be captured in a CUDA graph once the
+ * workspace and pointers are fixed.                                                     */
+gdn_status gdn_cpr_decode_step(const gdn_cpr_shape *shape, const void *q, const void *k,
+                               const void *v, const float *g, const float *beta,
+                               const int32_t *slot, const gdn_cpr_cache *cache, void *o,
+                               void *ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* Trainer forward (case "trainer_fwd" next to "engine_prefill" on the IsoExec page,
+ * section on contract structure).  Identical arithmetic to gdn_cpr_prefill -- o and
+ * state_out are bit-identical -- and additionally saves the boundary states:
+ *   saved_bnd [sum_s ceil(L_s/C), H_v, d_v, d_k] fp32: the state before every chunk, chunks
+ *             numbered in sequence order (chunk 0 of a sequence holds its state_in).     */
+gdn_status gdn_cpr_fwd(const gdn_cpr_shape *shape, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const float *state_in,
+                       const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host, void *o,
+                       float *state_out, float *saved_bnd, void *ws, size_t ws_bytes,
+                       gdn_stream_t stream);
+
+/* Trainer backward (IsoExec page, CPR timing table row "Trainer Fwd+Bwd").  Gradient of
+ * loss = <dO, o> + <dstate_out, state_out> with respect to every input, where o and
+ * state_out are gdn_cpr_fwd's outputs.  Uses saved_bnd from gdn_cpr_fwd on the same
+ * inputs.  Reverse chain over chunks for the boundary adjoints, then every chunk in
+ * parallel; grouped-head dq/dk are summed over the value heads of a group in ascending
+ * order; no atomics, so results are deterministic.
+ *   dO [T, H_v, d_v] out_dtype; dstate_out NULL (= 0) or [N, H_v, d_v, d_k] fp32
+ *   dq, dk [T, H_qk, d_k] fp32; dv [T, H_v, d_v] fp32; dg, dbeta [T, H_v] fp32
+ *   dstate_in NULL or [N, H_v, d_v, d_k] fp32                                            */
+gdn_status gdn_cpr_bwd(const gdn_cpr_shape *shape, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, const float *state_in,
+                       const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
+                       const float *saved_bnd, const void *dO, const float *dstate_out,
+                       float *dq, float *dk, float *dv, float *dg, float *dbeta,
+                       float *dstate_in, void *ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* Optional profiling hook (per calling thread; NULL disables it, the default).  While set,
+ * every entry point called from this thread records events[i] (cudaEvent_t handles created
+ * by the caller) on its stream at its stage boundaries -- events[0] before its first
+ * kernel, events[s] after stage s -- for as many stages as it has, up to n_events, and
+ * adds the number of kernels it launched to *kernels.  Stages:
+ *   prefill / fwd : 1 work list, 2 boundary pre-pass, 3 boundary chain, 4 intra-chunk
+ *                   recurrence, 5 cache tail (prefill with a cache only)
+ *   decode_step   : 1 token step, 2 resync pre-pass, 3 resync chain, 4 position advance
+ *   bwd           : see gdn_cpr_bwd's stages in the implementation notes
+ * The structure must stay valid while set.  Has no effect on results.                   */
+typedef struct {
+    void *events[16];   /* cudaEvent_t */
+    int32_t n_events;   /* how many of events[] are valid */
+    int32_t stages;     /* set by each call: how many stage events it recorded (incl. [0]) */
+    int64_t kernels;    /* incremented by each call by the kernels it launched */
+} gdn_cpr_profile;
+
+void gdn_cpr_set_profile(gdn_cpr_profile *profile);
+
+/* Synchronises `stream`, then reads the device error word of `ws` (the workspace of the
+ * last call queued with it) into *code (a gdn_device_error).  Returns GDN_OK when the
+ * word is clear, GDN_ERR_DEVICE when it is set, GDN_ERR_CUDA if the sync or copy fails. */
+gdn_status gdn_cpr_get_device_error(const void *ws, gdn_stream_t stream, int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_CPR_H */
