@@ -26,7 +26,8 @@ DEVERR = {0: "none", 1: "cu_seqlens mismatch", 2: "slot out of range", 3: "negat
 # every function the header declares (checked by the CPU test suite)
 EXPORTS = ("gdn_cpr_version", "gdn_cpr_status_string", "gdn_cpr_workspace_size",
            "gdn_cpr_prefill", "gdn_cpr_decode_step", "gdn_cpr_fwd", "gdn_cpr_bwd",
-           "gdn_cpr_get_device_error", "gdn_cpr_set_profile")
+           "gdn_cpr_get_device_error", "gdn_cpr_set_profile", "gdn_cpr_decode_step_noalloc")
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class GdnError(RuntimeError):
@@ -77,6 +78,8 @@ def load():
             lib.gdn_cpr_fwd.argtypes = [P] * 13 + [S, P]
             lib.gdn_cpr_bwd.argtypes = [P] * 19 + [S, P]
             lib.gdn_cpr_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
+            lib.gdn_cpr_decode_step_noalloc.argtypes = [P] * 10
+            lib.gdn_cpr_decode_step_noalloc.restype = I
             lib.gdn_cpr_set_profile.argtypes = [P]
             lib.gdn_cpr_set_profile.restype = None
             for fn in ("gdn_cpr_workspace_size", "gdn_cpr_prefill", "gdn_cpr_decode_step",
@@ -240,6 +243,25 @@ def decode_step(q, k, v, g, beta, slot, cache: Cache, out_dtype=None, ws=None, o
                                  _p(slot), ctypes.byref(cs), _p(o), _p(ws), ws.numel(),
                                  _stream(q.device))
     _check("gdn_cpr_decode_step", rc)
+    return o
+
+
+def decode_step_noalloc(q, k, v, g, beta, slot, cache: Cache, out_dtype=None, o=None):
+    """gdn_cpr_decode_step_noalloc: the decode step with its workspace in the library's
+    built-in device array, for callers that cannot allocate device memory.  The library
+    allocates nothing; only the output `o`, if not given, is allocated here by torch."""
+    lib = load()
+    N, hqk, d = k.shape
+    hv = v.shape[1]
+    od = out_dtype or q.dtype
+    shape = make_shape(N, N, hqk, hv, d, cache.chunk, q.dtype, od)
+    if o is None:
+        o = torch.empty((N, hv, d), dtype=od, device=q.device)
+    cs = cache.struct()
+    rc = lib.gdn_cpr_decode_step_noalloc(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g),
+                                         _p(beta), _p(slot), ctypes.byref(cs), _p(o),
+                                         _stream(q.device))
+    _check("gdn_cpr_decode_step_noalloc", rc)
     return o
 
 

@@ -224,6 +224,32 @@ typedef struct {
 
 void gdn_cpr_set_profile(gdn_cpr_profile *profile);
 
+/* Size of the built-in device scratch used by gdn_cpr_decode_step_noalloc (64 MiB). */
+#define GDN_CPR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* gdn_cpr_decode_step without a caller-provided workspace, for callers that cannot
+ * allocate device memory (a serving loop whose memory is reserved up front by another
+ * allocator, code that must not call cudaMalloc while other GPU work is captured or
+ * replayed, or a plain C host with no device allocator).  The IsoExec pages have no
+ * counterpart: this is a deployment convenience, not part of CPR.
+ *   Arguments, results and bits are exactly those of gdn_cpr_decode_step; only the
+ *   workspace differs.  It lives in one file-scope device array of
+ *   GDN_CPR_NOALLOC_SCRATCH_BYTES that every GPU which loads this library's module holds
+ *   until the process exits.  The call itself allocates nothing (no cudaMalloc/cudaFree).
+ *   Limit: the decode workspace of the shape (gdn_cpr_workspace_size with
+ *   GDN_MODE_DECODE) must fit the array -- about 1000 (token, value head) pairs per step at
+ *   d = 128, C = 64 (e.g. 31 slots x 32 heads); larger requests return GDN_ERR_WORKSPACE
+ *   and queue nothing.
+ *   The first call on a device looks up the array's device address (with that device
+ *   current); make that first call before capturing any stream into a CUDA graph.
+ *   Every call on a device shares the array and leaves its contents behind; the step
+ *   clears what must start at zero.  Calls that overlap on the GPU (other streams, other
+ *   threads, concurrent graph replays) race on the array: serialise them.               */
+gdn_status gdn_cpr_decode_step_noalloc(const gdn_cpr_shape *shape, const void *q, const void *k,
+                                       const void *v, const float *g, const float *beta,
+                                       const int32_t *slot, const gdn_cpr_cache *cache, void *o,
+                                       gdn_stream_t stream);
+
 /* Synchronises `stream`, then reads the device error word of `ws` (the workspace of the
  * last call queued with it) into *code (a gdn_device_error).  Returns GDN_OK when the
  * word is clear, GDN_ERR_DEVICE when it is set, GDN_ERR_CUDA if the sync or copy fails. */
