@@ -114,7 +114,8 @@ void launch_worklist(const int32_t* cu, int N, int T, int C, int64_t n_chunks, u
 // Shared-memory plan (floats): Ks[64][D+4] Vs[64][D+4] A[64][65] T[64][65] + 5 vectors.
 template <int D>
 constexpr size_t prep_smem_bytes() {
-  return sizeof(float) * (2 * kMaxChunk * (D + 4) + 2 * kMaxChunk * (kMaxChunk + 1) + 5 * kMaxChunk + 4);
+  return sizeof(float) * (2 * kMaxChunk * (D + 4) + 2 * kMaxChunk * (kMaxChunk + 1) + 5 * kMaxChunk +
+                          3 * 16 * 16 + 4);
 }
 
 template <int D, typename Tin>
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
   float* bs = Gs + kMaxChunk;
   float* bk = bs + kMaxChunk;
   float* dec = bk + kMaxChunk;
+  float* Xs = dec + kMaxChunk;  // off-diagonal block scratch of the triangular solve
 
   const int t = threadIdx.x;
   const int C = dm.C;
@@ -203,18 +205,43 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
     }
   }
   __syncthreads();
-  // 4. T = (I + A)^{-1} by forward substitution, one column per thread:
-  //    T[r][r] = 1,  T[i][r] = -sum_{m=r}^{i-1} A[i][m] T[m][r]  (m ascending)
+  // 4. T = (I + A)^{-1}, blocked by 16.  Diagonal blocks by forward substitution, one
+  //    column per thread:  T[r][r] = 1,  T[i][r] = -sum_{m=r}^{i-1} A[i][m] T[m][r].
+  //    Off-diagonal blocks (I > J) by increasing I - J:
+  //      X[i][r] = sum_{m=r}^{16I-1} A[i][m] T[m][r],   T[i][r] = -sum_{m=16I}^{i} T[i][m] X[m][r]
+  //    (every sum in ascending m, one accumulator).
+  constexpr int TB = 16;
+  const int nb = C / TB;
   if (t < C) {
-    const int r = t;
+    const int r = t, rend = (r / TB) * TB + TB;
     Tm[r * CP + r] = 1.f;
-    for (int i = r + 1; i < C; ++i) {
+    for (int i = r + 1; i < rend; ++i) {
       float acc = 0.f;
       for (int m = r; m < i; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
       Tm[i * CP + r] = -acc;
     }
   }
   __syncthreads();
+  for (int off = 1; off < nb; ++off) {
+    const int nel = (nb - off) * TB * TB;
+    for (int e = t; e < nel; e += kPrepThreads) {
+      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
+      const int i = I * TB + ii, r = (I - off) * TB + rr;
+      float acc = 0.f;
+      for (int m = r; m < I * TB; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
+      Xs[e] = acc;
+    }
+    __syncthreads();
+    for (int e = t; e < nel; e += kPrepThreads) {
+      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
+      const int i = I * TB + ii, r = (I - off) * TB + rr;
+      const float* X = Xs + (e / (TB * TB)) * TB * TB;
+      float acc = 0.f;
+      for (int m = I * TB; m <= i; ++m) acc = __fmaf_rn(Tm[i * CP + m], X[(m - I * TB) * TB + rr], acc);
+      Tm[i * CP + r] = -acc;
+    }
+    __syncthreads();
+  }
   // 5. TK = T diag(beta e^G) (into A), TV = T diag(beta) (in place)
   for (int o = t; o < C * C; o += kPrepThreads) {
     const int i = o / C, r = o % C;
@@ -226,18 +253,33 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
   }
   __syncthreads();
   // 6. Wd[i][c] = dec_i * sum_{r<=i} TK[i][r] K[r][c];  Ud[i][c] = dec_i * sum_{r<=i} TV[i][r] V[r][c]
+  //    (r ascending).  Each thread owns one column c and every RG-th row.
   constexpr int RG = kPrepThreads / D;  // row groups
-  const int c = t % D;
+  constexpr int RPT = kMaxChunk / RG;   // rows per thread at the largest chunk
+  const int c = t % D, i0 = t / D;
   float* Wo = Wout + ((item * dm.hv + h) * C) * (int64_t)D;
   float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
-  for (int i = t / D; i < C; i += RG) {
-    float aw = 0.f, au = 0.f;
-    for (int r = 0; r <= i; ++r) {
-      aw = __fmaf_rn(A[i * CP + r], Ks[r * DP + c], aw);
-      au = __fmaf_rn(Tm[i * CP + r], Vs[r * DP + c], au);
+  float aw[RPT], au[RPT];
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) aw[j] = au[j] = 0.f;
+  for (int r = 0; r < C; ++r) {
+    const float kv = Ks[r * DP + c], vv = Vs[r * DP + c];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int i = i0 + RG * j;
+      if (i >= r && i < C) {
+        aw[j] = __fmaf_rn(A[i * CP + r], kv, aw[j]);
+        au[j] = __fmaf_rn(Tm[i * CP + r], vv, au[j]);
+      }
     }
-    Wo[i * D + c] = __fmul_rn(dec[i], aw);
-    Uo[i * D + c] = __fmul_rn(dec[i], au);
+  }
+#pragma unroll
+  for (int j = 0; j < RPT; ++j) {
+    const int i = i0 + RG * j;
+    if (i < C) {
+      Wo[i * D + c] = __fmul_rn(dec[i], aw[j]);
+      Uo[i * D + c] = __fmul_rn(dec[i], au[j]);
+    }
   }
   if (t == 0) gamma_out[item * dm.hv + h] = expf(Gs[C - 1]);
 }
@@ -285,16 +327,50 @@ __device__ __forceinline__ void chain_step(float* Ss, float* Ws, float* Ks, floa
     *reinterpret_cast<float4*>(Us + s * R + 4 * i4) = *reinterpret_cast<const float4*>(Ug + s * D + r0 + 4 * i4);
   }
   __syncthreads();
-  for (int o = t; o < C * R; o += kChainThreads) {
-    const int s = o % C, i = o / C;
-    Vd[s * R + i] = __fsub_rn(Us[s * R + i], dot_canon<D>(Ws + s * DP, Ss + i * DP));
+  {  // Vd: thread owns row i = t / 16 and chunk rows s = t % 16 + 16 j
+    const int i = t / 16, s0 = t % 16;
+    constexpr int SJ = kMaxChunk / 16;
+    float p[SJ][4];
+#pragma unroll
+    for (int j = 0; j < SJ; ++j) p[j][0] = p[j][1] = p[j][2] = p[j][3] = 0.f;
+#pragma unroll 4
+    for (int m = 0; m < D / 4; ++m) {
+      const float4 sv = *reinterpret_cast<const float4*>(Ss + i * DP + 4 * m);
+#pragma unroll
+      for (int j = 0; j < SJ; ++j) {
+        if (s0 + 16 * j < C) {
+          const float4 wv = *reinterpret_cast<const float4*>(Ws + (s0 + 16 * j) * DP + 4 * m);
+          p[j][0] = __fmaf_rn(wv.x, sv.x, p[j][0]);
+          p[j][1] = __fmaf_rn(wv.y, sv.y, p[j][1]);
+          p[j][2] = __fmaf_rn(wv.z, sv.z, p[j][2]);
+          p[j][3] = __fmaf_rn(wv.w, sv.w, p[j][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < SJ; ++j) {
+      const int s = s0 + 16 * j;
+      if (s < C) {
+        const float dot = __fadd_rn(__fadd_rn(p[j][0], p[j][1]), __fadd_rn(p[j][2], p[j][3]));
+        Vd[s * R + i] = __fsub_rn(Us[s * R + i], dot);
+      }
+    }
   }
   __syncthreads();
-  for (int o = t; o < R * D; o += kChainThreads) {
-    const int i = o / D, c = o % D;
-    float acc = __fmul_rn(gamma, Ss[i * DP + c]);
-    for (int s = 0; s < C; ++s) acc = __fmaf_rn(Vd[s * R + i], Ks[s * DP + c], acc);
-    Ss[i * DP + c] = acc;
+  {  // S <- gamma S + Vd^T K: thread owns column c and rows i0 + RG j
+    constexpr int RG = kChainThreads / D;
+    constexpr int RJ = R / RG;
+    const int c = t % D, i0 = t / D;
+    float acc[RJ];
+#pragma unroll
+    for (int j = 0; j < RJ; ++j) acc[j] = __fmul_rn(gamma, Ss[(i0 + RG * j) * DP + c]);
+    for (int s = 0; s < C; ++s) {
+      const float kv = Ks[s * DP + c];
+#pragma unroll
+      for (int j = 0; j < RJ; ++j) acc[j] = __fmaf_rn(Vd[s * R + i0 + RG * j], kv, acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < RJ; ++j) Ss[(i0 + RG * j) * DP + c] = acc[j];
   }
   __syncthreads();
 }
@@ -399,7 +475,7 @@ constexpr size_t intra_smem_bytes() {
 }
 
 template <int D, typename Tin, typename Tout>
-__global__ void __launch_bounds__(2 * D) k_intra(Dims dm, TokenArrays in, IntraWork w,
+__global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, IntraWork w,
                                                  WsHeader* __restrict__ hdr) {
   extern __shared__ __align__(16) float sm[];
   float* ks = sm;
