@@ -97,6 +97,24 @@ DecLayout dec_layout(const gdn_cpr_shape* s) {
   return L;
 }
 
+struct BwdLayout {
+  size_t chunks, seqs, per_chunk, dq_part, dk_part, total;
+};
+
+BwdLayout bwd_layout(const gdn_cpr_shape* s, int64_t n_chunks) {
+  const size_t D = s->d_k, C = s->chunk, hv = s->h_v, T = s->total_tokens;
+  BwdLayout L;
+  size_t off = align_up(sizeof(WsHeader));
+  L.chunks = off;    off = align_up(off + sizeof(ChunkRec) * (size_t)n_chunks);
+  L.seqs = off;      off = align_up(off + sizeof(SeqRec) * (size_t)s->num_seqs);
+  L.per_chunk = off; off = align_up(off + sizeof(float) * (size_t)n_chunks * hv *
+                                              bwd_workspace_floats_per_chunk_head((int)C, (int)D));
+  L.dq_part = off;   off = align_up(off + sizeof(float) * T * hv * D);
+  L.dk_part = off;   off = align_up(off + sizeof(float) * T * hv * D);
+  L.total = off;
+  return L;
+}
+
 inline char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 
 gdn_status check_cache(const gdn_cpr_cache* c) {
@@ -130,6 +148,8 @@ struct Stages {
     ++next;
   }
 };
+
+void stage_mark(void* ctx, int kernels) { static_cast<Stages*>(ctx)->mark(kernels); }
 
 gdn_status finish(cudaStream_t st) {
   (void)st;
@@ -260,7 +280,7 @@ gdn_status gdn_cpr_workspace_size(const gdn_cpr_shape* shape, gdn_mode mode,
   switch (mode) {
     case GDN_MODE_PREFILL: *bytes = fwd_layout(shape, n_chunks, true).total; return GDN_OK;
     case GDN_MODE_FWD: *bytes = fwd_layout(shape, n_chunks, false).total; return GDN_OK;
-    case GDN_MODE_BWD: return GDN_ERR_UNSUPPORTED;
+    case GDN_MODE_BWD: *bytes = bwd_layout(shape, n_chunks).total; return GDN_OK;
     default: return GDN_ERR_INVALID_ARG;
   }
 }
@@ -357,11 +377,40 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k,
                        const float* saved_bnd, const void* dO, const float* dstate_out,
                        float* dq, float* dk, float* dv, float* dg, float* dbeta,
                        float* dstate_in, void* ws, size_t ws_bytes, gdn_stream_t stream) {
-  (void)shape; (void)q; (void)k; (void)v; (void)g; (void)beta; (void)state_in;
-  (void)cu_seqlens_dev; (void)cu_seqlens_host; (void)saved_bnd; (void)dO; (void)dstate_out;
-  (void)dq; (void)dk; (void)dv; (void)dg; (void)dbeta; (void)dstate_in; (void)ws;
-  (void)ws_bytes; (void)stream;
-  return GDN_ERR_UNSUPPORTED;
+  (void)state_in;  // its contribution reaches the backward through saved_bnd (chunk 0)
+  gdn_status rc = check_shape(shape);
+  if (rc != GDN_OK) return rc;
+  int64_t n_chunks = 0;
+  uint32_t hash = 0;
+  rc = scan_cu(shape, cu_seqlens_host, &n_chunks, &hash);
+  if (rc != GDN_OK) return rc;
+  const int N = shape->num_seqs;
+  const int64_t T = shape->total_tokens;
+  if (T > 0 && (!ok_ptr(q, 16) || !ok_ptr(k, 16) || !ok_ptr(v, 16) || !ok_ptr(g, 4) ||
+                !ok_ptr(beta, 4) || !ok_ptr(dO, 16) || !ok_ptr(dq, 16) || !ok_ptr(dk, 16) ||
+                !ok_ptr(dv, 16) || !ok_ptr(dg, 4) || !ok_ptr(dbeta, 4)))
+    return GDN_ERR_INVALID_ARG;
+  if (n_chunks > 0 && !ok_ptr(saved_bnd, 16)) return GDN_ERR_INVALID_ARG;
+  if (N > 0 && !ok_ptr(cu_seqlens_dev, 4)) return GDN_ERR_INVALID_ARG;
+  if ((dstate_out && !aligned(dstate_out, 16)) || (dstate_in && !aligned(dstate_in, 16)))
+    return GDN_ERR_INVALID_ARG;
+  const BwdLayout L = bwd_layout(shape, n_chunks);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if (N == 0) return GDN_OK;
+  const Dims d = dims_of(shape);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  ChunkRec* chunks = reinterpret_cast<ChunkRec*>(at(ws, L.chunks));
+  SeqRec* seqs = reinterpret_cast<SeqRec*>(at(ws, L.seqs));
+  TokenArrays in{q, k, v, g, beta};
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
+  Stages stg(stream);
+  launch_worklist(cu_seqlens_dev, N, (int)T, d.C, n_chunks, hash, chunks, seqs, hdr, stream);
+  stg.mark(1);
+  launch_bwd(d, in, dO, chunks, seqs, N, n_chunks, T, saved_bnd, dstate_out, dstate_in,
+             reinterpret_cast<float*>(at(ws, L.per_chunk)), reinterpret_cast<float*>(at(ws, L.dq_part)),
+             reinterpret_cast<float*>(at(ws, L.dk_part)), dq, dk, dv, dg, dbeta, hdr, stage_mark,
+             &stg, stream);
+  return finish(stream);
 }
 
 void gdn_cpr_set_profile(gdn_cpr_profile* profile) { t_profile = profile; }

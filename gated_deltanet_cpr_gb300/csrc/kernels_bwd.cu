@@ -1,0 +1,808 @@
+// kernels_bwd.cu -- reverse mode of CPR Gated DeltaNet for sm_103a (trainer backward; the
+// IsoExec page's CPR timing table, row "Trainer Fwd+Bwd").
+//
+// The backward follows the forward's schedule in reverse.  Chunk j (local tokens
+// i = 0..n-1, zero-padded to C) with start state S0 = S^(j) computes, in exact arithmetic,
+//     G = cumsum g,  Gam_is = e^{G_i - G_s},  A_is = beta_i Gam_is k_i.k_s (i > s),
+//     T = (I + A)^{-1},  W = T diag(beta e^G) K,  Ut = T diag(beta) V,  U = Ut - W S0^T,
+//     P_is = Gam_is q_i.k_s (i >= s),  O = diag(e^G) Q S0^T + P U,
+//     S_end = e^{G_last} S0 + U^T diag(dec) K,   dec_s = e^{G_last - G_s},
+// which is the token recurrence rewritten.  Its reverse mode:
+//   KB1 k_bwd_prep   per chunk: G, T, W, Ut, P and the chunk's own adjoint of S0,
+//                    L = dO^T (diag(e^G) Q - P W)
+//   KB2 k_bwd_chain  per (sequence, head, 16-row block), chunks in reverse order:
+//                    dS^(j) = L_j + e^{G_last} dS^(j+1) - (dS^(j+1) K^T) diag(dec) W,
+//                    starting from dstate_out; dstate_in = dS^(0)
+//   KB3 k_bwd_big    per chunk: the products with the d x d matrices S0 and dS_end:
+//                    U, dU = P^T dO + diag(dec) K dS_end^T, dO S0, U dS_end, dW = -dU S0,
+//                    <dS_end, S0>
+//   KB4 k_bwd_grad   per chunk: X = T^T dU, Y = T^T dW, dA = -(X Ut^T + Y W^T) (strictly lower)
+//                    and the gradients of q, k, v, g, beta (per value head)
+//   KB5 k_bwd_gqa    dq, dk summed over the value heads of each group, ascending
+// Every sum has one fixed order, there are no atomics, and nothing depends on the batch
+// composition, so the backward is deterministic.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "../../include/gdn_cpr.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace gdn {
+namespace {
+
+constexpr int NT = 256;
+constexpr int CP = kMaxChunk + 1;  // padded row of a C x C matrix in shared memory
+
+template <typename F>
+void ensure_smem_bwd(F* fn, size_t bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.insert({reinterpret_cast<const void*>(fn), dev}).second)
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// rows [0, n) of a row-major source (row r at src + r * stride), widened to fp32, into
+// dst[r * ld + c]; rows [n, C) are zero.
+template <int D, typename T>
+__device__ __forceinline__ void load_rows(float* dst, int ld, const T* src, int64_t stride, int n,
+                                          int C) {
+  for (int idx = threadIdx.x; idx < C * (D / 8); idx += NT) {
+    const int r = idx / (D / 8), c8 = idx % (D / 8);
+    float tmp[8];
+    if (r < n) {
+      load8(src + r * stride + 8 * c8, tmp);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) tmp[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[r * ld + 8 * c8 + e] = tmp[e];
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void load_rows_any(float* dst, int ld, const void* src, bool bf16,
+                                              int64_t stride, int n, int C) {
+  if (bf16)
+    load_rows<D>(dst, ld, static_cast<const __nv_bfloat16*>(src), stride, n, C);
+  else
+    load_rows<D>(dst, ld, static_cast<const float*>(src), stride, n, C);
+}
+
+// Each thread owns a TM x TN tile of the M x N product sum_k a(m, k) b(k, n) (k ascending,
+// one accumulator per output) and hands every output to epi(m, n, value).
+template <int TM, int TN, typename FA, typename FB, typename Epi>
+__device__ __forceinline__ void gemm(int M, int N, int K, FA a, FB b, Epi epi) {
+  const int ntn = N / TN;
+  const int tiles = (M / TM) * ntn;
+  for (int tile = threadIdx.x; tile < tiles; tile += NT) {
+    const int m0 = (tile / ntn) * TM, n0 = (tile % ntn) * TN;
+    float acc[TM][TN];
+#pragma unroll
+    for (int r = 0; r < TM; ++r)
+#pragma unroll
+      for (int c = 0; c < TN; ++c) acc[r][c] = 0.f;
+    for (int k = 0; k < K; ++k) {
+      float av[TM], bv[TN];
+#pragma unroll
+      for (int r = 0; r < TM; ++r) av[r] = a(m0 + r, k);
+#pragma unroll
+      for (int c = 0; c < TN; ++c) bv[c] = b(k, n0 + c);
+#pragma unroll
+      for (int r = 0; r < TM; ++r)
+#pragma unroll
+        for (int c = 0; c < TN; ++c) acc[r][c] = __fmaf_rn(av[r], bv[c], acc[r][c]);
+    }
+#pragma unroll
+    for (int r = 0; r < TM; ++r)
+#pragma unroll
+      for (int c = 0; c < TN; ++c) epi(m0 + r, n0 + c, acc[r][c]);
+  }
+}
+
+// T = (I + A)^{-1} for strictly lower A (C x C in shared memory, row stride CP), blocked
+// by 16: diagonal blocks by forward substitution (one column per thread), then the
+// off-diagonal blocks by increasing distance from the diagonal.  Xs: 3*16*16 floats.
+__device__ __forceinline__ void unit_lower_inverse(const float* A, float* Tm, float* Xs, int C) {
+  constexpr int TB = 16;
+  const int t = threadIdx.x;
+  const int nb = C / TB;
+  for (int idx = t; idx < C * C; idx += NT) Tm[(idx / C) * CP + idx % C] = 0.f;
+  __syncthreads();
+  if (t < C) {
+    const int r = t, rend = (r / TB) * TB + TB;
+    Tm[r * CP + r] = 1.f;
+    for (int i = r + 1; i < rend; ++i) {
+      float acc = 0.f;
+      for (int m = r; m < i; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
+      Tm[i * CP + r] = -acc;
+    }
+  }
+  __syncthreads();
+  for (int off = 1; off < nb; ++off) {
+    const int nel = (nb - off) * TB * TB;
+    for (int e = t; e < nel; e += NT) {
+      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
+      const int i = I * TB + ii, r = (I - off) * TB + rr;
+      float acc = 0.f;
+      for (int m = r; m < I * TB; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
+      Xs[e] = acc;
+    }
+    __syncthreads();
+    for (int e = t; e < nel; e += NT) {
+      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
+      const int i = I * TB + ii, r = (I - off) * TB + rr;
+      const float* X = Xs + (e / (TB * TB)) * TB * TB;
+      float acc = 0.f;
+      for (int m = I * TB; m <= i; ++m) acc = __fmaf_rn(Tm[i * CP + m], X[(m - I * TB) * TB + rr], acc);
+      Tm[i * CP + r] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
+// Per chunk-head workspace (floats), chunk length padded to C.
+struct BwdBufs {
+  float *W, *Ut, *T, *P, *G, *L, *dSE, *U, *dU, *dOS0, *UdSe, *dW, *sdot;
+  float *dq_part, *dk_part;  // [T, Hv, D]
+};
+
+struct BwdArgs {
+  Dims dm;
+  TokenArrays in;
+  const void* dO;
+  const ChunkRec* chunks;
+  const SeqRec* seqs;
+  const float* saved_bnd;
+  const float* dstate_out;
+  float* dstate_in;
+  BwdBufs b;
+  float *dq, *dk, *dv, *dg, *dbeta;
+  int64_t T;
+  WsHeader* hdr;
+};
+
+// ===================================================================  KB1  ====
+template <int D>
+constexpr size_t bprep_smem() {
+  return sizeof(float) * (4 * kMaxChunk * (D + 4) + 2 * kMaxChunk * CP + 6 * kMaxChunk + 3 * 256);
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(NT) k_bwd_prep(BwdArgs a) {
+  constexpr int DP = D + 4;
+  extern __shared__ __align__(16) float sm[];
+  float* B0 = sm;                 // K, then dO
+  float* B1 = B0 + kMaxChunk * DP;  // V, then Ut
+  float* B2 = B1 + kMaxChunk * DP;  // W
+  float* B3 = B2 + kMaxChunk * DP;  // Q, then Qt = diag(e^G) Q - P W
+  float* M0 = B3 + kMaxChunk * DP;  // A, then P
+  float* M1 = M0 + kMaxChunk * CP;  // T
+  float* gs = M1 + kMaxChunk * CP;
+  float* Gs = gs + kMaxChunk;
+  float* bs = Gs + kMaxChunk;
+  float* eG = bs + kMaxChunk;
+  float* bk = eG + kMaxChunk;
+  float* Xs = bk + 2 * kMaxChunk;
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, C = dm.C;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const ChunkRec rec = a.chunks[c];
+  const int n = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t ch = c * dm.hv + h;
+  const Tin* kin = static_cast<const Tin*>(a.in.k);
+  const Tin* vin = static_cast<const Tin*>(a.in.v);
+  const Tin* qin = static_cast<const Tin*>(a.in.q);
+
+  load_rows<D>(B0, DP, kin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
+  load_rows<D>(B1, DP, vin + (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n, C);
+  if (t < C) {
+    gs[t] = t < n ? a.in.g[(tok0 + t) * dm.hv + h] : 0.f;
+    bs[t] = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float run = gs[0];
+    Gs[0] = run;
+    for (int i = 1; i < C; ++i) {
+      run = __fadd_rn(run, gs[i]);
+      Gs[i] = run;
+    }
+  }
+  __syncthreads();
+  if (t < C) {
+    eG[t] = expf(Gs[t]);
+    bk[t] = __fmul_rn(bs[t], eG[t]);
+  }
+  for (int o = t; o < C * C; o += NT) {
+    const int i = o / C, s = o % C;
+    M0[i * CP + s] = (i > s) ? __fmul_rn(__fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s]))),
+                                         dot_canon<D>(B0 + i * DP, B0 + s * DP))
+                             : 0.f;
+  }
+  __syncthreads();
+  unit_lower_inverse(M0, M1, Xs, C);
+  // W = T diag(beta e^G) K, Ut = T diag(beta) V (r ascending)
+  constexpr int RG = NT / D;
+  constexpr int RPT = kMaxChunk / RG;
+  {
+    const int cc = t % D, i0 = t / D;
+    float aw[RPT], au[RPT];
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) aw[j] = au[j] = 0.f;
+    for (int r = 0; r < C; ++r) {
+      const float kv = B0[r * DP + cc], vv = B1[r * DP + cc];
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) {
+        const int i = i0 + RG * j;
+        if (i >= r && i < C) {
+          const float tr = M1[i * CP + r];
+          aw[j] = __fmaf_rn(__fmul_rn(tr, bk[r]), kv, aw[j]);
+          au[j] = __fmaf_rn(__fmul_rn(tr, bs[r]), vv, au[j]);
+        }
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int i = i0 + RG * j;
+      if (i < C) {
+        B2[i * DP + cc] = aw[j];
+        B1[i * DP + cc] = au[j];
+        a.b.W[ch * C * D + i * D + cc] = aw[j];
+        a.b.Ut[ch * C * D + i * D + cc] = au[j];
+      }
+    }
+  }
+  for (int o = t; o < C * C; o += NT) a.b.T[ch * C * C + o] = M1[(o / C) * CP + o % C];
+  if (t < C) a.b.G[ch * C + t] = Gs[t];
+  load_rows<D>(B3, DP, qin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
+  __syncthreads();
+  // P = Gam * (Q K^T), lower triangle with diagonal
+  gemm<4, 4>(C, C, D, [&](int i, int k) { return B3[i * DP + k]; },
+             [&](int k, int s) { return B0[s * DP + k]; },
+             [&](int i, int s, float v) {
+               const float p = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
+               M0[i * CP + s] = p;
+               a.b.P[ch * C * C + i * C + s] = p;
+             });
+  __syncthreads();
+  // Qt = diag(e^G) Q - P W (in place)
+  gemm<4, 8>(C, D, C, [&](int i, int s) { return M0[i * CP + s]; },
+             [&](int s, int k) { return B2[s * DP + k]; },
+             [&](int i, int k, float v) { B3[i * DP + k] = __fsub_rn(__fmul_rn(eG[i], B3[i * DP + k]), v); });
+  __syncthreads();
+  if (a.dm.out_bf16)
+    load_rows<D>(B0, DP, static_cast<const __nv_bfloat16*>(a.dO) + (tok0 * dm.hv + h) * D,
+                 (int64_t)dm.hv * D, n, C);
+  else
+    load_rows<D>(B0, DP, static_cast<const float*>(a.dO) + (tok0 * dm.hv + h) * D,
+                 (int64_t)dm.hv * D, n, C);
+  __syncthreads();
+  // L = dO^T Qt  (D x D)
+  gemm<8, 8>(D, D, C, [&](int p, int i) { return B0[i * DP + p]; },
+             [&](int i, int q) { return B3[i * DP + q]; },
+             [&](int p, int q, float v) { a.b.L[ch * D * D + p * D + q] = v; });
+}
+
+// ===================================================================  KB2  ====
+template <int D>
+constexpr size_t bchain_smem() {
+  return sizeof(float) * (2 * kMaxChunk * (D + 4) + 2 * kRowsPerChain * (D + 4) +
+                          kMaxChunk * kRowsPerChain + 2 * kMaxChunk);
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(NT) k_bwd_chain(BwdArgs a) {
+  constexpr int DP = D + 4;
+  constexpr int R = kRowsPerChain;
+  extern __shared__ __align__(16) float sm[];
+  float* Ks = sm;
+  float* Ws = Ks + kMaxChunk * DP;
+  float* dS = Ws + kMaxChunk * DP;
+  float* Ls = dS + R * DP;
+  float* Xd = Ls + R * DP;
+  float* dec = Xd + kMaxChunk * R;
+  float* gm = dec + kMaxChunk;
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, C = dm.C;
+  const int n = blockIdx.x, h = blockIdx.y, r0 = blockIdx.z * R;
+  const int hq = h / (dm.hv / dm.hqk);
+  const SeqRec rec = a.seqs[n];
+  const int64_t SZ = (int64_t)D * D;
+  const Tin* kin = static_cast<const Tin*>(a.in.k);
+  for (int idx = t; idx < R * D; idx += NT) {
+    const int i = idx / D, cc = idx % D;
+    dS[i * DP + cc] = a.dstate_out ? a.dstate_out[((int64_t)n * dm.hv + h) * SZ + (int64_t)(r0 + i) * D + cc] : 0.f;
+  }
+  __syncthreads();
+  for (int j = rec.nchunks - 1; j >= 0; --j) {
+    const int64_t c = (int64_t)rec.chunk0 + j;
+    const ChunkRec cr = a.chunks[c];
+    const int64_t ch = c * dm.hv + h;
+    for (int idx = t; idx < R * D; idx += NT) {
+      const int i = idx / D, cc = idx % D;
+      a.b.dSE[ch * SZ + (int64_t)(r0 + i) * D + cc] = dS[i * DP + cc];
+      Ls[i * DP + cc] = a.b.L[ch * SZ + (int64_t)(r0 + i) * D + cc];
+    }
+    load_rows<D>(Ks, DP, kin + ((int64_t)cr.tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, cr.len, C);
+    load_rows<D>(Ws, DP, a.b.W + ch * C * D, D, C, C);
+    if (t < C) dec[t] = expf(__fsub_rn(a.b.G[ch * C + C - 1], a.b.G[ch * C + t]));
+    if (t == 0) gm[0] = expf(a.b.G[ch * C + C - 1]);
+    __syncthreads();
+    {  // Xd[s][i] = -dec_s (k_s . dS_i)
+      const int i = t / 16, s0 = t % 16;
+      for (int s = s0; s < C; s += 16)
+        Xd[s * R + i] = __fmul_rn(-dec[s], dot_canon<D>(Ks + s * DP, dS + i * DP));
+    }
+    __syncthreads();
+    {  // dS <- L + gamma dS + sum_s Xd[s][i] W[s]
+      constexpr int RG = NT / D;
+      constexpr int RJ = R / RG;
+      const int cc = t % D, i0 = t / D;
+      const float g = gm[0];
+      float acc[RJ];
+#pragma unroll
+      for (int jj = 0; jj < RJ; ++jj) {
+        const int i = i0 + RG * jj;
+        acc[jj] = __fadd_rn(Ls[i * DP + cc], __fmul_rn(g, dS[i * DP + cc]));
+      }
+      for (int s = 0; s < C; ++s) {
+        const float wv = Ws[s * DP + cc];
+#pragma unroll
+        for (int jj = 0; jj < RJ; ++jj) acc[jj] = __fmaf_rn(Xd[s * R + i0 + RG * jj], wv, acc[jj]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int jj = 0; jj < RJ; ++jj) dS[(i0 + RG * jj) * DP + cc] = acc[jj];
+    }
+    __syncthreads();
+  }
+  if (a.dstate_in) {
+    for (int idx = t; idx < R * D; idx += NT) {
+      const int i = idx / D, cc = idx % D;
+      a.dstate_in[((int64_t)n * dm.hv + h) * SZ + (int64_t)(r0 + i) * D + cc] = dS[i * DP + cc];
+    }
+  }
+}
+
+// ===================================================================  KB3  ====
+template <int D>
+constexpr size_t bbig_smem() {
+  return sizeof(float) * (4 * kMaxChunk * (D + 4) + kMaxChunk * CP + D * (D + 4) + kMaxChunk + NT);
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(NT) k_bwd_big(BwdArgs a) {
+  constexpr int DP = D + 4;
+  extern __shared__ __align__(16) float sm[];
+  float* B0 = sm;                   // W, then dU
+  float* B1 = B0 + kMaxChunk * DP;  // Ut, then U
+  float* B2 = B1 + kMaxChunk * DP;  // dO
+  float* B3 = B2 + kMaxChunk * DP;  // K
+  float* M0 = B3 + kMaxChunk * DP;  // P
+  float* SM = M0 + kMaxChunk * CP;  // S0, dS_end, S0
+  float* dec = SM + D * DP;
+  float* red = dec + kMaxChunk;
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, C = dm.C;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const ChunkRec rec = a.chunks[c];
+  const int n = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t ch = c * dm.hv + h;
+  const int64_t SZ = (int64_t)D * D;
+  const Tin* kin = static_cast<const Tin*>(a.in.k);
+  load_rows<D>(B0, DP, a.b.W + ch * C * D, D, C, C);
+  load_rows<D>(B1, DP, a.b.Ut + ch * C * D, D, C, C);
+  load_rows_any<D>(B2, DP, a.dm.out_bf16
+                               ? static_cast<const void*>(static_cast<const __nv_bfloat16*>(a.dO) + (tok0 * dm.hv + h) * D)
+                               : static_cast<const void*>(static_cast<const float*>(a.dO) + (tok0 * dm.hv + h) * D),
+                   a.dm.out_bf16, (int64_t)dm.hv * D, n, C);
+  load_rows<D>(B3, DP, kin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
+  for (int o = t; o < C * C; o += NT) M0[(o / C) * CP + o % C] = a.b.P[ch * C * C + o];
+  if (t < C) dec[t] = expf(__fsub_rn(a.b.G[ch * C + C - 1], a.b.G[ch * C + t]));
+  load_rows<D>(SM, DP, a.saved_bnd + ch * SZ, D, D, D);
+  __syncthreads();
+  // U = Ut - W S0^T (in place), dO S0
+  gemm<4, 8>(C, D, D, [&](int s, int b) { return B0[s * DP + b]; },
+             [&](int b, int q) { return SM[q * DP + b]; },
+             [&](int s, int q, float v) {
+               const float u = __fsub_rn(B1[s * DP + q], v);
+               B1[s * DP + q] = u;
+               a.b.U[ch * C * D + s * D + q] = u;
+             });
+  gemm<4, 8>(C, D, D, [&](int i, int p) { return B2[i * DP + p]; },
+             [&](int p, int q) { return SM[p * DP + q]; },
+             [&](int i, int q, float v) { a.b.dOS0[ch * C * D + i * D + q] = v; });
+  __syncthreads();
+  {  // S0 -> dS_end, accumulating <dS_end, S0>
+    float part = 0.f;
+    for (int e = t; e < D * D; e += NT) {
+      const int p = e / D, q = e % D;
+      const float nw = a.b.dSE[ch * SZ + e];
+      part = __fmaf_rn(nw, SM[p * DP + q], part);
+      SM[p * DP + q] = nw;
+    }
+    red[t] = part;
+    __syncthreads();
+    for (int w = NT / 2; w > 0; w >>= 1) {
+      if (t < w) red[t] = __fadd_rn(red[t], red[t + w]);
+      __syncthreads();
+    }
+    if (t == 0) a.b.sdot[ch] = red[0];
+  }
+  // dU = P^T dO + diag(dec) K dS_end^T
+  gemm<4, 8>(C, D, C, [&](int s, int i) { return M0[i * CP + s]; },
+             [&](int i, int q) { return B2[i * DP + q]; },
+             [&](int s, int q, float v) { B0[s * DP + q] = v; });
+  __syncthreads();
+  gemm<4, 8>(C, D, D, [&](int s, int b) { return B3[s * DP + b]; },
+             [&](int b, int q) { return SM[q * DP + b]; },
+             [&](int s, int q, float v) {
+               const float du = __fmaf_rn(dec[s], v, B0[s * DP + q]);
+               B0[s * DP + q] = du;
+               a.b.dU[ch * C * D + s * D + q] = du;
+             });
+  // U dS_end
+  gemm<4, 8>(C, D, D, [&](int s, int p) { return B1[s * DP + p]; },
+             [&](int p, int q) { return SM[p * DP + q]; },
+             [&](int s, int q, float v) { a.b.UdSe[ch * C * D + s * D + q] = v; });
+  __syncthreads();
+  load_rows<D>(SM, DP, a.saved_bnd + ch * SZ, D, D, D);
+  __syncthreads();
+  // dW = -dU S0
+  gemm<4, 8>(C, D, D, [&](int s, int p) { return B0[s * DP + p]; },
+             [&](int p, int q) { return SM[p * DP + q]; },
+             [&](int s, int q, float v) { a.b.dW[ch * C * D + s * D + q] = -v; });
+}
+
+// ===================================================================  KB4  ====
+template <int D>
+constexpr size_t bgrad_smem() {
+  return sizeof(float) * (5 * kMaxChunk * (D + 4) + 2 * kMaxChunk * CP + 16 * kMaxChunk);
+}
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(NT) k_bwd_grad(BwdArgs a) {
+  constexpr int DP = D + 4;
+  extern __shared__ __align__(16) float sm[];
+  float* B0 = sm;                   // dO -> dU -> Y
+  float* B1 = B0 + kMaxChunk * DP;  // U -> dW -> W -> Ut -> U dS_end
+  float* B2 = B1 + kMaxChunk * DP;  // Q
+  float* B3 = B2 + kMaxChunk * DP;  // K
+  float* B4 = B3 + kMaxChunk * DP;  // dO S0 -> X
+  float* M0 = B4 + kMaxChunk * DP;  // Pm -> A' = Gam k.k
+  float* M1 = M0 + kMaxChunk * CP;  // QK -> T -> dA -> dAm
+  float* Gs = M1 + kMaxChunk * CP;
+  float* eG = Gs + kMaxChunk;
+  float* dec = eG + kMaxChunk;
+  float* bs = dec + kMaxChunk;
+  float* dGa = bs + kMaxChunk;
+  float* dGb = dGa + kMaxChunk;
+  float* dGe = dGb + kMaxChunk;
+  float* kY = dGe + kMaxChunk;
+  float* dba = kY + kMaxChunk;
+  float* dbc = dba + kMaxChunk;
+  float* cs = dbc + kMaxChunk;
+  float* dgv = cs + kMaxChunk;
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, C = dm.C;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const ChunkRec rec = a.chunks[c];
+  const int n = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t ch = c * dm.hv + h;
+  const Tin* kin = static_cast<const Tin*>(a.in.k);
+  const Tin* qin = static_cast<const Tin*>(a.in.q);
+  const Tin* vin = static_cast<const Tin*>(a.in.v);
+  const float* Gc = a.b.G + ch * C;
+
+  // ---- pass A: Pm = Gam * (dO U^T) (lower with diagonal), QK strictly lower, dG from P
+  load_rows_any<D>(B0, DP, a.dm.out_bf16
+                               ? static_cast<const void*>(static_cast<const __nv_bfloat16*>(a.dO) + (tok0 * dm.hv + h) * D)
+                               : static_cast<const void*>(static_cast<const float*>(a.dO) + (tok0 * dm.hv + h) * D),
+                   a.dm.out_bf16, (int64_t)dm.hv * D, n, C);
+  load_rows<D>(B1, DP, a.b.U + ch * C * D, D, C, C);
+  load_rows<D>(B2, DP, qin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
+  load_rows<D>(B3, DP, kin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
+  if (t < C) {
+    Gs[t] = Gc[t];
+    bs[t] = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
+  }
+  __syncthreads();
+  if (t < C) {
+    eG[t] = expf(Gs[t]);
+    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
+  }
+  gemm<4, 4>(C, C, D, [&](int i, int k) { return B0[i * DP + k]; },
+             [&](int k, int s) { return B1[s * DP + k]; },
+             [&](int i, int s, float v) {
+               M0[i * CP + s] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
+             });
+  gemm<4, 4>(C, C, D, [&](int i, int k) { return B2[i * DP + k]; },
+             [&](int k, int s) { return B3[s * DP + k]; },
+             [&](int i, int s, float v) { M1[i * CP + s] = (i > s) ? v : 0.f; });
+  __syncthreads();
+  if (t < C) {
+    float row = 0.f, col = 0.f;
+    for (int s = 0; s < t; ++s) row = __fmaf_rn(M0[t * CP + s], M1[t * CP + s], row);
+    for (int i = t + 1; i < C; ++i) col = __fmaf_rn(M0[i * CP + t], M1[i * CP + t], col);
+    dGb[t] = __fsub_rn(row, col);
+  }
+  // ---- pass B: dQ = diag(e^G) dO S0 + Pm K;  dK <- Pm^T Q
+  load_rows<D>(B4, DP, a.b.dOS0 + ch * C * D, D, C, C);
+  __syncthreads();
+  gemm<4, 8>(C, D, C, [&](int i, int s) { return M0[i * CP + s]; },
+             [&](int s, int k) { return B3[s * DP + k]; },
+             [&](int i, int k, float v) {
+               if (i < n) a.b.dq_part[((tok0 + i) * dm.hv + h) * D + k] = __fmaf_rn(eG[i], B4[i * DP + k], v);
+             });
+  if (t < C) dGa[t] = __fmul_rn(eG[t], dot_canon<D>(B4 + t * DP, B2 + t * DP));
+  constexpr int KTN = 8;
+  const int ntn = D / KTN;
+  const bool owns = t < (C / 4) * ntn;
+  const int km0 = (t / ntn) * 4, kn0 = (t % ntn) * KTN;
+  float dk[4][KTN];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int q = 0; q < KTN; ++q) dk[r][q] = 0.f;
+  if (owns) {
+    for (int i = 0; i < C; ++i) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float pm = M0[i * CP + km0 + r];
+#pragma unroll
+        for (int q = 0; q < KTN; ++q) dk[r][q] = __fmaf_rn(pm, B2[i * DP + kn0 + q], dk[r][q]);
+      }
+    }
+  }
+  __syncthreads();
+  // ---- pass C: X = T^T dU -> B4, Y = T^T dW -> B0, dV, kY, dbeta(v)
+  load_rows<D>(B0, DP, a.b.dU + ch * C * D, D, C, C);
+  load_rows<D>(B1, DP, a.b.dW + ch * C * D, D, C, C);
+  for (int o = t; o < C * C; o += NT) M1[(o / C) * CP + o % C] = a.b.T[ch * C * C + o];
+  __syncthreads();
+  gemm<4, 8>(C, D, C, [&](int s, int r) { return M1[r * CP + s]; },
+             [&](int r, int k) { return B0[r * DP + k]; },
+             [&](int s, int k, float v) { B4[s * DP + k] = v; });
+  __syncthreads();
+  gemm<4, 8>(C, D, C, [&](int s, int r) { return M1[r * CP + s]; },
+             [&](int r, int k) { return B1[r * DP + k]; },
+             [&](int s, int k, float v) { B0[s * DP + k] = v; });
+  __syncthreads();
+  for (int idx = t; idx < C * D; idx += NT) {
+    const int i = idx / D, k = idx % D;
+    if (i < n) a.dv[((tok0 + i) * dm.hv + h) * D + k] = __fmul_rn(bs[i], B4[i * DP + k]);
+  }
+  if (t < C) {
+    kY[t] = dot_canon<D>(B3 + t * DP, B0 + t * DP);
+    float acc = 0.f;
+    if (t < n) {
+      const Tin* vr = vin + ((tok0 + t) * dm.hv + h) * D;
+      for (int k = 0; k < D; ++k) acc = __fmaf_rn(to_f32(vr[k]), B4[t * DP + k], acc);
+    }
+    dba[t] = acc;
+  }
+  // ---- pass D: dA = -(Y W^T + X Ut^T) strictly lower; A' = Gam k.k; dG, dbeta from A
+  load_rows<D>(B1, DP, a.b.W + ch * C * D, D, C, C);
+  __syncthreads();
+  gemm<4, 4>(C, C, D, [&](int i, int k) { return B0[i * DP + k]; },
+             [&](int k, int s) { return B1[s * DP + k]; },
+             [&](int i, int s, float v) { M1[i * CP + s] = (i > s) ? -v : 0.f; });
+  __syncthreads();
+  load_rows<D>(B1, DP, a.b.Ut + ch * C * D, D, C, C);
+  __syncthreads();
+  gemm<4, 4>(C, C, D, [&](int i, int k) { return B4[i * DP + k]; },
+             [&](int k, int s) { return B1[s * DP + k]; },
+             [&](int i, int s, float v) {
+               if (i > s) M1[i * CP + s] = __fsub_rn(M1[i * CP + s], v);
+             });
+  gemm<4, 4>(C, C, D, [&](int i, int k) { return B3[i * DP + k]; },
+             [&](int k, int s) { return B3[s * DP + k]; },
+             [&](int i, int s, float v) {
+               M0[i * CP + s] = (i > s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
+             });
+  __syncthreads();
+  if (t < C) {
+    float b = 0.f, row = 0.f, col = 0.f;
+    for (int s = 0; s < t; ++s) {
+      b = __fmaf_rn(M1[t * CP + s], M0[t * CP + s], b);
+      row = __fmaf_rn(__fmul_rn(M1[t * CP + s], bs[t]), M0[t * CP + s], row);
+    }
+    for (int i = t + 1; i < C; ++i) col = __fmaf_rn(__fmul_rn(M1[i * CP + t], bs[i]), M0[i * CP + t], col);
+    dbc[t] = b;
+    dGe[t] = __fsub_rn(row, col);
+  }
+  __syncthreads();
+  for (int o = t; o < C * C; o += NT) {  // dAm = dA * beta_i * Gam_is
+    const int i = o / C, s = o % C;
+    if (i > s)
+      M1[i * CP + s] = __fmul_rn(__fmul_rn(M1[i * CP + s], bs[i]), expf(__fsub_rn(Gs[i], Gs[s])));
+  }
+  load_rows<D>(B1, DP, a.b.UdSe + ch * C * D, D, C, C);
+  __syncthreads();
+  // ---- pass E: dK += dAm K + dAm^T K + diag(dec) U dS_end + diag(beta e^G) Y
+  if (owns) {
+    for (int r = 0; r < C; ++r) {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const float am = M1[(km0 + rr) * CP + r];
+#pragma unroll
+        for (int q = 0; q < KTN; ++q) dk[rr][q] = __fmaf_rn(am, B3[r * DP + kn0 + q], dk[rr][q]);
+      }
+    }
+    for (int r = 0; r < C; ++r) {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const float am = M1[r * CP + km0 + rr];
+#pragma unroll
+        for (int q = 0; q < KTN; ++q) dk[rr][q] = __fmaf_rn(am, B3[r * DP + kn0 + q], dk[rr][q]);
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int s = km0 + rr;
+      const float bkv = __fmul_rn(bs[s], eG[s]);
+#pragma unroll
+      for (int q = 0; q < KTN; ++q) {
+        float v = __fmaf_rn(dec[s], B1[s * DP + kn0 + q], dk[rr][q]);
+        v = __fmaf_rn(bkv, B0[s * DP + kn0 + q], v);
+        if (s < n) a.b.dk_part[((tok0 + s) * dm.hv + h) * D + kn0 + q] = v;
+      }
+    }
+  }
+  if (t < C) cs[t] = __fmul_rn(dec[t], dot_canon<D>(B1 + t * DP, B3 + t * DP));
+  __syncthreads();
+  // ---- pass F: dG, reverse cumulative sum -> dg; dbeta
+  if (t == 0) {
+    float tot = 0.f;
+    for (int s = 0; s < C; ++s) tot = __fadd_rn(tot, cs[s]);
+    float run = 0.f;
+    for (int i = C - 1; i >= 0; --i) {
+      float v = __fadd_rn(dGa[i], dGb[i]);
+      v = __fsub_rn(v, cs[i]);
+      v = __fmaf_rn(__fmul_rn(bs[i], eG[i]), kY[i], v);
+      v = __fadd_rn(v, dGe[i]);
+      if (i == C - 1) v = __fadd_rn(v, __fmaf_rn(expf(Gs[C - 1]), a.b.sdot[ch], tot));
+      run = __fadd_rn(run, v);
+      dgv[i] = run;
+    }
+  }
+  __syncthreads();
+  if (t < n) {
+    a.dg[(tok0 + t) * dm.hv + h] = dgv[t];
+    a.dbeta[(tok0 + t) * dm.hv + h] = __fadd_rn(__fmaf_rn(eG[t], kY[t], dba[t]), dbc[t]);
+  }
+}
+
+// ===================================================================  KB5  ====
+__global__ void k_bwd_gqa(const float* __restrict__ dq_part, const float* __restrict__ dk_part,
+                          float* __restrict__ dq, float* __restrict__ dk, int64_t T, int hqk,
+                          int hv, int D, const WsHeader* __restrict__ hdr) {
+  if (!hdr->valid) return;
+  const int grp = hv / hqk;
+  const int64_t total = T * hqk * D;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tok = e / ((int64_t)hqk * D);
+    const int hq = (int)((e / D) % hqk), k = (int)(e % D);
+    const int64_t base = (tok * hv + (int64_t)hq * grp) * D + k;
+    float sq = dq_part[base], sk = dk_part[base];
+    for (int j = 1; j < grp; ++j) {
+      sq = __fadd_rn(sq, dq_part[base + (int64_t)j * D]);
+      sk = __fadd_rn(sk, dk_part[base + (int64_t)j * D]);
+    }
+    dq[e] = sq;
+    dk[e] = sk;
+  }
+}
+
+template <int D, typename Tin>
+void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, void* mark_ctx,
+                  cudaStream_t st) {
+  const dim3 gc((unsigned)n_chunks, a.dm.hv);
+  if (n_chunks > 0) {
+    ensure_smem_bwd(k_bwd_prep<D, Tin>, bprep_smem<D>());
+    k_bwd_prep<D, Tin><<<gc, NT, bprep_smem<D>(), st>>>(a);
+  }
+  mark(mark_ctx, n_chunks > 0 ? 1 : 0);
+  ensure_smem_bwd(k_bwd_chain<D, Tin>, bchain_smem<D>());
+  k_bwd_chain<D, Tin><<<dim3((unsigned)N, a.dm.hv, D / kRowsPerChain), NT, bchain_smem<D>(), st>>>(a);
+  mark(mark_ctx, 1);
+  if (n_chunks > 0) {
+    ensure_smem_bwd(k_bwd_big<D, Tin>, bbig_smem<D>());
+    k_bwd_big<D, Tin><<<gc, NT, bbig_smem<D>(), st>>>(a);
+  }
+  mark(mark_ctx, n_chunks > 0 ? 1 : 0);
+  if (n_chunks > 0) {
+    ensure_smem_bwd(k_bwd_grad<D, Tin>, bgrad_smem<D>());
+    k_bwd_grad<D, Tin><<<gc, NT, bgrad_smem<D>(), st>>>(a);
+  }
+  mark(mark_ctx, n_chunks > 0 ? 1 : 0);
+  if (a.T > 0) {
+    const int64_t total = a.T * a.dm.hqk * D;
+    const int blocks = (int)((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
+    k_bwd_gqa<<<blocks, 256, 0, st>>>(a.b.dq_part, a.b.dk_part, a.dq, a.dk, a.T, a.dm.hqk, a.dm.hv, D, a.hdr);
+  }
+  mark(mark_ctx, a.T > 0 ? 1 : 0);
+}
+
+}  // namespace
+
+size_t bwd_workspace_floats_per_chunk_head(int C, int D) {
+  return (size_t)7 * C * D + 2 * (size_t)C * C + C + 2 * (size_t)D * D + 1;
+}
+
+void launch_bwd(const Dims& d, const TokenArrays& in, const void* dO, const ChunkRec* chunks,
+                const SeqRec* seqs, int N, int64_t n_chunks, int64_t T, const float* saved_bnd,
+                const float* dstate_out, float* dstate_in, float* per_chunk, float* dq_part,
+                float* dk_part, float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                WsHeader* hdr, BwdStageFn mark, void* mark_ctx, cudaStream_t st) {
+  BwdArgs a{};
+  a.dm = d;
+  a.in = in;
+  a.dO = dO;
+  a.chunks = chunks;
+  a.seqs = seqs;
+  a.saved_bnd = saved_bnd;
+  a.dstate_out = dstate_out;
+  a.dstate_in = dstate_in;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dg = dg;
+  a.dbeta = dbeta;
+  a.T = T;
+  a.hdr = hdr;
+  const size_t C = d.C, D = d.D, nch = (size_t)n_chunks * d.hv;
+  float* p = per_chunk;
+  a.b.W = p;    p += nch * C * D;
+  a.b.Ut = p;   p += nch * C * D;
+  a.b.U = p;    p += nch * C * D;
+  a.b.dU = p;   p += nch * C * D;
+  a.b.dOS0 = p; p += nch * C * D;
+  a.b.UdSe = p; p += nch * C * D;
+  a.b.dW = p;   p += nch * C * D;
+  a.b.T = p;    p += nch * C * C;
+  a.b.P = p;    p += nch * C * C;
+  a.b.L = p;    p += nch * D * D;
+  a.b.dSE = p;  p += nch * D * D;
+  a.b.G = p;    p += nch * C;
+  a.b.sdot = p; p += nch;
+  a.b.dq_part = dq_part;
+  a.b.dk_part = dk_part;
+  if (d.in_bf16) {
+    switch (d.D) {
+      case 32: launch_bwd_t<32, __nv_bfloat16>(a, n_chunks, N, mark, mark_ctx, st); break;
+      case 64: launch_bwd_t<64, __nv_bfloat16>(a, n_chunks, N, mark, mark_ctx, st); break;
+      default: launch_bwd_t<128, __nv_bfloat16>(a, n_chunks, N, mark, mark_ctx, st); break;
+    }
+  } else {
+    switch (d.D) {
+      case 32: launch_bwd_t<32, float>(a, n_chunks, N, mark, mark_ctx, st); break;
+      case 64: launch_bwd_t<64, float>(a, n_chunks, N, mark, mark_ctx, st); break;
+      default: launch_bwd_t<128, float>(a, n_chunks, N, mark, mark_ctx, st); break;
+    }
+  }
+}
+
+}  // namespace gdn

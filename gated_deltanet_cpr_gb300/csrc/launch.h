@@ -109,4 +109,14 @@ void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, 
                       float* tail_g, float* tail_beta, int32_t* pos, WsHeader* hdr,
                       cudaStream_t st);
 
+// Backward (kernels_bwd.cu).  `mark(ctx, kernels)` is called after each stage (prep,
+// chain, big products, gradients, grouped-head sum) with the kernels it launched.
+typedef void (*BwdStageFn)(void* ctx, int kernels);
+size_t bwd_workspace_floats_per_chunk_head(int C, int D);
+void launch_bwd(const Dims& d, const TokenArrays& in, const void* dO, const ChunkRec* chunks,
+                const SeqRec* seqs, int N, int64_t n_chunks, int64_t T, const float* saved_bnd,
+                const float* dstate_out, float* dstate_in, float* per_chunk, float* dq_part,
+                float* dk_part, float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                WsHeader* hdr, BwdStageFn mark, void* mark_ctx, cudaStream_t st);
+
 }  // namespace gdn
