@@ -353,6 +353,11 @@ def run_cuda(args):
     pre_k = [pp.stage_ms() for pp, _, _ in profs]
     names = ["worklist", "boundary_prepass", "boundary_chain", "intra_chunk", "cache_tail"]
     kern = {n: statistics.mean(s[i] for s in pre_k) for i, n in enumerate(names) if all(len(s) > i for s in pre_k)}
+    bwd_k = [pf.stage_ms() for _, pf, _ in profs]
+    bnames = ["bwd_worklist", "bwd_prep", "bwd_chain", "bwd_big_products", "bwd_gradients", "bwd_gqa_sum"]
+    if have_bwd:
+        kern.update({n: statistics.mean(s[i] for s in bwd_k) for i, n in enumerate(bnames)
+                     if all(len(s) > i for s in bwd_k)})
 
     # dominant kernel: intra-chunk recurrence (FP32 ALU bound)
     intra_ms = kern["intra_chunk"]

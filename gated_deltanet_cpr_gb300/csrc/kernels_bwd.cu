@@ -37,7 +37,7 @@ namespace gdn {
 namespace {
 
 constexpr int NT = 256;
-constexpr int CP = kMaxChunk + 1;  // padded row of a C x C matrix in shared memory
+constexpr int CP = kMaxChunk + 4;  // padded row of a C x C matrix in shared memory (16-byte rows)
 
 template <typename F>
 void ensure_smem_bwd(F* fn, size_t bytes) {
@@ -78,35 +78,87 @@ __device__ __forceinline__ void load_rows_any(float* dst, int ld, const void* sr
     load_rows<D>(dst, ld, static_cast<const float*>(src), stride, n, C);
 }
 
-// Each thread owns a TM x TN tile of the M x N product sum_k a(m, k) b(k, n) (k ascending,
-// one accumulator per output) and hands every output to epi(m, n, value).
-template <int TM, int TN, typename FA, typename FB, typename Epi>
-__device__ __forceinline__ void gemm(int M, int N, int K, FA a, FB b, Epi epi) {
+// D(m, n) = sum_k A(m, k) B(k, n) over shared-memory operands, k ascending with one
+// accumulator per output, every output handed to epi(m, n, value).  Layouts:
+//   AT = false: A(m, k) = A[m * lda + k]      AT = true: A(m, k) = A[k * lda + m]
+//   BT = false: B(k, n) = B[k * ldb + n]      BT = true: B(k, n) = B[n * ldb + k]
+// NN and TN: a thread owns a contiguous TM x TN tile; B (and A when AT) are read as float4
+// rows along n (m).  NT: a thread owns rows m = mt + r M/TM and columns n = nt + c N/TN, and
+// both operands are read as float4 along k, so neighbouring threads read neighbouring rows
+// (row strides of 4 mod 32 words keep those reads free of bank conflicts).
+// Requires: TM, TN, K multiples of 4; lda, ldb multiples of 4; 16-byte aligned operands.
+template <int TM, int TN, bool AT, bool BT, typename Epi>
+__device__ __forceinline__ void gemm(int M, int N, int K, const float* __restrict__ A, int lda,
+                                     const float* __restrict__ B, int ldb, Epi epi) {
   const int ntn = N / TN;
   const int tiles = (M / TM) * ntn;
   for (int tile = threadIdx.x; tile < tiles; tile += NT) {
-    const int m0 = (tile / ntn) * TM, n0 = (tile % ntn) * TN;
     float acc[TM][TN];
 #pragma unroll
     for (int r = 0; r < TM; ++r)
 #pragma unroll
       for (int c = 0; c < TN; ++c) acc[r][c] = 0.f;
-    for (int k = 0; k < K; ++k) {
-      float av[TM], bv[TN];
+    if constexpr (BT) {
+      static_assert(!AT, "TT products are not used");
+      const int mt = tile / ntn, nt = tile % ntn;
+      const int ms = M / TM, ns = N / TN;
+      for (int k = 0; k < K; k += 4) {
+        float4 av[TM], bv[TN];
 #pragma unroll
-      for (int r = 0; r < TM; ++r) av[r] = a(m0 + r, k);
+        for (int r = 0; r < TM; ++r) av[r] = *reinterpret_cast<const float4*>(A + (mt + r * ms) * lda + k);
 #pragma unroll
-      for (int c = 0; c < TN; ++c) bv[c] = b(k, n0 + c);
+        for (int c = 0; c < TN; ++c) bv[c] = *reinterpret_cast<const float4*>(B + (nt + c * ns) * ldb + k);
+#pragma unroll
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+          for (int c = 0; c < TN; ++c) {
+            acc[r][c] = __fmaf_rn(av[r].x, bv[c].x, acc[r][c]);
+            acc[r][c] = __fmaf_rn(av[r].y, bv[c].y, acc[r][c]);
+            acc[r][c] = __fmaf_rn(av[r].z, bv[c].z, acc[r][c]);
+            acc[r][c] = __fmaf_rn(av[r].w, bv[c].w, acc[r][c]);
+          }
+      }
 #pragma unroll
       for (int r = 0; r < TM; ++r)
 #pragma unroll
-        for (int c = 0; c < TN; ++c) acc[r][c] = __fmaf_rn(av[r], bv[c], acc[r][c]);
+        for (int c = 0; c < TN; ++c) epi(mt + r * ms, nt + c * ns, acc[r][c]);
+    } else {
+      const int m0 = (tile / ntn) * TM, n0 = (tile % ntn) * TN;
+      for (int k = 0; k < K; ++k) {
+        float av[TM], bv[TN];
+        if constexpr (AT) {
+#pragma unroll
+          for (int r = 0; r < TM; r += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(A + k * lda + m0 + r);
+            av[r] = x.x; av[r + 1] = x.y; av[r + 2] = x.z; av[r + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < TM; ++r) av[r] = A[(m0 + r) * lda + k];
+        }
+#pragma unroll
+        for (int c = 0; c < TN; c += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(B + k * ldb + n0 + c);
+          bv[c] = x.x; bv[c + 1] = x.y; bv[c + 2] = x.z; bv[c + 3] = x.w;
+        }
+#pragma unroll
+        for (int r = 0; r < TM; ++r)
+#pragma unroll
+          for (int c = 0; c < TN; ++c) acc[r][c] = __fmaf_rn(av[r], bv[c], acc[r][c]);
+      }
+#pragma unroll
+      for (int r = 0; r < TM; ++r)
+#pragma unroll
+        for (int c = 0; c < TN; ++c) epi(m0 + r, n0 + c, acc[r][c]);
     }
-#pragma unroll
-    for (int r = 0; r < TM; ++r)
-#pragma unroll
-      for (int c = 0; c < TN; ++c) epi(m0 + r, n0 + c, acc[r][c]);
   }
+}
+
+// src (D x D, row-major, global) -> dst[r * DP + c] = src[c * D + r] (transposed) in shared memory
+template <int D>
+__device__ __forceinline__ void load_transposed(float* dst, const float* __restrict__ src) {
+  constexpr int DP = D + 4;
+  for (int e = threadIdx.x; e < D * D; e += NT) dst[(e % D) * DP + e / D] = src[e];
 }
 
 // T = (I + A)^{-1} for strictly lower A (C x C in shared memory, row stride CP), blocked
@@ -271,18 +323,16 @@ __global__ void __launch_bounds__(NT) k_bwd_prep(BwdArgs a) {
   load_rows<D>(B3, DP, qin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
   __syncthreads();
   // P = Gam * (Q K^T), lower triangle with diagonal
-  gemm<4, 4>(C, C, D, [&](int i, int k) { return B3[i * DP + k]; },
-             [&](int k, int s) { return B0[s * DP + k]; },
-             [&](int i, int s, float v) {
-               const float p = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
-               M0[i * CP + s] = p;
-               a.b.P[ch * C * C + i * C + s] = p;
-             });
+  gemm<4, 4, false, true>(C, C, D, B3, DP, B0, DP, [&](int i, int s, float v) {
+    const float p = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
+    M0[i * CP + s] = p;
+    a.b.P[ch * C * C + i * C + s] = p;
+  });
   __syncthreads();
   // Qt = diag(e^G) Q - P W (in place)
-  gemm<4, 8>(C, D, C, [&](int i, int s) { return M0[i * CP + s]; },
-             [&](int s, int k) { return B2[s * DP + k]; },
-             [&](int i, int k, float v) { B3[i * DP + k] = __fsub_rn(__fmul_rn(eG[i], B3[i * DP + k]), v); });
+  gemm<4, 8, false, false>(C, D, C, M0, CP, B2, DP, [&](int i, int k, float v) {
+    B3[i * DP + k] = __fsub_rn(__fmul_rn(eG[i], B3[i * DP + k]), v);
+  });
   __syncthreads();
   if (a.dm.out_bf16)
     load_rows<D>(B0, DP, static_cast<const __nv_bfloat16*>(a.dO) + (tok0 * dm.hv + h) * D,
@@ -292,9 +342,8 @@ __global__ void __launch_bounds__(NT) k_bwd_prep(BwdArgs a) {
                  (int64_t)dm.hv * D, n, C);
   __syncthreads();
   // L = dO^T Qt  (D x D)
-  gemm<8, 8>(D, D, C, [&](int p, int i) { return B0[i * DP + p]; },
-             [&](int i, int q) { return B3[i * DP + q]; },
-             [&](int p, int q, float v) { a.b.L[ch * D * D + p * D + q] = v; });
+  gemm<8, 8, true, false>(D, D, C, B0, DP, B3, DP,
+                          [&](int p, int q, float v) { a.b.L[ch * D * D + p * D + q] = v; });
 }
 
 // ===================================================================  KB2  ====
@@ -417,59 +466,53 @@ __global__ void __launch_bounds__(NT) k_bwd_big(BwdArgs a) {
   load_rows<D>(B3, DP, kin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
   for (int o = t; o < C * C; o += NT) M0[(o / C) * CP + o % C] = a.b.P[ch * C * C + o];
   if (t < C) dec[t] = expf(__fsub_rn(a.b.G[ch * C + C - 1], a.b.G[ch * C + t]));
+  load_transposed<D>(SM, a.saved_bnd + ch * SZ);
+  __syncthreads();
+  // U = Ut - W S0^T (in place; SM holds S0^T)
+  gemm<4, 8, false, false>(C, D, D, B0, DP, SM, DP, [&](int s, int q, float v) {
+    const float u = __fsub_rn(B1[s * DP + q], v);
+    B1[s * DP + q] = u;
+    a.b.U[ch * C * D + s * D + q] = u;
+  });
+  {  // <dS_end, S0> straight from global memory
+    float part = 0.f;
+    for (int e = t; e < D * D; e += NT) part = __fmaf_rn(a.b.dSE[ch * SZ + e], a.saved_bnd[ch * SZ + e], part);
+    red[t] = part;
+  }
+  __syncthreads();
+  for (int w = NT / 2; w > 0; w >>= 1) {
+    if (t < w) red[t] = __fadd_rn(red[t], red[t + w]);
+    __syncthreads();
+  }
+  if (t == 0) a.b.sdot[ch] = red[0];
   load_rows<D>(SM, DP, a.saved_bnd + ch * SZ, D, D, D);
   __syncthreads();
-  // U = Ut - W S0^T (in place), dO S0
-  gemm<4, 8>(C, D, D, [&](int s, int b) { return B0[s * DP + b]; },
-             [&](int b, int q) { return SM[q * DP + b]; },
-             [&](int s, int q, float v) {
-               const float u = __fsub_rn(B1[s * DP + q], v);
-               B1[s * DP + q] = u;
-               a.b.U[ch * C * D + s * D + q] = u;
-             });
-  gemm<4, 8>(C, D, D, [&](int i, int p) { return B2[i * DP + p]; },
-             [&](int p, int q) { return SM[p * DP + q]; },
-             [&](int i, int q, float v) { a.b.dOS0[ch * C * D + i * D + q] = v; });
+  // dO S0
+  gemm<4, 8, false, false>(C, D, D, B2, DP, SM, DP,
+                           [&](int i, int q, float v) { a.b.dOS0[ch * C * D + i * D + q] = v; });
+  // dU = P^T dO (+ below)
+  gemm<4, 8, true, false>(C, D, C, M0, CP, B2, DP, [&](int s, int q, float v) { B0[s * DP + q] = v; });
   __syncthreads();
-  {  // S0 -> dS_end, accumulating <dS_end, S0>
-    float part = 0.f;
-    for (int e = t; e < D * D; e += NT) {
-      const int p = e / D, q = e % D;
-      const float nw = a.b.dSE[ch * SZ + e];
-      part = __fmaf_rn(nw, SM[p * DP + q], part);
-      SM[p * DP + q] = nw;
-    }
-    red[t] = part;
-    __syncthreads();
-    for (int w = NT / 2; w > 0; w >>= 1) {
-      if (t < w) red[t] = __fadd_rn(red[t], red[t + w]);
-      __syncthreads();
-    }
-    if (t == 0) a.b.sdot[ch] = red[0];
-  }
-  // dU = P^T dO + diag(dec) K dS_end^T
-  gemm<4, 8>(C, D, C, [&](int s, int i) { return M0[i * CP + s]; },
-             [&](int i, int q) { return B2[i * DP + q]; },
-             [&](int s, int q, float v) { B0[s * DP + q] = v; });
+  load_transposed<D>(SM, a.b.dSE + ch * SZ);
   __syncthreads();
-  gemm<4, 8>(C, D, D, [&](int s, int b) { return B3[s * DP + b]; },
-             [&](int b, int q) { return SM[q * DP + b]; },
-             [&](int s, int q, float v) {
-               const float du = __fmaf_rn(dec[s], v, B0[s * DP + q]);
-               B0[s * DP + q] = du;
-               a.b.dU[ch * C * D + s * D + q] = du;
-             });
+  // dU += diag(dec) K dS_end^T (SM holds dS_end^T)
+  gemm<4, 8, false, false>(C, D, D, B3, DP, SM, DP, [&](int s, int q, float v) {
+    const float du = __fmaf_rn(dec[s], v, B0[s * DP + q]);
+    B0[s * DP + q] = du;
+    a.b.dU[ch * C * D + s * D + q] = du;
+  });
+  __syncthreads();
+  load_rows<D>(SM, DP, a.b.dSE + ch * SZ, D, D, D);
+  __syncthreads();
   // U dS_end
-  gemm<4, 8>(C, D, D, [&](int s, int p) { return B1[s * DP + p]; },
-             [&](int p, int q) { return SM[p * DP + q]; },
-             [&](int s, int q, float v) { a.b.UdSe[ch * C * D + s * D + q] = v; });
+  gemm<4, 8, false, false>(C, D, D, B1, DP, SM, DP,
+                           [&](int s, int q, float v) { a.b.UdSe[ch * C * D + s * D + q] = v; });
   __syncthreads();
   load_rows<D>(SM, DP, a.saved_bnd + ch * SZ, D, D, D);
   __syncthreads();
   // dW = -dU S0
-  gemm<4, 8>(C, D, D, [&](int s, int p) { return B0[s * DP + p]; },
-             [&](int p, int q) { return SM[p * DP + q]; },
-             [&](int s, int q, float v) { a.b.dW[ch * C * D + s * D + q] = -v; });
+  gemm<4, 8, false, false>(C, D, D, B0, DP, SM, DP,
+                           [&](int s, int q, float v) { a.b.dW[ch * C * D + s * D + q] = -v; });
 }
 
 // ===================================================================  KB4  ====
@@ -532,14 +575,11 @@ __global__ void __launch_bounds__(NT) k_bwd_grad(BwdArgs a) {
     eG[t] = expf(Gs[t]);
     dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
   }
-  gemm<4, 4>(C, C, D, [&](int i, int k) { return B0[i * DP + k]; },
-             [&](int k, int s) { return B1[s * DP + k]; },
-             [&](int i, int s, float v) {
-               M0[i * CP + s] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
-             });
-  gemm<4, 4>(C, C, D, [&](int i, int k) { return B2[i * DP + k]; },
-             [&](int k, int s) { return B3[s * DP + k]; },
-             [&](int i, int s, float v) { M1[i * CP + s] = (i > s) ? v : 0.f; });
+  gemm<4, 4, false, true>(C, C, D, B0, DP, B1, DP, [&](int i, int s, float v) {
+    M0[i * CP + s] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
+  });
+  gemm<4, 4, false, true>(C, C, D, B2, DP, B3, DP,
+                          [&](int i, int s, float v) { M1[i * CP + s] = (i > s) ? v : 0.f; });
   __syncthreads();
   if (t < C) {
     float row = 0.f, col = 0.f;
@@ -550,11 +590,9 @@ __global__ void __launch_bounds__(NT) k_bwd_grad(BwdArgs a) {
   // ---- pass B: dQ = diag(e^G) dO S0 + Pm K;  dK <- Pm^T Q
   load_rows<D>(B4, DP, a.b.dOS0 + ch * C * D, D, C, C);
   __syncthreads();
-  gemm<4, 8>(C, D, C, [&](int i, int s) { return M0[i * CP + s]; },
-             [&](int s, int k) { return B3[s * DP + k]; },
-             [&](int i, int k, float v) {
-               if (i < n) a.b.dq_part[((tok0 + i) * dm.hv + h) * D + k] = __fmaf_rn(eG[i], B4[i * DP + k], v);
-             });
+  gemm<4, 8, false, false>(C, D, C, M0, CP, B3, DP, [&](int i, int k, float v) {
+    if (i < n) a.b.dq_part[((tok0 + i) * dm.hv + h) * D + k] = __fmaf_rn(eG[i], B4[i * DP + k], v);
+  });
   if (t < C) dGa[t] = __fmul_rn(eG[t], dot_canon<D>(B4 + t * DP, B2 + t * DP));
   constexpr int KTN = 8;
   const int ntn = D / KTN;
@@ -581,13 +619,9 @@ __global__ void __launch_bounds__(NT) k_bwd_grad(BwdArgs a) {
   load_rows<D>(B1, DP, a.b.dW + ch * C * D, D, C, C);
   for (int o = t; o < C * C; o += NT) M1[(o / C) * CP + o % C] = a.b.T[ch * C * C + o];
   __syncthreads();
-  gemm<4, 8>(C, D, C, [&](int s, int r) { return M1[r * CP + s]; },
-             [&](int r, int k) { return B0[r * DP + k]; },
-             [&](int s, int k, float v) { B4[s * DP + k] = v; });
+  gemm<4, 8, true, false>(C, D, C, M1, CP, B0, DP, [&](int s, int k, float v) { B4[s * DP + k] = v; });
   __syncthreads();
-  gemm<4, 8>(C, D, C, [&](int s, int r) { return M1[r * CP + s]; },
-             [&](int r, int k) { return B1[r * DP + k]; },
-             [&](int s, int k, float v) { B0[s * DP + k] = v; });
+  gemm<4, 8, true, false>(C, D, C, M1, CP, B1, DP, [&](int s, int k, float v) { B0[s * DP + k] = v; });
   __syncthreads();
   for (int idx = t; idx < C * D; idx += NT) {
     const int i = idx / D, k = idx % D;
@@ -605,22 +639,17 @@ __global__ void __launch_bounds__(NT) k_bwd_grad(BwdArgs a) {
   // ---- pass D: dA = -(Y W^T + X Ut^T) strictly lower; A' = Gam k.k; dG, dbeta from A
   load_rows<D>(B1, DP, a.b.W + ch * C * D, D, C, C);
   __syncthreads();
-  gemm<4, 4>(C, C, D, [&](int i, int k) { return B0[i * DP + k]; },
-             [&](int k, int s) { return B1[s * DP + k]; },
-             [&](int i, int s, float v) { M1[i * CP + s] = (i > s) ? -v : 0.f; });
+  gemm<4, 4, false, true>(C, C, D, B0, DP, B1, DP,
+                          [&](int i, int s, float v) { M1[i * CP + s] = (i > s) ? -v : 0.f; });
   __syncthreads();
   load_rows<D>(B1, DP, a.b.Ut + ch * C * D, D, C, C);
   __syncthreads();
-  gemm<4, 4>(C, C, D, [&](int i, int k) { return B4[i * DP + k]; },
-             [&](int k, int s) { return B1[s * DP + k]; },
-             [&](int i, int s, float v) {
-               if (i > s) M1[i * CP + s] = __fsub_rn(M1[i * CP + s], v);
-             });
-  gemm<4, 4>(C, C, D, [&](int i, int k) { return B3[i * DP + k]; },
-             [&](int k, int s) { return B3[s * DP + k]; },
-             [&](int i, int s, float v) {
-               M0[i * CP + s] = (i > s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
-             });
+  gemm<4, 4, false, true>(C, C, D, B4, DP, B1, DP, [&](int i, int s, float v) {
+    if (i > s) M1[i * CP + s] = __fsub_rn(M1[i * CP + s], v);
+  });
+  gemm<4, 4, false, true>(C, C, D, B3, DP, B3, DP, [&](int i, int s, float v) {
+    M0[i * CP + s] = (i > s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
+  });
   __syncthreads();
   if (t < C) {
     float b = 0.f, row = 0.f, col = 0.f;

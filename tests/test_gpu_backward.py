@@ -2,9 +2,8 @@
 reverse recurrence (itself pinned by central finite differences in test_oracle_pins.py).
 
 Gradient of loss = <dO, o> + <dstate_out, state_out> with respect to q, k, v, g, beta and
-state_in.  Tolerance per tensor: max|GPU - oracle| / max|oracle|, <= 2e-3 for bf16 inputs;
-fp32 inputs use the same chunked arithmetic and are held to 1e-4 here (see the backward
-note in the design document for why the forward's 1e-5 does not carry over to dg).
+state_in.  Tolerance per tensor: max|GPU - oracle| / max|oracle|, <= 2e-3 for bf16 inputs
+and <= 1e-5 for fp32 inputs.
 """
 import numpy as np
 import pytest
@@ -16,7 +15,7 @@ from helpers import f64, rel_err, to_dev
 
 pytestmark = pytest.mark.gpu
 
-TOL = {synth.F32: 1e-4, synth.BF16: 2e-3}
+TOL = {synth.F32: 1e-5, synth.BF16: 2e-3}
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")
 
 
