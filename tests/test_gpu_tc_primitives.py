@@ -1,0 +1,51 @@
+"""GPU check of the tcgen05 building blocks (tc.cuh): one CTA computes D = [C +] A B^T for a
+128 x K bf16 A and an N x K bf16 B through shared-memory descriptors and a tensor-memory
+accumulator.  Products of bf16 values are exact in fp32, so the result must match an fp64
+reference to fp32 accumulation rounding."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+import torch
+
+from gated_deltanet_cpr_gb300 import build as gbuild
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    src = os.path.join(HERE, "cuda", "tc_selftest.cu")
+    out_dir = os.path.join(HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, "libtc_selftest.so")
+    subprocess.check_call([gbuild.nvcc(), *gbuild.ARCH, *gbuild.NVCC_FLAGS, "-shared", "-o", so, src])
+    L = ctypes.CDLL(so)
+    L.tc_selftest.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                      ctypes.c_void_p]
+    L.tc_selftest.restype = ctypes.c_int
+    return L
+
+
+@pytest.mark.parametrize("N,K,init", [(64, 128, False), (128, 64, False), (128, 128, True),
+                                      (16, 16, False), (256, 32, True)])
+def test_tcgen05_mma_matches_reference(lib, N, K, init):
+    g = torch.Generator().manual_seed(N * 1000 + K)
+    A = torch.randn((128, K), generator=g).to(torch.bfloat16)
+    B = torch.randn((N, K), generator=g).to(torch.bfloat16)
+    C = torch.randn((128, N), generator=g) if init else None
+    ref = A.double() @ B.double().T + (C.double() if init else 0.0)
+    dA, dB = A.cuda(), B.cuda()
+    dC = C.cuda() if init else None
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.tc_selftest(dA.data_ptr(), dB.data_ptr(), None if dC is None else dC.data_ptr(),
+                         D.data_ptr(), N, K, status.data_ptr(),
+                         torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, "bounded wait gave up"
+    err = (D.double().cpu() - ref).abs().max().item() / ref.abs().max().item()
+    assert err < 1e-5, err
