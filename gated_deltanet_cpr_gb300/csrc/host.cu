@@ -73,7 +73,7 @@ FwdLayout fwd_layout(const gdn_cpr_shape* s, int64_t n_chunks, bool own_bnd) {
   size_t off = align_up(sizeof(WsHeader));
   L.chunks = off; off = align_up(off + sizeof(ChunkRec) * (size_t)n_chunks);
   L.seqs = off;   off = align_up(off + sizeof(SeqRec) * (size_t)s->num_seqs);
-  L.W = off;      off = align_up(off + sizeof(float) * (size_t)n_chunks * hv * C * D);
+  L.W = off;      off = align_up(off + sizeof(float) * (size_t)n_chunks * hv * prep_w_floats((int)C, (int)D));
   L.U = off;      off = align_up(off + sizeof(float) * (size_t)n_chunks * hv * C * D);
   L.gamma = off;  off = align_up(off + sizeof(float) * (size_t)n_chunks * hv);
   L.bnd = off;
@@ -90,7 +90,7 @@ DecLayout dec_layout(const gdn_cpr_shape* s) {
   const size_t D = s->d_k, C = s->chunk, hv = s->h_v, N = s->num_seqs;
   DecLayout L;
   size_t off = align_up(sizeof(WsHeader));
-  L.W = off;     off = align_up(off + sizeof(float) * N * hv * C * D);
+  L.W = off;     off = align_up(off + sizeof(float) * N * hv * prep_w_floats((int)C, (int)D));
   L.U = off;     off = align_up(off + sizeof(float) * N * hv * C * D);
   L.gamma = off; off = align_up(off + sizeof(float) * N * hv);
   L.total = off;

@@ -24,6 +24,7 @@
 #include "../../include/gdn_cpr.h"
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace gdn {
 
@@ -118,7 +119,7 @@ constexpr size_t prep_smem_bytes() {
                           3 * 16 * 16 + 4);
 }
 
-template <int D, typename Tin>
+template <int D, typename Tin, bool TC>
 __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, PrepWork w,
                                                        float* __restrict__ Wout,
                                                        float* __restrict__ Uout,
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
   constexpr int RG = kPrepThreads / D;  // row groups
   constexpr int RPT = kMaxChunk / RG;   // rows per thread at the largest chunk
   const int c = t % D, i0 = t / D;
-  float* Wo = Wout + ((item * dm.hv + h) * C) * (int64_t)D;
+  float* Wo = Wout + (item * dm.hv + h) * (int64_t)prep_w_floats(C, D);
   float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
   float aw[RPT], au[RPT];
 #pragma unroll
@@ -273,24 +274,67 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
       }
     }
   }
+  if constexpr (!TC) {
 #pragma unroll
-  for (int j = 0; j < RPT; ++j) {
-    const int i = i0 + RG * j;
-    if (i < C) {
-      Wo[i * D + c] = __fmul_rn(dec[i], aw[j]);
-      Uo[i * D + c] = __fmul_rn(dec[i], au[j]);
+    for (int j = 0; j < RPT; ++j) {
+      const int i = i0 + RG * j;
+      if (i < C) {
+        Wo[i * D + c] = __fmul_rn(dec[i], aw[j]);
+        Uo[i * D + c] = __fmul_rn(dec[i], au[j]);
+      }
+    }
+  } else {
+    // Tensor-core chain operands, as ready-made K-major shared-memory images:
+    //   [Wd hi (C x D) | Wd lo (C x D) | K^T (D x C)] in bf16; Ud stays fp32.
+    unsigned char* img = reinterpret_cast<unsigned char*>(Wo);
+    unsigned char* imgK = img + 2 * C * D * 2;
+    for (int q = t; q < D * (C / 8); q += kPrepThreads) {  // K^T: row c, 8 keys at a time
+      const int cc = q / (C / 8), s0 = (q % (C / 8)) * 8;
+      uint32_t w4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t lo16 = __bfloat16_as_ushort(__float2bfloat16_rn(Ks[(s0 + 2 * e) * DP + cc]));
+        const uint32_t hi16 = __bfloat16_as_ushort(__float2bfloat16_rn(Ks[(s0 + 2 * e + 1) * DP + cc]));
+        w4[e] = lo16 | (hi16 << 16);
+      }
+      *reinterpret_cast<uint4*>(imgK + tc::kmajor_off(cc, s0, C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      const int i = i0 + RG * j;
+      if (i < C) {
+        Ks[i * DP + c] = __fmul_rn(dec[i], aw[j]);
+        Uo[i * D + c] = __fmul_rn(dec[i], au[j]);
+      }
+    }
+    __syncthreads();
+    for (int q = t; q < C * (D / 8); q += kPrepThreads) {  // Wd split: row s, 8 columns at a time
+      const int s = q / (D / 8), b0 = (q % (D / 8)) * 8;
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        tc::split_bf16(Ks[s * DP + b0 + 2 * e], h0, l0);
+        tc::split_bf16(Ks[s * DP + b0 + 2 * e + 1], h1, l1);
+        hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      const uint32_t off = tc::kmajor_off(s, b0, D);
+      *reinterpret_cast<uint4*>(img + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(img + C * D * 2 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
   }
   if (t == 0) gamma_out[item * dm.hv + h] = expf(Gs[C - 1]);
 }
 
-template <int D, typename Tin>
+template <int D, typename Tin, bool TC = false>
 static void launch_prep_t(const Dims& d, const TokenArrays& in, const PrepWork& w, float* W,
                           float* U, float* gamma, WsHeader* hdr, cudaStream_t st) {
   constexpr size_t smem = prep_smem_bytes<D>();
-  ensure_smem(k_prep<D, Tin>, smem);
+  ensure_smem(k_prep<D, Tin, TC>, smem);
   dim3 grid((unsigned)w.n_items, d.hv);
-  k_prep<D, Tin><<<grid, kPrepThreads, smem, st>>>(d, in, w, W, U, gamma, hdr);
+  k_prep<D, Tin, TC><<<grid, kPrepThreads, smem, st>>>(d, in, w, W, U, gamma, hdr);
 }
 
 // =====================================================================  K1b  ===
@@ -421,7 +465,7 @@ __global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* ke
       const int64_t c = (int64_t)rec.chunk0 + j;
       rows_to_global<D>(Ss, w.bnd + (c * dm.hv + h) * SZ + (int64_t)r0 * D);
       const int64_t wo = (c * dm.hv + h) * (int64_t)C * D;
-      chain_step<D, Tin>(Ss, Ws, Ks, Us, Vd, W + wo, U + wo, gamma[c * dm.hv + h], keys,
+      chain_step<D, Tin>(Ss, Ws, Ks, Us, Vd, W + (c * dm.hv + h) * (int64_t)prep_w_floats(C, D), U + wo, gamma[c * dm.hv + h], keys,
                          (int64_t)rec.tok0 + (int64_t)j * C, dm.hqk, hq, C, r0);
     }
     if (rec.len % C != 0) {
@@ -452,7 +496,8 @@ __global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* ke
     }
     __syncthreads();
     const int64_t wo = ((int64_t)n * dm.hv + h) * (int64_t)C * D;
-    chain_step<D, Tin>(Ss, Ws, Ks, Us, Vd, W + wo, U + wo, gamma[(int64_t)n * dm.hv + h], keys,
+    chain_step<D, Tin>(Ss, Ws, Ks, Us, Vd, W + ((int64_t)n * dm.hv + h) * (int64_t)prep_w_floats(C, D),
+                       U + wo, gamma[(int64_t)n * dm.hv + h], keys,
                        (int64_t)sl * C, dm.hqk, hq, C, r0);
     rows_to_global<D>(Ss, w.s_bnd + so);
     rows_to_global<D>(Ss, w.s_run + so);
@@ -466,6 +511,257 @@ static void launch_chain_t(const Dims& d, const void* keys, const float* W, cons
   ensure_smem(k_chain<D, Tin>, smem);
   dim3 grid((unsigned)w.N, d.hv, D / kRowsPerChain);
   k_chain<D, Tin><<<grid, kChainThreads, smem, st>>>(d, keys, W, U, gamma, w, hdr);
+}
+
+// ============================================================  K1b (tcgen05)  ===
+// Boundary chain on tensor cores for d = 128, C = 64, bf16 inputs.  One CTA of 128 threads
+// per (sequence, head): thread i owns state row i, which is also TMEM lane i.  The state
+// S^(j) lives in TMEM (fp32) between steps; each step is
+//     D1 (128 x 64)  = S Wd^T                        3 MMAs: S_hi Wd_hi + S_hi Wd_lo + S_lo Wd_hi
+//     Vd^T[i][s]     = Ud[s][i] - D1[i][s]           (registers; then split to bf16 hi/lo)
+//     D2 (128 x 128) = gamma S + Vd^T K               D2 preloaded with gamma S, 2 MMAs: Vd_hi K + Vd_lo K
+// with fp32 operands split as x = hi + lo (bf16 each) and bf16 inputs exact.  The pre-pass
+// wrote Wd hi/lo and K^T as ready-made shared-memory images, so a step's operands arrive by
+// one bulk copy, issued a step ahead into the other of two stage buffers.
+namespace tcc {
+constexpr int D = 128, C = 64;
+constexpr uint32_t A1_BYTES = 128 * D * 2;  // state operand, per hi / lo
+constexpr uint32_t A2_BYTES = 128 * C * 2;  // Vd^T operand, per hi / lo
+constexpr uint32_t STAGE_BYTES = 3 * C * D * 2;  // Wd hi | Wd lo | K^T
+constexpr size_t SMEM = 2 * (size_t)A1_BYTES + 2 * (size_t)A2_BYTES + 2 * (size_t)STAGE_BYTES + 64;
+constexpr uint32_t TMEM_COLS = 256, D1_COL = 0, D2_COL = 64;
+constexpr uint32_t IDESC1 = tc::idesc_bf16(128, C);
+constexpr uint32_t IDESC2 = tc::idesc_bf16(128, D);
+}  // namespace tcc
+
+// split 16 fp32 values of row `row` (columns k0..k0+15) into the hi/lo K-major images
+__device__ __forceinline__ void store_split16(unsigned char* hi, unsigned char* lo, int row, int k0, int K,
+                                             const float* v) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat16 h0, l0, h1, l1;
+      tc::split_bf16(v[8 * g + 2 * e], h0, l0);
+      tc::split_bf16(v[8 * g + 2 * e + 1], h1, l1);
+      hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    const uint32_t off = tc::kmajor_off(row, k0 + 8 * g, K);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+__device__ __forceinline__ void store_row16(float* dst, const float* v) {
+#pragma unroll
+  for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+}
+
+__global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __restrict__ Wimg,
+                                                     const float* __restrict__ U,
+                                                     const float* __restrict__ gamma, ChainWork w,
+                                                     WsHeader* __restrict__ hdr) {
+  using namespace tcc;
+  extern __shared__ __align__(128) unsigned char smc[];
+  unsigned char* A1h = smc;
+  unsigned char* A1l = A1h + A1_BYTES;
+  unsigned char* A2h = A1l + A1_BYTES;
+  unsigned char* A2l = A2h + A2_BYTES;
+  unsigned char* stage0 = A2l + A2_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage0 + 2 * STAGE_BYTES);  // load0, load1, mma
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  const int t = threadIdx.x, warp = t >> 5, row = t;
+  const int n = blockIdx.x, h = blockIdx.y;
+  const int64_t SZ = (int64_t)D * D;
+  const int64_t WS = (int64_t)prep_w_floats(C, D);
+
+  // ---- the work of this CTA (uniform)
+  int nfull, nchunks = 0, len = 0, sl = -1;
+  int64_t item0;
+  const float* src;  // S^(0) rows, or NULL for zero
+  if (w.seqs) {
+    if (!hdr->valid) return;
+    const SeqRec rec = w.seqs[n];
+    nfull = rec.len / C;
+    nchunks = rec.nchunks;
+    len = rec.len;
+    item0 = rec.chunk0;
+    src = w.state_in ? w.state_in + ((int64_t)n * dm.hv + h) * SZ : nullptr;
+    if (w.cache_bnd) {
+      sl = w.slot_of_seq ? w.slot_of_seq[n] : n;
+      if (sl < 0 || sl >= w.cache_slots) {
+        if (t == 0) set_error(hdr, GDN_DEVERR_SLOT);
+        sl = -1;
+      }
+    }
+  } else {
+    sl = w.slot[n];
+    if (sl < 0 || sl >= w.slots) return;  // reported by the decode step kernel
+    const int p = w.pos[sl];
+    if (p < 0 || (p + 1) % C != 0) return;
+    nfull = 1;
+    item0 = n;
+    src = w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ;
+  }
+  // outputs for the state after full chunk j (j = 1 .. nfull): rows of S^(j)
+  auto write_state = [&](int j, const float* v, int c0) {
+    if (w.seqs) {
+      if (j < nchunks) store_row16(w.bnd + ((item0 + j) * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+      if (j == nfull) {
+        if (len % C == 0 && w.state_out)
+          store_row16(w.state_out + ((int64_t)n * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+        if (sl >= 0) {
+          store_row16(w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+          if (len % C == 0)
+            store_row16(w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+        }
+      }
+    } else {
+      store_row16(w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+      store_row16(w.s_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+    }
+  };
+
+  if (nfull == 0) {  // no full chunk: S^(0) passes straight to the outputs
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
+      if (nchunks > 0) store_row16(w.bnd + (item0 * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+      write_state(0, v, c0);
+    }
+    return;
+  }
+
+  using namespace tc;
+  if (t == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);
+  if (t == 0) {
+    mbar_expect_tx(&bars[0], STAGE_BYTES);
+    bulk_g2s(stage0, Wimg + (item0 * dm.hv + h) * WS, STAGE_BYTES, &bars[0]);
+  }
+  {  // S^(0): A operand (split) and gamma_0 S^(0) into D2
+    const float g0 = gamma[item0 * dm.hv + h];
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
+      if (w.seqs) store_row16(w.bnd + (item0 * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+      store_split16(A1h, A1l, row, c0, D, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(g0, v[e]);
+      tmem_st16(tlane + D2_COL + c0, v);
+    }
+    tmem_st_wait();
+  }
+  fence_proxy_async();
+  fence_before_sync();
+  __syncthreads();
+
+  uint32_t mma_phase = 0;
+  int j = 0;
+  bool failed = false;
+  for (; j < nfull; ++j) {
+    const int64_t item = item0 + j;
+    const int buf = j & 1;
+    unsigned char* stg = stage0 + buf * STAGE_BYTES;
+    if (t == 0 && j + 1 < nfull) {
+      mbar_expect_tx(&bars[buf ^ 1], STAGE_BYTES);
+      bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, Wimg + ((item + 1) * dm.hv + h) * WS, STAGE_BYTES,
+               &bars[buf ^ 1]);
+    }
+    float ud[C];
+    {
+      const float* Ug = U + (item * dm.hv + h) * (int64_t)C * D + row;
+#pragma unroll
+      for (int s = 0; s < C; ++s) ud[s] = Ug[(int64_t)s * D];
+    }
+    if (!__syncthreads_and(mbar_wait(&bars[buf], (uint32_t)(j >> 1) & 1u))) { failed = true; break; }
+    if (t == 0) {  // D1 = S Wd^T (three split terms)
+      fence_after_sync();
+      const uint32_t a_hi = smem_u32(A1h), a_lo = smem_u32(A1l);
+      const uint32_t w_hi = smem_u32(stg), w_lo = w_hi + C * D * 2;
+      const uint32_t sboA = (D / 8) * 128, sboW = (D / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t a = term == 2 ? a_lo : a_hi;
+        const uint32_t b = term == 1 ? w_lo : w_hi;
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16(tbase + D1_COL, make_desc(a + kk * 256, 128, sboA), make_desc(b + kk * 256, 128, sboW),
+                   IDESC1, (term > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&bars[2]);
+    }
+    if (!__syncthreads_and(mbar_wait(&bars[2], mma_phase))) { failed = true; break; }
+    mma_phase ^= 1u;
+    fence_after_sync();
+    for (int s0 = 0; s0 < C; s0 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
+      float v[16];
+      tmem_ld16(tlane + D1_COL + s0, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s0 + e], v[e]);
+      store_split16(A2h, A2l, row, s0, C, v);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    if (t == 0) {  // D2 += Vd^T K (two split terms)
+      fence_after_sync();
+      const uint32_t k_img = smem_u32(stg) + 2 * C * D * 2;
+      const uint32_t sboA = (C / 8) * 128, sboK = (C / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t a = smem_u32(term == 0 ? A2h : A2l);
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16(tbase + D2_COL, make_desc(a + kk * 256, 128, sboA), make_desc(k_img + kk * 256, 128, sboK),
+                   IDESC2, 1u);
+      }
+      mma_commit(&bars[2]);
+    }
+    if (!__syncthreads_and(mbar_wait(&bars[2], mma_phase))) { failed = true; break; }
+    mma_phase ^= 1u;
+    fence_after_sync();
+    {  // S^(j+1): outputs, next step's A operand and gamma_{j+1} S^(j+1)
+      const bool more = j + 1 < nfull;
+      const float gn = more ? gamma[(item + 1) * dm.hv + h] : 0.f;
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + D2_COL + c0, v);
+        write_state(j + 1, v, c0);
+        if (more) {
+          store_split16(A1h, A1l, row, c0, D, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gn, v[e]);
+          tmem_st16(tlane + D2_COL + c0, v);
+        }
+      }
+      tmem_st_wait();
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+  }
+  if (failed) {
+    if (t == 0) set_error(hdr, GDN_DEVERR_TIMEOUT);
+    // let the operations this CTA may still have in flight finish before releasing TMEM
+    if (j + 1 < nfull) mbar_wait(&bars[(j & 1) ^ 1], (uint32_t)((j + 1) >> 1) & 1u);
+    mbar_wait(&bars[2], mma_phase);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
 
 // =====================================================================  K2  ====
@@ -696,7 +992,9 @@ void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, 
 void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float* W, float* U,
                  float* gamma, WsHeader* hdr, cudaStream_t st) {
   if (w.n_items <= 0) return;
-  if (d.in_bf16) {
+  if (boundary_on_tensor_cores(d)) {
+    launch_prep_t<128, __nv_bfloat16, true>(d, in, w, W, U, gamma, hdr, st);
+  } else if (d.in_bf16) {
     GDN_DISPATCH_D(d.D, launch_prep_t<DD, __nv_bfloat16>(d, in, w, W, U, gamma, hdr, st))
   } else {
     GDN_DISPATCH_D(d.D, launch_prep_t<DD, float>(d, in, w, W, U, gamma, hdr, st))
@@ -706,7 +1004,10 @@ void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float*
 void launch_chain(const Dims& d, const void* keys, const float* W, const float* U,
                   const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st) {
   if (w.N <= 0) return;
-  if (d.in_bf16) {
+  if (boundary_on_tensor_cores(d)) {
+    ensure_smem(k_chain_tc, tcc::SMEM);
+    k_chain_tc<<<dim3((unsigned)w.N, d.hv), 128, tcc::SMEM, st>>>(d, W, U, gamma, w, hdr);
+  } else if (d.in_bf16) {
     GDN_DISPATCH_D(d.D, launch_chain_t<DD, __nv_bfloat16>(d, keys, W, U, gamma, w, hdr, st))
   } else {
     GDN_DISPATCH_D(d.D, launch_chain_t<DD, float>(d, keys, W, U, gamma, w, hdr, st))

@@ -23,6 +23,16 @@ struct Dims {
   bool in_bf16, out_bf16;
 };
 
+// Floats reserved per (chunk, head) for the pre-pass's W output: fp32 Wd (C x D) on the
+// SIMT path, or three bf16 C x D shared-memory images (Wd hi, Wd lo, K^T) on the
+// tensor-core path.
+__host__ __device__ inline size_t prep_w_floats(int C, int D) { return (size_t)3 * C * D / 2; }
+
+// The boundary pass runs on tcgen05 tensor cores for bf16 inputs with d = 128, C = 64, and
+// on fp32 SIMT otherwise (fp32 inputs keep an fp32 boundary pass).  Prefill and decode
+// resynchronisation always take the same path for a given shape.
+__host__ __device__ inline bool boundary_on_tensor_cores(const Dims& d) { return d.in_bf16 && d.D == 128 && d.C == 64; }
+
 // K0: chunk and sequence records from the device cu_seqlens, checked against the host's
 // chunk count and a hash of the host copy.
 void launch_worklist(const int32_t* cu, int N, int T, int C, int64_t n_chunks, uint32_t cu_hash,

@@ -168,3 +168,29 @@ def test_device_errors_are_reported_not_faulted(gdn):
                        cu_seqlens_host=x["cu_seqlens"], ws=ws)
     assert gdn.device_error(ws) == 0
     assert torch.isfinite(o.float()).all()
+
+
+@pytest.mark.parametrize("L0,M", [(64, 64), (100, 90), (0, 130)])
+def test_decode_equals_prefill_tensor_core_boundary(gdn, L0, M):
+    """d = 128, C = 64, bf16: the shape whose boundary pass runs on tcgen05 tensor cores in
+    both prefill and decode resynchronisation; decode must still equal prefill bit for bit."""
+    C, d = 64, 128
+    lengths = [L0 + M, L0 + M + 5, 3]
+    x = synth.make_inputs(lengths, 2, 4, d, dtype=synth.BF16, seed=L0 + 7 * M, state_in=True,
+                          decay="slow")
+    o_full, s_full = prefill(gdn, x, C)
+    seqs = split(x)
+    head = pack([{n: (s[n][:min(L0, s["q"].shape[0])] if n != "state_in" else s[n]) for n in s}
+                 for s in seqs[:2]])
+    slots = torch.tensor([1, 0], dtype=torch.int32, device="cuda")
+    cache = gdn.Cache(2, 2, 4, d, C, dtype=torch.bfloat16)
+    prefill(gdn, head, C, cache=cache, slot_of_seq=slots)
+    cu = x["cu_seqlens"].tolist()
+    for i in range(M):
+        tok = [cu[s] + L0 + i for s in range(2)]
+        st = {n: x[n][tok].contiguous().cuda() for n in ("q", "k", "v", "g", "beta")}
+        od = gdn.decode_step(st["q"], st["k"], st["v"], st["g"], st["beta"], slots, cache,
+                             out_dtype=torch.float32)
+        for s in range(2):
+            assert torch.equal(od[s], o_full[tok[s]]), (i, s)
+    assert torch.equal(cache.s_run[1], s_full[0])
