@@ -133,6 +133,51 @@ __device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __r
   return __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
 }
 
+// T = (I + A)^{-1} for a strictly lower C x C matrix A in shared memory (row stride CP),
+// blocked by 16.  Diagonal blocks by forward substitution, one column per thread:
+//     T[r][r] = 1,  T[i][r] = -sum_{m=r}^{i-1} A[i][m] T[m][r];
+// then off-diagonal blocks (I > J) by increasing I - J:
+//     X[i][r] = sum_{m=r}^{16I-1} A[i][m] T[m][r],   T[i][r] = -sum_{m=16I}^{i} T[i][m] X[m][r]
+// (every sum in ascending m with one accumulator).  Only the lower triangle of T is
+// written.  Xs: 3 * 16 * 16 floats of scratch.  All NT threads of the block must call it.
+template <int NT>
+__device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float* Tm, float* Xs, int C,
+                                                           int CP) {
+  constexpr int TB = 16;
+  const int t = threadIdx.x;
+  const int nb = C / TB;
+  if (t < C) {
+    const int r = t, rend = (r / TB) * TB + TB;
+    Tm[r * CP + r] = 1.f;
+    for (int i = r + 1; i < rend; ++i) {
+      float acc = 0.f;
+      for (int m = r; m < i; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
+      Tm[i * CP + r] = -acc;
+    }
+  }
+  __syncthreads();
+  for (int off = 1; off < nb; ++off) {
+    const int nel = (nb - off) * TB * TB;
+    for (int e = t; e < nel; e += NT) {
+      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
+      const int i = I * TB + ii, r = (I - off) * TB + rr;
+      float acc = 0.f;
+      for (int m = r; m < I * TB; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
+      Xs[e] = acc;
+    }
+    __syncthreads();
+    for (int e = t; e < nel; e += NT) {
+      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
+      const int i = I * TB + ii, r = (I - off) * TB + rr;
+      const float* X = Xs + (e / (TB * TB)) * TB * TB;
+      float acc = 0.f;
+      for (int m = I * TB; m <= i; ++m) acc = __fmaf_rn(Tm[i * CP + m], X[(m - I * TB) * TB + rr], acc);
+      Tm[i * CP + r] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
 // State row i, half h: global float offset of register group m.
 template <int D>
 __device__ __forceinline__ int state_col(int m, int half) {

@@ -206,43 +206,8 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
     }
   }
   __syncthreads();
-  // 4. T = (I + A)^{-1}, blocked by 16.  Diagonal blocks by forward substitution, one
-  //    column per thread:  T[r][r] = 1,  T[i][r] = -sum_{m=r}^{i-1} A[i][m] T[m][r].
-  //    Off-diagonal blocks (I > J) by increasing I - J:
-  //      X[i][r] = sum_{m=r}^{16I-1} A[i][m] T[m][r],   T[i][r] = -sum_{m=16I}^{i} T[i][m] X[m][r]
-  //    (every sum in ascending m, one accumulator).
-  constexpr int TB = 16;
-  const int nb = C / TB;
-  if (t < C) {
-    const int r = t, rend = (r / TB) * TB + TB;
-    Tm[r * CP + r] = 1.f;
-    for (int i = r + 1; i < rend; ++i) {
-      float acc = 0.f;
-      for (int m = r; m < i; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
-      Tm[i * CP + r] = -acc;
-    }
-  }
-  __syncthreads();
-  for (int off = 1; off < nb; ++off) {
-    const int nel = (nb - off) * TB * TB;
-    for (int e = t; e < nel; e += kPrepThreads) {
-      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
-      const int i = I * TB + ii, r = (I - off) * TB + rr;
-      float acc = 0.f;
-      for (int m = r; m < I * TB; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
-      Xs[e] = acc;
-    }
-    __syncthreads();
-    for (int e = t; e < nel; e += kPrepThreads) {
-      const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
-      const int i = I * TB + ii, r = (I - off) * TB + rr;
-      const float* X = Xs + (e / (TB * TB)) * TB * TB;
-      float acc = 0.f;
-      for (int m = I * TB; m <= i; ++m) acc = __fmaf_rn(Tm[i * CP + m], X[(m - I * TB) * TB + rr], acc);
-      Tm[i * CP + r] = -acc;
-    }
-    __syncthreads();
-  }
+  // 4. T = (I + A)^{-1} (blocked forward substitution, fixed order)
+  blocked_unit_lower_inverse<kPrepThreads>(A, Tm, Xs, C, CP);
   // 5. TK = T diag(beta e^G) (into A), TV = T diag(beta) (in place)
   for (int o = t; o < C * C; o += kPrepThreads) {
     const int i = o / C, r = o % C;
@@ -764,6 +729,261 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
   if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
 
+// ============================================================  K1a (tcgen05)  ===
+// Boundary pre-pass on tensor cores for d = 128, C = 64, bf16 inputs, one CTA of 256
+// threads per (chunk, head) as k_prep:
+//   Gram = K K^T                        1 MMA chain (bf16 inputs exact, fp32 accumulation)
+//   A, T = (I + A)^{-1}                 fp32 SIMT (blocked forward substitution)
+//   W    = (T diag(beta e^G)) K         A = TK split hi/lo, B = K^T image
+//   U^T  = V^T (T diag(beta))^T         A = V^T image, B = TV split hi/lo
+// Outputs as k_prep's tensor-core variant: the chain's images [Wd hi | Wd lo | K^T]
+// (Wd = diag(dec) W) and Ud = diag(dec) U in fp32, plus gamma.  Gram and W use 128-row MMAs
+// of which rows 0..63 are the chunk (the other rows read neighbouring shared memory and
+// are never read back).
+namespace tcp {
+constexpr int D = 128, C = 64, CP = C + 1;
+constexpr uint32_t TILE = C * D * 2;                   // 16 KB: a C x D or D x C bf16 image
+constexpr uint32_t MAT = C * CP * 4;                   // fp32 C x C with padded rows
+constexpr size_t SMEM = 3 * (size_t)TILE + 2 * (size_t)MAT + 5 * C * 4 + 64;
+constexpr uint32_t TMEM_COLS = 256, W_COL = 0, UT_COL = 128, GRAM_COL = 0;
+}  // namespace tcp
+
+__global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, PrepWork w,
+                                                    float* __restrict__ Wout, float* __restrict__ Uout,
+                                                    float* __restrict__ gamma_out, WsHeader* __restrict__ hdr) {
+  using namespace tcp;
+  extern __shared__ __align__(128) unsigned char smp[];
+  unsigned char* R0 = smp;             // K image (C x D), then Xs, then TK hi | TK lo (C x C each)
+  unsigned char* KT = R0 + TILE;       // K^T image (D x C)
+  unsigned char* VT = KT + TILE;       // V^T image (D x C)
+  float* A = reinterpret_cast<float*>(VT + TILE);  // then TV hi | TV lo images
+  float* Tm = A + C * CP;
+  float* gs = Tm + C * CP;
+  float* Gs = gs + C;
+  float* bs = Gs + C;
+  float* bk = bs + C;
+  float* dec = bk + C;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dec + C);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  float* Xs = reinterpret_cast<float*>(R0);
+  unsigned char* TKh = R0;
+  unsigned char* TKl = R0 + C * C * 2;
+  unsigned char* TVh = reinterpret_cast<unsigned char*>(A);
+  unsigned char* TVl = TVh + C * C * 2;
+
+  const int t = threadIdx.x, warp = t >> 5;
+  const int h = blockIdx.y;
+  const int hq = h / (dm.hv / dm.hqk);
+  const int64_t item = blockIdx.x;
+  int64_t tok0;
+  if (w.chunks) {
+    if (!hdr->valid) return;
+    const ChunkRec rec = w.chunks[item];
+    if (rec.len != C) return;
+    tok0 = rec.tok0;
+  } else {
+    const int sl = w.slot[item];
+    if (sl < 0 || sl >= w.slots) {
+      if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_SLOT);
+      return;
+    }
+    const int p = w.pos[sl];
+    if (p < 0) {
+      if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_POS);
+      return;
+    }
+    if ((p + 1) % C != 0) return;
+    tok0 = (int64_t)sl * C;
+  }
+  const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(in.k);
+  const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(in.v);
+  const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
+  const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
+  const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
+
+  // 1. operand images straight from global memory
+  for (int q = t; q < C * (D / 8); q += 256) {  // K rows: 16-byte pieces
+    const int r = q / (D / 8), c0 = (q % (D / 8)) * 8;
+    *reinterpret_cast<uint4*>(R0 + tc::kmajor_off(r, c0, D)) = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
+  }
+  for (int q = t; q < D * (C / 8); q += 256) {  // K^T and V^T: column e, 8 tokens at a time
+    const int e = q % D, r0 = (q / D) * 8;
+    uint32_t kw[4], vw[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      kw[x] = (uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x) * kstride + e]) |
+              ((uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x + 1) * kstride + e]) << 16);
+      vw[x] = (uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x) * vstride + e]) |
+              ((uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x + 1) * vstride + e]) << 16);
+    }
+    *reinterpret_cast<uint4*>(KT + tc::kmajor_off(e, r0, C)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+    *reinterpret_cast<uint4*>(VT + tc::kmajor_off(e, r0, C)) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+  }
+  if (t < C) {
+    gs[t] = in.g[(tok0 + t) * dm.hv + h];
+    bs[t] = in.beta[(tok0 + t) * dm.hv + h];
+  }
+  if (t == 0) {
+    tc::mbar_init(bar, 1);
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) tc::tmem_alloc(tslot, TMEM_COLS);
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = *tslot;
+  uint32_t phase = 0;
+  bool ok = true;
+  // 2. Gram on the tensor cores while one thread forms G
+  if (t == 0) {
+    const uint32_t a = tc::smem_u32(R0);
+    for (int kk = 0; kk < D / 16; ++kk)
+      tc::mma_bf16(tbase + GRAM_COL, tc::make_desc(a + kk * 256, 128, (D / 8) * 128),
+                   tc::make_desc(a + kk * 256, 128, (D / 8) * 128), tc::idesc_bf16(128, C), kk > 0 ? 1u : 0u);
+    tc::mma_commit(bar);
+    float run = gs[0];
+    Gs[0] = run;
+    for (int i = 1; i < C; ++i) {
+      run = __fadd_rn(run, gs[i]);
+      Gs[i] = run;
+    }
+  }
+  __syncthreads();
+  if (t < C) {
+    bk[t] = __fmul_rn(bs[t], expf(Gs[t]));
+    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
+  }
+  {
+    const bool done = tc::mbar_wait(bar, phase);
+    if (done) phase ^= 1u;
+    ok = __syncthreads_and(done) != 0;
+  }
+  tc::fence_after_sync();
+  if (ok && (warp & 3) < 2) {  // rows 0..63: A_is = beta_i e^{G_i - G_s} Gram_is (i > s)
+    const int i = (warp & 3) * 32 + (t & 31);
+    const int cbase = (warp >> 2) * 32;
+    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+      float v[16];
+      tc::tmem_ld16(tc::tmem_lane_addr(tbase, warp, GRAM_COL + s0), v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int s = s0 + e;
+        A[i * CP + s] = (i > s) ? __fmul_rn(__fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s]))), v[e]) : 0.f;
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  // 3. T = (I + A)^{-1}
+  blocked_unit_lower_inverse<256>(A, Tm, Xs, C, CP);
+  // 4. TK = T diag(beta e^G), TV = T diag(beta), split into bf16 images (lower triangle)
+  for (int q = t; q < C * (C / 8); q += 256) {
+    const int i = q / (C / 8), r0 = (q % (C / 8)) * 8;
+    float tk[8], tv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int r = r0 + e;
+      const float x = (r <= i) ? Tm[i * CP + r] : 0.f;
+      tk[e] = __fmul_rn(x, bk[r]);
+      tv[e] = __fmul_rn(x, bs[r]);
+    }
+    uint32_t a[4], b[4], c2[4], d2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat16 h0, l0, h1, l1;
+      tc::split_bf16(tk[2 * e], h0, l0);
+      tc::split_bf16(tk[2 * e + 1], h1, l1);
+      a[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      b[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      tc::split_bf16(tv[2 * e], h0, l0);
+      tc::split_bf16(tv[2 * e + 1], h1, l1);
+      c2[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      d2[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    const uint32_t off = tc::kmajor_off(i, r0, C);
+    *reinterpret_cast<uint4*>(TKh + off) = make_uint4(a[0], a[1], a[2], a[3]);
+    *reinterpret_cast<uint4*>(TKl + off) = make_uint4(b[0], b[1], b[2], b[3]);
+    *reinterpret_cast<uint4*>(TVh + off) = make_uint4(c2[0], c2[1], c2[2], c2[3]);
+    *reinterpret_cast<uint4*>(TVl + off) = make_uint4(d2[0], d2[1], d2[2], d2[3]);
+  }
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  // 5. W = TK K (rows 0..63 of a 128-row MMA) and U^T = V^T TV^T
+  if (t == 0 && ok) {
+    tc::fence_after_sync();
+    const uint32_t sbo = (C / 8) * 128;
+    const uint32_t kt = tc::smem_u32(KT), vt = tc::smem_u32(VT);
+    for (int term = 0; term < 2; ++term) {
+      const uint32_t a = tc::smem_u32(term == 0 ? TKh : TKl);
+      const uint32_t b = tc::smem_u32(term == 0 ? TVh : TVl);
+      for (int kk = 0; kk < C / 16; ++kk) {
+        tc::mma_bf16(tbase + W_COL, tc::make_desc(a + kk * 256, 128, sbo), tc::make_desc(kt + kk * 256, 128, sbo),
+                     tc::idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_bf16(tbase + UT_COL, tc::make_desc(vt + kk * 256, 128, sbo), tc::make_desc(b + kk * 256, 128, sbo),
+                     tc::idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+      }
+    }
+    tc::mma_commit(bar);
+  }
+  if (ok) {
+    const bool done = tc::mbar_wait(bar, phase);
+    if (done) phase ^= 1u;
+    ok = __syncthreads_and(done) != 0;
+  }
+  tc::fence_after_sync();
+  float* Wo = Wout + (item * dm.hv + h) * (int64_t)prep_w_floats(C, D);
+  float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
+  unsigned char* img = reinterpret_cast<unsigned char*>(Wo);
+  if (ok) {
+    if ((warp & 3) < 2) {  // Wd rows 0..63 -> split image
+      const int i = (warp & 3) * 32 + (t & 31);
+      const int cbase = (warp >> 2) * 64;
+      for (int c0 = cbase; c0 < cbase + 64; c0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tc::tmem_lane_addr(tbase, warp, W_COL + c0), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(dec[i], v[e]);
+#pragma unroll
+        for (int g2 = 0; g2 < 2; ++g2) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat16 h0, l0, h1, l1;
+            tc::split_bf16(v[8 * g2 + 2 * e], h0, l0);
+            tc::split_bf16(v[8 * g2 + 2 * e + 1], h1, l1);
+            hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+            lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+          }
+          const uint32_t off = tc::kmajor_off(i, c0 + 8 * g2, D);
+          *reinterpret_cast<uint4*>(img + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(img + TILE + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
+    }
+    {  // Ud[i][e] = dec_i U^T[e][i]: lane e, columns i
+      const int e = (warp & 3) * 32 + (t & 31);
+      const int ibase = (warp >> 2) * 32;
+      for (int i0 = ibase; i0 < ibase + 32; i0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tc::tmem_lane_addr(tbase, warp, UT_COL + i0), v);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) Uo[(int64_t)(i0 + x) * D + e] = __fmul_rn(dec[i0 + x], v[x]);
+      }
+    }
+    for (int q = t; q < (int)(TILE / 16); q += 256)
+      reinterpret_cast<uint4*>(img + 2 * TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
+    if (t == 0) gamma_out[item * dm.hv + h] = expf(Gs[C - 1]);
+  } else if (t == 0) {
+    set_error(hdr, GDN_DEVERR_TIMEOUT);
+    tc::mbar_wait(bar, phase);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
 // =====================================================================  K2  ====
 template <int D>
 constexpr size_t intra_smem_bytes() {
@@ -993,7 +1213,8 @@ void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float*
                  float* gamma, WsHeader* hdr, cudaStream_t st) {
   if (w.n_items <= 0) return;
   if (boundary_on_tensor_cores(d)) {
-    launch_prep_t<128, __nv_bfloat16, true>(d, in, w, W, U, gamma, hdr, st);
+    ensure_smem(k_prep_tc, tcp::SMEM);
+    k_prep_tc<<<dim3((unsigned)w.n_items, d.hv), 256, tcp::SMEM, st>>>(d, in, w, W, U, gamma, hdr);
   } else if (d.in_bf16) {
     GDN_DISPATCH_D(d.D, launch_prep_t<DD, __nv_bfloat16>(d, in, w, W, U, gamma, hdr, st))
   } else {
