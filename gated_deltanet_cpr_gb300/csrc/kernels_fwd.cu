@@ -42,6 +42,22 @@ static void ensure_smem(F* fn, size_t bytes) {
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// Streaming multiprocessors of the current device (looked up once per device).
+static int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 // =====================================================================  K0  ====
 __global__ void __launch_bounds__(1024) k_worklist(const int32_t* __restrict__ cu, int N, int T,
                                                    int C, int64_t n_chunks, uint32_t cu_hash,
@@ -529,6 +545,7 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
                                                      const float* __restrict__ gamma, ChainWork w,
                                                      WsHeader* __restrict__ hdr) {
   using namespace tcc;
+  using namespace tc;
   extern __shared__ __align__(128) unsigned char smc[];
   unsigned char* A1h = smc;
   unsigned char* A1l = A1h + A1_BYTES;
@@ -538,69 +555,32 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage0 + 2 * STAGE_BYTES);  // load0, load1, mma
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
   const int t = threadIdx.x, warp = t >> 5, row = t;
-  const int n = blockIdx.x, h = blockIdx.y;
   const int64_t SZ = (int64_t)D * D;
   const int64_t WS = (int64_t)prep_w_floats(C, D);
-
-  // ---- the work of this CTA (uniform)
-  int nfull, nchunks = 0, len = 0, sl = -1;
-  int64_t item0;
-  const float* src;  // S^(0) rows, or NULL for zero
-  if (w.seqs) {
-    if (!hdr->valid) return;
-    const SeqRec rec = w.seqs[n];
-    nfull = rec.len / C;
-    nchunks = rec.nchunks;
-    len = rec.len;
-    item0 = rec.chunk0;
-    src = w.state_in ? w.state_in + ((int64_t)n * dm.hv + h) * SZ : nullptr;
-    if (w.cache_bnd) {
-      sl = w.slot_of_seq ? w.slot_of_seq[n] : n;
-      if (sl < 0 || sl >= w.cache_slots) {
-        if (t == 0) set_error(hdr, GDN_DEVERR_SLOT);
-        sl = -1;
+  if (w.seqs && !hdr->valid) return;
+  const int64_t total = (int64_t)w.N * dm.hv;
+  // This CTA's items (wi = blockIdx.x + j * gridDim.x) that have work, tested one per
+  // thread; a CTA with none exits before touching tensor memory.
+  __shared__ int64_t s_list[128];
+  __shared__ int s_cnt;
+  if (t == 0) s_cnt = 0;
+  __syncthreads();
+  {
+    const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
+    if (wi < total) {
+      bool work = true;
+      if (!w.seqs) {
+        const int sl = w.slot[wi / dm.hv];
+        work = sl >= 0 && sl < w.slots && w.pos[sl] >= 0 && (w.pos[sl] + 1) % C == 0;
       }
+      if (work) s_list[atomicAdd(&s_cnt, 1)] = wi;
     }
-  } else {
-    sl = w.slot[n];
-    if (sl < 0 || sl >= w.slots) return;  // reported by the decode step kernel
-    const int p = w.pos[sl];
-    if (p < 0 || (p + 1) % C != 0) return;
-    nfull = 1;
-    item0 = n;
-    src = w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ;
   }
-  // outputs for the state after full chunk j (j = 1 .. nfull): rows of S^(j)
-  auto write_state = [&](int j, const float* v, int c0) {
-    if (w.seqs) {
-      if (j < nchunks) store_row16(w.bnd + ((item0 + j) * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-      if (j == nfull) {
-        if (len % C == 0 && w.state_out)
-          store_row16(w.state_out + ((int64_t)n * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-        if (sl >= 0) {
-          store_row16(w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-          if (len % C == 0)
-            store_row16(w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-        }
-      }
-    } else {
-      store_row16(w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-      store_row16(w.s_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-    }
-  };
+  __syncthreads();
+  const int count = s_cnt;
+  if (count == 0) return;
 
-  if (nfull == 0) {  // no full chunk: S^(0) passes straight to the outputs
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      float v[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
-      if (nchunks > 0) store_row16(w.bnd + (item0 * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-      write_state(0, v, c0);
-    }
-    return;
-  }
-
-  using namespace tc;
+  // tensor memory and barriers, once per CTA
   if (t == 0) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
@@ -613,116 +593,191 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
   fence_after_sync();
   const uint32_t tbase = *tslot;
   const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);
-  if (t == 0) {
-    mbar_expect_tx(&bars[0], STAGE_BYTES);
-    bulk_g2s(stage0, Wimg + (item0 * dm.hv + h) * WS, STAGE_BYTES, &bars[0]);
-  }
-  {  // S^(0): A operand (split) and gamma_0 S^(0) into D2
-    const float g0 = gamma[item0 * dm.hv + h];
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      float v[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
-      if (w.seqs) store_row16(w.bnd + (item0 * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
-      store_split16(A1h, A1l, row, c0, D, v);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(g0, v[e]);
-      tmem_st16(tlane + D2_COL + c0, v);
-    }
-    tmem_st_wait();
-  }
-  fence_proxy_async();
-  fence_before_sync();
-  __syncthreads();
-
+  uint32_t uses[2] = {0u, 0u};  // completed waits per stage barrier
   uint32_t mma_phase = 0;
-  int j = 0;
-  bool failed = false;
-  for (; j < nfull; ++j) {
-    const int64_t item = item0 + j;
-    const int buf = j & 1;
-    unsigned char* stg = stage0 + buf * STAGE_BYTES;
-    if (t == 0 && j + 1 < nfull) {
-      mbar_expect_tx(&bars[buf ^ 1], STAGE_BYTES);
-      bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, Wimg + ((item + 1) * dm.hv + h) * WS, STAGE_BYTES,
-               &bars[buf ^ 1]);
-    }
-    float ud[C];
-    {
-      const float* Ug = U + (item * dm.hv + h) * (int64_t)C * D + row;
-#pragma unroll
-      for (int s = 0; s < C; ++s) ud[s] = Ug[(int64_t)s * D];
-    }
-    if (!__syncthreads_and(mbar_wait(&bars[buf], (uint32_t)(j >> 1) & 1u))) { failed = true; break; }
-    if (t == 0) {  // D1 = S Wd^T (three split terms)
-      fence_after_sync();
-      const uint32_t a_hi = smem_u32(A1h), a_lo = smem_u32(A1l);
-      const uint32_t w_hi = smem_u32(stg), w_lo = w_hi + C * D * 2;
-      const uint32_t sboA = (D / 8) * 128, sboW = (D / 8) * 128;
-#pragma unroll 1
-      for (int term = 0; term < 3; ++term) {
-        const uint32_t a = term == 2 ? a_lo : a_hi;
-        const uint32_t b = term == 1 ? w_lo : w_hi;
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16(tbase + D1_COL, make_desc(a + kk * 256, 128, sboA), make_desc(b + kk * 256, 128, sboW),
-                   IDESC1, (term > 0 || kk > 0) ? 1u : 0u);
+  uint32_t gstep = 0;           // steps run by this CTA (selects the stage buffer)
+  int pending = -1;             // stage buffer with a copy in flight
+  bool mma_pending = false;
+  bool ok = true;
+
+  for (int li = 0; li < count && ok; ++li) {
+    const int64_t wi = s_list[li];
+    const int n = (int)(wi / dm.hv), h = (int)(wi % dm.hv);
+    // ---- the work of this item (uniform)
+    int nfull, nchunks = 0, len = 0, sl = -1;
+    int64_t item0;
+    const float* src;  // S^(0) rows, or NULL for zero
+    if (w.seqs) {
+      const SeqRec rec = w.seqs[n];
+      nfull = rec.len / C;
+      nchunks = rec.nchunks;
+      len = rec.len;
+      item0 = rec.chunk0;
+      src = w.state_in ? w.state_in + ((int64_t)n * dm.hv + h) * SZ : nullptr;
+      if (w.cache_bnd) {
+        sl = w.slot_of_seq ? w.slot_of_seq[n] : n;
+        if (sl < 0 || sl >= w.cache_slots) {
+          if (t == 0) set_error(hdr, GDN_DEVERR_SLOT);
+          sl = -1;
+        }
       }
-      mma_commit(&bars[2]);
+    } else {
+      sl = w.slot[n];
+      if (sl < 0 || sl >= w.slots) continue;  // reported by the decode step kernel
+      const int p = w.pos[sl];
+      if (p < 0 || (p + 1) % C != 0) continue;
+      nfull = 1;
+      item0 = n;
+      src = w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ;
     }
-    if (!__syncthreads_and(mbar_wait(&bars[2], mma_phase))) { failed = true; break; }
-    mma_phase ^= 1u;
-    fence_after_sync();
-    for (int s0 = 0; s0 < C; s0 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
-      float v[16];
-      tmem_ld16(tlane + D1_COL + s0, v);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s0 + e], v[e]);
-      store_split16(A2h, A2l, row, s0, C, v);
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    if (t == 0) {  // D2 += Vd^T K (two split terms)
-      fence_after_sync();
-      const uint32_t k_img = smem_u32(stg) + 2 * C * D * 2;
-      const uint32_t sboA = (C / 8) * 128, sboK = (C / 8) * 128;
-#pragma unroll 1
-      for (int term = 0; term < 2; ++term) {
-        const uint32_t a = smem_u32(term == 0 ? A2h : A2l);
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16(tbase + D2_COL, make_desc(a + kk * 256, 128, sboA), make_desc(k_img + kk * 256, 128, sboK),
-                   IDESC2, 1u);
+    // outputs for the state after full chunk j (j = 0 .. nfull): rows of S^(j)
+    auto write_state = [&](int j, const float* v, int c0) {
+      if (w.seqs) {
+        if (j < nchunks) store_row16(w.bnd + ((item0 + j) * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+        if (j == nfull) {
+          if (len % C == 0 && w.state_out)
+            store_row16(w.state_out + ((int64_t)n * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+          if (sl >= 0) {
+            store_row16(w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+            if (len % C == 0)
+              store_row16(w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+          }
+        }
+      } else if (j > 0) {
+        store_row16(w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+        store_row16(w.s_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
       }
-      mma_commit(&bars[2]);
-    }
-    if (!__syncthreads_and(mbar_wait(&bars[2], mma_phase))) { failed = true; break; }
-    mma_phase ^= 1u;
-    fence_after_sync();
-    {  // S^(j+1): outputs, next step's A operand and gamma_{j+1} S^(j+1)
-      const bool more = j + 1 < nfull;
-      const float gn = more ? gamma[(item + 1) * dm.hv + h] : 0.f;
+    };
+    if (nfull == 0) {  // no full chunk: S^(0) passes straight to the outputs
       for (int c0 = 0; c0 < D; c0 += 16) {
         float v[16];
-        tmem_ld16(tlane + D2_COL + c0, v);
-        write_state(j + 1, v, c0);
-        if (more) {
-          store_split16(A1h, A1l, row, c0, D, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gn, v[e]);
-          tmem_st16(tlane + D2_COL + c0, v);
-        }
+        for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
+        write_state(0, v, c0);
+      }
+      continue;
+    }
+    if (t == 0) {
+      const int b = (int)(gstep & 1u);
+      mbar_expect_tx(&bars[b], STAGE_BYTES);
+      bulk_g2s(stage0 + b * STAGE_BYTES, Wimg + (item0 * dm.hv + h) * WS, STAGE_BYTES, &bars[b]);
+    }
+    pending = (int)(gstep & 1u);
+    {  // S^(0): outputs, A operand (split) and gamma_0 S^(0) into D2
+      const float g0 = gamma[item0 * dm.hv + h];
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
+        write_state(0, v, c0);
+        store_split16(A1h, A1l, row, c0, D, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(g0, v[e]);
+        tmem_st16(tlane + D2_COL + c0, v);
       }
       tmem_st_wait();
     }
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
+
+    for (int j = 0; j < nfull; ++j, ++gstep) {
+      const int64_t item = item0 + j;
+      const int buf = (int)(gstep & 1u);
+      unsigned char* stg = stage0 + buf * STAGE_BYTES;
+      if (j + 1 < nfull) {
+        if (t == 0) {
+          mbar_expect_tx(&bars[buf ^ 1], STAGE_BYTES);
+          bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, Wimg + ((item + 1) * dm.hv + h) * WS, STAGE_BYTES,
+                   &bars[buf ^ 1]);
+        }
+      }
+      float ud[C];
+      {
+        const float* Ug = U + (item * dm.hv + h) * (int64_t)C * D + row;
+#pragma unroll
+        for (int s = 0; s < C; ++s) ud[s] = Ug[(int64_t)s * D];
+      }
+      ok = __syncthreads_and(mbar_wait(&bars[buf], uses[buf] & 1u)) != 0;
+      if (!ok) break;
+      ++uses[buf];
+      pending = (j + 1 < nfull) ? (buf ^ 1) : -1;
+      if (t == 0) {  // D1 = S Wd^T (three split terms)
+        fence_after_sync();
+        const uint32_t a_hi = smem_u32(A1h), a_lo = smem_u32(A1l);
+        const uint32_t w_hi = smem_u32(stg), w_lo = w_hi + C * D * 2;
+        const uint32_t sbo = (D / 8) * 128;
+#pragma unroll 1
+        for (int term = 0; term < 3; ++term) {
+          const uint32_t a = term == 2 ? a_lo : a_hi;
+          const uint32_t b = term == 1 ? w_lo : w_hi;
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16(tbase + D1_COL, make_desc(a + kk * 256, 128, sbo), make_desc(b + kk * 256, 128, sbo), IDESC1,
+                     (term > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&bars[2]);
+      }
+      mma_pending = true;
+      ok = __syncthreads_and(mbar_wait(&bars[2], mma_phase)) != 0;
+      if (!ok) break;
+      mma_phase ^= 1u;
+      mma_pending = false;
+      fence_after_sync();
+      for (int s0 = 0; s0 < C; s0 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
+        float v[16];
+        tmem_ld16(tlane + D1_COL + s0, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s0 + e], v[e]);
+        store_split16(A2h, A2l, row, s0, C, v);
+      }
+      fence_proxy_async();
+      fence_before_sync();
+      __syncthreads();
+      if (t == 0) {  // D2 += Vd^T K (two split terms)
+        fence_after_sync();
+        const uint32_t k_img = smem_u32(stg) + 2 * C * D * 2;
+        const uint32_t sbo = (C / 8) * 128;
+#pragma unroll 1
+        for (int term = 0; term < 2; ++term) {
+          const uint32_t a = smem_u32(term == 0 ? A2h : A2l);
+          for (int kk = 0; kk < C / 16; ++kk)
+            mma_bf16(tbase + D2_COL, make_desc(a + kk * 256, 128, sbo), make_desc(k_img + kk * 256, 128, sbo),
+                     IDESC2, 1u);
+        }
+        mma_commit(&bars[2]);
+      }
+      mma_pending = true;
+      ok = __syncthreads_and(mbar_wait(&bars[2], mma_phase)) != 0;
+      if (!ok) break;
+      mma_phase ^= 1u;
+      mma_pending = false;
+      fence_after_sync();
+      {  // S^(j+1): outputs, next step's A operand and gamma_{j+1} S^(j+1)
+        const bool more = j + 1 < nfull;
+        const float gn = more ? gamma[(item + 1) * dm.hv + h] : 0.f;
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          float v[16];
+          tmem_ld16(tlane + D2_COL + c0, v);
+          write_state(j + 1, v, c0);
+          if (more) {
+            store_split16(A1h, A1l, row, c0, D, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(gn, v[e]);
+            tmem_st16(tlane + D2_COL + c0, v);
+          }
+        }
+        tmem_st_wait();
+      }
+      fence_proxy_async();
+      fence_before_sync();
+      __syncthreads();
+    }
   }
-  if (failed) {
-    if (t == 0) set_error(hdr, GDN_DEVERR_TIMEOUT);
+  if (!ok && t == 0) {
+    set_error(hdr, GDN_DEVERR_TIMEOUT);
     // let the operations this CTA may still have in flight finish before releasing TMEM
-    if (j + 1 < nfull) mbar_wait(&bars[(j & 1) ^ 1], (uint32_t)((j + 1) >> 1) & 1u);
-    mbar_wait(&bars[2], mma_phase);
+    if (pending >= 0) mbar_wait(&bars[pending], uses[pending] & 1u);
+    if (mma_pending) mbar_wait(&bars[2], mma_phase);
   }
   fence_before_sync();
   __syncthreads();
@@ -770,173 +825,203 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
   unsigned char* TKl = R0 + C * C * 2;
   unsigned char* TVh = reinterpret_cast<unsigned char*>(A);
   unsigned char* TVl = TVh + C * C * 2;
-
   const int t = threadIdx.x, warp = t >> 5;
-  const int h = blockIdx.y;
-  const int hq = h / (dm.hv / dm.hqk);
-  const int64_t item = blockIdx.x;
-  int64_t tok0;
-  if (w.chunks) {
-    if (!hdr->valid) return;
-    const ChunkRec rec = w.chunks[item];
-    if (rec.len != C) return;
-    tok0 = rec.tok0;
-  } else {
-    const int sl = w.slot[item];
-    if (sl < 0 || sl >= w.slots) {
-      if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_SLOT);
-      return;
+  if (w.chunks && !hdr->valid) return;
+  const int64_t total = w.n_items * dm.hv;
+  // Which of this CTA's items (wi = blockIdx.x + j * gridDim.x) need the pre-pass: all
+  // tested at once, one per thread; a CTA with none exits before touching tensor memory.
+  __shared__ int64_t s_list[256];
+  __shared__ int64_t s_tok0[256];
+  __shared__ int s_cnt;
+  if (t == 0) s_cnt = 0;
+  __syncthreads();
+  {
+    const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
+    if (wi < total) {
+      const int64_t item = wi / dm.hv;
+      const int h = (int)(wi % dm.hv);
+      int64_t tok0 = -1;
+      if (w.chunks) {
+        const ChunkRec rec = w.chunks[item];
+        if (rec.len == C) tok0 = rec.tok0;
+      } else {
+        const int sl = w.slot[item];
+        if (sl < 0 || sl >= w.slots) {
+          if (h == 0) set_error(hdr, GDN_DEVERR_SLOT);
+        } else {
+          const int p = w.pos[sl];
+          if (p < 0) {
+            if (h == 0) set_error(hdr, GDN_DEVERR_POS);
+          } else if ((p + 1) % C == 0) {
+            tok0 = (int64_t)sl * C;
+          }
+        }
+      }
+      if (tok0 >= 0) {
+        const int k = atomicAdd(&s_cnt, 1);
+        s_list[k] = wi;
+        s_tok0[k] = tok0;
+      }
     }
-    const int p = w.pos[sl];
-    if (p < 0) {
-      if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_POS);
-      return;
-    }
-    if ((p + 1) % C != 0) return;
-    tok0 = (int64_t)sl * C;
   }
-  const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(in.k);
-  const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(in.v);
-  const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
-  const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
-  const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
+  __syncthreads();
+  const int count = s_cnt;
+  if (count == 0) return;
 
-  // 1. operand images straight from global memory
-  for (int q = t; q < C * (D / 8); q += 256) {  // K rows: 16-byte pieces
-    const int r = q / (D / 8), c0 = (q % (D / 8)) * 8;
-    *reinterpret_cast<uint4*>(R0 + tc::kmajor_off(r, c0, D)) = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
-  }
-  for (int q = t; q < D * (C / 8); q += 256) {  // K^T and V^T: column e, 8 tokens at a time
-    const int e = q % D, r0 = (q / D) * 8;
-    uint32_t kw[4], vw[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      kw[x] = (uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x) * kstride + e]) |
-              ((uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x + 1) * kstride + e]) << 16);
-      vw[x] = (uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x) * vstride + e]) |
-              ((uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x + 1) * vstride + e]) << 16);
-    }
-    *reinterpret_cast<uint4*>(KT + tc::kmajor_off(e, r0, C)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
-    *reinterpret_cast<uint4*>(VT + tc::kmajor_off(e, r0, C)) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
-  }
-  if (t < C) {
-    gs[t] = in.g[(tok0 + t) * dm.hv + h];
-    bs[t] = in.beta[(tok0 + t) * dm.hv + h];
-  }
+  // tensor memory and the MMA barrier, once per CTA
   if (t == 0) {
     tc::mbar_init(bar, 1);
     tc::fence_mbar_init();
   }
   if (warp == 0) tc::tmem_alloc(tslot, TMEM_COLS);
-  tc::fence_proxy_async();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = *tslot;
   uint32_t phase = 0;
   bool ok = true;
-  // 2. Gram on the tensor cores while one thread forms G
-  if (t == 0) {
-    const uint32_t a = tc::smem_u32(R0);
-    for (int kk = 0; kk < D / 16; ++kk)
-      tc::mma_bf16(tbase + GRAM_COL, tc::make_desc(a + kk * 256, 128, (D / 8) * 128),
-                   tc::make_desc(a + kk * 256, 128, (D / 8) * 128), tc::idesc_bf16(128, C), kk > 0 ? 1u : 0u);
-    tc::mma_commit(bar);
-    float run = gs[0];
-    Gs[0] = run;
-    for (int i = 1; i < C; ++i) {
-      run = __fadd_rn(run, gs[i]);
-      Gs[i] = run;
+  const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(in.k);
+  const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(in.v);
+  const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
+
+  for (int li = 0; li < count && ok; ++li) {
+    const int64_t wi = s_list[li];
+    const int64_t item = wi / dm.hv;
+    const int h = (int)(wi % dm.hv);
+    const int hq = h / (dm.hv / dm.hqk);
+    const int64_t tok0 = s_tok0[li];
+    const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
+    const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
+
+    // 1. operand images straight from global memory
+    for (int q = t; q < C * (D / 8); q += 256) {  // K rows: 16-byte pieces
+      const int r = q / (D / 8), c0 = (q % (D / 8)) * 8;
+      *reinterpret_cast<uint4*>(R0 + tc::kmajor_off(r, c0, D)) = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
     }
-  }
-  __syncthreads();
-  if (t < C) {
-    bk[t] = __fmul_rn(bs[t], expf(Gs[t]));
-    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
-  }
-  {
-    const bool done = tc::mbar_wait(bar, phase);
-    if (done) phase ^= 1u;
-    ok = __syncthreads_and(done) != 0;
-  }
-  tc::fence_after_sync();
-  if (ok && (warp & 3) < 2) {  // rows 0..63: A_is = beta_i e^{G_i - G_s} Gram_is (i > s)
-    const int i = (warp & 3) * 32 + (t & 31);
-    const int cbase = (warp >> 2) * 32;
-    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
-      float v[16];
-      tc::tmem_ld16(tc::tmem_lane_addr(tbase, warp, GRAM_COL + s0), v);
+    for (int q = t; q < D * (C / 8); q += 256) {  // K^T and V^T: column e, 8 tokens at a time
+      const int e = q % D, r0 = (q / D) * 8;
+      uint32_t kw[4], vw[4];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int s = s0 + e;
-        A[i * CP + s] = (i > s) ? __fmul_rn(__fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s]))), v[e]) : 0.f;
+      for (int x = 0; x < 4; ++x) {
+        kw[x] = (uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x) * kstride + e]) |
+                ((uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x + 1) * kstride + e]) << 16);
+        vw[x] = (uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x) * vstride + e]) |
+                ((uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x + 1) * vstride + e]) << 16);
+      }
+      *reinterpret_cast<uint4*>(KT + tc::kmajor_off(e, r0, C)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+      *reinterpret_cast<uint4*>(VT + tc::kmajor_off(e, r0, C)) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+    }
+    if (t < C) {
+      gs[t] = in.g[(tok0 + t) * dm.hv + h];
+      bs[t] = in.beta[(tok0 + t) * dm.hv + h];
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    // 2. Gram on the tensor cores while one thread forms G
+    if (t == 0) {
+      tc::fence_after_sync();
+      const uint32_t a = tc::smem_u32(R0);
+      for (int kk = 0; kk < D / 16; ++kk)
+        tc::mma_bf16(tbase + GRAM_COL, tc::make_desc(a + kk * 256, 128, (D / 8) * 128),
+                     tc::make_desc(a + kk * 256, 128, (D / 8) * 128), tc::idesc_bf16(128, C), kk > 0 ? 1u : 0u);
+      tc::mma_commit(bar);
+      float run = gs[0];
+      Gs[0] = run;
+      for (int i = 1; i < C; ++i) {
+        run = __fadd_rn(run, gs[i]);
+        Gs[i] = run;
       }
     }
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  // 3. T = (I + A)^{-1}
-  blocked_unit_lower_inverse<256>(A, Tm, Xs, C, CP);
-  // 4. TK = T diag(beta e^G), TV = T diag(beta), split into bf16 images (lower triangle)
-  for (int q = t; q < C * (C / 8); q += 256) {
-    const int i = q / (C / 8), r0 = (q % (C / 8)) * 8;
-    float tk[8], tv[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int r = r0 + e;
-      const float x = (r <= i) ? Tm[i * CP + r] : 0.f;
-      tk[e] = __fmul_rn(x, bk[r]);
-      tv[e] = __fmul_rn(x, bs[r]);
+    __syncthreads();
+    if (t < C) {
+      bk[t] = __fmul_rn(bs[t], expf(Gs[t]));
+      dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
     }
-    uint32_t a[4], b[4], c2[4], d2[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __nv_bfloat16 h0, l0, h1, l1;
-      tc::split_bf16(tk[2 * e], h0, l0);
-      tc::split_bf16(tk[2 * e + 1], h1, l1);
-      a[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-      b[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-      tc::split_bf16(tv[2 * e], h0, l0);
-      tc::split_bf16(tv[2 * e + 1], h1, l1);
-      c2[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-      d2[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    {
+      const bool done = tc::mbar_wait(bar, phase);
+      ok = __syncthreads_and(done) != 0;
+      if (!ok) break;
+      phase ^= 1u;
     }
-    const uint32_t off = tc::kmajor_off(i, r0, C);
-    *reinterpret_cast<uint4*>(TKh + off) = make_uint4(a[0], a[1], a[2], a[3]);
-    *reinterpret_cast<uint4*>(TKl + off) = make_uint4(b[0], b[1], b[2], b[3]);
-    *reinterpret_cast<uint4*>(TVh + off) = make_uint4(c2[0], c2[1], c2[2], c2[3]);
-    *reinterpret_cast<uint4*>(TVl + off) = make_uint4(d2[0], d2[1], d2[2], d2[3]);
-  }
-  tc::fence_proxy_async();
-  tc::fence_before_sync();
-  __syncthreads();
-  // 5. W = TK K (rows 0..63 of a 128-row MMA) and U^T = V^T TV^T
-  if (t == 0 && ok) {
     tc::fence_after_sync();
-    const uint32_t sbo = (C / 8) * 128;
-    const uint32_t kt = tc::smem_u32(KT), vt = tc::smem_u32(VT);
-    for (int term = 0; term < 2; ++term) {
-      const uint32_t a = tc::smem_u32(term == 0 ? TKh : TKl);
-      const uint32_t b = tc::smem_u32(term == 0 ? TVh : TVl);
-      for (int kk = 0; kk < C / 16; ++kk) {
-        tc::mma_bf16(tbase + W_COL, tc::make_desc(a + kk * 256, 128, sbo), tc::make_desc(kt + kk * 256, 128, sbo),
-                     tc::idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_bf16(tbase + UT_COL, tc::make_desc(vt + kk * 256, 128, sbo), tc::make_desc(b + kk * 256, 128, sbo),
-                     tc::idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+    if ((warp & 3) < 2) {  // rows 0..63: A_is = beta_i e^{G_i - G_s} Gram_is (i > s)
+      const int i = (warp & 3) * 32 + (t & 31);
+      const int cbase = (warp >> 2) * 32;
+      for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+        float v[16];
+        tc::tmem_ld16(tc::tmem_lane_addr(tbase, warp, GRAM_COL + s0), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int s = s0 + e;
+          A[i * CP + s] = (i > s) ? __fmul_rn(__fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s]))), v[e]) : 0.f;
+        }
       }
     }
-    tc::mma_commit(bar);
-  }
-  if (ok) {
-    const bool done = tc::mbar_wait(bar, phase);
-    if (done) phase ^= 1u;
-    ok = __syncthreads_and(done) != 0;
-  }
-  tc::fence_after_sync();
-  float* Wo = Wout + (item * dm.hv + h) * (int64_t)prep_w_floats(C, D);
-  float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
-  unsigned char* img = reinterpret_cast<unsigned char*>(Wo);
-  if (ok) {
+    tc::fence_before_sync();
+    __syncthreads();
+    // 3. T = (I + A)^{-1}
+    blocked_unit_lower_inverse<256>(A, Tm, Xs, C, CP);
+    // 4. TK = T diag(beta e^G), TV = T diag(beta), split into bf16 images (lower triangle)
+    for (int q = t; q < C * (C / 8); q += 256) {
+      const int i = q / (C / 8), r0 = (q % (C / 8)) * 8;
+      float tk[8], tv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int r = r0 + e;
+        const float x = (r <= i) ? Tm[i * CP + r] : 0.f;
+        tk[e] = __fmul_rn(x, bk[r]);
+        tv[e] = __fmul_rn(x, bs[r]);
+      }
+      uint32_t a[4], b[4], c2[4], d2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        tc::split_bf16(tk[2 * e], h0, l0);
+        tc::split_bf16(tk[2 * e + 1], h1, l1);
+        a[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        b[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+        tc::split_bf16(tv[2 * e], h0, l0);
+        tc::split_bf16(tv[2 * e + 1], h1, l1);
+        c2[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        d2[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      const uint32_t off = tc::kmajor_off(i, r0, C);
+      *reinterpret_cast<uint4*>(TKh + off) = make_uint4(a[0], a[1], a[2], a[3]);
+      *reinterpret_cast<uint4*>(TKl + off) = make_uint4(b[0], b[1], b[2], b[3]);
+      *reinterpret_cast<uint4*>(TVh + off) = make_uint4(c2[0], c2[1], c2[2], c2[3]);
+      *reinterpret_cast<uint4*>(TVl + off) = make_uint4(d2[0], d2[1], d2[2], d2[3]);
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    // 5. W = TK K (rows 0..63 of a 128-row MMA) and U^T = V^T TV^T
+    if (t == 0) {
+      tc::fence_after_sync();
+      const uint32_t sbo = (C / 8) * 128;
+      const uint32_t kt = tc::smem_u32(KT), vt = tc::smem_u32(VT);
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t a = tc::smem_u32(term == 0 ? TKh : TKl);
+        const uint32_t b = tc::smem_u32(term == 0 ? TVh : TVl);
+        for (int kk = 0; kk < C / 16; ++kk) {
+          tc::mma_bf16(tbase + W_COL, tc::make_desc(a + kk * 256, 128, sbo), tc::make_desc(kt + kk * 256, 128, sbo),
+                       tc::idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_bf16(tbase + UT_COL, tc::make_desc(vt + kk * 256, 128, sbo), tc::make_desc(b + kk * 256, 128, sbo),
+                       tc::idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+        }
+      }
+      tc::mma_commit(bar);
+    }
+    {
+      const bool done = tc::mbar_wait(bar, phase);
+      ok = __syncthreads_and(done) != 0;
+      if (!ok) break;
+      phase ^= 1u;
+    }
+    tc::fence_after_sync();
+    float* Wo = Wout + (item * dm.hv + h) * (int64_t)prep_w_floats(C, D);
+    float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
+    unsigned char* img = reinterpret_cast<unsigned char*>(Wo);
     if ((warp & 3) < 2) {  // Wd rows 0..63 -> split image
       const int i = (warp & 3) * 32 + (t & 31);
       const int cbase = (warp >> 2) * 64;
@@ -975,9 +1060,12 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     for (int q = t; q < (int)(TILE / 16); q += 256)
       reinterpret_cast<uint4*>(img + 2 * TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
     if (t == 0) gamma_out[item * dm.hv + h] = expf(Gs[C - 1]);
-  } else if (t == 0) {
+    tc::fence_before_sync();
+    __syncthreads();  // shared memory and tensor memory are reused by the next item
+  }
+  if (!ok && t == 0) {
     set_error(hdr, GDN_DEVERR_TIMEOUT);
-    tc::mbar_wait(bar, phase);
+    tc::mbar_wait(bar, phase);  // let the MMA in flight finish before releasing its memory
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1077,7 +1165,7 @@ static void launch_intra_t(const Dims& d, const TokenArrays& in, const IntraWork
 
 // =====================================================================  K3  ====
 template <int D, typename Tin, typename Tout>
-__global__ void __launch_bounds__(2 * D) k_decode(Dims dm, TokenArrays in, DecodeWork w,
+__global__ void __launch_bounds__(2 * D, 2) k_decode(Dims dm, TokenArrays in, DecodeWork w,
                                                   WsHeader* __restrict__ hdr) {
   __shared__ __align__(16) float ks[D];
   __shared__ __align__(16) float qs[D];
@@ -1214,7 +1302,10 @@ void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float*
   if (w.n_items <= 0) return;
   if (boundary_on_tensor_cores(d)) {
     ensure_smem(k_prep_tc, tcp::SMEM);
-    k_prep_tc<<<dim3((unsigned)w.n_items, d.hv), 256, tcp::SMEM, st>>>(d, in, w, W, U, gamma, hdr);
+    const int64_t total = w.n_items * d.hv;
+    int64_t cap = w.chunks ? total : 2 * (int64_t)sm_count();
+    if ((total + cap - 1) / cap > 256) cap = (total + 255) / 256;  // at most 256 items per CTA
+    k_prep_tc<<<(unsigned)(total < cap ? total : cap), 256, tcp::SMEM, st>>>(d, in, w, W, U, gamma, hdr);
   } else if (d.in_bf16) {
     GDN_DISPATCH_D(d.D, launch_prep_t<DD, __nv_bfloat16>(d, in, w, W, U, gamma, hdr, st))
   } else {
@@ -1227,7 +1318,10 @@ void launch_chain(const Dims& d, const void* keys, const float* W, const float* 
   if (w.N <= 0) return;
   if (boundary_on_tensor_cores(d)) {
     ensure_smem(k_chain_tc, tcc::SMEM);
-    k_chain_tc<<<dim3((unsigned)w.N, d.hv), 128, tcc::SMEM, st>>>(d, W, U, gamma, w, hdr);
+    const int64_t total = (int64_t)w.N * d.hv;
+    int64_t cap = w.seqs ? total : (int64_t)sm_count();
+    if ((total + cap - 1) / cap > 128) cap = (total + 127) / 128;  // at most 128 items per CTA
+    k_chain_tc<<<(unsigned)(total < cap ? total : cap), 128, tcc::SMEM, st>>>(d, W, U, gamma, w, hdr);
   } else if (d.in_bf16) {
     GDN_DISPATCH_D(d.D, launch_chain_t<DD, __nv_bfloat16>(d, keys, W, U, gamma, w, hdr, st))
   } else {
