@@ -32,6 +32,7 @@
 #include "../../include/gdn_cpr.h"
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace gdn {
 namespace {
@@ -205,6 +206,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* A, float* Tm, fl
 // Per chunk-head workspace (floats), chunk length padded to C.
 struct BwdBufs {
   float *W, *Ut, *T, *P, *G, *L, *dSE, *U, *dU, *dOS0, *UdSe, *dW, *sdot;
+  float* img;  // tensor-core shapes: per chunk-head [K rows | W^T hi | W^T lo] bf16 images
   float *dq_part, *dk_part;  // [T, Hv, D]
 };
 
@@ -322,6 +324,35 @@ __global__ void __launch_bounds__(NT) k_bwd_prep(BwdArgs a) {
   if (t < C) a.b.G[ch * C + t] = Gs[t];
   load_rows<D>(B3, DP, qin + (tok0 * dm.hqk + hq) * D, (int64_t)dm.hqk * D, n, C);
   __syncthreads();
+  if constexpr (D == 128) {
+    if (boundary_on_tensor_cores(dm)) {  // operand images for the tensor-core reverse chain
+      unsigned char* img = reinterpret_cast<unsigned char*>(a.b.img + ch * (int64_t)prep_w_floats(C, D));
+      for (int q = t; q < C * (D / 8); q += NT) {  // K rows (exact in bf16)
+        const int r = q / (D / 8), c0 = (q % (D / 8)) * 8;
+        uint32_t w4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w4[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(B0[r * DP + c0 + 2 * e])) |
+                  ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(B0[r * DP + c0 + 2 * e + 1])) << 16);
+        *reinterpret_cast<uint4*>(img + tc::kmajor_off(r, c0, D)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+      for (int q = t; q < D * (C / 8); q += NT) {  // W^T split: row c, 8 chunk positions
+        const int cc = q % D, i0 = (q / D) * 8;
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          __nv_bfloat16 h0, l0, h1, l1;
+          tc::split_bf16(B2[(i0 + 2 * e) * DP + cc], h0, l0);
+          tc::split_bf16(B2[(i0 + 2 * e + 1) * DP + cc], h1, l1);
+          hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+        }
+        const uint32_t off = tc::kmajor_off(cc, i0, C);
+        *reinterpret_cast<uint4*>(img + C * D * 2 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(img + 2 * C * D * 2 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+    }
+  }
   // P = Gam * (Q K^T), lower triangle with diagonal
   gemm<4, 4, false, true>(C, C, D, B3, DP, B0, DP, [&](int i, int s, float v) {
     const float p = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v) : 0.f;
@@ -745,6 +776,211 @@ __global__ void k_bwd_gqa(const float* __restrict__ dq_part, const float* __rest
   }
 }
 
+// ============================================================  KB2 (tcgen05)  ===
+// Reverse boundary chain on tensor cores (bf16 inputs, d = 128, C = 64): one CTA of 128
+// threads per (sequence, head), thread i owns adjoint row i = TMEM lane i.  Per chunk j,
+// from the end adjoint dS = dS^(j+1):
+//     D1 (128 x 64)  = dS K^T                     2 MMAs: dS_hi K + dS_lo K (K exact)
+//     Xd[i][s]       = -dec_s D1[i][s]            (split to bf16 hi/lo)
+//     D2 (128 x 128) = (L_j + gamma_j dS) + Xd W   D2 preloaded, 3 MMAs with W = W_hi + W_lo
+// giving dS^(j).  Operands [K rows | W^T hi | W^T lo] come as one bulk copy per chunk,
+// prefetched a chunk ahead.
+namespace tcb {
+constexpr int D = 128, C = 64;
+constexpr uint32_t A1_BYTES = 128 * D * 2, A2_BYTES = 128 * C * 2, STAGE_BYTES = 3 * C * D * 2;
+constexpr size_t SMEM = 2 * (size_t)A1_BYTES + 2 * (size_t)A2_BYTES + 2 * (size_t)STAGE_BYTES + 64 * 4 + 64;
+constexpr uint32_t TMEM_COLS = 256, D1_COL = 0, D2_COL = 64;
+}  // namespace tcb
+
+__device__ __forceinline__ void split_store16(unsigned char* hi, unsigned char* lo, int row, int k0, int K,
+                                              const float* v) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat16 h0, l0, h1, l1;
+      tc::split_bf16(v[8 * g + 2 * e], h0, l0);
+      tc::split_bf16(v[8 * g + 2 * e + 1], h1, l1);
+      hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    const uint32_t off = tc::kmajor_off(row, k0 + 8 * g, K);
+    *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+__global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
+  using namespace tcb;
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smb[];
+  unsigned char* A1h = smb;
+  unsigned char* A1l = A1h + A1_BYTES;
+  unsigned char* A2h = A1l + A1_BYTES;
+  unsigned char* A2l = A2h + A2_BYTES;
+  unsigned char* stage0 = A2l + A2_BYTES;
+  float* decs = reinterpret_cast<float*>(stage0 + 2 * STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(decs + 64);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, warp = t >> 5, row = t;
+  const int n = blockIdx.x, h = blockIdx.y;
+  const SeqRec rec = a.seqs[n];
+  const int64_t SZ = (int64_t)D * D;
+  const int64_t IW = (int64_t)prep_w_floats(C, D);
+  const int64_t srow = ((int64_t)n * dm.hv + h) * SZ + (int64_t)row * D;
+  const int nch = rec.nchunks;
+  if (nch == 0) {  // no tokens: dstate_in = dstate_out
+    if (a.dstate_in)
+      for (int c0 = 0; c0 < D; ++c0) a.dstate_in[srow + c0] = a.dstate_out ? a.dstate_out[srow + c0] : 0.f;
+    return;
+  }
+  if (t == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    mbar_init(&bars[2], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);
+  auto chead = [&](int j) { return ((int64_t)rec.chunk0 + j) * dm.hv + h; };
+  auto gamma_of = [&](int j) { return expf(a.b.G[chead(j) * C + C - 1]); };
+  // prologue: dS^(nch) = dstate_out is the end adjoint of the last chunk
+  {
+    const int j = nch - 1;
+    if (t == 0) {
+      mbar_expect_tx(&bars[0], STAGE_BYTES);
+      bulk_g2s(stage0, a.b.img + chead(j) * IW, STAGE_BYTES, &bars[0]);
+    }
+    const float g = gamma_of(j);
+    const float* L = a.b.L + chead(j) * SZ + (int64_t)row * D;
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      float v[16], w[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = a.dstate_out ? a.dstate_out[srow + c0 + e] : 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(a.b.dSE + chead(j) * SZ + (int64_t)row * D + c0 + e) =
+            make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      split_store16(A1h, A1l, row, c0, D, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(L[c0 + e], __fmul_rn(g, v[e]));
+      tmem_st16(tlane + D2_COL + c0, w);
+    }
+    tmem_st_wait();
+  }
+  fence_proxy_async();
+  fence_before_sync();
+  __syncthreads();
+  uint32_t uses[2] = {0u, 0u}, mma_phase = 0;
+  int pending = 0;
+  bool mma_pending = false, ok = true;
+  int q = 0;
+  for (; q < nch; ++q) {
+    const int j = nch - 1 - q;
+    const int buf = q & 1;
+    unsigned char* stg = stage0 + buf * STAGE_BYTES;
+    if (j > 0 && t == 0) {
+      mbar_expect_tx(&bars[buf ^ 1], STAGE_BYTES);
+      bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, a.b.img + chead(j - 1) * IW, STAGE_BYTES, &bars[buf ^ 1]);
+    }
+    if (t < C) decs[t] = -expf(__fsub_rn(a.b.G[chead(j) * C + C - 1], a.b.G[chead(j) * C + t]));
+    ok = __syncthreads_and(mbar_wait(&bars[buf], uses[buf] & 1u)) != 0;
+    if (!ok) break;
+    ++uses[buf];
+    pending = j > 0 ? (buf ^ 1) : -1;
+    if (t == 0) {  // D1 = dS K^T
+      fence_after_sync();
+      const uint32_t kimg = smem_u32(stg), sbo = (D / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t aa = smem_u32(term == 0 ? A1h : A1l);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16(tbase + D1_COL, make_desc(aa + kk * 256, 128, sbo), make_desc(kimg + kk * 256, 128, sbo),
+                   idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&bars[2]);
+    }
+    mma_pending = true;
+    ok = __syncthreads_and(mbar_wait(&bars[2], mma_phase)) != 0;
+    if (!ok) break;
+    mma_phase ^= 1u;
+    mma_pending = false;
+    fence_after_sync();
+    for (int s0 = 0; s0 < C; s0 += 16) {  // Xd = -dec_s (dS K^T), split into A2
+      float v[16];
+      tmem_ld16(tlane + D1_COL + s0, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(decs[s0 + e], v[e]);
+      split_store16(A2h, A2l, row, s0, C, v);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    if (t == 0) {  // D2 += Xd W (three split terms)
+      fence_after_sync();
+      const uint32_t wh = smem_u32(stg) + C * D * 2, wl = wh + C * D * 2, sbo = (C / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t aa = smem_u32(term == 2 ? A2l : A2h);
+        const uint32_t bb = term == 1 ? wl : wh;
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16(tbase + D2_COL, make_desc(aa + kk * 256, 128, sbo), make_desc(bb + kk * 256, 128, sbo),
+                   idesc_bf16(128, D), 1u);
+      }
+      mma_commit(&bars[2]);
+    }
+    mma_pending = true;
+    ok = __syncthreads_and(mbar_wait(&bars[2], mma_phase)) != 0;
+    if (!ok) break;
+    mma_phase ^= 1u;
+    mma_pending = false;
+    fence_after_sync();
+    {  // dS^(j): end adjoint of chunk j-1 (or dstate_in), next A operand, next D2 preload
+      const bool more = j > 0;
+      const float g = more ? gamma_of(j - 1) : 0.f;
+      const float* L = more ? a.b.L + chead(j - 1) * SZ + (int64_t)row * D : nullptr;
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + D2_COL + c0, v);
+        if (more) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(a.b.dSE + chead(j - 1) * SZ + (int64_t)row * D + c0 + e) =
+                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          split_store16(A1h, A1l, row, c0, D, v);
+          float w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(L[c0 + e], __fmul_rn(g, v[e]));
+          tmem_st16(tlane + D2_COL + c0, w);
+        } else if (a.dstate_in) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(a.dstate_in + srow + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+      }
+      tmem_st_wait();
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+  }
+  if (!ok && t == 0) {
+    set_error(a.hdr, GDN_DEVERR_TIMEOUT);
+    if (pending >= 0) mbar_wait(&bars[pending], uses[pending] & 1u);
+    if (mma_pending) mbar_wait(&bars[2], mma_phase);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
+}
+
 template <int D, typename Tin>
 void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, void* mark_ctx,
                   cudaStream_t st) {
@@ -754,8 +990,13 @@ void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, vo
     k_bwd_prep<D, Tin><<<gc, NT, bprep_smem<D>(), st>>>(a);
   }
   mark(mark_ctx, n_chunks > 0 ? 1 : 0);
-  ensure_smem_bwd(k_bwd_chain<D, Tin>, bchain_smem<D>());
-  k_bwd_chain<D, Tin><<<dim3((unsigned)N, a.dm.hv, D / kRowsPerChain), NT, bchain_smem<D>(), st>>>(a);
+  if (boundary_on_tensor_cores(a.dm)) {
+    ensure_smem_bwd(k_bwd_chain_tc, tcb::SMEM);
+    k_bwd_chain_tc<<<dim3((unsigned)N, a.dm.hv), 128, tcb::SMEM, st>>>(a);
+  } else {
+    ensure_smem_bwd(k_bwd_chain<D, Tin>, bchain_smem<D>());
+    k_bwd_chain<D, Tin><<<dim3((unsigned)N, a.dm.hv, D / kRowsPerChain), NT, bchain_smem<D>(), st>>>(a);
+  }
   mark(mark_ctx, 1);
   if (n_chunks > 0) {
     ensure_smem_bwd(k_bwd_big<D, Tin>, bbig_smem<D>());
@@ -778,7 +1019,7 @@ void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, vo
 }  // namespace
 
 size_t bwd_workspace_floats_per_chunk_head(int C, int D) {
-  return (size_t)7 * C * D + 2 * (size_t)C * C + C + 2 * (size_t)D * D + 1;
+  return (size_t)7 * C * D + 2 * (size_t)C * C + C + 2 * (size_t)D * D + 1 + prep_w_floats(C, D) + 3;
 }
 
 void launch_bwd(const Dims& d, const TokenArrays& in, const void* dO, const ChunkRec* chunks,
@@ -817,6 +1058,8 @@ void launch_bwd(const Dims& d, const TokenArrays& in, const void* dO, const Chun
   a.b.dSE = p;  p += nch * D * D;
   a.b.G = p;    p += nch * C;
   a.b.sdot = p; p += nch;
+  p += (4 - ((p - per_chunk) & 3)) & 3;  // 16-byte alignment for the bulk-copied images
+  a.b.img = p;  p += nch * prep_w_floats((int)C, (int)D);
   a.b.dq_part = dq_part;
   a.b.dk_part = dk_part;
   if (d.in_bf16) {
