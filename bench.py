@@ -542,6 +542,7 @@ def run_ncu_case(args):
     """Small, fixed cases for ncu captures (a few hundred MB on the device):
     prefill   one 4096-token sequence, 16/32 heads, d=128, C=64, bf16: three prefills
     decode    64 slots x 32 heads of 128x128 states: three decode steps (no resync)
+    bwd       one 4096-token sequence: two trainer forward + backward passes
     """
     import torch
 
@@ -549,7 +550,15 @@ def run_ncu_case(args):
 
     dev = torch.device("cuda", 0)
     w = synth.workloads()[WORKLOAD]
-    if args.ncu_case == "prefill":
+    if args.ncu_case == "bwd":
+        x = synth.make_inputs([4096], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0, dout=True)
+        t = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta", "cu_seqlens", "dout")}
+        for _ in range(2):
+            _, _, saved = api.fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"],
+                                  chunk=w.chunk, cu_seqlens_host=x["cu_seqlens"])
+            api.bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], saved, t["dout"],
+                    chunk=w.chunk, cu_seqlens_host=x["cu_seqlens"])
+    elif args.ncu_case == "prefill":
         x = synth.make_inputs([4096], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0)
         t = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta", "cu_seqlens")}
         for _ in range(3):
@@ -578,7 +587,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "bwd"], default=None,
                     help="run a small fixed case for an ncu capture and exit")
     args = ap.parse_args(argv)
     if args.ncu_case:

@@ -328,7 +328,8 @@ __global__ void __launch_bounds__(NT) k_bwd_prep(BwdArgs a) {
     if (boundary_on_tensor_cores(dm)) {  // operand images for the tensor-core reverse chain
       unsigned char* img = reinterpret_cast<unsigned char*>(a.b.img + ch * (int64_t)prep_w_floats(C, D));
       for (int q = t; q < C * (D / 8); q += NT) {  // K rows (exact in bf16)
-        const int r = q / (D / 8), c0 = (q % (D / 8)) * 8;
+        int r, c0;
+        tc::kmajor_piece(q, D, r, c0);
         uint32_t w4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -891,6 +892,17 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
       bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, a.b.img + chead(j - 1) * IW, STAGE_BYTES, &bars[buf ^ 1]);
     }
     if (t < C) decs[t] = -expf(__fsub_rn(a.b.G[chead(j) * C + C - 1], a.b.G[chead(j) * C + t]));
+    float lpre[D];  // next step's L row, loaded while this step's MMAs run
+    float gpre = 0.f;
+    if (j > 0) {
+      const float4* L4 = reinterpret_cast<const float4*>(a.b.L + chead(j - 1) * SZ + (int64_t)row * D);
+#pragma unroll
+      for (int e = 0; e < D / 4; ++e) {
+        const float4 x = L4[e];
+        lpre[4 * e] = x.x; lpre[4 * e + 1] = x.y; lpre[4 * e + 2] = x.z; lpre[4 * e + 3] = x.w;
+      }
+      gpre = gamma_of(j - 1);
+    }
     ok = __syncthreads_and(mbar_wait(&bars[buf], uses[buf] & 1u)) != 0;
     if (!ok) break;
     ++uses[buf];
@@ -944,8 +956,8 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
     fence_after_sync();
     {  // dS^(j): end adjoint of chunk j-1 (or dstate_in), next A operand, next D2 preload
       const bool more = j > 0;
-      const float g = more ? gamma_of(j - 1) : 0.f;
-      const float* L = more ? a.b.L + chead(j - 1) * SZ + (int64_t)row * D : nullptr;
+      const float g = gpre;
+#pragma unroll
       for (int c0 = 0; c0 < D; c0 += 16) {
         float v[16];
         tmem_ld16(tlane + D2_COL + c0, v);
@@ -957,7 +969,7 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
           split_store16(A1h, A1l, row, c0, D, v);
           float w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(L[c0 + e], __fmul_rn(g, v[e]));
+          for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(lpre[c0 + e], __fmul_rn(g, v[e]));
           tmem_st16(tlane + D2_COL + c0, w);
         } else if (a.dstate_in) {
 #pragma unroll
@@ -981,6 +993,334 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
   if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
 
+// ============================================================  KB3 (tcgen05)  ===
+// The backward's products with the d x d matrices S0 = S^(j) and E = dS_end, on tensor
+// cores (bf16 inputs, d = 128, C = 64), one CTA of 256 threads per chunk-head.  Every
+// product is taken transposed so that a 128 x 128 state matrix is the A operand (M = 128):
+//   phase 1  A = S0     : U^T   = Ut^T - S0 W^T
+//   phase 2  A = E      : (E K^T) and, with A = dO^T, dO^T P  ->  dU^T = dO^T P + (E K^T) diag(dec)
+//   phase 3  A = E^T    : (U E)^T  = E^T U^T
+//   phase 4  A = S0^T   : (dO S0)^T = S0^T dO^T,   dW^T = -S0^T dU^T
+// fp32 operands are split into bf16 hi + lo (three MMAs per product, lo x lo dropped);
+// bf16 inputs are exact.  Results go to the same global arrays as the SIMT kernel.
+namespace tcg {
+constexpr int D = 128, C = 64;
+constexpr uint32_t RA = 2 * 128 * D * 2;       // A operand hi | lo (64 KB)
+constexpr uint32_t RB = 2 * C * D * 2;         // B region (32 KB)
+constexpr size_t SMEM = (size_t)RA + 2 * (size_t)RB + C * 4 + 256 * 4 + 64;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_U = 0, COL_E = 64, COL_DOP = 128, COL_UE = 192, COL_DOS = 256, COL_DW = 320;
+}  // namespace tcg
+
+// 8 fp32 values -> hi / lo bf16 16-byte pieces at byte offset `off` of the two images
+__device__ __forceinline__ void split8(unsigned char* hi, unsigned char* lo, uint32_t off, const float* v) {
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    __nv_bfloat16 h0, l0, h1, l1;
+    tc::split_bf16(v[2 * e], h0, l0);
+    tc::split_bf16(v[2 * e + 1], h1, l1);
+    hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+    lw[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+  }
+  *reinterpret_cast<uint4*>(hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+// R x K image pair (hi at `hi`, lo at `lo`) of a row-major fp32 matrix src[r * ld + k]
+// (rows >= nvalid are zero); TRANS takes src[k * ld + r] instead (columns >= nvalid zero).
+// All loads of the build are issued before any is used.
+template <bool TRANS, int R, int K>
+__device__ __forceinline__ void build_split(unsigned char* hi, unsigned char* lo, const float* __restrict__ src,
+                                            int ld, int nvalid) {
+  constexpr int ITER = R * (K / 8) / 256;
+  static_assert(ITER * 256 == R * (K / 8), "tile must split evenly over 256 threads");
+  float v[ITER][8];
+#pragma unroll
+  for (int it = 0; it < ITER; ++it) {
+    const int q = threadIdx.x + it * 256;
+    int r, k0;
+    if (TRANS) {
+      r = q % R;
+      k0 = (q / R) * 8;
+    } else {
+      tc::kmajor_piece(q, K, r, k0);
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (TRANS)
+        v[it][e] = (k0 + e < nvalid) ? src[(int64_t)(k0 + e) * ld + r] : 0.f;
+      else
+        v[it][e] = (r < nvalid) ? src[(int64_t)r * ld + k0 + e] : 0.f;
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < ITER; ++it) {
+    const int q = threadIdx.x + it * 256;
+    int r, k0;
+    if (TRANS) {
+      r = q % R;
+      k0 = (q / R) * 8;
+    } else {
+      tc::kmajor_piece(q, K, r, k0);
+    }
+    split8(hi, lo, tc::kmajor_off(r, k0, K), v[it]);
+  }
+}
+
+// D = A B^T over K with split operands: terms = 3 gives A_hi B_hi + A_hi B_lo + A_lo B_hi;
+// terms = 2 (B exact, blo ignored) gives A_hi B + A_lo B.
+__device__ __forceinline__ void mma_terms(uint32_t d, uint32_t ahi, uint32_t alo, uint32_t bhi, uint32_t blo,
+                                          int K, uint32_t idesc, int terms) {
+  const uint32_t sbo = (uint32_t)(K / 8) * 128;
+  for (int term = 0; term < terms; ++term) {
+    const uint32_t aa = (terms == 3 ? term == 2 : term == 1) ? alo : ahi;
+    const uint32_t bb = (terms == 3 && term == 1) ? blo : bhi;
+    for (int kk = 0; kk < K / 16; ++kk)
+      tc::mma_bf16(d, tc::make_desc(aa + kk * 256, 128, sbo), tc::make_desc(bb + kk * 256, 128, sbo), idesc,
+                   (term > 0 || kk > 0) ? 1u : 0u);
+  }
+}
+
+__global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
+  using namespace tcg;
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smg[];
+  unsigned char* Ah = smg;
+  unsigned char* Al = Ah + RA / 2;
+  unsigned char* B1h = smg + RA;
+  unsigned char* B1l = B1h + RB / 2;
+  unsigned char* B2 = B1h + RB;
+  float* dec = reinterpret_cast<float*>(B2 + RB);
+  float* red = dec + C;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 256);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, warp = t >> 5;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const ChunkRec rec = a.chunks[c];
+  const int n = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t ch = c * dm.hv + h;
+  const int64_t SZ = (int64_t)D * D, CD = (int64_t)C * D;
+  const float* S0 = a.saved_bnd + ch * SZ;
+  const float* E = a.b.dSE + ch * SZ;
+  const int lane_row = (warp & 3) * 32 + (t & 31);  // TMEM lane = row of the transposed result
+  const int cbase = (warp >> 2) * 32;               // this warp's 32 result columns
+  if (t < C) dec[t] = expf(__fsub_rn(a.b.G[ch * C + C - 1], a.b.G[ch * C + t]));
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tb = *tslot;
+  const uint32_t tl = tmem_lane_addr(tb, warp, 0);
+  uint32_t phase = 0;
+  bool ok = true;
+  auto run = [&]() {  // all threads: wait for the committed MMAs
+    const bool done = mbar_wait(bar, phase);
+    if (done) phase ^= 1u;
+    ok = __syncthreads_and(done) != 0;
+    fence_after_sync();
+  };
+  auto issue_begin = [&]() {
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+  };
+
+  // ---- phase 1: U^T = Ut^T - S0 W^T
+  build_split<false, 128, D>(Ah, Al, S0, D, 128);
+  build_split<false, C, D>(B1h, B1l, a.b.W + ch * CD, D, C);
+  issue_begin();
+  if (t == 0) {
+    fence_after_sync();
+    mma_terms(tb + COL_U, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
+    mma_commit(bar);
+  }
+  run();
+  if (ok) {
+    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+      float v[16];
+      tmem_ld16(tl + COL_U + s0, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int64_t o = ch * CD + (int64_t)(s0 + e) * D + lane_row;
+        a.b.U[o] = __fsub_rn(a.b.Ut[o], v[e]);
+      }
+    }
+  }
+  {  // <E, S0>: thread t takes float4 groups t, t + 256, ... (loads issued in batches of 8)
+    float part = 0.f;
+#pragma unroll
+    for (int b8 = 0; b8 < (D * D / 4) / 256; b8 += 8) {
+      float4 x[8], y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        x[u] = reinterpret_cast<const float4*>(E)[t + (b8 + u) * 256];
+        y[u] = reinterpret_cast<const float4*>(S0)[t + (b8 + u) * 256];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        part = __fmaf_rn(x[u].x, y[u].x, part);
+        part = __fmaf_rn(x[u].y, y[u].y, part);
+        part = __fmaf_rn(x[u].z, y[u].z, part);
+        part = __fmaf_rn(x[u].w, y[u].w, part);
+      }
+    }
+    red[t] = part;
+  }
+  fence_before_sync();
+  __syncthreads();
+  for (int w2 = 128; w2 > 0; w2 >>= 1) {
+    if (t < w2) red[t] = __fadd_rn(red[t], red[t + w2]);
+    __syncthreads();
+  }
+  if (t == 0) a.b.sdot[ch] = red[0];
+
+  // ---- phase 2: E K^T and dO^T P
+  if (ok) {
+    build_split<false, 128, D>(Ah, Al, E, D, 128);
+    {  // K rows (exact in bf16), rows >= n zero
+      const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + (tok0 * dm.hqk + hq) * D;
+      for (int q = t; q < C * (D / 8); q += 256) {
+        int r, k0;
+        kmajor_piece(q, D, r, k0);
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (r < n) x = *reinterpret_cast<const uint4*>(kb + (int64_t)r * dm.hqk * D + k0);
+        *reinterpret_cast<uint4*>(B2 + kmajor_off(r, k0, D)) = x;
+      }
+    }
+    // P^T (rows s, K = i) into the second half of B2; dO^T (rows a, K = i) into B1
+    build_split<true, C, C>(B2 + C * D * 2, B2 + C * D * 2 + C * C * 2, a.b.P + ch * C * C, C, C);
+    {
+      float v[4][8];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = k0 + e;
+          float x = 0.f;
+          if (i < n) {
+            const int64_t o = ((tok0 + i) * dm.hv + h) * D + r;
+            x = dm.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.dO)[o])
+                            : static_cast<const float*>(a.dO)[o];
+          }
+          v[it][e] = x;
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
+        split8(B1h, B1h + 128 * C * 2, kmajor_off(r, k0, C), v[it]);
+      }
+    }
+    issue_begin();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_E, smem_u32(Ah), smem_u32(Al), smem_u32(B2), smem_u32(B2), D, idesc_bf16(128, C), 2);
+      mma_terms(tb + COL_DOP, smem_u32(B1h), smem_u32(B1h) + 128 * C * 2, smem_u32(B2) + C * D * 2,
+                smem_u32(B2) + C * D * 2 + C * C * 2, C, idesc_bf16(128, C), 3);
+      mma_commit(bar);
+    }
+    run();
+  }
+  if (ok) {
+    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+      float e1[16], p1[16];
+      tmem_ld16(tl + COL_E + s0, e1);
+      tmem_ld16(tl + COL_DOP + s0, p1);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        a.b.dU[ch * CD + (int64_t)(s0 + e) * D + lane_row] = __fmaf_rn(dec[s0 + e], e1[e], p1[e]);
+    }
+    fence_before_sync();
+    __syncthreads();
+    // ---- phase 3: (U E)^T = E^T U^T
+    build_split<true, 128, D>(Ah, Al, E, D, 128);
+    build_split<false, C, D>(B1h, B1l, a.b.U + ch * CD, D, C);
+    issue_begin();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_UE, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
+      mma_commit(bar);
+    }
+    run();
+  }
+  if (ok) {
+    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+      float v[16];
+      tmem_ld16(tl + COL_UE + s0, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) a.b.UdSe[ch * CD + (int64_t)(s0 + e) * D + lane_row] = v[e];
+    }
+    fence_before_sync();
+    __syncthreads();
+    // ---- phase 4: (dO S0)^T = S0^T dO^T and dW^T = -S0^T dU^T
+    build_split<true, 128, D>(Ah, Al, S0, D, 128);
+    {  // dO rows (i, K = a), split
+      float v[4][8];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256;
+        int r, k0;
+        kmajor_piece(q, D, r, k0);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float x = 0.f;
+          if (r < n) {
+            const int64_t o = ((tok0 + r) * dm.hv + h) * D + k0 + e;
+            x = dm.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.dO)[o])
+                            : static_cast<const float*>(a.dO)[o];
+          }
+          v[it][e] = x;
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256;
+        int r, k0;
+        kmajor_piece(q, D, r, k0);
+        split8(B1h, B1l, kmajor_off(r, k0, D), v[it]);
+      }
+    }
+    build_split<false, C, D>(B2, B2 + C * D * 2, a.b.dU + ch * CD, D, C);
+    issue_begin();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_DOS, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
+      mma_terms(tb + COL_DW, smem_u32(Ah), smem_u32(Al), smem_u32(B2), smem_u32(B2) + C * D * 2, D,
+                idesc_bf16(128, C), 3);
+      mma_commit(bar);
+    }
+    run();
+  }
+  if (ok) {
+    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+      float v[16], w[16];
+      tmem_ld16(tl + COL_DOS + s0, v);
+      tmem_ld16(tl + COL_DW + s0, w);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        a.b.dOS0[ch * CD + (int64_t)(s0 + e) * D + lane_row] = v[e];
+        a.b.dW[ch * CD + (int64_t)(s0 + e) * D + lane_row] = -w[e];
+      }
+    }
+  } else if (t == 0) {
+    set_error(a.hdr, GDN_DEVERR_TIMEOUT);
+    mbar_wait(bar, phase);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
+}
+
 template <int D, typename Tin>
 void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, void* mark_ctx,
                   cudaStream_t st) {
@@ -999,8 +1339,13 @@ void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, vo
   }
   mark(mark_ctx, 1);
   if (n_chunks > 0) {
-    ensure_smem_bwd(k_bwd_big<D, Tin>, bbig_smem<D>());
-    k_bwd_big<D, Tin><<<gc, NT, bbig_smem<D>(), st>>>(a);
+    if (boundary_on_tensor_cores(a.dm)) {
+      ensure_smem_bwd(k_bwd_big_tc, tcg::SMEM);
+      k_bwd_big_tc<<<gc, 256, tcg::SMEM, st>>>(a);
+    } else {
+      ensure_smem_bwd(k_bwd_big<D, Tin>, bbig_smem<D>());
+      k_bwd_big<D, Tin><<<gc, NT, bbig_smem<D>(), st>>>(a);
+    }
   }
   mark(mark_ctx, n_chunks > 0 ? 1 : 0);
   if (n_chunks > 0) {

@@ -291,7 +291,8 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
     }
     __syncthreads();
     for (int q = t; q < C * (D / 8); q += kPrepThreads) {  // Wd split: row s, 8 columns at a time
-      const int s = q / (D / 8), b0 = (q % (D / 8)) * 8;
+      int s, b0;
+      tc::kmajor_piece(q, D, s, b0);
       uint32_t hw[4], lw[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -895,7 +896,8 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
 
     // 1. operand images straight from global memory
     for (int q = t; q < C * (D / 8); q += 256) {  // K rows: 16-byte pieces
-      const int r = q / (D / 8), c0 = (q % (D / 8)) * 8;
+      int r, c0;
+      tc::kmajor_piece(q, D, r, c0);
       *reinterpret_cast<uint4*>(R0 + tc::kmajor_off(r, c0, D)) = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
     }
     for (int q = t; q < D * (C / 8); q += 256) {  // K^T and V^T: column e, 8 tokens at a time
@@ -964,7 +966,8 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     blocked_unit_lower_inverse<256>(A, Tm, Xs, C, CP);
     // 4. TK = T diag(beta e^G), TV = T diag(beta), split into bf16 images (lower triangle)
     for (int q = t; q < C * (C / 8); q += 256) {
-      const int i = q / (C / 8), r0 = (q % (C / 8)) * 8;
+      int i, r0;
+      tc::kmajor_piece(q, C, i, r0);
       float tk[8], tv[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {

@@ -28,6 +28,15 @@ __device__ __forceinline__ uint32_t kmajor_off(int r, int k, int K) {
   return (uint32_t)((r >> 3) * (K >> 3) * 128 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
 }
 
+// Work index q over an R x K tile split into 16-byte pieces (8 bf16), ordered so that 8
+// consecutive q fill one 128-byte core matrix (consecutive rows of an 8-row group): stores
+// by neighbouring threads then hit different shared-memory banks.
+__device__ __forceinline__ void kmajor_piece(int q, int K, int& r, int& k0) {
+  const int kp = K / 8;
+  r = (q / (8 * kp)) * 8 + (q & 7);
+  k0 = ((q >> 3) % kp) * 8;
+}
+
 // Shared-memory matrix descriptor (no swizzle): start address, leading-dimension byte
 // offset (between core matrices adjacent along K), stride-dimension byte offset (between
 // 8-row groups), descriptor version 1 at bits 46-47, layout type 0 (no swizzle).
