@@ -1321,13 +1321,342 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
   if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
 }
 
+// ============================================================  KB1 (tcgen05)  ===
+// Backward prep on tensor cores (bf16 inputs, d = 128, C = 64), one CTA of 256 threads per
+// chunk-head, every chunk zero-padded to C:
+//   Gram = K K^T, T = (I + A)^{-1} (SIMT), W = TK K, U^T = V^T TV^T    (as the forward pre-pass)
+//   P    = Gam (.) (Q K^T), lower with diagonal                       (exact bf16 inputs)
+//   Qt   = diag(e^G) Q - P W                                          (P, W split hi/lo)
+//   L    = dO^T Qt                                                    (dO, Qt split)
+// Outputs W, Ut, T, G, P, L and the reverse chain's images.  Transposed operands are built
+// from rows just written to global memory (L2-resident) instead of extra shared memory;
+// Qt uses this chunk-head's dO S0 slot as scratch (rewritten by the next kernel).
+namespace tcq {
+constexpr int D = 128, C = 64, QCP = C + 1;
+constexpr uint32_t TILE = C * D * 2;  // 16 KB
+constexpr uint32_t OFF_K = 0, OFF_KT = TILE, OFF_VT = 2 * TILE, OFF_TK = 3 * TILE, OFF_TV = 4 * TILE,
+                   OFF_A = 5 * TILE, OFF_T = OFF_A + C * QCP * 4, OFF_VEC = OFF_T + C * QCP * 4;
+constexpr size_t SMEM = OFF_VEC + 6 * C * 4 + 64;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_G = 0, COL_W = 0, COL_UT = 128, COL_P = 192, COL_QT = 256, COL_L = 384;
+}  // namespace tcq
+
+__global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
+  using namespace tcq;
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smq[];
+  unsigned char* Ki = smq + OFF_K;
+  unsigned char* KT = smq + OFF_KT;
+  unsigned char* VT = smq + OFF_VT;
+  unsigned char* TKh = smq + OFF_TK;
+  unsigned char* TKl = TKh + C * C * 2;
+  unsigned char* TVh = smq + OFF_TV;
+  unsigned char* TVl = TVh + C * C * 2;
+  float* A = reinterpret_cast<float*>(smq + OFF_A);
+  float* Tm = reinterpret_cast<float*>(smq + OFF_T);
+  float* gs = reinterpret_cast<float*>(smq + OFF_VEC);
+  float* Gs = gs + C;
+  float* bs = Gs + C;
+  float* eG = bs + C;
+  float* bk = eG + C;
+  float* dec = bk + C;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dec + C);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  float* Xs = reinterpret_cast<float*>(TKh);
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, warp = t >> 5;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const ChunkRec rec = a.chunks[c];
+  const int n = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t ch = c * dm.hv + h;
+  const int64_t CD = (int64_t)C * D;
+  const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
+  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + tok0 * kstride + (int64_t)hq * D;
+  const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(a.in.v) + tok0 * vstride + (int64_t)h * D;
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.in.q) + tok0 * kstride + (int64_t)hq * D;
+  unsigned char* img = reinterpret_cast<unsigned char*>(a.b.img + ch * (int64_t)prep_w_floats(C, D));
+  float* Qt = a.b.dOS0 + ch * CD;  // scratch
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+
+  // ---- 1. images of K (rows), K^T, V^T; g, beta (zero beyond the chunk's tokens)
+  for (int q = t; q < C * (D / 8); q += 256) {
+    int r, c0;
+    kmajor_piece(q, D, r, c0);
+    *reinterpret_cast<uint4*>(Ki + kmajor_off(r, c0, D)) =
+        r < n ? *reinterpret_cast<const uint4*>(kb + r * kstride + c0) : z4;
+  }
+  for (int q = t; q < D * (C / 8); q += 256) {
+    const int e = q % D, r0 = (q / D) * 8;
+    uint32_t kw[4], vw[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const int r = r0 + 2 * x;
+      const uint32_t k0 = r < n ? __bfloat16_as_ushort(kb[r * kstride + e]) : 0u;
+      const uint32_t k1 = r + 1 < n ? __bfloat16_as_ushort(kb[(r + 1) * kstride + e]) : 0u;
+      const uint32_t v0 = r < n ? __bfloat16_as_ushort(vb[r * vstride + e]) : 0u;
+      const uint32_t v1 = r + 1 < n ? __bfloat16_as_ushort(vb[(r + 1) * vstride + e]) : 0u;
+      kw[x] = k0 | (k1 << 16);
+      vw[x] = v0 | (v1 << 16);
+    }
+    *reinterpret_cast<uint4*>(KT + kmajor_off(e, r0, C)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+    *reinterpret_cast<uint4*>(VT + kmajor_off(e, r0, C)) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+  }
+  if (t < C) {
+    gs[t] = t < n ? a.in.g[(tok0 + t) * dm.hv + h] : 0.f;
+    bs[t] = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
+  }
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_proxy_async();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tb = *tslot;
+  uint32_t phase = 0;
+  bool ok = true;
+  auto wait_mma = [&]() {
+    const bool done = mbar_wait(bar, phase);
+    if (done) phase ^= 1u;
+    ok = __syncthreads_and(done) != 0;
+    fence_after_sync();
+  };
+  auto sync_for_mma = [&]() {
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+  };
+  const int lrow = (warp & 3) * 32 + (t & 31);  // TMEM lane of this thread
+  const int chalf = warp >> 2;                  // which half of the columns this warp reads
+
+  // ---- 2. Gram, G
+  if (t == 0) {
+    const uint32_t ka = smem_u32(Ki);
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_bf16(tb + COL_G, make_desc(ka + kk * 256, 128, (D / 8) * 128), make_desc(ka + kk * 256, 128, (D / 8) * 128),
+               idesc_bf16(128, C), kk > 0 ? 1u : 0u);
+    mma_commit(bar);
+    float run = gs[0];
+    Gs[0] = run;
+    for (int i = 1; i < C; ++i) {
+      run = __fadd_rn(run, gs[i]);
+      Gs[i] = run;
+    }
+  }
+  __syncthreads();
+  if (t < C) {
+    eG[t] = expf(Gs[t]);
+    bk[t] = __fmul_rn(bs[t], eG[t]);
+    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
+    a.b.G[ch * C + t] = Gs[t];
+  }
+  wait_mma();
+  if (ok && (warp & 3) < 2) {
+    const int i = lrow;
+    for (int s0 = chalf * 32; s0 < chalf * 32 + 32; s0 += 16) {
+      float v[16];
+      tmem_ld16(tmem_lane_addr(tb, warp, COL_G + s0), v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int s = s0 + e;
+        A[i * QCP + s] = (i > s) ? __fmul_rn(__fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s]))), v[e]) : 0.f;
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  // ---- 3. T, TK, TV; W = TK K and U^T = V^T TV^T
+  blocked_unit_lower_inverse<256>(A, Tm, Xs, C, QCP);
+  for (int o = t; o < C * C; o += 256) {
+    const int i = o / C, r = o % C;
+    a.b.T[ch * C * C + o] = (r <= i) ? Tm[i * QCP + r] : 0.f;
+  }
+  for (int q = t; q < C * (C / 8); q += 256) {
+    int i, r0;
+    kmajor_piece(q, C, i, r0);
+    float tk[8], tv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int r = r0 + e;
+      const float x = (r <= i) ? Tm[i * QCP + r] : 0.f;
+      tk[e] = __fmul_rn(x, bk[r]);
+      tv[e] = __fmul_rn(x, bs[r]);
+    }
+    const uint32_t off = kmajor_off(i, r0, C);
+    split8(TKh, TKl, off, tk);
+    split8(TVh, TVl, off, tv);
+  }
+  sync_for_mma();
+  if (ok && t == 0) {
+    fence_after_sync();
+    const uint32_t sbo = (C / 8) * 128;
+    for (int term = 0; term < 2; ++term) {
+      const uint32_t ta = smem_u32(term == 0 ? TKh : TKl);
+      const uint32_t tv = smem_u32(term == 0 ? TVh : TVl);
+      for (int kk = 0; kk < C / 16; ++kk) {
+        mma_bf16(tb + COL_W, make_desc(ta + kk * 256, 128, sbo), make_desc(smem_u32(KT) + kk * 256, 128, sbo),
+                 idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
+        mma_bf16(tb + COL_UT, make_desc(smem_u32(VT) + kk * 256, 128, sbo), make_desc(tv + kk * 256, 128, sbo),
+                 idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+      }
+    }
+    mma_commit(bar);
+  }
+  if (ok) wait_mma();
+  if (ok) {
+    if ((warp & 3) < 2) {  // W rows (not decayed)
+      const int i = lrow;
+      for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem_lane_addr(tb, warp, COL_W + c0), v);
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(a.b.W + ch * CD + (int64_t)i * D + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      }
+    }
+    {  // Ut[i][e] = U^T[e][i]
+      const int e = lrow;
+      for (int i0 = chalf * 32; i0 < chalf * 32 + 32; i0 += 16) {
+        float v[16];
+        tmem_ld16(tmem_lane_addr(tb, warp, COL_UT + i0), v);
+#pragma unroll
+        for (int x = 0; x < 16; ++x) a.b.Ut[ch * CD + (int64_t)(i0 + x) * D + e] = v[x];
+      }
+    }
+  }
+  // ---- 4. P = Gam (.) (Q K^T); Q image into the (dead) A region
+  unsigned char* Qi = smq + OFF_A;
+  for (int q = t; q < C * (D / 8); q += 256) {
+    int r, c0;
+    kmajor_piece(q, D, r, c0);
+    *reinterpret_cast<uint4*>(Qi + kmajor_off(r, c0, D)) =
+        r < n ? *reinterpret_cast<const uint4*>(qb + r * kstride + c0) : z4;
+  }
+  for (int q = t; q < (int)(TILE / 16); q += 256)  // K rows image for the reverse chain
+    reinterpret_cast<uint4*>(img)[q] = reinterpret_cast<const uint4*>(Ki)[q];
+  sync_for_mma();
+  if (ok && t == 0) {
+    fence_after_sync();
+    const uint32_t qa = smem_u32(Qi), ka = smem_u32(Ki), sbo = (D / 8) * 128;
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_bf16(tb + COL_P, make_desc(qa + kk * 256, 128, sbo), make_desc(ka + kk * 256, 128, sbo),
+               idesc_bf16(128, C), kk > 0 ? 1u : 0u);
+    mma_commit(bar);
+  }
+  if (ok) wait_mma();
+  if (ok && (warp & 3) < 2) {
+    const int i = lrow;
+    for (int s0 = chalf * 32; s0 < chalf * 32 + 32; s0 += 16) {
+      float v[16];
+      tmem_ld16(tmem_lane_addr(tb, warp, COL_P + s0), v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int s = s0 + e;
+        a.b.P[ch * C * C + i * C + s] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v[e]) : 0.f;
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();  // W and P rows are in global memory for this CTA
+  // ---- 5. Qt = diag(e^G) Q - P W: A = P (rows i), B = W^T (rows c)
+  if (ok) {
+    build_split<true, D, C>(KT, VT, a.b.W + ch * CD, D, C);  // W^T hi | lo over the dead K^T, V^T
+    build_split<false, C, C>(TKh, TKl, a.b.P + ch * C * C, C, C);
+    sync_for_mma();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_QT, smem_u32(TKh), smem_u32(TKl), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
+      mma_commit(bar);
+    }
+    for (int q = t; q < (int)(2 * TILE / 16); q += 256)  // W^T images for the reverse chain
+      reinterpret_cast<uint4*>(img + TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
+    wait_mma();
+  }
+  if (ok && (warp & 3) < 2) {
+    const int i = lrow;
+    for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem_lane_addr(tb, warp, COL_QT + c0), v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float qv = i < n ? __bfloat162float(qb[i * kstride + c0 + e]) : 0.f;
+        Qt[(int64_t)i * D + c0 + e] = __fsub_rn(__fmul_rn(eG[i], qv), v[e]);
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  // ---- 6. L = dO^T Qt: A = dO^T (rows p, K = i), B = Qt^T (rows q, K = i)
+  if (ok) {
+    build_split<true, D, C>(smq + OFF_A, smq + OFF_A + TILE, Qt, D, C);
+    {
+      float v[4][8];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int i = k0 + e;
+          float x = 0.f;
+          if (i < n) {
+            const int64_t o = ((tok0 + i) * dm.hv + h) * D + r;
+            x = dm.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.dO)[o])
+                            : static_cast<const float*>(a.dO)[o];
+          }
+          v[it][e] = x;
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
+        split8(Ki, Ki + TILE, kmajor_off(r, k0, C), v[it]);  // over the dead K and K^T regions
+      }
+    }
+    sync_for_mma();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_L, smem_u32(Ki), smem_u32(Ki) + TILE, smem_u32(smq + OFF_A), smem_u32(smq + OFF_A) + TILE, C,
+                idesc_bf16(128, D), 3);
+      mma_commit(bar);
+    }
+    wait_mma();
+  }
+  if (ok) {
+    const int p = lrow;
+    for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem_lane_addr(tb, warp, COL_L + c0), v);
+#pragma unroll
+      for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(a.b.L + ch * (int64_t)D * D + (int64_t)p * D + c0 + e) =
+            make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+    }
+  } else if (t == 0) {
+    set_error(a.hdr, GDN_DEVERR_TIMEOUT);
+    mbar_wait(bar, phase);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
+}
+
 template <int D, typename Tin>
 void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, void* mark_ctx,
                   cudaStream_t st) {
   const dim3 gc((unsigned)n_chunks, a.dm.hv);
   if (n_chunks > 0) {
-    ensure_smem_bwd(k_bwd_prep<D, Tin>, bprep_smem<D>());
-    k_bwd_prep<D, Tin><<<gc, NT, bprep_smem<D>(), st>>>(a);
+    if (boundary_on_tensor_cores(a.dm)) {
+      ensure_smem_bwd(k_bwd_prep_tc, tcq::SMEM);
+      k_bwd_prep_tc<<<gc, 256, tcq::SMEM, st>>>(a);
+    } else {
+      ensure_smem_bwd(k_bwd_prep<D, Tin>, bprep_smem<D>());
+      k_bwd_prep<D, Tin><<<gc, NT, bprep_smem<D>(), st>>>(a);
+    }
   }
   mark(mark_ctx, n_chunks > 0 ? 1 : 0);
   if (boundary_on_tensor_cores(a.dm)) {
