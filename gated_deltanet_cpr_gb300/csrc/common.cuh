@@ -85,51 +85,67 @@ __device__ __forceinline__ float dot_canon(const float* __restrict__ a, const fl
 }
 
 // ---------------------------------------------------------------- token step ----
+// Packed fp32 pairs (Blackwell f32x2 instructions): each lane of the pair is rounded exactly
+// like the scalar __fmaf_rn / __fmul_rn, so these are the same arithmetic in half the
+// instructions.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)),
+        "l"(*reinterpret_cast<const uint64_t*>(&c)));
+  return *reinterpret_cast<const float2*>(&d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<const float2*>(&d);
+}
+
 // One gated delta-rule step on row i of the state, held by a pair of adjacent lanes
 // (half = lane & 1).  The pair splits the D columns into float4 groups: register group m
 // holds columns [8m + 4*half, 8m + 4*half + 4).  Order of operations (the recurrence's
 // own order):
 //     S <- a S;   p = S k;   u = beta (v_i - p);   S <- S + u k^T;   o_i = S q
-// Each dot is four partial sums over the lane's columns in ascending m, combined as
-// (p0 + p1) + (p2 + p3), then added to the partner lane's partial with one xor-shuffle;
-// fp32 addition is commutative, so both lanes hold identical bits.  k and q are fp32
-// copies in shared memory (exact widenings of the inputs).  All 32 lanes of the warp must
-// call this together.
+// Each dot is four partial sums over the lane's columns in ascending m (partial e takes
+// component e of every group), combined as (p0 + p1) + (p2 + p3), then added to the
+// partner lane's partial with one xor-shuffle; fp32 addition is commutative, so both lanes
+// hold identical bits.  k and q are fp32 copies in shared memory (exact widenings of the
+// inputs).  All 32 lanes of the warp must call this together.
 template <int D>
 __device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __restrict__ k_sh,
                                             const float* __restrict__ q_sh, float a, float beta,
                                             float v_i, int half) {
-  float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
+  const float2 a2 = make_float2(a, a);
+  float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int m = 0; m < D / 8; ++m) {
     const float4 kk = *reinterpret_cast<const float4*>(k_sh + 8 * m + 4 * half);
-    S[m].x = __fmul_rn(a, S[m].x);
-    S[m].y = __fmul_rn(a, S[m].y);
-    S[m].z = __fmul_rn(a, S[m].z);
-    S[m].w = __fmul_rn(a, S[m].w);
-    p0 = __fmaf_rn(S[m].x, kk.x, p0);
-    p1 = __fmaf_rn(S[m].y, kk.y, p1);
-    p2 = __fmaf_rn(S[m].z, kk.z, p2);
-    p3 = __fmaf_rn(S[m].w, kk.w, p3);
+    float2 s01 = mul2(a2, make_float2(S[m].x, S[m].y));
+    float2 s23 = mul2(a2, make_float2(S[m].z, S[m].w));
+    p01 = fma2(s01, make_float2(kk.x, kk.y), p01);
+    p23 = fma2(s23, make_float2(kk.z, kk.w), p23);
+    S[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
   }
-  float part = __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+  float part = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
   const float p = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
   const float u = __fmul_rn(beta, __fsub_rn(v_i, p));
-  p0 = p1 = p2 = p3 = 0.f;
+  const float2 u2 = make_float2(u, u);
+  p01 = make_float2(0.f, 0.f);
+  p23 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int m = 0; m < D / 8; ++m) {
     const float4 kk = *reinterpret_cast<const float4*>(k_sh + 8 * m + 4 * half);
     const float4 qq = *reinterpret_cast<const float4*>(q_sh + 8 * m + 4 * half);
-    S[m].x = __fmaf_rn(u, kk.x, S[m].x);
-    S[m].y = __fmaf_rn(u, kk.y, S[m].y);
-    S[m].z = __fmaf_rn(u, kk.z, S[m].z);
-    S[m].w = __fmaf_rn(u, kk.w, S[m].w);
-    p0 = __fmaf_rn(S[m].x, qq.x, p0);
-    p1 = __fmaf_rn(S[m].y, qq.y, p1);
-    p2 = __fmaf_rn(S[m].z, qq.z, p2);
-    p3 = __fmaf_rn(S[m].w, qq.w, p3);
+    const float2 s01 = fma2(u2, make_float2(kk.x, kk.y), make_float2(S[m].x, S[m].y));
+    const float2 s23 = fma2(u2, make_float2(kk.z, kk.w), make_float2(S[m].z, S[m].w));
+    p01 = fma2(s01, make_float2(qq.x, qq.y), p01);
+    p23 = fma2(s23, make_float2(qq.z, qq.w), p23);
+    S[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
   }
-  part = __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+  part = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
   return __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
 }
 
