@@ -56,17 +56,10 @@ void ensure_smem_bwd(F* fn, size_t bytes) {
 template <int D, typename T>
 __device__ __forceinline__ void load_rows(float* dst, int ld, const T* src, int64_t stride, int n,
                                           int C) {
-  for (int idx = threadIdx.x; idx < C * (D / 8); idx += NT) {
-    const int r = idx / (D / 8), c8 = idx % (D / 8);
-    float tmp[8];
-    if (r < n) {
-      load8(src + r * stride + 8 * c8, tmp);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) tmp[e] = 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dst[r * ld + 8 * c8 + e] = tmp[e];
+  for (int idx = threadIdx.x; idx < C * (D / 4); idx += NT) {
+    const int r = idx / (D / 4), c4 = idx % (D / 4);
+    const float4 x = (r < n) ? load4(src + r * stride + 4 * c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(dst + r * ld + 4 * c4) = x;
   }
 }
 
@@ -124,7 +117,11 @@ __device__ __forceinline__ void gemm(int M, int N, int K, const float* __restric
 #pragma unroll
         for (int c = 0; c < TN; ++c) epi(mt + r * ms, nt + c * ns, acc[r][c]);
     } else {
-      const int m0 = (tile / ntn) * TM, n0 = (tile % ntn) * TN;
+      // this thread's TN columns: TN/4 groups of 4, group g starting at g * (N / (TN/4)) + 4 * nt
+      const int m0 = (tile / ntn) * TM, nt = tile % ntn;
+      constexpr int NG = TN / 4;
+      const int gstride = N / NG;
+      auto col = [&](int c) { return (c / 4) * gstride + 4 * nt + (c % 4); };
       for (int k = 0; k < K; ++k) {
         float av[TM], bv[TN];
         if constexpr (AT) {
@@ -139,7 +136,7 @@ __device__ __forceinline__ void gemm(int M, int N, int K, const float* __restric
         }
 #pragma unroll
         for (int c = 0; c < TN; c += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(B + k * ldb + n0 + c);
+          const float4 x = *reinterpret_cast<const float4*>(B + k * ldb + col(c));
           bv[c] = x.x; bv[c + 1] = x.y; bv[c + 2] = x.z; bv[c + 3] = x.w;
         }
 #pragma unroll
@@ -150,7 +147,7 @@ __device__ __forceinline__ void gemm(int M, int N, int K, const float* __restric
 #pragma unroll
       for (int r = 0; r < TM; ++r)
 #pragma unroll
-        for (int c = 0; c < TN; ++c) epi(m0 + r, n0 + c, acc[r][c]);
+        for (int c = 0; c < TN; ++c) epi(m0 + r, col(c), acc[r][c]);
     }
   }
 }

@@ -184,15 +184,10 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
   const Tin* vin = static_cast<const Tin*>(in.v);
 
   // 1. chunk inputs -> fp32 shared memory
-  for (int idx = t; idx < C * (D / 8); idx += kPrepThreads) {
-    const int r = idx / (D / 8), c8 = idx % (D / 8);
-    float tmp[8];
-    load8(kin + ((tok0 + r) * dm.hqk + hq) * D + 8 * c8, tmp);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) Ks[r * DP + 8 * c8 + e] = tmp[e];
-    load8(vin + ((tok0 + r) * dm.hv + h) * D + 8 * c8, tmp);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) Vs[r * DP + 8 * c8 + e] = tmp[e];
+  for (int idx = t; idx < C * (D / 4); idx += kPrepThreads) {
+    const int r = idx / (D / 4), c4 = idx % (D / 4);
+    *reinterpret_cast<float4*>(Ks + r * DP + 4 * c4) = load4(kin + ((tok0 + r) * dm.hqk + hq) * D + 4 * c4);
+    *reinterpret_cast<float4*>(Vs + r * DP + 4 * c4) = load4(vin + ((tok0 + r) * dm.hv + h) * D + 4 * c4);
   }
   if (t < C) {
     gs[t] = in.g[(tok0 + t) * dm.hv + h];
@@ -1103,18 +1098,11 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const Tin* kin = static_cast<const Tin*>(in.k);
   const Tin* vin = static_cast<const Tin*>(in.v);
 
-  for (int idx = t; idx < len * (D / 8); idx += 2 * D) {
-    const int r = idx / (D / 8), c8 = idx % (D / 8);
-    float tmp[8];
-    load8(kin + ((tok0 + r) * dm.hqk + hq) * D + 8 * c8, tmp);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) ks[r * D + 8 * c8 + e] = tmp[e];
-    load8(qin + ((tok0 + r) * dm.hqk + hq) * D + 8 * c8, tmp);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) qs[r * D + 8 * c8 + e] = tmp[e];
-    load8(vin + ((tok0 + r) * dm.hv + h) * D + 8 * c8, tmp);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) vs[r * D + 8 * c8 + e] = tmp[e];
+  for (int idx = t; idx < len * (D / 4); idx += 2 * D) {
+    const int r = idx / (D / 4), c4 = idx % (D / 4);
+    *reinterpret_cast<float4*>(ks + r * D + 4 * c4) = load4(kin + ((tok0 + r) * dm.hqk + hq) * D + 4 * c4);
+    *reinterpret_cast<float4*>(qs + r * D + 4 * c4) = load4(qin + ((tok0 + r) * dm.hqk + hq) * D + 4 * c4);
+    *reinterpret_cast<float4*>(vs + r * D + 4 * c4) = load4(vin + ((tok0 + r) * dm.hv + h) * D + 4 * c4);
   }
   for (int r = t; r < len; r += 2 * D) {
     as[r] = expf(in.g[(tok0 + r) * dm.hv + h]);
