@@ -1026,56 +1026,70 @@ __device__ __forceinline__ void split8(unsigned char* hi, unsigned char* lo, uin
 
 // R x K image pair (hi at `hi`, lo at `lo`) of a row-major fp32 matrix src[r * ld + k]
 // (rows >= nvalid are zero); TRANS takes src[k * ld + r] instead (columns >= nvalid zero).
-// All loads of the build are issued before any is used.
+// SplitTile::load fetches the pieces of thread `tid` (of NTH) into registers and store
+// writes them, so that the loads of several builds can be in flight before the first store.
+template <bool TRANS, int R, int K, int NTH = 256>
+struct SplitTile {
+  static constexpr int ITER = R * (K / 8) / NTH;
+  static_assert(ITER * NTH == R * (K / 8), "tile must split evenly over the threads");
+  float v[ITER][8];
+  __device__ __forceinline__ static void piece(int q, int& r, int& k0) {
+    if (TRANS) {
+      r = q % R;
+      k0 = (q / R) * 8;
+    } else {
+      tc::kmajor_piece(q, K, r, k0);
+    }
+  }
+  __device__ __forceinline__ void load(const float* __restrict__ src, int ld, int nvalid, int tid) {
+#pragma unroll
+    for (int it = 0; it < ITER; ++it) {
+      int r, k0;
+      piece(tid + it * NTH, r, k0);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (TRANS)
+          v[it][e] = (k0 + e < nvalid) ? src[(int64_t)(k0 + e) * ld + r] : 0.f;
+        else
+          v[it][e] = (r < nvalid) ? src[(int64_t)r * ld + k0 + e] : 0.f;
+      }
+    }
+  }
+  __device__ __forceinline__ void store(unsigned char* hi, unsigned char* lo, int tid) const {
+#pragma unroll
+    for (int it = 0; it < ITER; ++it) {
+      int r, k0;
+      piece(tid + it * NTH, r, k0);
+      split8(hi, lo, tc::kmajor_off(r, k0, K), v[it]);
+    }
+  }
+  __device__ __forceinline__ void load(const float* __restrict__ src, int ld, int nvalid) {
+    load(src, ld, nvalid, (int)threadIdx.x);
+  }
+  __device__ __forceinline__ void store(unsigned char* hi, unsigned char* lo) const {
+    store(hi, lo, (int)threadIdx.x);
+  }
+};
+
 template <bool TRANS, int R, int K>
 __device__ __forceinline__ void build_split(unsigned char* hi, unsigned char* lo, const float* __restrict__ src,
                                             int ld, int nvalid) {
-  constexpr int ITER = R * (K / 8) / 256;
-  static_assert(ITER * 256 == R * (K / 8), "tile must split evenly over 256 threads");
-  float v[ITER][8];
-#pragma unroll
-  for (int it = 0; it < ITER; ++it) {
-    const int q = threadIdx.x + it * 256;
-    int r, k0;
-    if (TRANS) {
-      r = q % R;
-      k0 = (q / R) * 8;
-    } else {
-      tc::kmajor_piece(q, K, r, k0);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      if (TRANS)
-        v[it][e] = (k0 + e < nvalid) ? src[(int64_t)(k0 + e) * ld + r] : 0.f;
-      else
-        v[it][e] = (r < nvalid) ? src[(int64_t)r * ld + k0 + e] : 0.f;
-    }
-  }
-#pragma unroll
-  for (int it = 0; it < ITER; ++it) {
-    const int q = threadIdx.x + it * 256;
-    int r, k0;
-    if (TRANS) {
-      r = q % R;
-      k0 = (q / R) * 8;
-    } else {
-      tc::kmajor_piece(q, K, r, k0);
-    }
-    split8(hi, lo, tc::kmajor_off(r, k0, K), v[it]);
-  }
+  SplitTile<TRANS, R, K> tile;
+  tile.load(src, ld, nvalid);
+  tile.store(hi, lo);
 }
 
 // D = A B^T over K with split operands: terms = 3 gives A_hi B_hi + A_hi B_lo + A_lo B_hi;
-// terms = 2 (B exact, blo ignored) gives A_hi B + A_lo B.
+// terms = 2 (B exact, blo ignored) gives A_hi B + A_lo B; `accumulate` adds onto D.
 __device__ __forceinline__ void mma_terms(uint32_t d, uint32_t ahi, uint32_t alo, uint32_t bhi, uint32_t blo,
-                                          int K, uint32_t idesc, int terms) {
+                                          int K, uint32_t idesc, int terms, bool accumulate = false) {
   const uint32_t sbo = (uint32_t)(K / 8) * 128;
   for (int term = 0; term < terms; ++term) {
     const uint32_t aa = (terms == 3 ? term == 2 : term == 1) ? alo : ahi;
     const uint32_t bb = (terms == 3 && term == 1) ? blo : bhi;
     for (int kk = 0; kk < K / 16; ++kk)
       tc::mma_bf16(d, tc::make_desc(aa + kk * 256, 128, sbo), tc::make_desc(bb + kk * 256, 128, sbo), idesc,
-                   (term > 0 || kk > 0) ? 1u : 0u);
+                   (accumulate || term > 0 || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -1642,6 +1656,458 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
 }
 
+// ============================================================  KB4 (tcgen05)  ===
+// Backward gradients on tensor cores (bf16 inputs, d = 128, C = 64), one CTA of 256 threads
+// per chunk-head; the arithmetic of k_bwd_grad with its products as MMAs:
+//   phase 1  Pm = Gam (.) (dO U^T) (lower with diagonal), QK = Q K^T, A' = Gam (.) (K K^T)
+//   phase 2  dQ = diag(e^G) dO S0 + Pm K,  dK <- Pm^T Q,  X = T^T dU,  Y = T^T dW
+//   phase 3  dA = -(Y W^T + X Ut^T) (strictly lower), dAm = dA beta_i Gam
+//   phase 4  dK += dAm K + dAm^T K, then + diag(dec) U dS_end + diag(beta e^G) Y
+// with dg, dbeta from the same scalar terms.  Warps 0, 1, 4, 5 own TMEM lanes 0..63 (the
+// chunk rows) and read the accumulators out, one column half each; meanwhile warps 2, 3, 6, 7
+// build the next phase's operand images.  Every build and readout issues its global loads
+// before its first store.  K^T and Q^T stay resident from phase 1 on.  64-row operands use
+// 128-row MMAs whose extra rows read neighbouring arena bytes and are never read back.
+namespace tcd {
+constexpr int D = 128, C = 64, MP = C + 1;
+constexpr uint32_t KB = 1024;
+constexpr uint32_t ARENA = 144 * KB;
+// arena byte offsets; an image's lo half follows its hi half (8 KB for 64 x 64, 16 KB for
+// 64 x 128 and 128 x 64)
+constexpr uint32_t P1_DO = 0, P1_U = 32 * KB, P1_Q = 64 * KB, P1_K = 80 * KB;  // + overread to 112
+constexpr uint32_t QT = 112 * KB, KT = 128 * KB;
+constexpr uint32_t P2_PM = 0, P2_PMT = 16 * KB, P2_TT = 32 * KB, P2_DU = 48 * KB, P2_DW = 80 * KB;
+constexpr uint32_t P3_Y = 0, P3_X = 32 * KB, P3_W = 64 * KB, P3_UT = 96 * KB;
+constexpr uint32_t P4_AM = 0, P4_AMT = 16 * KB;
+constexpr uint32_t MAT = C * MP * 4;
+constexpr size_t SMEM = ARENA + 3 * (size_t)MAT + 16 * C * 4 + 64;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_PM = 0, COL_QK = 64, COL_AP = 128, COL_DQ = 0, COL_DK = 128, COL_X = 256,
+                   COL_Y = 384, COL_DA = 0;
+}  // namespace tcd
+
+__device__ __forceinline__ void unpack8(const uint4 u, float* o) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// dst = transpose of a shared-memory image: src is Ks rows x R columns (K-major, K = R),
+// dst is R rows x Ks columns (K = Ks); 256 threads.
+__device__ __forceinline__ void transpose_image(unsigned char* dst, const unsigned char* src, int R, int Ks) {
+  for (int q = threadIdx.x; q < R * (Ks / 8); q += 256) {
+    const int e = q % R, r0 = (q / R) * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t a0 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x, e, R));
+      const uint32_t a1 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x + 1, e, R));
+      w[x] = a0 | (a1 << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + tc::kmajor_off(e, r0, Ks)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
+  using namespace tcd;
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smd[];
+  unsigned char* ar = smd;
+  float* PM = reinterpret_cast<float*>(smd + ARENA);  // Pm, then dAm
+  float* AQ = PM + C * MP;                            // Q K^T, then dA
+  float* AP = AQ + C * MP;                            // A' = Gam (.) K K^T (strictly lower)
+  float* Gs = AP + C * MP;
+  float* eG = Gs + C;
+  float* dec = eG + C;
+  float* bs = dec + C;
+  float* dGa = bs + C;       // [2][C] partial sums, one per column half
+  float* dba = dGa + 2 * C;  // [2][C]
+  float* kY = dba + 2 * C;   // [2][C]
+  float* cs = kY + 2 * C;    // [2][C]
+  float* dGb = cs + 2 * C;
+  float* dGe = dGb + C;
+  float* dbc = dGe + C;
+  float* dgv = dbc + C;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dgv + C);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, warp = t >> 5;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const ChunkRec rec = a.chunks[c];
+  const int n = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t ch = c * dm.hv + h;
+  const int64_t CD = (int64_t)C * D;
+  const int64_t kstride = (int64_t)dm.hqk * D;
+  const int64_t vstride = (int64_t)dm.hv * D;
+  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + tok0 * kstride + (int64_t)hq * D;
+  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.in.q) + tok0 * kstride + (int64_t)hq * D;
+  const int64_t orow0 = tok0 * vstride + (int64_t)h * D;  // token 0 of this head in [T, Hv, D]
+  const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(a.in.v) + orow0;
+  const bool rowlane = (warp & 3) < 2;
+  const int row = (warp & 3) * 32 + (t & 31);
+  const int half = warp >> 2;
+  const int helper = half * 64 + ((warp & 3) - 2) * 32 + (t & 31);  // 0..127 on warps 2, 3, 6, 7
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+
+  // ---- phase 1 operands: dO (split), U (split), Q rows, K rows
+  {
+    float g0 = 0.f, b0 = 0.f;
+    if (t < C) {
+      g0 = a.b.G[ch * C + t];
+      b0 = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
+    }
+    float vo[4][8];
+    uint4 qr[4], kr[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      int r, k0;
+      kmajor_piece(t + it * 256, D, r, k0);
+      if (r < n) {
+        const int64_t o = orow0 + (int64_t)r * vstride + k0;
+        if (dm.out_bf16)
+          load8(static_cast<const __nv_bfloat16*>(a.dO) + o, vo[it]);
+        else
+          load8(static_cast<const float*>(a.dO) + o, vo[it]);
+        qr[it] = *reinterpret_cast<const uint4*>(qb + r * kstride + k0);
+        kr[it] = *reinterpret_cast<const uint4*>(kb + r * kstride + k0);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vo[it][e] = 0.f;
+        qr[it] = zero4;
+        kr[it] = zero4;
+      }
+    }
+    SplitTile<false, C, D> u;
+    u.load(a.b.U + ch * CD, D, C);
+    if (t < C) {
+      Gs[t] = g0;
+      bs[t] = b0;
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      int r, k0;
+      kmajor_piece(t + it * 256, D, r, k0);
+      const uint32_t off = kmajor_off(r, k0, D);
+      split8(ar + P1_DO, ar + P1_DO + 16 * KB, off, vo[it]);
+      *reinterpret_cast<uint4*>(ar + P1_Q + off) = qr[it];
+      *reinterpret_cast<uint4*>(ar + P1_K + off) = kr[it];
+    }
+    u.store(ar + P1_U, ar + P1_U + 16 * KB);
+  }
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_proxy_async();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tb = *tslot;
+  const uint32_t tl = tmem_lane_addr(tb, warp, 0);
+  const uint32_t sa = smem_u32(ar);
+  uint32_t phase = 0;
+  bool ok = true;
+  auto wait_mma = [&]() {
+    const bool done = mbar_wait(bar, phase);
+    if (done) phase ^= 1u;
+    ok = __syncthreads_and(done) != 0;
+    fence_after_sync();
+  };
+  auto sync_for_mma = [&]() {
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+  };
+  if (t == 0) {
+    mma_terms(tb + COL_PM, sa + P1_DO, sa + P1_DO + 16 * KB, sa + P1_U, sa + P1_U + 16 * KB, D,
+              idesc_bf16(128, C), 3);
+    mma_terms(tb + COL_QK, sa + P1_Q, sa + P1_Q, sa + P1_K, sa + P1_K, D, idesc_bf16(128, C), 1);
+    mma_terms(tb + COL_AP, sa + P1_K, sa + P1_K, sa + P1_K, sa + P1_K, D, idesc_bf16(128, C), 1);
+    mma_commit(bar);
+  }
+  // while the products run: K^T and Q^T images from the row images (reads of the operands only)
+  transpose_image(ar + QT, ar + P1_Q, D, C);
+  transpose_image(ar + KT, ar + P1_K, D, C);
+  if (t < C) {
+    eG[t] = expf(Gs[t]);
+    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
+  }
+  wait_mma();
+  // ---- phase 1 readout (row warps) || phase 2 operands T^T, dU^T, dW^T (other warps)
+  if (ok) {
+    if (rowlane) {
+      const int i = row;
+      for (int s0 = half * 32; s0 < half * 32 + 32; s0 += 16) {
+        float pm[16], qk[16], ap[16];
+        tmem_ld16(tl + COL_PM + s0, pm);
+        tmem_ld16(tl + COL_QK + s0, qk);
+        tmem_ld16(tl + COL_AP + s0, ap);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int s = s0 + e;
+          const float gam = expf(__fsub_rn(Gs[i], Gs[s]));
+          PM[i * MP + s] = (i >= s) ? __fmul_rn(gam, pm[e]) : 0.f;
+          AQ[i * MP + s] = (i > s) ? qk[e] : 0.f;
+          AP[i * MP + s] = (i > s) ? __fmul_rn(gam, ap[e]) : 0.f;
+        }
+      }
+    } else {
+      {
+        SplitTile<true, C, C, 128> tt;
+        SplitTile<true, D, C, 128> du;
+        tt.load(a.b.T + ch * C * C, C, C, helper);
+        du.load(a.b.dU + ch * CD, D, C, helper);
+        tt.store(ar + P2_TT, ar + P2_TT + 8 * KB, helper);
+        du.store(ar + P2_DU, ar + P2_DU + 16 * KB, helper);
+      }
+      SplitTile<true, D, C, 128> dw;
+      dw.load(a.b.dW + ch * CD, D, C, helper);
+      dw.store(ar + P2_DW, ar + P2_DW + 16 * KB, helper);
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  // ---- phase 2: dQ, dK <- Pm^T Q, X, Y
+  if (ok) {
+    build_split<false, C, C>(ar + P2_PM, ar + P2_PM + 8 * KB, PM, MP, C);
+    build_split<true, C, C>(ar + P2_PMT, ar + P2_PMT + 8 * KB, PM, MP, C);
+    sync_for_mma();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_DQ, sa + P2_PM, sa + P2_PM + 8 * KB, sa + KT, sa + KT, C, idesc_bf16(128, D), 2);
+      mma_terms(tb + COL_DK, sa + P2_PMT, sa + P2_PMT + 8 * KB, sa + QT, sa + QT, C, idesc_bf16(128, D), 2);
+      mma_terms(tb + COL_X, sa + P2_TT, sa + P2_TT + 8 * KB, sa + P2_DU, sa + P2_DU + 16 * KB, C,
+                idesc_bf16(128, D), 3);
+      mma_terms(tb + COL_Y, sa + P2_TT, sa + P2_TT + 8 * KB, sa + P2_DW, sa + P2_DW + 16 * KB, C,
+                idesc_bf16(128, D), 3);
+      mma_commit(bar);
+    }
+  }
+  if (t < C) {  // dG from P while the products run: sum_{s<t} Pm QK - sum_{i>t} Pm QK
+    float rw = 0.f, cl = 0.f;
+    for (int s2 = 0; s2 < t; ++s2) rw = __fmaf_rn(PM[t * MP + s2], AQ[t * MP + s2], rw);
+    for (int i2 = t + 1; i2 < C; ++i2) cl = __fmaf_rn(PM[i2 * MP + t], AQ[i2 * MP + t], cl);
+    dGb[t] = __fsub_rn(rw, cl);
+  }
+  if (ok) wait_mma();
+  // ---- phase 2 readout (row warps) || phase 3 operands W, Ut (other warps)
+  if (ok) {
+    if (rowlane) {
+      const int i = row;
+      const bool live = i < n;
+      const float egi = eG[i], bi = bs[i];
+      const float* dos_row = a.b.dOS0 + ch * CD + (int64_t)i * D;
+      float pga = 0.f, pba = 0.f, pky = 0.f;
+      for (int cb = half * 64; cb < half * 64 + 64; cb += 32) {
+        float4 ds4[8];
+        uint4 qv[4], kv[4], vv[4];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) ds4[x] = *reinterpret_cast<const float4*>(dos_row + cb + 4 * x);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          qv[x] = live ? *reinterpret_cast<const uint4*>(qb + i * kstride + cb + 8 * x) : zero4;
+          kv[x] = live ? *reinterpret_cast<const uint4*>(kb + i * kstride + cb + 8 * x) : zero4;
+          vv[x] = live ? *reinterpret_cast<const uint4*>(vb + i * vstride + cb + 8 * x) : zero4;
+        }
+#pragma unroll
+        for (int sub = 0; sub < 2; ++sub) {
+          const int c0 = cb + 16 * sub;
+          float dq[16], xr[16], yr[16], qf[16], kf[16], vf[16], ds[16];
+          tmem_ld16(tl + COL_DQ + c0, dq);
+          tmem_ld16(tl + COL_X + c0, xr);
+          tmem_ld16(tl + COL_Y + c0, yr);
+          unpack8(qv[2 * sub], qf);
+          unpack8(qv[2 * sub + 1], qf + 8);
+          unpack8(kv[2 * sub], kf);
+          unpack8(kv[2 * sub + 1], kf + 8);
+          unpack8(vv[2 * sub], vf);
+          unpack8(vv[2 * sub + 1], vf + 8);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            ds[4 * x] = ds4[4 * sub + x].x;
+            ds[4 * x + 1] = ds4[4 * sub + x].y;
+            ds[4 * x + 2] = ds4[4 * sub + x].z;
+            ds[4 * x + 3] = ds4[4 * sub + x].w;
+          }
+          float dqo[16], dvo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            dqo[e] = __fmaf_rn(egi, ds[e], dq[e]);
+            dvo[e] = __fmul_rn(bi, xr[e]);
+            pga = __fmaf_rn(ds[e], qf[e], pga);
+            pba = __fmaf_rn(vf[e], xr[e], pba);
+            pky = __fmaf_rn(kf[e], yr[e], pky);
+          }
+          if (live) {
+            float4* dqp = reinterpret_cast<float4*>(a.b.dq_part + orow0 + (int64_t)i * vstride + c0);
+            float4* dvp = reinterpret_cast<float4*>(a.dv + orow0 + (int64_t)i * vstride + c0);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              dqp[x] = make_float4(dqo[4 * x], dqo[4 * x + 1], dqo[4 * x + 2], dqo[4 * x + 3]);
+              dvp[x] = make_float4(dvo[4 * x], dvo[4 * x + 1], dvo[4 * x + 2], dvo[4 * x + 3]);
+            }
+          }
+          split8(ar + P3_X, ar + P3_X + 16 * KB, kmajor_off(i, c0, D), xr);
+          split8(ar + P3_X, ar + P3_X + 16 * KB, kmajor_off(i, c0 + 8, D), xr + 8);
+          split8(ar + P3_Y, ar + P3_Y + 16 * KB, kmajor_off(i, c0, D), yr);
+          split8(ar + P3_Y, ar + P3_Y + 16 * KB, kmajor_off(i, c0 + 8, D), yr + 8);
+        }
+      }
+      dGa[half * C + i] = pga;
+      dba[half * C + i] = pba;
+      kY[half * C + i] = pky;
+    } else {
+      {
+        SplitTile<false, C, D, 128> w;
+        w.load(a.b.W + ch * CD, D, C, helper);
+        w.store(ar + P3_W, ar + P3_W + 16 * KB, helper);
+      }
+      SplitTile<false, C, D, 128> ut;
+      ut.load(a.b.Ut + ch * CD, D, C, helper);
+      ut.store(ar + P3_UT, ar + P3_UT + 16 * KB, helper);
+    }
+  }
+  // ---- phase 3: dA = -(Y W^T + X Ut^T)
+  if (ok) {
+    sync_for_mma();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_DA, sa + P3_Y, sa + P3_Y + 16 * KB, sa + P3_W, sa + P3_W + 16 * KB, D,
+                idesc_bf16(128, C), 3);
+      mma_terms(tb + COL_DA, sa + P3_X, sa + P3_X + 16 * KB, sa + P3_UT, sa + P3_UT + 16 * KB, D,
+                idesc_bf16(128, C), 3, true);
+      mma_commit(bar);
+    }
+    wait_mma();
+  }
+  if (ok && rowlane) {  // dA (strictly lower) and dAm = dA beta_i Gam_is
+    const int i = row;
+    const float bi = bs[i];
+    for (int s0 = half * 32; s0 < half * 32 + 32; s0 += 16) {
+      float v[16];
+      tmem_ld16(tl + COL_DA + s0, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int s = s0 + e;
+        const bool low = i > s;
+        const float da = low ? -v[e] : 0.f;
+        AQ[i * MP + s] = da;
+        PM[i * MP + s] = low ? __fmul_rn(__fmul_rn(da, bi), expf(__fsub_rn(Gs[i], Gs[s]))) : 0.f;
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  // ---- phase 4: dK += dAm K + dAm^T K
+  if (ok) {
+    build_split<false, C, C>(ar + P4_AM, ar + P4_AM + 8 * KB, PM, MP, C);
+    build_split<true, C, C>(ar + P4_AMT, ar + P4_AMT + 8 * KB, PM, MP, C);
+    sync_for_mma();
+    if (t == 0) {
+      fence_after_sync();
+      mma_terms(tb + COL_DK, sa + P4_AM, sa + P4_AM + 8 * KB, sa + KT, sa + KT, C, idesc_bf16(128, D), 2, true);
+      mma_terms(tb + COL_DK, sa + P4_AMT, sa + P4_AMT + 8 * KB, sa + KT, sa + KT, C, idesc_bf16(128, D), 2, true);
+      mma_commit(bar);
+    }
+  }
+  if (t < C) {  // dbeta and dG from A while the products run
+    float b = 0.f, rw = 0.f, cl = 0.f;
+    for (int s2 = 0; s2 < t; ++s2) {
+      b = __fmaf_rn(AQ[t * MP + s2], AP[t * MP + s2], b);
+      rw = __fmaf_rn(__fmul_rn(AQ[t * MP + s2], bs[t]), AP[t * MP + s2], rw);
+    }
+    for (int i2 = t + 1; i2 < C; ++i2) cl = __fmaf_rn(__fmul_rn(AQ[i2 * MP + t], bs[i2]), AP[i2 * MP + t], cl);
+    dbc[t] = b;
+    dGe[t] = __fsub_rn(rw, cl);
+  }
+  if (ok) wait_mma();
+  if (ok && rowlane) {  // dK + dec U dS_end + beta e^G Y
+    const int s2 = row;
+    const bool live = s2 < n;
+    const float* ue_row = a.b.UdSe + ch * CD + (int64_t)s2 * D;
+    const float ds = dec[s2], bkv = __fmul_rn(bs[s2], eG[s2]);
+    float pcs = 0.f;
+    for (int cb = half * 64; cb < half * 64 + 64; cb += 32) {
+      float4 ue4[8];
+      uint4 kv[4];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) ue4[x] = *reinterpret_cast<const float4*>(ue_row + cb + 4 * x);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) kv[x] = live ? *reinterpret_cast<const uint4*>(kb + s2 * kstride + cb + 8 * x) : zero4;
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int c0 = cb + 16 * sub;
+        float v[16], yr[16], kf[16], ue[16], o[16];
+        tmem_ld16(tl + COL_DK + c0, v);
+        tmem_ld16(tl + COL_Y + c0, yr);
+        unpack8(kv[2 * sub], kf);
+        unpack8(kv[2 * sub + 1], kf + 8);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          ue[4 * x] = ue4[4 * sub + x].x;
+          ue[4 * x + 1] = ue4[4 * sub + x].y;
+          ue[4 * x + 2] = ue4[4 * sub + x].z;
+          ue[4 * x + 3] = ue4[4 * sub + x].w;
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          o[e] = __fmaf_rn(bkv, yr[e], __fmaf_rn(ds, ue[e], v[e]));
+          pcs = __fmaf_rn(ue[e], kf[e], pcs);
+        }
+        if (live) {
+          float4* dkp = reinterpret_cast<float4*>(a.b.dk_part + orow0 + (int64_t)s2 * vstride + c0);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) dkp[x] = make_float4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+        }
+      }
+    }
+    cs[half * C + s2] = pcs;
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (!ok) {
+    if (t == 0) {
+      set_error(a.hdr, GDN_DEVERR_TIMEOUT);
+      mbar_wait(bar, phase);
+    }
+  } else if (t == 0) {  // dG, reverse cumulative sum -> dg
+    float tot = 0.f;
+    for (int s2 = 0; s2 < C; ++s2) {
+      const float v = __fmul_rn(dec[s2], __fadd_rn(cs[s2], cs[C + s2]));
+      cs[s2] = v;
+      tot = __fadd_rn(tot, v);
+    }
+    float run = 0.f;
+    for (int i = C - 1; i >= 0; --i) {
+      const float ga = __fmul_rn(eG[i], __fadd_rn(dGa[i], dGa[C + i]));
+      const float ky = __fadd_rn(kY[i], kY[C + i]);
+      float v = __fadd_rn(ga, dGb[i]);
+      v = __fsub_rn(v, cs[i]);
+      v = __fmaf_rn(__fmul_rn(bs[i], eG[i]), ky, v);
+      v = __fadd_rn(v, dGe[i]);
+      if (i == C - 1) v = __fadd_rn(v, __fmaf_rn(expf(Gs[C - 1]), a.b.sdot[ch], tot));
+      run = __fadd_rn(run, v);
+      dgv[i] = run;
+    }
+  }
+  __syncthreads();
+  if (ok && t < n) {
+    const float ky = __fadd_rn(kY[t], kY[C + t]);
+    a.dg[(tok0 + t) * dm.hv + h] = dgv[t];
+    a.dbeta[(tok0 + t) * dm.hv + h] = __fadd_rn(__fmaf_rn(eG[t], ky, __fadd_rn(dba[t], dba[C + t])), dbc[t]);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
+}
+
 template <int D, typename Tin>
 void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, void* mark_ctx,
                   cudaStream_t st) {
@@ -1675,8 +2141,13 @@ void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, vo
   }
   mark(mark_ctx, n_chunks > 0 ? 1 : 0);
   if (n_chunks > 0) {
-    ensure_smem_bwd(k_bwd_grad<D, Tin>, bgrad_smem<D>());
-    k_bwd_grad<D, Tin><<<gc, NT, bgrad_smem<D>(), st>>>(a);
+    if (boundary_on_tensor_cores(a.dm)) {
+      ensure_smem_bwd(k_bwd_grad_tc, tcd::SMEM);
+      k_bwd_grad_tc<<<gc, 256, tcd::SMEM, st>>>(a);
+    } else {
+      ensure_smem_bwd(k_bwd_grad<D, Tin>, bgrad_smem<D>());
+      k_bwd_grad<D, Tin><<<gc, NT, bgrad_smem<D>(), st>>>(a);
+    }
   }
   mark(mark_ctx, n_chunks > 0 ? 1 : 0);
   if (a.T > 0) {
