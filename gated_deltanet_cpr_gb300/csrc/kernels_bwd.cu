@@ -1079,6 +1079,31 @@ __device__ __forceinline__ void build_split(unsigned char* hi, unsigned char* lo
   tile.store(hi, lo);
 }
 
+__device__ __forceinline__ void unpack8(const uint4 u, float* o) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = __uint_as_float(w[i] << 16);
+    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// dst = transpose of a shared-memory image: src is Ks rows x R columns (K-major, K = R),
+// dst is R rows x Ks columns (K = Ks); 256 threads.
+__device__ __forceinline__ void transpose_image(unsigned char* dst, const unsigned char* src, int R, int Ks) {
+  for (int q = threadIdx.x; q < R * (Ks / 8); q += 256) {
+    const int e = q % R, r0 = (q / R) * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t a0 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x, e, R));
+      const uint32_t a1 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x + 1, e, R));
+      w[x] = a0 | (a1 << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + tc::kmajor_off(e, r0, Ks)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // D = A B^T over K with split operands: terms = 3 gives A_hi B_hi + A_hi B_lo + A_lo B_hi;
 // terms = 2 (B exact, blo ignored) gives A_hi B + A_lo B; `accumulate` adds onto D.
 __device__ __forceinline__ void mma_terms(uint32_t d, uint32_t ahi, uint32_t alo, uint32_t bhi, uint32_t blo,
@@ -1154,19 +1179,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     mma_terms(tb + COL_U, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
     mma_commit(bar);
   }
-  run();
-  if (ok) {
-    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
-      float v[16];
-      tmem_ld16(tl + COL_U + s0, v);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int64_t o = ch * CD + (int64_t)(s0 + e) * D + lane_row;
-        a.b.U[o] = __fsub_rn(a.b.Ut[o], v[e]);
-      }
-    }
-  }
-  {  // <E, S0>: thread t takes float4 groups t, t + 256, ... (loads issued in batches of 8)
+  {  // <E, S0> while the product runs: thread t takes float4 groups t, t + 256, ... (batches of 8)
     float part = 0.f;
 #pragma unroll
     for (int b8 = 0; b8 < (D * D / 4) / 256; b8 += 8) {
@@ -1186,6 +1199,20 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     }
     red[t] = part;
   }
+  run();
+  if (ok) {  // U = Ut - (U^T)^T; the Ut loads all issued before the first store
+    float ut[32];
+#pragma unroll
+    for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
+#pragma unroll
+    for (int s1 = 0; s1 < 2; ++s1) {
+      float v[16];
+      tmem_ld16(tl + COL_U + cbase + 16 * s1, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        a.b.U[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = __fsub_rn(ut[16 * s1 + e], v[e]);
+    }
+  }
   fence_before_sync();
   __syncthreads();
   for (int w2 = 128; w2 > 0; w2 >>= 1) {
@@ -1196,19 +1223,28 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
 
   // ---- phase 2: E K^T and dO^T P
   if (ok) {
-    build_split<false, 128, D>(Ah, Al, E, D, 128);
-    {  // K rows (exact in bf16), rows >= n zero
+    {  // E (split) and K rows (exact in bf16, rows >= n zero): loads first
       const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + (tok0 * dm.hqk + hq) * D;
-      for (int q = t; q < C * (D / 8); q += 256) {
+      SplitTile<false, 128, D> et;
+      et.load(E, D, 128);
+      uint4 kr[4];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
         int r, k0;
-        kmajor_piece(q, D, r, k0);
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (r < n) x = *reinterpret_cast<const uint4*>(kb + (int64_t)r * dm.hqk * D + k0);
-        *reinterpret_cast<uint4*>(B2 + kmajor_off(r, k0, D)) = x;
+        kmajor_piece(t + it * 256, D, r, k0);
+        kr[it] = r < n ? *reinterpret_cast<const uint4*>(kb + (int64_t)r * dm.hqk * D + k0) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      et.store(Ah, Al);
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(t + it * 256, D, r, k0);
+        *reinterpret_cast<uint4*>(B2 + kmajor_off(r, k0, D)) = kr[it];
       }
     }
     // P^T (rows s, K = i) into the second half of B2; dO^T (rows a, K = i) into B1
-    build_split<true, C, C>(B2 + C * D * 2, B2 + C * D * 2 + C * C * 2, a.b.P + ch * C * C, C, C);
+    SplitTile<true, C, C> pt;
+    pt.load(a.b.P + ch * C * C, C, C);
     {
       float v[4][8];
 #pragma unroll
@@ -1226,6 +1262,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
           v[it][e] = x;
         }
       }
+      pt.store(B2 + C * D * 2, B2 + C * D * 2 + C * C * 2);
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
@@ -1275,6 +1312,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     __syncthreads();
     // ---- phase 4: (dO S0)^T = S0^T dO^T and dW^T = -S0^T dU^T
     build_split<true, 128, D>(Ah, Al, S0, D, 128);
+    SplitTile<false, C, D> dut;
+    dut.load(a.b.dU + ch * CD, D, C);
     {  // dO rows (i, K = a), split
       float v[4][8];
 #pragma unroll
@@ -1301,7 +1340,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
         split8(B1h, B1l, kmajor_off(r, k0, D), v[it]);
       }
     }
-    build_split<false, C, D>(B2, B2 + C * D * 2, a.b.dU + ch * CD, D, C);
+    dut.store(B2, B2 + C * D * 2);
     issue_begin();
     if (t == 0) {
       fence_after_sync();
@@ -1392,32 +1431,34 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   float* Qt = a.b.dOS0 + ch * CD;  // scratch
   const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
 
-  // ---- 1. images of K (rows), K^T, V^T; g, beta (zero beyond the chunk's tokens)
-  for (int q = t; q < C * (D / 8); q += 256) {
-    int r, c0;
-    kmajor_piece(q, D, r, c0);
-    *reinterpret_cast<uint4*>(Ki + kmajor_off(r, c0, D)) =
-        r < n ? *reinterpret_cast<const uint4*>(kb + r * kstride + c0) : z4;
-  }
-  for (int q = t; q < D * (C / 8); q += 256) {
-    const int e = q % D, r0 = (q / D) * 8;
-    uint32_t kw[4], vw[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const int r = r0 + 2 * x;
-      const uint32_t k0 = r < n ? __bfloat16_as_ushort(kb[r * kstride + e]) : 0u;
-      const uint32_t k1 = r + 1 < n ? __bfloat16_as_ushort(kb[(r + 1) * kstride + e]) : 0u;
-      const uint32_t v0 = r < n ? __bfloat16_as_ushort(vb[r * vstride + e]) : 0u;
-      const uint32_t v1 = r + 1 < n ? __bfloat16_as_ushort(vb[(r + 1) * vstride + e]) : 0u;
-      kw[x] = k0 | (k1 << 16);
-      vw[x] = v0 | (v1 << 16);
+  // ---- 1. images of K rows and V rows (V staged in the A region), g, beta (zero beyond
+  // the chunk's tokens); every load issued before the first store
+  unsigned char* Vi = smq + OFF_A;
+  {
+    float g0 = 0.f, b0 = 0.f;
+    if (t < n) {
+      g0 = a.in.g[(tok0 + t) * dm.hv + h];
+      b0 = a.in.beta[(tok0 + t) * dm.hv + h];
     }
-    *reinterpret_cast<uint4*>(KT + kmajor_off(e, r0, C)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
-    *reinterpret_cast<uint4*>(VT + kmajor_off(e, r0, C)) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
-  }
-  if (t < C) {
-    gs[t] = t < n ? a.in.g[(tok0 + t) * dm.hv + h] : 0.f;
-    bs[t] = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
+    uint4 kr[4], vr[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      int r, c0;
+      kmajor_piece(t + it * 256, D, r, c0);
+      kr[it] = r < n ? *reinterpret_cast<const uint4*>(kb + r * kstride + c0) : z4;
+      vr[it] = r < n ? *reinterpret_cast<const uint4*>(vb + r * vstride + c0) : z4;
+    }
+    if (t < C) {
+      gs[t] = g0;
+      bs[t] = b0;
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      int r, c0;
+      kmajor_piece(t + it * 256, D, r, c0);
+      *reinterpret_cast<uint4*>(Ki + kmajor_off(r, c0, D)) = kr[it];
+      *reinterpret_cast<uint4*>(Vi + kmajor_off(r, c0, D)) = vr[it];
+    }
   }
   if (t == 0) {
     mbar_init(bar, 1);
@@ -1459,6 +1500,9 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
       Gs[i] = run;
     }
   }
+  // K^T and V^T from the row images while the Gram product runs
+  transpose_image(KT, Ki, D, C);
+  transpose_image(VT, Vi, D, C);
   __syncthreads();
   if (t < C) {
     eG[t] = expf(Gs[t]);
@@ -1518,6 +1562,22 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
     }
     mma_commit(bar);
   }
+  unsigned char* Qi = smq + OFF_A;  // Q rows image over the dead A region, while the products run
+  {
+    uint4 qr[4];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      int r, c0;
+      kmajor_piece(t + it * 256, D, r, c0);
+      qr[it] = r < n ? *reinterpret_cast<const uint4*>(qb + r * kstride + c0) : z4;
+    }
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      int r, c0;
+      kmajor_piece(t + it * 256, D, r, c0);
+      *reinterpret_cast<uint4*>(Qi + kmajor_off(r, c0, D)) = qr[it];
+    }
+  }
   if (ok) wait_mma();
   if (ok) {
     if ((warp & 3) < 2) {  // W rows (not decayed)
@@ -1540,14 +1600,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
       }
     }
   }
-  // ---- 4. P = Gam (.) (Q K^T); Q image into the (dead) A region
-  unsigned char* Qi = smq + OFF_A;
-  for (int q = t; q < C * (D / 8); q += 256) {
-    int r, c0;
-    kmajor_piece(q, D, r, c0);
-    *reinterpret_cast<uint4*>(Qi + kmajor_off(r, c0, D)) =
-        r < n ? *reinterpret_cast<const uint4*>(qb + r * kstride + c0) : z4;
-  }
+  // ---- 4. P = Gam (.) (Q K^T)
   for (int q = t; q < (int)(TILE / 16); q += 256)  // K rows image for the reverse chain
     reinterpret_cast<uint4*>(img)[q] = reinterpret_cast<const uint4*>(Ki)[q];
   sync_for_mma();
@@ -1576,8 +1629,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   __syncthreads();  // W and P rows are in global memory for this CTA
   // ---- 5. Qt = diag(e^G) Q - P W: A = P (rows i), B = W^T (rows c)
   if (ok) {
-    build_split<true, D, C>(KT, VT, a.b.W + ch * CD, D, C);  // W^T hi | lo over the dead K^T, V^T
-    build_split<false, C, C>(TKh, TKl, a.b.P + ch * C * C, C, C);
+    {  // W^T hi | lo over the dead K^T, V^T; P rows over the dead TK
+      SplitTile<true, D, C> wt;
+      SplitTile<false, C, C> pr;
+      wt.load(a.b.W + ch * CD, D, C);
+      pr.load(a.b.P + ch * C * C, C, C);
+      wt.store(KT, VT);
+      pr.store(TKh, TKl);
+    }
     sync_for_mma();
     if (t == 0) {
       fence_after_sync();
@@ -1591,20 +1650,23 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   if (ok && (warp & 3) < 2) {
     const int i = lrow;
     for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 16) {
-      float v[16];
+      float v[16], qf[16];
       tmem_ld16(tmem_lane_addr(tb, warp, COL_QT + c0), v);
+      unpack8(*reinterpret_cast<const uint4*>(Qi + kmajor_off(i, c0, D)), qf);
+      unpack8(*reinterpret_cast<const uint4*>(Qi + kmajor_off(i, c0 + 8, D)), qf + 8);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float qv = i < n ? __bfloat162float(qb[i * kstride + c0 + e]) : 0.f;
-        Qt[(int64_t)i * D + c0 + e] = __fsub_rn(__fmul_rn(eG[i], qv), v[e]);
-      }
+      for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(Qt + (int64_t)i * D + c0 + e) =
+            make_float4(__fsub_rn(__fmul_rn(eG[i], qf[e]), v[e]), __fsub_rn(__fmul_rn(eG[i], qf[e + 1]), v[e + 1]),
+                        __fsub_rn(__fmul_rn(eG[i], qf[e + 2]), v[e + 2]), __fsub_rn(__fmul_rn(eG[i], qf[e + 3]), v[e + 3]));
     }
   }
   fence_before_sync();
   __syncthreads();
   // ---- 6. L = dO^T Qt: A = dO^T (rows p, K = i), B = Qt^T (rows q, K = i)
   if (ok) {
-    build_split<true, D, C>(smq + OFF_A, smq + OFF_A + TILE, Qt, D, C);
+    SplitTile<true, D, C> qtt;
+    qtt.load(Qt, D, C);
     {
       float v[4][8];
 #pragma unroll
@@ -1622,6 +1684,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
           v[it][e] = x;
         }
       }
+      qtt.store(smq + OFF_A, smq + OFF_A + TILE);
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
@@ -1685,31 +1748,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_PM = 0, COL_QK = 64, COL_AP = 128, COL_DQ = 0, COL_DK = 128, COL_X = 256,
                    COL_Y = 384, COL_DA = 0;
 }  // namespace tcd
-
-__device__ __forceinline__ void unpack8(const uint4 u, float* o) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o[2 * i] = __uint_as_float(w[i] << 16);
-    o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
-// dst = transpose of a shared-memory image: src is Ks rows x R columns (K-major, K = R),
-// dst is R rows x Ks columns (K = Ks); 256 threads.
-__device__ __forceinline__ void transpose_image(unsigned char* dst, const unsigned char* src, int R, int Ks) {
-  for (int q = threadIdx.x; q < R * (Ks / 8); q += 256) {
-    const int e = q % R, r0 = (q / R) * 8;
-    uint32_t w[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint32_t a0 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x, e, R));
-      const uint32_t a1 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x + 1, e, R));
-      w[x] = a0 | (a1 << 16);
-    }
-    *reinterpret_cast<uint4*>(dst + tc::kmajor_off(e, r0, Ks)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
 
 __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
   using namespace tcd;
