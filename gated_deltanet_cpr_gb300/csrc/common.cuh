@@ -112,6 +112,16 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return *reinterpret_cast<const float2*>(&d);
 }
 
+// shared-memory vector load that the compiler may not merge with an earlier load of the
+// same address (keeps the first pass's k out of registers during the update pass)
+__device__ __forceinline__ float4 lds4_fresh(const float* p) {
+  float4 v;
+  asm volatile("ld.volatile.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+  return v;
+}
+
 // One gated delta-rule step on row i of the state, held by a pair of adjacent lanes
 // (half = lane & 1).  The pair splits the D columns into float4 groups: register group m
 // holds columns [8m + 4*half, 8m + 4*half + 4).  Order of operations (the recurrence's
@@ -121,7 +131,9 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 // component e of every group), combined as (p0 + p1) + (p2 + p3), then added to the
 // partner lane's partial with one xor-shuffle; fp32 addition is commutative, so both lanes
 // hold identical bits.  k and q are fp32 copies in shared memory (exact widenings of the
-// inputs).  All 32 lanes of the warp must call this together.
+// inputs).  The update S <- S + u k^T and the output dot are two passes over the state
+// (the same operations on every element, in the same order), so that k and q are never
+// both held in registers.  All 32 lanes of the warp must call this together.
 template <int D>
 __device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __restrict__ k_sh,
                                             const float* __restrict__ q_sh, float a, float beta,
@@ -141,17 +153,20 @@ __device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __r
   const float p = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
   const float u = __fmul_rn(beta, __fsub_rn(v_i, p));
   const float2 u2 = make_float2(u, u);
+#pragma unroll
+  for (int m = 0; m < D / 8; ++m) {
+    const float4 kk = lds4_fresh(k_sh + 8 * m + 4 * half);
+    const float2 s01 = fma2(u2, make_float2(kk.x, kk.y), make_float2(S[m].x, S[m].y));
+    const float2 s23 = fma2(u2, make_float2(kk.z, kk.w), make_float2(S[m].z, S[m].w));
+    S[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
+  }
   p01 = make_float2(0.f, 0.f);
   p23 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int m = 0; m < D / 8; ++m) {
-    const float4 kk = *reinterpret_cast<const float4*>(k_sh + 8 * m + 4 * half);
     const float4 qq = *reinterpret_cast<const float4*>(q_sh + 8 * m + 4 * half);
-    const float2 s01 = fma2(u2, make_float2(kk.x, kk.y), make_float2(S[m].x, S[m].y));
-    const float2 s23 = fma2(u2, make_float2(kk.z, kk.w), make_float2(S[m].z, S[m].w));
-    p01 = fma2(s01, make_float2(qq.x, qq.y), p01);
-    p23 = fma2(s23, make_float2(qq.z, qq.w), p23);
-    S[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
+    p01 = fma2(make_float2(S[m].x, S[m].y), make_float2(qq.x, qq.y), p01);
+    p23 = fma2(make_float2(S[m].z, S[m].w), make_float2(qq.z, qq.w), p23);
   }
   part = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
   return __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));

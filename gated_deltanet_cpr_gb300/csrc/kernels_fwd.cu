@@ -1121,21 +1121,27 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
     if (half == 0) vs[tt * D + i] = o;
   }
   __syncthreads();
+  // the chunk record again (an L2 read instead of registers held through the token loop)
+  ChunkRec rc;
+  rc.seq = __ldcg(&w.chunks[c].seq);
+  rc.tok0 = __ldcg(&w.chunks[c].tok0);
+  rc.len = __ldcg(&w.chunks[c].len);
+  rc.jloc = __ldcg(&w.chunks[c].jloc);
   Tout* out = static_cast<Tout*>(w.o);
-  for (int idx = t; idx < len * D; idx += 2 * D) {
+  for (int idx = t; idx < rc.len * D; idx += 2 * D) {
     const int r = idx / D, e = idx % D;
-    store_out(out + ((tok0 + r) * dm.hv + h) * D + e, vs[idx]);
+    store_out(out + (((int64_t)rc.tok0 + r) * dm.hv + h) * D + e, vs[idx]);
   }
   // state decode continues from: the token recurrence through a final partial chunk
-  const SeqRec sr = w.seqs[rec.seq];
-  if (rec.jloc == sr.nchunks - 1 && (sr.len % dm.C) != 0) {
+  const SeqRec sr = w.seqs[rc.seq];
+  if (rc.jloc == sr.nchunks - 1 && (sr.len % dm.C) != 0) {
     if (w.state_out) {
-      float* dst = w.state_out + ((int64_t)rec.seq * dm.hv + h) * SZ + (int64_t)i * D;
+      float* dst = w.state_out + ((int64_t)rc.seq * dm.hv + h) * SZ + (int64_t)i * D;
 #pragma unroll
       for (int m = 0; m < D / 8; ++m) *reinterpret_cast<float4*>(dst + state_col<D>(m, half)) = S[m];
     }
     if (w.cache_run) {
-      const int sl = w.slot_of_seq ? w.slot_of_seq[rec.seq] : rec.seq;
+      const int sl = w.slot_of_seq ? w.slot_of_seq[rc.seq] : rc.seq;
       if (sl >= 0 && sl < w.cache_slots) {
         float* dst = w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)i * D;
 #pragma unroll
