@@ -23,6 +23,7 @@ Multi-GPU: one process per GPU (torchrun).  Every rank runs its own copy of the 
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -42,8 +43,35 @@ DECODE_SLOTS_BIG = 256
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
 
+# DRAM bytes (read + write) per unit of work from one ncu capture of each kernel (summaries
+# under profiles/), scaled to the benchmark's launch by the units it processes.  A figure is
+# reported only while the sources that define the kernel hash to the value they had when the
+# counters were taken; after any change it is null until recaptured.
+NCU_TRAFFIC = {
+    # 202,746,112 + 21,810,944 B for one 4096-token sequence x 32 value heads
+    "k_intra": {"src_sha": "ae1f827e94880b5f", "bytes_per_unit": (202746112 + 21810944) / (4096 * 32),
+                "unit": "token-head"},
+    "k_decode": {"src_sha": None, "bytes_per_unit": None, "unit": "slot-head"},
+}
+FWD_SOURCES = ("common.cuh", "kernels_fwd.cu", "launch.h")
+
 
 # ------------------------------------------------------------------ utilities ----
+def src_sha(files=FWD_SOURCES) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gated_deltanet_cpr_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, units: int):
+    rec = NCU_TRAFFIC[kernel]
+    if rec["bytes_per_unit"] is None or rec["src_sha"] != src_sha():
+        return None
+    return rec["bytes_per_unit"] * units
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -365,16 +393,42 @@ def run_cuda(args):
     alu_peak = 2 * SMS * FP32_LANES * SM_MAX_MHZ * 1e6 / 1e12
     ach_intra = flops_intra / (intra_ms * 1e-3) / 1e12
     roofline = {"bound": "alu", "kernel": "k_intra (intra-chunk recurrence)", "achieved": ach_intra,
-                "peak": alu_peak, "unit": "TFLOP/s", "frac": ach_intra / alu_peak, "traffic": None,
+                "peak": alu_peak, "unit": "TFLOP/s", "frac": ach_intra / alu_peak,
+                "traffic": ncu_traffic("k_intra", T * hv),
                 "peak_note": "FP32 FMA peak 2 x 152 SMs x 128 lanes x 2070 MHz; this op mix "
                              "(1 MUL + 3 FMA per state element) caps frac at 7/8"}
     chunk_heads_full = sum(L // C for L in w.lengths) * hv
     flops_bnd = chunk_heads_full * (6 * C * C * d + 4 * C * d * d)
     bnd_ms = kern["boundary_prepass"] + kern["boundary_chain"]
     tc_peak = float(P.get("bf16_tflops", PEAK_FALLBACK["bf16_tflops"]))
-    boundary = {"bound": "tensor", "achieved": flops_bnd / (bnd_ms * 1e-3) / 1e12, "peak": tc_peak,
-                "unit": "TFLOP/s", "frac": flops_bnd / (bnd_ms * 1e-3) / 1e12 / tc_peak,
-                "note": "boundary pass (pre-pass + chain) runs on FP32 SIMT in this build"}
+    hbm_peak = float(P.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
+    # algorithmic bytes of the boundary pass: K (per query/key head), V, g, beta read once,
+    # the boundary state before every chunk written once (fp32 d x d)
+    chunks = sum((L + C - 1) // C for L in w.lengths)
+    bnd_bytes = (chunks * C * d * 2 * (hqk + hv) + chunks * hv * C * 4 * 2 + chunks * hv * d * d * 4)
+    bnd_gbs = bnd_bytes / (bnd_ms * 1e-3) / 1e9
+    boundary = {"bound": "hbm", "achieved": bnd_gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": bnd_gbs / hbm_peak, "algorithmic_bytes": bnd_bytes,
+                "tensor": {"achieved": flops_bnd / (bnd_ms * 1e-3) / 1e12, "peak": tc_peak,
+                           "unit": "TFLOP/s", "frac": flops_bnd / (bnd_ms * 1e-3) / 1e12 / tc_peak,
+                           "flop": flops_bnd},
+                "note": ("pre-pass + chain on tcgen05 (split-bf16 operands, fp32 accumulation in "
+                         "TMEM); arithmetic intensity flop/algorithmic_bytes is below the bf16 "
+                         "ridge point peak_TFLOP/s / peak_GB/s, so HBM bounds this pass")}
+
+    # backward as a whole: inputs read once, gradients written once (algorithmic bytes)
+    bwd_roof = None
+    if have_bwd and grads is not None:
+        bwd_ms = sum(kern.get(n, 0.0) for n in bnames)
+        bwd_bytes = (sum(t[n].numel() * t[n].element_size() for n in ("q", "k", "v", "g", "beta", "dout"))
+                     + saved.numel() * saved.element_size()
+                     + sum(grads[n].numel() * grads[n].element_size()
+                           for n in ("dq", "dk", "dv", "dg", "dbeta")))
+        bwd_gbs = bwd_bytes / (bwd_ms * 1e-3) / 1e9
+        bwd_roof = {"bound": "hbm", "achieved": bwd_gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": bwd_gbs / hbm_peak, "algorithmic_bytes": bwd_bytes, "ms": bwd_ms,
+                    "note": "all backward kernels; the chunk-form workspace round trips are not "
+                            "algorithmic bytes"}
 
     # 256-slot decode (the decode workload's state shape), graph-replayed and per kernel
     dec = bench_decode_big(api, synth, torch, dev, w, P, seed)
@@ -391,7 +445,7 @@ def run_cuda(args):
                        "l2": "inputs larger than L2 (step working set > 2 GB of HBM traffic)",
                        "bwd_included": have_bwd},
             "stage_ms": stage_ms, "kernel_ms": kern, "roofline": roofline,
-            "boundary_roofline": boundary, "decode": dec, "e2e": e2e,
+            "boundary_roofline": boundary, "bwd_roofline": bwd_roof, "decode": dec, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk.summary(),
             "peaks_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -485,7 +539,8 @@ def bench_decode_big(api, synth, torch, dev, w, P, seed):
             "us_per_step_mean": us_per_step, "us_token_step_kernel_median": step_k3 * 1e3,
             "us_resync_step": resync_step_ms * 1e3, "tokens_per_s": N / (us_per_step * 1e-6),
             "roofline": {"bound": "hbm", "kernel": "k_decode (token step)", "achieved": ach,
-                         "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                         "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                         "traffic": ncu_traffic("k_decode", N * hv),
                          "algorithmic_bytes_per_launch": bytes_k3}}
 
 

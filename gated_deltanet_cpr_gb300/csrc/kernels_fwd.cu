@@ -491,8 +491,9 @@ static void launch_chain_t(const Dims& d, const void* keys, const float* W, cons
 }
 
 // ============================================================  K1b (tcgen05)  ===
-// Boundary chain on tensor cores for d = 128, C = 64, bf16 inputs.  One CTA of 128 threads
-// per (sequence, head): thread i owns state row i, which is also TMEM lane i.  The state
+// Boundary chain on tensor cores for d = 128, C = 64, bf16 inputs.  One CTA of 256 threads
+// per (sequence, head): state row i is TMEM lane i, read by the two warps of its lane
+// quadrant, one half of the columns each.  The state
 // S^(j) lives in TMEM (fp32) between steps; each step is
 //     D1 (128 x 64)  = S Wd^T                        3 MMAs: S_hi Wd_hi + S_hi Wd_lo + S_lo Wd_hi
 //     Vd^T[i][s]     = Ud[s][i] - D1[i][s]           (registers; then split to bf16 hi/lo)
@@ -536,7 +537,7 @@ __device__ __forceinline__ void store_row16(float* dst, const float* v) {
   for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
 }
 
-__global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __restrict__ Wimg,
+__global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __restrict__ Wimg,
                                                      const float* __restrict__ U,
                                                      const float* __restrict__ gamma, ChainWork w,
                                                      WsHeader* __restrict__ hdr) {
@@ -550,7 +551,9 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
   unsigned char* stage0 = A2l + A2_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage0 + 2 * STAGE_BYTES);  // load0, load1, mma
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
-  const int t = threadIdx.x, warp = t >> 5, row = t;
+  // warp w reads TMEM lanes 32 (w % 4) .. + 31 (state rows) and column half w / 4
+  const int t = threadIdx.x, warp = t >> 5, row = (warp & 3) * 32 + (t & 31), half = warp >> 2;
+  const int cs0 = half * (D / 2), us0 = half * (C / 2);  // first state column / first Ud column
   const int64_t SZ = (int64_t)D * D;
   const int64_t WS = (int64_t)prep_w_floats(C, D);
   if (w.seqs && !hdr->valid) return;
@@ -561,7 +564,7 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
   __shared__ int s_cnt;
   if (t == 0) s_cnt = 0;
   __syncthreads();
-  {
+  if (t < 128) {
     const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
     if (wi < total) {
       bool work = true;
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
       }
     };
     if (nfull == 0) {  // no full chunk: S^(0) passes straight to the outputs
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
     pending = (int)(gstep & 1u);
     {  // S^(0): outputs, A operand (split) and gamma_0 S^(0) into D2
       const float g0 = gamma[item0 * dm.hv + h];
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
         float v[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
@@ -688,11 +691,11 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
                    &bars[buf ^ 1]);
         }
       }
-      float ud[C];
+      float ud[C / 2];
       {
-        const float* Ug = U + (item * dm.hv + h) * (int64_t)C * D + row;
+        const float* Ug = U + (item * dm.hv + h) * (int64_t)C * D + (int64_t)us0 * D + row;
 #pragma unroll
-        for (int s = 0; s < C; ++s) ud[s] = Ug[(int64_t)s * D];
+        for (int s = 0; s < C / 2; ++s) ud[s] = Ug[(int64_t)s * D];
       }
       ok = __syncthreads_and(mbar_wait(&bars[buf], uses[buf] & 1u)) != 0;
       if (!ok) break;
@@ -719,12 +722,13 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
       mma_phase ^= 1u;
       mma_pending = false;
       fence_after_sync();
-      for (int s0 = 0; s0 < C; s0 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
-        float v[16];
-        tmem_ld16(tlane + D1_COL + s0, v);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s0 + e], v[e]);
-        store_split16(A2h, A2l, row, s0, C, v);
+      for (int s1 = 0; s1 < C / 2; s1 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
+        float v[16];
+        tmem_ld16(tlane + D1_COL + us0 + s1, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s1 + e], v[e]);
+        store_split16(A2h, A2l, row, us0 + s1, C, v);
       }
       fence_proxy_async();
       fence_before_sync();
@@ -751,7 +755,7 @@ __global__ void __launch_bounds__(128, 1) k_chain_tc(Dims dm, const float* __res
       {  // S^(j+1): outputs, next step's A operand and gamma_{j+1} S^(j+1)
         const bool more = j + 1 < nfull;
         const float gn = more ? gamma[(item + 1) * dm.hv + h] : 0.f;
-        for (int c0 = 0; c0 < D; c0 += 16) {
+        for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
           float v[16];
           tmem_ld16(tlane + D2_COL + c0, v);
           write_state(j + 1, v, c0);
@@ -1318,7 +1322,7 @@ void launch_chain(const Dims& d, const void* keys, const float* W, const float* 
     const int64_t total = (int64_t)w.N * d.hv;
     int64_t cap = w.seqs ? total : (int64_t)sm_count();
     if ((total + cap - 1) / cap > 128) cap = (total + 127) / 128;  // at most 128 items per CTA
-    k_chain_tc<<<(unsigned)(total < cap ? total : cap), 128, tcc::SMEM, st>>>(d, W, U, gamma, w, hdr);
+    k_chain_tc<<<(unsigned)(total < cap ? total : cap), 256, tcc::SMEM, st>>>(d, W, U, gamma, w, hdr);
   } else if (d.in_bf16) {
     GDN_DISPATCH_D(d.D, launch_chain_t<DD, __nv_bfloat16>(d, keys, W, U, gamma, w, hdr, st))
   } else {
