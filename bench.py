@@ -45,29 +45,38 @@ SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
 
 # DRAM bytes (read + write) per unit of work from one ncu capture of each kernel (summaries
 # under profiles/), scaled to the benchmark's launch by the units it processes.  A figure is
-# reported only while the sources that define the kernel hash to the value they had when the
-# counters were taken; after any change it is null until recaptured.
+# reported only while the kernel's source (its function text plus common.cuh) hashes to the
+# value it had when the counters were taken; after any change it is null until recaptured.
 NCU_TRAFFIC = {
     # 202,746,112 + 21,810,944 B for one 4096-token sequence x 32 value heads
-    "k_intra": {"src_sha": "ae1f827e94880b5f", "bytes_per_unit": (202746112 + 21810944) / (4096 * 32),
+    "k_intra": {"src_sha": "832e57efb113358e", "bytes_per_unit": (202746112 + 21810944) / (4096 * 32),
                 "unit": "token-head"},
     "k_decode": {"src_sha": None, "bytes_per_unit": None, "unit": "slot-head"},
 }
-FWD_SOURCES = ("common.cuh", "kernels_fwd.cu", "launch.h")
+KERNEL_TEXT = {  # file, first line of the kernel, first line after it
+    "k_intra": ("kernels_fwd.cu", "__global__ void __launch_bounds__(2 * D, 2) k_intra(",
+                "static void launch_intra_t("),
+    "k_decode": ("kernels_fwd.cu", "__global__ void __launch_bounds__(2 * D, 2) k_decode(",
+                 "static void launch_decode_t("),
+}
 
 
 # ------------------------------------------------------------------ utilities ----
-def src_sha(files=FWD_SOURCES) -> str:
-    h = hashlib.sha256()
-    for f in files:
-        with open(os.path.join(ROOT, "gated_deltanet_cpr_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
-    return h.hexdigest()[:16]
+def src_sha(kernel: str) -> str:
+    csrc = os.path.join(ROOT, "gated_deltanet_cpr_gb300", "csrc")
+    f, first, after = KERNEL_TEXT[kernel]
+    with open(os.path.join(csrc, f)) as fh:
+        text = fh.read()
+    i = text.index(first)
+    body = text[i:text.index(after, i)]
+    with open(os.path.join(csrc, "common.cuh")) as fh:
+        common = fh.read()
+    return hashlib.sha256((common + "\0" + body).encode()).hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str, units: int):
     rec = NCU_TRAFFIC[kernel]
-    if rec["bytes_per_unit"] is None or rec["src_sha"] != src_sha():
+    if rec["bytes_per_unit"] is None or rec["src_sha"] != src_sha(kernel):
         return None
     return rec["bytes_per_unit"] * units
 
