@@ -1041,11 +1041,25 @@ struct SplitTile {
       tc::kmajor_piece(q, K, r, k0);
     }
   }
+  // A row-major source whose row stride is a multiple of 4 floats (16-byte aligned rows) is
+  // read as two float4 per piece; otherwise (and for TRANS, whose warps read consecutive
+  // rows of one column) element by element.
   __device__ __forceinline__ void load(const float* __restrict__ src, int ld, int nvalid, int tid) {
+    const bool vec = !TRANS && (ld & 3) == 0;
 #pragma unroll
     for (int it = 0; it < ITER; ++it) {
       int r, k0;
       piece(tid + it * NTH, r, k0);
+      if (vec) {
+        float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+        if (r < nvalid) {
+          x0 = *reinterpret_cast<const float4*>(src + (int64_t)r * ld + k0);
+          x1 = *reinterpret_cast<const float4*>(src + (int64_t)r * ld + k0 + 4);
+        }
+        v[it][0] = x0.x; v[it][1] = x0.y; v[it][2] = x0.z; v[it][3] = x0.w;
+        v[it][4] = x1.x; v[it][5] = x1.y; v[it][6] = x1.z; v[it][7] = x1.w;
+        continue;
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         if (TRANS)
@@ -1102,6 +1116,49 @@ __device__ __forceinline__ void transpose_image(unsigned char* dst, const unsign
     }
     *reinterpret_cast<uint4*>(dst + tc::kmajor_off(e, r0, Ks)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+// dO pieces of 256 threads for d = 128, C = 64 (4 per thread), tokens >= n zero.  The
+// dtype branch is outside the loops, so that all of a thread's loads are in flight together.
+// load_dO_T: piece q = t + 256 it is value dim r = q % 128 of tokens (q / 128) * 8 .. + 7
+// (a K-major image of dO^T); load_dO_rows: piece q is 8 consecutive dims of one token, in
+// kmajor_piece order (a K-major image of dO), read as one 16-byte (bf16) or two (fp32) loads.
+template <typename T>
+__device__ __forceinline__ void load_dO_T_t(float (&v)[4][8], const T* p, int64_t tstride, int n) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int q = threadIdx.x + it * 256, r = q % 128, k0 = (q / 128) * 8;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[it][e] = (k0 + e < n) ? to_f32(p[(int64_t)(k0 + e) * tstride + r]) : 0.f;
+  }
+}
+__device__ __forceinline__ void load_dO_T(float (&v)[4][8], const void* dO, bool bf16, int64_t base,
+                                          int64_t tstride, int n) {
+  if (bf16)
+    load_dO_T_t(v, static_cast<const __nv_bfloat16*>(dO) + base, tstride, n);
+  else
+    load_dO_T_t(v, static_cast<const float*>(dO) + base, tstride, n);
+}
+template <typename T>
+__device__ __forceinline__ void load_dO_rows_t(float (&v)[4][8], const T* p, int64_t tstride, int n) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    int r, k0;
+    tc::kmajor_piece(threadIdx.x + it * 256, 128, r, k0);
+    if (r < n) {
+      load8(p + (int64_t)r * tstride + k0, v[it]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[it][e] = 0.f;
+    }
+  }
+}
+__device__ __forceinline__ void load_dO_rows(float (&v)[4][8], const void* dO, bool bf16, int64_t base,
+                                             int64_t tstride, int n) {
+  if (bf16)
+    load_dO_rows_t(v, static_cast<const __nv_bfloat16*>(dO) + base, tstride, n);
+  else
+    load_dO_rows_t(v, static_cast<const float*>(dO) + base, tstride, n);
 }
 
 // D = A B^T over K with split operands: terms = 3 gives A_hi B_hi + A_hi B_lo + A_lo B_hi;
@@ -1170,8 +1227,20 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     __syncthreads();
   };
 
-  // ---- phase 1: U^T = Ut^T - S0 W^T
-  build_split<false, 128, D>(Ah, Al, S0, D, 128);
+  // ---- phase 1: U^T = Ut^T - S0 W^T; <E, S0> from the same loads (thread t sums its own
+  // pieces in order, then a fixed tree over the threads)
+  {
+    SplitTile<false, 128, D> s0t, et;
+    s0t.load(S0, D, 128);
+    et.load(E, D, 128);
+    float part = 0.f;
+#pragma unroll
+    for (int it = 0; it < SplitTile<false, 128, D>::ITER; ++it)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) part = __fmaf_rn(et.v[it][e], s0t.v[it][e], part);
+    red[t] = part;
+    s0t.store(Ah, Al);
+  }
   build_split<false, C, D>(B1h, B1l, a.b.W + ch * CD, D, C);
   issue_begin();
   if (t == 0) {
@@ -1179,31 +1248,11 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     mma_terms(tb + COL_U, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
     mma_commit(bar);
   }
-  {  // <E, S0> while the product runs: thread t takes float4 groups t, t + 256, ... (batches of 8)
-    float part = 0.f;
+  float ut[32];  // Ut for the readout, loaded while the product runs
 #pragma unroll
-    for (int b8 = 0; b8 < (D * D / 4) / 256; b8 += 8) {
-      float4 x[8], y[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        x[u] = reinterpret_cast<const float4*>(E)[t + (b8 + u) * 256];
-        y[u] = reinterpret_cast<const float4*>(S0)[t + (b8 + u) * 256];
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        part = __fmaf_rn(x[u].x, y[u].x, part);
-        part = __fmaf_rn(x[u].y, y[u].y, part);
-        part = __fmaf_rn(x[u].z, y[u].z, part);
-        part = __fmaf_rn(x[u].w, y[u].w, part);
-      }
-    }
-    red[t] = part;
-  }
+  for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
   run();
-  if (ok) {  // U = Ut - (U^T)^T; the Ut loads all issued before the first store
-    float ut[32];
-#pragma unroll
-    for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
+  if (ok) {  // U = Ut - (U^T)^T
 #pragma unroll
     for (int s1 = 0; s1 < 2; ++s1) {
       float v[16];
@@ -1247,21 +1296,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     pt.load(a.b.P + ch * C * C, C, C);
     {
       float v[4][8];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = k0 + e;
-          float x = 0.f;
-          if (i < n) {
-            const int64_t o = ((tok0 + i) * dm.hv + h) * D + r;
-            x = dm.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.dO)[o])
-                            : static_cast<const float*>(a.dO)[o];
-          }
-          v[it][e] = x;
-        }
-      }
+      load_dO_T(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
       pt.store(B2 + C * D * 2, B2 + C * D * 2 + C * C * 2);
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
@@ -1291,8 +1326,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     fence_before_sync();
     __syncthreads();
     // ---- phase 3: (U E)^T = E^T U^T
-    build_split<true, 128, D>(Ah, Al, E, D, 128);
-    build_split<false, C, D>(B1h, B1l, a.b.U + ch * CD, D, C);
+    {
+      SplitTile<true, 128, D> ett;
+      SplitTile<false, C, D> ut;
+      ett.load(E, D, 128);
+      ut.load(a.b.U + ch * CD, D, C);
+      ett.store(Ah, Al);
+      ut.store(B1h, B1l);
+    }
     issue_begin();
     if (t == 0) {
       fence_after_sync();
@@ -1311,27 +1352,12 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
     fence_before_sync();
     __syncthreads();
     // ---- phase 4: (dO S0)^T = S0^T dO^T and dW^T = -S0^T dU^T
-    build_split<true, 128, D>(Ah, Al, S0, D, 128);
     SplitTile<false, C, D> dut;
     dut.load(a.b.dU + ch * CD, D, C);
-    {  // dO rows (i, K = a), split
+    {  // dO rows (i, K = a), split; loads in flight with dU's and S0's
       float v[4][8];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256;
-        int r, k0;
-        kmajor_piece(q, D, r, k0);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float x = 0.f;
-          if (r < n) {
-            const int64_t o = ((tok0 + r) * dm.hv + h) * D + k0 + e;
-            x = dm.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.dO)[o])
-                            : static_cast<const float*>(a.dO)[o];
-          }
-          v[it][e] = x;
-        }
-      }
+      load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+      build_split<true, 128, D>(Ah, Al, S0, D, 128);
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         const int q = t + it * 256;
@@ -1669,21 +1695,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
     qtt.load(Qt, D, C);
     {
       float v[4][8];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = k0 + e;
-          float x = 0.f;
-          if (i < n) {
-            const int64_t o = ((tok0 + i) * dm.hv + h) * D + r;
-            x = dm.out_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.dO)[o])
-                            : static_cast<const float*>(a.dO)[o];
-          }
-          v[it][e] = x;
-        }
-      }
+      load_dO_T(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
       qtt.store(smq + OFF_A, smq + OFF_A + TILE);
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
