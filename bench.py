@@ -546,7 +546,10 @@ def bench_decode_big(api, synth, torch, dev, w, P, seed):
     ach = bytes_k3 / (step_k3 * 1e-3) / 1e9
     return {"slots": N, "heads": hv, "d": d, "steps": DECODE_STEPS,
             "us_per_step_mean": us_per_step, "us_token_step_kernel_median": step_k3 * 1e3,
-            "us_resync_step": resync_step_ms * 1e3, "tokens_per_s": N / (us_per_step * 1e-6),
+            "us_resync_step": resync_step_ms * 1e3,
+            "us_resync_stages": dict(zip(("token_step", "prepass", "chain", "advance"),
+                                         (x * 1e3 for x in stages[-1]))),
+            "tokens_per_s": N / (us_per_step * 1e-6),
             "roofline": {"bound": "hbm", "kernel": "k_decode (token step)", "achieved": ach,
                          "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                          "traffic": ncu_traffic("k_decode", N * hv),

@@ -647,12 +647,27 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
         store_row16(w.s_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
       }
     };
-    if (nfull == 0) {  // no full chunk: S^(0) passes straight to the outputs
-      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
-        float v[16];
+    // this thread's half row of S^(0), all loads in flight at once
+    float4 s0v[D / 8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
-        write_state(0, v, c0);
+    for (int x = 0; x < D / 8; ++x)
+      s0v[x] = src ? *reinterpret_cast<const float4*>(src + (int64_t)row * D + cs0 + 4 * x)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    auto s0_cols = [&](int g, float* v) {  // columns cs0 + 16 g .. + 15
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        v[4 * x] = s0v[4 * g + x].x;
+        v[4 * x + 1] = s0v[4 * g + x].y;
+        v[4 * x + 2] = s0v[4 * g + x].z;
+        v[4 * x + 3] = s0v[4 * g + x].w;
+      }
+    };
+    if (nfull == 0) {  // no full chunk: S^(0) passes straight to the outputs
+#pragma unroll
+      for (int g = 0; g < D / 32; ++g) {
+        float v[16];
+        s0_cols(g, v);
+        write_state(0, v, cs0 + 16 * g);
       }
       continue;
     }
@@ -664,10 +679,11 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
     pending = (int)(gstep & 1u);
     {  // S^(0): outputs, A operand (split) and gamma_0 S^(0) into D2
       const float g0 = gamma[item0 * dm.hv + h];
-      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
-        float v[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = src ? src[(int64_t)row * D + c0 + e] : 0.f;
+      for (int g = 0; g < D / 32; ++g) {
+        const int c0 = cs0 + 16 * g;
+        float v[16];
+        s0_cols(g, v);
         write_state(0, v, c0);
         store_split16(A1h, A1l, row, c0, D, v);
 #pragma unroll
