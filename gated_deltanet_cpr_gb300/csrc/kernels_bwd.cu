@@ -1102,21 +1102,6 @@ __device__ __forceinline__ void unpack8(const uint4 u, float* o) {
   }
 }
 
-// dst = transpose of a shared-memory image: src is Ks rows x R columns (K-major, K = R),
-// dst is R rows x Ks columns (K = Ks); 256 threads.
-__device__ __forceinline__ void transpose_image(unsigned char* dst, const unsigned char* src, int R, int Ks) {
-  for (int q = threadIdx.x; q < R * (Ks / 8); q += 256) {
-    const int e = q % R, r0 = (q / R) * 8;
-    uint32_t w[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint32_t a0 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x, e, R));
-      const uint32_t a1 = *reinterpret_cast<const uint16_t*>(src + tc::kmajor_off(r0 + 2 * x + 1, e, R));
-      w[x] = a0 | (a1 << 16);
-    }
-    *reinterpret_cast<uint4*>(dst + tc::kmajor_off(e, r0, Ks)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
 
 // dO pieces of 256 threads for d = 128, C = 64 (4 per thread), tokens >= n zero.  The
 // dtype branch is outside the loops, so that all of a thread's loads are in flight together.
@@ -1527,8 +1512,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
     }
   }
   // K^T and V^T from the row images while the Gram product runs
-  transpose_image(KT, Ki, D, C);
-  transpose_image(VT, Vi, D, C);
+  tc::transpose_image(KT, Ki, D, C);
+  tc::transpose_image(VT, Vi, D, C);
   __syncthreads();
   if (t < C) {
     eG[t] = expf(Gs[t]);
@@ -1883,8 +1868,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
     mma_commit(bar);
   }
   // while the products run: K^T and Q^T images from the row images (reads of the operands only)
-  transpose_image(ar + QT, ar + P1_Q, D, C);
-  transpose_image(ar + KT, ar + P1_K, D, C);
+  tc::transpose_image(ar + QT, ar + P1_Q, D, C);
+  tc::transpose_image(ar + KT, ar + P1_K, D, C);
   if (t < C) {
     eG[t] = expf(Gs[t]);
     dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));

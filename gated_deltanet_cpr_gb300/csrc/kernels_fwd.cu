@@ -909,28 +909,33 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
     const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
 
-    // 1. operand images straight from global memory
-    for (int q = t; q < C * (D / 8); q += 256) {  // K rows: 16-byte pieces
-      int r, c0;
-      tc::kmajor_piece(q, D, r, c0);
-      *reinterpret_cast<uint4*>(R0 + tc::kmajor_off(r, c0, D)) = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
-    }
-    for (int q = t; q < D * (C / 8); q += 256) {  // K^T and V^T: column e, 8 tokens at a time
-      const int e = q % D, r0 = (q / D) * 8;
-      uint32_t kw[4], vw[4];
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        kw[x] = (uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x) * kstride + e]) |
-                ((uint32_t)__bfloat16_as_ushort(kb[(r0 + 2 * x + 1) * kstride + e]) << 16);
-        vw[x] = (uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x) * vstride + e]) |
-                ((uint32_t)__bfloat16_as_ushort(vb[(r0 + 2 * x + 1) * vstride + e]) << 16);
+    // 1. K rows and V rows (staged in the A region, free until the Gram readout) straight
+    // from global memory, g and beta: every load issued before the first store
+    {
+      uint4 kr[4], vr[4];
+      float g0 = 0.f, b0 = 0.f;
+      if (t < C) {
+        g0 = in.g[(tok0 + t) * dm.hv + h];
+        b0 = in.beta[(tok0 + t) * dm.hv + h];
       }
-      *reinterpret_cast<uint4*>(KT + tc::kmajor_off(e, r0, C)) = make_uint4(kw[0], kw[1], kw[2], kw[3]);
-      *reinterpret_cast<uint4*>(VT + tc::kmajor_off(e, r0, C)) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
-    }
-    if (t < C) {
-      gs[t] = in.g[(tok0 + t) * dm.hv + h];
-      bs[t] = in.beta[(tok0 + t) * dm.hv + h];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {  // C * D / 8 = 1024 pieces of 16 bytes
+        int r, c0;
+        tc::kmajor_piece(t + it * 256, D, r, c0);
+        kr[it] = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
+        vr[it] = *reinterpret_cast<const uint4*>(vb + r * vstride + c0);
+      }
+      if (t < C) {
+        gs[t] = g0;
+        bs[t] = b0;
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, c0;
+        tc::kmajor_piece(t + it * 256, D, r, c0);
+        *reinterpret_cast<uint4*>(R0 + tc::kmajor_off(r, c0, D)) = kr[it];
+        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(A) + tc::kmajor_off(r, c0, D)) = vr[it];
+      }
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
@@ -950,6 +955,9 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
         Gs[i] = run;
       }
     }
+    // K^T and V^T images from the row images while the Gram product runs (it reads only R0)
+    tc::transpose_image(KT, R0, D, C);
+    tc::transpose_image(VT, reinterpret_cast<const unsigned char*>(A), D, C);
     __syncthreads();
     if (t < C) {
       bk[t] = __fmul_rn(bs[t], expf(Gs[t]));

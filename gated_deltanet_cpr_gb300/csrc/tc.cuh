@@ -171,5 +171,21 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(hi)));
 }
 
+// dst = transpose of a shared-memory image: src is Ks rows x R columns (K-major, K = R),
+// dst is R rows x Ks columns (K = Ks); 256 threads.
+__device__ __forceinline__ void transpose_image(unsigned char* dst, const unsigned char* src, int R, int Ks) {
+  for (int q = threadIdx.x; q < R * (Ks / 8); q += 256) {
+    const int e = q % R, r0 = (q / R) * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t a0 = *reinterpret_cast<const uint16_t*>(src + kmajor_off(r0 + 2 * x, e, R));
+      const uint32_t a1 = *reinterpret_cast<const uint16_t*>(src + kmajor_off(r0 + 2 * x + 1, e, R));
+      w[x] = a0 | (a1 << 16);
+    }
+    *reinterpret_cast<uint4*>(dst + kmajor_off(e, r0, Ks)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace tc
 }  // namespace gdn
