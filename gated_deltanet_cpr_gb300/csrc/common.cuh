@@ -185,14 +185,22 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float
   constexpr int TB = 16;
   const int t = threadIdx.x;
   const int nb = C / TB;
-  if (t < C) {
-    const int r = t, rend = (r / TB) * TB + TB;
-    Tm[r * CP + r] = 1.f;
-    for (int i = r + 1; i < rend; ++i) {
+  if (t < C) {  // column r of its diagonal block, kept in registers (col[k] = T[rb + k][r])
+    const int r = t, rb = (r / TB) * TB, rr = r - rb;
+    float col[TB];
+#pragma unroll
+    for (int k = 0; k < TB; ++k) col[k] = (k == rr) ? 1.f : 0.f;
+#pragma unroll
+    for (int ii = 1; ii < TB; ++ii) {
       float acc = 0.f;
-      for (int m = r; m < i; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
-      Tm[i * CP + r] = -acc;
+#pragma unroll
+      for (int m = 0; m < ii; ++m)
+        if (m >= rr) acc = __fmaf_rn(A[(rb + ii) * CP + rb + m], col[m], acc);
+      if (ii > rr) col[ii] = -acc;
     }
+#pragma unroll
+    for (int k = 0; k < TB; ++k)
+      if (k >= rr) Tm[(rb + k) * CP + r] = col[k];
   }
   __syncthreads();
   for (int off = 1; off < nb; ++off) {
@@ -201,6 +209,7 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float
       const int I = off + e / (TB * TB), ii = (e / TB) % TB, rr = e % TB;
       const int i = I * TB + ii, r = (I - off) * TB + rr;
       float acc = 0.f;
+#pragma unroll 4
       for (int m = r; m < I * TB; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
       Xs[e] = acc;
     }
@@ -210,6 +219,7 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float
       const int i = I * TB + ii, r = (I - off) * TB + rr;
       const float* X = Xs + (e / (TB * TB)) * TB * TB;
       float acc = 0.f;
+#pragma unroll 4
       for (int m = I * TB; m <= i; ++m) acc = __fmaf_rn(Tm[i * CP + m], X[(m - I * TB) * TB + rr], acc);
       Tm[i * CP + r] = -acc;
     }
