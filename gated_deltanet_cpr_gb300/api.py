@@ -26,7 +26,8 @@ DEVERR = {0: "none", 1: "cu_seqlens mismatch", 2: "slot out of range", 3: "negat
 # every function the header declares (checked by the CPU test suite)
 EXPORTS = ("gdn_cpr_version", "gdn_cpr_status_string", "gdn_cpr_workspace_size",
            "gdn_cpr_prefill", "gdn_cpr_decode_step", "gdn_cpr_fwd", "gdn_cpr_bwd",
-           "gdn_cpr_get_device_error", "gdn_cpr_set_profile", "gdn_cpr_decode_step_noalloc")
+           "gdn_cpr_get_device_error", "gdn_cpr_set_profile", "gdn_cpr_decode_step_noalloc",
+           "gdn_cpr_policy_digest")
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -82,6 +83,8 @@ def load():
             lib.gdn_cpr_decode_step_noalloc.restype = I
             lib.gdn_cpr_set_profile.argtypes = [P]
             lib.gdn_cpr_set_profile.restype = None
+            lib.gdn_cpr_policy_digest.argtypes = [P, P, P, S]
+            lib.gdn_cpr_policy_digest.restype = I
             for fn in ("gdn_cpr_workspace_size", "gdn_cpr_prefill", "gdn_cpr_decode_step",
                        "gdn_cpr_fwd", "gdn_cpr_bwd", "gdn_cpr_get_device_error"):
                 getattr(lib, fn).restype = I
@@ -123,6 +126,19 @@ def _check(fn, rc):
 def make_shape(num_seqs, total_tokens, h_qk, h_v, d, chunk, in_dtype, out_dtype) -> Shape:
     return Shape(int(num_seqs), int(total_tokens), int(h_qk), int(h_v), int(d), int(d),
                  int(chunk), _dt(in_dtype), _dt(out_dtype))
+
+
+def policy_digest(d, chunk, in_dtype=torch.bfloat16, out_dtype=None, h_qk=1, h_v=1,
+                  num_seqs=1, total_tokens=0):
+    """gdn_cpr_policy_digest: (hex SHA-256 of the numerical policy, its canonical text)."""
+    lib = load()
+    shape = make_shape(num_seqs, total_tokens, h_qk, h_v, d, chunk, in_dtype,
+                       in_dtype if out_dtype is None else out_dtype)
+    dig = (ctypes.c_ubyte * 32)()
+    buf = ctypes.create_string_buffer(4096)
+    _check("gdn_cpr_policy_digest",
+           lib.gdn_cpr_policy_digest(ctypes.byref(shape), dig, buf, ctypes.sizeof(buf)))
+    return bytes(dig).hex(), buf.value.decode()
 
 
 def _host_cu(cu_seqlens, cu_seqlens_host):

@@ -205,6 +205,22 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape *shape, const void *q, const void *k,
                        float *dq, float *dk, float *dv, float *dg, float *dbeta,
                        float *dstate_in, void *ws, size_t ws_bytes, gdn_stream_t stream);
 
+/* Numerical-policy identity (IsoExec pages, section on the structure of the execution
+ * contract, item "Identities": SHA-256 digests by which trainer and rollout engine check
+ * that they run the same verified numerical policy).  Writes into digest[32] the SHA-256
+ * (FIPS 180-4) of a canonical text listing every choice that decides the bits of this
+ * library's results for the given shape: d_k, d_v, chunk length, input and output dtypes,
+ * the boundary path (tensor cores with split-bf16 operands, or fp32 SIMT), the reduction
+ * orders of the token step, the triangular solve and the cumulative sum, the exponential,
+ * the rounding of the output and the library version.  The number of sequences, tokens
+ * and heads do not enter it: shapes whose results are bit-identical share a digest.
+ * When text is non-NULL it also receives that text, NUL-terminated and truncated to
+ * text_len bytes.  Host only, no GPU work.  Returns GDN_ERR_INVALID_ARG for a NULL shape
+ * or digest and GDN_ERR_UNSUPPORTED / GDN_ERR_INVALID_ARG for shapes the calls reject.
+ * This library's own addition: the pages name the digests but define no content.     */
+gdn_status gdn_cpr_policy_digest(const gdn_cpr_shape *shape, unsigned char digest[32], char *text,
+                                 size_t text_len);
+
 /* Optional profiling hook (per calling thread; NULL disables it, the default).  While set,
  * every entry point called from this thread records events[i] (cudaEvent_t handles created
  * by the caller) on its stream at its stage boundaries -- events[0] before its first
