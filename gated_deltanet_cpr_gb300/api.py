@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libgdn_cpr.so")
 
 GDN_F32, GDN_BF16 = 0, 1
-MODE_PREFILL, MODE_DECODE, MODE_FWD, MODE_BWD = 0, 1, 2, 3
+MODE_PREFILL, MODE_DECODE, MODE_FWD, MODE_BWD, MODE_CONTINUE = 0, 1, 2, 3, 4
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "workspace missing, misaligned or too small", 5: "device-side error recorded"}
 DEVERR = {0: "none", 1: "cu_seqlens mismatch", 2: "slot out of range", 3: "negative position",
@@ -27,7 +27,7 @@ DEVERR = {0: "none", 1: "cu_seqlens mismatch", 2: "slot out of range", 3: "negat
 EXPORTS = ("gdn_cpr_version", "gdn_cpr_status_string", "gdn_cpr_workspace_size",
            "gdn_cpr_prefill", "gdn_cpr_decode_step", "gdn_cpr_fwd", "gdn_cpr_bwd",
            "gdn_cpr_get_device_error", "gdn_cpr_set_profile", "gdn_cpr_decode_step_noalloc",
-           "gdn_cpr_policy_digest")
+           "gdn_cpr_policy_digest", "gdn_cpr_prefill_continue")
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -85,6 +85,8 @@ def load():
             lib.gdn_cpr_set_profile.restype = None
             lib.gdn_cpr_policy_digest.argtypes = [P, P, P, S]
             lib.gdn_cpr_policy_digest.restype = I
+            lib.gdn_cpr_prefill_continue.argtypes = [P] * 14 + [S, P]
+            lib.gdn_cpr_prefill_continue.restype = I
             for fn in ("gdn_cpr_workspace_size", "gdn_cpr_prefill", "gdn_cpr_decode_step",
                        "gdn_cpr_fwd", "gdn_cpr_bwd", "gdn_cpr_get_device_error"):
                 getattr(lib, fn).restype = I
@@ -213,6 +215,39 @@ def prefill(q, k, v, g, beta, cu_seqlens, chunk=64, state_in=None, out_dtype=Non
                              ctypes.byref(cs) if cs is not None else None, _p(slot_of_seq),
                              _p(ws), ws.numel(), _stream(q.device))
     _check("gdn_cpr_prefill", rc)
+    return o, state_out
+
+
+def prefill_continue(q, k, v, g, beta, cu_seqlens, slots, cache: Cache, pos_host=None,
+                     cu_seqlens_host=None, out_dtype=None, want_state=False, ws=None, o=None,
+                     state_out=None):
+    """gdn_cpr_prefill_continue: append the packed tokens of sequence i to cache slot
+    slots[i] at its current position.  pos_host defaults to a host copy of cache.pos[slots]
+    (a device read).  Returns (o, state_out)."""
+    lib = load()
+    cu_host = _host_cu(cu_seqlens, cu_seqlens_host)
+    N = cu_host.numel() - 1
+    T, hqk, d = k.shape
+    hv = v.shape[1]
+    od = out_dtype or q.dtype
+    shape = make_shape(N, T, hqk, hv, d, cache.chunk, q.dtype, od)
+    if pos_host is None:
+        pos_host = cache.pos.index_select(0, slots.long()).cpu()
+    if not isinstance(pos_host, torch.Tensor):
+        pos_host = torch.tensor(list(pos_host), dtype=torch.int32)
+    pos_host = pos_host.to(torch.int32).contiguous()
+    if o is None:
+        o = torch.empty((T, hv, d), dtype=od, device=q.device)
+    if state_out is None and want_state:
+        state_out = torch.empty((N, hv, d, d), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = alloc_workspace(workspace_bytes(shape, MODE_CONTINUE, cu_host), q.device)
+    cs = cache.struct()
+    rc = lib.gdn_cpr_prefill_continue(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g), _p(beta),
+                                      _p(cu_seqlens), _p(cu_host), _p(slots), _p(pos_host),
+                                      ctypes.byref(cs), _p(o), _p(state_out), _p(ws), ws.numel(),
+                                      _stream(q.device))
+    _check("gdn_cpr_prefill_continue", rc)
     return o, state_out
 
 

@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <vector>
+
 #include "../../include/gdn_cpr.h"
 #include "launch.h"
 
@@ -131,6 +133,51 @@ thread_local gdn_cpr_profile* t_profile = nullptr;
 
 // Stage marker of the profiling hook: event `stage` after the stage's kernels, and the
 // count of kernels those stages launched.
+// Continued prefill: the virtual prefill's regions, then the virtual cu_seqlens, tail
+// lengths, base positions, the gathered q, k, v, g, beta and the virtual output.
+struct ContLayout {
+  FwdLayout f;
+  size_t vcu, rlen, base, q, k, v, g, beta, o, total;
+};
+
+ContLayout cont_layout(const gdn_cpr_shape* sv, int64_t vchunks) {
+  ContLayout L;
+  L.f = fwd_layout(sv, vchunks, true);
+  const size_t N = sv->num_seqs, vT = sv->total_tokens, D = sv->d_k, hqk = sv->h_qk, hv = sv->h_v;
+  const size_t esz = sv->in_dtype == GDN_BF16 ? 2 : 4, osz = sv->out_dtype == GDN_BF16 ? 2 : 4;
+  size_t off = L.f.total;
+  L.vcu = off;  off = align_up(off + sizeof(int32_t) * (N + 1));
+  L.rlen = off; off = align_up(off + sizeof(int32_t) * N);
+  L.base = off; off = align_up(off + sizeof(int32_t) * N);
+  L.q = off;    off = align_up(off + vT * hqk * D * esz);
+  L.k = off;    off = align_up(off + vT * hqk * D * esz);
+  L.v = off;    off = align_up(off + vT * hv * D * esz);
+  L.g = off;    off = align_up(off + vT * hv * sizeof(float));
+  L.beta = off; off = align_up(off + vT * hv * sizeof(float));
+  L.o = off;    off = align_up(off + vT * hv * D * osz);
+  L.total = off;
+  return L;
+}
+
+// Virtual cu_seqlens of a continued prefill: sequence i is r_i = pos_i % C tail tokens plus
+// its new tokens (pos NULL: the largest tail, C - 1, for the workspace bound).
+gdn_status virtual_cu(const gdn_cpr_shape* s, const int32_t* cu, const int32_t* pos, std::vector<int32_t>& vcu) {
+  const int N = s->num_seqs;
+  vcu.assign((size_t)N + 1, 0);
+  int64_t acc = 0;
+  for (int i = 0; i < N; ++i) {
+    int32_t r = s->chunk - 1;
+    if (pos) {
+      if (pos[i] < 0) return GDN_ERR_INVALID_ARG;
+      r = pos[i] % s->chunk;
+    }
+    acc += r + (int64_t)(cu[i + 1] - cu[i]);
+    if (acc > INT32_MAX) return GDN_ERR_INVALID_ARG;
+    vcu[(size_t)i + 1] = (int32_t)acc;
+  }
+  return GDN_OK;
+}
+
 struct Stages {
   cudaStream_t st;
   int next = 0;
@@ -240,7 +287,7 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
 
   if (cache) {
     launch_tail_fill(d, in, seqs, N, slot_of_seq, cache->slots, cache->tail_k, cache->tail_v,
-                     cache->tail_g, cache->tail_beta, cache->pos, hdr, st);
+                     cache->tail_g, cache->tail_beta, cache->pos, nullptr, hdr, st);
     stg.mark(1);
   }
   return finish(st);
@@ -281,6 +328,19 @@ gdn_status gdn_cpr_workspace_size(const gdn_cpr_shape* shape, gdn_mode mode,
     case GDN_MODE_PREFILL: *bytes = fwd_layout(shape, n_chunks, true).total; return GDN_OK;
     case GDN_MODE_FWD: *bytes = fwd_layout(shape, n_chunks, false).total; return GDN_OK;
     case GDN_MODE_BWD: *bytes = bwd_layout(shape, n_chunks).total; return GDN_OK;
+    case GDN_MODE_CONTINUE: {
+      std::vector<int32_t> vcu;
+      rc = virtual_cu(shape, cu_seqlens_host, nullptr, vcu);
+      if (rc != GDN_OK) return rc;
+      gdn_cpr_shape sv = *shape;
+      sv.total_tokens = vcu[(size_t)shape->num_seqs];
+      int64_t vchunks = 0;
+      uint32_t vhash = 0;
+      rc = scan_cu(&sv, vcu.data(), &vchunks, &vhash);
+      if (rc != GDN_OK) return rc;
+      *bytes = cont_layout(&sv, vchunks).total;
+      return GDN_OK;
+    }
     default: return GDN_ERR_INVALID_ARG;
   }
 }
@@ -414,6 +474,106 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k,
 }
 
 void gdn_cpr_set_profile(gdn_cpr_profile* profile) { t_profile = profile; }
+
+gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, const void* k,
+                                    const void* v, const float* g, const float* beta,
+                                    const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host,
+                                    const int32_t* slot_dev, const int32_t* pos_host,
+                                    const gdn_cpr_cache* cache, void* o, float* state_out, void* ws,
+                                    size_t ws_bytes, gdn_stream_t stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gdn_status rc = check_shape(shape);
+  if (rc != GDN_OK) return rc;
+  int64_t n_chunks = 0;
+  uint32_t hash = 0;
+  rc = scan_cu(shape, cu_seqlens_host, &n_chunks, &hash);
+  if (rc != GDN_OK) return rc;
+  const int N = shape->num_seqs;
+  const int64_t T = shape->total_tokens;
+  if (!cache) return GDN_ERR_INVALID_ARG;
+  rc = check_cache(cache);
+  if (rc != GDN_OK) return rc;
+  if (T > 0 && (!ok_ptr(q, 16) || !ok_ptr(k, 16) || !ok_ptr(v, 16) || !ok_ptr(g, 4) ||
+                !ok_ptr(beta, 4) || !ok_ptr(o, 16)))
+    return GDN_ERR_INVALID_ARG;
+  if (N > 0 && (!ok_ptr(cu_seqlens_dev, 4) || !ok_ptr(slot_dev, 4) || !pos_host)) return GDN_ERR_INVALID_ARG;
+  if (state_out && !aligned(state_out, 16)) return GDN_ERR_INVALID_ARG;
+  std::vector<int32_t> vcu_h;
+  rc = virtual_cu(shape, cu_seqlens_host, pos_host, vcu_h);
+  if (rc != GDN_OK) return rc;
+  gdn_cpr_shape sv = *shape;
+  sv.total_tokens = vcu_h[(size_t)N];
+  int64_t vchunks = 0;
+  uint32_t vhash = 0;
+  rc = scan_cu(&sv, vcu_h.data(), &vchunks, &vhash);
+  if (rc != GDN_OK) return rc;
+  const ContLayout L = cont_layout(&sv, vchunks);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if (N == 0) return GDN_OK;
+
+  const Dims d = dims_of(shape);
+  const int64_t vT = sv.total_tokens;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  ChunkRec* chunks = reinterpret_cast<ChunkRec*>(at(ws, L.f.chunks));
+  SeqRec* seqs = reinterpret_cast<SeqRec*>(at(ws, L.f.seqs));
+  float* W = reinterpret_cast<float*>(at(ws, L.f.W));
+  float* U = reinterpret_cast<float*>(at(ws, L.f.U));
+  float* gamma = reinterpret_cast<float*>(at(ws, L.f.gamma));
+  float* bnd = reinterpret_cast<float*>(at(ws, L.f.bnd));
+  int32_t* vcu = reinterpret_cast<int32_t*>(at(ws, L.vcu));
+  int32_t* rlen = reinterpret_cast<int32_t*>(at(ws, L.rlen));
+  int32_t* base = reinterpret_cast<int32_t*>(at(ws, L.base));
+  void* vo = at(ws, L.o);
+  TokenArrays in{q, k, v, g, beta};
+  TokenArrays vin{at(ws, L.q), at(ws, L.k), at(ws, L.v), reinterpret_cast<const float*>(at(ws, L.g)),
+                  reinterpret_cast<const float*>(at(ws, L.beta))};
+
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
+  Stages stg(st);
+  launch_continue_prep(cu_seqlens_dev, slot_dev, cache->pos, cache->slots, N, d.C, vcu, rlen, base, hdr, st);
+  launch_worklist(vcu, N, (int)vT, d.C, vchunks, vhash, chunks, seqs, hdr, st);
+  launch_continue_gather(d, in, cu_seqlens_dev, vcu, rlen, slot_dev, N, vT, *cache, vin, hdr, st);
+  stg.mark(3);
+
+  PrepWork pw{};
+  pw.chunks = chunks;
+  pw.n_items = vchunks;
+  launch_prep(d, vin, pw, W, U, gamma, hdr, st);
+  stg.mark(vchunks > 0 ? 1 : 0);
+
+  ChainWork cw{};
+  cw.seqs = seqs;
+  cw.N = N;
+  cw.state_in = cache->s_bnd;
+  cw.state_in_slot = slot_dev;
+  cw.bnd = bnd;
+  cw.state_out = state_out;
+  cw.cache_bnd = cache->s_bnd;
+  cw.cache_run = cache->s_run;
+  cw.cache_slots = cache->slots;
+  cw.slot_of_seq = slot_dev;
+  launch_chain(d, vin.k, W, U, gamma, cw, hdr, st);
+  stg.mark(1);
+
+  IntraWork iw{};
+  iw.chunks = chunks;
+  iw.seqs = seqs;
+  iw.n_chunks = vchunks;
+  iw.bnd = bnd;
+  iw.o = vo;
+  iw.state_out = state_out;
+  iw.cache_run = cache->s_run;
+  iw.cache_slots = cache->slots;
+  iw.slot_of_seq = slot_dev;
+  launch_intra(d, vin, iw, hdr, st);
+  stg.mark(vchunks > 0 ? 1 : 0);
+
+  launch_tail_fill(d, vin, seqs, N, slot_dev, cache->slots, cache->tail_k, cache->tail_v, cache->tail_g,
+                   cache->tail_beta, cache->pos, base, hdr, st);
+  launch_continue_scatter(d, cu_seqlens_dev, vcu, rlen, N, T, vo, o, hdr, st);
+  stg.mark(2);
+  return finish(st);
+}
 
 gdn_status gdn_cpr_get_device_error(const void* ws, gdn_stream_t stream, int32_t* code) {
   if (!ws || !code) return GDN_ERR_INVALID_ARG;

@@ -434,7 +434,9 @@ __global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* ke
     for (int idx = t; idx < R * (D / 4); idx += kChainThreads) {
       const int i = idx / (D / 4), c4 = idx % (D / 4);
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (w.state_in) x = reinterpret_cast<const float4*>(w.state_in + ((int64_t)n * dm.hv + h) * SZ + (int64_t)(r0 + i) * D)[c4];
+      if (w.state_in)
+        x = reinterpret_cast<const float4*>(w.state_in + ((int64_t)(w.state_in_slot ? w.state_in_slot[n] : n) * dm.hv + h) * SZ +
+                                            (int64_t)(r0 + i) * D)[c4];
       *reinterpret_cast<float4*>(Ss + i * DP + 4 * c4) = x;
     }
     __syncthreads();
@@ -612,7 +614,8 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       nchunks = rec.nchunks;
       len = rec.len;
       item0 = rec.chunk0;
-      src = w.state_in ? w.state_in + ((int64_t)n * dm.hv + h) * SZ : nullptr;
+      src = w.state_in ? w.state_in + ((int64_t)(w.state_in_slot ? w.state_in_slot[n] : n) * dm.hv + h) * SZ
+                       : nullptr;
       if (w.cache_bnd) {
         sl = w.slot_of_seq ? w.slot_of_seq[n] : n;
         if (sl < 0 || sl >= w.cache_slots) {
@@ -1272,7 +1275,7 @@ template <typename Tin>
 __global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ seqs,
                             const int32_t* __restrict__ slot_of_seq, int slots, Tin* tail_k,
                             Tin* tail_v, float* tail_g, float* tail_beta, int32_t* pos,
-                            WsHeader* __restrict__ hdr) {
+                            const int32_t* __restrict__ pos_base, WsHeader* __restrict__ hdr) {
   if (!hdr->valid) return;
   const int n = blockIdx.x;
   const SeqRec rec = seqs[n];
@@ -1295,23 +1298,23 @@ __global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ 
     tail_g[(int64_t)sl * C * dm.hv + e] = in.g[base * dm.hv + e];
     tail_beta[(int64_t)sl * C * dm.hv + e] = in.beta[base * dm.hv + e];
   }
-  if (threadIdx.x == 0) pos[sl] = rec.len;
+  if (threadIdx.x == 0) pos[sl] = (pos_base ? pos_base[n] : 0) + rec.len;
 }
 
 void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, int N,
                       const int32_t* slot_of_seq, int slots, void* tail_k, void* tail_v,
-                      float* tail_g, float* tail_beta, int32_t* pos, WsHeader* hdr,
-                      cudaStream_t st) {
+                      float* tail_g, float* tail_beta, int32_t* pos, const int32_t* pos_base,
+                      WsHeader* hdr, cudaStream_t st) {
   if (N <= 0) return;
   if (d.in_bf16)
     k_tail_fill<__nv_bfloat16><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
                                                   static_cast<__nv_bfloat16*>(tail_k),
                                                   static_cast<__nv_bfloat16*>(tail_v), tail_g,
-                                                  tail_beta, pos, hdr);
+                                                  tail_beta, pos, pos_base, hdr);
   else
     k_tail_fill<float><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
                                           static_cast<float*>(tail_k), static_cast<float*>(tail_v),
-                                          tail_g, tail_beta, pos, hdr);
+                                          tail_g, tail_beta, pos, pos_base, hdr);
 }
 
 // ================================================================= dispatch ====
@@ -1388,6 +1391,162 @@ void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, Ws
       GDN_DISPATCH_D(d.D, (launch_decode_t<DD, float, float>(d, in, w, hdr, st)))
     }
   }
+}
+
+
+// =====================================================================  K5  ====
+// Prefill continued from a decode cache (chunked prefill, multi-token decode): sequence s
+// is replayed as a virtual sequence made of its cache tail (the r_s = pos % C tokens since
+// its last chunk boundary; their outputs already exist, so q is zero) followed by its L_s
+// new tokens, from that chunk boundary and the cache's boundary state.  Chunk boundaries of
+// the virtual sequence are those of the whole sequence, so the prefill kernels that run on
+// it give the bits one prefill of the whole sequence gives.
+
+// One block: tail length and base position of every sequence from the device cache, and
+// the virtual cu_seqlens (a fixed-order prefix sum).  A slot or position out of range sets
+// the error word and poisons the virtual total, which the work-list check then rejects.
+__global__ void __launch_bounds__(1024) k_continue_prep(const int32_t* __restrict__ cu,
+                                                        const int32_t* __restrict__ slot,
+                                                        const int32_t* __restrict__ pos, int slots, int N,
+                                                        int C, int32_t* __restrict__ vcu,
+                                                        int32_t* __restrict__ rlen, int32_t* __restrict__ base,
+                                                        WsHeader* __restrict__ hdr) {
+  __shared__ int32_t scan[1024];
+  __shared__ int bad;
+  const int t = threadIdx.x;
+  if (t == 0) bad = 0;
+  __syncthreads();
+  int32_t carry = 0;
+  for (int b0 = 0; b0 < N; b0 += 1024) {
+    const int s = b0 + t;
+    int32_t V = 0;
+    if (s < N) {
+      const int sl = slot[s];
+      int32_t r = 0, p = 0;
+      if (sl < 0 || sl >= slots) {
+        bad = 1;
+        set_error(hdr, GDN_DEVERR_SLOT);
+      } else {
+        p = pos[sl];
+        if (p < 0) {
+          bad = 1;
+          set_error(hdr, GDN_DEVERR_POS);
+          p = 0;
+        } else {
+          r = p % C;
+        }
+      }
+      rlen[s] = r;
+      base[s] = p - r;
+      V = r + (cu[s + 1] - cu[s]);
+    }
+    scan[t] = V;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      const int32_t x = (t >= off) ? scan[t - off] : 0;
+      __syncthreads();
+      scan[t] += x;
+      __syncthreads();
+    }
+    if (s < N) vcu[s + 1] = carry + scan[t];
+    carry += scan[1023];
+    __syncthreads();
+  }
+  if (t == 0) {
+    vcu[0] = 0;
+    if (bad) vcu[N] = -1;
+  }
+}
+
+// index s with cu[s] <= x < cu[s + 1] (cu non-decreasing, cu[0] <= x < cu[n])
+__device__ __forceinline__ int seq_of(const int32_t* __restrict__ cu, int n, int64_t x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// bytes (a multiple of 16) from src to dst, 16 at a time, by the block's threads; src NULL
+// writes zeros
+__device__ __forceinline__ void copy16(void* dst, const void* src, int64_t bytes) {
+  uint4* d = static_cast<uint4*>(dst);
+  const uint4* s = static_cast<const uint4*>(src);
+  for (int64_t e = threadIdx.x; e < bytes / 16; e += blockDim.x) d[e] = s ? s[e] : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// One block per virtual token: its q, k, v, g, beta rows, from the cache tail or the inputs.
+__global__ void k_continue_gather(Dims dm, TokenArrays in, const int32_t* __restrict__ cu,
+                                  const int32_t* __restrict__ vcu, const int32_t* __restrict__ rlen,
+                                  const int32_t* __restrict__ slot, int N, int esz, const void* tail_k,
+                                  const void* tail_v, const float* __restrict__ tail_g,
+                                  const float* __restrict__ tail_beta, TokenArrays out,
+                                  const WsHeader* __restrict__ hdr) {
+  if (!hdr->valid) return;
+  const int64_t vt = blockIdx.x;
+  const int s = seq_of(vcu, N, vt);
+  const int local = (int)(vt - vcu[s]);
+  const int r = rlen[s];
+  const int64_t nq = (int64_t)dm.hqk * dm.D * esz, nv = (int64_t)dm.hv * dm.D * esz;
+  const int64_t ng = (int64_t)dm.hv;
+  char* qo = static_cast<char*>(const_cast<void*>(out.q)) + vt * nq;
+  char* ko = static_cast<char*>(const_cast<void*>(out.k)) + vt * nq;
+  char* vo = static_cast<char*>(const_cast<void*>(out.v)) + vt * nv;
+  float* go = const_cast<float*>(out.g) + vt * ng;
+  float* bo = const_cast<float*>(out.beta) + vt * ng;
+  if (local < r) {
+    const int64_t row = (int64_t)slot[s] * dm.C + local;  // tail row of the slot
+    copy16(qo, nullptr, nq);
+    copy16(ko, static_cast<const char*>(tail_k) + row * nq, nq);
+    copy16(vo, static_cast<const char*>(tail_v) + row * nv, nv);
+    for (int64_t e = threadIdx.x; e < ng; e += blockDim.x) {
+      go[e] = tail_g[row * ng + e];
+      bo[e] = tail_beta[row * ng + e];
+    }
+  } else {
+    const int64_t src = (int64_t)cu[s] + (local - r);
+    copy16(qo, static_cast<const char*>(in.q) + src * nq, nq);
+    copy16(ko, static_cast<const char*>(in.k) + src * nq, nq);
+    copy16(vo, static_cast<const char*>(in.v) + src * nv, nv);
+    for (int64_t e = threadIdx.x; e < ng; e += blockDim.x) {
+      go[e] = in.g[src * ng + e];
+      bo[e] = in.beta[src * ng + e];
+    }
+  }
+}
+
+// One block per new token: its output row from the virtual sequence's output.
+__global__ void k_continue_scatter(const int32_t* __restrict__ cu, const int32_t* __restrict__ vcu,
+                                   const int32_t* __restrict__ rlen, int N, int64_t row_bytes,
+                                   const void* __restrict__ vo, void* __restrict__ o,
+                                   const WsHeader* __restrict__ hdr) {
+  if (!hdr->valid) return;
+  const int64_t tk = blockIdx.x;
+  const int s = seq_of(cu, N, tk);
+  const int64_t vrow = (int64_t)vcu[s] + rlen[s] + (tk - cu[s]);
+  copy16(static_cast<char*>(o) + tk * row_bytes, static_cast<const char*>(vo) + vrow * row_bytes, row_bytes);
+}
+
+void launch_continue_prep(const int32_t* cu, const int32_t* slot, const int32_t* pos, int slots, int N, int C,
+                          int32_t* vcu, int32_t* rlen, int32_t* base, WsHeader* hdr, cudaStream_t st) {
+  if (N > 0) k_continue_prep<<<1, 1024, 0, st>>>(cu, slot, pos, slots, N, C, vcu, rlen, base, hdr);
+}
+
+void launch_continue_gather(const Dims& d, const TokenArrays& in, const int32_t* cu, const int32_t* vcu,
+                            const int32_t* rlen, const int32_t* slot, int N, int64_t vT,
+                            const gdn_cpr_cache& cache, const TokenArrays& out, WsHeader* hdr, cudaStream_t st) {
+  if (vT > 0)
+    k_continue_gather<<<(unsigned)vT, 256, 0, st>>>(d, in, cu, vcu, rlen, slot, N, d.in_bf16 ? 2 : 4,
+                                                    cache.tail_k, cache.tail_v, cache.tail_g, cache.tail_beta,
+                                                    out, hdr);
+}
+
+void launch_continue_scatter(const Dims& d, const int32_t* cu, const int32_t* vcu, const int32_t* rlen, int N,
+                             int64_t T, const void* vo, void* o, WsHeader* hdr, cudaStream_t st) {
+  if (T > 0)
+    k_continue_scatter<<<(unsigned)T, 128, 0, st>>>(cu, vcu, rlen, N, (int64_t)d.hv * d.D * (d.out_bf16 ? 2 : 4),
+                                                    vo, o, hdr);
 }
 
 }  // namespace gdn

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/gdn_cpr.h"
 #include "common.cuh"
 
 namespace gdn {
@@ -62,6 +63,7 @@ struct ChainWork {
   const SeqRec* seqs;  // NULL in decode mode
   int N;
   const float* state_in;
+  const int32_t* state_in_slot;  // state_in row of sequence n is state_in_slot[n] (NULL: n)
   float* bnd;
   float* state_out;
   float* cache_bnd;  // cache s_bnd (prefill with cache) or NULL
@@ -113,11 +115,22 @@ void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, Ws
 void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st);
 
 // Prefill with a cache: copy the last L % C tokens of every sequence to its slot's tail and
-// set pos = L.
+// set pos = L, plus pos_base[n] when given (a continued prefill's chunk-aligned start).
 void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, int N,
                       const int32_t* slot_of_seq, int slots, void* tail_k, void* tail_v,
-                      float* tail_g, float* tail_beta, int32_t* pos, WsHeader* hdr,
-                      cudaStream_t st);
+                      float* tail_g, float* tail_beta, int32_t* pos, const int32_t* pos_base,
+                      WsHeader* hdr, cudaStream_t st);
+
+// K5: prefill continued from a decode cache.  prep: per sequence the cache tail length and
+// base position, and the virtual cu_seqlens (tail + new tokens); gather: the virtual
+// sequences' q, k, v, g, beta; scatter: the new tokens' outputs.
+void launch_continue_prep(const int32_t* cu, const int32_t* slot, const int32_t* pos, int slots, int N, int C,
+                          int32_t* vcu, int32_t* rlen, int32_t* base, WsHeader* hdr, cudaStream_t st);
+void launch_continue_gather(const Dims& d, const TokenArrays& in, const int32_t* cu, const int32_t* vcu,
+                            const int32_t* rlen, const int32_t* slot, int N, int64_t vT,
+                            const gdn_cpr_cache& cache, const TokenArrays& out, WsHeader* hdr, cudaStream_t st);
+void launch_continue_scatter(const Dims& d, const int32_t* cu, const int32_t* vcu, const int32_t* rlen, int N,
+                             int64_t T, const void* vo, void* o, WsHeader* hdr, cudaStream_t st);
 
 // Backward (kernels_bwd.cu).  `mark(ctx, kernels)` is called after each stage (prep,
 // chain, big products, gradients, grouped-head sum) with the kernels it launched.

@@ -91,7 +91,8 @@ typedef enum {
     GDN_MODE_PREFILL = 0, /* gdn_cpr_prefill */
     GDN_MODE_DECODE = 1,  /* gdn_cpr_decode_step */
     GDN_MODE_FWD = 2,     /* gdn_cpr_fwd */
-    GDN_MODE_BWD = 3      /* gdn_cpr_bwd */
+    GDN_MODE_BWD = 3,     /* gdn_cpr_bwd */
+    GDN_MODE_CONTINUE = 4 /* gdn_cpr_prefill_continue (upper bound over cache positions) */
 } gdn_mode;
 
 typedef struct {
@@ -204,6 +205,30 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape *shape, const void *q, const void *k,
                        const float *saved_bnd, const void *dO, const float *dstate_out,
                        float *dq, float *dk, float *dv, float *dg, float *dbeta,
                        float *dstate_in, void *ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* Prefill continued from a decode cache at any position: chunked prefill, and decode of
+ * several tokens per sequence at once (the IsoExec page's CPR section: decode continues the
+ * same recurrence and resynchronises every C tokens; this extends a cached sequence by any
+ * number of tokens with the bits of one prefill of the whole sequence).  Sequence i appends
+ * L_i = cu_seqlens[i+1] - cu_seqlens[i] tokens to cache slot slot_dev[i], whose position
+ * pos_host[i] (host copy of cache->pos[slot_dev[i]]; checked on the device, a mismatch sets
+ * GDN_DEVERR_CU_SEQLENS and nothing runs) may lie inside a chunk.  The r_i = pos_host[i] % C
+ * tokens of the slot's tail are replayed with the new ones from the slot's boundary state,
+ * so that every output and the updated cache are bit-identical to a single gdn_cpr_prefill
+ * of the whole sequence (and to gdn_cpr_decode_step token by token).
+ *   q, k, v, g, beta, o  the new tokens only, laid out as for gdn_cpr_prefill
+ *   slot_dev [N] int32 device, distinct slots; cache  updated in place: s_run, s_bnd, tail,
+ *                        pos += L_i
+ *   state_out            NULL or [N, H_v, d_v, d_k]: the state after the last token
+ *   ws, ws_bytes         gdn_cpr_workspace_size(GDN_MODE_CONTINUE, cu_seqlens_host) bytes
+ * Argument errors (NULL or misaligned pointers, negative positions) are returned; a slot
+ * out of range on the device sets GDN_DEVERR_SLOT.                                        */
+gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape *shape, const void *q, const void *k,
+                                    const void *v, const float *g, const float *beta,
+                                    const int32_t *cu_seqlens_dev, const int32_t *cu_seqlens_host,
+                                    const int32_t *slot_dev, const int32_t *pos_host,
+                                    const gdn_cpr_cache *cache, void *o, float *state_out, void *ws,
+                                    size_t ws_bytes, gdn_stream_t stream);
 
 /* Numerical-policy identity (IsoExec pages, section on the structure of the execution
  * contract, item "Identities": SHA-256 digests by which trainer and rollout engine check
