@@ -442,6 +442,9 @@ def run_cuda(args):
     # 256-slot decode (the decode workload's state shape), graph-replayed and per kernel
     dec = bench_decode_big(api, synth, torch, dev, w, P, seed)
 
+    # prefill continued from a cache: chunked prefill and multi-token decode
+    cont = bench_continue(api, synth, torch, dev, w, seed, stage_ms["prefill"])
+
     # end to end through host buffers: H2D inputs each step, D2H results each step
     e2e = bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call,
                     t, dq_in, o_pre, o_dec, lambda: grads, step_tok, world)
@@ -454,7 +457,8 @@ def run_cuda(args):
                        "l2": "inputs larger than L2 (step working set > 2 GB of HBM traffic)",
                        "bwd_included": have_bwd},
             "stage_ms": stage_ms, "kernel_ms": kern, "roofline": roofline,
-            "boundary_roofline": boundary, "bwd_roofline": bwd_roof, "decode": dec, "e2e": e2e,
+            "boundary_roofline": boundary, "bwd_roofline": bwd_roof, "decode": dec,
+            "continue": cont, "e2e": e2e,
             "gpu_launches": launches, "clocks": clk.summary(),
             "peaks_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -554,6 +558,92 @@ def bench_decode_big(api, synth, torch, dev, w, P, seed):
                          "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                          "traffic": ncu_traffic("k_decode", N * hv),
                          "algorithmic_bytes_per_launch": bytes_k3}}
+
+
+def bench_continue(api, synth, torch, dev, w, seed, prefill_ms):
+    """Prefill continued from a cache: (1) the prefill workload's sequences fed in unaligned
+    pieces after a first prefill (1000 + 1100 + 1000 + 996 tokens), the continued pieces timed;
+    (2) 256 slots extended by 4 tokens per call (multi-token decode).  Both bit-identical to
+    one prefill (tests/test_gpu_continue.py).  The cache is restored between repetitions,
+    outside the timed region."""
+    C, d, hqk, hv = w.chunk, w.d, w.h_qk, w.h_v
+    nseq, L = len(w.lengths), w.lengths[0]
+    cuts = [0, 1000, 2100, 3100, L]
+    x = synth.make_inputs(w.lengths, hqk, hv, d, dtype=w.dtype, seed=seed + 21)
+    cu = x["cu_seqlens"].tolist()
+    names = ("q", "k", "v", "g", "beta")
+
+    def piece(a, b):
+        t = {n: torch.cat([x[n][cu[i] + a:cu[i] + b] for i in range(nseq)]).to(dev) for n in names}
+        return t, synth.cu_seqlens_of([b - a] * nseq)
+
+    cache = api.Cache(nseq, hqk, hv, d, C, dtype=torch.bfloat16, device=dev)
+    slots = torch.arange(nseq, dtype=torch.int32, device=dev)
+    t0, cu0 = piece(0, cuts[1])
+    api.prefill(t0["q"], t0["k"], t0["v"], t0["g"], t0["beta"], cu0.to(dev), chunk=C, cache=cache,
+                slot_of_seq=slots, cu_seqlens_host=cu0)
+    start_state = {n: getattr(cache, n).clone() for n in api.Cache.TENSORS}
+    pieces = [piece(cuts[i], cuts[i + 1]) for i in range(1, len(cuts) - 1)]
+    plans = []
+    for (tp, cup), a in zip(pieces, cuts[1:-1]):
+        shp = api.make_shape(nseq, int(cup[-1]), hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
+        plans.append((tp, cup, cup.to(dev), [a] * nseq,
+                      api.alloc_workspace(api.workspace_bytes(shp, api.MODE_CONTINUE, cup), dev),
+                      torch.empty((int(cup[-1]), hv, d), dtype=torch.bfloat16, device=dev)))
+    times = []
+    for rep in range(4):
+        for n in api.Cache.TENSORS:
+            getattr(cache, n).copy_(start_state[n])
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for tp, cup, cud, pos, ws, o in plans:
+            api.prefill_continue(tp["q"], tp["k"], tp["v"], tp["g"], tp["beta"], cud, slots, cache,
+                                 pos_host=pos, cu_seqlens_host=cup, ws=ws, o=o)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        if rep > 0:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    tok = nseq * (L - cuts[1])
+    # multi-token decode: 256 slots, 4 tokens each per call
+    N, K = DECODE_SLOTS_BIG, 4
+    dc = api.Cache(N, hqk, hv, d, C, dtype=torch.bfloat16, device=dev)
+    gen = torch.Generator(device=dev).manual_seed(seed + 23)
+    dc.s_run.normal_(generator=gen).mul_(0.05)
+    dc.s_bnd.copy_(dc.s_run)
+    dc.tail_k.normal_(generator=gen).mul_(0.09)
+    dc.tail_v.normal_(generator=gen)
+    dc.tail_g.uniform_(-1.5, -0.1, generator=gen)
+    dc.tail_beta.uniform_(0.2, 0.8, generator=gen)
+    dc.pos.fill_(2048 + 30)
+    xd = synth.make_inputs([K] * N, hqk, hv, d, dtype=w.dtype, seed=seed + 25)
+    td = {n: xd[n].to(dev) for n in names}
+    cud = xd["cu_seqlens"]
+    dslots = torch.arange(N, dtype=torch.int32, device=dev)
+    shp = api.make_shape(N, N * K, hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
+    wsd = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_CONTINUE, cud), dev)
+    od = torch.empty((N * K, hv, d), dtype=torch.bfloat16, device=dev)
+    saved = {n: getattr(dc, n).clone() for n in api.Cache.TENSORS}
+    dt = []
+    for rep in range(6):
+        for n in api.Cache.TENSORS:
+            getattr(dc, n).copy_(saved[n])
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.prefill_continue(td["q"], td["k"], td["v"], td["g"], td["beta"], cud.to(dev), dslots, dc,
+                             pos_host=[2048 + 30] * N, cu_seqlens_host=cud, ws=wsd, o=od)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        if rep > 0:
+            dt.append(e0.elapsed_time(e1))
+    us = statistics.median(dt) * 1e3
+    return {"chunked_prefill": {"pieces": [b - a for a, b in zip(cuts[1:-1], cuts[2:])], "sequences": nseq,
+                                "tokens": tok, "ms": ms, "tokens_per_s": tok / (ms * 1e-3),
+                                "one_shot_prefill_tokens_per_s": nseq * L / (prefill_ms * 1e-3)},
+            "multi_token_decode": {"slots": N, "tokens_per_slot": K, "pos_mod_C": 30,
+                                   "us_per_call": us, "tokens_per_s": N * K / (us * 1e-6)}}
 
 
 def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call, t, dq_in,

@@ -541,6 +541,21 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   launch_prep(d, vin, pw, W, U, gamma, hdr, st);
   stg.mark(vchunks > 0 ? 1 : 0);
 
+  IntraWork iw{};
+  iw.chunks = chunks;
+  iw.seqs = seqs;
+  iw.n_chunks = vchunks;
+  iw.bnd = bnd;
+  iw.o = vo;
+  iw.state_out = state_out;
+  iw.cache_run = cache->s_run;
+  iw.cache_slots = cache->slots;
+  iw.slot_of_seq = slot_dev;
+  iw.skip = rlen;  // the tail is already in the cache's running state
+  iw.run_state = cache->s_run;
+  iw.run_slot = slot_dev;
+  iw.part = 1;  // chunks that start from the cache's running state, before anything writes it
+  launch_intra(d, vin, iw, hdr, st);
   ChainWork cw{};
   cw.seqs = seqs;
   cw.N = N;
@@ -552,19 +567,12 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   cw.cache_run = cache->s_run;
   cw.cache_slots = cache->slots;
   cw.slot_of_seq = slot_dev;
+  cw.bnd_in_place = true;
+  cw.bnd_skip = rlen;
   launch_chain(d, vin.k, W, U, gamma, cw, hdr, st);
-  stg.mark(1);
+  stg.mark(vchunks > 0 ? 2 : 1);  // intra part 1 and the chain
 
-  IntraWork iw{};
-  iw.chunks = chunks;
-  iw.seqs = seqs;
-  iw.n_chunks = vchunks;
-  iw.bnd = bnd;
-  iw.o = vo;
-  iw.state_out = state_out;
-  iw.cache_run = cache->s_run;
-  iw.cache_slots = cache->slots;
-  iw.slot_of_seq = slot_dev;
+  iw.part = 2;
   launch_intra(d, vin, iw, hdr, st);
   stg.mark(vchunks > 0 ? 1 : 0);
 

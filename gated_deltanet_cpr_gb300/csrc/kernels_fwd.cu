@@ -632,15 +632,21 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       item0 = n;
       src = w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ;
     }
+    // continued prefill: S^(0) already in place in the cache, and not needed in bnd when
+    // the first chunk starts from the running state
+    const bool skip0 = w.seqs && w.bnd_skip && w.bnd_skip[n] > 0;
+    if (w.seqs && nfull == 0 && skip0 && w.bnd_in_place && len % C != 0) continue;  // nothing to write
     // outputs for the state after full chunk j (j = 0 .. nfull): rows of S^(j)
     auto write_state = [&](int j, const float* v, int c0) {
       if (w.seqs) {
-        if (j < nchunks) store_row16(w.bnd + ((item0 + j) * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+        if (j < nchunks && !(j == 0 && skip0))
+          store_row16(w.bnd + ((item0 + j) * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
         if (j == nfull) {
           if (len % C == 0 && w.state_out)
             store_row16(w.state_out + ((int64_t)n * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
           if (sl >= 0) {
-            store_row16(w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
+            if (!(j == 0 && w.bnd_in_place))
+              store_row16(w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
             if (len % C == 0)
               store_row16(w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
           }
@@ -1107,7 +1113,7 @@ constexpr size_t intra_smem_bytes() {
   return sizeof(float) * (3 * kMaxChunk * D + 2 * kMaxChunk);
 }
 
-template <int D, typename Tin, typename Tout>
+template <int D, typename Tin, typename Tout, bool kSkip>
 __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, IntraWork w,
                                                  WsHeader* __restrict__ hdr) {
   extern __shared__ __align__(16) float sm[];
@@ -1122,6 +1128,10 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const int h = blockIdx.y;
   const int hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = w.chunks[c];
+  if constexpr (kSkip) {  // this launch's part of the chunks
+    const bool from_run = rec.jloc == 0 && w.skip[rec.seq] > 0;
+    if (from_run != (w.part == 1)) return;
+  }
   const int len = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t SZ = (int64_t)D * D;
@@ -1142,11 +1152,18 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const int i = t >> 1, half = t & 1;
   float4 S[D / 8];
   const float* src = w.bnd + (c * dm.hv + h) * SZ + (int64_t)i * D;
+  int first = 0;  // first token of the recurrence in this chunk (continued prefill only)
+  if constexpr (kSkip) {
+    if (rec.jloc == 0 && w.skip[rec.seq] > 0) {
+      first = w.skip[rec.seq];
+      src = w.run_state + ((int64_t)w.run_slot[rec.seq] * dm.hv + h) * SZ + (int64_t)i * D;
+    }
+  }
 #pragma unroll
   for (int m = 0; m < D / 8; ++m) S[m] = *reinterpret_cast<const float4*>(src + state_col<D>(m, half));
   __syncthreads();
 
-  for (int tt = 0; tt < len; ++tt) {
+  for (int tt = first; tt < len; ++tt) {
     const float o = token_step<D>(S, ks + tt * D, qs + tt * D, as[tt], bs[tt], vs[tt * D + i], half);
     __syncwarp();
     if (half == 0) vs[tt * D + i] = o;
@@ -1159,7 +1176,7 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   rc.len = __ldcg(&w.chunks[c].len);
   rc.jloc = __ldcg(&w.chunks[c].jloc);
   Tout* out = static_cast<Tout*>(w.o);
-  for (int idx = t; idx < rc.len * D; idx += 2 * D) {
+  for (int idx = first * D + t; idx < rc.len * D; idx += 2 * D) {
     const int r = idx / D, e = idx % D;
     store_out(out + (((int64_t)rc.tok0 + r) * dm.hv + h) * D + e, vs[idx]);
   }
@@ -1186,9 +1203,14 @@ template <int D, typename Tin, typename Tout>
 static void launch_intra_t(const Dims& d, const TokenArrays& in, const IntraWork& w, WsHeader* hdr,
                            cudaStream_t st) {
   constexpr size_t smem = intra_smem_bytes<D>();
-  ensure_smem(k_intra<D, Tin, Tout>, smem);
   dim3 grid((unsigned)w.n_chunks, d.hv);
-  k_intra<D, Tin, Tout><<<grid, 2 * D, smem, st>>>(d, in, w, hdr);
+  if (w.skip) {
+    ensure_smem(k_intra<D, Tin, Tout, true>, smem);
+    k_intra<D, Tin, Tout, true><<<grid, 2 * D, smem, st>>>(d, in, w, hdr);
+  } else {
+    ensure_smem(k_intra<D, Tin, Tout, false>, smem);
+    k_intra<D, Tin, Tout, false><<<grid, 2 * D, smem, st>>>(d, in, w, hdr);
+  }
 }
 
 // =====================================================================  K3  ====

@@ -70,6 +70,11 @@ struct ChainWork {
   float* cache_run;  // cache s_run (prefill with cache, written when L % C == 0) or NULL
   const int32_t* slot_of_seq;
   int cache_slots;
+  // continued prefill: state_in is cache_bnd under the same slot map (S^(0) need not be
+  // written back), and a sequence with bnd_skip[n] > 0 starts its first chunk from the
+  // cache's running state (S^(0) is not needed in bnd)
+  bool bnd_in_place;
+  const int32_t* bnd_skip;
   // decode
   const int32_t* slot;
   const int32_t* pos;
@@ -91,6 +96,16 @@ struct IntraWork {
   float* cache_run;
   const int32_t* slot_of_seq;
   int cache_slots;
+  // continued prefill: the first skip[seq] tokens of a sequence's first chunk are already in
+  // run_state[run_slot[seq]] (the cache's running state), so that chunk's recurrence starts
+  // there, from token skip[seq]; NULL otherwise
+  const int32_t* skip;
+  const float* run_state;
+  const int32_t* run_slot;
+  // with skip: 1 = only the chunks that start from run_state, 2 = all other chunks.  The
+  // continued prefill launches part 1 before the boundary chain and part 2 after it, so
+  // that every read of the cache's running state precedes every write to it.
+  int part;
 };
 void launch_intra(const Dims& d, const TokenArrays& in, const IntraWork& w, WsHeader* hdr,
                   cudaStream_t st);
