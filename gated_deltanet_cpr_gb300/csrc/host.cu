@@ -287,7 +287,7 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
 
   if (cache) {
     launch_tail_fill(d, in, seqs, N, slot_of_seq, cache->slots, cache->tail_k, cache->tail_v,
-                     cache->tail_g, cache->tail_beta, cache->pos, nullptr, hdr, st);
+                     cache->tail_g, cache->tail_beta, cache->pos, nullptr, nullptr, hdr, st);
     stg.mark(1);
   }
   return finish(st);
@@ -577,7 +577,7 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   stg.mark(vchunks > 0 ? 1 : 0);
 
   launch_tail_fill(d, vin, seqs, N, slot_dev, cache->slots, cache->tail_k, cache->tail_v, cache->tail_g,
-                   cache->tail_beta, cache->pos, base, hdr, st);
+                   cache->tail_beta, cache->pos, base, rlen, hdr, st);
   launch_continue_scatter(d, cu_seqlens_dev, vcu, rlen, N, T, vo, o, hdr, st);
   stg.mark(2);
   return finish(st);

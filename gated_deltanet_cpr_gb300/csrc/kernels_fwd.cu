@@ -573,6 +573,10 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       if (!w.seqs) {
         const int sl = w.slot[wi / dm.hv];
         work = sl >= 0 && sl < w.slots && w.pos[sl] >= 0 && (w.pos[sl] + 1) % C == 0;
+      } else if (w.bnd_in_place && w.bnd_skip) {  // continued prefill: see the item loop
+        const int n2 = (int)(wi / dm.hv);
+        const int len2 = w.seqs[n2].len;
+        work = !(len2 < C && w.bnd_skip[n2] > 0);
       }
       if (work) s_list[atomicAdd(&s_cnt, 1)] = wi;
     }
@@ -1139,25 +1143,27 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const Tin* kin = static_cast<const Tin*>(in.k);
   const Tin* vin = static_cast<const Tin*>(in.v);
 
-  for (int idx = t; idx < len * (D / 4); idx += 2 * D) {
+  // first token of the recurrence in this chunk: a continued prefill resumes its first chunk
+  // from the cache's running state after the tail tokens it already holds
+  int first = 0;
+  if constexpr (kSkip) {
+    if (rec.jloc == 0) first = w.skip[rec.seq];
+  }
+  for (int idx = first * (D / 4) + t; idx < len * (D / 4); idx += 2 * D) {
     const int r = idx / (D / 4), c4 = idx % (D / 4);
     *reinterpret_cast<float4*>(ks + r * D + 4 * c4) = load4(kin + ((tok0 + r) * dm.hqk + hq) * D + 4 * c4);
     *reinterpret_cast<float4*>(qs + r * D + 4 * c4) = load4(qin + ((tok0 + r) * dm.hqk + hq) * D + 4 * c4);
     *reinterpret_cast<float4*>(vs + r * D + 4 * c4) = load4(vin + ((tok0 + r) * dm.hv + h) * D + 4 * c4);
   }
-  for (int r = t; r < len; r += 2 * D) {
+  for (int r = first + t; r < len; r += 2 * D) {
     as[r] = expf(in.g[(tok0 + r) * dm.hv + h]);
     bs[r] = in.beta[(tok0 + r) * dm.hv + h];
   }
   const int i = t >> 1, half = t & 1;
   float4 S[D / 8];
   const float* src = w.bnd + (c * dm.hv + h) * SZ + (int64_t)i * D;
-  int first = 0;  // first token of the recurrence in this chunk (continued prefill only)
   if constexpr (kSkip) {
-    if (rec.jloc == 0 && w.skip[rec.seq] > 0) {
-      first = w.skip[rec.seq];
-      src = w.run_state + ((int64_t)w.run_slot[rec.seq] * dm.hv + h) * SZ + (int64_t)i * D;
-    }
+    if (first > 0) src = w.run_state + ((int64_t)w.run_slot[rec.seq] * dm.hv + h) * SZ + (int64_t)i * D;
   }
 #pragma unroll
   for (int m = 0; m < D / 8; ++m) S[m] = *reinterpret_cast<const float4*>(src + state_col<D>(m, half));
@@ -1297,7 +1303,8 @@ template <typename Tin>
 __global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ seqs,
                             const int32_t* __restrict__ slot_of_seq, int slots, Tin* tail_k,
                             Tin* tail_v, float* tail_g, float* tail_beta, int32_t* pos,
-                            const int32_t* __restrict__ pos_base, WsHeader* __restrict__ hdr) {
+                            const int32_t* __restrict__ pos_base, const int32_t* __restrict__ keep_rows,
+                            WsHeader* __restrict__ hdr) {
   if (!hdr->valid) return;
   const int n = blockIdx.x;
   const SeqRec rec = seqs[n];
@@ -1308,15 +1315,17 @@ __global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ 
   }
   const int C = dm.C, D = dm.D;
   const int nt = rec.len % C;
+  // rows the slot's tail already holds (continued prefill whose chunk stays open)
+  const int k0 = (keep_rows && rec.len < C) ? keep_rows[n] : 0;
   const int64_t base = (int64_t)rec.tok0 + rec.len - nt;
   const Tin* kin = static_cast<const Tin*>(in.k);
   const Tin* vin = static_cast<const Tin*>(in.v);
   const int64_t nk = (int64_t)nt * dm.hqk * D, nv = (int64_t)nt * dm.hv * D, ng = (int64_t)nt * dm.hv;
-  for (int64_t e = threadIdx.x; e < nk; e += blockDim.x)
+  for (int64_t e = (int64_t)k0 * dm.hqk * D + threadIdx.x; e < nk; e += blockDim.x)
     tail_k[(int64_t)sl * C * dm.hqk * D + e] = kin[base * dm.hqk * D + e];
-  for (int64_t e = threadIdx.x; e < nv; e += blockDim.x)
+  for (int64_t e = (int64_t)k0 * dm.hv * D + threadIdx.x; e < nv; e += blockDim.x)
     tail_v[(int64_t)sl * C * dm.hv * D + e] = vin[base * dm.hv * D + e];
-  for (int64_t e = threadIdx.x; e < ng; e += blockDim.x) {
+  for (int64_t e = (int64_t)k0 * dm.hv + threadIdx.x; e < ng; e += blockDim.x) {
     tail_g[(int64_t)sl * C * dm.hv + e] = in.g[base * dm.hv + e];
     tail_beta[(int64_t)sl * C * dm.hv + e] = in.beta[base * dm.hv + e];
   }
@@ -1326,17 +1335,17 @@ __global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ 
 void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, int N,
                       const int32_t* slot_of_seq, int slots, void* tail_k, void* tail_v,
                       float* tail_g, float* tail_beta, int32_t* pos, const int32_t* pos_base,
-                      WsHeader* hdr, cudaStream_t st) {
+                      const int32_t* keep_rows, WsHeader* hdr, cudaStream_t st) {
   if (N <= 0) return;
   if (d.in_bf16)
     k_tail_fill<__nv_bfloat16><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
                                                   static_cast<__nv_bfloat16*>(tail_k),
                                                   static_cast<__nv_bfloat16*>(tail_v), tail_g,
-                                                  tail_beta, pos, pos_base, hdr);
+                                                  tail_beta, pos, pos_base, keep_rows, hdr);
   else
     k_tail_fill<float><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
                                           static_cast<float*>(tail_k), static_cast<float*>(tail_v),
-                                          tail_g, tail_beta, pos, pos_base, hdr);
+                                          tail_g, tail_beta, pos, pos_base, keep_rows, hdr);
 }
 
 // ================================================================= dispatch ====
@@ -1510,6 +1519,9 @@ __global__ void k_continue_gather(Dims dm, TokenArrays in, const int32_t* __rest
   const int s = seq_of(vcu, N, vt);
   const int local = (int)(vt - vcu[s]);
   const int r = rlen[s];
+  // a tail token is read only by the pre-pass of a completed first chunk (the recurrence
+  // resumes after the tail, and the cache keeps its tail rows when the chunk stays open)
+  if (local < r && vcu[s + 1] - vcu[s] < dm.C) return;
   const int64_t nq = (int64_t)dm.hqk * dm.D * esz, nv = (int64_t)dm.hv * dm.D * esz;
   const int64_t ng = (int64_t)dm.hv;
   char* qo = static_cast<char*>(const_cast<void*>(out.q)) + vt * nq;

@@ -130,11 +130,12 @@ void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, Ws
 void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st);
 
 // Prefill with a cache: copy the last L % C tokens of every sequence to its slot's tail and
-// set pos = L, plus pos_base[n] when given (a continued prefill's chunk-aligned start).
+// set pos = L, plus pos_base[n] when given (a continued prefill's chunk-aligned start); with
+// keep_rows, a sequence shorter than C leaves its first keep_rows[n] tail rows as they are.
 void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, int N,
                       const int32_t* slot_of_seq, int slots, void* tail_k, void* tail_v,
                       float* tail_g, float* tail_beta, int32_t* pos, const int32_t* pos_base,
-                      WsHeader* hdr, cudaStream_t st);
+                      const int32_t* keep_rows, WsHeader* hdr, cudaStream_t st);
 
 // K5: prefill continued from a decode cache.  prep: per sequence the cache tail length and
 // base position, and the virtual cu_seqlens (tail + new tokens); gather: the virtual
