@@ -1740,7 +1740,7 @@ constexpr uint32_t P2_PM = 0, P2_PMT = 16 * KB, P2_TT = 32 * KB, P2_DU = 48 * KB
 constexpr uint32_t P3_Y = 0, P3_X = 32 * KB, P3_W = 64 * KB, P3_UT = 96 * KB;
 constexpr uint32_t P4_AM = 0, P4_AMT = 16 * KB;
 constexpr uint32_t MAT = C * MP * 4;
-constexpr size_t SMEM = ARENA + 3 * (size_t)MAT + 16 * C * 4 + 64;
+constexpr size_t SMEM = ARENA + 3 * (size_t)MAT + 17 * C * 4 + 64;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_PM = 0, COL_QK = 64, COL_AP = 128, COL_DQ = 0, COL_DK = 128, COL_X = 256,
                    COL_Y = 384, COL_DA = 0;
@@ -1766,7 +1766,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
   float* dGe = dGb + C;
   float* dbc = dGe + C;
   float* dgv = dbc + C;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(dgv + C);
+  float* csv = dgv + C;  // per token dec * (U dS_end . k)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(csv + C);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
@@ -2112,21 +2113,30 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
       set_error(a.hdr, GDN_DEVERR_TIMEOUT);
       mbar_wait(bar, phase);
     }
-  } else if (t == 0) {  // dG, reverse cumulative sum -> dg
+  }
+  // dG per token (independent terms, one thread each), then thread 0 takes the two
+  // sequential sums: the total of the U dS_end terms and the reverse cumulative sum -> dg
+  if (ok && t < C) {
+    const int i = t;
+    const float csi = __fmul_rn(dec[i], __fadd_rn(cs[i], cs[C + i]));
+    const float ga = __fmul_rn(eG[i], __fadd_rn(dGa[i], dGa[C + i]));
+    const float ky = __fadd_rn(kY[i], kY[C + i]);
+    float v = __fadd_rn(ga, dGb[i]);
+    v = __fsub_rn(v, csi);
+    v = __fmaf_rn(__fmul_rn(bs[i], eG[i]), ky, v);
+    v = __fadd_rn(v, dGe[i]);
+    dgv[i] = v;
+    csv[i] = csi;
+  }
+  __syncthreads();
+  if (ok && t == 0) {
     float tot = 0.f;
-    for (int s2 = 0; s2 < C; ++s2) {
-      const float v = __fmul_rn(dec[s2], __fadd_rn(cs[s2], cs[C + s2]));
-      cs[s2] = v;
-      tot = __fadd_rn(tot, v);
-    }
+#pragma unroll
+    for (int s2 = 0; s2 < C; ++s2) tot = __fadd_rn(tot, csv[s2]);
     float run = 0.f;
+#pragma unroll
     for (int i = C - 1; i >= 0; --i) {
-      const float ga = __fmul_rn(eG[i], __fadd_rn(dGa[i], dGa[C + i]));
-      const float ky = __fadd_rn(kY[i], kY[C + i]);
-      float v = __fadd_rn(ga, dGb[i]);
-      v = __fsub_rn(v, cs[i]);
-      v = __fmaf_rn(__fmul_rn(bs[i], eG[i]), ky, v);
-      v = __fadd_rn(v, dGe[i]);
+      float v = dgv[i];
       if (i == C - 1) v = __fadd_rn(v, __fmaf_rn(expf(Gs[C - 1]), a.b.sdot[ch], tot));
       run = __fadd_rn(run, v);
       dgv[i] = run;

@@ -660,6 +660,24 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
         store_row16(w.s_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)row * D + c0, v);
       }
     };
+    // the same outputs for one float4 of state row r2, columns c2 .. c2 + 3
+    auto write_state4 = [&](int j, int r2, int c2, float4 x) {
+      const int64_t o = (int64_t)r2 * D + c2;
+      auto put = [&](float* base) { *reinterpret_cast<float4*>(base + o) = x; };
+      if (w.seqs) {
+        if (j < nchunks && !(j == 0 && skip0)) put(w.bnd + ((item0 + j) * dm.hv + h) * SZ);
+        if (j == nfull) {
+          if (len % C == 0 && w.state_out) put(w.state_out + ((int64_t)n * dm.hv + h) * SZ);
+          if (sl >= 0) {
+            if (!(j == 0 && w.bnd_in_place)) put(w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ);
+            if (len % C == 0) put(w.cache_run + ((int64_t)sl * dm.hv + h) * SZ);
+          }
+        }
+      } else if (j > 0) {
+        put(w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ);
+        put(w.s_run + ((int64_t)sl * dm.hv + h) * SZ);
+      }
+    };
     // this thread's half row of S^(0), all loads in flight at once
     float4 s0v[D / 8];
 #pragma unroll
@@ -784,10 +802,23 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       {  // S^(j+1): outputs, next step's A operand and gamma_{j+1} S^(j+1)
         const bool more = j + 1 < nfull;
         const float gn = more ? gamma[(item + 1) * dm.hv + h] : 0.f;
+        // S^(j+1) leaves through a per-warp staging tile in the (now free) Vd^T operand
+        // region, so that each store instruction writes 8 rows x 64 contiguous bytes
+        float* tile = reinterpret_cast<float*>(A2h) + warp * (32 * 20);
+        const int lane = t & 31, rq = (warp & 3) * 32;
         for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
           float v[16];
           tmem_ld16(tlane + D2_COL + c0, v);
-          write_state(j + 1, v, c0);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            *reinterpret_cast<float4*>(tile + lane * 20 + 4 * x) = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const int rl = 8 * k2 + (lane >> 2), f = lane & 3;
+            write_state4(j + 1, rq + rl, c0 + 4 * f, *reinterpret_cast<const float4*>(tile + rl * 20 + 4 * f));
+          }
+          __syncwarp();
           if (more) {
             store_split16(A1h, A1l, row, c0, D, v);
 #pragma unroll
