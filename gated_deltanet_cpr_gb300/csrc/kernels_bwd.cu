@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(NT) k_bwd_prep(BwdArgs a) {
   if (t == 0) {
     float run = gs[0];
     Gs[0] = run;
+#pragma unroll 8
     for (int i = 1; i < C; ++i) {
       run = __fadd_rn(run, gs[i]);
       Gs[i] = run;
@@ -999,14 +1000,17 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
 //   phase 3  A = E^T    : (U E)^T  = E^T U^T
 //   phase 4  A = S0^T   : (dO S0)^T = S0^T dO^T,   dW^T = -S0^T dU^T
 // fp32 operands are split into bf16 hi + lo (three MMAs per product, lo x lo dropped);
-// bf16 inputs are exact.  Results go to the same global arrays as the SIMT kernel.
+// bf16 inputs are exact.  Results go to the same global arrays as the SIMT kernel.  Sized
+// for two CTAs per SM (one A and one B operand image, 128 TMEM columns, 128 registers), so
+// that one CTA's loads and waits overlap the other's work: the two products of phase 2 and
+// of phase 4 run one after the other, and the 128 x 128 images are built in halves.
 namespace tcg {
 constexpr int D = 128, C = 64;
 constexpr uint32_t RA = 2 * 128 * D * 2;       // A operand hi | lo (64 KB)
-constexpr uint32_t RB = 2 * C * D * 2;         // B region (32 KB)
-constexpr size_t SMEM = (size_t)RA + 2 * (size_t)RB + C * 4 + 256 * 4 + 64;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_U = 0, COL_E = 64, COL_DOP = 128, COL_UE = 192, COL_DOS = 256, COL_DW = 320;
+constexpr uint32_t RB = 2 * C * D * 2;         // B operand hi | lo (32 KB)
+constexpr size_t SMEM = (size_t)RA + (size_t)RB + C * 4 + 256 * 4 + 64;  // two CTAs per SM
+constexpr uint32_t TMEM_COLS = 128;
+constexpr uint32_t COL_0 = 0, COL_1 = 64;      // at most two 128 x 64 results alive
 }  // namespace tcg
 
 // 8 fp32 values -> hi / lo bf16 16-byte pieces at byte offset `off` of the two images
@@ -1146,6 +1150,18 @@ __device__ __forceinline__ void load_dO_rows(float (&v)[4][8], const void* dO, b
     load_dO_rows_t(v, static_cast<const float*>(dO) + base, tstride, n);
 }
 
+// 128 x 128 image pair of a row-major fp32 d x d matrix (TRANS: of its transpose), built in
+// two 64-row halves so that a thread holds 32 values at a time
+template <bool TRANS>
+__device__ __forceinline__ void build_dd(unsigned char* hi, unsigned char* lo, const float* src) {
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    SplitTile<TRANS, 64, 128> tile;
+    tile.load(TRANS ? src + hh * 64 : src + hh * 64 * 128, 128, TRANS ? 128 : 64);
+    tile.store(hi + hh * 16384, lo + hh * 16384);
+  }
+}
+
 // D = A B^T over K with split operands: terms = 3 gives A_hi B_hi + A_hi B_lo + A_lo B_hi;
 // terms = 2 (B exact, blo ignored) gives A_hi B + A_lo B; `accumulate` adds onto D.
 __device__ __forceinline__ void mma_terms(uint32_t d, uint32_t ahi, uint32_t alo, uint32_t bhi, uint32_t blo,
@@ -1160,16 +1176,15 @@ __device__ __forceinline__ void mma_terms(uint32_t d, uint32_t ahi, uint32_t alo
   }
 }
 
-__global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
+__global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   using namespace tcg;
   using namespace tc;
   extern __shared__ __align__(128) unsigned char smg[];
-  unsigned char* Ah = smg;
+  unsigned char* Ah = smg;            // A operand: 128 x 128 (d x d) or 128 x 64 (dO^T)
   unsigned char* Al = Ah + RA / 2;
-  unsigned char* B1h = smg + RA;
-  unsigned char* B1l = B1h + RB / 2;
-  unsigned char* B2 = B1h + RB;
-  float* dec = reinterpret_cast<float*>(B2 + RB);
+  unsigned char* Bh = smg + RA;       // B operand: 64 x 128 or 64 x 64 (P^T)
+  unsigned char* Bl = Bh + RB / 2;
+  float* dec = reinterpret_cast<float*>(Bh + RB);
   float* red = dec + C;
   uint64_t* bar = reinterpret_cast<uint64_t*>(red + 256);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
@@ -1187,6 +1202,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
   const float* E = a.b.dSE + ch * SZ;
   const int lane_row = (warp & 3) * 32 + (t & 31);  // TMEM lane = row of the transposed result
   const int cbase = (warp >> 2) * 32;               // this warp's 32 result columns
+  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + (tok0 * dm.hqk + hq) * D;
   if (t < C) dec[t] = expf(__fsub_rn(a.b.G[ch * C + C - 1], a.b.G[ch * C + t]));
   if (t == 0) {
     mbar_init(bar, 1);
@@ -1199,183 +1215,176 @@ __global__ void __launch_bounds__(256, 1) k_bwd_big_tc(BwdArgs a) {
   const uint32_t tb = *tslot;
   const uint32_t tl = tmem_lane_addr(tb, warp, 0);
   uint32_t phase = 0;
-  bool ok = true;
+  bool ok = true, pending = false;
   auto run = [&]() {  // all threads: wait for the committed MMAs
     const bool done = mbar_wait(bar, phase);
-    if (done) phase ^= 1u;
+    if (done) {
+      phase ^= 1u;
+      pending = false;
+    }
     ok = __syncthreads_and(done) != 0;
     fence_after_sync();
   };
-  auto issue_begin = [&]() {
+  auto issue = [&](auto&& mmas) {  // operands written -> one thread issues and commits
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
+    if (t == 0) {
+      fence_after_sync();
+      mmas();
+      mma_commit(bar);
+    }
+    pending = true;
   };
+  const uint32_t sa_h = smem_u32(Ah), sa_l = smem_u32(Al), sb_h = smem_u32(Bh), sb_l = smem_u32(Bl);
 
-  // ---- phase 1: U^T = Ut^T - S0 W^T; <E, S0> from the same loads (thread t sums its own
-  // pieces in order, then a fixed tree over the threads)
+  // ---- phase 1: U^T = Ut^T - S0 W^T
+  build_dd<false>(Ah, Al, S0);
+  build_split<false, C, D>(Bh, Bl, a.b.W + ch * CD, D, C);
+  issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
   {
-    SplitTile<false, 128, D> s0t, et;
-    s0t.load(S0, D, 128);
-    et.load(E, D, 128);
-    float part = 0.f;
+    float ut[32];  // Ut for the readout, loaded while the product runs
 #pragma unroll
-    for (int it = 0; it < SplitTile<false, 128, D>::ITER; ++it)
+    for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
+    run();
+    if (ok) {  // U = Ut - (U^T)^T
 #pragma unroll
-      for (int e = 0; e < 8; ++e) part = __fmaf_rn(et.v[it][e], s0t.v[it][e], part);
-    red[t] = part;
-    s0t.store(Ah, Al);
-  }
-  build_split<false, C, D>(B1h, B1l, a.b.W + ch * CD, D, C);
-  issue_begin();
-  if (t == 0) {
-    fence_after_sync();
-    mma_terms(tb + COL_U, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
-    mma_commit(bar);
-  }
-  float ut[32];  // Ut for the readout, loaded while the product runs
+      for (int s1 = 0; s1 < 2; ++s1) {
+        float v[16];
+        tmem_ld16(tl + COL_0 + cbase + 16 * s1, v);
 #pragma unroll
-  for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
-  run();
-  if (ok) {  // U = Ut - (U^T)^T
-#pragma unroll
-    for (int s1 = 0; s1 < 2; ++s1) {
-      float v[16];
-      tmem_ld16(tl + COL_U + cbase + 16 * s1, v);
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        a.b.U[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = __fsub_rn(ut[16 * s1 + e], v[e]);
+        for (int e = 0; e < 16; ++e)
+          a.b.U[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = __fsub_rn(ut[16 * s1 + e], v[e]);
+      }
     }
   }
   fence_before_sync();
   __syncthreads();
+
+  // ---- phase 2: E K^T, then dO^T P (the A region is reused); <E, S0> from the E build
+  if (ok) {
+    float part = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {  // E image by halves, with S0 at the same positions
+      SplitTile<false, 64, D> et, st;
+      et.load(E + hh * 64 * D, D, 64);
+      st.load(S0 + hh * 64 * D, D, 64);
+#pragma unroll
+      for (int it = 0; it < SplitTile<false, 64, D>::ITER; ++it)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part = __fmaf_rn(et.v[it][e], st.v[it][e], part);
+      et.store(Ah + hh * 16384, Al + hh * 16384);
+    }
+    red[t] = part;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {  // K rows (exact in bf16, rows >= n zero)
+      int r, k0;
+      kmajor_piece(t + it * 256, D, r, k0);
+      *reinterpret_cast<uint4*>(Bh + kmajor_off(r, k0, D)) =
+          r < n ? *reinterpret_cast<const uint4*>(kb + (int64_t)r * dm.hqk * D + k0) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_h, D, idesc_bf16(128, C), 2); });
+  }
+  {
+    // dO^T (rows a, K = i) and P^T (rows s, K = i) loaded while E K^T runs
+    SplitTile<true, C, C> pt;
+    pt.load(a.b.P + ch * C * C, C, C);
+    float v[4][8];
+    load_dO_T(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+    if (ok) run();
+    if (ok) {
+      pt.store(Bh, Bh + C * C * 2);
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
+        split8(Ah, Ah + 128 * C * 2, kmajor_off(r, k0, C), v[it]);
+      }
+      issue([&] {
+        mma_terms(tb + COL_1, sa_h, sa_h + 128 * C * 2, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C), 3);
+      });
+      run();
+    }
+  }
   for (int w2 = 128; w2 > 0; w2 >>= 1) {
     if (t < w2) red[t] = __fadd_rn(red[t], red[t + w2]);
     __syncthreads();
   }
   if (t == 0) a.b.sdot[ch] = red[0];
-
-  // ---- phase 2: E K^T and dO^T P
-  if (ok) {
-    {  // E (split) and K rows (exact in bf16, rows >= n zero): loads first
-      const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + (tok0 * dm.hqk + hq) * D;
-      SplitTile<false, 128, D> et;
-      et.load(E, D, 128);
-      uint4 kr[4];
+  if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec)
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        int r, k0;
-        kmajor_piece(t + it * 256, D, r, k0);
-        kr[it] = r < n ? *reinterpret_cast<const uint4*>(kb + (int64_t)r * dm.hqk * D + k0) : make_uint4(0u, 0u, 0u, 0u);
-      }
-      et.store(Ah, Al);
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        int r, k0;
-        kmajor_piece(t + it * 256, D, r, k0);
-        *reinterpret_cast<uint4*>(B2 + kmajor_off(r, k0, D)) = kr[it];
-      }
-    }
-    // P^T (rows s, K = i) into the second half of B2; dO^T (rows a, K = i) into B1
-    SplitTile<true, C, C> pt;
-    pt.load(a.b.P + ch * C * C, C, C);
-    {
-      float v[4][8];
-      load_dO_T(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
-      pt.store(B2 + C * D * 2, B2 + C * D * 2 + C * C * 2);
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
-        split8(B1h, B1h + 128 * C * 2, kmajor_off(r, k0, C), v[it]);
-      }
-    }
-    issue_begin();
-    if (t == 0) {
-      fence_after_sync();
-      mma_terms(tb + COL_E, smem_u32(Ah), smem_u32(Al), smem_u32(B2), smem_u32(B2), D, idesc_bf16(128, C), 2);
-      mma_terms(tb + COL_DOP, smem_u32(B1h), smem_u32(B1h) + 128 * C * 2, smem_u32(B2) + C * D * 2,
-                smem_u32(B2) + C * D * 2 + C * C * 2, C, idesc_bf16(128, C), 3);
-      mma_commit(bar);
-    }
-    run();
-  }
-  if (ok) {
-    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+    for (int s1 = 0; s1 < 2; ++s1) {
       float e1[16], p1[16];
-      tmem_ld16(tl + COL_E + s0, e1);
-      tmem_ld16(tl + COL_DOP + s0, p1);
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        a.b.dU[ch * CD + (int64_t)(s0 + e) * D + lane_row] = __fmaf_rn(dec[s0 + e], e1[e], p1[e]);
-    }
-    fence_before_sync();
-    __syncthreads();
-    // ---- phase 3: (U E)^T = E^T U^T
-    {
-      SplitTile<true, 128, D> ett;
-      SplitTile<false, C, D> ut;
-      ett.load(E, D, 128);
-      ut.load(a.b.U + ch * CD, D, C);
-      ett.store(Ah, Al);
-      ut.store(B1h, B1l);
-    }
-    issue_begin();
-    if (t == 0) {
-      fence_after_sync();
-      mma_terms(tb + COL_UE, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
-      mma_commit(bar);
-    }
-    run();
-  }
-  if (ok) {
-    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
-      float v[16];
-      tmem_ld16(tl + COL_UE + s0, v);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) a.b.UdSe[ch * CD + (int64_t)(s0 + e) * D + lane_row] = v[e];
-    }
-    fence_before_sync();
-    __syncthreads();
-    // ---- phase 4: (dO S0)^T = S0^T dO^T and dW^T = -S0^T dU^T
-    SplitTile<false, C, D> dut;
-    dut.load(a.b.dU + ch * CD, D, C);
-    {  // dO rows (i, K = a), split; loads in flight with dU's and S0's
-      float v[4][8];
-      load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
-      build_split<true, 128, D>(Ah, Al, S0, D, 128);
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256;
-        int r, k0;
-        kmajor_piece(q, D, r, k0);
-        split8(B1h, B1l, kmajor_off(r, k0, D), v[it]);
-      }
-    }
-    dut.store(B2, B2 + C * D * 2);
-    issue_begin();
-    if (t == 0) {
-      fence_after_sync();
-      mma_terms(tb + COL_DOS, smem_u32(Ah), smem_u32(Al), smem_u32(B1h), smem_u32(B1l), D, idesc_bf16(128, C), 3);
-      mma_terms(tb + COL_DW, smem_u32(Ah), smem_u32(Al), smem_u32(B2), smem_u32(B2) + C * D * 2, D,
-                idesc_bf16(128, C), 3);
-      mma_commit(bar);
-    }
-    run();
-  }
-  if (ok) {
-    for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
-      float v[16], w[16];
-      tmem_ld16(tl + COL_DOS + s0, v);
-      tmem_ld16(tl + COL_DW + s0, w);
+      tmem_ld16(tl + COL_0 + cbase + 16 * s1, e1);
+      tmem_ld16(tl + COL_1 + cbase + 16 * s1, p1);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        a.b.dOS0[ch * CD + (int64_t)(s0 + e) * D + lane_row] = v[e];
-        a.b.dW[ch * CD + (int64_t)(s0 + e) * D + lane_row] = -w[e];
+        const int s = cbase + 16 * s1 + e;
+        a.b.dU[ch * CD + (int64_t)s * D + lane_row] = __fmaf_rn(dec[s], e1[e], p1[e]);
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+
+  // ---- phase 3: (U E)^T = E^T U^T
+  if (ok) {
+    build_dd<true>(Ah, Al, E);
+    build_split<false, C, D>(Bh, Bl, a.b.U + ch * CD, D, C);
+    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+  }
+  {
+    float v[4][8];  // dO rows for phase 4, loaded while the product runs
+    load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+    if (ok) run();
+    if (ok) {
+#pragma unroll
+      for (int s1 = 0; s1 < 2; ++s1) {
+        float w[16];
+        tmem_ld16(tl + COL_0 + cbase + 16 * s1, w);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a.b.UdSe[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = w[e];
+      }
+    }
+    fence_before_sync();
+    __syncthreads();
+    // ---- phase 4: (dO S0)^T = S0^T dO^T, then dW^T = -S0^T dU^T (the B region is reused)
+    if (ok) {
+      build_dd<true>(Ah, Al, S0);
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(t + it * 256, D, r, k0);
+        split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
+      }
+      issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+    }
+  }
+  if (ok) {
+    SplitTile<false, C, D> dut;  // dU rows, loaded while the first product runs
+    dut.load(a.b.dU + ch * CD, D, C);
+    run();
+    if (ok) {
+      dut.store(Bh, Bl);
+      issue([&] { mma_terms(tb + COL_1, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+      run();
+    }
+  }
+  if (ok) {
+#pragma unroll
+    for (int s1 = 0; s1 < 2; ++s1) {
+      float v[16], w[16];
+      tmem_ld16(tl + COL_0 + cbase + 16 * s1, v);
+      tmem_ld16(tl + COL_1 + cbase + 16 * s1, w);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int64_t o = ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row;
+        a.b.dOS0[o] = v[e];
+        a.b.dW[o] = -w[e];
       }
     }
   } else if (t == 0) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
-    mbar_wait(bar, phase);
+    if (pending) mbar_wait(bar, phase);  // let this CTA's products finish before TMEM goes
   }
   fence_before_sync();
   __syncthreads();
@@ -1506,6 +1515,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
     mma_commit(bar);
     float run = gs[0];
     Gs[0] = run;
+#pragma unroll
     for (int i = 1; i < C; ++i) {
       run = __fadd_rn(run, gs[i]);
       Gs[i] = run;
