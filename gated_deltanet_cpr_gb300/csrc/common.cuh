@@ -172,7 +172,8 @@ __device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __r
   return __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
 }
 
-// T = (I + A)^{-1} for a strictly lower C x C matrix A in shared memory (row stride CP),
+// T = (I + A)^{-1} for a strictly lower C x C matrix A in shared memory (row stride CPA; T
+// written with row stride CPT),
 // blocked by 16.  Diagonal blocks by forward substitution, one column per thread:
 //     T[r][r] = 1,  T[i][r] = -sum_{m=r}^{i-1} A[i][m] T[m][r];
 // then off-diagonal blocks (I > J) by increasing I - J:
@@ -180,8 +181,8 @@ __device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __r
 // (every sum in ascending m with one accumulator).  Only the lower triangle of T is
 // written.  Xs: 3 * 16 * 16 floats of scratch.  All NT threads of the block must call it.
 template <int NT>
-__device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float* Tm, float* Xs, int C,
-                                                           int CP) {
+__device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, int CPA, float* Tm, int CPT, float* Xs,
+                                                           int C) {
   constexpr int TB = 16;
   const int t = threadIdx.x;
   const int nb = C / TB;
@@ -195,12 +196,12 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float
       float acc = 0.f;
 #pragma unroll
       for (int m = 0; m < ii; ++m)
-        if (m >= rr) acc = __fmaf_rn(A[(rb + ii) * CP + rb + m], col[m], acc);
+        if (m >= rr) acc = __fmaf_rn(A[(rb + ii) * CPA + rb + m], col[m], acc);
       if (ii > rr) col[ii] = -acc;
     }
 #pragma unroll
     for (int k = 0; k < TB; ++k)
-      if (k >= rr) Tm[(rb + k) * CP + r] = col[k];
+      if (k >= rr) Tm[(rb + k) * CPT + r] = col[k];
   }
   __syncthreads();
   for (int off = 1; off < nb; ++off) {
@@ -210,7 +211,7 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float
       const int i = I * TB + ii, r = (I - off) * TB + rr;
       float acc = 0.f;
 #pragma unroll 4
-      for (int m = r; m < I * TB; ++m) acc = __fmaf_rn(A[i * CP + m], Tm[m * CP + r], acc);
+      for (int m = r; m < I * TB; ++m) acc = __fmaf_rn(A[i * CPA + m], Tm[m * CPT + r], acc);
       Xs[e] = acc;
     }
     __syncthreads();
@@ -220,11 +221,17 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float
       const float* X = Xs + (e / (TB * TB)) * TB * TB;
       float acc = 0.f;
 #pragma unroll 4
-      for (int m = I * TB; m <= i; ++m) acc = __fmaf_rn(Tm[i * CP + m], X[(m - I * TB) * TB + rr], acc);
-      Tm[i * CP + r] = -acc;
+      for (int m = I * TB; m <= i; ++m) acc = __fmaf_rn(Tm[i * CPT + m], X[(m - I * TB) * TB + rr], acc);
+      Tm[i * CPT + r] = -acc;
     }
     __syncthreads();
   }
+}
+
+// The same with one row stride for A and T.
+template <int NT>
+__device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float* Tm, float* Xs, int C, int CP) {
+  blocked_unit_lower_inverse<NT>(A, CP, Tm, CP, Xs, C);
 }
 
 // State row i, half h: global float offset of register group m.

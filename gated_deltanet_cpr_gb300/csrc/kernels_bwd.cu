@@ -1402,16 +1402,16 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 // from rows just written to global memory (L2-resident) instead of extra shared memory;
 // Qt uses this chunk-head's dO S0 slot as scratch (rewritten by the next kernel).
 namespace tcq {
-constexpr int D = 128, C = 64, QCP = C + 1;
+constexpr int D = 128, C = 64, QCP = C + 1, TCP = C;  // row strides of A (padded) and T
 constexpr uint32_t TILE = C * D * 2;  // 16 KB
 constexpr uint32_t OFF_K = 0, OFF_KT = TILE, OFF_VT = 2 * TILE, OFF_TK = 3 * TILE, OFF_TV = 4 * TILE,
-                   OFF_A = 5 * TILE, OFF_T = OFF_A + C * QCP * 4, OFF_VEC = OFF_T + C * QCP * 4;
-constexpr size_t SMEM = OFF_VEC + 6 * C * 4 + 64;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_G = 0, COL_W = 0, COL_UT = 128, COL_P = 192, COL_QT = 256, COL_L = 384;
+                   OFF_A = 5 * TILE, OFF_T = OFF_A + C * QCP * 4, OFF_VEC = OFF_T + C * TCP * 4;
+constexpr size_t SMEM = OFF_VEC + 2 * C * 4 + 64;  // fits two CTAs per SM
+constexpr uint32_t TMEM_COLS = 256;  // the products run one after another: W and U^T (192) at most
+constexpr uint32_t COL_G = 0, COL_W = 0, COL_UT = 128, COL_P = 0, COL_QT = 0, COL_L = 0;
 }  // namespace tcq
 
-__global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
+__global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   using namespace tcq;
   using namespace tc;
   extern __shared__ __align__(128) unsigned char smq[];
@@ -1424,13 +1424,9 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   unsigned char* TVl = TVh + C * C * 2;
   float* A = reinterpret_cast<float*>(smq + OFF_A);
   float* Tm = reinterpret_cast<float*>(smq + OFF_T);
-  float* gs = reinterpret_cast<float*>(smq + OFF_VEC);
-  float* Gs = gs + C;
+  float* Gs = reinterpret_cast<float*>(smq + OFF_VEC);  // g, then its cumulative sum G
   float* bs = Gs + C;
-  float* eG = bs + C;
-  float* bk = eG + C;
-  float* dec = bk + C;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(dec + C);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(bs + C);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
   float* Xs = reinterpret_cast<float*>(TKh);
   if (!a.hdr->valid) return;
@@ -1469,7 +1465,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
       vr[it] = r < n ? *reinterpret_cast<const uint4*>(vb + r * vstride + c0) : z4;
     }
     if (t < C) {
-      gs[t] = g0;
+      Gs[t] = g0;
       bs[t] = b0;
     }
 #pragma unroll
@@ -1513,11 +1509,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
       mma_bf16(tb + COL_G, make_desc(ka + kk * 256, 128, (D / 8) * 128), make_desc(ka + kk * 256, 128, (D / 8) * 128),
                idesc_bf16(128, C), kk > 0 ? 1u : 0u);
     mma_commit(bar);
-    float run = gs[0];
-    Gs[0] = run;
+    float run = Gs[0];  // in place: G_i = G_{i-1} + g_i
 #pragma unroll
     for (int i = 1; i < C; ++i) {
-      run = __fadd_rn(run, gs[i]);
+      run = __fadd_rn(run, Gs[i]);
       Gs[i] = run;
     }
   }
@@ -1525,12 +1520,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   tc::transpose_image(KT, Ki, D, C);
   tc::transpose_image(VT, Vi, D, C);
   __syncthreads();
-  if (t < C) {
-    eG[t] = expf(Gs[t]);
-    bk[t] = __fmul_rn(bs[t], eG[t]);
-    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
-    a.b.G[ch * C + t] = Gs[t];
-  }
+  if (t < C) a.b.G[ch * C + t] = Gs[t];
   wait_mma();
   if (ok && (warp & 3) < 2) {
     const int i = lrow;
@@ -1547,10 +1537,10 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   fence_before_sync();
   __syncthreads();
   // ---- 3. T, TK, TV; W = TK K and U^T = V^T TV^T
-  blocked_unit_lower_inverse<256>(A, Tm, Xs, C, QCP);
+  blocked_unit_lower_inverse<256>(A, QCP, Tm, TCP, Xs, C);
   for (int o = t; o < C * C; o += 256) {
     const int i = o / C, r = o % C;
-    a.b.T[ch * C * C + o] = (r <= i) ? Tm[i * QCP + r] : 0.f;
+    a.b.T[ch * C * C + o] = (r <= i) ? Tm[i * TCP + r] : 0.f;
   }
   for (int q = t; q < C * (C / 8); q += 256) {
     int i, r0;
@@ -1559,8 +1549,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
       const int r = r0 + e;
-      const float x = (r <= i) ? Tm[i * QCP + r] : 0.f;
-      tk[e] = __fmul_rn(x, bk[r]);
+      const float x = (r <= i) ? Tm[i * TCP + r] : 0.f;
+      tk[e] = __fmul_rn(x, __fmul_rn(bs[r], expf(Gs[r])));  // beta e^G
       tv[e] = __fmul_rn(x, bs[r]);
     }
     const uint32_t off = kmajor_off(i, r0, C);
@@ -1670,6 +1660,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
   }
   if (ok && (warp & 3) < 2) {
     const int i = lrow;
+    const float egi = expf(Gs[i]);
     for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 16) {
       float v[16], qf[16];
       tmem_ld16(tmem_lane_addr(tb, warp, COL_QT + c0), v);
@@ -1678,8 +1669,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_prep_tc(BwdArgs a) {
 #pragma unroll
       for (int e = 0; e < 16; e += 4)
         *reinterpret_cast<float4*>(Qt + (int64_t)i * D + c0 + e) =
-            make_float4(__fsub_rn(__fmul_rn(eG[i], qf[e]), v[e]), __fsub_rn(__fmul_rn(eG[i], qf[e + 1]), v[e + 1]),
-                        __fsub_rn(__fmul_rn(eG[i], qf[e + 2]), v[e + 2]), __fsub_rn(__fmul_rn(eG[i], qf[e + 3]), v[e + 3]));
+            make_float4(__fsub_rn(__fmul_rn(egi, qf[e]), v[e]), __fsub_rn(__fmul_rn(egi, qf[e + 1]), v[e + 1]),
+                        __fsub_rn(__fmul_rn(egi, qf[e + 2]), v[e + 2]), __fsub_rn(__fmul_rn(egi, qf[e + 3]), v[e + 3]));
     }
   }
   fence_before_sync();

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
   if (t == 0) {
     float run = gs[0];
     Gs[0] = run;
+#pragma unroll 8
     for (int i = 1; i < C; ++i) {
       run = __fadd_rn(run, gs[i]);
       Gs[i] = run;
@@ -994,6 +995,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
       tc::mma_commit(bar);
       float run = gs[0];
       Gs[0] = run;
+#pragma unroll
       for (int i = 1; i < C; ++i) {
         run = __fadd_rn(run, gs[i]);
         Gs[i] = run;
