@@ -810,7 +810,7 @@ __device__ __forceinline__ void split_store16(unsigned char* hi, unsigned char* 
   }
 }
 
-__global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
+__global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   using namespace tcb;
   using namespace tc;
   extern __shared__ __align__(128) unsigned char smb[];
@@ -824,7 +824,9 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
-  const int t = threadIdx.x, warp = t >> 5, row = t;
+  // warp w reads TMEM lanes 32 (w % 4) .. + 31 (state rows) and column half w / 4
+  const int t = threadIdx.x, warp = t >> 5, row = (warp & 3) * 32 + (t & 31), half = warp >> 2;
+  const int cs0 = half * (D / 2), us0 = half * (C / 2);
   const int n = blockIdx.x, h = blockIdx.y;
   const SeqRec rec = a.seqs[n];
   const int64_t SZ = (int64_t)D * D;
@@ -833,7 +835,7 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
   const int nch = rec.nchunks;
   if (nch == 0) {  // no tokens: dstate_in = dstate_out
     if (a.dstate_in)
-      for (int c0 = 0; c0 < D; ++c0) a.dstate_in[srow + c0] = a.dstate_out ? a.dstate_out[srow + c0] : 0.f;
+      for (int c0 = cs0; c0 < cs0 + D / 2; ++c0) a.dstate_in[srow + c0] = a.dstate_out ? a.dstate_out[srow + c0] : 0.f;
     return;
   }
   if (t == 0) {
@@ -859,7 +861,7 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
     }
     const float g = gamma_of(j);
     const float* L = a.b.L + chead(j) * SZ + (int64_t)row * D;
-    for (int c0 = 0; c0 < D; c0 += 16) {
+    for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
       float v[16], w[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) v[e] = a.dstate_out ? a.dstate_out[srow + c0 + e] : 0.f;
@@ -890,12 +892,12 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
       bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, a.b.img + chead(j - 1) * IW, STAGE_BYTES, &bars[buf ^ 1]);
     }
     if (t < C) decs[t] = -expf(__fsub_rn(a.b.G[chead(j) * C + C - 1], a.b.G[chead(j) * C + t]));
-    float lpre[D];  // next step's L row, loaded while this step's MMAs run
+    float lpre[D / 2];  // next step's L half row, loaded while this step's MMAs run
     float gpre = 0.f;
     if (j > 0) {
-      const float4* L4 = reinterpret_cast<const float4*>(a.b.L + chead(j - 1) * SZ + (int64_t)row * D);
+      const float4* L4 = reinterpret_cast<const float4*>(a.b.L + chead(j - 1) * SZ + (int64_t)row * D + cs0);
 #pragma unroll
-      for (int e = 0; e < D / 4; ++e) {
+      for (int e = 0; e < D / 8; ++e) {
         const float4 x = L4[e];
         lpre[4 * e] = x.x; lpre[4 * e + 1] = x.y; lpre[4 * e + 2] = x.z; lpre[4 * e + 3] = x.w;
       }
@@ -923,7 +925,8 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
     mma_phase ^= 1u;
     mma_pending = false;
     fence_after_sync();
-    for (int s0 = 0; s0 < C; s0 += 16) {  // Xd = -dec_s (dS K^T), split into A2
+#pragma unroll
+    for (int s0 = us0; s0 < us0 + C / 2; s0 += 16) {  // Xd = -dec_s (dS K^T), split into A2
       float v[16];
       tmem_ld16(tlane + D1_COL + s0, v);
 #pragma unroll
@@ -955,19 +958,30 @@ __global__ void __launch_bounds__(128, 1) k_bwd_chain_tc(BwdArgs a) {
     {  // dS^(j): end adjoint of chunk j-1 (or dstate_in), next A operand, next D2 preload
       const bool more = j > 0;
       const float g = gpre;
+      // dS^(j) leaves through a per-warp staging tile in the (now free) Xd operand region,
+      // so that each store instruction writes 8 rows x 64 contiguous bytes
+      float* tile = reinterpret_cast<float*>(A2h) + warp * (32 * 20);
+      const int lane = t & 31, rq = (warp & 3) * 32;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
         float v[16];
         tmem_ld16(tlane + D2_COL + c0, v);
         if (more) {
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(a.b.dSE + chead(j - 1) * SZ + (int64_t)row * D + c0 + e) =
-                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          for (int x = 0; x < 4; ++x)
+            *reinterpret_cast<float4*>(tile + lane * 20 + 4 * x) = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const int rl = 8 * k2 + (lane >> 2), f = lane & 3;
+            *reinterpret_cast<float4*>(a.b.dSE + chead(j - 1) * SZ + (int64_t)(rq + rl) * D + c0 + 4 * f) =
+                *reinterpret_cast<const float4*>(tile + rl * 20 + 4 * f);
+          }
+          __syncwarp();
           split_store16(A1h, A1l, row, c0, D, v);
           float w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(lpre[c0 + e], __fmul_rn(g, v[e]));
+          for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(lpre[c0 - cs0 + e], __fmul_rn(g, v[e]));
           tmem_st16(tlane + D2_COL + c0, w);
         } else if (a.dstate_in) {
 #pragma unroll
@@ -2170,7 +2184,7 @@ void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, vo
   mark(mark_ctx, n_chunks > 0 ? 1 : 0);
   if (boundary_on_tensor_cores(a.dm)) {
     ensure_smem_bwd(k_bwd_chain_tc, tcb::SMEM);
-    k_bwd_chain_tc<<<dim3((unsigned)N, a.dm.hv), 128, tcb::SMEM, st>>>(a);
+    k_bwd_chain_tc<<<dim3((unsigned)N, a.dm.hv), 256, tcb::SMEM, st>>>(a);
   } else {
     ensure_smem_bwd(k_bwd_chain<D, Tin>, bchain_smem<D>());
     k_bwd_chain<D, Tin><<<dim3((unsigned)N, a.dm.hv, D / kRowsPerChain), NT, bchain_smem<D>(), st>>>(a);
