@@ -48,10 +48,12 @@ SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
 # reported only while the kernel's source (its function text plus common.cuh) hashes to the
 # value it had when the counters were taken; after any change it is null until recaptured.
 NCU_TRAFFIC = {
-    # 202,746,112 + 21,810,944 B for one 4096-token sequence x 32 value heads
-    "k_intra": {"src_sha": "832e57efb113358e", "bytes_per_unit": (202746112 + 21810944) / (4096 * 32),
+    # 202,745,600 + 21,815,552 B for one 4096-token sequence x 32 value heads
+    "k_intra": {"src_sha": "9cb58c197a155185", "bytes_per_unit": (202745600 + 21815552) / (4096 * 32),
                 "unit": "token-head"},
-    "k_decode": {"src_sha": None, "bytes_per_unit": None, "unit": "slot-head"},
+    # 541,289,472 + 486,616,576 B for the full 256-slot x 32-head launch (one-pass capture)
+    "k_decode": {"src_sha": "21ffd2cd2457bd1a", "bytes_per_unit": (541289472 + 486616576) / (256 * 32),
+                 "unit": "slot-head"},
 }
 KERNEL_TEXT = {  # file, first line of the kernel, first line after it
     "k_intra": ("kernels_fwd.cu", "__global__ void __launch_bounds__(2 * D, 2) k_intra(",
@@ -699,6 +701,8 @@ def run_ncu_case(args):
     """Small, fixed cases for ncu captures (a few hundred MB on the device):
     prefill   one 4096-token sequence, 16/32 heads, d=128, C=64, bf16: three prefills
     decode    64 slots x 32 heads of 128x128 states: three decode steps (no resync)
+    decode256 the decode workload's 256 slots x 32 heads: three decode steps (no resync), for
+              one-pass DRAM counters of the full-size launch
     bwd       one 4096-token sequence: two trainer forward + backward passes
     """
     import torch
@@ -722,7 +726,7 @@ def run_ncu_case(args):
             api.prefill(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], chunk=w.chunk,
                         cu_seqlens_host=x["cu_seqlens"])
     else:
-        N = 64
+        N = 256 if args.ncu_case == "decode256" else 64
         cache = api.Cache(N, w.h_qk, w.h_v, w.d, w.chunk, dtype=torch.bfloat16, device=dev)
         cache.s_run.normal_()
         cache.pos.fill_(2048)
@@ -744,7 +748,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "bwd"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode256", "bwd"], default=None,
                     help="run a small fixed case for an ncu capture and exit")
     args = ap.parse_args(argv)
     if args.ncu_case:
