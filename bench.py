@@ -123,7 +123,8 @@ def barrier(world: int):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons."""
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons; entering waits (up
+    to 5 s) for the first sample so that the timed region is covered."""
 
     FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -139,10 +140,17 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        if self.proc is not None:
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and self.proc.poll() is None:
+                self.f.flush()
+                if os.path.getsize(self.path) > 0:
+                    break
+                time.sleep(0.05)
         return self
 
     def __exit__(self, *exc):
@@ -208,6 +216,24 @@ def oracle_rates(x, hv, fwd_tokens: int, bwd_tokens: int, threads: int):
                sl("beta", bwd_tokens), [0, bwd_tokens], sl("dout", bwd_tokens), n_threads=threads)
     t_bwd = time.perf_counter() - t0
     return fwd_tokens * hv / t_fwd, bwd_tokens * hv / t_bwd, t_fwd + t_bwd
+
+
+def oracle_rates_all(x, hv, threads: int):
+    """The oracle (as it stands) forward and backward over all sequences of x.  Returns
+    token-heads/s for forward and for backward, and the wall time."""
+    import oracle
+    from gated_deltanet_cpr_gb300.synth import as_f64 as f
+
+    cu = x["cu_seqlens"].numpy()
+    T = int(cu[-1])
+    t0 = time.perf_counter()
+    oracle.fwd(f(x["q"]), f(x["k"]), f(x["v"]), f(x["g"]), f(x["beta"]), cu, n_threads=threads)
+    t_fwd = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.bwd(f(x["q"]), f(x["k"]), f(x["v"]), f(x["g"]), f(x["beta"]), cu, f(x["dout"]),
+               n_threads=threads)
+    t_bwd = time.perf_counter() - t0
+    return T * hv / t_fwd, T * hv / t_bwd, t_fwd + t_bwd
 
 
 def step_tokens(w):
@@ -465,13 +491,13 @@ def run_cuda(args):
             "peaks_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = threads_available()
-        rf, rb, dt = oracle_rates(x, hv, 4096, 1024, threads)
+        rf, rb, dt = oracle_rates_all(x, hv, threads)
         est = oracle_step_estimate(w, rf, rb)
         line["cpu_baseline"] = {
             "value": step_tok / est, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": (f"oracle fwd on 4096 tokens x {hv} heads and oracle bwd on 1024 tokens x "
-                       f"{hv} heads of sequence 0 ({dt:.1f} s wall); whole-step time "
-                       f"extrapolated linearly in token-heads")}
+            "sample": (f"oracle fwd and oracle bwd over the whole prefill workload "
+                       f"({T} tokens x {hv} heads each, {dt:.1f} s wall on {threads} threads); "
+                       f"step time = those rates applied to the step's token-heads")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -744,7 +770,7 @@ def run_ncu_case(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
