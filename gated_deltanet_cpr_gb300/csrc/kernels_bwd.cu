@@ -1732,61 +1732,57 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
 }
 
 // ============================================================  KB4 (tcgen05)  ===
-// Backward gradients on tensor cores (bf16 inputs, d = 128, C = 64), one CTA of 256 threads
-// per chunk-head; the arithmetic of k_bwd_grad with its products as MMAs:
-//   phase 1  Pm = Gam (.) (dO U^T) (lower with diagonal), QK = Q K^T, A' = Gam (.) (K K^T)
-//   phase 2  dQ = diag(e^G) dO S0 + Pm K,  dK <- Pm^T Q,  X = T^T dU,  Y = T^T dW
-//   phase 3  dA = -(Y W^T + X Ut^T) (strictly lower), dAm = dA beta_i Gam
-//   phase 4  dK += dAm K + dAm^T K, then + diag(dec) U dS_end + diag(beta e^G) Y
-// with dg, dbeta from the same scalar terms.  Warps 0, 1, 4, 5 own TMEM lanes 0..63 (the
-// chunk rows) and read the accumulators out, one column half each; meanwhile warps 2, 3, 6, 7
-// build the next phase's operand images.  Every build and readout issues its global loads
-// before its first store.  K^T and Q^T stay resident from phase 1 on.  64-row operands use
-// 128-row MMAs whose extra rows read neighbouring arena bytes and are never read back.
+// Backward gradients on tensor cores (bf16 inputs, d = 128, C = 64) as two kernels, each
+// sized for two CTAs per SM (96 KB operand arena, at most 256 TMEM columns, 128 registers)
+// so that one CTA's loads and waits overlap the other's work; the arithmetic of k_bwd_grad
+// with its products as MMAs:
+//   G1  Pm = Gam (.) (dO U^T) (lower with diagonal), QK = Q K^T      -> dG_b sums, Pm image
+//       dQ = diag(e^G) dO S0 + Pm K,  dK1 = Pm^T Q                   -> dq, dG_a
+//       X = T^T dU,  Y = T^T dW                                       -> dv, dbeta_a, kY;
+//       dk <- dK1 + diag(beta e^G) Y; X and Y as operand images for G2
+//   G2  dA = -(Y W^T + X Ut^T) (strictly lower), A' = Gam (.) (K K^T)  -> dbeta_c, dG_e sums
+//       dAm = dA beta_i Gam,  dK2 = dAm K + dAm^T K                   -> dk += dK2 + diag(dec) U dS_end
+//       dG, reverse cumulative sum -> dg, dbeta
+// The row and column sums of the dG terms come straight from the TMEM readouts (per-thread
+// row sums, warp-shuffle column sums in a fixed tree).  X and Y travel through the
+// workspace (the adjoint L, dead after the reverse chain) as ready-made images that G2
+// brings in by bulk copy; the per-token partial sums go through the image workspace.
+// 64-row operands use 128-row MMAs whose extra rows read neighbouring arena bytes and are
+// never read back.
 namespace tcd {
-constexpr int D = 128, C = 64, MP = C + 1;
-constexpr uint32_t KB = 1024;
-constexpr uint32_t ARENA = 144 * KB;
-// arena byte offsets; an image's lo half follows its hi half (8 KB for 64 x 64, 16 KB for
-// 64 x 128 and 128 x 64)
-constexpr uint32_t P1_DO = 0, P1_U = 32 * KB, P1_Q = 64 * KB, P1_K = 80 * KB;  // + overread to 112
-constexpr uint32_t QT = 112 * KB, KT = 128 * KB;
-constexpr uint32_t P2_PM = 0, P2_PMT = 16 * KB, P2_TT = 32 * KB, P2_DU = 48 * KB, P2_DW = 80 * KB;
-constexpr uint32_t P3_Y = 0, P3_X = 32 * KB, P3_W = 64 * KB, P3_UT = 96 * KB;
-constexpr uint32_t P4_AM = 0, P4_AMT = 16 * KB;
-constexpr uint32_t MAT = C * MP * 4;
-constexpr size_t SMEM = ARENA + 3 * (size_t)MAT + 17 * C * 4 + 64;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_PM = 0, COL_QK = 64, COL_AP = 128, COL_DQ = 0, COL_DK = 128, COL_X = 256,
-                   COL_Y = 384, COL_DA = 0;
+constexpr int D = 128, C = 64;
+constexpr uint32_t KB = 1024, ARENA = 96 * KB;
+constexpr uint32_t IMG = 16 * KB;  // a 64 x 128 or 128 x 64 bf16 image (hi or lo)
+constexpr size_t SMEM1 = ARENA + 13 * C * 4 + 64;
+constexpr size_t SMEM2 = ARENA + 18 * C * 4 + 64;
+constexpr uint32_t TMEM1 = 256, TMEM2 = 128;
 }  // namespace tcd
 
-__global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
+// fixed-order warp sum (xor tree); every lane gets the total
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
+  return x;
+}
+
+__global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   using namespace tcd;
   using namespace tc;
   extern __shared__ __align__(128) unsigned char smd[];
   unsigned char* ar = smd;
-  float* PM = reinterpret_cast<float*>(smd + ARENA);  // Pm, then dAm
-  float* AQ = PM + C * MP;                            // Q K^T, then dA
-  float* AP = AQ + C * MP;                            // A' = Gam (.) K K^T (strictly lower)
-  float* Gs = AP + C * MP;
+  float* Gs = reinterpret_cast<float*>(smd + ARENA);
   float* eG = Gs + C;
-  float* dec = eG + C;
-  float* bs = dec + C;
-  float* dGa = bs + C;       // [2][C] partial sums, one per column half
-  float* dba = dGa + 2 * C;  // [2][C]
-  float* kY = dba + 2 * C;   // [2][C]
-  float* cs = kY + 2 * C;    // [2][C]
-  float* dGb = cs + 2 * C;
-  float* dGe = dGb + C;
-  float* dbc = dGe + C;
-  float* dgv = dbc + C;
-  float* csv = dgv + C;  // per token dec * (U dS_end . k)
-  uint64_t* bar = reinterpret_cast<uint64_t*>(csv + C);
+  float* bs = eG + C;
+  float* rowp = bs + C;      // [2][C] dG_b row sums, one per column half
+  float* colp = rowp + 2 * C;  // [2][C] dG_b column sums, one per row half
+  float* dGa = colp + 2 * C;   // [2][C]
+  float* dba = dGa + 2 * C;    // [2][C]
+  float* kY = dba + 2 * C;     // [2][C]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(kY + 2 * C);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
-  const int t = threadIdx.x, warp = t >> 5;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = a.chunks[c];
@@ -1794,19 +1790,20 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
   const int64_t CD = (int64_t)C * D;
-  const int64_t kstride = (int64_t)dm.hqk * D;
-  const int64_t vstride = (int64_t)dm.hv * D;
+  const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
   const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + tok0 * kstride + (int64_t)hq * D;
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.in.q) + tok0 * kstride + (int64_t)hq * D;
   const int64_t orow0 = tok0 * vstride + (int64_t)h * D;  // token 0 of this head in [T, Hv, D]
   const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(a.in.v) + orow0;
-  const bool rowlane = (warp & 3) < 2;
-  const int row = (warp & 3) * 32 + (t & 31);
+  unsigned char* gX = reinterpret_cast<unsigned char*>(a.b.L + ch * (int64_t)D * D);  // X hi | lo images
+  unsigned char* gY = gX + 2 * IMG;                                                   // Y hi | lo images
+  const bool rowlane = (warp & 3) < 2;  // TMEM lanes 0..63 = the chunk's rows
+  const int row = (warp & 3) * 32 + lane;
   const int half = warp >> 2;
-  const int helper = half * 64 + ((warp & 3) - 2) * 32 + (t & 31);  // 0..127 on warps 2, 3, 6, 7
+  const int helper = half * 64 + ((warp & 3) - 2) * 32 + lane;  // 0..127 on warps 2, 3, 6, 7
   const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-
-  // ---- phase 1 operands: dO (split), U (split), Q rows, K rows
+  // arena: round 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U hi/lo @64/@80; then Pm hi/lo
+  // @32/@40, Pm^T @48/@56, K^T @64, Q^T @80; then T^T @0/@8, dU^T @16/@32, dW^T @48/@64
   {
     float g0 = 0.f, b0 = 0.f;
     if (t < C) {
@@ -1834,8 +1831,6 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
         kr[it] = zero4;
       }
     }
-    SplitTile<false, C, D> u;
-    u.load(a.b.U + ch * CD, D, C);
     if (t < C) {
       Gs[t] = g0;
       bs[t] = b0;
@@ -1845,17 +1840,17 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
       int r, k0;
       kmajor_piece(t + it * 256, D, r, k0);
       const uint32_t off = kmajor_off(r, k0, D);
-      split8(ar + P1_DO, ar + P1_DO + 16 * KB, off, vo[it]);
-      *reinterpret_cast<uint4*>(ar + P1_Q + off) = qr[it];
-      *reinterpret_cast<uint4*>(ar + P1_K + off) = kr[it];
+      split8(ar + 32 * KB, ar + 48 * KB, off, vo[it]);
+      *reinterpret_cast<uint4*>(ar + off) = qr[it];
+      *reinterpret_cast<uint4*>(ar + 16 * KB + off) = kr[it];
     }
-    u.store(ar + P1_U, ar + P1_U + 16 * KB);
   }
+  build_split<false, C, D>(ar + 64 * KB, ar + 80 * KB, a.b.U + ch * CD, D, C);
   if (t == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  if (warp == 0) tmem_alloc(tslot, TMEM1);
   fence_proxy_async();
   fence_before_sync();
   __syncthreads();
@@ -1864,259 +1859,439 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
   const uint32_t tl = tmem_lane_addr(tb, warp, 0);
   const uint32_t sa = smem_u32(ar);
   uint32_t phase = 0;
-  bool ok = true;
+  bool ok = true, pending = false;
   auto wait_mma = [&]() {
     const bool done = mbar_wait(bar, phase);
-    if (done) phase ^= 1u;
+    if (done) {
+      phase ^= 1u;
+      pending = false;
+    }
     ok = __syncthreads_and(done) != 0;
     fence_after_sync();
   };
-  auto sync_for_mma = [&]() {
+  auto issue = [&](auto&& mmas) {
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
+    if (t == 0) {
+      fence_after_sync();
+      mmas();
+      mma_commit(bar);
+    }
+    pending = true;
   };
+  // ---- round 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64
   if (t == 0) {
-    mma_terms(tb + COL_PM, sa + P1_DO, sa + P1_DO + 16 * KB, sa + P1_U, sa + P1_U + 16 * KB, D,
-              idesc_bf16(128, C), 3);
-    mma_terms(tb + COL_QK, sa + P1_Q, sa + P1_Q, sa + P1_K, sa + P1_K, D, idesc_bf16(128, C), 1);
-    mma_terms(tb + COL_AP, sa + P1_K, sa + P1_K, sa + P1_K, sa + P1_K, D, idesc_bf16(128, C), 1);
+    mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C), 3);
+    mma_terms(tb + 64, sa, sa, sa + 16 * KB, sa + 16 * KB, D, idesc_bf16(128, C), 1);
     mma_commit(bar);
   }
-  // while the products run: K^T and Q^T images from the row images (reads of the operands only)
-  tc::transpose_image(ar + QT, ar + P1_Q, D, C);
-  tc::transpose_image(ar + KT, ar + P1_K, D, C);
-  if (t < C) {
-    eG[t] = expf(Gs[t]);
-    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
-  }
+  pending = true;
+  if (t < C) eG[t] = expf(Gs[t]);
   wait_mma();
-  // ---- phase 1 readout (row warps) || phase 2 operands T^T, dU^T, dW^T (other warps)
-  if (ok) {
-    if (rowlane) {
-      const int i = row;
-      for (int s0 = half * 32; s0 < half * 32 + 32; s0 += 16) {
-        float pm[16], qk[16], ap[16];
-        tmem_ld16(tl + COL_PM + s0, pm);
-        tmem_ld16(tl + COL_QK + s0, qk);
-        tmem_ld16(tl + COL_AP + s0, ap);
+  if (ok && rowlane) {  // Pm, dG_b row / column sums, Pm image
+    const int i = row;
+    float rp = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int s = s0 + e;
-          const float gam = expf(__fsub_rn(Gs[i], Gs[s]));
-          PM[i * MP + s] = (i >= s) ? __fmul_rn(gam, pm[e]) : 0.f;
-          AQ[i * MP + s] = (i > s) ? qk[e] : 0.f;
-          AP[i * MP + s] = (i > s) ? __fmul_rn(gam, ap[e]) : 0.f;
-        }
+    for (int s1 = 0; s1 < 2; ++s1) {
+      const int s0 = half * 32 + 16 * s1;
+      float pm[16], qk[16];
+      tmem_ld16(tl + 0 + s0, pm);
+      tmem_ld16(tl + 64 + s0, qk);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int s = s0 + e;
+        const float pv = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), pm[e]) : 0.f;
+        const float pr = (i > s) ? __fmul_rn(pv, qk[e]) : 0.f;
+        pm[e] = pv;
+        qk[e] = pr;
+        rp = __fadd_rn(rp, pr);
       }
-    } else {
-      {
-        SplitTile<true, C, C, 128> tt;
-        SplitTile<true, D, C, 128> du;
-        tt.load(a.b.T + ch * C * C, C, C, helper);
-        du.load(a.b.dU + ch * CD, D, C, helper);
-        tt.store(ar + P2_TT, ar + P2_TT + 8 * KB, helper);
-        du.store(ar + P2_DU, ar + P2_DU + 16 * KB, helper);
+      split8(ar + 32 * KB, ar + 40 * KB, kmajor_off(i, s0, C), pm);
+      split8(ar + 32 * KB, ar + 40 * KB, kmajor_off(i, s0 + 8, C), pm + 8);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float cs = warp_sum(qk[e]);
+        if (lane == 0) colp[(warp & 3) * C + s0 + e] = cs;
       }
-      SplitTile<true, D, C, 128> dw;
-      dw.load(a.b.dW + ch * CD, D, C, helper);
-      dw.store(ar + P2_DW, ar + P2_DW + 16 * KB, helper);
     }
+    rowp[half * C + i] = rp;
   }
   fence_before_sync();
   __syncthreads();
-  // ---- phase 2: dQ, dK <- Pm^T Q, X, Y
+  // ---- round 2: dQ = Pm K -> TMEM 0, dK1 = Pm^T Q -> TMEM 128
   if (ok) {
-    build_split<false, C, C>(ar + P2_PM, ar + P2_PM + 8 * KB, PM, MP, C);
-    build_split<true, C, C>(ar + P2_PMT, ar + P2_PMT + 8 * KB, PM, MP, C);
-    sync_for_mma();
-    if (t == 0) {
-      fence_after_sync();
-      mma_terms(tb + COL_DQ, sa + P2_PM, sa + P2_PM + 8 * KB, sa + KT, sa + KT, C, idesc_bf16(128, D), 2);
-      mma_terms(tb + COL_DK, sa + P2_PMT, sa + P2_PMT + 8 * KB, sa + QT, sa + QT, C, idesc_bf16(128, D), 2);
-      mma_terms(tb + COL_X, sa + P2_TT, sa + P2_TT + 8 * KB, sa + P2_DU, sa + P2_DU + 16 * KB, C,
-                idesc_bf16(128, D), 3);
-      mma_terms(tb + COL_Y, sa + P2_TT, sa + P2_TT + 8 * KB, sa + P2_DW, sa + P2_DW + 16 * KB, C,
-                idesc_bf16(128, D), 3);
-      mma_commit(bar);
-    }
+    tc::transpose_image(ar + 48 * KB, ar + 32 * KB, C, C);  // Pm^T hi
+    tc::transpose_image(ar + 56 * KB, ar + 40 * KB, C, C);  // Pm^T lo
+    tc::transpose_image(ar + 64 * KB, ar + 16 * KB, D, C);  // K^T
+    tc::transpose_image(ar + 80 * KB, ar, D, C);            // Q^T
+    issue([&] {
+      mma_terms(tb + 0, sa + 32 * KB, sa + 40 * KB, sa + 64 * KB, sa + 64 * KB, C, idesc_bf16(128, D), 2);
+      mma_terms(tb + 128, sa + 48 * KB, sa + 56 * KB, sa + 80 * KB, sa + 80 * KB, C, idesc_bf16(128, D), 2);
+    });
+    wait_mma();
   }
-  if (t < C) {  // dG from P while the products run: sum_{s<t} Pm QK - sum_{i>t} Pm QK
-    float rw = 0.f, cl = 0.f;
-    for (int s2 = 0; s2 < t; ++s2) rw = __fmaf_rn(PM[t * MP + s2], AQ[t * MP + s2], rw);
-    for (int i2 = t + 1; i2 < C; ++i2) cl = __fmaf_rn(PM[i2 * MP + t], AQ[i2 * MP + t], cl);
-    dGb[t] = __fsub_rn(rw, cl);
-  }
-  if (ok) wait_mma();
-  // ---- phase 2 readout (row warps) || phase 3 operands W, Ut (other warps)
+  // dQ readout (row warps) || round 3 operands T^T, dU^T, dW^T (other warps)
   if (ok) {
     if (rowlane) {
       const int i = row;
       const bool live = i < n;
-      const float egi = eG[i], bi = bs[i];
+      const float egi = eG[i];
       const float* dos_row = a.b.dOS0 + ch * CD + (int64_t)i * D;
-      float pga = 0.f, pba = 0.f, pky = 0.f;
-      for (int cb = half * 64; cb < half * 64 + 64; cb += 32) {
-        float4 ds4[8];
-        uint4 qv[4], kv[4], vv[4];
+      float pga = 0.f;
+      for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+        float4 ds4[4];
+        uint4 qv[2];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) ds4[x] = *reinterpret_cast<const float4*>(dos_row + cb + 4 * x);
+        for (int x = 0; x < 4; ++x) ds4[x] = *reinterpret_cast<const float4*>(dos_row + c0 + 4 * x);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) qv[x] = live ? *reinterpret_cast<const uint4*>(qb + i * kstride + c0 + 8 * x) : zero4;
+        float dq[16], qf[16], ds[16];
+        tmem_ld16(tl + 0 + c0, dq);
+        unpack8(qv[0], qf);
+        unpack8(qv[1], qf + 8);
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
-          qv[x] = live ? *reinterpret_cast<const uint4*>(qb + i * kstride + cb + 8 * x) : zero4;
-          kv[x] = live ? *reinterpret_cast<const uint4*>(kb + i * kstride + cb + 8 * x) : zero4;
-          vv[x] = live ? *reinterpret_cast<const uint4*>(vb + i * vstride + cb + 8 * x) : zero4;
+          ds[4 * x] = ds4[x].x;
+          ds[4 * x + 1] = ds4[x].y;
+          ds[4 * x + 2] = ds4[x].z;
+          ds[4 * x + 3] = ds4[x].w;
         }
 #pragma unroll
-        for (int sub = 0; sub < 2; ++sub) {
-          const int c0 = cb + 16 * sub;
-          float dq[16], xr[16], yr[16], qf[16], kf[16], vf[16], ds[16];
-          tmem_ld16(tl + COL_DQ + c0, dq);
-          tmem_ld16(tl + COL_X + c0, xr);
-          tmem_ld16(tl + COL_Y + c0, yr);
-          unpack8(qv[2 * sub], qf);
-          unpack8(qv[2 * sub + 1], qf + 8);
-          unpack8(kv[2 * sub], kf);
-          unpack8(kv[2 * sub + 1], kf + 8);
-          unpack8(vv[2 * sub], vf);
-          unpack8(vv[2 * sub + 1], vf + 8);
+        for (int e = 0; e < 16; ++e) {
+          pga = __fmaf_rn(ds[e], qf[e], pga);
+          dq[e] = __fmaf_rn(egi, ds[e], dq[e]);
+        }
+        if (live) {
+          float4* dqp = reinterpret_cast<float4*>(a.b.dq_part + orow0 + (int64_t)i * vstride + c0);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            ds[4 * x] = ds4[4 * sub + x].x;
-            ds[4 * x + 1] = ds4[4 * sub + x].y;
-            ds[4 * x + 2] = ds4[4 * sub + x].z;
-            ds[4 * x + 3] = ds4[4 * sub + x].w;
-          }
-          float dqo[16], dvo[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            dqo[e] = __fmaf_rn(egi, ds[e], dq[e]);
-            dvo[e] = __fmul_rn(bi, xr[e]);
-            pga = __fmaf_rn(ds[e], qf[e], pga);
-            pba = __fmaf_rn(vf[e], xr[e], pba);
-            pky = __fmaf_rn(kf[e], yr[e], pky);
-          }
-          if (live) {
-            float4* dqp = reinterpret_cast<float4*>(a.b.dq_part + orow0 + (int64_t)i * vstride + c0);
-            float4* dvp = reinterpret_cast<float4*>(a.dv + orow0 + (int64_t)i * vstride + c0);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              dqp[x] = make_float4(dqo[4 * x], dqo[4 * x + 1], dqo[4 * x + 2], dqo[4 * x + 3]);
-              dvp[x] = make_float4(dvo[4 * x], dvo[4 * x + 1], dvo[4 * x + 2], dvo[4 * x + 3]);
-            }
-          }
-          split8(ar + P3_X, ar + P3_X + 16 * KB, kmajor_off(i, c0, D), xr);
-          split8(ar + P3_X, ar + P3_X + 16 * KB, kmajor_off(i, c0 + 8, D), xr + 8);
-          split8(ar + P3_Y, ar + P3_Y + 16 * KB, kmajor_off(i, c0, D), yr);
-          split8(ar + P3_Y, ar + P3_Y + 16 * KB, kmajor_off(i, c0 + 8, D), yr + 8);
+          for (int x = 0; x < 4; ++x) dqp[x] = make_float4(dq[4 * x], dq[4 * x + 1], dq[4 * x + 2], dq[4 * x + 3]);
         }
       }
       dGa[half * C + i] = pga;
-      dba[half * C + i] = pba;
-      kY[half * C + i] = pky;
     } else {
       {
-        SplitTile<false, C, D, 128> w;
-        w.load(a.b.W + ch * CD, D, C, helper);
-        w.store(ar + P3_W, ar + P3_W + 16 * KB, helper);
+        SplitTile<true, C, C, 128> tt;
+        tt.load(a.b.T + ch * C * C, C, C, helper);
+        tt.store(ar, ar + 8 * KB, helper);
       }
-      SplitTile<false, C, D, 128> ut;
-      ut.load(a.b.Ut + ch * CD, D, C, helper);
-      ut.store(ar + P3_UT, ar + P3_UT + 16 * KB, helper);
+      {
+        SplitTile<true, D, C, 128> du;
+        du.load(a.b.dU + ch * CD, D, C, helper);
+        du.store(ar + 16 * KB, ar + 32 * KB, helper);
+      }
+      SplitTile<true, D, C, 128> dw;
+      dw.load(a.b.dW + ch * CD, D, C, helper);
+      dw.store(ar + 48 * KB, ar + 64 * KB, helper);
     }
   }
-  // ---- phase 3: dA = -(Y W^T + X Ut^T)
+  // ---- round 3: X = T^T dU -> TMEM 0
   if (ok) {
-    sync_for_mma();
-    if (t == 0) {
-      fence_after_sync();
-      mma_terms(tb + COL_DA, sa + P3_Y, sa + P3_Y + 16 * KB, sa + P3_W, sa + P3_W + 16 * KB, D,
-                idesc_bf16(128, C), 3);
-      mma_terms(tb + COL_DA, sa + P3_X, sa + P3_X + 16 * KB, sa + P3_UT, sa + P3_UT + 16 * KB, D,
-                idesc_bf16(128, C), 3, true);
-      mma_commit(bar);
-    }
+    issue([&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 16 * KB, sa + 32 * KB, C, idesc_bf16(128, D), 3); });
     wait_mma();
   }
-  if (ok && rowlane) {  // dA (strictly lower) and dAm = dA beta_i Gam_is
+  if (ok && rowlane) {  // dv, dbeta_a; X image -> workspace
     const int i = row;
+    const bool live = i < n;
     const float bi = bs[i];
-    for (int s0 = half * 32; s0 < half * 32 + 32; s0 += 16) {
-      float v[16];
-      tmem_ld16(tl + COL_DA + s0, v);
+    float pba = 0.f;
+    for (int cb = half * 64; cb < half * 64 + 64; cb += 32) {
+      uint4 vv[4];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int s = s0 + e;
-        const bool low = i > s;
-        const float da = low ? -v[e] : 0.f;
-        AQ[i * MP + s] = da;
-        PM[i * MP + s] = low ? __fmul_rn(__fmul_rn(da, bi), expf(__fsub_rn(Gs[i], Gs[s]))) : 0.f;
+      for (int x = 0; x < 4; ++x) vv[x] = live ? *reinterpret_cast<const uint4*>(vb + i * vstride + cb + 8 * x) : zero4;
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        const int c0 = cb + 16 * sub;
+        float xr[16], vf[16], dv[16];
+        tmem_ld16(tl + 0 + c0, xr);
+        unpack8(vv[2 * sub], vf);
+        unpack8(vv[2 * sub + 1], vf + 8);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          dv[e] = __fmul_rn(bi, xr[e]);
+          pba = __fmaf_rn(vf[e], xr[e], pba);
+        }
+        if (live) {
+          float4* dvp = reinterpret_cast<float4*>(a.dv + orow0 + (int64_t)i * vstride + c0);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) dvp[x] = make_float4(dv[4 * x], dv[4 * x + 1], dv[4 * x + 2], dv[4 * x + 3]);
+        }
+        split8(gX, gX + IMG, kmajor_off(i, c0, D), xr);
+        split8(gX, gX + IMG, kmajor_off(i, c0 + 8, D), xr + 8);
       }
     }
+    dba[half * C + i] = pba;
   }
-  fence_before_sync();
-  __syncthreads();
-  // ---- phase 4: dK += dAm K + dAm^T K
+  // ---- round 4: Y = T^T dW -> TMEM 0 (operands already in place)
   if (ok) {
-    build_split<false, C, C>(ar + P4_AM, ar + P4_AM + 8 * KB, PM, MP, C);
-    build_split<true, C, C>(ar + P4_AMT, ar + P4_AMT + 8 * KB, PM, MP, C);
-    sync_for_mma();
-    if (t == 0) {
-      fence_after_sync();
-      mma_terms(tb + COL_DK, sa + P4_AM, sa + P4_AM + 8 * KB, sa + KT, sa + KT, C, idesc_bf16(128, D), 2, true);
-      mma_terms(tb + COL_DK, sa + P4_AMT, sa + P4_AMT + 8 * KB, sa + KT, sa + KT, C, idesc_bf16(128, D), 2, true);
-      mma_commit(bar);
-    }
+    issue([&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 48 * KB, sa + 64 * KB, C, idesc_bf16(128, D), 3); });
+    wait_mma();
   }
-  if (t < C) {  // dbeta and dG from A while the products run
-    float b = 0.f, rw = 0.f, cl = 0.f;
-    for (int s2 = 0; s2 < t; ++s2) {
-      b = __fmaf_rn(AQ[t * MP + s2], AP[t * MP + s2], b);
-      rw = __fmaf_rn(__fmul_rn(AQ[t * MP + s2], bs[t]), AP[t * MP + s2], rw);
-    }
-    for (int i2 = t + 1; i2 < C; ++i2) cl = __fmaf_rn(__fmul_rn(AQ[i2 * MP + t], bs[i2]), AP[i2 * MP + t], cl);
-    dbc[t] = b;
-    dGe[t] = __fsub_rn(rw, cl);
-  }
-  if (ok) wait_mma();
-  if (ok && rowlane) {  // dK + dec U dS_end + beta e^G Y
+  if (ok && rowlane) {  // kY; dk <- dK1 + beta e^G Y; Y image -> workspace
     const int s2 = row;
     const bool live = s2 < n;
-    const float* ue_row = a.b.UdSe + ch * CD + (int64_t)s2 * D;
-    const float ds = dec[s2], bkv = __fmul_rn(bs[s2], eG[s2]);
-    float pcs = 0.f;
+    const float bkv = __fmul_rn(bs[s2], eG[s2]);
+    float pky = 0.f;
     for (int cb = half * 64; cb < half * 64 + 64; cb += 32) {
-      float4 ue4[8];
       uint4 kv[4];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) ue4[x] = *reinterpret_cast<const float4*>(ue_row + cb + 4 * x);
 #pragma unroll
       for (int x = 0; x < 4; ++x) kv[x] = live ? *reinterpret_cast<const uint4*>(kb + s2 * kstride + cb + 8 * x) : zero4;
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
         const int c0 = cb + 16 * sub;
-        float v[16], yr[16], kf[16], ue[16], o[16];
-        tmem_ld16(tl + COL_DK + c0, v);
-        tmem_ld16(tl + COL_Y + c0, yr);
+        float yr[16], d1[16], kf[16];
+        tmem_ld16(tl + 0 + c0, yr);
+        tmem_ld16(tl + 128 + c0, d1);
         unpack8(kv[2 * sub], kf);
         unpack8(kv[2 * sub + 1], kf + 8);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          ue[4 * x] = ue4[4 * sub + x].x;
-          ue[4 * x + 1] = ue4[4 * sub + x].y;
-          ue[4 * x + 2] = ue4[4 * sub + x].z;
-          ue[4 * x + 3] = ue4[4 * sub + x].w;
-        }
-#pragma unroll
         for (int e = 0; e < 16; ++e) {
-          o[e] = __fmaf_rn(bkv, yr[e], __fmaf_rn(ds, ue[e], v[e]));
-          pcs = __fmaf_rn(ue[e], kf[e], pcs);
+          pky = __fmaf_rn(kf[e], yr[e], pky);
+          d1[e] = __fmaf_rn(bkv, yr[e], d1[e]);
         }
         if (live) {
           float4* dkp = reinterpret_cast<float4*>(a.b.dk_part + orow0 + (int64_t)s2 * vstride + c0);
 #pragma unroll
-          for (int x = 0; x < 4; ++x) dkp[x] = make_float4(o[4 * x], o[4 * x + 1], o[4 * x + 2], o[4 * x + 3]);
+          for (int x = 0; x < 4; ++x) dkp[x] = make_float4(d1[4 * x], d1[4 * x + 1], d1[4 * x + 2], d1[4 * x + 3]);
         }
+        split8(gY, gY + IMG, kmajor_off(s2, c0, D), yr);
+        split8(gY, gY + IMG, kmajor_off(s2, c0 + 8, D), yr + 8);
+      }
+    }
+    kY[half * C + s2] = pky;
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (ok && t < C) {  // per-token partial sums for G2
+    float* gp = a.b.img + ch * (int64_t)prep_w_floats(C, D) + C * D / 2;  // after the K rows image
+    gp[t] = __fmul_rn(eG[t], __fadd_rn(dGa[t], dGa[C + t]));                                // e^G dO S0 . q
+    gp[C + t] = __fsub_rn(__fadd_rn(rowp[t], rowp[C + t]), __fadd_rn(colp[t], colp[C + t]));  // dG_b
+    gp[2 * C + t] = __fadd_rn(dba[t], dba[C + t]);                                          // v . X
+    gp[3 * C + t] = __fadd_rn(kY[t], kY[C + t]);                                            // k . Y
+  }
+  if (!ok && t == 0) {
+    set_error(a.hdr, GDN_DEVERR_TIMEOUT);
+    if (pending) mbar_wait(bar, phase);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tb, TMEM1);
+}
+
+__global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
+  using namespace tcd;
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smd[];
+  unsigned char* ar = smd;
+  float* Gs = reinterpret_cast<float*>(smd + ARENA);
+  float* eG = Gs + C;
+  float* dec = eG + C;
+  float* bs = dec + C;
+  float* gp = bs + C;          // [4][C] G1's per-token sums
+  float* rowb = gp + 4 * C;    // [2][C] dbeta_c row sums, one per column half
+  float* rowg = rowb + 2 * C;  // [2][C] dG_e row sums
+  float* colg = rowg + 2 * C;  // [2][C] dG_e column sums, one per row half
+  float* cs = colg + 2 * C;    // [2][C] U dS_end . k
+  float* dgv = cs + 2 * C;
+  float* csv = dgv + C;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(csv + C);  // [0] MMA, [1] bulk copies
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+  if (!a.hdr->valid) return;
+  const Dims dm = a.dm;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int64_t c = blockIdx.x;
+  const int h = blockIdx.y;
+  const ChunkRec rec = a.chunks[c];
+  const int n = rec.len;
+  const int64_t tok0 = rec.tok0;
+  const int64_t ch = c * dm.hv + h;
+  const int64_t CD = (int64_t)C * D;
+  const int64_t vstride = (int64_t)dm.hv * D;
+  const int64_t orow0 = tok0 * vstride + (int64_t)h * D;
+  const unsigned char* gX = reinterpret_cast<const unsigned char*>(a.b.L + ch * (int64_t)D * D);
+  const unsigned char* gY = gX + 2 * IMG;
+  const float* img = a.b.img + ch * (int64_t)prep_w_floats(C, D);  // K rows image, then G1's sums
+  const bool rowlane = (warp & 3) < 2;
+  const int row = (warp & 3) * 32 + lane;
+  const int half = warp >> 2;
+  // arena: round A W hi/lo @0/@16, Y hi|lo @32, K rows @64; round B Ut hi/lo @0/@16,
+  // X hi|lo @32, K^T @80; round C dAm hi/lo @0/@8, dAm^T hi/lo @16/@24
+  if (t == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+    mbar_expect_tx(&bar[1], 3 * IMG);
+    bulk_g2s(ar + 32 * KB, gY, 2 * IMG, &bar[1]);
+    bulk_g2s(ar + 64 * KB, img, IMG, &bar[1]);
+  }
+  {
+    SplitTile<false, C, D> w;
+    w.load(a.b.W + ch * CD, D, C);
+    float g0 = 0.f, b0 = 0.f, p0 = 0.f;
+    if (t < C) {
+      g0 = a.b.G[ch * C + t];
+      b0 = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
+    }
+    p0 = img[C * D / 2 + t];  // t < 4 C
+    w.store(ar, ar + 16 * KB);
+    if (t < C) {
+      Gs[t] = g0;
+      bs[t] = b0;
+    }
+    gp[t] = p0;
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM2);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tb = *tslot;
+  const uint32_t tl = tmem_lane_addr(tb, warp, 0);
+  const uint32_t sa = smem_u32(ar);
+  uint32_t phase = 0, cphase = 0;
+  bool ok = true, pending = false, cpending = true;
+  auto wait_mma = [&]() {
+    const bool done = mbar_wait(&bar[0], phase);
+    if (done) {
+      phase ^= 1u;
+      pending = false;
+    }
+    ok = __syncthreads_and(done) != 0;
+    fence_after_sync();
+  };
+  // all threads: generic-proxy writes -> tensor core; thread 0 waits for the bulk copies
+  // (copies = true), then issues; every thread learns whether the copies arrived
+  auto issue = [&](bool copies, auto&& mmas) {
+    fence_proxy_async();
+    fence_before_sync();
+    bool got = true;
+    if (t == 0 && copies) {
+      got = mbar_wait(&bar[1], cphase);
+      if (got) {
+        cphase ^= 1u;
+        cpending = false;
+      }
+    }
+    ok = __syncthreads_and(got) != 0;
+    if (ok && t == 0) {
+      fence_after_sync();
+      mmas();
+      mma_commit(&bar[0]);
+      pending = true;
+    }
+  };
+  // ---- round A: dA = Y W^T -> TMEM 0, K K^T -> TMEM 64
+  issue(true, [&] {
+    mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa, sa + 16 * KB, D, idesc_bf16(128, C), 3);
+    mma_terms(tb + 64, sa + 64 * KB, sa + 64 * KB, sa + 64 * KB, sa + 64 * KB, D, idesc_bf16(128, C), 1);
+  });
+  SplitTile<false, C, D> ut;
+  ut.load(a.b.Ut + ch * CD, D, C);
+  if (t < C) {
+    eG[t] = expf(Gs[t]);
+    dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
+  }
+  if (ok) wait_mma();
+  // ---- round B: dA += X Ut^T
+  if (ok) {
+    if (t == 0) {
+      mbar_expect_tx(&bar[1], 2 * IMG);
+      bulk_g2s(ar + 32 * KB, gX, 2 * IMG, &bar[1]);
+      cpending = true;
+    }
+    ut.store(ar, ar + 16 * KB);
+    transpose_image(ar + 80 * KB, ar + 64 * KB, D, C);  // K^T
+    issue(true, [&] {
+      mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa, sa + 16 * KB, D, idesc_bf16(128, C), 3, true);
+    });
+    if (ok) wait_mma();
+  }
+  if (ok && rowlane) {  // dA (strictly lower), A' = Gam (.) K K^T; dbeta_c, dG_e sums; dAm image
+    const int i = row;
+    const float bi = bs[i], gi = Gs[i];
+    float rb = 0.f, rg = 0.f;
+#pragma unroll
+    for (int s1 = 0; s1 < 2; ++s1) {
+      const int s0 = half * 32 + 16 * s1;
+      float v[16], kk[16];
+      tmem_ld16(tl + 0 + s0, v);
+      tmem_ld16(tl + 64 + s0, kk);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int s = s0 + e;
+        const bool low = i > s;
+        const float gam = expf(__fsub_rn(gi, Gs[s]));
+        const float da = low ? -v[e] : 0.f;
+        const float ap = low ? __fmul_rn(gam, kk[e]) : 0.f;
+        const float dab = __fmul_rn(da, bi);
+        rb = __fmaf_rn(da, ap, rb);
+        const float tg = __fmul_rn(dab, ap);
+        rg = __fadd_rn(rg, tg);
+        v[e] = low ? __fmul_rn(dab, gam) : 0.f;
+        kk[e] = tg;
+      }
+      split8(ar, ar + 8 * KB, kmajor_off(i, s0, C), v);
+      split8(ar, ar + 8 * KB, kmajor_off(i, s0 + 8, C), v + 8);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float cg = warp_sum(kk[e]);
+        if (lane == 0) colg[(warp & 3) * C + s0 + e] = cg;
+      }
+    }
+    rowb[half * C + i] = rb;
+    rowg[half * C + i] = rg;
+  }
+  fence_before_sync();
+  __syncthreads();
+  // ---- round C: dK2 = dAm K + dAm^T K -> TMEM 0
+  if (ok) {
+    transpose_image(ar + 16 * KB, ar, C, C);
+    transpose_image(ar + 24 * KB, ar + 8 * KB, C, C);
+    issue(false, [&] {
+      mma_terms(tb + 0, sa, sa + 8 * KB, sa + 80 * KB, sa + 80 * KB, C, idesc_bf16(128, D), 2);
+      mma_terms(tb + 0, sa + 16 * KB, sa + 24 * KB, sa + 80 * KB, sa + 80 * KB, C, idesc_bf16(128, D), 2, true);
+    });
+    if (ok) wait_mma();
+  }
+  if (ok && rowlane) {  // dk = G1's part + dK2 + dec U dS_end; U dS_end . k
+    const int s2 = row;
+    const bool live = s2 < n;
+    const float* ue_row = a.b.UdSe + ch * CD + (int64_t)s2 * D;
+    float* dk_row = a.b.dk_part + orow0 + (int64_t)s2 * vstride;
+    const float ds = dec[s2];
+    float pcs = 0.f;
+    for (int cb = half * 64; cb < half * 64 + 64; cb += 16) {
+      float4 ue4[4], pk4[4];
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        ue4[x] = *reinterpret_cast<const float4*>(ue_row + cb + 4 * x);
+        pk4[x] = live ? *reinterpret_cast<const float4*>(dk_row + cb + 4 * x) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      const uint4 k0 = *reinterpret_cast<const uint4*>(ar + 64 * KB + kmajor_off(s2, cb, D));
+      const uint4 k1 = *reinterpret_cast<const uint4*>(ar + 64 * KB + kmajor_off(s2, cb + 8, D));
+      float v[16], kf[16], ue[16], pk[16];
+      tmem_ld16(tl + 0 + cb, v);
+      unpack8(k0, kf);
+      unpack8(k1, kf + 8);
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        ue[4 * x] = ue4[x].x;
+        ue[4 * x + 1] = ue4[x].y;
+        ue[4 * x + 2] = ue4[x].z;
+        ue[4 * x + 3] = ue4[x].w;
+        pk[4 * x] = pk4[x].x;
+        pk[4 * x + 1] = pk4[x].y;
+        pk[4 * x + 2] = pk4[x].z;
+        pk[4 * x + 3] = pk4[x].w;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        v[e] = __fmaf_rn(ds, ue[e], __fadd_rn(pk[e], v[e]));
+        pcs = __fmaf_rn(ue[e], kf[e], pcs);
+      }
+      if (live) {
+        float4* o4 = reinterpret_cast<float4*>(dk_row + cb);
+#pragma unroll
+        for (int x = 0; x < 4; ++x) o4[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
       }
     }
     cs[half * C + s2] = pcs;
@@ -2126,7 +2301,8 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
   if (!ok) {
     if (t == 0) {
       set_error(a.hdr, GDN_DEVERR_TIMEOUT);
-      mbar_wait(bar, phase);
+      if (pending) mbar_wait(&bar[0], phase);
+      if (cpending) mbar_wait(&bar[1], cphase);
     }
   }
   // dG per token (independent terms, one thread each), then thread 0 takes the two
@@ -2134,12 +2310,11 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
   if (ok && t < C) {
     const int i = t;
     const float csi = __fmul_rn(dec[i], __fadd_rn(cs[i], cs[C + i]));
-    const float ga = __fmul_rn(eG[i], __fadd_rn(dGa[i], dGa[C + i]));
-    const float ky = __fadd_rn(kY[i], kY[C + i]);
-    float v = __fadd_rn(ga, dGb[i]);
+    const float dGe = __fsub_rn(__fadd_rn(rowg[i], rowg[C + i]), __fadd_rn(colg[i], colg[C + i]));
+    float v = __fadd_rn(gp[i], gp[C + i]);
     v = __fsub_rn(v, csi);
-    v = __fmaf_rn(__fmul_rn(bs[i], eG[i]), ky, v);
-    v = __fadd_rn(v, dGe[i]);
+    v = __fmaf_rn(__fmul_rn(bs[i], eG[i]), gp[3 * C + i], v);
+    v = __fadd_rn(v, dGe);
     dgv[i] = v;
     csv[i] = csi;
   }
@@ -2159,15 +2334,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_grad_tc(BwdArgs a) {
   }
   __syncthreads();
   if (ok && t < n) {
-    const float ky = __fadd_rn(kY[t], kY[C + t]);
+    const float dbc = __fadd_rn(rowb[t], rowb[C + t]);
     a.dg[(tok0 + t) * dm.hv + h] = dgv[t];
-    a.dbeta[(tok0 + t) * dm.hv + h] = __fadd_rn(__fmaf_rn(eG[t], ky, __fadd_rn(dba[t], dba[C + t])), dbc[t]);
+    a.dbeta[(tok0 + t) * dm.hv + h] = __fadd_rn(__fmaf_rn(eG[t], gp[3 * C + t], gp[2 * C + t]), dbc);
   }
   fence_before_sync();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
+  if (warp == 0) tmem_dealloc(tb, TMEM2);
 }
-
 template <int D, typename Tin>
 void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, void* mark_ctx,
                   cudaStream_t st) {
@@ -2202,14 +2376,16 @@ void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, vo
   mark(mark_ctx, n_chunks > 0 ? 1 : 0);
   if (n_chunks > 0) {
     if (boundary_on_tensor_cores(a.dm)) {
-      ensure_smem_bwd(k_bwd_grad_tc, tcd::SMEM);
-      k_bwd_grad_tc<<<gc, 256, tcd::SMEM, st>>>(a);
+      ensure_smem_bwd(k_bwd_grad1_tc, tcd::SMEM1);
+      k_bwd_grad1_tc<<<gc, 256, tcd::SMEM1, st>>>(a);
+      ensure_smem_bwd(k_bwd_grad2_tc, tcd::SMEM2);
+      k_bwd_grad2_tc<<<gc, 256, tcd::SMEM2, st>>>(a);
     } else {
       ensure_smem_bwd(k_bwd_grad<D, Tin>, bgrad_smem<D>());
       k_bwd_grad<D, Tin><<<gc, NT, bgrad_smem<D>(), st>>>(a);
     }
   }
-  mark(mark_ctx, n_chunks > 0 ? 1 : 0);
+  mark(mark_ctx, n_chunks > 0 ? (boundary_on_tensor_cores(a.dm) ? 2 : 1) : 0);
   if (a.T > 0) {
     const int64_t total = a.T * a.dm.hqk * D;
     const int blocks = (int)((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
