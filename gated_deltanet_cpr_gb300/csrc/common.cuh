@@ -2,7 +2,7 @@
 //
 // Bit-exactness across prefill, trainer forward and decode rests on two routines that
 // every mode calls with the same operands in the same order:
-//   * token_step  -- one step of the gated delta rule on a state row (the recurrence that
+//   * token_step  -- one step of the gated delta rule on the register-held state (the recurrence that
 //                    CPR keeps as its main computation; IsoExec page, section
 //                    "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet");
 //   * the boundary routines (prep_* and chain_*) -- the chunk (WY/UT) form that advances
@@ -112,64 +112,121 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return *reinterpret_cast<const float2*>(&d);
 }
 
-// shared-memory vector load that the compiler may not merge with an earlier load of the
-// same address (keeps the first pass's k out of registers during the update pass)
-__device__ __forceinline__ float4 lds4_fresh(const float* p) {
-  float4 v;
-  asm volatile("ld.volatile.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"((uint32_t)__cvta_generic_to_shared(p)));
-  return v;
+// Register layout of the state for the token step.  A warp holds 16 state rows; lane l is in
+// row group g = l >> 3 (rows 16 w + 4 g + r, r = 0..3, of warp w) at column block b = l & 7,
+// and holds the float4 column groups 8 j + b (columns 32 j + 4 b .. + 3, j = 0 .. d/32 - 1)
+// of its 4 rows: S[r][j].  A d x d state takes 2 d threads (d / 16 warps), d / 2 floats each.
+template <int D>
+struct StateLayout {
+  static constexpr int J = D / 32;
+  int row0;  // first of the lane's 4 rows
+  int b;     // column block
+  __device__ __forceinline__ explicit StateLayout(int t) : row0(16 * (t >> 5) + 4 * ((t & 31) >> 3)), b(t & 7) {}
+  __device__ __forceinline__ int col(int j) const { return 32 * j + 4 * b; }
+  // the row whose output this lane's reduction ends with, and whether the lane writes it
+  __device__ __forceinline__ int out_row() const { return row0 + ((b >> 1) & 3); }
+  __device__ __forceinline__ bool writes_out() const { return (b & 1) == 0; }
+  // state rows start at src (row stride D floats)
+  __device__ __forceinline__ void load(float4 (&S)[4][J], const float* src) const {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < J; ++j) S[r][j] = *reinterpret_cast<const float4*>(src + (int64_t)(row0 + r) * D + col(j));
+  }
+  __device__ __forceinline__ void store(const float4 (&S)[4][J], float* dst) const {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < J; ++j) *reinterpret_cast<float4*>(dst + (int64_t)(row0 + r) * D + col(j)) = S[r][j];
+  }
+};
+
+// Sum over the 8 lanes of a row group of x[r] (r = 0..3, one value per row of the group):
+// a fixed xor-4, xor-2, xor-1 tree.  The xor-4 step leaves rows 0, 1 on lanes with bit 2
+// clear and rows 2, 3 on the others, the xor-2 step one row per lane, the xor-1 step adds
+// the partner holding the same row; lane b ends with the total of row (b >> 1) & 3.  Every
+// total is one fixed expression of the 8 lane values (fp32 addition is commutative, so the
+// two lanes holding a total hold the same bits).
+__device__ __forceinline__ float group_reduce4(const float (&x)[4], int b) {
+  const bool h2 = (b & 4) != 0, h1 = (b & 2) != 0;
+  const float y0 = __fadd_rn(h2 ? x[2] : x[0], __shfl_xor_sync(0xffffffffu, h2 ? x[0] : x[2], 4));
+  const float y1 = __fadd_rn(h2 ? x[3] : x[1], __shfl_xor_sync(0xffffffffu, h2 ? x[1] : x[3], 4));
+  const float z = __fadd_rn(h1 ? y1 : y0, __shfl_xor_sync(0xffffffffu, h1 ? y0 : y1, 2));
+  return __fadd_rn(z, __shfl_xor_sync(0xffffffffu, z, 1));
+}
+// group_reduce4, then every lane of the group gets all four totals (two more exchanges)
+__device__ __forceinline__ void group_allreduce4(const float (&x)[4], float (&tot)[4], int b) {
+  const bool h2 = (b & 4) != 0, h1 = (b & 2) != 0;
+  const float mine = group_reduce4(x, b);                        // row 2 h2 + h1
+  const float other = __shfl_xor_sync(0xffffffffu, mine, 2);     // row 2 h2 + !h1
+  const float lo = h1 ? other : mine, hi = h1 ? mine : other;     // rows 2 h2, 2 h2 + 1
+  const float lo_x = __shfl_xor_sync(0xffffffffu, lo, 4), hi_x = __shfl_xor_sync(0xffffffffu, hi, 4);
+  tot[0] = h2 ? lo_x : lo;
+  tot[1] = h2 ? hi_x : hi;
+  tot[2] = h2 ? lo : lo_x;
+  tot[3] = h2 ? hi : hi_x;
 }
 
-// One gated delta-rule step on row i of the state, held by a pair of adjacent lanes
-// (half = lane & 1).  The pair splits the D columns into float4 groups: register group m
-// holds columns [8m + 4*half, 8m + 4*half + 4).  Order of operations (the recurrence's
-// own order):
-//     S <- a S;   p = S k;   u = beta (v_i - p);   S <- S + u k^T;   o_i = S q
-// Each dot is four partial sums over the lane's columns in ascending m (partial e takes
-// component e of every group), combined as (p0 + p1) + (p2 + p3), then added to the
-// partner lane's partial with one xor-shuffle; fp32 addition is commutative, so both lanes
-// hold identical bits.  k and q are fp32 copies in shared memory (exact widenings of the
-// inputs).  The update S <- S + u k^T and the output dot are two passes over the state
-// (the same operations on every element, in the same order), so that k and q are never
-// both held in registers.  All 32 lanes of the warp must call this together.
+// One gated delta-rule step on the lane's 4 state rows (StateLayout), in the recurrence's
+// own order of operations:
+//     S <- a S;   p = S k;   u = beta (v - p);   S <- S + u k^T;   o = S q
+// Each row's dot: per lane two float2 partials over the lane's column groups in ascending j
+// (.x/.y = columns 4b, 4b+1 and 4b+2, 4b+3 of the group), combined as (x0 + y0) + (x1 + y1)
+// for (p01, p23), then group_reduce4 over the 8 lanes.  k (kept in registers from the dot to
+// the update) and q are fp32 copies in shared memory (exact widenings of the inputs); v4 is
+// v of the lane's 4 rows.  Returns o of row out_row().  All 32 lanes of the warp call this
+// together.
 template <int D>
-__device__ __forceinline__ float token_step(float4 (&S)[D / 8], const float* __restrict__ k_sh,
-                                            const float* __restrict__ q_sh, float a, float beta,
-                                            float v_i, int half) {
+__device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], const float* __restrict__ k_sh,
+                                            const float* __restrict__ q_sh, float a, float beta, float4 v4,
+                                            int b) {
+  constexpr int J = D / 32;
+  float4 kk[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) kk[j] = *reinterpret_cast<const float4*>(k_sh + 32 * j + 4 * b);
   const float2 a2 = make_float2(a, a);
-  float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
+  float part[4];
 #pragma unroll
-  for (int m = 0; m < D / 8; ++m) {
-    const float4 kk = *reinterpret_cast<const float4*>(k_sh + 8 * m + 4 * half);
-    float2 s01 = mul2(a2, make_float2(S[m].x, S[m].y));
-    float2 s23 = mul2(a2, make_float2(S[m].z, S[m].w));
-    p01 = fma2(s01, make_float2(kk.x, kk.y), p01);
-    p23 = fma2(s23, make_float2(kk.z, kk.w), p23);
-    S[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
-  }
-  float part = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
-  const float p = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
-  const float u = __fmul_rn(beta, __fsub_rn(v_i, p));
-  const float2 u2 = make_float2(u, u);
+  for (int r = 0; r < 4; ++r) {
+    float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int m = 0; m < D / 8; ++m) {
-    const float4 kk = lds4_fresh(k_sh + 8 * m + 4 * half);
-    const float2 s01 = fma2(u2, make_float2(kk.x, kk.y), make_float2(S[m].x, S[m].y));
-    const float2 s23 = fma2(u2, make_float2(kk.z, kk.w), make_float2(S[m].z, S[m].w));
-    S[m] = make_float4(s01.x, s01.y, s23.x, s23.y);
+    for (int j = 0; j < J; ++j) {
+      const float2 s01 = mul2(a2, make_float2(S[r][j].x, S[r][j].y));
+      const float2 s23 = mul2(a2, make_float2(S[r][j].z, S[r][j].w));
+      p01 = fma2(s01, make_float2(kk[j].x, kk[j].y), p01);
+      p23 = fma2(s23, make_float2(kk[j].z, kk[j].w), p23);
+      S[r][j] = make_float4(s01.x, s01.y, s23.x, s23.y);
+    }
+    part[r] = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
   }
-  p01 = make_float2(0.f, 0.f);
-  p23 = make_float2(0.f, 0.f);
+  float p[4];
+  group_allreduce4(part, p, b);
+  const float v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-  for (int m = 0; m < D / 8; ++m) {
-    const float4 qq = *reinterpret_cast<const float4*>(q_sh + 8 * m + 4 * half);
-    p01 = fma2(make_float2(S[m].x, S[m].y), make_float2(qq.x, qq.y), p01);
-    p23 = fma2(make_float2(S[m].z, S[m].w), make_float2(qq.z, qq.w), p23);
+  for (int r = 0; r < 4; ++r) {
+    const float u = __fmul_rn(beta, __fsub_rn(v[r], p[r]));
+    const float2 u2 = make_float2(u, u);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const float2 s01 = fma2(u2, make_float2(kk[j].x, kk[j].y), make_float2(S[r][j].x, S[r][j].y));
+      const float2 s23 = fma2(u2, make_float2(kk[j].z, kk[j].w), make_float2(S[r][j].z, S[r][j].w));
+      S[r][j] = make_float4(s01.x, s01.y, s23.x, s23.y);
+    }
   }
-  part = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
-  return __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
+  float4 qq[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) qq[j] = *reinterpret_cast<const float4*>(q_sh + 32 * j + 4 * b);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      p01 = fma2(make_float2(S[r][j].x, S[r][j].y), make_float2(qq[j].x, qq[j].y), p01);
+      p23 = fma2(make_float2(S[r][j].z, S[r][j].w), make_float2(qq[j].z, qq[j].w), p23);
+    }
+    part[r] = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
+  }
+  return group_reduce4(part, b);
 }
 
 // T = (I + A)^{-1} for a strictly lower C x C matrix A in shared memory (row stride CPA; T
@@ -232,12 +289,6 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, int C
 template <int NT>
 __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float* Tm, float* Xs, int C, int CP) {
   blocked_unit_lower_inverse<NT>(A, CP, Tm, CP, Xs, C);
-}
-
-// State row i, half h: global float offset of register group m.
-template <int D>
-__device__ __forceinline__ int state_col(int m, int half) {
-  return 8 * m + 4 * half;
 }
 
 }  // namespace gdn

@@ -1192,20 +1192,22 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
     as[r] = expf(in.g[(tok0 + r) * dm.hv + h]);
     bs[r] = in.beta[(tok0 + r) * dm.hv + h];
   }
-  const int i = t >> 1, half = t & 1;
-  float4 S[D / 8];
-  const float* src = w.bnd + (c * dm.hv + h) * SZ + (int64_t)i * D;
+  const StateLayout<D> lay(t);
+  float4 S[4][D / 32];
+  const float* src = w.bnd + (c * dm.hv + h) * SZ;
   if constexpr (kSkip) {
-    if (first > 0) src = w.run_state + ((int64_t)w.run_slot[rec.seq] * dm.hv + h) * SZ + (int64_t)i * D;
+    if (first > 0) src = w.run_state + ((int64_t)w.run_slot[rec.seq] * dm.hv + h) * SZ;
   }
-#pragma unroll
-  for (int m = 0; m < D / 8; ++m) S[m] = *reinterpret_cast<const float4*>(src + state_col<D>(m, half));
+  lay.load(S, src);
   __syncthreads();
 
+  const int orow = lay.out_row();
+  const bool writer = lay.writes_out();
   for (int tt = first; tt < len; ++tt) {
-    const float o = token_step<D>(S, ks + tt * D, qs + tt * D, as[tt], bs[tt], vs[tt * D + i], half);
+    const float4 v4 = *reinterpret_cast<const float4*>(vs + tt * D + lay.row0);
+    const float o = token_step<D>(S, ks + tt * D, qs + tt * D, as[tt], bs[tt], v4, lay.b);
     __syncwarp();
-    if (half == 0) vs[tt * D + i] = o;
+    if (writer) vs[tt * D + orow] = o;
   }
   __syncthreads();
   // the chunk record again (an L2 read instead of registers held through the token loop)
@@ -1222,18 +1224,10 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   // state decode continues from: the token recurrence through a final partial chunk
   const SeqRec sr = w.seqs[rc.seq];
   if (rc.jloc == sr.nchunks - 1 && (sr.len % dm.C) != 0) {
-    if (w.state_out) {
-      float* dst = w.state_out + ((int64_t)rc.seq * dm.hv + h) * SZ + (int64_t)i * D;
-#pragma unroll
-      for (int m = 0; m < D / 8; ++m) *reinterpret_cast<float4*>(dst + state_col<D>(m, half)) = S[m];
-    }
+    if (w.state_out) lay.store(S, w.state_out + ((int64_t)rc.seq * dm.hv + h) * SZ);
     if (w.cache_run) {
       const int sl = w.slot_of_seq ? w.slot_of_seq[rc.seq] : rc.seq;
-      if (sl >= 0 && sl < w.cache_slots) {
-        float* dst = w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)i * D;
-#pragma unroll
-        for (int m = 0; m < D / 8; ++m) *reinterpret_cast<float4*>(dst + state_col<D>(m, half)) = S[m];
-      }
+      if (sl >= 0 && sl < w.cache_slots) lay.store(S, w.cache_run + ((int64_t)sl * dm.hv + h) * SZ);
     }
   }
 }
@@ -1286,23 +1280,21 @@ __global__ void __launch_bounds__(2 * D, 2) k_decode(Dims dm, TokenArrays in, De
 #pragma unroll
     for (int e = 0; e < 8; ++e) qs[8 * t + e] = tmp[e];
   }
-  const int i = t >> 1, half = t & 1;
-  float4 S[D / 8];
-  float* srow = w.s_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)i * D;
-#pragma unroll
-  for (int m = 0; m < D / 8; ++m) S[m] = *reinterpret_cast<const float4*>(srow + state_col<D>(m, half));
+  const StateLayout<D> lay(t);
+  float4 S[4][D / 32];
+  float* st = w.s_run + ((int64_t)sl * dm.hv + h) * SZ;
+  lay.load(S, st);
   const float a = expf(in.g[(int64_t)n * dm.hv + h]);
   const float b = in.beta[(int64_t)n * dm.hv + h];
-  const Tin vraw = vin[((int64_t)n * dm.hv + h) * D + i];
+  const Tin* vrow = vin + ((int64_t)n * dm.hv + h) * D;
+  const float4 v4 = make_float4(to_f32(vrow[lay.row0]), to_f32(vrow[lay.row0 + 1]), to_f32(vrow[lay.row0 + 2]),
+                                to_f32(vrow[lay.row0 + 3]));
   __syncthreads();
-  const float o = token_step<D>(S, ks, qs, a, b, to_f32(vraw), half);
-#pragma unroll
-  for (int m = 0; m < D / 8; ++m) *reinterpret_cast<float4*>(srow + state_col<D>(m, half)) = S[m];
+  const float o = token_step<D>(S, ks, qs, a, b, v4, lay.b);
+  lay.store(S, st);
   const int ti = p % C;
-  if (half == 0) {
-    store_out(static_cast<Tout*>(w.o) + ((int64_t)n * dm.hv + h) * D + i, o);
-    static_cast<Tin*>(w.tail_v)[(((int64_t)sl * C + ti) * dm.hv + h) * D + i] = vraw;
-  }
+  if (lay.writes_out()) store_out(static_cast<Tout*>(w.o) + ((int64_t)n * dm.hv + h) * D + lay.out_row(), o);
+  if (t < D) static_cast<Tin*>(w.tail_v)[(((int64_t)sl * C + ti) * dm.hv + h) * D + t] = vrow[t];
   if (t == 0) {
     w.tail_g[((int64_t)sl * C + ti) * dm.hv + h] = in.g[(int64_t)n * dm.hv + h];
     w.tail_beta[((int64_t)sl * C + ti) * dm.hv + h] = b;

@@ -127,8 +127,10 @@ std::string policy_text(const gdn_cpr_shape* s) {
            "chunks=aligned to each sequence's first token; state_out = token recurrence through a partial last chunk\n"
            "contraction=none (explicit round-to-nearest fma/mul/add)\n"
            "exp=expf\n"
-           "token_step=lane pair per state row; S*=a; p=S.k; u=beta*(v-p); S+=u k^T; o=S.q; "
-           "each dot: 4 partials per lane over ascending column groups, (p0+p1)+(p2+p3), then one xor-1 shuffle add\n"
+           "token_step=4 state rows x d/8 columns per lane (columns 32j+4b..+3), 8 lanes per row group; "
+           "S*=a; p=S.k; u=beta*(v-p); S+=u k^T; o=S.q; "
+           "each dot: per lane and row two float2 partials over ascending j, (x0+y0)+(x1+y1), "
+           "then across the 8 lanes a fixed xor-4, xor-2, xor-1 tree\n"
            "cumsum_g=sequential fp32, ascending token\n"
            "triangular_solve=(I+A)^-1 blocked by 16: diagonal blocks by forward substitution, "
            "off-diagonal blocks by increasing distance, every sum ascending with one accumulator\n"
