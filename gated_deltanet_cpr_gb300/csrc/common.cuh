@@ -174,18 +174,22 @@ __device__ __forceinline__ void group_allreduce4(const float (&x)[4], float (&to
 // (.x/.y = columns 4b, 4b+1 and 4b+2, 4b+3 of the group), combined as (x0 + y0) + (x1 + y1)
 // for (p01, p23), then group_reduce4 over the 8 lanes.  k (kept in registers from the dot to
 // the update) and q are fp32 copies in shared memory (exact widenings of the inputs); v4 is
-// v of the lane's 4 rows.  Returns o of row out_row().  All 32 lanes of the warp call this
-// together.
+// v of the lane's 4 rows.  The step is split in two sweeps so that a token loop can overlap
+// the output reduction of one token with the first sweep of the next:
+//   ts_decay_dot   S <- a S, k into registers, the lane's partials of S k
+//   ts_update_dot  (after group_allreduce4 of those partials) the update and the lane's
+//                  partials of S q, to be reduced by group_reduce4
+// token_step is the whole step.  All 32 lanes of the warp call these together.
+__device__ __forceinline__ float ts_combine(float2 p01, float2 p23) {
+  return __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
+}
 template <int D>
-__device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], const float* __restrict__ k_sh,
-                                            const float* __restrict__ q_sh, float a, float beta, float4 v4,
-                                            int b) {
+__device__ __forceinline__ void ts_decay_dot(float4 (&S)[4][D / 32], const float* __restrict__ k_sh, float a, int b,
+                                             float4 (&kk)[D / 32], float (&part)[4]) {
   constexpr int J = D / 32;
-  float4 kk[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) kk[j] = *reinterpret_cast<const float4*>(k_sh + 32 * j + 4 * b);
   const float2 a2 = make_float2(a, a);
-  float part[4];
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
@@ -197,10 +201,14 @@ __device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], const float*
       p23 = fma2(s23, make_float2(kk[j].z, kk[j].w), p23);
       S[r][j] = make_float4(s01.x, s01.y, s23.x, s23.y);
     }
-    part[r] = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
+    part[r] = ts_combine(p01, p23);
   }
-  float p[4];
-  group_allreduce4(part, p, b);
+}
+template <int D>
+__device__ __forceinline__ void ts_update_dot(float4 (&S)[4][D / 32], const float4 (&kk)[D / 32],
+                                              const float* __restrict__ q_sh, float beta, float4 v4,
+                                              const float (&p)[4], int b, float (&opart)[4]) {
+  constexpr int J = D / 32;
   const float v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -224,9 +232,20 @@ __device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], const float*
       p01 = fma2(make_float2(S[r][j].x, S[r][j].y), make_float2(qq[j].x, qq[j].y), p01);
       p23 = fma2(make_float2(S[r][j].z, S[r][j].w), make_float2(qq[j].z, qq[j].w), p23);
     }
-    part[r] = __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
+    opart[r] = ts_combine(p01, p23);
   }
-  return group_reduce4(part, b);
+}
+// The whole step; returns o of row out_row().
+template <int D>
+__device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], const float* __restrict__ k_sh,
+                                            const float* __restrict__ q_sh, float a, float beta, float4 v4,
+                                            int b) {
+  float4 kk[D / 32];
+  float part[4], p[4], opart[4];
+  ts_decay_dot<D>(S, k_sh, a, b, kk, part);
+  group_allreduce4(part, p, b);
+  ts_update_dot<D>(S, kk, q_sh, beta, v4, p, b, opart);
+  return group_reduce4(opart, b);
 }
 
 // T = (I + A)^{-1} for a strictly lower C x C matrix A in shared memory (row stride CPA; T

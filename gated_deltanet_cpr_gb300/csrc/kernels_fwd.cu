@@ -1201,13 +1201,25 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   lay.load(S, src);
   __syncthreads();
 
+  // The token steps (token_step, split in its two sweeps): the output reduction of token
+  // tt - 1 runs in the same block as the first sweep of token tt, which does not depend on it.
+  // o overwrites v in place: every lane of the row group read that v before contributing to o.
   const int orow = lay.out_row();
   const bool writer = lay.writes_out();
+  float opart[4] = {0.f, 0.f, 0.f, 0.f};
   for (int tt = first; tt < len; ++tt) {
+    float4 kk[D / 32];
+    float part[4], p[4];
     const float4 v4 = *reinterpret_cast<const float4*>(vs + tt * D + lay.row0);
-    const float o = token_step<D>(S, ks + tt * D, qs + tt * D, as[tt], bs[tt], v4, lay.b);
-    __syncwarp();
-    if (writer) vs[tt * D + orow] = o;
+    ts_decay_dot<D>(S, ks + tt * D, as[tt], lay.b, kk, part);
+    const float o_prev = group_reduce4(opart, lay.b);
+    if (writer && tt > first) vs[(tt - 1) * D + orow] = o_prev;
+    group_allreduce4(part, p, lay.b);
+    ts_update_dot<D>(S, kk, qs + tt * D, bs[tt], v4, p, lay.b, opart);
+  }
+  if (first < len) {
+    const float o_last = group_reduce4(opart, lay.b);
+    if (writer) vs[(len - 1) * D + orow] = o_last;
   }
   __syncthreads();
   // the chunk record again (an L2 read instead of registers held through the token loop)
