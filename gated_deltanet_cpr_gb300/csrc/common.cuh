@@ -154,25 +154,25 @@ __device__ __forceinline__ float group_reduce4(const float (&x)[4], int b) {
   const float z = __fadd_rn(h1 ? y1 : y0, __shfl_xor_sync(0xffffffffu, h1 ? y0 : y1, 2));
   return __fadd_rn(z, __shfl_xor_sync(0xffffffffu, z, 1));
 }
-// group_reduce4, then every lane of the group gets all four totals (two more exchanges)
-__device__ __forceinline__ void group_allreduce4(const float (&x)[4], float (&tot)[4], int b) {
-  const bool h2 = (b & 4) != 0, h1 = (b & 2) != 0;
-  const float mine = group_reduce4(x, b);                        // row 2 h2 + h1
-  const float other = __shfl_xor_sync(0xffffffffu, mine, 2);     // row 2 h2 + !h1
-  const float lo = h1 ? other : mine, hi = h1 ? mine : other;     // rows 2 h2, 2 h2 + 1
-  const float lo_x = __shfl_xor_sync(0xffffffffu, lo, 4), hi_x = __shfl_xor_sync(0xffffffffu, hi, 4);
-  tot[0] = h2 ? lo_x : lo;
-  tot[1] = h2 ? hi_x : hi;
-  tot[2] = h2 ? lo : lo_x;
-  tot[3] = h2 ? hi : hi_x;
+// The same four totals on every lane of the group, by an xor-4, xor-2, xor-1 butterfly over
+// all four values: the same tree as group_reduce4 (each level adds the two halves of the
+// level below, in either order), so the same bits, in three exchange levels instead of five.
+__device__ __forceinline__ void group_allreduce4(const float (&x)[4], float (&tot)[4]) {
+  float y[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) y[r] = __fadd_rn(x[r], __shfl_xor_sync(0xffffffffu, x[r], 4));
+#pragma unroll
+  for (int r = 0; r < 4; ++r) y[r] = __fadd_rn(y[r], __shfl_xor_sync(0xffffffffu, y[r], 2));
+#pragma unroll
+  for (int r = 0; r < 4; ++r) tot[r] = __fadd_rn(y[r], __shfl_xor_sync(0xffffffffu, y[r], 1));
 }
 
 // One gated delta-rule step on the lane's 4 state rows (StateLayout), in the recurrence's
 // own order of operations:
 //     S <- a S;   p = S k;   u = beta (v - p);   S <- S + u k^T;   o = S q
-// Each row's dot: per lane two float2 partials over the lane's column groups in ascending j
-// (.x/.y = columns 4b, 4b+1 and 4b+2, 4b+3 of the group), combined as (x0 + y0) + (x1 + y1)
-// for (p01, p23), then group_reduce4 over the 8 lanes.  k (kept in registers from the dot to
+// Each row's dot: per lane one float2 partial over the lane's columns in the order (j, pair):
+// .x takes columns 32j + 4b, then 32j + 4b + 2, .y columns 32j + 4b + 1, then 32j + 4b + 3,
+// ascending j; then x + y, then group_reduce4 over the 8 lanes.  k (kept in registers from the dot to
 // the update) and q are fp32 copies in shared memory (exact widenings of the inputs); v4 is
 // v of the lane's 4 rows.  The step is split in two sweeps so that a token loop can overlap
 // the output reduction of one token with the first sweep of the next:
@@ -180,9 +180,6 @@ __device__ __forceinline__ void group_allreduce4(const float (&x)[4], float (&to
 //   ts_update_dot  (after group_allreduce4 of those partials) the update and the lane's
 //                  partials of S q, to be reduced by group_reduce4
 // token_step is the whole step.  All 32 lanes of the warp call these together.
-__device__ __forceinline__ float ts_combine(float2 p01, float2 p23) {
-  return __fadd_rn(__fadd_rn(p01.x, p01.y), __fadd_rn(p23.x, p23.y));
-}
 template <int D>
 __device__ __forceinline__ void ts_decay_dot(float4 (&S)[4][D / 32], const float* __restrict__ k_sh, float a, int b,
                                              float4 (&kk)[D / 32], float (&part)[4]) {
@@ -192,16 +189,16 @@ __device__ __forceinline__ void ts_decay_dot(float4 (&S)[4][D / 32], const float
   const float2 a2 = make_float2(a, a);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
+    float2 pr = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const float2 s01 = mul2(a2, make_float2(S[r][j].x, S[r][j].y));
       const float2 s23 = mul2(a2, make_float2(S[r][j].z, S[r][j].w));
-      p01 = fma2(s01, make_float2(kk[j].x, kk[j].y), p01);
-      p23 = fma2(s23, make_float2(kk[j].z, kk[j].w), p23);
+      pr = fma2(s01, make_float2(kk[j].x, kk[j].y), pr);
+      pr = fma2(s23, make_float2(kk[j].z, kk[j].w), pr);
       S[r][j] = make_float4(s01.x, s01.y, s23.x, s23.y);
     }
-    part[r] = ts_combine(p01, p23);
+    part[r] = __fadd_rn(pr.x, pr.y);
   }
 }
 template <int D>
@@ -226,13 +223,13 @@ __device__ __forceinline__ void ts_update_dot(float4 (&S)[4][D / 32], const floa
   for (int j = 0; j < J; ++j) qq[j] = *reinterpret_cast<const float4*>(q_sh + 32 * j + 4 * b);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
-    float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
+    float2 pr = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      p01 = fma2(make_float2(S[r][j].x, S[r][j].y), make_float2(qq[j].x, qq[j].y), p01);
-      p23 = fma2(make_float2(S[r][j].z, S[r][j].w), make_float2(qq[j].z, qq[j].w), p23);
+      pr = fma2(make_float2(S[r][j].x, S[r][j].y), make_float2(qq[j].x, qq[j].y), pr);
+      pr = fma2(make_float2(S[r][j].z, S[r][j].w), make_float2(qq[j].z, qq[j].w), pr);
     }
-    opart[r] = ts_combine(p01, p23);
+    opart[r] = __fadd_rn(pr.x, pr.y);
   }
 }
 // The whole step; returns o of row out_row().
@@ -243,7 +240,7 @@ __device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], const float*
   float4 kk[D / 32];
   float part[4], p[4], opart[4];
   ts_decay_dot<D>(S, k_sh, a, b, kk, part);
-  group_allreduce4(part, p, b);
+  group_allreduce4(part, p);
   ts_update_dot<D>(S, kk, q_sh, beta, v4, p, b, opart);
   return group_reduce4(opart, b);
 }

@@ -1458,7 +1458,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(a.in.v) + tok0 * vstride + (int64_t)h * D;
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.in.q) + tok0 * kstride + (int64_t)hq * D;
   unsigned char* img = reinterpret_cast<unsigned char*>(a.b.img + ch * (int64_t)prep_w_floats(C, D));
-  float* Qt = a.b.dOS0 + ch * CD;  // scratch
   const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
 
   // ---- 1. images of K rows and V rows (V staged in the A region), g, beta (zero beyond
@@ -1604,6 +1603,9 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     }
   }
   if (ok) wait_mma();
+  // W, P and Qt also leave their readouts as split images in shared memory (the transposed
+  // operands are built there), so that nothing this CTA wrote is read back from global memory
+  unsigned char* Wr = smq + OFF_TK;  // W rows hi | lo (32 KB over the dead TK and TV)
   if (ok) {
     if ((warp & 3) < 2) {  // W rows (not decayed)
       const int i = lrow;
@@ -1613,6 +1615,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
 #pragma unroll
         for (int e = 0; e < 16; e += 4)
           *reinterpret_cast<float4*>(a.b.W + ch * CD + (int64_t)i * D + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        split8(Wr, Wr + TILE, kmajor_off(i, c0, D), v);
+        split8(Wr, Wr + TILE, kmajor_off(i, c0 + 8, D), v + 8);
       }
     }
     {  // Ut[i][e] = U^T[e][i]
@@ -1625,7 +1629,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       }
     }
   }
-  // ---- 4. P = Gam (.) (Q K^T)
+  // ---- 4. P = Gam (.) (Q K^T); meanwhile W^T hi | lo from the W rows (over the dead K^T, V^T)
   for (int q = t; q < (int)(TILE / 16); q += 256)  // K rows image for the reverse chain
     reinterpret_cast<uint4*>(img)[q] = reinterpret_cast<const uint4*>(Ki)[q];
   sync_for_mma();
@@ -1637,8 +1641,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
                idesc_bf16(128, C), kk > 0 ? 1u : 0u);
     mma_commit(bar);
   }
+  tc::transpose_image(KT, Wr, D, C);
+  tc::transpose_image(VT, Wr + TILE, D, C);
   if (ok) wait_mma();
-  if (ok && (warp & 3) < 2) {
+  if (ok && (warp & 3) < 2) {  // P rows -> global and as the split image (over the dead W rows)
     const int i = lrow;
     for (int s0 = chalf * 32; s0 < chalf * 32 + 32; s0 += 16) {
       float v[16];
@@ -1646,32 +1652,32 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int s = s0 + e;
-        a.b.P[ch * C * C + i * C + s] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v[e]) : 0.f;
+        v[e] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v[e]) : 0.f;
       }
+#pragma unroll
+      for (int e = 0; e < 16; e += 4)
+        *reinterpret_cast<float4*>(a.b.P + ch * C * C + i * C + s0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      split8(TKh, TKl, kmajor_off(i, s0, C), v);
+      split8(TKh, TKl, kmajor_off(i, s0 + 8, C), v + 8);
     }
   }
-  fence_before_sync();
-  __syncthreads();  // W and P rows are in global memory for this CTA
   // ---- 5. Qt = diag(e^G) Q - P W: A = P (rows i), B = W^T (rows c)
+  float dov[4][8];  // dO^T pieces for step 6, loaded while the product runs
   if (ok) {
-    {  // W^T hi | lo over the dead K^T, V^T; P rows over the dead TK
-      SplitTile<true, D, C> wt;
-      SplitTile<false, C, C> pr;
-      wt.load(a.b.W + ch * CD, D, C);
-      pr.load(a.b.P + ch * C * C, C, C);
-      wt.store(KT, VT);
-      pr.store(TKh, TKl);
-    }
     sync_for_mma();
     if (t == 0) {
       fence_after_sync();
       mma_terms(tb + COL_QT, smem_u32(TKh), smem_u32(TKl), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
       mma_commit(bar);
     }
+    load_dO_T(dov, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
     for (int q = t; q < (int)(2 * TILE / 16); q += 256)  // W^T images for the reverse chain
       reinterpret_cast<uint4*>(img + TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
     wait_mma();
   }
+  // Qt rows hi | lo over the dead TV and T regions
+  unsigned char* Qrh = smq + OFF_TV;
+  unsigned char* Qrl = smq + OFF_T;
   if (ok && (warp & 3) < 2) {
     const int i = lrow;
     const float egi = expf(Gs[i]);
@@ -1681,33 +1687,27 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       unpack8(*reinterpret_cast<const uint4*>(Qi + kmajor_off(i, c0, D)), qf);
       unpack8(*reinterpret_cast<const uint4*>(Qi + kmajor_off(i, c0 + 8, D)), qf + 8);
 #pragma unroll
-      for (int e = 0; e < 16; e += 4)
-        *reinterpret_cast<float4*>(Qt + (int64_t)i * D + c0 + e) =
-            make_float4(__fsub_rn(__fmul_rn(egi, qf[e]), v[e]), __fsub_rn(__fmul_rn(egi, qf[e + 1]), v[e + 1]),
-                        __fsub_rn(__fmul_rn(egi, qf[e + 2]), v[e + 2]), __fsub_rn(__fmul_rn(egi, qf[e + 3]), v[e + 3]));
+      for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(__fmul_rn(egi, qf[e]), v[e]);
+      split8(Qrh, Qrl, kmajor_off(i, c0, D), v);
+      split8(Qrh, Qrl, kmajor_off(i, c0 + 8, D), v + 8);
     }
   }
   fence_before_sync();
   __syncthreads();
-  // ---- 6. L = dO^T Qt: A = dO^T (rows p, K = i), B = Qt^T (rows q, K = i)
+  // ---- 6. L = dO^T Qt: A = dO^T (rows p, K = i) over the dead K rows and P, B = Qt^T (rows q,
+  // K = i) over the dead W^T
   if (ok) {
-    SplitTile<true, D, C> qtt;
-    qtt.load(Qt, D, C);
-    {
-      float v[4][8];
-      load_dO_T(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
-      qtt.store(smq + OFF_A, smq + OFF_A + TILE);
+    tc::transpose_image(KT, Qrh, D, C);
+    tc::transpose_image(VT, Qrl, D, C);
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
-        split8(Ki, Ki + TILE, kmajor_off(r, k0, C), v[it]);  // over the dead K and K^T regions
-      }
+    for (int it = 0; it < 4; ++it) {
+      const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
+      split8(Ki, TKh, kmajor_off(r, k0, C), dov[it]);
     }
     sync_for_mma();
     if (t == 0) {
       fence_after_sync();
-      mma_terms(tb + COL_L, smem_u32(Ki), smem_u32(Ki) + TILE, smem_u32(smq + OFF_A), smem_u32(smq + OFF_A) + TILE, C,
-                idesc_bf16(128, D), 3);
+      mma_terms(tb + COL_L, smem_u32(Ki), smem_u32(TKh), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
       mma_commit(bar);
     }
     wait_mma();

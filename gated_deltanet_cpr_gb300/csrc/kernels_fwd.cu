@@ -1214,7 +1214,7 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
     ts_decay_dot<D>(S, ks + tt * D, as[tt], lay.b, kk, part);
     const float o_prev = group_reduce4(opart, lay.b);
     if (writer && tt > first) vs[(tt - 1) * D + orow] = o_prev;
-    group_allreduce4(part, p, lay.b);
+    group_allreduce4(part, p);
     ts_update_dot<D>(S, kk, qs + tt * D, bs[tt], v4, p, lay.b, opart);
   }
   if (first < len) {

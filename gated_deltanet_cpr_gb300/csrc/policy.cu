@@ -129,8 +129,8 @@ std::string policy_text(const gdn_cpr_shape* s) {
            "exp=expf\n"
            "token_step=4 state rows x d/8 columns per lane (columns 32j+4b..+3), 8 lanes per row group; "
            "S*=a; p=S.k; u=beta*(v-p); S+=u k^T; o=S.q; "
-           "each dot: per lane and row two float2 partials over ascending j, (x0+y0)+(x1+y1), "
-           "then across the 8 lanes a fixed xor-4, xor-2, xor-1 tree\n"
+           "each dot: per lane and row one float2 partial (x: columns 4b, 4b+2; y: 4b+1, 4b+3; ascending j), x+y, "
+           "then across the 8 lanes the tree ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7))\n"
            "cumsum_g=sequential fp32, ascending token\n"
            "triangular_solve=(I+A)^-1 blocked by 16: diagonal blocks by forward substitution, "
            "off-diagonal blocks by increasing distance, every sum ascending with one accumulator\n"
