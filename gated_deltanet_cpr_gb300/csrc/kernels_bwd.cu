@@ -1534,6 +1534,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   tc::transpose_image(VT, Vi, D, C);
   __syncthreads();
   if (t < C) a.b.G[ch * C + t] = Gs[t];
+  // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs (V^T is built), by all
+  // threads; the readout multiplies in place
+  for (int e = t; e < C * C; e += 256) {
+    const int i = e / C, s = e % C;
+    if (i > s) A[i * QCP + s] = __fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s])));
+  }
   wait_mma();
   if (ok && (warp & 3) < 2) {
     const int i = lrow;
@@ -1543,7 +1549,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int s = s0 + e;
-        A[i * QCP + s] = (i > s) ? __fmul_rn(__fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s]))), v[e]) : 0.f;
+        A[i * QCP + s] = (i > s) ? __fmul_rn(A[i * QCP + s], v[e]) : 0.f;
       }
     }
   }

@@ -1009,6 +1009,12 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
       bk[t] = __fmul_rn(bs[t], expf(Gs[t]));
       dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
     }
+    // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs (the V rows staged
+    // there are transposed), by all threads; the readout multiplies in place
+    for (int e = t; e < C * C; e += 256) {
+      const int i = e / C, s = e % C;
+      if (i > s) A[i * CP + s] = __fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s])));
+    }
     {
       const bool done = tc::mbar_wait(bar, phase);
       ok = __syncthreads_and(done) != 0;
@@ -1025,7 +1031,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int s = s0 + e;
-          A[i * CP + s] = (i > s) ? __fmul_rn(__fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s]))), v[e]) : 0.f;
+          A[i * CP + s] = (i > s) ? __fmul_rn(A[i * CP + s], v[e]) : 0.f;
         }
       }
     }

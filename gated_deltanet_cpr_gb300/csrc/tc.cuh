@@ -172,18 +172,27 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
 }
 
 // dst = transpose of a shared-memory image: src is Ks rows x R columns (K-major, K = R),
-// dst is R rows x Ks columns (K = Ks); 256 threads.
+// dst is R rows x Ks columns (K = Ks); 256 threads, R and Ks multiples of 16 (whole groups of
+// four core matrices).  In the no-swizzle K-major layout an 8 x 8 core matrix is 8 rows of 16
+// contiguous bytes, and core matrix (xb, yb) of dst is the transpose of core matrix (yb, xb)
+// of src: each warp moves four at a time with ldmatrix .trans and stmatrix (eight 16-byte
+// rows per matrix on each side, one wavefront each).
 __device__ __forceinline__ void transpose_image(unsigned char* dst, const unsigned char* src, int R, int Ks) {
-  for (int q = threadIdx.x; q < R * (Ks / 8); q += 256) {
-    const int e = q % R, r0 = (q / R) * 8;
-    uint32_t w[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint32_t a0 = *reinterpret_cast<const uint16_t*>(src + kmajor_off(r0 + 2 * x, e, R));
-      const uint32_t a1 = *reinterpret_cast<const uint16_t*>(src + kmajor_off(r0 + 2 * x + 1, e, R));
-      w[x] = a0 | (a1 << 16);
-    }
-    *reinterpret_cast<uint4*>(dst + kmajor_off(e, r0, Ks)) = make_uint4(w[0], w[1], w[2], w[3]);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int xbs = R / 8, ncore = (Ks / 8) * xbs;
+  const uint32_t sbo_s = (uint32_t)xbs * 128, sbo_d = (uint32_t)(Ks / 8) * 128;
+  const uint32_t s0 = smem_u32(src) + (lane & 7) * 16, d0 = smem_u32(dst) + (lane & 7) * 16;
+  for (int q0 = warp * 4; q0 < ncore; q0 += 32) {
+    const int q = q0 + (lane >> 3);  // this lane's row address is in matrix lane / 8
+    const int yb = q / xbs, xb = q % xbs;
+    uint32_t r0, r1, r2, r3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(s0 + yb * sbo_s + xb * 128)
+                 : "memory");
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(d0 + xb * sbo_d + yb * 128),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
   }
 }
 

@@ -83,3 +83,27 @@ extern "C" int tc_selftest(const void* A, const void* B, const float* Cinit, flo
                                        status);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
+
+// transpose_image: a Ks x R bf16 matrix X (row-major in global memory) into its K-major
+// shared-memory image, transposed there by all 256 threads, read back as the R x Ks image of X^T
+__global__ void __launch_bounds__(256) k_transpose_selftest(const uint16_t* X, uint16_t* Y, int R, int Ks) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  unsigned char* src = sm;
+  unsigned char* dst = sm + R * Ks * 2;
+  for (int e = threadIdx.x; e < Ks * R; e += 256)
+    *reinterpret_cast<uint16_t*>(src + kmajor_off(e / R, e % R, R)) = X[e];
+  __syncthreads();
+  transpose_image(dst, src, R, Ks);
+  __syncthreads();
+  for (int e = threadIdx.x; e < R * Ks; e += 256) Y[e] = *reinterpret_cast<const uint16_t*>(dst + kmajor_off(e / Ks, e % Ks, Ks));
+}
+
+extern "C" int transpose_selftest(const void* X, void* Y, int R, int Ks, cudaStream_t st) {
+  if (R % 16 || Ks % 16 || R < 16 || Ks < 16 || R * Ks > 128 * 128) return 1;
+  const size_t smem = (size_t)2 * R * Ks * 2;
+  if (cudaFuncSetAttribute(k_transpose_selftest, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return 2;
+  k_transpose_selftest<<<1, 256, smem, st>>>(static_cast<const uint16_t*>(X), static_cast<uint16_t*>(Y), R, Ks);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}

@@ -26,6 +26,9 @@ def lib():
     L.tc_selftest.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                       ctypes.c_void_p]
     L.tc_selftest.restype = ctypes.c_int
+    L.transpose_selftest.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_void_p]
+    L.transpose_selftest.restype = ctypes.c_int
     return L
 
 
@@ -49,3 +52,17 @@ def test_tcgen05_mma_matches_reference(lib, N, K, init):
     assert int(status.item()) == 0, "bounded wait gave up"
     err = (D.double().cpu() - ref).abs().max().item() / ref.abs().max().item()
     assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("R,Ks", [(128, 64), (64, 64), (64, 128), (16, 32), (128, 128)])
+def test_transpose_image_is_exact(lib, R, Ks):
+    """The shared-memory image transpose (ldmatrix .trans + stmatrix over core matrices) moves
+    every bf16 bit pattern to its transposed place."""
+    g = torch.Generator().manual_seed(R * 7 + Ks)
+    X = torch.randint(0, 1 << 16, (Ks, R), generator=g, dtype=torch.int32).to(torch.int16)
+    dX = X.cuda()
+    Y = torch.zeros((R, Ks), dtype=torch.int16, device="cuda")
+    rc = lib.transpose_selftest(dX.data_ptr(), Y.data_ptr(), R, Ks, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.equal(Y.cpu(), X.T.contiguous())
