@@ -301,6 +301,86 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, int C
   }
 }
 
+// The same inverse for C = 64 on 256 threads, with the same operations in the same order:
+// thread t takes, in round `off`, the elements e = t + 256 q (q = 0 .. 3 - off) of the
+// generic loop (all at the same (ii, rr), so their sums have the same length) and runs them
+// side by side; every sum is unrolled over its longest length with a per-lane select in
+// place of the loop bounds (a skipped term leaves the accumulator unchanged, so each
+// accumulator sees exactly the generic sequence of fma).  Operands outside a sum's range are
+// read (inside the matrices) and discarded.  A compiler-only fence every 8 terms bounds the
+// loads held in registers.
+__device__ __forceinline__ void unit_lower_inverse64(const float* A, int CPA, float* Tm, int CPT, float* Xs) {
+  constexpr int TB = 16, C = 64, NB = C / TB;
+  const int t = threadIdx.x;
+  if (t < C) {  // diagonal blocks as in blocked_unit_lower_inverse
+    const int r = t, rb = (r / TB) * TB, rr = r - rb;
+    float col[TB];
+#pragma unroll
+    for (int k = 0; k < TB; ++k) col[k] = (k == rr) ? 1.f : 0.f;
+#pragma unroll
+    for (int ii = 1; ii < TB; ++ii) {
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < ii; ++m)
+        if (m >= rr) acc = __fmaf_rn(A[(rb + ii) * CPA + rb + m], col[m], acc);
+      if (ii > rr) col[ii] = -acc;
+    }
+#pragma unroll
+    for (int k = 0; k < TB; ++k)
+      if (k >= rr) Tm[(rb + k) * CPT + r] = col[k];
+  }
+  __syncthreads();
+  const int ii = t / TB, rr = t % TB;
+#pragma unroll
+  for (int off = 1; off < NB; ++off) {
+    constexpr int QMAX = NB - 1;
+    const int nq = NB - off;
+    float acc[QMAX];
+#pragma unroll
+    for (int q = 0; q < QMAX; ++q) acc[q] = 0.f;
+    // X[e] = sum_{m = r}^{16 I - 1} A[i][m] T[m][r],  m = 16 (I - off) + k,  k = rr .. 16 off - 1
+#pragma unroll
+    for (int k = 0; k < off * TB; ++k) {
+#pragma unroll
+      for (int q = 0; q < QMAX; ++q) {
+        if (q < nq) {
+          const int I = off + q, i = I * TB + ii, r = (I - off) * TB + rr, m = (I - off) * TB + k;
+          const float v = __fmaf_rn(A[i * CPA + m], Tm[m * CPT + r], acc[q]);
+          acc[q] = (k >= rr) ? v : acc[q];
+        }
+      }
+      if ((k & 7) == 7) asm volatile("" ::: "memory");
+    }
+#pragma unroll
+    for (int q = 0; q < QMAX; ++q)
+      if (q < nq) Xs[q * 256 + t] = acc[q];
+    __syncthreads();
+    // T[i][r] = -sum_{m = 16 I}^{i} T[i][m] X[m - 16 I][rr],  m = 16 I + k,  k = 0 .. ii
+#pragma unroll
+    for (int q = 0; q < QMAX; ++q) acc[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < TB; ++k) {
+#pragma unroll
+      for (int q = 0; q < QMAX; ++q) {
+        if (q < nq) {
+          const int I = off + q, i = I * TB + ii;
+          const float v = __fmaf_rn(Tm[i * CPT + I * TB + k], Xs[q * 256 + k * TB + rr], acc[q]);
+          acc[q] = (k <= ii) ? v : acc[q];
+        }
+      }
+      if ((k & 7) == 7) asm volatile("" ::: "memory");
+    }
+#pragma unroll
+    for (int q = 0; q < QMAX; ++q) {
+      if (q < nq) {
+        const int I = off + q, i = I * TB + ii, r = (I - off) * TB + rr;
+        Tm[i * CPT + r] = -acc[q];
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // The same with one row stride for A and T.
 template <int NT>
 __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, float* Tm, float* Xs, int C, int CP) {

@@ -1556,7 +1556,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   fence_before_sync();
   __syncthreads();
   // ---- 3. T, TK, TV; W = TK K and U^T = V^T TV^T
-  blocked_unit_lower_inverse<256>(A, QCP, Tm, TCP, Xs, C);
+  unit_lower_inverse64(A, QCP, Tm, TCP, Xs);
   for (int o = t; o < C * C; o += 256) {
     const int i = o / C, r = o % C;
     a.b.T[ch * C * C + o] = (r <= i) ? Tm[i * TCP + r] : 0.f;

@@ -1038,7 +1038,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     tc::fence_before_sync();
     __syncthreads();
     // 3. T = (I + A)^{-1}
-    blocked_unit_lower_inverse<256>(A, Tm, Xs, C, CP);
+    unit_lower_inverse64(A, CP, Tm, CP, Xs);
     // 4. TK = T diag(beta e^G), TV = T diag(beta), split into bf16 images (lower triangle)
     for (int q = t; q < C * (C / 8); q += 256) {
       int i, r0;

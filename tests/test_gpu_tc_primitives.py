@@ -32,6 +32,19 @@ def lib():
     return L
 
 
+@pytest.fixture(scope="module")
+def inv_lib():
+    src = os.path.join(HERE, "cuda", "inverse_selftest.cu")
+    out_dir = os.path.join(HERE, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, "libinverse_selftest.so")
+    subprocess.check_call([gbuild.nvcc(), *gbuild.ARCH, *gbuild.NVCC_FLAGS, "-shared", "-o", so, src])
+    L = ctypes.CDLL(so)
+    L.inverse_selftest.argtypes = [ctypes.c_void_p] * 4
+    L.inverse_selftest.restype = ctypes.c_int
+    return L
+
+
 @pytest.mark.parametrize("N,K,init", [(64, 128, False), (128, 64, False), (128, 128, True),
                                       (16, 16, False), (256, 32, True)])
 def test_tcgen05_mma_matches_reference(lib, N, K, init):
@@ -66,3 +79,21 @@ def test_transpose_image_is_exact(lib, R, Ks):
     assert rc == 0
     torch.cuda.synchronize()
     assert torch.equal(Y.cpu(), X.T.contiguous())
+
+
+@pytest.mark.parametrize("seed,scale", [(0, 0.1), (1, 0.5), (4, 0.2), (5, 0.3), (3, 0.02)])
+def test_unrolled_inverse_matches_generic_bits(inv_lib, seed, scale):
+    """The unrolled C = 64 inverse of the tensor-core pre-passes performs the generic blocked
+    inverse's operations in the same order: same bits, and T (I + A) = I to fp32 accuracy."""
+    g = torch.Generator().manual_seed(seed)
+    A = (torch.randn((64, 64), generator=g) * scale).tril(-1).contiguous()
+    dA = A.cuda()
+    Tg = torch.full((64, 64), float("nan"), device="cuda")
+    Tf = torch.full((64, 64), float("nan"), device="cuda")
+    assert inv_lib.inverse_selftest(dA.data_ptr(), Tg.data_ptr(), Tf.data_ptr(),
+                                    torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(Tf, Tg)
+    T = Tg.double().cpu()
+    resid = (T @ (torch.eye(64, dtype=torch.float64) + A.double()) - torch.eye(64, dtype=torch.float64))
+    assert resid.abs().max().item() <= 1e-4 * max(1.0, T.abs().max().item())
