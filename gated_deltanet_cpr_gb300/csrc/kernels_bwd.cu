@@ -1324,7 +1324,9 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     __syncthreads();
   }
   if (t == 0) a.b.sdot[ch] = red[0];
-  if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec)
+  if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec): fp32 dU rows, and the dU^T operand image
+    // (rows d, K = s; hi | lo) for the gradients kernel in this chunk-head's adjoint L slot
+    unsigned char* uimg = reinterpret_cast<unsigned char*>(a.b.L + ch * SZ);
 #pragma unroll
     for (int s1 = 0; s1 < 2; ++s1) {
       float e1[16], p1[16];
@@ -1333,8 +1335,11 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int s = cbase + 16 * s1 + e;
-        a.b.dU[ch * CD + (int64_t)s * D + lane_row] = __fmaf_rn(dec[s], e1[e], p1[e]);
+        p1[e] = __fmaf_rn(dec[s], e1[e], p1[e]);
+        a.b.dU[ch * CD + (int64_t)s * D + lane_row] = p1[e];
       }
+      split8(uimg, uimg + C * D * 2, kmajor_off(lane_row, cbase + 16 * s1, C), p1);
+      split8(uimg, uimg + C * D * 2, kmajor_off(lane_row, cbase + 16 * s1 + 8, C), p1 + 8);
     }
   }
   fence_before_sync();
@@ -1383,7 +1388,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       run();
     }
   }
-  if (ok) {
+  if (ok) {  // dO S0 rows (fp32) and the dW^T operand image (rows d, K = s; hi | lo)
+    unsigned char* wimg = reinterpret_cast<unsigned char*>(a.b.dW + ch * CD);
 #pragma unroll
     for (int s1 = 0; s1 < 2; ++s1) {
       float v[16], w[16];
@@ -1391,10 +1397,11 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       tmem_ld16(tl + COL_1 + cbase + 16 * s1, w);
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const int64_t o = ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row;
-        a.b.dOS0[o] = v[e];
-        a.b.dW[o] = -w[e];
+        a.b.dOS0[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = v[e];
+        w[e] = -w[e];
       }
+      split8(wimg, wimg + C * D * 2, kmajor_off(lane_row, cbase + 16 * s1, C), w);
+      split8(wimg, wimg + C * D * 2, kmajor_off(lane_row, cbase + 16 * s1 + 8, C), w + 8);
     }
   } else if (t == 0) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
@@ -1412,9 +1419,9 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 //   P    = Gam (.) (Q K^T), lower with diagonal                       (exact bf16 inputs)
 //   Qt   = diag(e^G) Q - P W                                          (P, W split hi/lo)
 //   L    = dO^T Qt                                                    (dO, Qt split)
-// Outputs W, Ut, T, G, P, L and the reverse chain's images.  Transposed operands are built
-// from rows just written to global memory (L2-resident) instead of extra shared memory;
-// Qt uses this chunk-head's dO S0 slot as scratch (rewritten by the next kernel).
+// Outputs W, Ut, G, P, L, the reverse chain's images and the T^T operand image of the
+// gradients kernel (in T's slot).  W, P and Qt also leave their readouts as split images in
+// shared memory, where the transposed operands are built.
 namespace tcq {
 constexpr int D = 128, C = 64, QCP = C + 1, TCP = C;  // row strides of A (padded) and T
 constexpr uint32_t TILE = C * D * 2;  // 16 KB
@@ -1557,9 +1564,16 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   __syncthreads();
   // ---- 3. T, TK, TV; W = TK K and U^T = V^T TV^T
   unit_lower_inverse64(A, QCP, Tm, TCP, Xs);
-  for (int o = t; o < C * C; o += 256) {
-    const int i = o / C, r = o % C;
-    a.b.T[ch * C * C + o] = (r <= i) ? Tm[i * TCP + r] : 0.f;
+  {  // T^T as the gradients kernel's operand image (rows r, K = i; hi | lo), T lower
+    unsigned char* timg = reinterpret_cast<unsigned char*>(a.b.T + ch * C * C);
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const int q = t + it * 256, r = q % C, i0 = (q / C) * 8;
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = (r <= i0 + e) ? Tm[(i0 + e) * TCP + r] : 0.f;
+      split8(timg, timg + C * C * 2, kmajor_off(r, i0, C), v);
+    }
   }
   for (int q = t; q < C * (C / 8); q += 256) {
     int i, r0;
@@ -1750,9 +1764,11 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
 //       dAm = dA beta_i Gam,  dK2 = dAm K + dAm^T K                   -> dk += dK2 + diag(dec) U dS_end
 //       dG, reverse cumulative sum -> dg, dbeta
 // The row and column sums of the dG terms come straight from the TMEM readouts (per-thread
-// row sums, warp-shuffle column sums in a fixed tree).  X and Y travel through the
-// workspace (the adjoint L, dead after the reverse chain) as ready-made images that G2
-// brings in by bulk copy; the per-token partial sums go through the image workspace.
+// row sums, warp-shuffle column sums in a fixed tree).  G1's operands T^T, dU^T and dW^T
+// arrive as ready-made images by bulk copy (the prep and big-products kernels write them),
+// as do the K rows; X and Y travel through the workspace (the adjoint L, dead after the
+// reverse chain) as images that G2 brings in the same way; the per-token partial sums go
+// through the image workspace.
 // 64-row operands use 128-row MMAs whose extra rows read neighbouring arena bytes and are
 // never read back.
 namespace tcd {
@@ -1784,8 +1800,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   float* dGa = colp + 2 * C;   // [2][C]
   float* dba = dGa + 2 * C;    // [2][C]
   float* kY = dba + 2 * C;     // [2][C]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(kY + 2 * C);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(kY + 2 * C);  // [0] MMA, [1] bulk copies
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -1853,7 +1869,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   }
   build_split<false, C, D>(ar + 64 * KB, ar + 80 * KB, a.b.U + ch * CD, D, C);
   if (t == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, TMEM1);
@@ -1865,9 +1882,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const uint32_t tl = tmem_lane_addr(tb, warp, 0);
   const uint32_t sa = smem_u32(ar);
   uint32_t phase = 0;
-  bool ok = true, pending = false;
+  uint32_t cphase = 0;
+  bool ok = true, pending = false, cpending = false;
   auto wait_mma = [&]() {
-    const bool done = mbar_wait(bar, phase);
+    const bool done = mbar_wait(&bar[0], phase);
     if (done) {
       phase ^= 1u;
       pending = false;
@@ -1875,22 +1893,32 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     ok = __syncthreads_and(done) != 0;
     fence_after_sync();
   };
-  auto issue = [&](auto&& mmas) {
+  // all threads: generic-proxy writes -> tensor core; with copies, thread 0 first waits for
+  // the bulk copies in flight and every thread learns whether they arrived
+  auto issue = [&](bool copies, auto&& mmas) {
     fence_proxy_async();
     fence_before_sync();
-    __syncthreads();
-    if (t == 0) {
+    bool got = true;
+    if (t == 0 && copies) {
+      got = mbar_wait(&bar[1], cphase);
+      if (got) {
+        cphase ^= 1u;
+        cpending = false;
+      }
+    }
+    ok = __syncthreads_and(got) != 0;
+    if (ok && t == 0) {
       fence_after_sync();
       mmas();
-      mma_commit(bar);
+      mma_commit(&bar[0]);
+      pending = true;
     }
-    pending = true;
   };
   // ---- round 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64
   if (t == 0) {
     mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C), 3);
     mma_terms(tb + 64, sa, sa, sa + 16 * KB, sa + 16 * KB, D, idesc_bf16(128, C), 1);
-    mma_commit(bar);
+    mma_commit(&bar[0]);
   }
   pending = true;
   if (t < C) eG[t] = expf(Gs[t]);
@@ -1931,13 +1959,22 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     tc::transpose_image(ar + 56 * KB, ar + 40 * KB, C, C);  // Pm^T lo
     tc::transpose_image(ar + 64 * KB, ar + 16 * KB, D, C);  // K^T
     tc::transpose_image(ar + 80 * KB, ar, D, C);            // Q^T
-    issue([&] {
+    issue(false, [&] {
       mma_terms(tb + 0, sa + 32 * KB, sa + 40 * KB, sa + 64 * KB, sa + 64 * KB, C, idesc_bf16(128, D), 2);
       mma_terms(tb + 128, sa + 48 * KB, sa + 56 * KB, sa + 80 * KB, sa + 80 * KB, C, idesc_bf16(128, D), 2);
     });
-    wait_mma();
+    if (ok) wait_mma();
   }
-  // dQ readout (row warps) || round 3 operands T^T, dU^T, dW^T (other warps)
+  // round 3 and 4 operands T^T, dU^T, dW^T: ready-made images (the prep and big-products
+  // kernels wrote them), one bulk copy each into the dead round-1/2 operands
+  if (ok && t == 0) {
+    mbar_expect_tx(&bar[1], 2 * C * C * 2 + 4 * IMG);
+    bulk_g2s(ar, a.b.T + ch * C * C, 2 * C * C * 2, &bar[1]);
+    bulk_g2s(ar + 16 * KB, a.b.L + ch * (int64_t)D * D, 2 * IMG, &bar[1]);
+    bulk_g2s(ar + 48 * KB, a.b.dW + ch * CD, 2 * IMG, &bar[1]);
+    cpending = true;
+  }
+  // dQ readout (row warps) || V rows image for the dv readout over the dead Q^T (other warps)
   if (ok) {
     if (rowlane) {
       const int i = row;
@@ -1976,25 +2013,31 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       }
       dGa[half * C + i] = pga;
     } else {
-      {
-        SplitTile<true, C, C, 128> tt;
-        tt.load(a.b.T + ch * C * C, C, C, helper);
-        tt.store(ar, ar + 8 * KB, helper);
+      uint4 vr[8];
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        int r, k0;
+        kmajor_piece(helper + it * 128, D, r, k0);
+        vr[it] = r < n ? *reinterpret_cast<const uint4*>(vb + r * vstride + k0) : zero4;
       }
-      {
-        SplitTile<true, D, C, 128> du;
-        du.load(a.b.dU + ch * CD, D, C, helper);
-        du.store(ar + 16 * KB, ar + 32 * KB, helper);
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        int r, k0;
+        kmajor_piece(helper + it * 128, D, r, k0);
+        *reinterpret_cast<uint4*>(ar + 80 * KB + kmajor_off(r, k0, D)) = vr[it];
       }
-      SplitTile<true, D, C, 128> dw;
-      dw.load(a.b.dW + ch * CD, D, C, helper);
-      dw.store(ar + 48 * KB, ar + 64 * KB, helper);
     }
   }
   // ---- round 3: X = T^T dU -> TMEM 0
   if (ok) {
-    issue([&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 16 * KB, sa + 32 * KB, C, idesc_bf16(128, D), 3); });
-    wait_mma();
+    issue(true, [&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 16 * KB, sa + 32 * KB, C, idesc_bf16(128, D), 3); });
+    if (ok) wait_mma();
+  }
+  // K rows image (the prep kernel's) for the dk readout over the dead dU^T
+  if (ok && t == 0) {
+    mbar_expect_tx(&bar[1], IMG);
+    bulk_g2s(ar + 16 * KB, a.b.img + ch * (int64_t)prep_w_floats(C, D), IMG, &bar[1]);
+    cpending = true;
   }
   if (ok && rowlane) {  // dv, dbeta_a; X image -> workspace
     const int i = row;
@@ -2004,7 +2047,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     for (int cb = half * 64; cb < half * 64 + 64; cb += 32) {
       uint4 vv[4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) vv[x] = live ? *reinterpret_cast<const uint4*>(vb + i * vstride + cb + 8 * x) : zero4;
+      for (int x = 0; x < 4; ++x) vv[x] = *reinterpret_cast<const uint4*>(ar + 80 * KB + kmajor_off(i, cb + 8 * x, D));
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
         const int c0 = cb + 16 * sub;
@@ -2028,10 +2071,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     }
     dba[half * C + i] = pba;
   }
-  // ---- round 4: Y = T^T dW -> TMEM 0 (operands already in place)
+  // ---- round 4: Y = T^T dW -> TMEM 0 (operands already in place; the K rows copy lands first)
   if (ok) {
-    issue([&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 48 * KB, sa + 64 * KB, C, idesc_bf16(128, D), 3); });
-    wait_mma();
+    issue(true, [&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 48 * KB, sa + 64 * KB, C, idesc_bf16(128, D), 3); });
+    if (ok) wait_mma();
   }
   if (ok && rowlane) {  // kY; dk <- dK1 + beta e^G Y; Y image -> workspace
     const int s2 = row;
@@ -2041,7 +2084,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     for (int cb = half * 64; cb < half * 64 + 64; cb += 32) {
       uint4 kv[4];
 #pragma unroll
-      for (int x = 0; x < 4; ++x) kv[x] = live ? *reinterpret_cast<const uint4*>(kb + s2 * kstride + cb + 8 * x) : zero4;
+      for (int x = 0; x < 4; ++x) kv[x] = *reinterpret_cast<const uint4*>(ar + 16 * KB + kmajor_off(s2, cb + 8 * x, D));
 #pragma unroll
       for (int sub = 0; sub < 2; ++sub) {
         const int c0 = cb + 16 * sub;
@@ -2077,7 +2120,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   }
   if (!ok && t == 0) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
-    if (pending) mbar_wait(bar, phase);
+    if (pending) mbar_wait(&bar[0], phase);
+    if (cpending) mbar_wait(&bar[1], cphase);
   }
   fence_before_sync();
   __syncthreads();
