@@ -1023,8 +1023,8 @@ constexpr int D = 128, C = 64;
 constexpr uint32_t RA = 2 * 128 * D * 2;       // A operand hi | lo (64 KB)
 constexpr uint32_t RB = 2 * C * D * 2;         // B operand hi | lo (32 KB)
 constexpr size_t SMEM = (size_t)RA + (size_t)RB + C * 4 + 256 * 4 + 64;  // two CTAs per SM
-constexpr uint32_t TMEM_COLS = 128;
-constexpr uint32_t COL_0 = 0, COL_1 = 64;      // at most two 128 x 64 results alive
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t COL_0 = 0, COL_1 = 64, COL_2 = 128;  // 128 x 64 results
 }  // namespace tcg
 
 // 8 fp32 values -> hi / lo bf16 16-byte pieces at byte offset `off` of the two images
@@ -1200,13 +1200,13 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   unsigned char* Bl = Bh + RB / 2;
   float* dec = reinterpret_cast<float*>(Bh + RB);
   float* red = dec + C;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 256);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 256);  // [0] MMA, [1] bulk copies
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
   const int t = threadIdx.x, warp = t >> 5;
   const int64_t c = blockIdx.x;
-  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const int h = blockIdx.y;
   const ChunkRec rec = a.chunks[c];
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
@@ -1216,10 +1216,11 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   const float* E = a.b.dSE + ch * SZ;
   const int lane_row = (warp & 3) * 32 + (t & 31);  // TMEM lane = row of the transposed result
   const int cbase = (warp >> 2) * 32;               // this warp's 32 result columns
-  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + (tok0 * dm.hqk + hq) * D;
+  constexpr uint32_t IMGB = C * D * 2;  // one 64 x 128 (or 128 x 64) bf16 image
   if (t < C) dec[t] = expf(__fsub_rn(a.b.G[ch * C + C - 1], a.b.G[ch * C + t]));
   if (t == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
@@ -1228,10 +1229,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   fence_after_sync();
   const uint32_t tb = *tslot;
   const uint32_t tl = tmem_lane_addr(tb, warp, 0);
-  uint32_t phase = 0;
-  bool ok = true, pending = false;
+  uint32_t phase = 0, cphase = 0;
+  bool ok = true, pending = false, cpending = false;
   auto run = [&]() {  // all threads: wait for the committed MMAs
-    const bool done = mbar_wait(bar, phase);
+    const bool done = mbar_wait(&bar[0], phase);
     if (done) {
       phase ^= 1u;
       pending = false;
@@ -1246,9 +1247,30 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     if (t == 0) {
       fence_after_sync();
       mmas();
-      mma_commit(bar);
+      mma_commit(&bar[0]);
     }
     pending = true;
+  };
+  // the same after thread 0 has waited for the bulk copies in flight; every thread learns
+  // whether they arrived
+  auto issue_copies = [&](auto&& mmas) {
+    fence_proxy_async();
+    fence_before_sync();
+    bool got = true;
+    if (t == 0) {
+      got = mbar_wait(&bar[1], cphase);
+      if (got) {
+        cphase ^= 1u;
+        cpending = false;
+      }
+    }
+    ok = __syncthreads_and(got) != 0;
+    if (ok && t == 0) {
+      fence_after_sync();
+      mmas();
+      mma_commit(&bar[0]);
+    }
+    pending = ok;
   };
   const uint32_t sa_h = smem_u32(Ah), sa_l = smem_u32(Al), sb_h = smem_u32(Bh), sb_l = smem_u32(Bl);
 
@@ -1275,8 +1297,14 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   fence_before_sync();
   __syncthreads();
 
-  // ---- phase 2: E K^T, then dO^T P (the A region is reused); <E, S0> from the E build
+  // ---- phase 2a: E K^T (K rows: the prep kernel's image, one bulk copy); <E, S0> from the
+  // E build
   if (ok) {
+    if (t == 0) {
+      mbar_expect_tx(&bar[1], IMGB);
+      bulk_g2s(Bh, a.b.img + ch * (int64_t)prep_w_floats(C, D), IMGB, &bar[1]);
+      cpending = true;
+    }
     float part = 0.f;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {  // E image by halves, with S0 at the same positions
@@ -1290,33 +1318,18 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       et.store(Ah + hh * 16384, Al + hh * 16384);
     }
     red[t] = part;
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {  // K rows (exact in bf16, rows >= n zero)
-      int r, k0;
-      kmajor_piece(t + it * 256, D, r, k0);
-      *reinterpret_cast<uint4*>(Bh + kmajor_off(r, k0, D)) =
-          r < n ? *reinterpret_cast<const uint4*>(kb + (int64_t)r * dm.hqk * D + k0) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_h, D, idesc_bf16(128, C), 2); });
+    issue_copies([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_h, D, idesc_bf16(128, C), 2); });
   }
-  {
-    // dO^T (rows a, K = i) and P^T (rows s, K = i) loaded while E K^T runs
-    SplitTile<true, C, C> pt;
-    pt.load(a.b.P + ch * C * C, C, C);
-    float v[4][8];
-    load_dO_T(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
-    if (ok) run();
+  // ---- phase 3: (U E)^T = E^T U^T, E^T by transposing the E image in place
+  if (ok) {
+    SplitTile<false, C, D> ur;  // U rows, loaded while E K^T runs
+    ur.load(a.b.U + ch * CD, D, C);
+    run();
     if (ok) {
-      pt.store(Bh, Bh + C * C * 2);
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
-        split8(Ah, Ah + 128 * C * 2, kmajor_off(r, k0, C), v[it]);
-      }
-      issue([&] {
-        mma_terms(tb + COL_1, sa_h, sa_h + 128 * C * 2, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C), 3);
-      });
-      run();
+      transpose_image_inplace(Ah, D);
+      transpose_image_inplace(Al, D);
+      ur.store(Bh, Bl);
+      issue([&] { mma_terms(tb + COL_2, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
     }
   }
   for (int w2 = 128; w2 > 0; w2 >>= 1) {
@@ -1324,6 +1337,42 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     __syncthreads();
   }
   if (t == 0) a.b.sdot[ch] = red[0];
+  // ---- phase 2b: dO^T P: dO^T from the dO rows image (transposed in shared memory), P^T the
+  // prep kernel's image (one bulk copy)
+  if (ok) {
+    float v[4][8];  // dO rows, loaded while E^T U^T runs
+    load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+    run();
+    if (ok) {
+      if (t == 0) {
+        mbar_expect_tx(&bar[1], C * C * 4);
+        bulk_g2s(Bh, a.b.P + ch * C * C, C * C * 4, &bar[1]);
+        cpending = true;
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(t + it * 256, D, r, k0);
+        split8(Ah + 2 * IMGB, Ah + 3 * IMGB, kmajor_off(r, k0, D), v[it]);  // rows hi | lo
+      }
+      __syncthreads();
+      transpose_image(Ah, Ah + 2 * IMGB, D, C);
+      transpose_image(Ah + IMGB, Ah + 3 * IMGB, D, C);
+      issue_copies([&] {
+        mma_terms(tb + COL_1, sa_h, sa_h + IMGB, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C), 3);
+      });
+    }
+  }
+  if (ok) {  // U dS_end while dO^T P runs
+#pragma unroll
+    for (int s1 = 0; s1 < 2; ++s1) {
+      float w[16];
+      tmem_ld16(tl + COL_2 + cbase + 16 * s1, w);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) a.b.UdSe[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = w[e];
+    }
+    run();
+  }
   if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec): fp32 dU rows, and the dU^T operand image
     // (rows d, K = s; hi | lo) for the gradients kernel in this chunk-head's adjoint L slot
     unsigned char* uimg = reinterpret_cast<unsigned char*>(a.b.L + ch * SZ);
@@ -1344,39 +1393,22 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   }
   fence_before_sync();
   __syncthreads();
-
-  // ---- phase 3: (U E)^T = E^T U^T
+  // ---- phase 4: (dO S0)^T = S0^T dO^T, then dW^T = -S0^T dU^T (the B region is reused);
+  // S0^T by transposing the S0 image in place
   if (ok) {
-    build_dd<true>(Ah, Al, E);
-    build_split<false, C, D>(Bh, Bl, a.b.U + ch * CD, D, C);
-    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
-  }
-  {
-    float v[4][8];  // dO rows for phase 4, loaded while the product runs
+    float v[4][8];
     load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
-    if (ok) run();
-    if (ok) {
+    build_dd<false>(Ah, Al, S0);
 #pragma unroll
-      for (int s1 = 0; s1 < 2; ++s1) {
-        float w[16];
-        tmem_ld16(tl + COL_0 + cbase + 16 * s1, w);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) a.b.UdSe[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = w[e];
-      }
+    for (int it = 0; it < 4; ++it) {
+      int r, k0;
+      kmajor_piece(t + it * 256, D, r, k0);
+      split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
     }
-    fence_before_sync();
     __syncthreads();
-    // ---- phase 4: (dO S0)^T = S0^T dO^T, then dW^T = -S0^T dU^T (the B region is reused)
-    if (ok) {
-      build_dd<true>(Ah, Al, S0);
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        int r, k0;
-        kmajor_piece(t + it * 256, D, r, k0);
-        split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
-      }
-      issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
-    }
+    transpose_image_inplace(Ah, D);
+    transpose_image_inplace(Al, D);
+    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
   }
   if (ok) {
     SplitTile<false, C, D> dut;  // dU rows, loaded while the first product runs
@@ -1405,7 +1437,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     }
   } else if (t == 0) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
-    if (pending) mbar_wait(bar, phase);  // let this CTA's products finish before TMEM goes
+    if (pending) mbar_wait(&bar[0], phase);  // let this CTA's products and copies finish
+    if (cpending) mbar_wait(&bar[1], cphase);
   }
   fence_before_sync();
   __syncthreads();
@@ -1419,8 +1452,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 //   P    = Gam (.) (Q K^T), lower with diagonal                       (exact bf16 inputs)
 //   Qt   = diag(e^G) Q - P W                                          (P, W split hi/lo)
 //   L    = dO^T Qt                                                    (dO, Qt split)
-// Outputs W, Ut, G, P, L, the reverse chain's images and the T^T operand image of the
-// gradients kernel (in T's slot).  W, P and Qt also leave their readouts as split images in
+// Outputs W, Ut, G, L, the reverse chain's images and two operand images: P^T for the
+// big-products kernel (in P's slot) and T^T for the gradients kernel (in T's slot).  W, P and Qt also leave their readouts as split images in
 // shared memory, where the transposed operands are built.
 namespace tcq {
 constexpr int D = 128, C = 64, QCP = C + 1, TCP = C;  // row strides of A (padded) and T
@@ -1674,9 +1707,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
         const int s = s0 + e;
         v[e] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v[e]) : 0.f;
       }
-#pragma unroll
-      for (int e = 0; e < 16; e += 4)
-        *reinterpret_cast<float4*>(a.b.P + ch * C * C + i * C + s0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
       split8(TKh, TKl, kmajor_off(i, s0, C), v);
       split8(TKh, TKl, kmajor_off(i, s0 + 8, C), v + 8);
     }
@@ -1693,6 +1723,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     load_dO_T(dov, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
     for (int q = t; q < (int)(2 * TILE / 16); q += 256)  // W^T images for the reverse chain
       reinterpret_cast<uint4*>(img + TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
+    // P^T hi | lo (over the dead TV) -> P's slot: the big-products kernel's operand image
+    tc::transpose_image(smq + OFF_TV, TKh, C, C);
+    tc::transpose_image(smq + OFF_TV + C * C * 2, TKl, C, C);
+    __syncthreads();
+    for (int q = t; q < C * C * 4 / 16; q += 256)
+      reinterpret_cast<uint4*>(a.b.P + ch * C * C)[q] = reinterpret_cast<const uint4*>(smq + OFF_TV)[q];
     wait_mma();
   }
   // Qt rows hi | lo over the dead TV and T regions

@@ -196,5 +196,44 @@ __device__ __forceinline__ void transpose_image(unsigned char* dst, const unsign
   }
 }
 
+// In-place transpose of a square N x N K-major image (N = 64 or 128); 256 threads.  Core
+// matrices (a, b) and (b, a) trade places, each transposed, two pairs per warp instruction;
+// then the diagonal cores, four per instruction.  A core is read and rewritten by one warp
+// only, and a warp's ldmatrix completes before its stmatrix (the registers carry the data).
+__device__ __forceinline__ void transpose_image_inplace(unsigned char* img, int N) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nb = N / 8, npair_ops = nb * (nb - 1) / 4, nops = npair_ops + nb / 4;
+  const uint32_t sbo = (uint32_t)nb * 128;
+  const uint32_t base = smem_u32(img) + (lane & 7) * 16;
+  const int slot = lane >> 3;
+  for (int o = warp; o < nops; o += 8) {
+    int y, x, ys, xs;  // core loaded by this lane's slot, core its slot stores to
+    if (o < npair_ops) {
+      int p = 2 * o + (slot >> 1), a = 0, rowlen = nb - 1;  // p-th pair (a, b), a < b, row by row
+      while (p >= rowlen) {
+        p -= rowlen;
+        ++a;
+        --rowlen;
+      }
+      const int b = a + 1 + p;
+      y = (slot & 1) ? b : a;
+      x = (slot & 1) ? a : b;
+      ys = x;
+      xs = y;
+    } else {
+      y = x = ys = xs = 4 * (o - npair_ops) + slot;
+    }
+    uint32_t r0, r1, r2, r3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(base + y * sbo + x * 128)
+                 : "memory");
+    // register i holds the transpose of slot i's core; slot i's lanes give the address it goes to
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(base + ys * sbo + xs * 128),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+  }
+}
+
 }  // namespace tc
 }  // namespace gdn

@@ -107,3 +107,24 @@ extern "C" int transpose_selftest(const void* X, void* Y, int R, int Ks, cudaStr
   k_transpose_selftest<<<1, 256, smem, st>>>(static_cast<const uint16_t*>(X), static_cast<uint16_t*>(Y), R, Ks);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
+
+// transpose_image_inplace: an N x N bf16 matrix X into its K-major image, transposed in place
+__global__ void __launch_bounds__(256) k_transpose_inplace_selftest(const uint16_t* X, uint16_t* Y, int N) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  for (int e = threadIdx.x; e < N * N; e += 256)
+    *reinterpret_cast<uint16_t*>(sm + kmajor_off(e / N, e % N, N)) = X[e];
+  __syncthreads();
+  transpose_image_inplace(sm, N);
+  __syncthreads();
+  for (int e = threadIdx.x; e < N * N; e += 256) Y[e] = *reinterpret_cast<const uint16_t*>(sm + kmajor_off(e / N, e % N, N));
+}
+
+extern "C" int transpose_inplace_selftest(const void* X, void* Y, int N, cudaStream_t st) {
+  if (N != 64 && N != 128) return 1;
+  const size_t smem = (size_t)N * N * 2;
+  if (cudaFuncSetAttribute(k_transpose_inplace_selftest, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return 2;
+  k_transpose_inplace_selftest<<<1, 256, smem, st>>>(static_cast<const uint16_t*>(X), static_cast<uint16_t*>(Y), N);
+  return cudaGetLastError() == cudaSuccess ? 0 : 3;
+}

@@ -29,6 +29,8 @@ def lib():
     L.transpose_selftest.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_void_p]
     L.transpose_selftest.restype = ctypes.c_int
+    L.transpose_inplace_selftest.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    L.transpose_inplace_selftest.restype = ctypes.c_int
     return L
 
 
@@ -97,3 +99,17 @@ def test_unrolled_inverse_matches_generic_bits(inv_lib, seed, scale):
     T = Tg.double().cpu()
     resid = (T @ (torch.eye(64, dtype=torch.float64) + A.double()) - torch.eye(64, dtype=torch.float64))
     assert resid.abs().max().item() <= 1e-4 * max(1.0, T.abs().max().item())
+
+
+@pytest.mark.parametrize("N", [64, 128])
+def test_transpose_image_inplace_is_exact(lib, N):
+    """The in-place square image transpose (core-matrix pairs swapped through ldmatrix .trans +
+    stmatrix) moves every bf16 bit pattern to its transposed place."""
+    g = torch.Generator().manual_seed(N)
+    X = torch.randint(0, 1 << 16, (N, N), generator=g, dtype=torch.int32).to(torch.int16)
+    dX = X.cuda()
+    Y = torch.zeros((N, N), dtype=torch.int16, device="cuda")
+    rc = lib.transpose_inplace_selftest(dX.data_ptr(), Y.data_ptr(), N, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert torch.equal(Y.cpu(), X.T.contiguous())
