@@ -171,67 +171,91 @@ __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(__fsub_rn(x, __bfloat162float(hi)));
 }
 
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
 // dst = transpose of a shared-memory image: src is Ks rows x R columns (K-major, K = R),
 // dst is R rows x Ks columns (K = Ks); 256 threads, R and Ks multiples of 16 (whole groups of
-// four core matrices).  In the no-swizzle K-major layout an 8 x 8 core matrix is 8 rows of 16
-// contiguous bytes, and core matrix (xb, yb) of dst is the transpose of core matrix (yb, xb)
-// of src: each warp moves four at a time with ldmatrix .trans and stmatrix (eight 16-byte
-// rows per matrix on each side, one wavefront each).
+// four core matrices).  In the no-swizzle K-major layout an 8 x 8
+// core matrix is 8 rows of 16 contiguous bytes, and core matrix (xb, yb) of dst is the
+// transpose of core matrix (yb, xb) of src: each warp moves four at a time with ldmatrix
+// .trans and stmatrix (eight 16-byte rows per matrix on each side, one wavefront each), in
+// batches of 128 cores with a warp's loads before its stores.
 __device__ __forceinline__ void transpose_image(unsigned char* dst, const unsigned char* src, int R, int Ks) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int xbs = R / 8, ncore = (Ks / 8) * xbs;
   const uint32_t sbo_s = (uint32_t)xbs * 128, sbo_d = (uint32_t)(Ks / 8) * 128;
   const uint32_t s0 = smem_u32(src) + (lane & 7) * 16, d0 = smem_u32(dst) + (lane & 7) * 16;
-  for (int q0 = warp * 4; q0 < ncore; q0 += 32) {
-    const int q = q0 + (lane >> 3);  // this lane's row address is in matrix lane / 8
-    const int yb = q / xbs, xb = q % xbs;
-    uint32_t r0, r1, r2, r3;
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(s0 + yb * sbo_s + xb * 128)
-                 : "memory");
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(d0 + xb * sbo_d + yb * 128),
-                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-                 : "memory");
+  for (int c0 = 0; c0 < ncore; c0 += 128) {  // batches of 128 cores
+    uint32_t r[4][4], da[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // op k of this warp: cores c0 + 32 k + 4 warp .. + 3
+      const int q = c0 + 32 * k + 4 * warp + (lane >> 3);  // this lane's row address is in matrix lane / 8
+      if (c0 + 32 * k + 4 * warp < ncore) {
+        const int yb = q / xbs, xb = q % xbs;
+        ldsm_x4_trans(s0 + yb * sbo_s + xb * 128, r[k]);
+        da[k] = d0 + xb * sbo_d + yb * 128;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (c0 + 32 * k + 4 * warp < ncore) stsm_x4(da[k], r[k]);
   }
 }
 
 // In-place transpose of a square N x N K-major image (N = 64 or 128); 256 threads.  Core
 // matrices (a, b) and (b, a) trade places, each transposed, two pairs per warp instruction;
-// then the diagonal cores, four per instruction.  A core is read and rewritten by one warp
-// only, and a warp's ldmatrix completes before its stmatrix (the registers carry the data).
+// then the diagonal cores, four per instruction.  With nb = N / 8 cores a side, unordered
+// pair p < nb (nb/2 - 1) is (a, a + k mod nb), k = 1 + p / nb, a = p mod nb, and the others
+// are (a, a + nb/2).  A core is read and rewritten by one warp only, and each batch of a
+// warp's ldmatrix completes before its stmatrix (the registers carry the data).
 __device__ __forceinline__ void transpose_image_inplace(unsigned char* img, int N) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nb = N / 8, npair_ops = nb * (nb - 1) / 4, nops = npair_ops + nb / 4;
+  const int nfirst = nb * (nb / 2 - 1);
   const uint32_t sbo = (uint32_t)nb * 128;
   const uint32_t base = smem_u32(img) + (lane & 7) * 16;
   const int slot = lane >> 3;
-  for (int o = warp; o < nops; o += 8) {
-    int y, x, ys, xs;  // core loaded by this lane's slot, core its slot stores to
-    if (o < npair_ops) {
-      int p = 2 * o + (slot >> 1), a = 0, rowlen = nb - 1;  // p-th pair (a, b), a < b, row by row
-      while (p >= rowlen) {
-        p -= rowlen;
-        ++a;
-        --rowlen;
+  for (int o0 = warp; o0 < nops; o0 += 32) {  // batches of up to four ops per warp
+    uint32_t r[4][4], da[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int o = o0 + 8 * k;
+      if (o < nops) {
+        int y, x;  // core loaded by this lane's slot; the slot stores to core (x, y)
+        if (o < npair_ops) {
+          const int p = 2 * o + (slot >> 1);
+          int pa, pb;
+          if (p < nfirst) {
+            pa = p % nb;
+            pb = (pa + 1 + p / nb) % nb;
+          } else {
+            pa = p - nfirst;
+            pb = pa + nb / 2;
+          }
+          y = (slot & 1) ? pb : pa;
+          x = (slot & 1) ? pa : pb;
+        } else {
+          y = x = 4 * (o - npair_ops) + slot;
+        }
+        ldsm_x4_trans(base + y * sbo + x * 128, r[k]);
+        da[k] = base + x * sbo + y * 128;
       }
-      const int b = a + 1 + p;
-      y = (slot & 1) ? b : a;
-      x = (slot & 1) ? a : b;
-      ys = x;
-      xs = y;
-    } else {
-      y = x = ys = xs = 4 * (o - npair_ops) + slot;
     }
-    uint32_t r0, r1, r2, r3;
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(base + y * sbo + x * 128)
-                 : "memory");
-    // register i holds the transpose of slot i's core; slot i's lanes give the address it goes to
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(base + ys * sbo + xs * 128),
-                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-                 : "memory");
+    // register i holds the transpose of slot i's core; slot i's lanes give the address it
+    // goes to
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (o0 + 8 * k < nops) stsm_x4(da[k], r[k]);
   }
 }
 
