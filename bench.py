@@ -48,11 +48,11 @@ SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
 # reported only while the kernel's source (its function text plus common.cuh) hashes to the
 # value it had when the counters were taken; after any change it is null until recaptured.
 NCU_TRAFFIC = {
-    # 202,745,600 + 21,815,552 B for one 4096-token sequence x 32 value heads
-    "k_intra": {"src_sha": "9cb58c197a155185", "bytes_per_unit": (202745600 + 21815552) / (4096 * 32),
+    # 202,417,152 + 21,302,272 B for one 4096-token sequence x 32 value heads
+    "k_intra": {"src_sha": "0e9b2b896cd17890", "bytes_per_unit": (202417152 + 21302272) / (4096 * 32),
                 "unit": "token-head"},
-    # 541,289,472 + 486,616,576 B for the full 256-slot x 32-head launch (one-pass capture)
-    "k_decode": {"src_sha": "21ffd2cd2457bd1a", "bytes_per_unit": (541289472 + 486616576) / (256 * 32),
+    # 541,309,184 + 482,726,912 B for the full 256-slot x 32-head launch (one-pass capture)
+    "k_decode": {"src_sha": "074ccdf2bcef8277", "bytes_per_unit": (541309184 + 482726912) / (256 * 32),
                  "unit": "slot-head"},
 }
 KERNEL_TEXT = {  # file, first line of the kernel, first line after it
