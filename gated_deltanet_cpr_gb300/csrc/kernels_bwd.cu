@@ -758,21 +758,25 @@ __global__ void k_bwd_gqa(const float* __restrict__ dq_part, const float* __rest
                           float* __restrict__ dq, float* __restrict__ dk, int64_t T, int hqk,
                           int hv, int D, const WsHeader* __restrict__ hdr) {
   if (!hdr->valid) return;
-  const int grp = hv / hqk;
-  const int64_t total = T * hqk * D;
-  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t tok = e / ((int64_t)hqk * D);
-    const int hq = (int)((e / D) % hqk), k = (int)(e % D);
-    const int64_t base = (tok * hv + (int64_t)hq * grp) * D + k;
-    float sq = dq_part[base], sk = dk_part[base];
-    for (int j = 1; j < grp; ++j) {
-      sq = __fadd_rn(sq, dq_part[base + (int64_t)j * D]);
-      sk = __fadd_rn(sk, dk_part[base + (int64_t)j * D]);
-    }
-    dq[e] = sq;
-    dk[e] = sk;
+  // one thread per float4 of one (token, query/key head) row; a block covers 256 / (D / 4)
+  // rows; the value heads of the group are summed in ascending order
+  const int grp = hv / hqk, d4 = D / 4;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / d4) + threadIdx.x / d4;
+  if (row >= T * hqk) return;
+  const int c = 4 * (threadIdx.x % d4);
+  const int64_t tok = row / hqk;
+  const int hq = (int)(row - tok * hqk);
+  const int64_t base = (tok * hv + (int64_t)hq * grp) * D + c;
+  float4 sq = *reinterpret_cast<const float4*>(dq_part + base);
+  float4 sk = *reinterpret_cast<const float4*>(dk_part + base);
+  for (int j = 1; j < grp; ++j) {
+    const float4 xq = *reinterpret_cast<const float4*>(dq_part + base + (int64_t)j * D);
+    const float4 xk = *reinterpret_cast<const float4*>(dk_part + base + (int64_t)j * D);
+    sq = make_float4(__fadd_rn(sq.x, xq.x), __fadd_rn(sq.y, xq.y), __fadd_rn(sq.z, xq.z), __fadd_rn(sq.w, xq.w));
+    sk = make_float4(__fadd_rn(sk.x, xk.x), __fadd_rn(sk.y, xk.y), __fadd_rn(sk.z, xk.z), __fadd_rn(sk.w, xk.w));
   }
+  *reinterpret_cast<float4*>(dq + row * D + c) = sq;
+  *reinterpret_cast<float4*>(dk + row * D + c) = sk;
 }
 
 // ============================================================  KB2 (tcgen05)  ===
@@ -1811,10 +1815,17 @@ namespace tcd {
 constexpr int D = 128, C = 64;
 constexpr uint32_t KB = 1024, ARENA = 96 * KB;
 constexpr uint32_t IMG = 16 * KB;  // a 64 x 128 or 128 x 64 bf16 image (hi or lo)
-constexpr size_t SMEM1 = ARENA + 13 * C * 4 + 64;
-constexpr size_t SMEM2 = ARENA + 18 * C * 4 + 64;
+constexpr int TRI = C * (C + 1) / 2;  // packed lower triangle with the diagonal
+constexpr size_t SMEM1 = ARENA + (13 * C + TRI) * 4 + 64;
+constexpr size_t SMEM2 = ARENA + (18 * C + TRI) * 4 + 64;
 constexpr uint32_t TMEM1 = 256, TMEM2 = 128;
 }  // namespace tcd
+
+// e^{G_i - G_s} for s <= i, packed by rows at i (i + 1) / 2 + s; all 256 threads, C = 64
+__device__ __forceinline__ void decay_table_lower(float* tab, const float* Gs) {
+  const int i = threadIdx.x & 63;
+  for (int s = threadIdx.x >> 6; s <= i; s += 4) tab[i * (i + 1) / 2 + s] = expf(__fsub_rn(Gs[i], Gs[s]));
+}
 
 // fixed-order warp sum (xor tree); every lane gets the total
 __device__ __forceinline__ float warp_sum(float x) {
@@ -1836,7 +1847,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   float* dGa = colp + 2 * C;   // [2][C]
   float* dba = dGa + 2 * C;    // [2][C]
   float* kY = dba + 2 * C;     // [2][C]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(kY + 2 * C);  // [0] MMA, [1] bulk copies
+  float* gam = kY + 2 * C;     // e^{G_i - G_s}, s <= i (decay_table_lower)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gam + TRI);  // [0] MMA, [1] bulk copies
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
@@ -1958,6 +1970,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   }
   pending = true;
   if (t < C) eG[t] = expf(Gs[t]);
+  decay_table_lower(gam, Gs);  // while the products run
   wait_mma();
   if (ok && rowlane) {  // Pm, dG_b row / column sums, Pm image
     const int i = row;
@@ -1971,7 +1984,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int s = s0 + e;
-        const float pv = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), pm[e]) : 0.f;
+        const float pv = (i >= s) ? __fmul_rn(gam[i * (i + 1) / 2 + s], pm[e]) : 0.f;
         const float pr = (i > s) ? __fmul_rn(pv, qk[e]) : 0.f;
         pm[e] = pv;
         qk[e] = pr;
@@ -2180,7 +2193,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   float* cs = colg + 2 * C;    // [2][C] U dS_end . k
   float* dgv = cs + 2 * C;
   float* csv = dgv + C;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(csv + C);  // [0] MMA, [1] bulk copies
+  float* gtab = csv + C;  // e^{G_i - G_s}, s <= i (decay_table_lower)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gtab + TRI);  // [0] MMA, [1] bulk copies
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
@@ -2276,6 +2290,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
     eG[t] = expf(Gs[t]);
     dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
   }
+  decay_table_lower(gtab, Gs);  // while the products run
   if (ok) wait_mma();
   // ---- round B: dA += X Ut^T
   if (ok) {
@@ -2293,7 +2308,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   }
   if (ok && rowlane) {  // dA (strictly lower), A' = Gam (.) K K^T; dbeta_c, dG_e sums; dAm image
     const int i = row;
-    const float bi = bs[i], gi = Gs[i];
+    const float bi = bs[i];
     float rb = 0.f, rg = 0.f;
 #pragma unroll
     for (int s1 = 0; s1 < 2; ++s1) {
@@ -2305,7 +2320,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
       for (int e = 0; e < 16; ++e) {
         const int s = s0 + e;
         const bool low = i > s;
-        const float gam = expf(__fsub_rn(gi, Gs[s]));
+        const float gam = low ? gtab[i * (i + 1) / 2 + s] : 0.f;
         const float da = low ? -v[e] : 0.f;
         const float ap = low ? __fmul_rn(gam, kk[e]) : 0.f;
         const float dab = __fmul_rn(da, bi);
@@ -2473,9 +2488,9 @@ void launch_bwd_t(const BwdArgs& a, int64_t n_chunks, int N, BwdStageFn mark, vo
   }
   mark(mark_ctx, n_chunks > 0 ? (boundary_on_tensor_cores(a.dm) ? 2 : 1) : 0);
   if (a.T > 0) {
-    const int64_t total = a.T * a.dm.hqk * D;
-    const int blocks = (int)((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
-    k_bwd_gqa<<<blocks, 256, 0, st>>>(a.b.dq_part, a.b.dk_part, a.dq, a.dk, a.T, a.dm.hqk, a.dm.hv, D, a.hdr);
+    const int64_t rows = a.T * a.dm.hqk, per_block = 256 / (D / 4);
+    k_bwd_gqa<<<(unsigned)((rows + per_block - 1) / per_block), 256, 0, st>>>(a.b.dq_part, a.b.dk_part, a.dq, a.dk,
+                                                                              a.T, a.dm.hqk, a.dm.hv, D, a.hdr);
   }
   mark(mark_ctx, a.T > 0 ? 1 : 0);
 }
