@@ -426,14 +426,15 @@ def run_cuda(args):
 
     # dominant kernel: intra-chunk recurrence (FP32 ALU bound)
     intra_ms = kern["intra_chunk"]
-    flops_intra = T * hv * 7 * d * d  # per token-head: d^2 MUL + 3 d^2 FMA (FMA = 2 FLOP)
+    flops_intra = T * hv * 6 * d * d  # per token-head: 3 d^2 FMA (FMA = 2 FLOP); the decay is a scalar
     alu_peak = 2 * SMS * FP32_LANES * SM_MAX_MHZ * 1e6 / 1e12
     ach_intra = flops_intra / (intra_ms * 1e-3) / 1e12
     roofline = {"bound": "alu", "kernel": "k_intra (intra-chunk recurrence)", "achieved": ach_intra,
                 "peak": alu_peak, "unit": "TFLOP/s", "frac": ach_intra / alu_peak,
                 "traffic": ncu_traffic("k_intra", T * hv),
-                "peak_note": "FP32 FMA peak 2 x 152 SMs x 128 lanes x 2070 MHz; this op mix "
-                             "(1 MUL + 3 FMA per state element) caps frac at 7/8"}
+                "peak_note": "FP32 FMA peak 2 x 152 SMs x 128 lanes x 2070 MHz; the token step is "
+                             "three FMA sweeps per state element (the decay is carried as a scalar "
+                             "scale of the state), so the work is 6 d^2 FLOP per token-head"}
     chunk_heads_full = sum(L // C for L in w.lengths) * hv
     flops_bnd = chunk_heads_full * (6 * C * C * d + 4 * C * d * d)
     bnd_ms = kern["boundary_prepass"] + kern["boundary_chain"]

@@ -45,7 +45,7 @@ class Shape(ctypes.Structure):
 
 
 class CacheStruct(ctypes.Structure):
-    _fields_ = [("s_run", ctypes.c_void_p), ("s_bnd", ctypes.c_void_p),
+    _fields_ = [("s_run", ctypes.c_void_p), ("c_run", ctypes.c_void_p), ("s_bnd", ctypes.c_void_p),
                 ("tail_k", ctypes.c_void_p), ("tail_v", ctypes.c_void_p),
                 ("tail_g", ctypes.c_void_p), ("tail_beta", ctypes.c_void_p),
                 ("pos", ctypes.c_void_p), ("slots", ctypes.c_int32)]
@@ -165,13 +165,15 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 
 class Cache:
-    """Decode cache (see gdn_cpr_cache): running state, boundary state, chunk tail, position.
+    """Decode cache (see gdn_cpr_cache): running state (held as c_run * s_run, see
+    running_state), boundary state, chunk tail, position.
     Also the full checkpoint of every decoding sequence: copying these tensors out and back
     resumes decoding bit-exactly."""
 
     def __init__(self, slots, h_qk, h_v, d, chunk, dtype=torch.bfloat16, device="cuda"):
         self.slots, self.h_qk, self.h_v, self.d, self.chunk, self.dtype = slots, h_qk, h_v, d, chunk, dtype
         self.s_run = torch.zeros((slots, h_v, d, d), dtype=torch.float32, device=device)
+        self.c_run = torch.ones((slots, h_v), dtype=torch.float32, device=device)
         self.s_bnd = torch.zeros((slots, h_v, d, d), dtype=torch.float32, device=device)
         self.tail_k = torch.zeros((slots, chunk, h_qk, d), dtype=dtype, device=device)
         self.tail_v = torch.zeros((slots, chunk, h_v, d), dtype=dtype, device=device)
@@ -179,7 +181,13 @@ class Cache:
         self.tail_beta = torch.zeros((slots, chunk, h_v), dtype=torch.float32, device=device)
         self.pos = torch.zeros((slots,), dtype=torch.int32, device=device)
 
-    TENSORS = ("s_run", "s_bnd", "tail_k", "tail_v", "tail_g", "tail_beta", "pos")
+    TENSORS = ("s_run", "c_run", "s_bnd", "tail_k", "tail_v", "tail_g", "tail_beta", "pos")
+
+    def running_state(self, slots=None):
+        """The running state c_run * s_run (fp32, [slots, H_v, d, d]; all slots if None), as
+        the kernels form state_out: one round-to-nearest product per element."""
+        s, c = (self.s_run, self.c_run) if slots is None else (self.s_run[slots], self.c_run[slots])
+        return s * c[..., None, None]
 
     def struct(self) -> CacheStruct:
         return CacheStruct(*(_p(getattr(self, n)) for n in self.TENSORS), self.slots)

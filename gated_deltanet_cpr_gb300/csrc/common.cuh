@@ -139,6 +139,16 @@ struct StateLayout {
 #pragma unroll
       for (int j = 0; j < J; ++j) *reinterpret_cast<float4*>(dst + (int64_t)(row0 + r) * D + col(j)) = S[r][j];
   }
+  // the explicit state c S (one round-to-nearest product per element)
+  __device__ __forceinline__ void store_scaled(const float4 (&S)[4][J], float c, float* dst) const {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        *reinterpret_cast<float4*>(dst + (int64_t)(row0 + r) * D + col(j)) =
+            make_float4(__fmul_rn(c, S[r][j].x), __fmul_rn(c, S[r][j].y), __fmul_rn(c, S[r][j].z),
+                        __fmul_rn(c, S[r][j].w));
+  }
 };
 
 // Sum over the 8 lanes of a row group of x[r] (r = 0..3, one value per row of the group):
@@ -167,50 +177,77 @@ __device__ __forceinline__ void group_allreduce4(const float (&x)[4], float (&to
   for (int r = 0; r < 4; ++r) tot[r] = __fadd_rn(y[r], __shfl_xor_sync(0xffffffffu, y[r], 1));
 }
 
-// One gated delta-rule step on the lane's 4 state rows (StateLayout), in the recurrence's
-// own order of operations:
+// One gated delta-rule step on the lane's 4 state rows (StateLayout).  The recurrence
 //     S <- a S;   p = S k;   u = beta (v - p);   S <- S + u k^T;   o = S q
-// Each row's dot: per lane one float2 partial over the lane's columns in the order (j, pair):
-// .x takes columns 32j + 4b, then 32j + 4b + 2, .y columns 32j + 4b + 1, then 32j + 4b + 3,
-// ascending j; then x + y, then group_reduce4 over the 8 lanes.  k (kept in registers from the dot to
-// the update) and q are fp32 copies in shared memory (exact widenings of the inputs); v4 is
-// v of the lane's 4 rows.  The step is split in two sweeps so that a token loop can overlap
-// the output reduction of one token with the first sweep of the next:
-//   ts_decay_dot   S <- a S, k into registers, the lane's partials of S k
-//   ts_update_dot  (after group_allreduce4 of those partials) the update and the lane's
-//                  partials of S q, to be reduced by group_reduce4
+// runs on a scaled copy: the state is S = c S~ (c the product of the decays since S~ was
+// last made equal to S), so the decay is one scalar product instead of a pass over the state:
+//     c <- c a;   p = c (S~ k);   u = beta (v - p);   S~ <- S~ + (u / c) k^T;   o = c (S~ q)
+// (u / c as u * rcp(c), rcp correctly rounded).  Whenever c leaves [2^-64, 2^64] the state is
+// made explicit first (S~ <- c S~, c <- 1), so S~ stays within 2^64 of S and no scale under-
+// or overflows; c is the same in every lane, so the choice is warp-uniform.  Each row's dot:
+// per lane one float2 partial over the lane's columns in the order (j, pair): .x takes
+// columns 32j + 4b, then 32j + 4b + 2, .y columns 32j + 4b + 1, then 32j + 4b + 3, ascending j;
+// then x + y, then the 8 lanes' fixed tree (group_reduce4; for p every lane needs all four
+// rows, group_allreduce4, the same tree).  k (kept in registers from the dot to the update)
+// and q are fp32 copies in shared memory (exact widenings of the inputs); v4 is v of the
+// lane's 4 rows.  The step is split in two sweeps so that a token loop can overlap the output
+// reduction of one token with the first sweep of the next:
+//   ts_dot_k       k into registers, the lane's partials of S~ k
+//   ts_update_dot  S~ <- S~ + us_r k^T (us_r = u_r / c per row), the lane's partials of S~ q
 // token_step is the whole step.  All 32 lanes of the warp call these together.
+constexpr float kScaleLo = 0x1p-64f, kScaleHi = 0x1p64f;
+
+// c <- c a; if c leaves [2^-64, 2^64] the state becomes explicit (S~ <- c S~, c <- 1)
 template <int D>
-__device__ __forceinline__ void ts_decay_dot(float4 (&S)[4][D / 32], const float* __restrict__ k_sh, float a, int b,
-                                             float4 (&kk)[D / 32], float (&part)[4]) {
+__device__ __forceinline__ void ts_decay(float4 (&S)[4][D / 32], float& c, float a) {
+  constexpr int J = D / 32;
+  c = __fmul_rn(c, a);
+  if (!(c >= kScaleLo && c <= kScaleHi)) {
+    const float2 c2 = make_float2(c, c);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const float2 s01 = mul2(c2, make_float2(S[r][j].x, S[r][j].y));
+        const float2 s23 = mul2(c2, make_float2(S[r][j].z, S[r][j].w));
+        S[r][j] = make_float4(s01.x, s01.y, s23.x, s23.y);
+      }
+    c = 1.f;
+  }
+}
+template <int D>
+__device__ __forceinline__ void ts_dot_k(const float4 (&S)[4][D / 32], const float* __restrict__ k_sh, int b,
+                                         float4 (&kk)[D / 32], float (&part)[4]) {
   constexpr int J = D / 32;
 #pragma unroll
   for (int j = 0; j < J; ++j) kk[j] = *reinterpret_cast<const float4*>(k_sh + 32 * j + 4 * b);
-  const float2 a2 = make_float2(a, a);
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     float2 pr = make_float2(0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      const float2 s01 = mul2(a2, make_float2(S[r][j].x, S[r][j].y));
-      const float2 s23 = mul2(a2, make_float2(S[r][j].z, S[r][j].w));
-      pr = fma2(s01, make_float2(kk[j].x, kk[j].y), pr);
-      pr = fma2(s23, make_float2(kk[j].z, kk[j].w), pr);
-      S[r][j] = make_float4(s01.x, s01.y, s23.x, s23.y);
+      pr = fma2(make_float2(S[r][j].x, S[r][j].y), make_float2(kk[j].x, kk[j].y), pr);
+      pr = fma2(make_float2(S[r][j].z, S[r][j].w), make_float2(kk[j].z, kk[j].w), pr);
     }
     part[r] = __fadd_rn(pr.x, pr.y);
   }
 }
-template <int D>
-__device__ __forceinline__ void ts_update_dot(float4 (&S)[4][D / 32], const float4 (&kk)[D / 32],
-                                              const float* __restrict__ q_sh, float beta, float4 v4,
-                                              const float (&p)[4], int b, float (&opart)[4]) {
-  constexpr int J = D / 32;
+// us_r = u_r / c for the lane's rows from the reduced S~ k (p4, all four rows): u = beta (v - c p)
+__device__ __forceinline__ void ts_scaled_u(const float (&p4)[4], float4 v4, float beta, float c,
+                                            float (&us)[4]) {
+  const float ic = __frcp_rn(c);
   const float v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
+  for (int r = 0; r < 4; ++r) us[r] = __fmul_rn(__fmul_rn(beta, __fsub_rn(v[r], __fmul_rn(c, p4[r]))), ic);
+}
+template <int D>
+__device__ __forceinline__ void ts_update_dot(float4 (&S)[4][D / 32], const float4 (&kk)[D / 32],
+                                              const float* __restrict__ q_sh, const float (&us)[4], int b,
+                                              float (&opart)[4]) {
+  constexpr int J = D / 32;
+#pragma unroll
   for (int r = 0; r < 4; ++r) {
-    const float u = __fmul_rn(beta, __fsub_rn(v[r], p[r]));
-    const float2 u2 = make_float2(u, u);
+    const float2 u2 = make_float2(us[r], us[r]);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const float2 s01 = fma2(u2, make_float2(kk[j].x, kk[j].y), make_float2(S[r][j].x, S[r][j].y));
@@ -232,17 +269,19 @@ __device__ __forceinline__ void ts_update_dot(float4 (&S)[4][D / 32], const floa
     opart[r] = __fadd_rn(pr.x, pr.y);
   }
 }
-// The whole step; returns o of row out_row().
+// The whole step on S~ with scale c (updated); returns o of row out_row().
 template <int D>
-__device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], const float* __restrict__ k_sh,
+__device__ __forceinline__ float token_step(float4 (&S)[4][D / 32], float& c, const float* __restrict__ k_sh,
                                             const float* __restrict__ q_sh, float a, float beta, float4 v4,
                                             int b) {
   float4 kk[D / 32];
-  float part[4], p[4], opart[4];
-  ts_decay_dot<D>(S, k_sh, a, b, kk, part);
+  float part[4], p[4], us[4], opart[4];
+  ts_decay<D>(S, c, a);
+  ts_dot_k<D>(S, k_sh, b, kk, part);
   group_allreduce4(part, p);
-  ts_update_dot<D>(S, kk, q_sh, beta, v4, p, b, opart);
-  return group_reduce4(opart, b);
+  ts_scaled_u(p, v4, beta, c, us);
+  ts_update_dot<D>(S, kk, q_sh, us, b, opart);
+  return __fmul_rn(c, group_reduce4(opart, b));
 }
 
 // T = (I + A)^{-1} for a strictly lower C x C matrix A in shared memory (row stride CPA; T

@@ -10,7 +10,7 @@
 #include "../../include/gdn_cpr.h"
 #include "launch.h"
 
-#define GDN_VERSION_NUM 100  // 0.1.0
+#define GDN_VERSION_NUM 200  // 0.2.0
 
 namespace {
 using namespace gdn;
@@ -122,7 +122,7 @@ inline char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 gdn_status check_cache(const gdn_cpr_cache* c) {
   if (!c) return GDN_ERR_INVALID_ARG;
   if (c->slots <= 0) return GDN_ERR_INVALID_ARG;
-  if (!ok_ptr(c->s_run, 16) || !ok_ptr(c->s_bnd, 16) || !ok_ptr(c->tail_k, 16) ||
+  if (!ok_ptr(c->s_run, 16) || !ok_ptr(c->c_run, 4) || !ok_ptr(c->s_bnd, 16) || !ok_ptr(c->tail_k, 16) ||
       !ok_ptr(c->tail_v, 16) || !ok_ptr(c->tail_g, 4) || !ok_ptr(c->tail_beta, 4) ||
       !ok_ptr(c->pos, 4))
     return GDN_ERR_INVALID_ARG;
@@ -264,6 +264,7 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   if (cache) {
     cw.cache_bnd = cache->s_bnd;
     cw.cache_run = cache->s_run;
+    cw.cache_c_run = cache->c_run;
     cw.cache_slots = cache->slots;
     cw.slot_of_seq = slot_of_seq;
   }
@@ -279,6 +280,7 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   iw.state_out = state_out;
   if (cache) {
     iw.cache_run = cache->s_run;
+    iw.cache_c_run = cache->c_run;
     iw.cache_slots = cache->slots;
     iw.slot_of_seq = slot_of_seq;
   }
@@ -395,6 +397,7 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
   dw.slot = slot;
   dw.slots = cache->slots;
   dw.s_run = cache->s_run;
+  dw.c_run = cache->c_run;
   dw.tail_k = cache->tail_k;
   dw.tail_v = cache->tail_v;
   dw.tail_g = cache->tail_g;
@@ -422,6 +425,7 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
   cw.pos = cache->pos;
   cw.s_bnd = cache->s_bnd;
   cw.s_run = cache->s_run;
+  cw.c_run = cache->c_run;
   cw.slots = cache->slots;
   launch_chain(d, cache->tail_k, W, U, gamma, cw, hdr, stream);
   stg.mark(1);
@@ -549,10 +553,12 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   iw.o = vo;
   iw.state_out = state_out;
   iw.cache_run = cache->s_run;
+  iw.cache_c_run = cache->c_run;
   iw.cache_slots = cache->slots;
   iw.slot_of_seq = slot_dev;
   iw.skip = rlen;  // the tail is already in the cache's running state
   iw.run_state = cache->s_run;
+  iw.run_c = cache->c_run;
   iw.run_slot = slot_dev;
   iw.part = 1;  // chunks that start from the cache's running state, before anything writes it
   launch_intra(d, vin, iw, hdr, st);
@@ -565,6 +571,7 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   cw.state_out = state_out;
   cw.cache_bnd = cache->s_bnd;
   cw.cache_run = cache->s_run;
+  cw.cache_c_run = cache->c_run;
   cw.cache_slots = cache->slots;
   cw.slot_of_seq = slot_dev;
   cw.bnd_in_place = true;

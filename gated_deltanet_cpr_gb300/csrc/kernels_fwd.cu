@@ -461,8 +461,10 @@ __global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* ke
         return;
       }
       rows_to_global<D>(Ss, w.cache_bnd + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)r0 * D);
-      if (rec.len % C == 0)
+      if (rec.len % C == 0) {  // an explicit running state: scale 1
         rows_to_global<D>(Ss, w.cache_run + ((int64_t)sl * dm.hv + h) * SZ + (int64_t)r0 * D);
+        if (t == 0 && blockIdx.z == 0) w.cache_c_run[(int64_t)sl * dm.hv + h] = 1.f;
+      }
     }
   } else {  // ---------------------------------------------------- decode resync
     const int sl = w.slot[n];
@@ -481,6 +483,7 @@ __global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* ke
                        (int64_t)sl * C, dm.hqk, hq, C, r0);
     rows_to_global<D>(Ss, w.s_bnd + so);
     rows_to_global<D>(Ss, w.s_run + so);
+    if (t == 0 && blockIdx.z == 0) w.c_run[(int64_t)sl * dm.hv + h] = 1.f;  // explicit: scale 1
   }
 }
 
@@ -641,6 +644,13 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
     // the first chunk starts from the running state
     const bool skip0 = w.seqs && w.bnd_skip && w.bnd_skip[n] > 0;
     if (w.seqs && nfull == 0 && skip0 && w.bnd_in_place && len % C != 0) continue;  // nothing to write
+    // a running state written below is explicit: its scale is 1
+    if (t == 0) {
+      if (!w.seqs)
+        w.c_run[(int64_t)sl * dm.hv + h] = 1.f;
+      else if (sl >= 0 && len % C == 0)
+        w.cache_c_run[(int64_t)sl * dm.hv + h] = 1.f;
+    }
     // outputs for the state after full chunk j (j = 0 .. nfull): rows of S^(j)
     auto write_state = [&](int j, const float* v, int c0) {
       if (w.seqs) {
@@ -1201,8 +1211,13 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const StateLayout<D> lay(t);
   float4 S[4][D / 32];
   const float* src = w.bnd + (c * dm.hv + h) * SZ;
+  float cs = 1.f;  // the state is cs * S (token_step)
   if constexpr (kSkip) {
-    if (first > 0) src = w.run_state + ((int64_t)w.run_slot[rec.seq] * dm.hv + h) * SZ;
+    if (first > 0) {
+      const int64_t rs = (int64_t)w.run_slot[rec.seq] * dm.hv + h;
+      src = w.run_state + rs * SZ;
+      cs = w.run_c[rs];
+    }
   }
   lay.load(S, src);
   __syncthreads();
@@ -1213,21 +1228,25 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const int orow = lay.out_row();
   const bool writer = lay.writes_out();
   float opart[4] = {0.f, 0.f, 0.f, 0.f};
+  float cprev = 1.f;  // the scale of the previous token's output partials
   // warps w and w + 4 share a scheduler: start the upper four about half a token later so
   // that one warp's reduction waits fall in the other's arithmetic
   if (t >= 128) __nanosleep(300);
   for (int tt = first; tt < len; ++tt) {
     float4 kk[D / 32];
-    float part[4], p[4];
+    float part[4], p[4], us[4];
     const float4 v4 = *reinterpret_cast<const float4*>(vs + tt * D + lay.row0);
-    ts_decay_dot<D>(S, ks + tt * D, as[tt], lay.b, kk, part);
-    const float o_prev = group_reduce4(opart, lay.b);
+    ts_decay<D>(S, cs, as[tt]);
+    ts_dot_k<D>(S, ks + tt * D, lay.b, kk, part);
+    const float o_prev = __fmul_rn(cprev, group_reduce4(opart, lay.b));
     if (writer && tt > first) vs[(tt - 1) * D + orow] = o_prev;
     group_allreduce4(part, p);
-    ts_update_dot<D>(S, kk, qs + tt * D, bs[tt], v4, p, lay.b, opart);
+    ts_scaled_u(p, v4, bs[tt], cs, us);
+    ts_update_dot<D>(S, kk, qs + tt * D, us, lay.b, opart);
+    cprev = cs;
   }
   if (first < len) {
-    const float o_last = group_reduce4(opart, lay.b);
+    const float o_last = __fmul_rn(cprev, group_reduce4(opart, lay.b));
     if (writer) vs[(len - 1) * D + orow] = o_last;
   }
   __syncthreads();
@@ -1245,10 +1264,13 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   // state decode continues from: the token recurrence through a final partial chunk
   const SeqRec sr = w.seqs[rc.seq];
   if (rc.jloc == sr.nchunks - 1 && (sr.len % dm.C) != 0) {
-    if (w.state_out) lay.store(S, w.state_out + ((int64_t)rc.seq * dm.hv + h) * SZ);
-    if (w.cache_run) {
+    if (w.state_out) lay.store_scaled(S, cs, w.state_out + ((int64_t)rc.seq * dm.hv + h) * SZ);
+    if (w.cache_run) {  // the scaled state and its scale, for decode to continue from
       const int sl = w.slot_of_seq ? w.slot_of_seq[rc.seq] : rc.seq;
-      if (sl >= 0 && sl < w.cache_slots) lay.store(S, w.cache_run + ((int64_t)sl * dm.hv + h) * SZ);
+      if (sl >= 0 && sl < w.cache_slots) {
+        lay.store(S, w.cache_run + ((int64_t)sl * dm.hv + h) * SZ);
+        if (t == 0) w.cache_c_run[(int64_t)sl * dm.hv + h] = cs;
+      }
     }
   }
 }
@@ -1304,15 +1326,18 @@ __global__ void __launch_bounds__(2 * D, 2) k_decode(Dims dm, TokenArrays in, De
   const StateLayout<D> lay(t);
   float4 S[4][D / 32];
   float* st = w.s_run + ((int64_t)sl * dm.hv + h) * SZ;
+  float* cst = w.c_run + (int64_t)sl * dm.hv + h;
   lay.load(S, st);
+  float cs = *cst;  // the running state is cs * S (token_step)
   const float a = expf(in.g[(int64_t)n * dm.hv + h]);
   const float b = in.beta[(int64_t)n * dm.hv + h];
   const Tin* vrow = vin + ((int64_t)n * dm.hv + h) * D;
   const float4 v4 = make_float4(to_f32(vrow[lay.row0]), to_f32(vrow[lay.row0 + 1]), to_f32(vrow[lay.row0 + 2]),
                                 to_f32(vrow[lay.row0 + 3]));
   __syncthreads();
-  const float o = token_step<D>(S, ks, qs, a, b, v4, lay.b);
+  const float o = token_step<D>(S, cs, ks, qs, a, b, v4, lay.b);
   lay.store(S, st);
+  if (t == 0) *cst = cs;
   const int ti = p % C;
   if (lay.writes_out()) store_out(static_cast<Tout*>(w.o) + ((int64_t)n * dm.hv + h) * D + lay.out_row(), o);
   if (t < D) static_cast<Tin*>(w.tail_v)[(((int64_t)sl * C + ti) * dm.hv + h) * D + t] = vrow[t];

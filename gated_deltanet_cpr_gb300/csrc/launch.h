@@ -68,6 +68,7 @@ struct ChainWork {
   float* state_out;
   float* cache_bnd;  // cache s_bnd (prefill with cache) or NULL
   float* cache_run;  // cache s_run (prefill with cache, written when L % C == 0) or NULL
+  float* cache_c_run;  // its scale c_run, set to 1 with it
   const int32_t* slot_of_seq;
   int cache_slots;
   // continued prefill: state_in is cache_bnd under the same slot map (S^(0) need not be
@@ -80,6 +81,7 @@ struct ChainWork {
   const int32_t* pos;
   float* s_bnd;
   float* s_run;
+  float* c_run;  // set to 1 with s_run
   int slots;
 };
 void launch_chain(const Dims& d, const void* keys, const float* W, const float* U,
@@ -93,7 +95,8 @@ struct IntraWork {
   const float* bnd;
   void* o;
   float* state_out;
-  float* cache_run;
+  float* cache_run;    // the running state after a final partial chunk, scaled: s_run and
+  float* cache_c_run;  // its scale c_run (the state is c_run * s_run)
   const int32_t* slot_of_seq;
   int cache_slots;
   // continued prefill: the first skip[seq] tokens of a sequence's first chunk are already in
@@ -101,6 +104,7 @@ struct IntraWork {
   // there, from token skip[seq]; NULL otherwise
   const int32_t* skip;
   const float* run_state;
+  const float* run_c;  // the scale of run_state
   const int32_t* run_slot;
   // with skip: 1 = only the chunks that start from run_state, 2 = all other chunks.  The
   // continued prefill launches part 1 before the boundary chain and part 2 after it, so
@@ -116,6 +120,7 @@ struct DecodeWork {
   const int32_t* slot;
   int slots;
   float* s_run;
+  float* c_run;
   void* tail_k;
   void* tail_v;
   float* tail_g;

@@ -110,7 +110,9 @@ typedef struct {
 /* Decode cache: everything needed to continue a sequence bit-exactly (also the full
  * checkpoint of a decoding sequence: copy it out and back to resume).  All arrays are
  * caller-owned device memory, indexed by slot.
- *   s_run     [slots, H_v, d_v, d_k] fp32   running state (recurrent since the last boundary)
+ *   s_run     [slots, H_v, d_v, d_k] fp32   running state (recurrent since the last boundary),
+ *                                             held scaled: the state is c_run * s_run
+ *   c_run     [slots, H_v] fp32           its scale (1 right after a boundary; see token_step)
  *   s_bnd     [slots, H_v, d_v, d_k] fp32   boundary state before the current chunk
  *   tail_k    [slots, C, H_qk, d_k]  in_dtype  keys of the current, unfinished chunk
  *   tail_v    [slots, C, H_v,  d_v]  in_dtype  values of the current chunk
@@ -119,6 +121,7 @@ typedef struct {
  *   pos       [slots] int32          tokens consumed so far by the slot's sequence          */
 typedef struct {
     float *s_run;
+    float *c_run;
     float *s_bnd;
     void *tail_k;
     void *tail_v;

@@ -99,7 +99,7 @@ def test_prefill_rejects_bad_arguments_before_any_launch(lib):
 
 def test_decode_and_bwd_argument_checks(lib):
     sh = shape(num_seqs=4, total_tokens=5)
-    cache = api.CacheStruct(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 4)
+    cache = api.CacheStruct(1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 1 << 20, 4)
     fake = 1 << 20
     rc = lib.gdn_cpr_decode_step(ctypes.byref(sh), fake, fake, fake, fake, fake, fake,
                                  ctypes.byref(cache), fake, fake, 1 << 30, None)

@@ -117,8 +117,8 @@ def test_decode_equals_prefill(gdn, L0, M, C):
         od = gdn.decode_step(st["q"], st["k"], st["v"], st["g"], st["beta"], slots[1:], cache,
                              out_dtype=torch.float32)
         assert torch.equal(od[0], o_full[tok[0]])
-    assert torch.equal(cache.s_run[3], s_full[0])
-    assert torch.equal(cache.s_run[1], s_full[1])
+    assert torch.equal(cache.running_state(3), s_full[0])
+    assert torch.equal(cache.running_state(1), s_full[1])
 
 
 def test_decode_checkpoint_resume(gdn):
@@ -144,7 +144,7 @@ def test_decode_checkpoint_resume(gdn):
         od = gdn.decode_step(st["q"], st["k"], st["v"], st["g"], st["beta"], slot, cache,
                              out_dtype=torch.float32)
         assert torch.equal(od[0], o_full[i])
-    assert torch.equal(cache.s_run[0], s_full[0])
+    assert torch.equal(cache.running_state(0), s_full[0])
 
 
 def test_device_errors_are_reported_not_faulted(gdn):
@@ -193,4 +193,4 @@ def test_decode_equals_prefill_tensor_core_boundary(gdn, L0, M):
                              out_dtype=torch.float32)
         for s in range(2):
             assert torch.equal(od[s], o_full[tok[s]]), (i, s)
-    assert torch.equal(cache.s_run[1], s_full[0])
+    assert torch.equal(cache.running_state(1), s_full[0])

@@ -44,6 +44,7 @@ def cut(seqs, a, b):
 
 def same_cache(cache_a, slot_a, cache_b, slot_b, pos, C):
     assert torch.equal(cache_a.s_run[slot_a], cache_b.s_run[slot_b])
+    assert torch.equal(cache_a.c_run[slot_a], cache_b.c_run[slot_b])
     assert torch.equal(cache_a.s_bnd[slot_a], cache_b.s_bnd[slot_b])
     assert int(cache_a.pos[slot_a]) == int(cache_b.pos[slot_b]) == pos
     r = pos % C

@@ -82,5 +82,5 @@ def test_decode_workload_equals_prefill(gdn):
         od = gdn.decode_step(st["q"], st["k"], st["v"], st["g"], st["beta"], slots, cache,
                              out_dtype=torch.bfloat16)
         assert torch.equal(od, o_full.index_select(0, tok)), i
-    assert torch.equal(cache.s_run[slots.long()], s_full)
+    assert torch.equal(cache.running_state(slots.long()), s_full)
     assert torch.equal(cache.pos.cpu(), torch.full((N,), L0 + M, dtype=torch.int32))

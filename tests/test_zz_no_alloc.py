@@ -65,7 +65,7 @@ def test_noalloc_refuses_requests_beyond_its_scratch(gdn):
     need = gdn.workspace_bytes(shape, gdn.MODE_DECODE)
     assert need > gdn.NOALLOC_SCRATCH_BYTES
     fake = 1 << 20  # never dereferenced: the size check comes first and nothing is queued
-    cache = gdn.CacheStruct(fake, fake, fake, fake, fake, fake, fake, 64)
+    cache = gdn.CacheStruct(fake, fake, fake, fake, fake, fake, fake, fake, 64)
     rc = lib.gdn_cpr_decode_step_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, fake,
                                          ctypes.byref(cache), fake, None)
     assert rc == 4  # GDN_ERR_WORKSPACE
