@@ -182,7 +182,8 @@ __device__ __forceinline__ void group_allreduce4(const float (&x)[4], float (&to
 // runs on a scaled copy: the state is S = c S~ (c the product of the decays since S~ was
 // last made equal to S), so the decay is one scalar product instead of a pass over the state:
 //     c <- c a;   p = c (S~ k);   u = beta (v - p);   S~ <- S~ + (u / c) k^T;   o = c (S~ q)
-// (u / c as u * rcp(c), rcp correctly rounded).  Whenever c leaves [2^-64, 2^64] the state is
+// with u / c = beta (v / c - S~ k) formed as fma(beta rcp(c), v, -(beta (S~ k))), rcp the
+// hardware reciprocal approximation.  Whenever c leaves [2^-64, 2^64] the state is
 // made explicit first (S~ <- c S~, c <- 1), so S~ stays within 2^64 of S and no scale under-
 // or overflows; c is the same in every lane, so the choice is warp-uniform.  Each row's dot:
 // per lane one float2 partial over the lane's columns in the order (j, pair): .x takes
@@ -232,13 +233,20 @@ __device__ __forceinline__ void ts_dot_k(const float4 (&S)[4][D / 32], const flo
     part[r] = __fadd_rn(pr.x, pr.y);
   }
 }
-// us_r = u_r / c for the lane's rows from the reduced S~ k (p4, all four rows): u = beta (v - c p)
+// hardware reciprocal approximation (one MUFU instruction; deterministic, c is normal here)
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// us_r = u_r / c for the lane's rows from the reduced S~ k (p4, all four rows), as
+// us = beta (v / c - p) = fma(beta rcp(c), v, -(beta p))
 __device__ __forceinline__ void ts_scaled_u(const float (&p4)[4], float4 v4, float beta, float c,
                                             float (&us)[4]) {
-  const float ic = __frcp_rn(c);
+  const float bic = __fmul_rn(beta, rcp_approx(c));
   const float v[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
-  for (int r = 0; r < 4; ++r) us[r] = __fmul_rn(__fmul_rn(beta, __fsub_rn(v[r], __fmul_rn(c, p4[r]))), ic);
+  for (int r = 0; r < 4; ++r) us[r] = __fmaf_rn(bic, v[r], -__fmul_rn(beta, p4[r]));
 }
 template <int D>
 __device__ __forceinline__ void ts_update_dot(float4 (&S)[4][D / 32], const float4 (&kk)[D / 32],

@@ -128,8 +128,8 @@ std::string policy_text(const gdn_cpr_shape* s) {
            "contraction=none (explicit round-to-nearest fma/mul/add)\n"
            "exp=expf\n"
            "token_step=4 state rows x d/8 columns per lane (columns 32j+4b..+3), 8 lanes per row group; "
-           "state held as c*S~: c*=a; if c outside [2^-64,2^64] then S~*=c, c=1; p=c*(S~.k); u=beta*(v-p); "
-           "S~+=(u*rcp(c)) k^T; o=c*(S~.q); running state out = c*S~ elementwise; "
+           "state held as c*S~: c*=a; if c outside [2^-64,2^64] then S~*=c, c=1; "
+           "S~+=fma(beta*rcp.approx(c), v, -(beta*(S~.k))) k^T; o=c*(S~.q); running state out = c*S~ elementwise; "
            "each dot: per lane and row one float2 partial (x: columns 4b, 4b+2; y: 4b+1, 4b+3; ascending j), x+y, "
            "then across the 8 lanes the tree ((l0+l4)+(l2+l6))+((l1+l5)+(l3+l7))\n"
            "cumsum_g=sequential fp32, ascending token\n"
