@@ -48,11 +48,11 @@ SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
 # reported only while the kernel's source (its function text plus common.cuh) hashes to the
 # value it had when the counters were taken; after any change it is null until recaptured.
 NCU_TRAFFIC = {
-    # 202,417,152 + 21,302,272 B for one 4096-token sequence x 32 value heads
-    "k_intra": {"src_sha": "0e9b2b896cd17890", "bytes_per_unit": (202417152 + 21302272) / (4096 * 32),
+    # 202,411,008 + 21,403,392 B for one 4096-token sequence x 32 value heads
+    "k_intra": {"src_sha": "74d8c0ca878a95b7", "bytes_per_unit": (202411008 + 21403392) / (4096 * 32),
                 "unit": "token-head"},
-    # 541,309,184 + 482,726,912 B for the full 256-slot x 32-head launch (one-pass capture)
-    "k_decode": {"src_sha": "074ccdf2bcef8277", "bytes_per_unit": (541309184 + 482726912) / (256 * 32),
+    # 541,314,304 + 482,651,648 B for the full 256-slot x 32-head launch (one-pass capture)
+    "k_decode": {"src_sha": "e875afd522d68d5e", "bytes_per_unit": (541314304 + 482651648) / (256 * 32),
                  "unit": "slot-head"},
 }
 KERNEL_TEXT = {  # file, first line of the kernel, first line after it
