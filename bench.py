@@ -28,6 +28,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -133,7 +134,7 @@ class ClockSampler:
     def __init__(self, bus_id: str | None):
         self.bus_id = (bus_id or "").lower()
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"gdn_cpr_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:

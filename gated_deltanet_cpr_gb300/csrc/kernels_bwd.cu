@@ -1872,7 +1872,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const int half = warp >> 2;
   const int helper = half * 64 + ((warp & 3) - 2) * 32 + lane;  // 0..127 on warps 2, 3, 6, 7
   const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-  // arena: round 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U hi/lo @64/@80; then Pm hi/lo
+  // arena: products 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U hi/lo @64/@80; then Pm hi/lo
   // @32/@40, Pm^T @48/@56, K^T @64, Q^T @80; then T^T @0/@8, dU^T @16/@32, dW^T @48/@64
   {
     float g0 = 0.f, b0 = 0.f;
@@ -1962,7 +1962,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       pending = true;
     }
   };
-  // ---- round 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64
+  // ---- products 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64
   if (t == 0) {
     mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C), 3);
     mma_terms(tb + 64, sa, sa, sa + 16 * KB, sa + 16 * KB, D, idesc_bf16(128, C), 1);
@@ -2002,7 +2002,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   }
   fence_before_sync();
   __syncthreads();
-  // ---- round 2: dQ = Pm K -> TMEM 0, dK1 = Pm^T Q -> TMEM 128
+  // ---- products 2: dQ = Pm K -> TMEM 0, dK1 = Pm^T Q -> TMEM 128
   if (ok) {
     tc::transpose_image(ar + 48 * KB, ar + 32 * KB, C, C);  // Pm^T hi
     tc::transpose_image(ar + 56 * KB, ar + 40 * KB, C, C);  // Pm^T lo
@@ -2014,8 +2014,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     });
     if (ok) wait_mma();
   }
-  // round 3 and 4 operands T^T, dU^T, dW^T: ready-made images (the prep and big-products
-  // kernels wrote them), one bulk copy each into the dead round-1/2 operands
+  // products 3 and 4: operands T^T, dU^T, dW^T: ready-made images (the prep and big-products
+  // kernels wrote them), one bulk copy each into the dead operands of products 1 and 2
   if (ok && t == 0) {
     mbar_expect_tx(&bar[1], 2 * C * C * 2 + 4 * IMG);
     bulk_g2s(ar, a.b.T + ch * C * C, 2 * C * C * 2, &bar[1]);
@@ -2077,7 +2077,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       }
     }
   }
-  // ---- round 3: X = T^T dU -> TMEM 0
+  // ---- products 3: X = T^T dU -> TMEM 0
   if (ok) {
     issue(true, [&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 16 * KB, sa + 32 * KB, C, idesc_bf16(128, D), 3); });
     if (ok) wait_mma();
@@ -2120,7 +2120,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     }
     dba[half * C + i] = pba;
   }
-  // ---- round 4: Y = T^T dW -> TMEM 0 (operands already in place; the K rows copy lands first)
+  // ---- products 4: Y = T^T dW -> TMEM 0 (operands already in place; the K rows copy lands first)
   if (ok) {
     issue(true, [&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 48 * KB, sa + 64 * KB, C, idesc_bf16(128, D), 3); });
     if (ok) wait_mma();
@@ -2214,8 +2214,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   const bool rowlane = (warp & 3) < 2;
   const int row = (warp & 3) * 32 + lane;
   const int half = warp >> 2;
-  // arena: round A W hi/lo @0/@16, Y hi|lo @32, K rows @64; round B Ut hi/lo @0/@16,
-  // X hi|lo @32, K^T @80; round C dAm hi/lo @0/@8, dAm^T hi/lo @16/@24
+  // arena: products A W hi/lo @0/@16, Y hi|lo @32, K rows @64; products B Ut hi/lo @0/@16,
+  // X hi|lo @32, K^T @80; products C dAm hi/lo @0/@8, dAm^T hi/lo @16/@24
   if (t == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -2279,7 +2279,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
       pending = true;
     }
   };
-  // ---- round A: dA = Y W^T -> TMEM 0, K K^T -> TMEM 64
+  // ---- products A: dA = Y W^T -> TMEM 0, K K^T -> TMEM 64
   issue(true, [&] {
     mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa, sa + 16 * KB, D, idesc_bf16(128, C), 3);
     mma_terms(tb + 64, sa + 64 * KB, sa + 64 * KB, sa + 64 * KB, sa + 64 * KB, D, idesc_bf16(128, C), 1);
@@ -2292,7 +2292,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   }
   decay_table_lower(gtab, Gs);  // while the products run
   if (ok) wait_mma();
-  // ---- round B: dA += X Ut^T
+  // ---- products B: dA += X Ut^T
   if (ok) {
     if (t == 0) {
       mbar_expect_tx(&bar[1], 2 * IMG);
@@ -2343,7 +2343,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   }
   fence_before_sync();
   __syncthreads();
-  // ---- round C: dK2 = dAm K + dAm^T K -> TMEM 0
+  // ---- products C: dK2 = dAm K + dAm^T K -> TMEM 0
   if (ok) {
     transpose_image(ar + 16 * KB, ar, C, C);
     transpose_image(ar + 24 * KB, ar + 8 * KB, C, C);
