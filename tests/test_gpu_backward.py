@@ -95,17 +95,18 @@ def test_deterministic(gdn):
 def test_full_size_trainer_sampled(gdn):
     """The trainer workload (8 packed sequences, lengths U[512, 8192], 16/32 heads, d = 128,
     C = 64, bf16) in the benchmark's launch configuration; the oracle recomputes a seeded
-    sample of (sequence, key head) groups of the shortest sequence."""
+    sample of (sequence, key head) groups of the shortest and of the longest sequence (the
+    longest reverse chain)."""
     w = synth.workloads()["trainer"]
     x = synth.make_inputs(w.lengths, w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0, dout=True)
     gr = gpu_grads(gdn, x, w.chunk)
     for name in NAMES:
         assert torch.isfinite(gr[name]).all(), name
     cu = x["cu_seqlens"].tolist()
-    s = int(np.argmin(w.lengths))
-    a, b = cu[s], cu[s + 1]
     grp = w.h_v // w.h_qk
-    for hq in (0, 11):
+    for s, hq in ((int(np.argmin(w.lengths)), 0), (int(np.argmin(w.lengths)), 11),
+                  (int(np.argmax(w.lengths)), 6)):
+        a, b = cu[s], cu[s + 1]
         hs = slice(hq * grp, (hq + 1) * grp)
         sub = {n: x[n][a:b, hq:hq + 1] for n in ("q", "k")}
         sub.update({n: x[n][a:b, hs] for n in ("v", "g", "beta", "dout")})

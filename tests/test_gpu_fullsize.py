@@ -2,7 +2,8 @@
 
 - Long context: 64 sequences with lengths log-uniform in [128, 32768] (about 3.8e5 tokens),
   16/32 heads, d = 128, C = 64, bf16, prefilled in batches of 1, 7 and 64 with the packing
-  order shuffled (seed 1): every sequence's o and final state are bit-identical.
+  order shuffled (seed 1): every sequence's o and final state are bit-identical, and the
+  longest sequence matches the fp64 oracle on sampled heads.
 - Decode: 256 sequences prefilled with 2048 tokens, then 128 decode steps with a
   resynchronisation every 64 tokens: every decode output and the final running states
   equal a single prefill of all 2176 tokens, bit for bit.
@@ -14,6 +15,7 @@ import pytest
 import torch
 
 from gated_deltanet_cpr_gb300 import synth
+from helpers import oracle_pairs, rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +61,17 @@ def test_long_context_batch_invariance(gdn):
             assert torch.equal(o_b[i], ref_o[i]), (batch, i)
             assert torch.equal(s_b[i], ref_s[i]), (batch, i)
     assert all(torch.isfinite(ref_o[i].float()).all() for i in range(len(seqs)))
+    # the longest sequence (511 chained chunk steps) against the fp64 oracle on sampled
+    # heads, from an fp32-output run whose RNE is the batched bf16 output
+    i = int(np.argmax(w.lengths))
+    x, cu = pack(seqs, [i])
+    o32, st32 = gdn.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], cu.cuda(), chunk=64,
+                            cu_seqlens_host=cu, out_dtype=torch.float32)
+    assert torch.equal(o32.to(torch.bfloat16), ref_o[i])
+    assert torch.equal(st32[0], ref_s[i])
+    for (_, h), (o_ref, st_ref, _) in oracle_pairs(seqs[i], [(0, 5), (0, 30)]).items():
+        assert rel_err(o32[:, h], o_ref) <= 2e-3, h
+        assert rel_err(st32[0, h], st_ref) <= 2e-3, h
 
 
 def test_decode_workload_equals_prefill(gdn):

@@ -69,3 +69,25 @@ def test_noalloc_refuses_requests_beyond_its_scratch(gdn):
     rc = lib.gdn_cpr_decode_step_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake, fake,
                                          ctypes.byref(cache), fake, None)
     assert rc == 4  # GDN_ERR_WORKSPACE
+
+
+def test_noalloc_device_errors_are_readable(gdn):
+    """A slot index outside the cache is a device-side error; the no-alloc call records it in
+    its built-in array's error word, which gdn_cpr_noalloc_device_error reads back.  The next
+    valid call clears it."""
+    hqk, hv, d, C = 2, 4, 64, 16
+    cache = make_cache(gdn, 2, hqk, hv, d, C, [3, 20], seed=7)
+    x = synth.make_inputs([2], hqk, hv, d, dtype=synth.BF16, seed=8)
+    t = {n: x[n].cuda() for n in ("q", "k", "v", "g", "beta")}
+    before = {n: getattr(cache, n).clone() for n in gdn.Cache.TENSORS}
+    bad = torch.tensor([0, 5], dtype=torch.int32, device="cuda")
+    gdn.decode_step_noalloc(t["q"], t["k"], t["v"], t["g"], t["beta"], bad, cache)
+    assert gdn.noalloc_device_error() == 2  # GDN_DEVERR_SLOT
+    # the valid slot 0 still stepped; slot 1 was not touched
+    assert cache.pos.tolist() == [4, 20]
+    for name in ("s_run", "s_bnd", "tail_g"):
+        assert torch.equal(getattr(cache, name)[1], before[name][1]), name
+    good = torch.tensor([1, 0], dtype=torch.int32, device="cuda")
+    gdn.decode_step_noalloc(t["q"], t["k"], t["v"], t["g"], t["beta"], good, cache)
+    assert gdn.noalloc_device_error() == 0
+    assert cache.pos.tolist() == [5, 21]
