@@ -27,7 +27,8 @@ DEVERR = {0: "none", 1: "cu_seqlens mismatch", 2: "slot out of range", 3: "negat
 EXPORTS = ("gdn_cpr_version", "gdn_cpr_status_string", "gdn_cpr_workspace_size",
            "gdn_cpr_prefill", "gdn_cpr_decode_step", "gdn_cpr_fwd", "gdn_cpr_bwd",
            "gdn_cpr_get_device_error", "gdn_cpr_set_profile", "gdn_cpr_decode_step_noalloc",
-           "gdn_cpr_policy_digest", "gdn_cpr_prefill_continue")
+           "gdn_cpr_policy_digest", "gdn_cpr_prefill_continue", "gdn_cpr_running_state",
+           "gdn_cpr_noalloc_device_error", "gdn_cpr_test_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -87,6 +88,12 @@ def load():
             lib.gdn_cpr_policy_digest.restype = I
             lib.gdn_cpr_prefill_continue.argtypes = [P] * 14 + [S, P]
             lib.gdn_cpr_prefill_continue.restype = I
+            lib.gdn_cpr_running_state.argtypes = [P, P, P, ctypes.c_int32, P, P]
+            lib.gdn_cpr_running_state.restype = I
+            lib.gdn_cpr_noalloc_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
+            lib.gdn_cpr_noalloc_device_error.restype = I
+            lib.gdn_cpr_test_wait_timeout.argtypes = [ctypes.c_int32]
+            lib.gdn_cpr_test_wait_timeout.restype = None
             for fn in ("gdn_cpr_workspace_size", "gdn_cpr_prefill", "gdn_cpr_decode_step",
                        "gdn_cpr_fwd", "gdn_cpr_bwd", "gdn_cpr_get_device_error"):
                 getattr(lib, fn).restype = I
@@ -184,10 +191,26 @@ class Cache:
     TENSORS = ("s_run", "c_run", "s_bnd", "tail_k", "tail_v", "tail_g", "tail_beta", "pos")
 
     def running_state(self, slots=None):
-        """The running state c_run * s_run (fp32, [slots, H_v, d, d]; all slots if None), as
-        the kernels form state_out: one round-to-nearest product per element."""
-        s, c = (self.s_run, self.c_run) if slots is None else (self.s_run[slots], self.c_run[slots])
-        return s * c[..., None, None]
+        """gdn_cpr_running_state: the explicit running state c_run * s_run of the given
+        slots (a sequence or device tensor of indices; all slots if None), fp32
+        [n, H_v, d, d], formed by the library as the kernels form state_out."""
+        lib = load()
+        dev = self.s_run.device
+        if slots is None:
+            sel, n = None, self.slots
+        else:
+            sel = torch.as_tensor(slots, device=dev).to(torch.int32).reshape(-1).contiguous()
+            n = sel.numel()
+        out = torch.empty((n, self.h_v, self.d, self.d), dtype=torch.float32, device=dev)
+        shape = make_shape(n, n, self.h_qk, self.h_v, self.d, self.chunk, self.dtype, torch.float32)
+        cs = self.struct()
+        _check("gdn_cpr_running_state",
+               lib.gdn_cpr_running_state(ctypes.byref(shape), ctypes.byref(cs), _p(sel), n, _p(out),
+                                         _stream(dev)))
+        if slots is not None and not isinstance(slots, torch.Tensor) and \
+                not isinstance(slots, (list, tuple)):
+            return out[0]  # a single slot index
+        return out
 
     def struct(self) -> CacheStruct:
         return CacheStruct(*(_p(getattr(self, n)) for n in self.TENSORS), self.slots)
@@ -350,6 +373,24 @@ def bwd(q, k, v, g, beta, cu_seqlens, saved_bnd, dout, chunk=64, state_in=None,
                          ws.numel(), _stream(dev))
     _check("gdn_cpr_bwd", rc)
     return out
+
+
+def noalloc_device_error(device=None) -> int:
+    """gdn_cpr_noalloc_device_error: synchronise the current stream and return the device
+    error code of the last no-alloc decode step on the current device."""
+    lib = load()
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    code = ctypes.c_int32(0)
+    rc = lib.gdn_cpr_noalloc_device_error(_stream(dev), ctypes.byref(code))
+    if rc not in (0, 5):
+        raise GdnError("gdn_cpr_noalloc_device_error", rc)
+    return int(code.value)
+
+
+def test_wait_timeout(calls: int) -> None:
+    """gdn_cpr_test_wait_timeout (test hook): the next `calls` tensor-core prefills from
+    this thread make one boundary-chain CTA's bounded wait run out."""
+    load().gdn_cpr_test_wait_timeout(int(calls))
 
 
 def device_error(ws: torch.Tensor) -> int:

@@ -130,6 +130,9 @@ gdn_status check_cache(const gdn_cpr_cache* c) {
 }
 
 thread_local gdn_cpr_profile* t_profile = nullptr;
+// gdn_cpr_test_wait_timeout: calls left that make the tensor-core chain's first CTA give up
+// a wait that nothing completes
+thread_local int32_t t_wait_fault = 0;
 
 // Stage marker of the profiling hook: event `stage` after the stage's kernels, and the
 // count of kernels those stages launched.
@@ -267,6 +270,10 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
     cw.cache_c_run = cache->c_run;
     cw.cache_slots = cache->slots;
     cw.slot_of_seq = slot_of_seq;
+  }
+  if (t_wait_fault > 0 && boundary_on_tensor_cores(d)) {
+    cw.fault_wait = 1;
+    --t_wait_fault;
   }
   launch_chain(d, k, W, U, gamma, cw, hdr, st);
   stg.mark(1);
@@ -589,6 +596,22 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   stg.mark(2);
   return finish(st);
 }
+
+gdn_status gdn_cpr_running_state(const gdn_cpr_shape* shape, const gdn_cpr_cache* cache,
+                                 const int32_t* slots_dev, int32_t n, float* out, gdn_stream_t stream) {
+  gdn_status rc = check_shape(shape);
+  if (rc != GDN_OK) return rc;
+  rc = check_cache(cache);
+  if (rc != GDN_OK) return rc;
+  if (n < 0 || (!slots_dev && n > cache->slots)) return GDN_ERR_INVALID_ARG;
+  if (n == 0) return GDN_OK;
+  if (!ok_ptr(out, 16) || (slots_dev && !aligned(slots_dev, 4))) return GDN_ERR_INVALID_ARG;
+  launch_running_state(shape->d_k, shape->h_v, cache->s_run, cache->c_run, cache->slots, slots_dev, n, out,
+                       static_cast<cudaStream_t>(stream));
+  return finish(static_cast<cudaStream_t>(stream));
+}
+
+void gdn_cpr_test_wait_timeout(int32_t calls) { t_wait_fault = calls > 0 ? calls : 0; }
 
 gdn_status gdn_cpr_get_device_error(const void* ws, gdn_stream_t stream, int32_t* code) {
   if (!ws || !code) return GDN_ERR_INVALID_ARG;

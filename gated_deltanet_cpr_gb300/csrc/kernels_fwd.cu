@@ -608,6 +608,8 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
   int pending = -1;             // stage buffer with a copy in flight
   bool mma_pending = false;
   bool ok = true;
+  if (w.fault_wait && blockIdx.x == 0)  // test hook: phase 0 of bars[0] never completes here
+    ok = __syncthreads_and(t == 0 ? mbar_wait(&bars[0], 0u, 1024u) : true) != 0;
 
   for (int li = 0; li < count && ok; ++li) {
     const int64_t wi = s_list[li];
@@ -1368,6 +1370,37 @@ __global__ void k_advance(int N, const int32_t* __restrict__ slot, int slots, in
 
 void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st) {
   k_advance<<<(N + 255) / 256, 256, 0, st>>>(N, slot, slots, pos);
+}
+
+// The explicit running state of selected cache slots: out[i] = c_run[s] * s_run[s] for
+// s = sel[i] (sel NULL: s = i), one round-to-nearest product per element, exactly as the
+// kernels form state_out from a scaled state (StateLayout::store_scaled).  A slot outside
+// [0, slots) gives an all-NaN block, so a bad index cannot pass for a state.
+__global__ void __launch_bounds__(256) k_running_state(int D, int hv, const float* __restrict__ s_run,
+                                                       const float* __restrict__ c_run, int slots,
+                                                       const int32_t* __restrict__ sel,
+                                                       float* __restrict__ out) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int s = sel ? sel[i] : i;
+  const int64_t SZ = (int64_t)D * D;
+  float4* dst = reinterpret_cast<float4*>(out + ((int64_t)i * hv + h) * SZ);
+  if (s < 0 || s >= slots) {
+    const float nan = __int_as_float(0x7fffffff);
+    for (int64_t e = threadIdx.x; e < SZ / 4; e += blockDim.x) dst[e] = make_float4(nan, nan, nan, nan);
+    return;
+  }
+  const float c = c_run[(int64_t)s * hv + h];
+  const float4* src = reinterpret_cast<const float4*>(s_run + ((int64_t)s * hv + h) * SZ);
+  for (int64_t e = threadIdx.x; e < SZ / 4; e += blockDim.x) {
+    const float4 x = src[e];
+    dst[e] = make_float4(__fmul_rn(c, x.x), __fmul_rn(c, x.y), __fmul_rn(c, x.z), __fmul_rn(c, x.w));
+  }
+}
+
+void launch_running_state(int D, int hv, const float* s_run, const float* c_run, int slots,
+                          const int32_t* sel, int n, float* out, cudaStream_t st) {
+  if (n <= 0) return;
+  k_running_state<<<dim3((unsigned)n, (unsigned)hv), 256, 0, st>>>(D, hv, s_run, c_run, slots, sel, out);
 }
 
 template <typename Tin>

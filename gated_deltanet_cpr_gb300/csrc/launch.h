@@ -83,6 +83,10 @@ struct ChainWork {
   float* s_run;
   float* c_run;  // set to 1 with s_run
   int slots;
+  // test hook (tensor-core chain only): nonzero makes CTA 0 wait, before any copy or MMA, on
+  // a barrier phase that nothing completes, with a short poll limit, so that the bounded
+  // wait runs out and the CTA records GDN_DEVERR_TIMEOUT, frees its tensor memory and exits
+  int fault_wait;
 };
 void launch_chain(const Dims& d, const void* keys, const float* W, const float* U,
                   const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st);
@@ -133,6 +137,11 @@ void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, Ws
 
 // pos[slot[n]] += 1 for every valid n (last kernel of a decode step).
 void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st);
+
+// out[i] = c_run[s] * s_run[s] (s = sel[i], or i if sel is NULL) for i < n, all heads:
+// the explicit running state of cache slots.
+void launch_running_state(int D, int hv, const float* s_run, const float* c_run, int slots,
+                          const int32_t* sel, int n, float* out, cudaStream_t st);
 
 // Prefill with a cache: copy the last L % C tokens of every sequence to its slot's tail and
 // set pos = L, plus pos_base[n] when given (a continued prefill's chunk-aligned start); with

@@ -79,24 +79,31 @@ def cu_seqlens_of(lengths) -> torch.Tensor:
 
 def make_inputs(lengths, h_qk: int, h_v: int, d_k: int, d_v: int | None = None,
                 dtype: str = BF16, seed: int = 0, decay: str = "default",
-                state_in: bool = False, dout: bool = False, out_dtype: str | None = None):
-    """Draw one packed batch on the CPU.  Returns a dict of CPU tensors:
-    q, k [T,Hqk,dk] and v [T,Hv,dv] in `dtype`; g, beta [T,Hv] fp32; cu_seqlens [N+1] int32;
-    state_in [N,Hv,dv,dk] fp32 (N(0,1)/sqrt(dk)) or None; dout [T,Hv,dv] or None."""
+                state_in: bool = False, dout: bool = False, out_dtype: str | None = None,
+                device=None):
+    """Draw one packed batch.  Returns a dict of tensors on `device` (default: the CPU):
+    q, k [T,Hqk,dk] and v [T,Hv,dv] in `dtype`; g, beta [T,Hv] fp32; cu_seqlens [N+1] int32
+    (always on the CPU); state_in [N,Hv,dv,dk] fp32 (N(0,1)/sqrt(dk)) or None; dout [T,Hv,dv]
+    or None.  A device generator draws the same distributions but not the same values as
+    the CPU one (used where the CPU would take too long to draw a large workload)."""
     d_v = d_k if d_v is None else d_v
     T = int(sum(lengths))
-    gen = torch.Generator().manual_seed(seed)
+    dev = torch.device("cpu") if device is None else torch.device(device)
+    gen = torch.Generator(device=dev).manual_seed(seed)
     td = _TORCH_DTYPE[dtype]
 
+    def randn(shape):
+        return torch.randn(shape, generator=gen, dtype=torch.float32, device=dev)
+
     def unit_rows(shape):
-        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        x = randn(shape)
         return (x / x.norm(dim=-1, keepdim=True).clamp_min(1e-12)).to(td)
 
     q = unit_rows((T, h_qk, d_k))
     k = unit_rows((T, h_qk, d_k))
-    v = torch.randn((T, h_v, d_v), generator=gen, dtype=torch.float32).to(td)
-    beta = torch.sigmoid(torch.randn((T, h_v), generator=gen, dtype=torch.float32))
-    z = torch.randn((T, h_v), generator=gen, dtype=torch.float32)
+    v = randn((T, h_v, d_v)).to(td)
+    beta = torch.sigmoid(randn((T, h_v)))
+    z = randn((T, h_v))
     if decay == "default":
         g = -torch.nn.functional.softplus(z)
     elif decay == "slow":
@@ -109,11 +116,10 @@ def make_inputs(lengths, h_qk: int, h_v: int, d_k: int, d_v: int | None = None,
                cu_seqlens=cu_seqlens_of(lengths), state_in=None, dout=None)
     n = len(lengths)
     if state_in:
-        out["state_in"] = torch.randn((n, h_v, d_v, d_k), generator=gen,
-                                      dtype=torch.float32) / math.sqrt(d_k)
+        out["state_in"] = randn((n, h_v, d_v, d_k)) / math.sqrt(d_k)
     if dout:
         od = _TORCH_DTYPE[out_dtype or dtype]
-        out["dout"] = torch.randn((T, h_v, d_v), generator=gen, dtype=torch.float32).to(od)
+        out["dout"] = randn((T, h_v, d_v)).to(od)
     return out
 
 

@@ -41,7 +41,8 @@
  *
  * Ownership: the caller allocates and owns every buffer, including the workspace.  The
  * library allocates no device memory and keeps no mutable global state apart from the
- * optional per-thread profiling hook (gdn_cpr_set_profile).
+ * optional per-thread hooks (gdn_cpr_set_profile, gdn_cpr_test_wait_timeout) and the
+ * built-in scratch array of gdn_cpr_decode_step_noalloc.
  *
  * Execution: every call only queues work on `stream` and returns; nothing synchronises
  * except gdn_cpr_get_device_error.  Inputs must stay valid until the stream reaches the
@@ -233,6 +234,23 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape *shape, const void *q, c
                                     const gdn_cpr_cache *cache, void *o, float *state_out, void *ws,
                                     size_t ws_bytes, gdn_stream_t stream);
 
+/* The explicit running state of decode cache slots (the state decode continues from, as
+ * gdn_cpr_prefill returns it in state_out): out[i] = c_run[s] * s_run[s] for s = slots_dev[i],
+ * every value head, one round-to-nearest fp32 product per element -- the same product the
+ * kernels use when a scaled running state leaves them as state_out, so a cache read back
+ * here equals the state_out of the same sequence bit for bit.  (IsoExec page, section
+ * "Chunkwise-Parallel Recurrent (CPR) Gated DeltaNet": decode continues the recurrence on a
+ * running state; the cache holds it as c_run * s_run, see gdn_cpr_cache.)
+ *   shape      only h_v, d_k = d_v (and the configuration checks) are used
+ *   cache      the decode cache to read (device)
+ *   slots_dev  [n] int32 device slot indices, or NULL for slots 0 .. n-1 (n <= cache->slots)
+ *   out        [n, H_v, d_v, d_k] fp32 device, 16-byte aligned
+ * Queues one kernel on `stream`.  A slot index outside [0, cache->slots) on the device gives
+ * an all-NaN block for that entry.  Argument errors are returned and nothing is queued. */
+gdn_status gdn_cpr_running_state(const gdn_cpr_shape *shape, const gdn_cpr_cache *cache,
+                                 const int32_t *slots_dev, int32_t n, float *out,
+                                 gdn_stream_t stream);
+
 /* Numerical-policy identity (IsoExec pages, section on the structure of the execution
  * contract, item "Identities": SHA-256 digests by which trainer and rollout engine check
  * that they run the same verified numerical policy).  Writes into digest[32] the SHA-256
@@ -285,7 +303,11 @@ void gdn_cpr_set_profile(gdn_cpr_profile *profile);
  *   d = 128, C = 64 (e.g. 31 slots x 32 heads); larger requests return GDN_ERR_WORKSPACE
  *   and queue nothing.
  *   The first call on a device looks up the array's device address (with that device
- *   current); make that first call before capturing any stream into a CUDA graph.
+ *   current); make that first call before capturing any stream into a CUDA graph.  The
+ *   address is kept with the identity of the context it belongs to; after a device reset
+ *   the next call looks it up again (and is again a first call in that sense).
+ *   Device-side errors of these calls (a slot out of range, ...) are recorded in the
+ *   array's own error word: read them with gdn_cpr_noalloc_device_error.
  *   Every call on a device shares the array and leaves its contents behind; the step
  *   clears what must start at zero.  Calls that overlap on the GPU (other streams, other
  *   threads, concurrent graph replays) race on the array: serialise them.               */
@@ -293,6 +315,23 @@ gdn_status gdn_cpr_decode_step_noalloc(const gdn_cpr_shape *shape, const void *q
                                        const void *v, const float *g, const float *beta,
                                        const int32_t *slot, const gdn_cpr_cache *cache, void *o,
                                        gdn_stream_t stream);
+
+/* Synchronises `stream`, then reads the device error word of the built-in scratch array
+ * of the current device, which gdn_cpr_decode_step_noalloc uses as its workspace: the
+ * device-side error (slot out of range, negative position, a bounded wait that gave up) of
+ * the last no-alloc call on this device, as gdn_cpr_get_device_error reports it for a
+ * caller-provided workspace.  Returns GDN_OK when the word is clear, GDN_ERR_DEVICE with
+ * *code set when it is not, GDN_ERR_CUDA if the sync or read fails.  Allocates nothing.  */
+gdn_status gdn_cpr_noalloc_device_error(gdn_stream_t stream, int32_t *code);
+
+/* Test hook of the failure path (per calling thread; off by default): the next `calls`
+ * prefill or trainer-forward calls from this thread whose boundary pass runs on tensor
+ * cores make one CTA of the boundary chain wait, before it issues any copy or MMA, on a
+ * barrier phase that nothing completes.  Its bounded wait (a short poll limit here) gives
+ * up, the CTA records GDN_DEVERR_TIMEOUT in the workspace's error word, frees its tensor
+ * memory and exits, so gdn_cpr_get_device_error reports the timeout and the context stays
+ * usable.  The outputs of such a call are not valid.  calls <= 0 switches it off.       */
+void gdn_cpr_test_wait_timeout(int32_t calls);
 
 /* Synchronises `stream`, then reads the device error word of `ws` (the workspace of the
  * last call queued with it) into *code (a gdn_device_error).  Returns GDN_OK when the
