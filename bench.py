@@ -260,37 +260,63 @@ def threads_available():
 
 # ---------------------------------------------------------------- reference ----
 def run_reference(args):
+    """The fp64 CPU oracle as it stands, timed on the host cores.  Each step is a bounded
+    sample of the benchmark step with the same mix of work (1/16 of every part): oracle
+    forward over 1024 tokens (the prefill part), forward over the next 16 tokens (the decode
+    part: the oracle's token recurrence is the decode step), forward and backward over 1024
+    tokens (the trainer part), all 32 value heads of sequence 0.  value = the sample's tokens
+    / its measured wall time; ms_per_step = that measured time (nothing is extrapolated)."""
     rank, _, world = dist_env()
     if rank != 0:
         return 0
+    import oracle
     from gated_deltanet_cpr_gb300 import synth
+    from gated_deltanet_cpr_gb300.synth import as_f64 as f
 
     w = synth.workloads()[WORKLOAD]
-    x = synth.make_inputs(w.lengths[:1], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0, dout=True)
+    tk = step_tokens(w)
+    frac = 16
+    n_pre, n_dec, n_trn = tk["prefill"] // frac, tk["decode"] // frac, tk["trainer"] // frac
+    x = synth.make_inputs([n_pre + n_dec], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0, dout=True)
+    a = {n: f(x[n]) for n in ("q", "k", "v", "g", "beta", "dout")}
     threads = threads_available()
-    fwd_tok, bwd_tok = 512, 256
-    times = []
-    for i in range(args.warmup + args.steps):
-        rf, rb, dt = oracle_rates(x, w.h_v, fwd_tok, bwd_tok, threads)
-        if i >= args.warmup:
-            times.append((rf, rb, dt))
-    rf = statistics.median(t[0] for t in times)
-    rb = statistics.median(t[1] for t in times)
-    est = oracle_step_estimate(w, rf, rb)
-    tk = sum(step_tokens(w).values())
-    value = tk / est
-    sample = (f"per step: oracle fwd on {fwd_tok} tokens x {w.h_v} heads and oracle bwd on "
-              f"{bwd_tok} tokens x {w.h_v} heads of sequence 0; whole-step time extrapolated "
-              f"linearly in token-heads")
+
+    def sample_step():
+        t0 = time.perf_counter()
+        oracle.fwd(*(a[n][:n_pre] for n in ("q", "k", "v", "g", "beta")), [0, n_pre], n_threads=threads)
+        oracle.fwd(*(a[n][n_pre:] for n in ("q", "k", "v", "g", "beta")), [0, n_dec], n_threads=threads)
+        oracle.fwd(*(a[n][:n_trn] for n in ("q", "k", "v", "g", "beta")), [0, n_trn], n_threads=threads)
+        oracle.bwd(*(a[n][:n_trn] for n in ("q", "k", "v", "g", "beta")), [0, n_trn], a["dout"][:n_trn],
+                   n_threads=threads)
+        return time.perf_counter() - t0
+
+    for _ in range(args.warmup):
+        sample_step()
+    times = [sample_step() for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    sample_tokens = n_pre + n_dec + n_trn
+    value = sample_tokens / sec
+    sample = (f"each step 1/{frac} of the benchmark step with its mix of work, all {w.h_v} value heads "
+              f"of sequence 0: oracle fwd over {n_pre} tokens (prefill part), fwd over {n_dec} "
+              f"tokens (decode part), fwd + bwd over {n_trn} tokens (trainer part); "
+              f"{sample_tokens} tokens per step, measured wall time")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": est * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": w.name, "tokens_per_step": tk},
+            "data": "synthetic (seeded N(0,1) inputs, q/k L2-normalised, beta=sigmoid, g=-softplus)",
+            "config": step_config(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def step_config(w):
+    tokens = step_tokens(w)
+    return {"workload": w.name, "tokens_per_step": sum(tokens.values()), "stages": tokens,
+            "l2": "inputs larger than L2 (step working set > 2 GB of HBM traffic)",
+            "bwd_included": True}
 
 
 # ---------------------------------------------------------------- CUDA arm ----
@@ -363,7 +389,7 @@ def run_cuda(args):
         if have_bwd:
             grads = api.bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], saved,
                             t["dout"], chunk=C, cu_seqlens_host=cu_host, ws=ws_bwd,
-                            want_dstate_in=False)
+                            want_dstate_in=True)
 
     # the 64 decode steps as one CUDA graph (fixed pointers, device-side resync decision)
     prefill_call()
@@ -462,44 +488,53 @@ def run_cuda(args):
         bwd_bytes = (sum(t[n].numel() * t[n].element_size() for n in ("q", "k", "v", "g", "beta", "dout"))
                      + saved.numel() * saved.element_size()
                      + sum(grads[n].numel() * grads[n].element_size()
-                           for n in ("dq", "dk", "dv", "dg", "dbeta")))
+                           for n in ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")))
         bwd_gbs = bwd_bytes / (bwd_ms * 1e-3) / 1e9
         bwd_roof = {"bound": "hbm", "achieved": bwd_gbs, "peak": hbm_peak, "unit": "GB/s",
                     "frac": bwd_gbs / hbm_peak, "algorithmic_bytes": bwd_bytes, "ms": bwd_ms,
                     "note": "all backward kernels; the chunk-form workspace round trips are not "
                             "algorithmic bytes"}
 
-    # 256-slot decode (the decode workload's state shape), graph-replayed and per kernel
+    # the decode workload: 256 sequences prefilled with 2048 tokens, then 128 graph-replayed
+    # decode steps, per kernel and per step
     dec = bench_decode_big(api, synth, torch, dev, w, P, seed)
+    # the trainer workload (8 packed varlen sequences) and the long-context prefill
+    trainer_cfg = bench_trainer_workload(api, synth, torch, dev, seed)
+    longctx_cfg = bench_longctx_workload(api, synth, torch, dev, seed)
 
     # prefill continued from a cache: chunked prefill and multi-token decode
     cont = bench_continue(api, synth, torch, dev, w, seed, stage_ms["prefill"])
 
     # end to end through host buffers: H2D inputs each step, D2H results each step
     e2e = bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call,
-                    t, dq_in, o_pre, o_dec, lambda: grads, step_tok, world)
+                    t, dq_in, o_pre, o_dec, lambda: grads, step_tok, world, ms)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) inputs, q/k L2-normalised, beta=sigmoid, g=-softplus)",
-            "config": {"workload": w.name, "tokens_per_step": step_tok, "stages": tokens,
-                       "l2": "inputs larger than L2 (step working set > 2 GB of HBM traffic)",
-                       "bwd_included": have_bwd},
+            "config": dict(step_config(w), bwd_included=have_bwd),
             "stage_ms": stage_ms, "kernel_ms": kern, "roofline": roofline,
             "boundary_roofline": boundary, "bwd_roofline": bwd_roof, "decode": dec,
-            "continue": cont, "e2e": e2e,
+            "continue": cont, "trainer_workload": trainer_cfg, "longctx_workload": longctx_cfg,
+            "e2e": e2e,
             "gpu_launches": launches, "clocks": clk.summary(),
             "peaks_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else peak_kind}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = threads_available()
         rf, rb, dt = oracle_rates_all(x, hv, threads)
         est = oracle_step_estimate(w, rf, rb)
+        rf1, rb1, dt1 = oracle_rates(x, hv, 512, 256, 1)
+        est1 = oracle_step_estimate(w, rf1, rb1)
         line["cpu_baseline"] = {
             "value": step_tok / est, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": (f"oracle fwd and oracle bwd over the whole prefill workload "
                        f"({T} tokens x {hv} heads each, {dt:.1f} s wall on {threads} threads); "
-                       f"step time = those rates applied to the step's token-heads")}
+                       f"step time = those rates applied to the step's token-heads"),
+            "single_core": {"value": step_tok / est1, "unit": UNIT, "cores": 1,
+                            "sample": (f"oracle fwd over 512 tokens and bwd over 256 tokens x {hv} "
+                                       f"heads of sequence 0 on one thread ({dt1:.1f} s wall); step "
+                                       f"time = those rates applied to the step's token-heads")}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -510,25 +545,29 @@ def run_cuda(args):
 
 
 def bench_decode_big(api, synth, torch, dev, w, P, seed):
-    """256 slots x 32 heads of 128x128 fp32 states, positions at 2048 (so 64 steps contain one
-    resync at step 63), random resident states and tails."""
-    N, C, d, hqk, hv = DECODE_SLOTS_BIG, w.chunk, w.d, w.h_qk, w.h_v
+    """The decode workload: 256 sequences, each first prefilled with 2048 tokens (through
+    gdn_cpr_prefill with a cache, 64 sequences per call), then 128 decode steps of one token
+    per sequence with a resynchronisation every 64 tokens (the steps whose token is the
+    sequence's 2112th and 2176th), replayed from one CUDA graph.  Inputs are drawn on the
+    device from seeded generators (the same distributions as the other workloads)."""
+    wd = synth.workloads()["decode"]
+    N, L0, M = len(wd.lengths), wd.lengths[0], wd.decode_steps
+    C, d, hqk, hv = wd.chunk, wd.d, wd.h_qk, wd.h_v
     cache = api.Cache(N, hqk, hv, d, C, dtype=torch.bfloat16, device=dev)
-    gen = torch.Generator(device=dev).manual_seed(seed + 11)
-    cache.s_run.normal_(generator=gen).mul_(0.05)
-    cache.s_bnd.copy_(cache.s_run)
-    cache.tail_k.normal_(generator=gen).mul_(0.09)
-    cache.tail_v.normal_(generator=gen)
-    cache.tail_g.uniform_(-1.5, -0.1, generator=gen)
-    cache.tail_beta.uniform_(0.2, 0.8, generator=gen)
-    cache.pos.fill_(2048)
-    xd = synth.make_inputs([DECODE_STEPS * N], hqk, hv, d, dtype=w.dtype, seed=seed + 13)
-    din = {n: xd[n].view(DECODE_STEPS, N, *xd[n].shape[1:]).contiguous().to(dev)
-           for n in ("q", "k", "v", "g", "beta")}
+    B = 64
+    for b0 in range(0, N, B):
+        xp = synth.make_inputs([L0] * B, hqk, hv, d, dtype=wd.dtype, seed=seed + 31 + b0, device=dev)
+        sl = torch.arange(b0, b0 + B, dtype=torch.int32, device=dev)
+        api.prefill(xp["q"], xp["k"], xp["v"], xp["g"], xp["beta"], xp["cu_seqlens"].to(dev), chunk=C,
+                    cache=cache, slot_of_seq=sl, cu_seqlens_host=xp["cu_seqlens"], want_state=False)
+        torch.cuda.synchronize(dev)
+        del xp
+    xd = synth.make_inputs([M * N], hqk, hv, d, dtype=wd.dtype, seed=seed + 13, device=dev)
+    din = {n: xd[n].view(M, N, *xd[n].shape[1:]) for n in ("q", "k", "v", "g", "beta")}
     slots = torch.arange(N, dtype=torch.int32, device=dev)
     shp = api.make_shape(N, N, hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
     ws = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_DECODE), dev)
-    o = torch.empty((DECODE_STEPS, N, hv, d), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((M, N, hv, d), dtype=torch.bfloat16, device=dev)
     saved = {n: getattr(cache, n).clone() for n in api.Cache.TENSORS}
 
     def call(i):
@@ -542,24 +581,26 @@ def bench_decode_big(api, synth, torch, dev, w, P, seed):
     # per-kernel times from the library's stage events (direct launches)
     reset()
     per = []
-    for i in range(DECODE_STEPS):
+    for i in range(M):
         prof = api.Profiler(5)
         with prof:
             call(i)
         per.append(prof)
     torch.cuda.synchronize(dev)
     stages = [p.stage_ms() for p in per]
-    normal = [s for i, s in enumerate(stages) if i != DECODE_STEPS - 1]
+    resync_steps = [i for i in range(M) if (L0 + i + 1) % C == 0]
+    normal = [s for i, s in enumerate(stages) if i not in resync_steps]
     step_k3 = statistics.median(s[0] for s in normal)
-    resync_step_ms = sum(stages[-1])
-    # graph replay of all 64 steps
+    step_p50 = statistics.median(sum(s) for s in normal)
+    resync_ms = [sum(stages[i]) for i in resync_steps]
+    # graph replay of all 128 steps
     reset()
     call(0)
     reset()
     torch.cuda.synchronize(dev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for i in range(DECODE_STEPS):
+        for i in range(M):
             call(i)
     times = []
     for _ in range(3):
@@ -571,23 +612,91 @@ def bench_decode_big(api, synth, torch, dev, w, P, seed):
         e1.record()
         torch.cuda.synchronize(dev)
         times.append(e0.elapsed_time(e1))
-    us_per_step = statistics.median(times) * 1e3 / DECODE_STEPS
+    us_per_step = statistics.median(times) * 1e3 / M
     # K3 algorithmic bytes: state read+write, q,k per qk head, v, o, tail appends, g, beta
     bpe = 2
     bytes_k3 = (N * hv * d * d * 4 * 2 + N * hqk * d * bpe * 2 + N * hv * d * bpe
                 + N * hv * d * bpe + N * hqk * d * bpe + N * hv * d * bpe + N * hv * 4 * 4)
     hbm = float(P.get("hbm_gbs", PEAK_FALLBACK["hbm_gbs"]))
     ach = bytes_k3 / (step_k3 * 1e-3) / 1e9
-    return {"slots": N, "heads": hv, "d": d, "steps": DECODE_STEPS,
-            "us_per_step_mean": us_per_step, "us_token_step_kernel_median": step_k3 * 1e3,
-            "us_resync_step": resync_step_ms * 1e3,
+    return {"workload": wd.name, "slots": N, "heads": hv, "d": d, "steps": M,
+            "start_state": f"a {L0}-token prefill of every sequence into the cache",
+            "us_per_step_mean": us_per_step, "us_per_step_p50": step_p50 * 1e3,
+            "us_token_step_kernel_median": step_k3 * 1e3,
+            "resync_steps": len(resync_steps),
+            "us_resync_step": statistics.mean(resync_ms) * 1e3,
             "us_resync_stages": dict(zip(("token_step", "prepass", "chain", "advance"),
-                                         (x * 1e3 for x in stages[-1]))),
+                                         (x * 1e3 for x in stages[resync_steps[0]]))),
             "tokens_per_s": N / (us_per_step * 1e-6),
             "roofline": {"bound": "hbm", "kernel": "k_decode (token step)", "achieved": ach,
                          "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
                          "traffic": ncu_traffic("k_decode", N * hv),
                          "algorithmic_bytes_per_launch": bytes_k3}}
+
+
+def bench_trainer_workload(api, synth, torch, dev, seed):
+    """Trainer forward + backward on the trainer workload (8 packed sequences, lengths
+    uniform in [512, 8192]), all six gradients including state_in's.  Inputs drawn on the
+    device from seeded generators."""
+    wt = synth.workloads()["trainer"]
+    C, d, hqk, hv = wt.chunk, wt.d, wt.h_qk, wt.h_v
+    x = synth.make_inputs(wt.lengths, hqk, hv, d, dtype=wt.dtype, seed=seed + 41, dout=True, device=dev)
+    cu_host = x["cu_seqlens"]
+    cu = cu_host.to(dev)
+    N, T = len(wt.lengths), wt.total_tokens
+    shp = api.make_shape(N, T, hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
+    ws_f = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_FWD, cu_host), dev)
+    ws_b = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_BWD, cu_host), dev)
+    nch = sum((L + C - 1) // C for L in wt.lengths)
+    saved = torch.empty((nch, hv, d, d), dtype=torch.float32, device=dev)
+    o = torch.empty((T, hv, d), dtype=torch.bfloat16, device=dev)
+    st = torch.empty((N, hv, d, d), dtype=torch.float32, device=dev)
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    res = []
+    for rep in range(6):
+        e = [mk(), mk(), mk()]
+        e[0].record()
+        api.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, chunk=C, cu_seqlens_host=cu_host,
+                ws=ws_f, o=o, state_out=st, saved_bnd=saved)
+        e[1].record()
+        api.bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, saved, x["dout"], chunk=C,
+                cu_seqlens_host=cu_host, ws=ws_b, want_dstate_in=True)
+        e[2].record()
+        torch.cuda.synchronize(dev)
+        if rep >= 2:
+            res.append((e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2])))
+    f_ms = statistics.median(r[0] for r in res)
+    b_ms = statistics.median(r[1] for r in res)
+    return {"workload": wt.name, "lengths": wt.lengths, "tokens": T, "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "ms": f_ms + b_ms, "tokens_per_s": T / ((f_ms + b_ms) * 1e-3)}
+
+
+def bench_longctx_workload(api, synth, torch, dev, seed):
+    """Rollout prefill of the long-context workload: 64 sequences with lengths log-uniform in
+    [128, 32768] in one call.  Inputs drawn on the device from seeded generators."""
+    wl = synth.workloads()["longctx"]
+    C, d, hqk, hv = wl.chunk, wl.d, wl.h_qk, wl.h_v
+    x = synth.make_inputs(wl.lengths, hqk, hv, d, dtype=wl.dtype, seed=seed + 51, device=dev)
+    cu_host = x["cu_seqlens"]
+    cu = cu_host.to(dev)
+    N, T = len(wl.lengths), wl.total_tokens
+    shp = api.make_shape(N, T, hqk, hv, d, C, torch.bfloat16, torch.bfloat16)
+    ws = api.alloc_workspace(api.workspace_bytes(shp, api.MODE_PREFILL, cu_host), dev)
+    o = torch.empty((T, hv, d), dtype=torch.bfloat16, device=dev)
+    st = torch.empty((N, hv, d, d), dtype=torch.float32, device=dev)
+    times = []
+    for rep in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, chunk=C, cu_seqlens_host=cu_host,
+                    ws=ws, o=o, state_out=st)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        if rep >= 1:
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    return {"workload": wl.name, "sequences": N, "tokens": T, "longest": max(wl.lengths), "ms": ms,
+            "tokens_per_s": T / (ms * 1e-3)}
 
 
 def bench_continue(api, synth, torch, dev, w, seed, prefill_ms):
@@ -677,7 +786,7 @@ def bench_continue(api, synth, torch, dev, w, seed, prefill_ms):
 
 
 def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call, t, dq_in,
-              o_pre, o_dec, get_grads, step_tok, world):
+              o_pre, o_dec, get_grads, step_tok, world, compute_ms):
     """Same step through the public API with host buffers: every step copies its inputs from
     pinned host memory and reads its results back, pipelined as a serving or training loop
     would run it: step i + 1's inputs go up on one copy stream (into the second of two input
@@ -696,7 +805,7 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_c
         if part == "dec":
             return {"o_decode": o_dec}
         gr = get_grads()
-        return {} if gr is None else {n: gr[n] for n in ("dq", "dk", "dv", "dg", "dbeta")}
+        return {} if gr is None else {n: gr[n] for n in ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")}
 
     comp = torch.cuda.current_stream(dev)
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -771,8 +880,27 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_c
             if not torch.equal(res_host[n], v.cpu()):
                 raise RuntimeError(f"pipelined end-to-end read-back of {n} differs from the device result")
     ms = reduce_max(e0.elapsed_time(e1) / args.steps, world)
+    # the machine's host<->device copy rates (pinned host memory, one 256 MiB copy each way,
+    # best of 3) and what the step's copies cost at those rates if nothing overlapped
+    hb = torch.empty(1 << 28, dtype=torch.uint8, pin_memory=True)
+    db = torch.empty(1 << 28, dtype=torch.uint8, device=dev)
+    bw = {}
+    for name, dst, src in (("h2d", db, hb), ("d2h", hb, db)):
+        best = None
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(comp)
+            dst.copy_(src, non_blocking=True)
+            c1.record(comp)
+            torch.cuda.synchronize(dev)
+            best = c0.elapsed_time(c1) if best is None else min(best, c0.elapsed_time(c1))
+        bw[name] = hb.numel() / (best * 1e-3) / 1e9
+    del hb, db
+    copy_ms = (h2d / bw["h2d"] + d2h / bw["d2h"]) / 1e6
     return {"value": world * step_tok / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "h2d_gbs": bw["h2d"], "d2h_gbs": bw["d2h"], "copy_ms_per_step_serial": copy_ms,
+            "exposed_ms_per_step": ms - compute_ms,
             "pipelined": "inputs of step i+1 uploaded during step i (two input buffers); "
                          "results read back on a second copy stream as each part finishes"}
 
