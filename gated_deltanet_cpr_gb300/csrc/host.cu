@@ -2,6 +2,7 @@
 // launch sequence of every mode.  The host never touches tensor data; it only reads the
 // caller's host copy of cu_seqlens to size grids and the workspace.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -181,15 +182,39 @@ gdn_status virtual_cu(const gdn_cpr_shape* s, const int32_t* cu, const int32_t* 
   return GDN_OK;
 }
 
+// NVTX range over one entry point (host-side markers for profilers such as Nsight; no
+// effect without a tool attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+// Stage boundaries of one call: the profiling hook's events and kernel counts, and a nested
+// NVTX range per stage (names[i] is stage i + 1; NULL-terminated).
 struct Stages {
   cudaStream_t st;
+  const char* const* names;
   int next = 0;
-  explicit Stages(cudaStream_t s) : st(s) {
+  bool open = false;
+  Stages(cudaStream_t s, const char* const* stage_names) : st(s), names(stage_names) {
     if (t_profile) t_profile->stages = 0;
     mark(0);
   }
+  ~Stages() {
+    if (open) nvtxRangePop();
+  }
+  Stages(const Stages&) = delete;
+  Stages& operator=(const Stages&) = delete;
   void mark(int kernels) {
-    if (!t_profile) return;
+    if (open) nvtxRangePop();
+    open = names && names[next] != nullptr;
+    if (open) nvtxRangePushA(names[next]);
+    if (!t_profile) {
+      ++next;
+      return;
+    }
     t_profile->kernels += kernels;
     if (next < t_profile->n_events && next < 16 && t_profile->events[next]) {
       cudaEventRecord(static_cast<cudaEvent_t>(t_profile->events[next]), st);
@@ -198,6 +223,16 @@ struct Stages {
     ++next;
   }
 };
+
+const char* const kFwdStages[] = {"work list", "boundary pre-pass", "boundary chain", "intra-chunk recurrence",
+                                  "cache tail", nullptr};
+const char* const kDecodeStages[] = {"decode token step", "resync pre-pass", "resync chain", "position advance",
+                                     nullptr};
+const char* const kBwdStages[] = {"work list", "backward prep", "reverse boundary chain", "backward products",
+                                  "backward gradients", "grouped-head sum", nullptr};
+const char* const kContStages[] = {"continue: positions, work list, gather", "boundary pre-pass",
+                                   "intra-chunk (cached part) + boundary chain", "intra-chunk recurrence",
+                                   "cache tail + scatter", nullptr};
 
 void stage_mark(void* ctx, int kernels) { static_cast<Stages*>(ctx)->mark(kernels); }
 
@@ -248,7 +283,7 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   TokenArrays in{q, k, v, g, beta};
 
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
-  Stages stg(st);
+  Stages stg(st, kFwdStages);
   launch_worklist(cu_dev, N, (int)T, d.C, n_chunks, hash, chunks, seqs, hdr, st);
   stg.mark(1);
 
@@ -360,6 +395,7 @@ gdn_status gdn_cpr_prefill(const gdn_cpr_shape* shape, const void* q, const void
                            const int32_t* cu_seqlens_host, void* o, float* state_out,
                            const gdn_cpr_cache* cache_out, const int32_t* slot_of_seq, void* ws,
                            size_t ws_bytes, gdn_stream_t stream) {
+  NvtxRange nvtx("gdn_cpr_prefill");
   return run_forward(shape, q, k, v, g, beta, state_in, cu_seqlens_dev, cu_seqlens_host, o,
                      state_out, cache_out, slot_of_seq, nullptr, ws, ws_bytes, stream);
 }
@@ -369,6 +405,7 @@ gdn_status gdn_cpr_fwd(const gdn_cpr_shape* shape, const void* q, const void* k,
                        const int32_t* cu_seqlens_dev, const int32_t* cu_seqlens_host, void* o,
                        float* state_out, float* saved_bnd, void* ws, size_t ws_bytes,
                        gdn_stream_t stream) {
+  NvtxRange nvtx("gdn_cpr_fwd");
   if (!saved_bnd) return GDN_ERR_INVALID_ARG;
   return run_forward(shape, q, k, v, g, beta, state_in, cu_seqlens_dev, cu_seqlens_host, o,
                      state_out, nullptr, nullptr, saved_bnd, ws, ws_bytes, stream);
@@ -378,6 +415,7 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
                                const void* v, const float* g, const float* beta,
                                const int32_t* slot, const gdn_cpr_cache* cache, void* o,
                                void* ws, size_t ws_bytes, gdn_stream_t stream) {
+  NvtxRange nvtx("gdn_cpr_decode_step");
   gdn_status rc = check_shape(shape);
   if (rc != GDN_OK) return rc;
   const int N = shape->num_seqs;
@@ -397,7 +435,7 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
   float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
   TokenArrays in{q, k, v, g, beta};
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
-  Stages stg(stream);
+  Stages stg(stream, kDecodeStages);
 
   DecodeWork dw{};
   dw.N = N;
@@ -448,6 +486,7 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k,
                        const float* saved_bnd, const void* dO, const float* dstate_out,
                        float* dq, float* dk, float* dv, float* dg, float* dbeta,
                        float* dstate_in, void* ws, size_t ws_bytes, gdn_stream_t stream) {
+  NvtxRange nvtx("gdn_cpr_bwd");
   (void)state_in;  // its contribution reaches the backward through saved_bnd (chunk 0)
   gdn_status rc = check_shape(shape);
   if (rc != GDN_OK) return rc;
@@ -474,7 +513,7 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k,
   SeqRec* seqs = reinterpret_cast<SeqRec*>(at(ws, L.seqs));
   TokenArrays in{q, k, v, g, beta};
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
-  Stages stg(stream);
+  Stages stg(stream, kBwdStages);
   launch_worklist(cu_seqlens_dev, N, (int)T, d.C, n_chunks, hash, chunks, seqs, hdr, stream);
   stg.mark(1);
   launch_bwd(d, in, dO, chunks, seqs, N, n_chunks, T, saved_bnd, dstate_out, dstate_in,
@@ -492,6 +531,7 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
                                     const int32_t* slot_dev, const int32_t* pos_host,
                                     const gdn_cpr_cache* cache, void* o, float* state_out, void* ws,
                                     size_t ws_bytes, gdn_stream_t stream) {
+  NvtxRange nvtx("gdn_cpr_prefill_continue");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   gdn_status rc = check_shape(shape);
   if (rc != GDN_OK) return rc;
@@ -540,7 +580,7 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
                   reinterpret_cast<const float*>(at(ws, L.beta))};
 
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
-  Stages stg(st);
+  Stages stg(st, kContStages);
   launch_continue_prep(cu_seqlens_dev, slot_dev, cache->pos, cache->slots, N, d.C, vcu, rlen, base, hdr, st);
   launch_worklist(vcu, N, (int)vT, d.C, vchunks, vhash, chunks, seqs, hdr, st);
   launch_continue_gather(d, in, cu_seqlens_dev, vcu, rlen, slot_dev, N, vT, *cache, vin, hdr, st);
@@ -599,6 +639,7 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
 
 gdn_status gdn_cpr_running_state(const gdn_cpr_shape* shape, const gdn_cpr_cache* cache,
                                  const int32_t* slots_dev, int32_t n, float* out, gdn_stream_t stream) {
+  NvtxRange nvtx("gdn_cpr_running_state");
   gdn_status rc = check_shape(shape);
   if (rc != GDN_OK) return rc;
   rc = check_cache(cache);
