@@ -14,14 +14,16 @@ import threading
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libgdn_cpr.so")
+# GDN_CPR_CHECKED=1 selects the bounds-checked debug build (build.build(checked=True))
+LIB_PATH = os.path.join(HERE, "libgdn_cpr_checked.so" if os.environ.get("GDN_CPR_CHECKED") == "1"
+                        else "libgdn_cpr.so")
 
 GDN_F32, GDN_BF16 = 0, 1
 MODE_PREFILL, MODE_DECODE, MODE_FWD, MODE_BWD, MODE_CONTINUE = 0, 1, 2, 3, 4
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "workspace missing, misaligned or too small", 5: "device-side error recorded"}
 DEVERR = {0: "none", 1: "cu_seqlens mismatch", 2: "slot out of range", 3: "negative position",
-          4: "bounded wait timed out"}
+          4: "bounded wait timed out", 5: "index range outside a buffer (bounds-checked build)"}
 
 # every function the header declares (checked by the CPU test suite)
 EXPORTS = ("gdn_cpr_version", "gdn_cpr_status_string", "gdn_cpr_workspace_size",

@@ -41,6 +41,24 @@ struct SeqRec {  // one sequence
 
 __device__ __forceinline__ void set_error(WsHeader* h, int code) { atomicCAS(&h->err, 0, code); }
 
+// Bounds-checked builds (compiled with -DGDN_CHECKED=1): every kernel checks the index range
+// of each work item it derives from device data (chunk and sequence records, slots, positions)
+// against the buffers it was given, and an item outside them records GDN_DEVERR_BOUNDS and is
+// skipped instead of touching memory.  In ordinary builds the check compiles to nothing.
+#ifndef GDN_CHECKED
+#define GDN_CHECKED 0
+#endif
+__device__ __forceinline__ bool in_bounds(WsHeader* h, bool ok) {
+#if GDN_CHECKED
+  if (!ok) set_error(h, GDN_DEVERR_BOUNDS);
+  return ok;
+#else
+  (void)h;
+  (void)ok;
+  return true;
+#endif
+}
+
 // ---------------------------------------------------------------- conversions ----
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }

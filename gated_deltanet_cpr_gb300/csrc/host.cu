@@ -280,7 +280,7 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   float* U = reinterpret_cast<float*>(at(ws, L.U));
   float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
   float* bnd = saved_bnd ? saved_bnd : reinterpret_cast<float*>(at(ws, L.bnd));
-  TokenArrays in{q, k, v, g, beta};
+  TokenArrays in{q, k, v, g, beta, T};
 
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(st, kFwdStages);
@@ -296,6 +296,8 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   ChainWork cw{};
   cw.seqs = seqs;
   cw.N = N;
+  cw.n_chunks = n_chunks;
+  cw.n_tokens = T;
   cw.state_in = state_in;
   cw.bnd = bnd;
   cw.state_out = state_out;
@@ -316,6 +318,7 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   IntraWork iw{};
   iw.chunks = chunks;
   iw.seqs = seqs;
+  iw.n_seqs = N;
   iw.n_chunks = n_chunks;
   iw.bnd = bnd;
   iw.o = o;
@@ -433,7 +436,7 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
   float* W = reinterpret_cast<float*>(at(ws, L.W));
   float* U = reinterpret_cast<float*>(at(ws, L.U));
   float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
-  TokenArrays in{q, k, v, g, beta};
+  TokenArrays in{q, k, v, g, beta, N};
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(stream, kDecodeStages);
 
@@ -453,7 +456,8 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
   stg.mark(1);
 
   // resynchronisation: the same boundary pre-pass and chain step as prefill, on the tail
-  TokenArrays tail{nullptr, cache->tail_k, cache->tail_v, cache->tail_g, cache->tail_beta};
+  const int64_t tail_rows = (int64_t)cache->slots * d.C;
+  TokenArrays tail{nullptr, cache->tail_k, cache->tail_v, cache->tail_g, cache->tail_beta, tail_rows};
   PrepWork pw{};
   pw.chunks = nullptr;
   pw.n_items = N;
@@ -472,6 +476,8 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
   cw.s_run = cache->s_run;
   cw.c_run = cache->c_run;
   cw.slots = cache->slots;
+  cw.n_chunks = N;
+  cw.n_tokens = tail_rows;
   launch_chain(d, cache->tail_k, W, U, gamma, cw, hdr, stream);
   stg.mark(1);
 
@@ -511,7 +517,7 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k,
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   ChunkRec* chunks = reinterpret_cast<ChunkRec*>(at(ws, L.chunks));
   SeqRec* seqs = reinterpret_cast<SeqRec*>(at(ws, L.seqs));
-  TokenArrays in{q, k, v, g, beta};
+  TokenArrays in{q, k, v, g, beta, T};
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(stream, kBwdStages);
   launch_worklist(cu_seqlens_dev, N, (int)T, d.C, n_chunks, hash, chunks, seqs, hdr, stream);
@@ -575,9 +581,9 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   int32_t* rlen = reinterpret_cast<int32_t*>(at(ws, L.rlen));
   int32_t* base = reinterpret_cast<int32_t*>(at(ws, L.base));
   void* vo = at(ws, L.o);
-  TokenArrays in{q, k, v, g, beta};
+  TokenArrays in{q, k, v, g, beta, T};
   TokenArrays vin{at(ws, L.q), at(ws, L.k), at(ws, L.v), reinterpret_cast<const float*>(at(ws, L.g)),
-                  reinterpret_cast<const float*>(at(ws, L.beta))};
+                  reinterpret_cast<const float*>(at(ws, L.beta)), vT};
 
   if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(st, kContStages);
@@ -595,6 +601,7 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   IntraWork iw{};
   iw.chunks = chunks;
   iw.seqs = seqs;
+  iw.n_seqs = N;
   iw.n_chunks = vchunks;
   iw.bnd = bnd;
   iw.o = vo;
@@ -612,6 +619,8 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   ChainWork cw{};
   cw.seqs = seqs;
   cw.N = N;
+  cw.n_chunks = vchunks;
+  cw.n_tokens = vT;
   cw.state_in = cache->s_bnd;
   cw.state_in_slot = slot_dev;
   cw.bnd = bnd;
@@ -632,7 +641,7 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
 
   launch_tail_fill(d, vin, seqs, N, slot_dev, cache->slots, cache->tail_k, cache->tail_v, cache->tail_g,
                    cache->tail_beta, cache->pos, base, rlen, hdr, st);
-  launch_continue_scatter(d, cu_seqlens_dev, vcu, rlen, N, T, vo, o, hdr, st);
+  launch_continue_scatter(d, cu_seqlens_dev, vcu, rlen, N, T, vT, vo, o, hdr, st);
   stg.mark(2);
   return finish(st);
 }

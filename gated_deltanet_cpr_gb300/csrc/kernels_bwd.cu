@@ -219,6 +219,8 @@ struct BwdArgs {
   BwdBufs b;
   float *dq, *dk, *dv, *dg, *dbeta;
   int64_t T;
+  int64_t n_chunks;  // chunk records (rows of saved_bnd and of the per-chunk workspace)
+  int N;             // sequences
   WsHeader* hdr;
 };
 
@@ -250,6 +252,8 @@ __global__ void __launch_bounds__(NT) k_bwd_prep(BwdArgs a) {
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = a.chunks[c];
+  if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
@@ -401,6 +405,9 @@ __global__ void __launch_bounds__(NT) k_bwd_chain(BwdArgs a) {
   const int n = blockIdx.x, h = blockIdx.y, r0 = blockIdx.z * R;
   const int hq = h / (dm.hv / dm.hqk);
   const SeqRec rec = a.seqs[n];
+  if (!in_bounds(a.hdr, rec.chunk0 >= 0 && (int64_t)rec.chunk0 + rec.nchunks <= a.n_chunks && rec.tok0 >= 0 &&
+                            (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int64_t SZ = (int64_t)D * D;
   const Tin* kin = static_cast<const Tin*>(a.in.k);
   for (int idx = t; idx < R * D; idx += NT) {
@@ -482,6 +489,8 @@ __global__ void __launch_bounds__(NT) k_bwd_big(BwdArgs a) {
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = a.chunks[c];
+  if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
@@ -580,6 +589,8 @@ __global__ void __launch_bounds__(NT) k_bwd_grad(BwdArgs a) {
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = a.chunks[c];
+  if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
@@ -833,6 +844,9 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   const int cs0 = half * (D / 2), us0 = half * (C / 2);
   const int n = blockIdx.x, h = blockIdx.y;
   const SeqRec rec = a.seqs[n];
+  if (!in_bounds(a.hdr, rec.chunk0 >= 0 && (int64_t)rec.chunk0 + rec.nchunks <= a.n_chunks && rec.tok0 >= 0 &&
+                            (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int64_t SZ = (int64_t)D * D;
   const int64_t IW = (int64_t)prep_w_floats(C, D);
   const int64_t srow = ((int64_t)n * dm.hv + h) * SZ + (int64_t)row * D;
@@ -1212,6 +1226,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y;
   const ChunkRec rec = a.chunks[c];
+  if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
@@ -1493,6 +1509,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = a.chunks[c];
+  if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
@@ -1856,6 +1874,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = a.chunks[c];
+  if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
@@ -2202,6 +2222,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   const int64_t c = blockIdx.x;
   const int h = blockIdx.y;
   const ChunkRec rec = a.chunks[c];
+  if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
+    return;
   const int n = rec.len;
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
@@ -2521,6 +2543,8 @@ void launch_bwd(const Dims& d, const TokenArrays& in, const void* dO, const Chun
   a.dg = dg;
   a.dbeta = dbeta;
   a.T = T;
+  a.n_chunks = n_chunks;
+  a.N = N;
   a.hdr = hdr;
   const size_t C = d.C, D = d.D, nch = (size_t)n_chunks * d.hv;
   float* p = per_chunk;

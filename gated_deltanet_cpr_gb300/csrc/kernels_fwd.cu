@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
     const ChunkRec rec = w.chunks[item];
     if (rec.len != C) return;  // only full chunks advance a boundary state
     tok0 = rec.tok0;
+    if (!in_bounds(hdr, tok0 >= 0 && tok0 + C <= in.n_tokens)) return;
   } else {  // decode: the slot's tail, when this token completes it
     const int sl = w.slot[item];
     if (sl < 0 || sl >= w.slots) {
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(Dims dm, TokenArrays in, 
     }
     if ((p + 1) % C != 0) return;
     tok0 = (int64_t)sl * C;
+    if (!in_bounds(hdr, tok0 + C <= in.n_tokens)) return;
   }
   const Tin* kin = static_cast<const Tin*>(in.k);
   const Tin* vin = static_cast<const Tin*>(in.v);
@@ -431,6 +433,9 @@ __global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* ke
     if (!hdr->valid) return;
     const SeqRec rec = w.seqs[n];
     const int nfull = rec.len / C;
+    if (!in_bounds(hdr, rec.chunk0 >= 0 && (int64_t)rec.chunk0 + rec.nchunks <= w.n_chunks && rec.tok0 >= 0 &&
+                            (int64_t)rec.tok0 + rec.len <= w.n_tokens))
+      return;
     // S <- state_in rows (or 0)
     for (int idx = t; idx < R * (D / 4); idx += kChainThreads) {
       const int i = idx / (D / 4), c4 = idx % (D / 4);
@@ -471,6 +476,7 @@ __global__ void __launch_bounds__(kChainThreads) k_chain(Dims dm, const void* ke
     if (sl < 0 || sl >= w.slots) return;  // reported by k_decode
     const int p = w.pos[sl];
     if (p < 0 || (p + 1) % C != 0) return;
+    if (!in_bounds(hdr, ((int64_t)sl + 1) * C <= w.n_tokens && n < w.n_chunks)) return;
     const int64_t so = ((int64_t)sl * dm.hv + h) * SZ + (int64_t)r0 * D;
     for (int idx = t; idx < R * (D / 4); idx += kChainThreads) {
       const int i = idx / (D / 4), c4 = idx % (D / 4);
@@ -624,6 +630,7 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       nchunks = rec.nchunks;
       len = rec.len;
       item0 = rec.chunk0;
+      if (!in_bounds(hdr, rec.chunk0 >= 0 && (int64_t)rec.chunk0 + rec.nchunks <= w.n_chunks)) continue;
       src = w.state_in ? w.state_in + ((int64_t)(w.state_in_slot ? w.state_in_slot[n] : n) * dm.hv + h) * SZ
                        : nullptr;
       if (w.cache_bnd) {
@@ -638,6 +645,7 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       if (sl < 0 || sl >= w.slots) continue;  // reported by the decode step kernel
       const int p = w.pos[sl];
       if (p < 0 || (p + 1) % C != 0) continue;
+      if (!in_bounds(hdr, n < w.n_chunks)) continue;
       nfull = 1;
       item0 = n;
       src = w.s_bnd + ((int64_t)sl * dm.hv + h) * SZ;
@@ -930,6 +938,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
           }
         }
       }
+      if (tok0 >= 0 && !in_bounds(hdr, tok0 + C <= in.n_tokens)) tok0 = -1;
       if (tok0 >= 0) {
         const int k = atomicAdd(&s_cnt, 1);
         s_list[k] = wi;
@@ -1183,6 +1192,9 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const int h = blockIdx.y;
   const int hq = h / (dm.hv / dm.hqk);
   const ChunkRec rec = w.chunks[c];
+  if (!in_bounds(hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= dm.C && (int64_t)rec.tok0 + rec.len <= in.n_tokens &&
+                          rec.seq >= 0 && rec.seq < w.n_seqs))
+    return;
   if constexpr (kSkip) {  // this launch's part of the chunks
     const bool from_run = rec.jloc == 0 && w.skip[rec.seq] > 0;
     if (from_run != (w.part == 1)) return;
@@ -1419,6 +1431,7 @@ __global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ 
   }
   const int C = dm.C, D = dm.D;
   const int nt = rec.len % C;
+  if (!in_bounds(hdr, rec.tok0 >= 0 && (int64_t)rec.tok0 + rec.len <= in.n_tokens)) return;
   // rows the slot's tail already holds (continued prefill whose chunk stays open)
   const int k0 = (keep_rows && rec.len < C) ? keep_rows[n] : 0;
   const int64_t base = (int64_t)rec.tok0 + rec.len - nt;
@@ -1644,6 +1657,7 @@ __global__ void k_continue_gather(Dims dm, TokenArrays in, const int32_t* __rest
     }
   } else {
     const int64_t src = (int64_t)cu[s] + (local - r);
+    if (!in_bounds(const_cast<WsHeader*>(hdr), src >= 0 && src < in.n_tokens)) return;
     copy16(qo, static_cast<const char*>(in.q) + src * nq, nq);
     copy16(ko, static_cast<const char*>(in.k) + src * nq, nq);
     copy16(vo, static_cast<const char*>(in.v) + src * nv, nv);
@@ -1656,13 +1670,14 @@ __global__ void k_continue_gather(Dims dm, TokenArrays in, const int32_t* __rest
 
 // One block per new token: its output row from the virtual sequence's output.
 __global__ void k_continue_scatter(const int32_t* __restrict__ cu, const int32_t* __restrict__ vcu,
-                                   const int32_t* __restrict__ rlen, int N, int64_t row_bytes,
+                                   const int32_t* __restrict__ rlen, int N, int64_t vT, int64_t row_bytes,
                                    const void* __restrict__ vo, void* __restrict__ o,
                                    const WsHeader* __restrict__ hdr) {
   if (!hdr->valid) return;
   const int64_t tk = blockIdx.x;
   const int s = seq_of(cu, N, tk);
   const int64_t vrow = (int64_t)vcu[s] + rlen[s] + (tk - cu[s]);
+  if (!in_bounds(const_cast<WsHeader*>(hdr), vrow >= 0 && vrow < vT)) return;
   copy16(static_cast<char*>(o) + tk * row_bytes, static_cast<const char*>(vo) + vrow * row_bytes, row_bytes);
 }
 
@@ -1681,9 +1696,9 @@ void launch_continue_gather(const Dims& d, const TokenArrays& in, const int32_t*
 }
 
 void launch_continue_scatter(const Dims& d, const int32_t* cu, const int32_t* vcu, const int32_t* rlen, int N,
-                             int64_t T, const void* vo, void* o, WsHeader* hdr, cudaStream_t st) {
+                             int64_t T, int64_t vT, const void* vo, void* o, WsHeader* hdr, cudaStream_t st) {
   if (T > 0)
-    k_continue_scatter<<<(unsigned)T, 128, 0, st>>>(cu, vcu, rlen, N, (int64_t)d.hv * d.D * (d.out_bf16 ? 2 : 4),
+    k_continue_scatter<<<(unsigned)T, 128, 0, st>>>(cu, vcu, rlen, N, vT, (int64_t)d.hv * d.D * (d.out_bf16 ? 2 : 4),
                                                     vo, o, hdr);
 }
 

@@ -17,6 +17,7 @@ struct TokenArrays {
   const void* v;
   const float* g;
   const float* beta;
+  int64_t n_tokens;  // rows the arrays hold (bounds-checked builds check every range against it)
 };
 
 struct Dims {
@@ -76,6 +77,8 @@ struct ChainWork {
   // cache's running state (S^(0) is not needed in bnd)
   bool bnd_in_place;
   const int32_t* bnd_skip;
+  int64_t n_chunks;  // chunk records (rows of the pre-pass outputs and of bnd)
+  int64_t n_tokens;  // token rows behind `keys`
   // decode
   const int32_t* slot;
   const int32_t* pos;
@@ -95,6 +98,7 @@ void launch_chain(const Dims& d, const void* keys, const float* W, const float* 
 struct IntraWork {
   const ChunkRec* chunks;
   const SeqRec* seqs;
+  int n_seqs;
   int64_t n_chunks;
   const float* bnd;
   void* o;
@@ -160,7 +164,7 @@ void launch_continue_gather(const Dims& d, const TokenArrays& in, const int32_t*
                             const int32_t* rlen, const int32_t* slot, int N, int64_t vT,
                             const gdn_cpr_cache& cache, const TokenArrays& out, WsHeader* hdr, cudaStream_t st);
 void launch_continue_scatter(const Dims& d, const int32_t* cu, const int32_t* vcu, const int32_t* rlen, int N,
-                             int64_t T, const void* vo, void* o, WsHeader* hdr, cudaStream_t st);
+                             int64_t T, int64_t vT, const void* vo, void* o, WsHeader* hdr, cudaStream_t st);
 
 // Backward (kernels_bwd.cu).  `mark(ctx, kernels)` is called after each stage (prep,
 // chain, big products, gradients, grouped-head sum) with the kernels it launched.

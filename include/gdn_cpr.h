@@ -83,7 +83,9 @@ typedef enum {
     GDN_DEVERR_CU_SEQLENS = 1, /* device cu_seqlens disagree with cu_seqlens_host */
     GDN_DEVERR_SLOT = 2,       /* decode slot index outside [0, cache.slots) */
     GDN_DEVERR_POS = 3,        /* negative cache position */
-    GDN_DEVERR_TIMEOUT = 4     /* a bounded on-device wait gave up */
+    GDN_DEVERR_TIMEOUT = 4,    /* a bounded on-device wait gave up */
+    GDN_DEVERR_BOUNDS = 5      /* bounds-checked builds only (GDN_CHECKED): a work item's index
+                                  range fell outside its buffer; the item was skipped */
 } gdn_device_error;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;

@@ -111,3 +111,14 @@ def test_decode_and_bwd_argument_checks(lib):
     assert rc == 1  # empty cache
     rc = lib.gdn_cpr_get_device_error(None, None, None)
     assert rc == 1
+
+
+def test_checked_build_exports_every_declared_symbol():
+    """The bounds-checked debug variant (GDN_CHECKED=1) builds and exports the same ABI."""
+    import ctypes as ct
+
+    path = build.build(checked=True)
+    assert path.endswith("libgdn_cpr_checked.so")
+    lib = ct.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
