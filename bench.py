@@ -49,11 +49,11 @@ SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
 # reported only while the kernel's source (its function text plus common.cuh) hashes to the
 # value it had when the counters were taken; after any change it is null until recaptured.
 NCU_TRAFFIC = {
-    # 202,411,008 + 21,403,392 B for one 4096-token sequence x 32 value heads
-    "k_intra": {"src_sha": "74d8c0ca878a95b7", "bytes_per_unit": (202411008 + 21403392) / (4096 * 32),
+    # 202,427,136 + 21,451,008 B for one 4096-token sequence x 32 value heads
+    "k_intra": {"src_sha": "a8a39bb5e32bb4ba", "bytes_per_unit": (202427136 + 21451008) / (4096 * 32),
                 "unit": "token-head"},
-    # 541,314,304 + 482,651,648 B for the full 256-slot x 32-head launch (one-pass capture)
-    "k_decode": {"src_sha": "e875afd522d68d5e", "bytes_per_unit": (541314304 + 482651648) / (256 * 32),
+    # 541,318,400 + 482,635,520 B for the full 256-slot x 32-head launch (one-pass capture)
+    "k_decode": {"src_sha": "96c57dc03655655e", "bytes_per_unit": (541318400 + 482635520) / (256 * 32),
                  "unit": "slot-head"},
 }
 KERNEL_TEXT = {  # file, first line of the kernel, first line after it
@@ -374,13 +374,23 @@ def run_cuda(args):
     slots = torch.arange(nseq, dtype=torch.int32, device=dev)
     grads = None
 
-    def prefill_call():
+    def prefill_call(o=None):
         api.prefill(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], chunk=C,
-                    cache=cache, cu_seqlens_host=cu_host, ws=ws_pre, o=o_pre, state_out=st_pre)
+                    cache=cache, cu_seqlens_host=cu_host, ws=ws_pre, o=o_pre if o is None else o,
+                    state_out=st_pre)
 
-    def decode_call(i):
-        api.decode_step(dq_in["q"][i], dq_in["k"][i], dq_in["v"][i], dq_in["g"][i],
-                        dq_in["beta"][i], slots, cache, ws=ws_dec, o=o_dec[i])
+    def decode_call(i, src=None):
+        s_ = dq_in if src is None else src
+        api.decode_step(s_["q"][i], s_["k"][i], s_["v"][i], s_["g"][i], s_["beta"][i], slots, cache,
+                        ws=ws_dec, o=o_dec[i])
+
+    def capture_decode(src):
+        """A CUDA graph of the 64 decode steps reading their tokens from `src`."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(DECODE_STEPS):
+                decode_call(i, src)
+        return g
 
     def trainer_call():
         nonlocal grads
@@ -515,7 +525,7 @@ def run_cuda(args):
     cont = bench_continue(api, synth, torch, dev, w, seed, stage_ms["prefill"])
 
     # end to end through host buffers: H2D inputs each step, D2H results each step
-    e2e = bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call,
+    e2e = bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_decode, trainer_call,
                     t, dq_in, o_pre, o_dec, lambda: grads, step_tok, world, ms)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -794,23 +804,29 @@ def bench_continue(api, synth, torch, dev, w, seed, prefill_ms):
                                    "us_per_call": us, "tokens_per_s": N * K / (us * 1e-6)}}
 
 
-def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_call, t, dq_in,
+def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_decode, trainer_call, t, dq_in,
               o_pre, o_dec, get_grads, step_tok, world, compute_ms):
     """Same step through the public API with host buffers: every step copies its inputs from
     pinned host memory and reads its results back, pipelined as a serving or training loop
-    would run it: step i + 1's inputs go up on one copy stream (into the second of two input
-    buffers) while step i computes, and every result comes back on another copy stream as
-    soon as its kernels finish; the timed region opens before the first input copy and
-    closes after the last read-back."""
+    would run it: step i + 1's inputs (prefill / trainer tokens and the decode tokens) go up on
+    one copy stream (into the second of two input buffers, the decode steps replayed from one
+    CUDA graph per buffer) while step i computes, and every result comes back on another copy
+    stream as soon as its kernels finish; the prefill output alternates between two buffers and the
+    gradients are new tensors every step, so a step's compute never waits for the previous
+    step's read-back of them; the timed region opens before the first input copy and closes
+    after the last read-back."""
     nseq = len(w.lengths)
     dhost = {n: xd[n].view(DECODE_STEPS, nseq, *xd[n].shape[1:]).contiguous().pin_memory()
              for n in ("q", "k", "v", "g", "beta")}
     h2d = sum(v.numel() * v.element_size() for v in host.values()) + \
         sum(v.numel() * v.element_size() for v in dhost.values())
 
+    o_pre_bufs = [o_pre, torch.empty_like(o_pre)]
+    cur = {"pre": o_pre}
+
     def result_tensors(part):
         if part == "pre":
-            return {"o_prefill": o_pre}
+            return {"o_prefill": cur["pre"]}
         if part == "dec":
             return {"o_decode": o_dec}
         gr = get_grads()
@@ -820,13 +836,15 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_c
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     t0 = dict(t)
     bufs = [t0, {n: torch.empty_like(v) for n, v in t0.items()}]
+    dq_bufs = [dq_in, {n: torch.empty_like(v) for n, v in dq_in.items()}]
+    graphs = [graph, capture_decode(dq_bufs[1])]
     trainer_call()  # so that the gradient tensors exist for sizing the host buffers
     torch.cuda.synchronize(dev)
     res_host = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                 for part in ("pre", "dec", "trn") for n, v in result_tensors(part).items()}
     d2h = sum(v.numel() * v.element_size() for v in res_host.values())
     mk = torch.cuda.Event
-    up_done, in_free = [mk(), mk()], [mk(), mk()]
+    up_done, in_free, pre_free = [mk(), mk()], [mk(), mk()], [mk(), mk()]
     produced = {p: mk() for p in ("pre", "dec", "trn")}
     read_back = {p: mk() for p in ("pre", "dec", "trn")}
 
@@ -837,6 +855,8 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_c
             up.wait_event(in_free[b])
             for n in host:
                 bufs[b][n].copy_(host[n], non_blocking=True)
+            for n in dhost:
+                dq_bufs[b][n].copy_(dhost[n], non_blocking=True)
             up_done[b].record(up)
 
     def download(part):
@@ -854,19 +874,18 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, trainer_c
             comp.wait_event(up_done[b])
             if i + 1 < n_steps:
                 upload(1 - b)
-            for n in dhost:
-                dq_in[n].copy_(dhost[n], non_blocking=True)
             t.update(bufs[b])
-            comp.wait_event(read_back["pre"])
-            prefill_call()
+            cur["pre"] = o_pre_bufs[b]
+            comp.wait_event(pre_free[b])  # the read-back of this buffer two steps ago
+            prefill_call(cur["pre"])
             produced["pre"].record(comp)
             download("pre")
+            pre_free[b].record(down)
             comp.wait_event(read_back["dec"])
-            graph.replay()
+            graphs[b].replay()
             produced["dec"].record(comp)
             download("dec")
-            comp.wait_event(read_back["trn"])
-            trainer_call()
+            trainer_call()  # new gradient tensors (the read-back of the last ones holds theirs)
             produced["trn"].record(comp)
             in_free[b].record(comp)
             download("trn")

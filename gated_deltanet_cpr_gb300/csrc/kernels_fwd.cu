@@ -1243,9 +1243,6 @@ __global__ void __launch_bounds__(2 * D, 2) k_intra(Dims dm, TokenArrays in, Int
   const bool writer = lay.writes_out();
   float opart[4] = {0.f, 0.f, 0.f, 0.f};
   float cprev = 1.f;  // the scale of the previous token's output partials
-  // warps w and w + 4 share a scheduler: start the upper four about half a token later so
-  // that one warp's reduction waits fall in the other's arithmetic
-  if (t >= 128) __nanosleep(300);
   for (int tt = first; tt < len; ++tt) {
     float4 kk[D / 32];
     float part[4], p[4], us[4];
