@@ -379,10 +379,12 @@ def run_cuda(args):
                     cache=cache, cu_seqlens_host=cu_host, ws=ws_pre, o=o_pre if o is None else o,
                     state_out=st_pre)
 
+    # every step's prefill leaves each sequence at position L, so decode step i of a step
+    # starts at L + i: the host knows the positions (gdn_cpr_decode_step_pos)
     def decode_call(i, src=None):
         s_ = dq_in if src is None else src
         api.decode_step(s_["q"][i], s_["k"][i], s_["v"][i], s_["g"][i], s_["beta"][i], slots, cache,
-                        ws=ws_dec, o=o_dec[i])
+                        ws=ws_dec, o=o_dec[i], pos_host=[L + i for L in w.lengths])
 
     def capture_decode(src):
         """A CUDA graph of the 64 decode steps reading their tokens from `src`."""
@@ -591,7 +593,7 @@ def bench_decode_big(api, synth, torch, dev, w, P, seed):
 
     def call(i):
         api.decode_step(din["q"][i], din["k"][i], din["v"][i], din["g"][i], din["beta"][i],
-                        slots, cache, ws=ws, o=o[i])
+                        slots, cache, ws=ws, o=o[i], pos_host=[L0 + i] * N)
 
     def reset():
         for n in api.Cache.TENSORS:

@@ -23,14 +23,15 @@ MODE_PREFILL, MODE_DECODE, MODE_FWD, MODE_BWD, MODE_CONTINUE = 0, 1, 2, 3, 4
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "workspace missing, misaligned or too small", 5: "device-side error recorded"}
 DEVERR = {0: "none", 1: "cu_seqlens mismatch", 2: "slot out of range", 3: "negative position",
-          4: "bounded wait timed out", 5: "index range outside a buffer (bounds-checked build)"}
+          4: "bounded wait timed out", 5: "index range outside a buffer (bounds-checked build)",
+          6: "host positions disagree with the cache (step skipped)"}
 
 # every function the header declares (checked by the CPU test suite)
 EXPORTS = ("gdn_cpr_version", "gdn_cpr_status_string", "gdn_cpr_workspace_size",
            "gdn_cpr_prefill", "gdn_cpr_decode_step", "gdn_cpr_fwd", "gdn_cpr_bwd",
            "gdn_cpr_get_device_error", "gdn_cpr_set_profile", "gdn_cpr_decode_step_noalloc",
            "gdn_cpr_policy_digest", "gdn_cpr_prefill_continue", "gdn_cpr_running_state",
-           "gdn_cpr_noalloc_device_error", "gdn_cpr_test_wait_timeout")
+           "gdn_cpr_noalloc_device_error", "gdn_cpr_test_wait_timeout", "gdn_cpr_decode_step_pos")
 NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
@@ -79,6 +80,8 @@ def load():
             lib.gdn_cpr_workspace_size.argtypes = [P, I, P, ctypes.POINTER(S)]
             lib.gdn_cpr_prefill.argtypes = [P] * 14 + [S, P]
             lib.gdn_cpr_decode_step.argtypes = [P] * 10 + [S, P]
+            lib.gdn_cpr_decode_step_pos.argtypes = [P] * 11 + [S, P]
+            lib.gdn_cpr_decode_step_pos.restype = I
             lib.gdn_cpr_fwd.argtypes = [P] * 13 + [S, P]
             lib.gdn_cpr_bwd.argtypes = [P] * 19 + [S, P]
             lib.gdn_cpr_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
@@ -310,9 +313,11 @@ def fwd(q, k, v, g, beta, cu_seqlens, chunk=64, state_in=None, out_dtype=None,
     return o, state_out, saved_bnd[:n_chunks]
 
 
-def decode_step(q, k, v, g, beta, slot, cache: Cache, out_dtype=None, ws=None, o=None):
+def decode_step(q, k, v, g, beta, slot, cache: Cache, out_dtype=None, ws=None, o=None, pos_host=None):
     """gdn_cpr_decode_step: one token per slot.  q,k [N,Hqk,d], v [N,Hv,d], g,beta [N,Hv],
-    slot [N] int32 (device).  Returns o [N,Hv,d]."""
+    slot [N] int32 (device).  With pos_host (the host's copy of cache.pos[slot], a sequence
+    or CPU tensor), gdn_cpr_decode_step_pos: the resync kernels are skipped when no token
+    completes a chunk.  Returns o [N,Hv,d]."""
     lib = load()
     N, hqk, d = k.shape
     hv = v.shape[1]
@@ -323,6 +328,13 @@ def decode_step(q, k, v, g, beta, slot, cache: Cache, out_dtype=None, ws=None, o
     if ws is None:
         ws = alloc_workspace(workspace_bytes(shape, MODE_DECODE), q.device)
     cs = cache.struct()
+    if pos_host is not None:
+        ph = torch.as_tensor(pos_host, dtype=torch.int32).cpu().contiguous()
+        rc = lib.gdn_cpr_decode_step_pos(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g), _p(beta),
+                                         _p(slot), _p(ph), ctypes.byref(cs), _p(o), _p(ws), ws.numel(),
+                                         _stream(q.device))
+        _check("gdn_cpr_decode_step_pos", rc)
+        return o
     rc = lib.gdn_cpr_decode_step(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g), _p(beta),
                                  _p(slot), ctypes.byref(cs), _p(o), _p(ws), ws.numel(),
                                  _stream(q.device))

@@ -340,6 +340,94 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   return finish(st);
 }
 
+// One decode step (gdn_cpr_decode_step; with pos_host, gdn_cpr_decode_step_pos): the token
+// step, then the resynchronisation (the same boundary pre-pass and chain step as prefill, on
+// the cached chunk) for the tokens that complete a chunk, then the position advance.  With a
+// host copy of the positions that shows no token completing a chunk, the resync kernels are
+// not launched and the token step checks that claim on the device.
+gdn_status run_decode(const gdn_cpr_shape* shape, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, const int32_t* slot, const int32_t* pos_host, const gdn_cpr_cache* cache,
+                      void* o, void* ws, size_t ws_bytes, gdn_stream_t stream) {
+  gdn_status rc = check_shape(shape);
+  if (rc != GDN_OK) return rc;
+  const int N = shape->num_seqs;
+  if (shape->total_tokens != N) return GDN_ERR_INVALID_ARG;
+  rc = check_cache(cache);
+  if (rc != GDN_OK) return rc;
+  if (N > 0 && (!ok_ptr(q, 16) || !ok_ptr(k, 16) || !ok_ptr(v, 16) || !ok_ptr(g, 4) ||
+                !ok_ptr(beta, 4) || !ok_ptr(o, 16) || !ok_ptr(slot, 4)))
+    return GDN_ERR_INVALID_ARG;
+  bool resync = true;  // whether any token of this step may complete a chunk
+  if (pos_host) {
+    resync = false;
+    for (int n = 0; n < N; ++n) {
+      if (pos_host[n] < 0) return GDN_ERR_INVALID_ARG;
+      if ((pos_host[n] + 1) % shape->chunk == 0) resync = true;
+    }
+  }
+  const DecLayout L = dec_layout(shape);
+  if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
+  if (N == 0) return GDN_OK;
+  const Dims d = dims_of(shape);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* W = reinterpret_cast<float*>(at(ws, L.W));
+  float* U = reinterpret_cast<float*>(at(ws, L.U));
+  float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
+  TokenArrays in{q, k, v, g, beta, N};
+  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
+  Stages stg(stream, kDecodeStages);
+
+  DecodeWork dw{};
+  dw.N = N;
+  dw.slot = slot;
+  dw.slots = cache->slots;
+  dw.s_run = cache->s_run;
+  dw.c_run = cache->c_run;
+  dw.tail_k = cache->tail_k;
+  dw.tail_v = cache->tail_v;
+  dw.tail_g = cache->tail_g;
+  dw.tail_beta = cache->tail_beta;
+  dw.pos = cache->pos;
+  dw.o = o;
+  dw.no_resync = resync ? 0 : 1;
+  launch_decode(d, in, dw, hdr, stream);
+  stg.mark(1);
+
+  if (resync) {
+    const int64_t tail_rows = (int64_t)cache->slots * d.C;
+    TokenArrays tail{nullptr, cache->tail_k, cache->tail_v, cache->tail_g, cache->tail_beta, tail_rows};
+    PrepWork pw{};
+    pw.chunks = nullptr;
+    pw.n_items = N;
+    pw.slot = slot;
+    pw.pos = cache->pos;
+    pw.slots = cache->slots;
+    launch_prep(d, tail, pw, W, U, gamma, hdr, stream);
+    stg.mark(1);
+
+    ChainWork cw{};
+    cw.seqs = nullptr;
+    cw.N = N;
+    cw.slot = slot;
+    cw.pos = cache->pos;
+    cw.s_bnd = cache->s_bnd;
+    cw.s_run = cache->s_run;
+    cw.c_run = cache->c_run;
+    cw.slots = cache->slots;
+    cw.n_chunks = N;
+    cw.n_tokens = tail_rows;
+    launch_chain(d, cache->tail_k, W, U, gamma, cw, hdr, stream);
+    stg.mark(1);
+  } else {
+    stg.mark(0);
+    stg.mark(0);
+  }
+
+  launch_advance(N, slot, cache->slots, cache->pos, hdr, stream);
+  stg.mark(1);
+  return finish(stream);
+}
+
 }  // namespace
 
 extern "C" {
@@ -419,71 +507,17 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape* shape, const void* q, const 
                                const int32_t* slot, const gdn_cpr_cache* cache, void* o,
                                void* ws, size_t ws_bytes, gdn_stream_t stream) {
   NvtxRange nvtx("gdn_cpr_decode_step");
-  gdn_status rc = check_shape(shape);
-  if (rc != GDN_OK) return rc;
-  const int N = shape->num_seqs;
-  if (shape->total_tokens != N) return GDN_ERR_INVALID_ARG;
-  rc = check_cache(cache);
-  if (rc != GDN_OK) return rc;
-  if (N > 0 && (!ok_ptr(q, 16) || !ok_ptr(k, 16) || !ok_ptr(v, 16) || !ok_ptr(g, 4) ||
-                !ok_ptr(beta, 4) || !ok_ptr(o, 16) || !ok_ptr(slot, 4)))
-    return GDN_ERR_INVALID_ARG;
-  const DecLayout L = dec_layout(shape);
-  if (!ws || !aligned(ws, kAlign) || ws_bytes < L.total) return GDN_ERR_WORKSPACE;
-  if (N == 0) return GDN_OK;
-  const Dims d = dims_of(shape);
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  float* W = reinterpret_cast<float*>(at(ws, L.W));
-  float* U = reinterpret_cast<float*>(at(ws, L.U));
-  float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
-  TokenArrays in{q, k, v, g, beta, N};
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
-  Stages stg(stream, kDecodeStages);
+  return run_decode(shape, q, k, v, g, beta, slot, nullptr, cache, o, ws, ws_bytes, stream);
+}
 
-  DecodeWork dw{};
-  dw.N = N;
-  dw.slot = slot;
-  dw.slots = cache->slots;
-  dw.s_run = cache->s_run;
-  dw.c_run = cache->c_run;
-  dw.tail_k = cache->tail_k;
-  dw.tail_v = cache->tail_v;
-  dw.tail_g = cache->tail_g;
-  dw.tail_beta = cache->tail_beta;
-  dw.pos = cache->pos;
-  dw.o = o;
-  launch_decode(d, in, dw, hdr, stream);
-  stg.mark(1);
-
-  // resynchronisation: the same boundary pre-pass and chain step as prefill, on the tail
-  const int64_t tail_rows = (int64_t)cache->slots * d.C;
-  TokenArrays tail{nullptr, cache->tail_k, cache->tail_v, cache->tail_g, cache->tail_beta, tail_rows};
-  PrepWork pw{};
-  pw.chunks = nullptr;
-  pw.n_items = N;
-  pw.slot = slot;
-  pw.pos = cache->pos;
-  pw.slots = cache->slots;
-  launch_prep(d, tail, pw, W, U, gamma, hdr, stream);
-  stg.mark(1);
-
-  ChainWork cw{};
-  cw.seqs = nullptr;
-  cw.N = N;
-  cw.slot = slot;
-  cw.pos = cache->pos;
-  cw.s_bnd = cache->s_bnd;
-  cw.s_run = cache->s_run;
-  cw.c_run = cache->c_run;
-  cw.slots = cache->slots;
-  cw.n_chunks = N;
-  cw.n_tokens = tail_rows;
-  launch_chain(d, cache->tail_k, W, U, gamma, cw, hdr, stream);
-  stg.mark(1);
-
-  launch_advance(N, slot, cache->slots, cache->pos, stream);
-  stg.mark(1);
-  return finish(stream);
+gdn_status gdn_cpr_decode_step_pos(const gdn_cpr_shape* shape, const void* q, const void* k,
+                                   const void* v, const float* g, const float* beta,
+                                   const int32_t* slot, const int32_t* pos_host,
+                                   const gdn_cpr_cache* cache, void* o, void* ws, size_t ws_bytes,
+                                   gdn_stream_t stream) {
+  NvtxRange nvtx("gdn_cpr_decode_step_pos");
+  if (!pos_host && shape && shape->num_seqs > 0) return GDN_ERR_INVALID_ARG;
+  return run_decode(shape, q, k, v, g, beta, slot, pos_host, cache, o, ws, ws_bytes, stream);
 }
 
 gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k, const void* v,

@@ -1311,6 +1311,17 @@ __global__ void __launch_bounds__(2 * D, 2) k_decode(Dims dm, TokenArrays in, De
   const int grp = dm.hv / dm.hqk;
   const int hq = h / grp;
   const int C = dm.C;
+  if (w.no_resync) {  // the host's claim: no token of this step completes a chunk
+    bool bad = false;
+    for (int m = t; m < w.N; m += 2 * D) {
+      const int s2 = w.slot[m];
+      if (s2 >= 0 && s2 < w.slots && (w.pos[s2] + 1) % C == 0) bad = true;
+    }
+    if (__syncthreads_or(bad)) {
+      if (t == 0 && n == 0 && h == 0) set_error(hdr, GDN_DEVERR_POS_HOST);
+      return;
+    }
+  }
   const int sl = w.slot[n];
   if (sl < 0 || sl >= w.slots) {
     if (t == 0 && h == 0) set_error(hdr, GDN_DEVERR_SLOT);
@@ -1370,15 +1381,17 @@ static void launch_decode_t(const Dims& d, const TokenArrays& in, const DecodeWo
 }
 
 // ============================================================ small helpers ====
-__global__ void k_advance(int N, const int32_t* __restrict__ slot, int slots, int32_t* pos) {
+__global__ void k_advance(int N, const int32_t* __restrict__ slot, int slots, int32_t* pos,
+                          const WsHeader* __restrict__ hdr) {
+  if (hdr->err == GDN_DEVERR_POS_HOST) return;  // the step was refused
   for (int n = blockIdx.x * blockDim.x + threadIdx.x; n < N; n += gridDim.x * blockDim.x) {
     const int sl = slot[n];
     if (sl >= 0 && sl < slots && pos[sl] >= 0) pos[sl] += 1;
   }
 }
 
-void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st) {
-  k_advance<<<(N + 255) / 256, 256, 0, st>>>(N, slot, slots, pos);
+void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, const WsHeader* hdr, cudaStream_t st) {
+  k_advance<<<(N + 255) / 256, 256, 0, st>>>(N, slot, slots, pos, hdr);
 }
 
 // The explicit running state of selected cache slots: out[i] = c_run[s] * s_run[s] for

@@ -135,12 +135,16 @@ struct DecodeWork {
   float* tail_beta;
   const int32_t* pos;
   void* o;
+  // the host said no token of this step completes a chunk: every CTA first checks that on
+  // the device and, if it is false for any slot, the step does nothing (GDN_DEVERR_POS_HOST)
+  int no_resync;
 };
 void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, WsHeader* hdr,
                    cudaStream_t st);
 
-// pos[slot[n]] += 1 for every valid n (last kernel of a decode step).
-void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, cudaStream_t st);
+// pos[slot[n]] += 1 for every valid n (last kernel of a decode step), unless the step was
+// refused (GDN_DEVERR_POS_HOST in the error word).
+void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, const WsHeader* hdr, cudaStream_t st);
 
 // out[i] = c_run[s] * s_run[s] (s = sel[i], or i if sel is NULL) for i < n, all heads:
 // the explicit running state of cache slots.

@@ -84,8 +84,10 @@ typedef enum {
     GDN_DEVERR_SLOT = 2,       /* decode slot index outside [0, cache.slots) */
     GDN_DEVERR_POS = 3,        /* negative cache position */
     GDN_DEVERR_TIMEOUT = 4,    /* a bounded on-device wait gave up */
-    GDN_DEVERR_BOUNDS = 5      /* bounds-checked builds only (GDN_CHECKED): a work item's index
+    GDN_DEVERR_BOUNDS = 5,     /* bounds-checked builds only (GDN_CHECKED): a work item's index
                                   range fell outside its buffer; the item was skipped */
+    GDN_DEVERR_POS_HOST = 6    /* gdn_cpr_decode_step_pos: the host positions said no token
+                                  completes a chunk, the cache says one does; step skipped */
 } gdn_device_error;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -184,6 +186,23 @@ gdn_status gdn_cpr_decode_step(const gdn_cpr_shape *shape, const void *q, const 
                                const void *v, const float *g, const float *beta,
                                const int32_t *slot, const gdn_cpr_cache *cache, void *o,
                                void *ws, size_t ws_bytes, gdn_stream_t stream);
+
+/* gdn_cpr_decode_step for callers that know the slots' positions on the host (a serving
+ * scheduler tracks every sequence's length): pos_host [N] is the host copy of
+ * cache->pos[slot[n]] before this step, read during the call and not kept.  When no token of
+ * the step completes a chunk ((pos_host[n] + 1) % C != 0 for every n), the resynchronisation
+ * kernels are not launched at all -- two launches fewer per step; otherwise the call is
+ * exactly gdn_cpr_decode_step.  Results and bits are those of gdn_cpr_decode_step.  The
+ * claim is checked on the device: if a slot's cache position does complete a chunk after
+ * all, the whole step is skipped (nothing in the cache changes, o is not written) and the
+ * workspace's error word reads GDN_DEVERR_POS_HOST.  A negative pos_host entry returns
+ * GDN_ERR_INVALID_ARG.  The launch sequence depends on pos_host, so a CUDA graph captured
+ * with it is valid only for steps at those positions.                                     */
+gdn_status gdn_cpr_decode_step_pos(const gdn_cpr_shape *shape, const void *q, const void *k,
+                                   const void *v, const float *g, const float *beta,
+                                   const int32_t *slot, const int32_t *pos_host,
+                                   const gdn_cpr_cache *cache, void *o, void *ws, size_t ws_bytes,
+                                   gdn_stream_t stream);
 
 /* Trainer forward (case "trainer_fwd" next to "engine_prefill" on the IsoExec page,
  * section on contract structure).  Identical arithmetic to gdn_cpr_prefill -- o and
