@@ -865,6 +865,210 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
   if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
 
+// ====================================================  K1b decode resync (tcgen05)  ===
+// The decode resynchronisation on tensor cores (d = 128, C = 64, bf16): one boundary step per
+// (step token n, head) whose slot completes a chunk with this token,
+//     s_bnd <- gamma s_bnd + (Ud - Wd s_bnd^T)^T K,   s_run <- s_bnd,   c_run <- 1,
+// with exactly the operands, MMAs and readouts of k_chain_tc's step (so the same bits).  Every
+// item is a single step, so instead of k_chain_tc's stage double buffer this kernel keeps one
+// stage, places the Vd^T operand over the stage's Wd images once the first product has read
+// them, and loads S^(0) in column slices, which fits two CTAs per SM: one CTA's loads and waits
+// overlap the other's work.
+namespace tcr {
+constexpr int D = 128, C = 64;
+constexpr uint32_t A1_BYTES = 128 * D * 2;       // state operand, per hi / lo
+constexpr uint32_t A2_BYTES = 128 * C * 2;       // Vd^T operand, per hi / lo (over Wd hi / Wd lo)
+constexpr uint32_t STAGE_BYTES = 3 * C * D * 2;  // Wd hi | Wd lo | K^T
+constexpr size_t SMEM = 2 * (size_t)A1_BYTES + STAGE_BYTES + 64;
+constexpr int MAX_ITEMS = 64;  // items per CTA (the launch sizes the grid for it)
+constexpr uint32_t TMEM_COLS = 256, D1_COL = 0, D2_COL = 64;
+constexpr uint32_t IDESC1 = tc::idesc_bf16(128, C);
+constexpr uint32_t IDESC2 = tc::idesc_bf16(128, D);
+static_assert(A2_BYTES == C * D * 2, "Vd^T hi / lo occupy exactly the Wd hi / lo images");
+}  // namespace tcr
+
+__global__ void __launch_bounds__(256, 2) k_resync_tc(Dims dm, const float* __restrict__ Wimg,
+                                                      const float* __restrict__ U,
+                                                      const float* __restrict__ gamma, ChainWork w,
+                                                      WsHeader* __restrict__ hdr) {
+  using namespace tcr;
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smr[];
+  unsigned char* A1h = smr;
+  unsigned char* A1l = A1h + A1_BYTES;
+  unsigned char* stg = A1l + A1_BYTES;  // Wd hi | Wd lo | K^T
+  unsigned char* A2h = stg;             // Vd^T hi over Wd hi, after the first product
+  unsigned char* A2l = stg + A2_BYTES;  // Vd^T lo over Wd lo
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + STAGE_BYTES);  // load, mma
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  // warp w reads TMEM lanes 32 (w % 4) .. + 31 (state rows) and column half w / 4
+  const int t = threadIdx.x, warp = t >> 5, row = (warp & 3) * 32 + (t & 31), half = warp >> 2;
+  const int cs0 = half * (D / 2), us0 = half * (C / 2);
+  const int64_t SZ = (int64_t)D * D;
+  const int64_t WS = (int64_t)prep_w_floats(C, D);
+  const int64_t total = (int64_t)w.N * dm.hv;
+  // this CTA's items (wi = blockIdx.x + j * gridDim.x) whose slot resynchronises
+  __shared__ int64_t s_list[MAX_ITEMS];
+  __shared__ int s_cnt;
+  if (t == 0) s_cnt = 0;
+  __syncthreads();
+  if (t < MAX_ITEMS) {
+    const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
+    if (wi < total) {
+      const int sl = w.slot[wi / dm.hv];
+      if (sl >= 0 && sl < w.slots && w.pos[sl] >= 0 && (w.pos[sl] + 1) % C == 0 &&
+          in_bounds(hdr, wi / dm.hv < w.n_chunks))
+        s_list[atomicAdd(&s_cnt, 1)] = wi;
+    }
+  }
+  __syncthreads();
+  const int count = s_cnt;
+  if (count == 0) return;
+
+  if (t == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);
+  uint32_t lphase = 0, mphase = 0;
+  bool ok = true, lpending = false, mpending = false;
+
+  for (int li = 0; li < count && ok; ++li) {
+    const int64_t wi = s_list[li];
+    const int n = (int)(wi / dm.hv), h = (int)(wi % dm.hv);
+    const int sl = w.slot[n];
+    const int64_t so = ((int64_t)sl * dm.hv + h) * SZ;
+    if (t == 0) {
+      mbar_expect_tx(&bars[0], STAGE_BYTES);
+      bulk_g2s(stg, Wimg + ((int64_t)n * dm.hv + h) * WS, STAGE_BYTES, &bars[0]);
+      w.c_run[(int64_t)sl * dm.hv + h] = 1.f;  // the running state written below is explicit
+    }
+    lpending = true;
+    {  // S^(0): A operand (split) and gamma_0 S^(0) into D2, one 16-column slice at a time
+      const float g0 = gamma[(int64_t)n * dm.hv + h];
+      const float* src = w.s_bnd + so + (int64_t)row * D;
+#pragma unroll 1
+      for (int g = 0; g < D / 32; ++g) {
+        const int c0 = cs0 + 16 * g;
+        float v[16];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float4 f = *reinterpret_cast<const float4*>(src + c0 + 4 * x);
+          v[4 * x] = f.x; v[4 * x + 1] = f.y; v[4 * x + 2] = f.z; v[4 * x + 3] = f.w;
+        }
+        store_split16(A1h, A1l, row, c0, D, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(g0, v[e]);
+        tmem_st16(tlane + D2_COL + c0, v);
+      }
+      tmem_st_wait();
+    }
+    float ud[C / 2];
+    {
+      const float* Ug = U + ((int64_t)n * dm.hv + h) * (int64_t)C * D + (int64_t)us0 * D + row;
+#pragma unroll
+      for (int s2 = 0; s2 < C / 2; ++s2) ud[s2] = Ug[(int64_t)s2 * D];
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    ok = __syncthreads_and(t != 0 || mbar_wait(&bars[0], lphase)) != 0;
+    if (!ok) break;
+    lphase ^= 1u;
+    lpending = false;
+    if (t == 0) {  // D1 = S Wd^T (three split terms)
+      fence_after_sync();
+      const uint32_t a_hi = smem_u32(A1h), a_lo = smem_u32(A1l);
+      const uint32_t w_hi = smem_u32(stg), w_lo = w_hi + C * D * 2;
+      const uint32_t sbo = (D / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t a = term == 2 ? a_lo : a_hi;
+        const uint32_t b = term == 1 ? w_lo : w_hi;
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16(tbase + D1_COL, make_desc(a + kk * 256, 128, sbo), make_desc(b + kk * 256, 128, sbo), IDESC1,
+                   (term > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(&bars[1]);
+    }
+    mpending = true;
+    ok = __syncthreads_and(mbar_wait(&bars[1], mphase)) != 0;
+    if (!ok) break;
+    mphase ^= 1u;
+    mpending = false;
+    fence_after_sync();
+#pragma unroll
+    for (int s1 = 0; s1 < C / 2; s1 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
+      float v[16];
+      tmem_ld16(tlane + D1_COL + us0 + s1, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s1 + e], v[e]);
+      store_split16(A2h, A2l, row, us0 + s1, C, v);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    if (t == 0) {  // D2 += Vd^T K (two split terms)
+      fence_after_sync();
+      const uint32_t k_img = smem_u32(stg) + 2 * C * D * 2;
+      const uint32_t sbo = (C / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t a = smem_u32(term == 0 ? A2h : A2l);
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16(tbase + D2_COL, make_desc(a + kk * 256, 128, sbo), make_desc(k_img + kk * 256, 128, sbo), IDESC2,
+                   1u);
+      }
+      mma_commit(&bars[1]);
+    }
+    mpending = true;
+    ok = __syncthreads_and(mbar_wait(&bars[1], mphase)) != 0;
+    if (!ok) break;
+    mphase ^= 1u;
+    mpending = false;
+    fence_after_sync();
+    {  // S^(1) -> s_bnd and s_run through a per-warp staging tile over the dead Vd^T operand,
+       // so that each store instruction writes 8 rows x 64 contiguous bytes
+      float* tile = reinterpret_cast<float*>(A2h) + warp * (32 * 20);
+      const int lane = t & 31, rq = (warp & 3) * 32;
+      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + D2_COL + c0, v);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          *reinterpret_cast<float4*>(tile + lane * 20 + 4 * x) = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int rl = 8 * k2 + (lane >> 2), f = lane & 3;
+          const int64_t o = so + (int64_t)(rq + rl) * D + c0 + 4 * f;
+          const float4 x4 = *reinterpret_cast<const float4*>(tile + rl * 20 + 4 * f);
+          *reinterpret_cast<float4*>(w.s_bnd + o) = x4;
+          *reinterpret_cast<float4*>(w.s_run + o) = x4;
+        }
+        __syncwarp();
+      }
+    }
+    fence_proxy_async();  // the tiles' generic writes before the next item's bulk copy over them
+    fence_before_sync();
+    __syncthreads();  // the stage and the tiles are reused by the next item
+  }
+  if (!ok && t == 0) {
+    set_error(hdr, GDN_DEVERR_TIMEOUT);
+    // let the operations this CTA may still have in flight finish before releasing TMEM
+    if (lpending) mbar_wait(&bars[0], lphase);
+    if (mpending) mbar_wait(&bars[1], mphase);
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
+}
+
 // ============================================================  K1a (tcgen05)  ===
 // Boundary pre-pass on tensor cores for d = 128, C = 64, bf16 inputs, one CTA of 256
 // threads per (chunk, head) as k_prep:
@@ -1503,9 +1707,16 @@ void launch_chain(const Dims& d, const void* keys, const float* W, const float* 
                   const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st) {
   if (w.N <= 0) return;
   if (boundary_on_tensor_cores(d)) {
-    ensure_smem(k_chain_tc, tcc::SMEM);
     const int64_t total = (int64_t)w.N * d.hv;
-    int64_t cap = w.seqs ? total : (int64_t)sm_count();
+    if (!w.seqs) {  // decode resync: single steps, two CTAs per SM
+      ensure_smem(k_resync_tc, tcr::SMEM);
+      int64_t cap = 2 * (int64_t)sm_count();
+      if ((total + cap - 1) / cap > tcr::MAX_ITEMS) cap = (total + tcr::MAX_ITEMS - 1) / tcr::MAX_ITEMS;
+      k_resync_tc<<<(unsigned)(total < cap ? total : cap), 256, tcr::SMEM, st>>>(d, W, U, gamma, w, hdr);
+      return;
+    }
+    ensure_smem(k_chain_tc, tcc::SMEM);
+    int64_t cap = total;
     if ((total + cap - 1) / cap > 128) cap = (total + 127) / 128;  // at most 128 items per CTA
     k_chain_tc<<<(unsigned)(total < cap ? total : cap), 256, tcc::SMEM, st>>>(d, W, U, gamma, w, hdr);
   } else if (d.in_bf16) {
