@@ -941,6 +941,8 @@ def run_ncu_case(args):
     decode    64 slots x 32 heads of 128x128 states: three decode steps (no resync)
     decode256 the decode workload's 256 slots x 32 heads: three decode steps (no resync), for
               one-pass DRAM counters of the full-size launch
+    resync64  64 slots x 32 heads whose every step completes a chunk: three decode steps, each
+              with its resync (pre-pass and k_resync_tc)
     bwd       one 4096-token sequence: two trainer forward + backward passes
     """
     import torch
@@ -965,14 +967,20 @@ def run_ncu_case(args):
                         cu_seqlens_host=x["cu_seqlens"])
     else:
         N = 256 if args.ncu_case == "decode256" else 64
+        p0 = 2047 if args.ncu_case == "resync64" else 2048
         cache = api.Cache(N, w.h_qk, w.h_v, w.d, w.chunk, dtype=torch.bfloat16, device=dev)
         cache.s_run.normal_()
-        cache.pos.fill_(2048)
+        cache.s_bnd.normal_().mul_(0.05)
+        cache.tail_k.normal_().mul_(0.09)
+        cache.tail_v.normal_()
+        cache.tail_g.uniform_(-1.5, -0.1)
+        cache.tail_beta.uniform_(0.2, 0.8)
+        cache.pos.fill_(p0)
         x = synth.make_inputs([N], w.h_qk, w.h_v, w.d, dtype=w.dtype, seed=0)
         t = {n: x[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
         slots = torch.arange(N, dtype=torch.int32, device=dev)
         for _ in range(3):
-            cache.pos.fill_(2048)
+            cache.pos.fill_(p0)
             api.decode_step(t["q"], t["k"], t["v"], t["g"], t["beta"], slots, cache)
     torch.cuda.synchronize(dev)
     print(json.dumps({"ncu_case": args.ncu_case, "ok": True}))
@@ -986,7 +994,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode256", "bwd"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode256", "resync64", "bwd"], default=None,
                     help="run a small fixed case for an ncu capture and exit")
     args = ap.parse_args(argv)
     if args.ncu_case:
