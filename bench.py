@@ -394,14 +394,14 @@ def run_cuda(args):
                 decode_call(i, src)
         return g
 
-    def trainer_call():
+    def trainer_call(grad_out=None):
         nonlocal grads
         api.fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], chunk=C,
                 cu_seqlens_host=cu_host, ws=ws_fwd, o=o_fwd, state_out=st_fwd, saved_bnd=saved)
         if have_bwd:
             grads = api.bwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu_seqlens"], saved,
                             t["dout"], chunk=C, cu_seqlens_host=cu_host, ws=ws_bwd,
-                            want_dstate_in=True)
+                            want_dstate_in=True, out=grad_out)
 
     # the 64 decode steps as one CUDA graph (fixed pointers, device-side resync decision)
     prefill_call()
@@ -813,10 +813,10 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
     would run it: step i + 1's inputs (prefill / trainer tokens and the decode tokens) go up on
     one copy stream (into the second of two input buffers, the decode steps replayed from one
     CUDA graph per buffer) while step i computes, and every result comes back on another copy
-    stream as soon as its kernels finish; the prefill output alternates between two buffers and the
-    gradients are new tensors every step, so a step's compute never waits for the previous
-    step's read-back of them; the timed region opens before the first input copy and closes
-    after the last read-back."""
+    stream as soon as its kernels finish; the prefill output and the gradients alternate
+    between two sets of buffers, so a step's compute never waits for the previous step's
+    read-back of them; the timed region opens before the first input copy and closes after
+    the last read-back."""
     nseq = len(w.lengths)
     dhost = {n: xd[n].view(DECODE_STEPS, nseq, *xd[n].shape[1:]).contiguous().pin_memory()
              for n in ("q", "k", "v", "g", "beta")}
@@ -824,14 +824,14 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
         sum(v.numel() * v.element_size() for v in dhost.values())
 
     o_pre_bufs = [o_pre, torch.empty_like(o_pre)]
-    cur = {"pre": o_pre}
+    cur = {"pre": o_pre, "trn": None}
 
     def result_tensors(part):
         if part == "pre":
             return {"o_prefill": cur["pre"]}
         if part == "dec":
             return {"o_decode": o_dec}
-        gr = get_grads()
+        gr = get_grads() if cur["trn"] is None else cur["trn"]
         return {} if gr is None else {n: gr[n] for n in ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")}
 
     comp = torch.cuda.current_stream(dev)
@@ -842,11 +842,12 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
     graphs = [graph, capture_decode(dq_bufs[1])]
     trainer_call()  # so that the gradient tensors exist for sizing the host buffers
     torch.cuda.synchronize(dev)
+    grad_bufs = [{n: torch.empty_like(v) for n, v in get_grads().items()} for _ in range(2)]
     res_host = {n: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
                 for part in ("pre", "dec", "trn") for n, v in result_tensors(part).items()}
     d2h = sum(v.numel() * v.element_size() for v in res_host.values())
     mk = torch.cuda.Event
-    up_done, in_free, pre_free = [mk(), mk()], [mk(), mk()], [mk(), mk()]
+    up_done, in_free, pre_free, trn_free = [mk(), mk()], [mk(), mk()], [mk(), mk()], [mk(), mk()]
     produced = {p: mk() for p in ("pre", "dec", "trn")}
     read_back = {p: mk() for p in ("pre", "dec", "trn")}
 
@@ -887,10 +888,13 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
             graphs[b].replay()
             produced["dec"].record(comp)
             download("dec")
-            trainer_call()  # new gradient tensors (the read-back of the last ones holds theirs)
+            cur["trn"] = grad_bufs[b]
+            comp.wait_event(trn_free[b])  # the read-back of this set two steps ago
+            trainer_call(cur["trn"])
             produced["trn"].record(comp)
             in_free[b].record(comp)
             download("trn")
+            trn_free[b].record(down)
         comp.wait_stream(down)
 
     run(max(1, args.warmup))

@@ -362,8 +362,9 @@ def decode_step_noalloc(q, k, v, g, beta, slot, cache: Cache, out_dtype=None, o=
 
 
 def bwd(q, k, v, g, beta, cu_seqlens, saved_bnd, dout, chunk=64, state_in=None,
-        dstate_out=None, cu_seqlens_host=None, ws=None, want_dstate_in=True):
-    """gdn_cpr_bwd.  Returns dict dq, dk, dv, dg, dbeta, dstate_in (fp32)."""
+        dstate_out=None, cu_seqlens_host=None, ws=None, want_dstate_in=True, out=None):
+    """gdn_cpr_bwd.  Returns dict dq, dk, dv, dg, dbeta, dstate_in (fp32); `out`, if given, is
+    such a dict of preallocated tensors to write into."""
     lib = load()
     cu_host = _host_cu(cu_seqlens, cu_seqlens_host)
     N = cu_host.numel() - 1
@@ -371,13 +372,14 @@ def bwd(q, k, v, g, beta, cu_seqlens, saved_bnd, dout, chunk=64, state_in=None,
     hv = v.shape[1]
     shape = make_shape(N, T, hqk, hv, d, chunk, q.dtype, dout.dtype)
     dev = q.device
-    out = dict(dq=torch.empty((T, hqk, d), dtype=torch.float32, device=dev),
-               dk=torch.empty((T, hqk, d), dtype=torch.float32, device=dev),
-               dv=torch.empty((T, hv, d), dtype=torch.float32, device=dev),
-               dg=torch.empty((T, hv), dtype=torch.float32, device=dev),
-               dbeta=torch.empty((T, hv), dtype=torch.float32, device=dev),
-               dstate_in=torch.empty((N, hv, d, d), dtype=torch.float32, device=dev)
-               if want_dstate_in else None)
+    if out is None:
+        out = dict(dq=torch.empty((T, hqk, d), dtype=torch.float32, device=dev),
+                   dk=torch.empty((T, hqk, d), dtype=torch.float32, device=dev),
+                   dv=torch.empty((T, hv, d), dtype=torch.float32, device=dev),
+                   dg=torch.empty((T, hv), dtype=torch.float32, device=dev),
+                   dbeta=torch.empty((T, hv), dtype=torch.float32, device=dev),
+                   dstate_in=torch.empty((N, hv, d, d), dtype=torch.float32, device=dev)
+                   if want_dstate_in else None)
     if ws is None:
         ws = alloc_workspace(workspace_bytes(shape, MODE_BWD, cu_host), dev)
     rc = lib.gdn_cpr_bwd(ctypes.byref(shape), _p(q), _p(k), _p(v), _p(g), _p(beta),
