@@ -1693,7 +1693,7 @@ void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float*
   if (boundary_on_tensor_cores(d)) {
     ensure_smem(k_prep_tc, tcp::SMEM);
     const int64_t total = w.n_items * d.hv;
-    int64_t cap = w.chunks ? total : 2 * (int64_t)sm_count();
+    int64_t cap = 2 * (int64_t)sm_count();  // persistent: two CTAs per SM walk the items
     if ((total + cap - 1) / cap > 256) cap = (total + 255) / 256;  // at most 256 items per CTA
     k_prep_tc<<<(unsigned)(total < cap ? total : cap), 256, tcp::SMEM, st>>>(d, in, w, W, U, gamma, hdr);
   } else if (d.in_bf16) {
