@@ -646,7 +646,7 @@ def bench_decode_big(api, synth, torch, dev, w, P, seed):
             "us_token_step_kernel_median": step_k3 * 1e3,
             "resync_steps": len(resync_steps),
             "us_resync_step": statistics.mean(resync_ms) * 1e3,
-            "us_resync_stages": dict(zip(("token_step", "prepass", "chain", "advance"),
+            "us_resync_stages": dict(zip(("token_step", "resync", "advance"),
                                          (x * 1e3 for x in stages[resync_steps[0]]))),
             "tokens_per_s": N / (us_per_step * 1e-6),
             "roofline": {"bound": "hbm", "kernel": "k_decode (token step)", "achieved": ach,
@@ -946,7 +946,7 @@ def run_ncu_case(args):
     decode256 the decode workload's 256 slots x 32 heads: three decode steps (no resync), for
               one-pass DRAM counters of the full-size launch
     resync64  64 slots x 32 heads whose every step completes a chunk: three decode steps, each
-              with its resync (pre-pass and k_resync_tc)
+              with its resync (k_resync_fused_tc)
     bwd       one 4096-token sequence: two trainer forward + backward passes
     """
     import torch

@@ -226,8 +226,7 @@ struct Stages {
 
 const char* const kFwdStages[] = {"work list", "boundary pre-pass", "boundary chain", "intra-chunk recurrence",
                                   "cache tail", nullptr};
-const char* const kDecodeStages[] = {"decode token step", "resync pre-pass", "resync chain", "position advance",
-                                     nullptr};
+const char* const kDecodeStages[] = {"decode token step", "resync", "position advance", nullptr};
 const char* const kBwdStages[] = {"work list", "backward prep", "reverse boundary chain", "backward products",
                                   "backward gradients", "grouped-head sum", nullptr};
 const char* const kContStages[] = {"continue: positions, work list, gather", "boundary pre-pass",
@@ -402,9 +401,6 @@ gdn_status run_decode(const gdn_cpr_shape* shape, const void* q, const void* k, 
     pw.slot = slot;
     pw.pos = cache->pos;
     pw.slots = cache->slots;
-    launch_prep(d, tail, pw, W, U, gamma, hdr, stream);
-    stg.mark(1);
-
     ChainWork cw{};
     cw.seqs = nullptr;
     cw.N = N;
@@ -416,10 +412,14 @@ gdn_status run_decode(const gdn_cpr_shape* shape, const void* q, const void* k, 
     cw.slots = cache->slots;
     cw.n_chunks = N;
     cw.n_tokens = tail_rows;
-    launch_chain(d, cache->tail_k, W, U, gamma, cw, hdr, stream);
-    stg.mark(1);
+    if (launch_resync_fused(d, tail, pw, cw, hdr, stream)) {
+      stg.mark(1);
+    } else {
+      launch_prep(d, tail, pw, W, U, gamma, hdr, stream);
+      launch_chain(d, cache->tail_k, W, U, gamma, cw, hdr, stream);
+      stg.mark(2);
+    }
   } else {
-    stg.mark(0);
     stg.mark(0);
   }
 

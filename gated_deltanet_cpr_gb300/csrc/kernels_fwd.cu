@@ -865,210 +865,6 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
   if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
 
-// ====================================================  K1b decode resync (tcgen05)  ===
-// The decode resynchronisation on tensor cores (d = 128, C = 64, bf16): one boundary step per
-// (step token n, head) whose slot completes a chunk with this token,
-//     s_bnd <- gamma s_bnd + (Ud - Wd s_bnd^T)^T K,   s_run <- s_bnd,   c_run <- 1,
-// with exactly the operands, MMAs and readouts of k_chain_tc's step (so the same bits).  Every
-// item is a single step, so instead of k_chain_tc's stage double buffer this kernel keeps one
-// stage, places the Vd^T operand over the stage's Wd images once the first product has read
-// them, and loads S^(0) in column slices, which fits two CTAs per SM: one CTA's loads and waits
-// overlap the other's work.
-namespace tcr {
-constexpr int D = 128, C = 64;
-constexpr uint32_t A1_BYTES = 128 * D * 2;       // state operand, per hi / lo
-constexpr uint32_t A2_BYTES = 128 * C * 2;       // Vd^T operand, per hi / lo (over Wd hi / Wd lo)
-constexpr uint32_t STAGE_BYTES = 3 * C * D * 2;  // Wd hi | Wd lo | K^T
-constexpr size_t SMEM = 2 * (size_t)A1_BYTES + STAGE_BYTES + 64;
-constexpr int MAX_ITEMS = 64;  // items per CTA (the launch sizes the grid for it)
-constexpr uint32_t TMEM_COLS = 256, D1_COL = 0, D2_COL = 64;
-constexpr uint32_t IDESC1 = tc::idesc_bf16(128, C);
-constexpr uint32_t IDESC2 = tc::idesc_bf16(128, D);
-static_assert(A2_BYTES == C * D * 2, "Vd^T hi / lo occupy exactly the Wd hi / lo images");
-}  // namespace tcr
-
-__global__ void __launch_bounds__(256, 2) k_resync_tc(Dims dm, const float* __restrict__ Wimg,
-                                                      const float* __restrict__ U,
-                                                      const float* __restrict__ gamma, ChainWork w,
-                                                      WsHeader* __restrict__ hdr) {
-  using namespace tcr;
-  using namespace tc;
-  extern __shared__ __align__(128) unsigned char smr[];
-  unsigned char* A1h = smr;
-  unsigned char* A1l = A1h + A1_BYTES;
-  unsigned char* stg = A1l + A1_BYTES;  // Wd hi | Wd lo | K^T
-  unsigned char* A2h = stg;             // Vd^T hi over Wd hi, after the first product
-  unsigned char* A2l = stg + A2_BYTES;  // Vd^T lo over Wd lo
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + STAGE_BYTES);  // load, mma
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
-  // warp w reads TMEM lanes 32 (w % 4) .. + 31 (state rows) and column half w / 4
-  const int t = threadIdx.x, warp = t >> 5, row = (warp & 3) * 32 + (t & 31), half = warp >> 2;
-  const int cs0 = half * (D / 2), us0 = half * (C / 2);
-  const int64_t SZ = (int64_t)D * D;
-  const int64_t WS = (int64_t)prep_w_floats(C, D);
-  const int64_t total = (int64_t)w.N * dm.hv;
-  // this CTA's items (wi = blockIdx.x + j * gridDim.x) whose slot resynchronises
-  __shared__ int64_t s_list[MAX_ITEMS];
-  __shared__ int s_cnt;
-  if (t == 0) s_cnt = 0;
-  __syncthreads();
-  if (t < MAX_ITEMS) {
-    const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
-    if (wi < total) {
-      const int sl = w.slot[wi / dm.hv];
-      if (sl >= 0 && sl < w.slots && w.pos[sl] >= 0 && (w.pos[sl] + 1) % C == 0 &&
-          in_bounds(hdr, wi / dm.hv < w.n_chunks))
-        s_list[atomicAdd(&s_cnt, 1)] = wi;
-    }
-  }
-  __syncthreads();
-  const int count = s_cnt;
-  if (count == 0) return;
-
-  if (t == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
-  fence_before_sync();
-  __syncthreads();
-  fence_after_sync();
-  const uint32_t tbase = *tslot;
-  const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);
-  uint32_t lphase = 0, mphase = 0;
-  bool ok = true, lpending = false, mpending = false;
-
-  for (int li = 0; li < count && ok; ++li) {
-    const int64_t wi = s_list[li];
-    const int n = (int)(wi / dm.hv), h = (int)(wi % dm.hv);
-    const int sl = w.slot[n];
-    const int64_t so = ((int64_t)sl * dm.hv + h) * SZ;
-    if (t == 0) {
-      mbar_expect_tx(&bars[0], STAGE_BYTES);
-      bulk_g2s(stg, Wimg + ((int64_t)n * dm.hv + h) * WS, STAGE_BYTES, &bars[0]);
-      w.c_run[(int64_t)sl * dm.hv + h] = 1.f;  // the running state written below is explicit
-    }
-    lpending = true;
-    {  // S^(0): A operand (split) and gamma_0 S^(0) into D2, one 16-column slice at a time
-      const float g0 = gamma[(int64_t)n * dm.hv + h];
-      const float* src = w.s_bnd + so + (int64_t)row * D;
-#pragma unroll 1
-      for (int g = 0; g < D / 32; ++g) {
-        const int c0 = cs0 + 16 * g;
-        float v[16];
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const float4 f = *reinterpret_cast<const float4*>(src + c0 + 4 * x);
-          v[4 * x] = f.x; v[4 * x + 1] = f.y; v[4 * x + 2] = f.z; v[4 * x + 3] = f.w;
-        }
-        store_split16(A1h, A1l, row, c0, D, v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(g0, v[e]);
-        tmem_st16(tlane + D2_COL + c0, v);
-      }
-      tmem_st_wait();
-    }
-    float ud[C / 2];
-    {
-      const float* Ug = U + ((int64_t)n * dm.hv + h) * (int64_t)C * D + (int64_t)us0 * D + row;
-#pragma unroll
-      for (int s2 = 0; s2 < C / 2; ++s2) ud[s2] = Ug[(int64_t)s2 * D];
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    ok = __syncthreads_and(t != 0 || mbar_wait(&bars[0], lphase)) != 0;
-    if (!ok) break;
-    lphase ^= 1u;
-    lpending = false;
-    if (t == 0) {  // D1 = S Wd^T (three split terms)
-      fence_after_sync();
-      const uint32_t a_hi = smem_u32(A1h), a_lo = smem_u32(A1l);
-      const uint32_t w_hi = smem_u32(stg), w_lo = w_hi + C * D * 2;
-      const uint32_t sbo = (D / 8) * 128;
-#pragma unroll 1
-      for (int term = 0; term < 3; ++term) {
-        const uint32_t a = term == 2 ? a_lo : a_hi;
-        const uint32_t b = term == 1 ? w_lo : w_hi;
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16(tbase + D1_COL, make_desc(a + kk * 256, 128, sbo), make_desc(b + kk * 256, 128, sbo), IDESC1,
-                   (term > 0 || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(&bars[1]);
-    }
-    mpending = true;
-    ok = __syncthreads_and(mbar_wait(&bars[1], mphase)) != 0;
-    if (!ok) break;
-    mphase ^= 1u;
-    mpending = false;
-    fence_after_sync();
-#pragma unroll
-    for (int s1 = 0; s1 < C / 2; s1 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
-      float v[16];
-      tmem_ld16(tlane + D1_COL + us0 + s1, v);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s1 + e], v[e]);
-      store_split16(A2h, A2l, row, us0 + s1, C, v);
-    }
-    fence_proxy_async();
-    fence_before_sync();
-    __syncthreads();
-    if (t == 0) {  // D2 += Vd^T K (two split terms)
-      fence_after_sync();
-      const uint32_t k_img = smem_u32(stg) + 2 * C * D * 2;
-      const uint32_t sbo = (C / 8) * 128;
-#pragma unroll 1
-      for (int term = 0; term < 2; ++term) {
-        const uint32_t a = smem_u32(term == 0 ? A2h : A2l);
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16(tbase + D2_COL, make_desc(a + kk * 256, 128, sbo), make_desc(k_img + kk * 256, 128, sbo), IDESC2,
-                   1u);
-      }
-      mma_commit(&bars[1]);
-    }
-    mpending = true;
-    ok = __syncthreads_and(mbar_wait(&bars[1], mphase)) != 0;
-    if (!ok) break;
-    mphase ^= 1u;
-    mpending = false;
-    fence_after_sync();
-    {  // S^(1) -> s_bnd and s_run through a per-warp staging tile over the dead Vd^T operand,
-       // so that each store instruction writes 8 rows x 64 contiguous bytes
-      float* tile = reinterpret_cast<float*>(A2h) + warp * (32 * 20);
-      const int lane = t & 31, rq = (warp & 3) * 32;
-      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
-        float v[16];
-        tmem_ld16(tlane + D2_COL + c0, v);
-#pragma unroll
-        for (int x = 0; x < 4; ++x)
-          *reinterpret_cast<float4*>(tile + lane * 20 + 4 * x) = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
-        __syncwarp();
-#pragma unroll
-        for (int k2 = 0; k2 < 4; ++k2) {
-          const int rl = 8 * k2 + (lane >> 2), f = lane & 3;
-          const int64_t o = so + (int64_t)(rq + rl) * D + c0 + 4 * f;
-          const float4 x4 = *reinterpret_cast<const float4*>(tile + rl * 20 + 4 * f);
-          *reinterpret_cast<float4*>(w.s_bnd + o) = x4;
-          *reinterpret_cast<float4*>(w.s_run + o) = x4;
-        }
-        __syncwarp();
-      }
-    }
-    fence_proxy_async();  // the tiles' generic writes before the next item's bulk copy over them
-    fence_before_sync();
-    __syncthreads();  // the stage and the tiles are reused by the next item
-  }
-  if (!ok && t == 0) {
-    set_error(hdr, GDN_DEVERR_TIMEOUT);
-    // let the operations this CTA may still have in flight finish before releasing TMEM
-    if (lpending) mbar_wait(&bars[0], lphase);
-    if (mpending) mbar_wait(&bars[1], mphase);
-  }
-  fence_before_sync();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
-}
-
 // ============================================================  K1a (tcgen05)  ===
 // Boundary pre-pass on tensor cores for d = 128, C = 64, bf16 inputs, one CTA of 256
 // threads per (chunk, head) as k_prep:
@@ -1178,6 +974,19 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     const int64_t tok0 = s_tok0[li];
     const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
     const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
+    if (li + 1 < count) {  // L2 prefetch of the next item's K and V rows, g and beta (128-byte lines)
+      const int h2 = (int)(s_list[li + 1] % dm.hv), hq2 = h2 / (dm.hv / dm.hqk);
+      const int64_t tk = s_tok0[li + 1];
+      for (int q = t; q < 2 * C; q += 256) {  // a row of D bf16 = two lines
+        const int r = q >> 1, part = (q & 1) * (D / 2);
+        tc::prefetch_l2(kin + (tk + r) * kstride + (int64_t)hq2 * D + part);
+        tc::prefetch_l2(vin + (tk + r) * vstride + (int64_t)h2 * D + part);
+      }
+      if (t < C) {
+        tc::prefetch_l2(in.g + (tk + t) * dm.hv + h2);
+        tc::prefetch_l2(in.beta + (tk + t) * dm.hv + h2);
+      }
+    }
 
     // 1. K rows and V rows (staged in the A region, free until the Gram readout) straight
     // from global memory, g and beta: every load issued before the first store
@@ -1373,6 +1182,422 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
+}
+
+// ====================================================  K1c decode resync, fused (tcgen05)  ===
+// The decode resynchronisation in one kernel (d = 128, C = 64, bf16): for every (step token
+// n, head) whose slot completes a chunk with this token, k_prep_tc's pre-pass on the slot's
+// chunk tail followed by one step of k_chain_tc,
+//     s_bnd <- gamma s_bnd + (Ud - Wd s_bnd^T)^T K,   s_run <- s_bnd,   c_run <- 1,
+// with the pre-pass outputs kept on chip: the Wd hi / lo and K^T images stay in shared
+// memory where the step reads them, Ud goes from the U^T readout straight into the
+// registers of the thread that owns the state row, gamma is recomputed.  Every value is
+// formed by the same operations in the same order as in those two kernels, which the
+// prefill's boundary pass runs, so a resynchronised boundary state has the bits the prefill
+// of the same tokens gives.  The CTAs are persistent, two per SM (shared memory: the state
+// operand hi | lo, 64 KB, and the stage [Wd hi | Wd lo | K^T], 48 KB; the pre-pass's K / V
+// images, A, T and vectors live in the state operand and the Wd images while those are
+// still unwritten), and each prefetches its next item's operands into L2.
+namespace tcf {
+constexpr int D = 128, C = 64, CP = C + 1;
+constexpr uint32_t TILE = C * D * 2;        // a C x D or D x C bf16 image
+constexpr uint32_t MAT = C * CP * 4;        // fp32 C x C with padded rows
+constexpr uint32_t A1_BYTES = 128 * D * 2;  // state operand, per hi / lo
+constexpr uint32_t OFF_A1H = 0, OFF_A1L = A1_BYTES, OFF_STG = 2 * A1_BYTES, OFF_KT = OFF_STG + 2 * TILE;
+constexpr uint32_t OFF_R0 = 0, OFF_VT = TILE, OFF_A = A1_BYTES, OFF_VEC = OFF_A + MAT, OFF_T = OFF_STG;
+constexpr size_t SMEM = OFF_STG + 3 * (size_t)TILE + 64;
+constexpr int MAX_ITEMS = 64;  // items per CTA (the launch sizes the grid for it)
+constexpr uint32_t TMEM_COLS = 256, GRAM_COL = 0, W_COL = 0, UT_COL = 128, D1_COL = 0, D2_COL = 64;
+static_assert(OFF_VEC + 5 * C * 4 <= OFF_A1L + A1_BYTES, "pre-pass vectors inside the lo state image");
+static_assert(OFF_T + MAT <= OFF_KT, "T inside the Wd images");
+}  // namespace tcf
+
+__global__ void __launch_bounds__(256, 2) k_resync_fused_tc(Dims dm, TokenArrays in, PrepWork pw, ChainWork w,
+                                                            WsHeader* __restrict__ hdr) {
+  using namespace tcf;
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smf[];
+  unsigned char* A1h = smf + OFF_A1H;
+  unsigned char* A1l = smf + OFF_A1L;
+  unsigned char* stg = smf + OFF_STG;  // Wd hi | Wd lo | K^T
+  unsigned char* KT = smf + OFF_KT;
+  unsigned char* A2h = stg;         // Vd^T hi over Wd hi, after the first product
+  unsigned char* A2l = stg + TILE;  // Vd^T lo over Wd lo
+  unsigned char* R0 = smf + OFF_R0;  // K image, then Xs, then TK hi | lo
+  unsigned char* VT = smf + OFF_VT;
+  float* A = reinterpret_cast<float*>(smf + OFF_A);  // V rows, then A, then TV hi | lo
+  float* Tm = reinterpret_cast<float*>(smf + OFF_T);
+  float* gs = reinterpret_cast<float*>(smf + OFF_VEC);
+  float* Gs = gs + C;
+  float* bs = Gs + C;
+  float* bk = bs + C;
+  float* dec = bk + C;
+  float* Xs = reinterpret_cast<float*>(R0);
+  unsigned char* TKh = R0;
+  unsigned char* TKl = R0 + C * C * 2;
+  unsigned char* TVh = reinterpret_cast<unsigned char*>(A);
+  unsigned char* TVl = TVh + C * C * 2;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smf + OFF_STG + 3 * TILE);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  // warp w reads TMEM lanes 32 (w % 4) .. + 31 (state rows) and column half w / 4
+  const int t = threadIdx.x, warp = t >> 5, row = (warp & 3) * 32 + (t & 31), half = warp >> 2;
+  const int cs0 = half * (D / 2), us0 = half * (C / 2);
+  const int64_t SZ = (int64_t)D * D;
+  const int64_t total = pw.n_items * dm.hv;
+  // this CTA's items (wi = blockIdx.x + j * gridDim.x) whose slot resynchronises
+  __shared__ int64_t s_list[MAX_ITEMS];
+  __shared__ int s_cnt;
+  if (t == 0) s_cnt = 0;
+  __syncthreads();
+  if (t < MAX_ITEMS) {
+    const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
+    if (wi < total) {
+      const int64_t n = wi / dm.hv;
+      const int h = (int)(wi % dm.hv);
+      const int sl = pw.slot[n];
+      if (sl < 0 || sl >= pw.slots) {
+        if (h == 0) set_error(hdr, GDN_DEVERR_SLOT);
+      } else {
+        const int p = pw.pos[sl];
+        if (p < 0) {
+          if (h == 0) set_error(hdr, GDN_DEVERR_POS);
+        } else if ((p + 1) % C == 0 &&
+                   in_bounds(hdr, (int64_t)sl * C + C <= in.n_tokens && n < w.n_chunks && sl < w.slots)) {
+          s_list[atomicAdd(&s_cnt, 1)] = wi;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int count = s_cnt;
+  if (count == 0) return;
+
+  // tensor memory and the MMA barrier, once per CTA
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);
+  uint32_t phase = 0;
+  bool ok = true, pending = false;
+  auto wait_mma = [&]() {
+    const bool done = mbar_wait(bar, phase);
+    ok = __syncthreads_and(done) != 0;
+    if (ok) {
+      phase ^= 1u;
+      pending = false;
+    }
+  };
+  const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(in.k);
+  const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(in.v);
+  const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
+
+  // L2 prefetch of an item's reads: K and V rows, g, beta of the slot's chunk tail and (state)
+  // its boundary state; 128-byte lines spread over the threads
+  auto prefetch_item = [&](int64_t wj, bool state) {
+    const int64_t n2 = wj / dm.hv;
+    const int h2 = (int)(wj % dm.hv), hq2 = h2 / (dm.hv / dm.hqk);
+    const int64_t tk = (int64_t)pw.slot[n2] * C;
+    for (int q = t; q < 2 * C; q += 256) {  // a row of D bf16 = two lines
+      const int r = q >> 1, part = (q & 1) * (D / 2);
+      prefetch_l2(kin + (tk + r) * kstride + (int64_t)hq2 * D + part);
+      prefetch_l2(vin + (tk + r) * vstride + (int64_t)h2 * D + part);
+    }
+    if (t < C) {
+      prefetch_l2(in.g + (tk + t) * dm.hv + h2);
+      prefetch_l2(in.beta + (tk + t) * dm.hv + h2);
+    }
+    if (state) {
+      const float* sp = w.s_bnd + ((int64_t)pw.slot[n2] * dm.hv + h2) * SZ;
+      for (int q = t; q < D * D / 32; q += 256) prefetch_l2(sp + 32 * q);
+    }
+  };
+  if (count > 0) {
+    const int64_t w0 = s_list[0];
+    const float* sp = w.s_bnd + ((int64_t)pw.slot[w0 / dm.hv] * dm.hv + (int)(w0 % dm.hv)) * SZ;
+    for (int q = t; q < D * D / 32; q += 256) prefetch_l2(sp + 32 * q);
+  }
+
+  for (int li = 0; li < count && ok; ++li) {
+    const int64_t wi = s_list[li];
+    const int64_t n = wi / dm.hv;
+    const int h = (int)(wi % dm.hv);
+    const int hq = h / (dm.hv / dm.hqk);
+    const int sl = pw.slot[n];
+    const int64_t tok0 = (int64_t)sl * C;  // the slot's chunk tail
+    if (li + 1 < count) prefetch_item(s_list[li + 1], true);
+    const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
+    const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
+
+    // ---- the pre-pass, k_prep_tc's steps
+    // 1. K rows image, V rows (in the A region), g, beta: every load issued before the first store
+    {
+      uint4 kr[4], vr[4];
+      float g0 = 0.f, b0 = 0.f;
+      if (t < C) {
+        g0 = in.g[(tok0 + t) * dm.hv + h];
+        b0 = in.beta[(tok0 + t) * dm.hv + h];
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {  // C * D / 8 = 1024 pieces of 16 bytes
+        int r, c0;
+        kmajor_piece(t + it * 256, D, r, c0);
+        kr[it] = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
+        vr[it] = *reinterpret_cast<const uint4*>(vb + r * vstride + c0);
+      }
+      if (t < C) {
+        gs[t] = g0;
+        bs[t] = b0;
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, c0;
+        kmajor_piece(t + it * 256, D, r, c0);
+        *reinterpret_cast<uint4*>(R0 + kmajor_off(r, c0, D)) = kr[it];
+        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(A) + kmajor_off(r, c0, D)) = vr[it];
+      }
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    // 2. Gram on the tensor cores while one thread forms G
+    if (t == 0) {
+      fence_after_sync();
+      const uint32_t a = smem_u32(R0);
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16(tbase + GRAM_COL, make_desc(a + kk * 256, 128, (D / 8) * 128), make_desc(a + kk * 256, 128, (D / 8) * 128),
+                 idesc_bf16(128, C), kk > 0 ? 1u : 0u);
+      mma_commit(bar);
+      float run = gs[0];
+      Gs[0] = run;
+#pragma unroll
+      for (int i = 1; i < C; ++i) {
+        run = __fadd_rn(run, gs[i]);
+        Gs[i] = run;
+      }
+    }
+    pending = true;
+    // K^T and V^T images from the row images while the Gram product runs (it reads only R0)
+    transpose_image(KT, R0, D, C);
+    transpose_image(VT, reinterpret_cast<const unsigned char*>(A), D, C);
+    __syncthreads();
+    if (t < C) {
+      bk[t] = __fmul_rn(bs[t], expf(Gs[t]));
+      dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
+    }
+    // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs; the readout multiplies
+    for (int e = t; e < C * C; e += 256) {
+      const int i = e / C, s = e % C;
+      if (i > s) A[i * CP + s] = __fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s])));
+    }
+    wait_mma();
+    if (!ok) break;
+    fence_after_sync();
+    if ((warp & 3) < 2) {  // rows 0..63: A_is = beta_i e^{G_i - G_s} Gram_is (i > s)
+      const int i = row;
+      const int cbase = half * 32;
+      for (int s0 = cbase; s0 < cbase + 32; s0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + GRAM_COL + s0, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int s = s0 + e;
+          A[i * CP + s] = (i > s) ? __fmul_rn(A[i * CP + s], v[e]) : 0.f;
+        }
+      }
+    }
+    fence_before_sync();
+    __syncthreads();
+    // 3. T = (I + A)^{-1}
+    unit_lower_inverse64(A, CP, Tm, CP, Xs);
+    // 4. TK = T diag(beta e^G), TV = T diag(beta), split into bf16 images (lower triangle)
+    for (int q = t; q < C * (C / 8); q += 256) {
+      int i, r0;
+      kmajor_piece(q, C, i, r0);
+      float tk[8], tv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int r = r0 + e;
+        const float x = (r <= i) ? Tm[i * CP + r] : 0.f;
+        tk[e] = __fmul_rn(x, bk[r]);
+        tv[e] = __fmul_rn(x, bs[r]);
+      }
+      uint32_t a[4], b[4], c2[4], d2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        split_bf16(tk[2 * e], h0, l0);
+        split_bf16(tk[2 * e + 1], h1, l1);
+        a[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        b[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+        split_bf16(tv[2 * e], h0, l0);
+        split_bf16(tv[2 * e + 1], h1, l1);
+        c2[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        d2[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      const uint32_t off = kmajor_off(i, r0, C);
+      *reinterpret_cast<uint4*>(TKh + off) = make_uint4(a[0], a[1], a[2], a[3]);
+      *reinterpret_cast<uint4*>(TKl + off) = make_uint4(b[0], b[1], b[2], b[3]);
+      *reinterpret_cast<uint4*>(TVh + off) = make_uint4(c2[0], c2[1], c2[2], c2[3]);
+      *reinterpret_cast<uint4*>(TVl + off) = make_uint4(d2[0], d2[1], d2[2], d2[3]);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    // 5. W = TK K (rows 0..63 of a 128-row MMA) and U^T = V^T TV^T
+    if (t == 0) {
+      fence_after_sync();
+      const uint32_t sbo = (C / 8) * 128;
+      const uint32_t kt = smem_u32(KT), vt = smem_u32(VT);
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t a = smem_u32(term == 0 ? TKh : TKl);
+        const uint32_t b = smem_u32(term == 0 ? TVh : TVl);
+        for (int kk = 0; kk < C / 16; ++kk) {
+          mma_bf16(tbase + W_COL, make_desc(a + kk * 256, 128, sbo), make_desc(kt + kk * 256, 128, sbo),
+                   idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16(tbase + UT_COL, make_desc(vt + kk * 256, 128, sbo), make_desc(b + kk * 256, 128, sbo),
+                   idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+        }
+      }
+      mma_commit(bar);
+    }
+    pending = true;
+    wait_mma();
+    if (!ok) break;
+    fence_after_sync();
+    // 6. Wd = diag(dec) W rows 0..63 -> the stage's split image; Ud column of this thread's
+    // state row (Ud[s][row] = dec_s U^T[row][s]) -> registers; gamma
+    if ((warp & 3) < 2) {
+      const int i = row;
+      const int cbase = half * 64;
+      for (int c0 = cbase; c0 < cbase + 64; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + W_COL + c0, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(dec[i], v[e]);
+        store_split16(stg, stg + TILE, i, c0, D, v);
+      }
+    }
+    float ud[C / 2];
+#pragma unroll
+    for (int s1 = 0; s1 < C / 2; s1 += 16) {
+      float v[16];
+      tmem_ld16(tlane + UT_COL + us0 + s1, v);
+#pragma unroll
+      for (int x = 0; x < 16; ++x) ud[s1 + x] = __fmul_rn(dec[us0 + s1 + x], v[x]);
+    }
+    const float g0 = expf(Gs[C - 1]);
+    fence_before_sync();
+    __syncthreads();  // W, U^T and the vectors are read before the state overwrites them
+
+    // ---- the boundary step (k_chain_tc's step on one chunk)
+    const int64_t so = ((int64_t)sl * dm.hv + h) * SZ;
+    if (t == 0) w.c_run[(int64_t)sl * dm.hv + h] = 1.f;  // the running state written below is explicit
+    {  // S^(0): A operand (split) and gamma_0 S^(0) into D2, one 16-column slice at a time
+      const float* src = w.s_bnd + so + (int64_t)row * D;
+#pragma unroll 1
+      for (int g = 0; g < D / 32; ++g) {
+        const int c0 = cs0 + 16 * g;
+        float v[16];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const float4 f = *reinterpret_cast<const float4*>(src + c0 + 4 * x);
+          v[4 * x] = f.x; v[4 * x + 1] = f.y; v[4 * x + 2] = f.z; v[4 * x + 3] = f.w;
+        }
+        store_split16(A1h, A1l, row, c0, D, v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = __fmul_rn(g0, v[e]);
+        tmem_st16(tlane + D2_COL + c0, v);
+      }
+      tmem_st_wait();
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    if (t == 0) {  // D1 = S Wd^T (three split terms)
+      fence_after_sync();
+      const uint32_t a_hi = smem_u32(A1h), a_lo = smem_u32(A1l);
+      const uint32_t w_hi = smem_u32(stg), w_lo = w_hi + TILE;
+      const uint32_t sbo = (D / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t a = term == 2 ? a_lo : a_hi;
+        const uint32_t b = term == 1 ? w_lo : w_hi;
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16(tbase + D1_COL, make_desc(a + kk * 256, 128, sbo), make_desc(b + kk * 256, 128, sbo),
+                   idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(bar);
+    }
+    pending = true;
+    wait_mma();
+    if (!ok) break;
+    fence_after_sync();
+#pragma unroll
+    for (int s1 = 0; s1 < C / 2; s1 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
+      float v[16];
+      tmem_ld16(tlane + D1_COL + us0 + s1, v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s1 + e], v[e]);
+      store_split16(A2h, A2l, row, us0 + s1, C, v);
+    }
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
+    if (t == 0) {  // D2 += Vd^T K (two split terms)
+      fence_after_sync();
+      const uint32_t k_img = smem_u32(KT);
+      const uint32_t sbo = (C / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t a = smem_u32(term == 0 ? A2h : A2l);
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16(tbase + D2_COL, make_desc(a + kk * 256, 128, sbo), make_desc(k_img + kk * 256, 128, sbo),
+                   idesc_bf16(128, D), 1u);
+      }
+      mma_commit(bar);
+    }
+    pending = true;
+    wait_mma();
+    if (!ok) break;
+    fence_after_sync();
+    {  // S^(1) -> s_bnd and s_run through a per-warp staging tile over the dead Vd^T operand,
+       // so that each store instruction writes 8 rows x 64 contiguous bytes
+      float* tile = reinterpret_cast<float*>(A2h) + warp * (32 * 20);
+      const int lane = t & 31, rq = (warp & 3) * 32;
+      for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + D2_COL + c0, v);
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          *reinterpret_cast<float4*>(tile + lane * 20 + 4 * x) = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+          const int rl = 8 * k2 + (lane >> 2), f = lane & 3;
+          const int64_t o = so + (int64_t)(rq + rl) * D + c0 + 4 * f;
+          const float4 x4 = *reinterpret_cast<const float4*>(tile + rl * 20 + 4 * f);
+          *reinterpret_cast<float4*>(w.s_bnd + o) = x4;
+          *reinterpret_cast<float4*>(w.s_run + o) = x4;
+        }
+        __syncwarp();
+      }
+    }
+    fence_before_sync();
+    __syncthreads();  // shared and tensor memory are reused by the next item
+  }
+  if (!ok && t == 0) {
+    set_error(hdr, GDN_DEVERR_TIMEOUT);
+    if (pending) mbar_wait(bar, phase);  // let the MMA in flight finish before releasing its memory
+  }
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, TMEM_COLS);
 }
 
 // =====================================================================  K2  ====
@@ -1703,18 +1928,23 @@ void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float*
   }
 }
 
+bool launch_resync_fused(const Dims& d, const TokenArrays& tail, const PrepWork& pw, const ChainWork& cw,
+                         WsHeader* hdr, cudaStream_t st) {
+  if (!boundary_on_tensor_cores(d)) return false;
+  if (pw.n_items <= 0) return true;
+  ensure_smem(k_resync_fused_tc, tcf::SMEM);
+  const int64_t total = pw.n_items * d.hv;
+  int64_t cap = 2 * (int64_t)sm_count();  // persistent: two CTAs per SM walk the items
+  if ((total + cap - 1) / cap > tcf::MAX_ITEMS) cap = (total + tcf::MAX_ITEMS - 1) / tcf::MAX_ITEMS;
+  k_resync_fused_tc<<<(unsigned)(total < cap ? total : cap), 256, tcf::SMEM, st>>>(d, tail, pw, cw, hdr);
+  return true;
+}
+
 void launch_chain(const Dims& d, const void* keys, const float* W, const float* U,
                   const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st) {
   if (w.N <= 0) return;
   if (boundary_on_tensor_cores(d)) {
     const int64_t total = (int64_t)w.N * d.hv;
-    if (!w.seqs) {  // decode resync: single steps, two CTAs per SM
-      ensure_smem(k_resync_tc, tcr::SMEM);
-      int64_t cap = 2 * (int64_t)sm_count();
-      if ((total + cap - 1) / cap > tcr::MAX_ITEMS) cap = (total + tcr::MAX_ITEMS - 1) / tcr::MAX_ITEMS;
-      k_resync_tc<<<(unsigned)(total < cap ? total : cap), 256, tcr::SMEM, st>>>(d, W, U, gamma, w, hdr);
-      return;
-    }
     ensure_smem(k_chain_tc, tcc::SMEM);
     int64_t cap = total;
     if ((total + cap - 1) / cap > 128) cap = (total + 127) / 128;  // at most 128 items per CTA

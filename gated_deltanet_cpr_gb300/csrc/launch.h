@@ -91,6 +91,11 @@ struct ChainWork {
   // wait runs out and the CTA records GDN_DEVERR_TIMEOUT, frees its tensor memory and exits
   int fault_wait;
 };
+// K1c: the decode resync's pre-pass and boundary step as one kernel on the tensor cores
+// (the same values as launch_prep followed by launch_chain).  Returns false, launching
+// nothing, for shapes without the tensor-core boundary path.
+bool launch_resync_fused(const Dims& d, const TokenArrays& tail, const PrepWork& pw, const ChainWork& cw,
+                         WsHeader* hdr, cudaStream_t st);
 void launch_chain(const Dims& d, const void* keys, const float* W, const float* U,
                   const float* gamma, const ChainWork& w, WsHeader* hdr, cudaStream_t st);
 

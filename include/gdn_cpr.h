@@ -295,7 +295,7 @@ gdn_status gdn_cpr_policy_digest(const gdn_cpr_shape *shape, unsigned char diges
  * adds the number of kernels it launched to *kernels.  Stages:
  *   prefill / fwd : 1 work list, 2 boundary pre-pass, 3 boundary chain, 4 intra-chunk
  *                   recurrence, 5 cache tail (prefill with a cache only)
- *   decode_step   : 1 token step, 2 resync pre-pass, 3 resync chain, 4 position advance
+ *   decode_step   : 1 token step, 2 resync (pre-pass and boundary step), 3 position advance
  *   bwd           : see gdn_cpr_bwd's stages in the implementation notes
  * The structure must stay valid while set.  Has no effect on results.                   */
 typedef struct {
