@@ -49,11 +49,11 @@ SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
 # reported only while the kernel's source (its function text plus common.cuh) hashes to the
 # value it had when the counters were taken; after any change it is null until recaptured.
 NCU_TRAFFIC = {
-    # 202,427,136 + 21,451,008 B for one 4096-token sequence x 32 value heads
-    "k_intra": {"src_sha": "a8a39bb5e32bb4ba", "bytes_per_unit": (202427136 + 21451008) / (4096 * 32),
+    # 202,414,592 + 21,460,224 B for one 4096-token sequence x 32 value heads
+    "k_intra": {"src_sha": "f0a18de335243fe2", "bytes_per_unit": (202414592 + 21460224) / (4096 * 32),
                 "unit": "token-head"},
-    # 541,318,400 + 482,635,520 B for the full 256-slot x 32-head launch (one-pass capture)
-    "k_decode": {"src_sha": "96c57dc03655655e", "bytes_per_unit": (541318400 + 482635520) / (256 * 32),
+    # 541,331,968 + 482,812,160 B for the full 256-slot x 32-head launch (one-pass capture)
+    "k_decode": {"src_sha": "e6c9318da9ca39cb", "bytes_per_unit": (541331968 + 482812160) / (256 * 32),
                  "unit": "slot-head"},
 }
 KERNEL_TEXT = {  # file, first line of the kernel, first line after it

@@ -366,14 +366,14 @@ __device__ __forceinline__ void blocked_unit_lower_inverse(const float* A, int C
   }
 }
 
-// The same inverse for C = 64 on 256 threads, with the same operations in the same order:
-// thread t takes, in round `off`, the elements e = t + 256 q (q = 0 .. 3 - off) of the
-// generic loop (all at the same (ii, rr), so their sums have the same length) and runs them
-// side by side; every sum is unrolled over its longest length with a per-lane select in
-// place of the loop bounds (a skipped term leaves the accumulator unchanged, so each
-// accumulator sees exactly the generic sequence of fma).  Operands outside a sum's range are
-// read (inside the matrices) and discarded.  A compiler-only fence every 8 terms bounds the
-// loads held in registers.
+// The same inverse for C = 64 on 256 threads, with the same operations in the same order.
+// The off-diagonal rounds are bound by shared-memory loads (two per fma when every thread
+// owns one element), so a thread owns a 2 x 2 tile of one block instead (rows ii, ii + 8,
+// columns rr, rr + 8; round `off` has 4 - off blocks, 64 threads each) and every value it
+// loads feeds two fma.  Each element's sum is still the generic loop's sequence of fma: it
+// is unrolled over its longest length with a per-element select in place of the loop
+// bounds (a skipped term leaves the accumulator unchanged).  Operands outside a sum's range
+// are read (inside the matrices) and discarded.
 __device__ __forceinline__ void unit_lower_inverse64(const float* A, int CPA, float* Tm, int CPT, float* Xs) {
   constexpr int TB = 16, C = 64, NB = C / TB;
   const int t = threadIdx.x;
@@ -395,52 +395,53 @@ __device__ __forceinline__ void unit_lower_inverse64(const float* A, int CPA, fl
       if (k >= rr) Tm[(rb + k) * CPT + r] = col[k];
   }
   __syncthreads();
-  const int ii = t / TB, rr = t % TB;
+  const int q = t >> 6, ii = (t >> 3) & 7, rr = t & 7;  // block q of the round, tile corner
 #pragma unroll
   for (int off = 1; off < NB; ++off) {
-    constexpr int QMAX = NB - 1;
-    const int nq = NB - off;
-    float acc[QMAX];
+    const bool live = q < NB - off;
+    const int I = off + q, J = I - off;  // block row I, block column J
+    if (live) {
+      // X[e] = sum_{m = r}^{16 I - 1} A[i][m] T[m][r],  m = 16 J + k,  k = rr .. 16 off - 1
+      const float* a0 = A + (I * TB + ii) * CPA + J * TB;
+      const float* a1 = a0 + 8 * CPA;
+      const float* t0 = Tm + (J * TB) * CPT + J * TB + rr;
+      float x00 = 0.f, x01 = 0.f, x10 = 0.f, x11 = 0.f;
 #pragma unroll
-    for (int q = 0; q < QMAX; ++q) acc[q] = 0.f;
-    // X[e] = sum_{m = r}^{16 I - 1} A[i][m] T[m][r],  m = 16 (I - off) + k,  k = rr .. 16 off - 1
-#pragma unroll
-    for (int k = 0; k < off * TB; ++k) {
-#pragma unroll
-      for (int q = 0; q < QMAX; ++q) {
-        if (q < nq) {
-          const int I = off + q, i = I * TB + ii, r = (I - off) * TB + rr, m = (I - off) * TB + k;
-          const float v = __fmaf_rn(A[i * CPA + m], Tm[m * CPT + r], acc[q]);
-          acc[q] = (k >= rr) ? v : acc[q];
-        }
+      for (int k = 0; k < off * TB; ++k) {
+        const float p0 = a0[k], p1 = a1[k], y0 = t0[k * CPT], y1 = t0[k * CPT + 8];
+        x00 = (k >= rr) ? __fmaf_rn(p0, y0, x00) : x00;
+        x01 = (k >= rr + 8) ? __fmaf_rn(p0, y1, x01) : x01;
+        x10 = (k >= rr) ? __fmaf_rn(p1, y0, x10) : x10;
+        x11 = (k >= rr + 8) ? __fmaf_rn(p1, y1, x11) : x11;
+        if ((k & 7) == 7) asm volatile("" ::: "memory");
       }
-      if ((k & 7) == 7) asm volatile("" ::: "memory");
+      float* xs = Xs + q * 256;
+      xs[ii * TB + rr] = x00;
+      xs[ii * TB + rr + 8] = x01;
+      xs[(ii + 8) * TB + rr] = x10;
+      xs[(ii + 8) * TB + rr + 8] = x11;
     }
-#pragma unroll
-    for (int q = 0; q < QMAX; ++q)
-      if (q < nq) Xs[q * 256 + t] = acc[q];
     __syncthreads();
-    // T[i][r] = -sum_{m = 16 I}^{i} T[i][m] X[m - 16 I][rr],  m = 16 I + k,  k = 0 .. ii
+    if (live) {
+      // T[i][r] = -sum_{m = 16 I}^{i} T[i][m] X[m - 16 I][rr],  m = 16 I + k,  k = 0 .. ii
+      const float* p0r = Tm + (I * TB + ii) * CPT + I * TB;
+      const float* p1r = p0r + 8 * CPT;
+      const float* xq = Xs + q * 256 + rr;
+      float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll
-    for (int q = 0; q < QMAX; ++q) acc[q] = 0.f;
-#pragma unroll
-    for (int k = 0; k < TB; ++k) {
-#pragma unroll
-      for (int q = 0; q < QMAX; ++q) {
-        if (q < nq) {
-          const int I = off + q, i = I * TB + ii;
-          const float v = __fmaf_rn(Tm[i * CPT + I * TB + k], Xs[q * 256 + k * TB + rr], acc[q]);
-          acc[q] = (k <= ii) ? v : acc[q];
-        }
+      for (int k = 0; k < TB; ++k) {
+        const float p0 = p0r[k], p1 = p1r[k], x0 = xq[k * TB], x1 = xq[k * TB + 8];
+        y00 = (k <= ii) ? __fmaf_rn(p0, x0, y00) : y00;
+        y01 = (k <= ii) ? __fmaf_rn(p0, x1, y01) : y01;
+        y10 = (k <= ii + 8) ? __fmaf_rn(p1, x0, y10) : y10;
+        y11 = (k <= ii + 8) ? __fmaf_rn(p1, x1, y11) : y11;
+        if ((k & 7) == 7) asm volatile("" ::: "memory");
       }
-      if ((k & 7) == 7) asm volatile("" ::: "memory");
-    }
-#pragma unroll
-    for (int q = 0; q < QMAX; ++q) {
-      if (q < nq) {
-        const int I = off + q, i = I * TB + ii, r = (I - off) * TB + rr;
-        Tm[i * CPT + r] = -acc[q];
-      }
+      float* o0 = Tm + (I * TB + ii) * CPT + J * TB + rr;
+      o0[0] = -y00;
+      o0[8] = -y01;
+      o0[8 * CPT] = -y10;
+      o0[8 * CPT + 8] = -y11;
     }
     __syncthreads();
   }
