@@ -790,10 +790,11 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       mma_phase ^= 1u;
       mma_pending = false;
       fence_after_sync();
+      float d1[C / 2];  // this thread's half of its D1 row, one load
+      tmem_ld32(tlane + D1_COL + us0, d1);
 #pragma unroll
       for (int s1 = 0; s1 < C / 2; s1 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
-        float v[16];
-        tmem_ld16(tlane + D1_COL + us0 + s1, v);
+        float* v = d1 + s1;
 #pragma unroll
         for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ud[s1 + e], v[e]);
         store_split16(A2h, A2l, row, us0 + s1, C, v);
@@ -827,9 +828,11 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
         // region, so that each store instruction writes 8 rows x 64 contiguous bytes
         float* tile = reinterpret_cast<float*>(A2h) + warp * (32 * 20);
         const int lane = t & 31, rq = (warp & 3) * 32;
+        float s1v[D / 2];  // this thread's half of its state row, one load
+        tmem_ld64(tlane + D2_COL + cs0, s1v);
+#pragma unroll
         for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
-          float v[16];
-          tmem_ld16(tlane + D2_COL + c0, v);
+          float* v = s1v + (c0 - cs0);
 #pragma unroll
           for (int x = 0; x < 4; ++x)
             *reinterpret_cast<float4*>(tile + lane * 20 + 4 * x) = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
