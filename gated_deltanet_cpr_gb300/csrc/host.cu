@@ -207,6 +207,10 @@ struct Stages {
   }
   Stages(const Stages&) = delete;
   Stages& operator=(const Stages&) = delete;
+  // a kernel launched at the start of the first stage (counted, no event of its own)
+  void count(int kernels) {
+    if (t_profile) t_profile->kernels += kernels;
+  }
   void mark(int kernels) {
     if (open) nvtxRangePop();
     open = names && names[next] != nullptr;
@@ -281,8 +285,9 @@ gdn_status run_forward(const gdn_cpr_shape* shape, const void* q, const void* k,
   float* bnd = saved_bnd ? saved_bnd : reinterpret_cast<float*>(at(ws, L.bnd));
   TokenArrays in{q, k, v, g, beta, T};
 
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(st, kFwdStages);
+  launch_reset_header(hdr, st);  // error word and work-list flag of this call
+  stg.count(1);
   launch_worklist(cu_dev, N, (int)T, d.C, n_chunks, hash, chunks, seqs, hdr, st);
   stg.mark(1);
 
@@ -373,8 +378,9 @@ gdn_status run_decode(const gdn_cpr_shape* shape, const void* q, const void* k, 
   float* U = reinterpret_cast<float*>(at(ws, L.U));
   float* gamma = reinterpret_cast<float*>(at(ws, L.gamma));
   TokenArrays in{q, k, v, g, beta, N};
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(stream, kDecodeStages);
+  launch_reset_header(hdr, stream);  // error word and work-list flag of this call
+  stg.count(1);
 
   DecodeWork dw{};
   dw.N = N;
@@ -552,8 +558,9 @@ gdn_status gdn_cpr_bwd(const gdn_cpr_shape* shape, const void* q, const void* k,
   ChunkRec* chunks = reinterpret_cast<ChunkRec*>(at(ws, L.chunks));
   SeqRec* seqs = reinterpret_cast<SeqRec*>(at(ws, L.seqs));
   TokenArrays in{q, k, v, g, beta, T};
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), stream) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(stream, kBwdStages);
+  launch_reset_header(hdr, stream);  // error word and work-list flag of this call
+  stg.count(1);
   launch_worklist(cu_seqlens_dev, N, (int)T, d.C, n_chunks, hash, chunks, seqs, hdr, stream);
   stg.mark(1);
   launch_bwd(d, in, dO, chunks, seqs, N, n_chunks, T, saved_bnd, dstate_out, dstate_in,
@@ -619,8 +626,9 @@ gdn_status gdn_cpr_prefill_continue(const gdn_cpr_shape* shape, const void* q, c
   TokenArrays vin{at(ws, L.q), at(ws, L.k), at(ws, L.v), reinterpret_cast<const float*>(at(ws, L.g)),
                   reinterpret_cast<const float*>(at(ws, L.beta)), vT};
 
-  if (cudaMemsetAsync(hdr, 0, sizeof(WsHeader), st) != cudaSuccess) return GDN_ERR_CUDA;
   Stages stg(st, kContStages);
+  launch_reset_header(hdr, st);  // error word and work-list flag of this call
+  stg.count(1);
   launch_continue_prep(cu_seqlens_dev, slot_dev, cache->pos, cache->slots, N, d.C, vcu, rlen, base, hdr, st);
   launch_worklist(vcu, N, (int)vT, d.C, vchunks, vhash, chunks, seqs, hdr, st);
   launch_continue_gather(d, in, cu_seqlens_dev, vcu, rlen, slot_dev, N, vT, *cache, vin, hdr, st);

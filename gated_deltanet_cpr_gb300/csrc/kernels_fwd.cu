@@ -1822,6 +1822,14 @@ __global__ void k_advance(int N, const int32_t* __restrict__ slot, int slots, in
   }
 }
 
+// The workspace header zeroed by one small kernel: a memset node costs several microseconds
+// more per call in a replayed CUDA graph, which a decode step's few-microsecond kernels feel.
+__global__ void k_reset_header(WsHeader* hdr) { reinterpret_cast<int32_t*>(hdr)[threadIdx.x] = 0; }
+
+void launch_reset_header(WsHeader* hdr, cudaStream_t st) {
+  k_reset_header<<<1, sizeof(WsHeader) / sizeof(int32_t), 0, st>>>(hdr);
+}
+
 void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, const WsHeader* hdr, cudaStream_t st) {
   k_advance<<<(N + 255) / 256, 256, 0, st>>>(N, slot, slots, pos, hdr);
 }

@@ -147,6 +147,9 @@ struct DecodeWork {
 void launch_decode(const Dims& d, const TokenArrays& in, const DecodeWork& w, WsHeader* hdr,
                    cudaStream_t st);
 
+// Zero the workspace header (first kernel of every call).
+void launch_reset_header(WsHeader* hdr, cudaStream_t st);
+
 // pos[slot[n]] += 1 for every valid n (last kernel of a decode step), unless the step was
 // refused (GDN_DEVERR_POS_HOST in the error word).
 void launch_advance(int N, const int32_t* slot, int slots, int32_t* pos, const WsHeader* hdr, cudaStream_t st);
