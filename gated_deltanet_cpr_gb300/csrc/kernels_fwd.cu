@@ -969,56 +969,38 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
   const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(in.v);
   const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
 
+  // Item lj's K rows (as the image in R0), V rows (staged in the A region), g and beta by
+  // asynchronous copies, 16 bytes a piece; item 0's before the loop, every later one's as
+  // soon as the previous item's W and U^T products have consumed those regions, so that
+  // they land while that item writes its outputs.
+  auto load_item = [&](int lj) {
+    const int64_t wj = s_list[lj];
+    const int hj = (int)(wj % dm.hv), hqj = hj / (dm.hv / dm.hqk);
+    const int64_t tj = s_tok0[lj];
+    const __nv_bfloat16* kbj = kin + tj * kstride + (int64_t)hqj * D;
+    const __nv_bfloat16* vbj = vin + tj * vstride + (int64_t)hj * D;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {  // C * D / 8 = 1024 pieces of 16 bytes
+      int r, c0;
+      tc::kmajor_piece(t + it * 256, D, r, c0);
+      tc::cp_async16(R0 + tc::kmajor_off(r, c0, D), kbj + r * kstride + c0);
+      tc::cp_async16(reinterpret_cast<unsigned char*>(A) + tc::kmajor_off(r, c0, D), vbj + r * vstride + c0);
+    }
+    if (t < C) {
+      tc::cp_async4(gs + t, in.g + (tj + t) * dm.hv + hj);
+      tc::cp_async4(bs + t, in.beta + (tj + t) * dm.hv + hj);
+    }
+    tc::cp_async_commit();
+  };
+  load_item(0);
+
   for (int li = 0; li < count && ok; ++li) {
     const int64_t wi = s_list[li];
     const int64_t item = wi / dm.hv;
     const int h = (int)(wi % dm.hv);
-    const int hq = h / (dm.hv / dm.hqk);
-    const int64_t tok0 = s_tok0[li];
-    const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
-    const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
-    if (li + 1 < count) {  // L2 prefetch of the next item's K and V rows, g and beta (128-byte lines)
-      const int h2 = (int)(s_list[li + 1] % dm.hv), hq2 = h2 / (dm.hv / dm.hqk);
-      const int64_t tk = s_tok0[li + 1];
-      for (int q = t; q < 2 * C; q += 256) {  // a row of D bf16 = two lines
-        const int r = q >> 1, part = (q & 1) * (D / 2);
-        tc::prefetch_l2(kin + (tk + r) * kstride + (int64_t)hq2 * D + part);
-        tc::prefetch_l2(vin + (tk + r) * vstride + (int64_t)h2 * D + part);
-      }
-      if (t < C) {
-        tc::prefetch_l2(in.g + (tk + t) * dm.hv + h2);
-        tc::prefetch_l2(in.beta + (tk + t) * dm.hv + h2);
-      }
-    }
 
-    // 1. K rows and V rows (staged in the A region, free until the Gram readout) straight
-    // from global memory, g and beta: every load issued before the first store
-    {
-      uint4 kr[4], vr[4];
-      float g0 = 0.f, b0 = 0.f;
-      if (t < C) {
-        g0 = in.g[(tok0 + t) * dm.hv + h];
-        b0 = in.beta[(tok0 + t) * dm.hv + h];
-      }
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {  // C * D / 8 = 1024 pieces of 16 bytes
-        int r, c0;
-        tc::kmajor_piece(t + it * 256, D, r, c0);
-        kr[it] = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
-        vr[it] = *reinterpret_cast<const uint4*>(vb + r * vstride + c0);
-      }
-      if (t < C) {
-        gs[t] = g0;
-        bs[t] = b0;
-      }
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        int r, c0;
-        tc::kmajor_piece(t + it * 256, D, r, c0);
-        *reinterpret_cast<uint4*>(R0 + tc::kmajor_off(r, c0, D)) = kr[it];
-        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(A) + tc::kmajor_off(r, c0, D)) = vr[it];
-      }
-    }
+    // 1. this item's K, V, g and beta in shared memory
+    tc::cp_async_wait_all();
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -1134,6 +1116,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
       phase ^= 1u;
     }
     tc::fence_after_sync();
+    if (li + 1 < count) load_item(li + 1);  // R0, the A region, g and beta are free now
     float* Wo = Wout + (item * dm.hv + h) * (int64_t)prep_w_floats(C, D);
     float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
     unsigned char* img = reinterpret_cast<unsigned char*>(Wo);
@@ -1178,6 +1161,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     tc::fence_before_sync();
     __syncthreads();  // shared memory and tensor memory are reused by the next item
   }
+  tc::cp_async_wait_all();  // no copy of this thread still in flight
   if (!ok && t == 0) {
     set_error(hdr, GDN_DEVERR_TIMEOUT);
     tc::mbar_wait(bar, phase);  // let the MMA in flight finish before releasing its memory
@@ -1300,71 +1284,43 @@ __global__ void __launch_bounds__(256, 2) k_resync_fused_tc(Dims dm, TokenArrays
   const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(in.v);
   const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
 
-  // L2 prefetch of an item's reads: K and V rows, g, beta of the slot's chunk tail and (state)
-  // its boundary state; 128-byte lines spread over the threads
-  auto prefetch_item = [&](int64_t wj, bool state) {
-    const int64_t n2 = wj / dm.hv;
-    const int h2 = (int)(wj % dm.hv), hq2 = h2 / (dm.hv / dm.hqk);
-    const int64_t tk = (int64_t)pw.slot[n2] * C;
-    for (int q = t; q < 2 * C; q += 256) {  // a row of D bf16 = two lines
-      const int r = q >> 1, part = (q & 1) * (D / 2);
-      prefetch_l2(kin + (tk + r) * kstride + (int64_t)hq2 * D + part);
-      prefetch_l2(vin + (tk + r) * vstride + (int64_t)h2 * D + part);
+  // Item lj's K rows (as the image in R0), V rows (staged in the A region), g and beta of the
+  // slot's chunk tail by asynchronous copies, 16 bytes a piece: item 0's before the loop,
+  // every later one's as soon as the previous item's first boundary product has consumed
+  // the state operand those regions lie in.  Its boundary state goes to L2 meanwhile.
+  auto load_item = [&](int lj) {
+    const int64_t wj = s_list[lj];
+    const int64_t nj = wj / dm.hv;
+    const int hj = (int)(wj % dm.hv), hqj = hj / (dm.hv / dm.hqk);
+    const int64_t tj = (int64_t)pw.slot[nj] * C;
+    const __nv_bfloat16* kbj = kin + tj * kstride + (int64_t)hqj * D;
+    const __nv_bfloat16* vbj = vin + tj * vstride + (int64_t)hj * D;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {  // C * D / 8 = 1024 pieces of 16 bytes
+      int r, c0;
+      kmajor_piece(t + it * 256, D, r, c0);
+      cp_async16(R0 + kmajor_off(r, c0, D), kbj + r * kstride + c0);
+      cp_async16(reinterpret_cast<unsigned char*>(A) + kmajor_off(r, c0, D), vbj + r * vstride + c0);
     }
     if (t < C) {
-      prefetch_l2(in.g + (tk + t) * dm.hv + h2);
-      prefetch_l2(in.beta + (tk + t) * dm.hv + h2);
+      cp_async4(gs + t, in.g + (tj + t) * dm.hv + hj);
+      cp_async4(bs + t, in.beta + (tj + t) * dm.hv + hj);
     }
-    if (state) {
-      const float* sp = w.s_bnd + ((int64_t)pw.slot[n2] * dm.hv + h2) * SZ;
-      for (int q = t; q < D * D / 32; q += 256) prefetch_l2(sp + 32 * q);
-    }
-  };
-  if (count > 0) {
-    const int64_t w0 = s_list[0];
-    const float* sp = w.s_bnd + ((int64_t)pw.slot[w0 / dm.hv] * dm.hv + (int)(w0 % dm.hv)) * SZ;
+    cp_async_commit();
+    const float* sp = w.s_bnd + ((int64_t)pw.slot[nj] * dm.hv + hj) * SZ;
     for (int q = t; q < D * D / 32; q += 256) prefetch_l2(sp + 32 * q);
-  }
+  };
+  load_item(0);
 
   for (int li = 0; li < count && ok; ++li) {
     const int64_t wi = s_list[li];
     const int64_t n = wi / dm.hv;
     const int h = (int)(wi % dm.hv);
-    const int hq = h / (dm.hv / dm.hqk);
     const int sl = pw.slot[n];
-    const int64_t tok0 = (int64_t)sl * C;  // the slot's chunk tail
-    if (li + 1 < count) prefetch_item(s_list[li + 1], true);
-    const __nv_bfloat16* kb = kin + tok0 * kstride + (int64_t)hq * D;
-    const __nv_bfloat16* vb = vin + tok0 * vstride + (int64_t)h * D;
 
     // ---- the pre-pass, k_prep_tc's steps
-    // 1. K rows image, V rows (in the A region), g, beta: every load issued before the first store
-    {
-      uint4 kr[4], vr[4];
-      float g0 = 0.f, b0 = 0.f;
-      if (t < C) {
-        g0 = in.g[(tok0 + t) * dm.hv + h];
-        b0 = in.beta[(tok0 + t) * dm.hv + h];
-      }
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {  // C * D / 8 = 1024 pieces of 16 bytes
-        int r, c0;
-        kmajor_piece(t + it * 256, D, r, c0);
-        kr[it] = *reinterpret_cast<const uint4*>(kb + r * kstride + c0);
-        vr[it] = *reinterpret_cast<const uint4*>(vb + r * vstride + c0);
-      }
-      if (t < C) {
-        gs[t] = g0;
-        bs[t] = b0;
-      }
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        int r, c0;
-        kmajor_piece(t + it * 256, D, r, c0);
-        *reinterpret_cast<uint4*>(R0 + kmajor_off(r, c0, D)) = kr[it];
-        *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(A) + kmajor_off(r, c0, D)) = vr[it];
-      }
-    }
+    // 1. this item's K, V, g and beta in shared memory
+    cp_async_wait_all();
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
@@ -1541,6 +1497,7 @@ __global__ void __launch_bounds__(256, 2) k_resync_fused_tc(Dims dm, TokenArrays
     wait_mma();
     if (!ok) break;
     fence_after_sync();
+    if (li + 1 < count) load_item(li + 1);  // the state operand is consumed
 #pragma unroll
     for (int s1 = 0; s1 < C / 2; s1 += 16) {  // Vd^T row = Ud column - D1 row, split into A2
       float v[16];
@@ -1594,6 +1551,7 @@ __global__ void __launch_bounds__(256, 2) k_resync_fused_tc(Dims dm, TokenArrays
     fence_before_sync();
     __syncthreads();  // shared and tensor memory are reused by the next item
   }
+  cp_async_wait_all();  // no copy of this thread still in flight
   if (!ok && t == 0) {
     set_error(hdr, GDN_DEVERR_TIMEOUT);
     if (pending) mbar_wait(bar, phase);  // let the MMA in flight finish before releasing its memory

@@ -93,6 +93,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Asynchronous global -> shared copies (generic proxy) that a thread issues and later waits
+// for: 16 bytes (both addresses 16-byte aligned) or 4 bytes.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// every copy this thread issued has landed (the CTA still needs a barrier to see the others')
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Hint: bring the 128-byte line holding p into L2 (no register result, no wait).  A CTA that
 // walks items issues these for its next item's operands, so that their loads hit L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
