@@ -1598,10 +1598,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   if (t < C) a.b.G[ch * C + t] = Gs[t];
   // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs (V^T is built), by all
   // threads; the readout multiplies in place
-  for (int e = t; e < C * C; e += 256) {
-    const int i = e / C, s = e % C;
-    if (i > s) A[i * QCP + s] = __fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s])));
-  }
+  tc::decay_matrix64(A, QCP, bs, Gs);
   wait_mma();
   if (ok && (warp & 3) < 2) {
     const int i = lrow;

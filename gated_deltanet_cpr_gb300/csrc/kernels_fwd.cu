@@ -1030,10 +1030,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     }
     // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs (the V rows staged
     // there are transposed), by all threads; the readout multiplies in place
-    for (int e = t; e < C * C; e += 256) {
-      const int i = e / C, s = e % C;
-      if (i > s) A[i * CP + s] = __fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s])));
-    }
+    tc::decay_matrix64(A, CP, bs, Gs);
     {
       const bool done = tc::mbar_wait(bar, phase);
       ok = __syncthreads_and(done) != 0;
@@ -1350,10 +1347,7 @@ __global__ void __launch_bounds__(256, 2) k_resync_fused_tc(Dims dm, TokenArrays
       dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
     }
     // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs; the readout multiplies
-    for (int e = t; e < C * C; e += 256) {
-      const int i = e / C, s = e % C;
-      if (i > s) A[i * CP + s] = __fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s])));
-    }
+    tc::decay_matrix64(A, CP, bs, Gs);
     wait_mma();
     if (!ok) break;
     fence_after_sync();

@@ -93,6 +93,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// A[i][s] = beta_i e^{G_i - G_s} for s < i, C = 64, all 256 threads of the block.  Rows i
+// and 63 - i are paired (63 entries between them) and each pair gets 8 threads, so every
+// thread forms 7 or 8 entries and no lane idles on the upper triangle.
+__device__ __forceinline__ void decay_matrix64(float* A, int CPA, const float* bs, const float* Gs) {
+  const int p = threadIdx.x >> 3, q = threadIdx.x & 7;  // row pair p = 0 .. 31
+  for (int e = q; e < 63; e += 8) {
+    const int i = e < p ? p : 63 - p;
+    const int s = e < p ? e : e - p;
+    A[i * CPA + s] = __fmul_rn(bs[i], expf(__fsub_rn(Gs[i], Gs[s])));
+  }
+}
+
 // Asynchronous global -> shared copies (generic proxy) that a thread issues and later waits
 // for: 16 bytes (both addresses 16-byte aligned) or 4 bytes.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
