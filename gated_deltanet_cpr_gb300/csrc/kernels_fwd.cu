@@ -1141,6 +1141,10 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
           *reinterpret_cast<uint4*>(img + TILE + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
+    } else {  // the other warps meanwhile: the K^T image
+      const int th = (warp >> 2) * 64 + ((warp & 3) - 2) * 32 + (t & 31);  // 0 .. 127
+      for (int q = th; q < (int)(TILE / 16); q += 128)
+        reinterpret_cast<uint4*>(img + 2 * TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
     }
     {  // Ud[i][e] = dec_i U^T[e][i]: lane e, columns i
       const int e = (warp & 3) * 32 + (t & 31);
@@ -1152,8 +1156,6 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
         for (int x = 0; x < 16; ++x) Uo[(int64_t)(i0 + x) * D + e] = __fmul_rn(dec[i0 + x], v[x]);
       }
     }
-    for (int q = t; q < (int)(TILE / 16); q += 256)
-      reinterpret_cast<uint4*>(img + 2 * TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
     if (t == 0) gamma_out[item * dm.hv + h] = expf(Gs[C - 1]);
     tc::fence_before_sync();
     __syncthreads();  // shared memory and tensor memory are reused by the next item
