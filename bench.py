@@ -851,23 +851,36 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
     produced = {p: mk() for p in ("pre", "dec", "trn")}
     read_back = {p: mk() for p in ("pre", "dec", "trn")}
 
+    copy_ev = {"up": [], "down": []}  # (start, end) of every upload / read-back of the timed run
+
+    def timed(kind, stream):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        copy_ev[kind].append((a_, b_))
+        return a_, b_
+
     def upload(b, after=None):
         with torch.cuda.stream(up):
             if after is not None:
                 up.wait_event(after)
             up.wait_event(in_free[b])
+            ea, eb = timed("up", up)
+            ea.record(up)
             for n in host:
                 bufs[b][n].copy_(host[n], non_blocking=True)
             for n in dhost:
                 dq_bufs[b][n].copy_(dhost[n], non_blocking=True)
+            eb.record(up)
             up_done[b].record(up)
 
     def download(part):
         with torch.cuda.stream(down):
             down.wait_event(produced[part])
+            ea, eb = timed("down", down)
+            ea.record(down)
             for n, v in result_tensors(part).items():
                 v.record_stream(down)
                 res_host[n].copy_(v, non_blocking=True)
+            eb.record(down)
             read_back[part].record(down)
 
     def run(n_steps, e_start=None):
@@ -900,12 +913,18 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
     run(max(1, args.warmup))
     torch.cuda.synchronize(dev)
     barrier(world)
+    copy_ev["up"].clear()
+    copy_ev["down"].clear()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
     run(args.steps, e0)
     e1.record(comp)
     torch.cuda.synchronize(dev)
     barrier(world)
+    # how long the copies of a step took while the step computed (against the serial rates
+    # measured below, this shows whether the box slowed them down)
+    up_ms = sum(a_.elapsed_time(b_) for a_, b_ in copy_ev["up"]) / args.steps
+    down_ms = sum(a_.elapsed_time(b_) for a_, b_ in copy_ev["down"]) / args.steps
     t.update(t0)
     # every step recomputes the same results (bit-exact), so the host copies must equal the
     # device results: a race between the streams would show here
@@ -934,6 +953,7 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
     return {"value": world * step_tok / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "h2d_gbs": bw["h2d"], "d2h_gbs": bw["d2h"], "copy_ms_per_step_serial": copy_ms,
+            "h2d_ms_per_step_during_run": up_ms, "d2h_ms_per_step_during_run": down_ms,
             "exposed_ms_per_step": ms - compute_ms,
             "pipelined": "inputs of step i+1 uploaded during step i (two input buffers); "
                          "results read back on a second copy stream as each part finishes"}
