@@ -1731,7 +1731,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     }
   }
   // ---- 5. Qt = diag(e^G) Q - P W: A = P (rows i), B = W^T (rows c)
-  float dov[4][8];  // dO^T pieces for step 6, loaded while the product runs
+  // dO for step 6, loaded while the product runs: bf16 dO as rows (four 16-byte pieces per
+  // thread, held bit for bit in dov[it][0..3]) for an image transposed in shared memory; fp32
+  // dO as dO^T pieces to split
+  float dov[4][8];
   if (ok) {
     sync_for_mma();
     if (t == 0) {
@@ -1739,7 +1742,21 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       mma_terms(tb + COL_QT, smem_u32(TKh), smem_u32(TKl), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
       mma_commit(bar);
     }
-    load_dO_T(dov, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+    if (dm.out_bf16) {
+      const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(a.dO) + (tok0 * dm.hv + h) * D;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, c0;
+        kmajor_piece(t + it * 256, D, r, c0);
+        const uint4 x = r < n ? *reinterpret_cast<const uint4*>(ob + (int64_t)r * dm.hv * D + c0) : z4;
+        dov[it][0] = __uint_as_float(x.x);
+        dov[it][1] = __uint_as_float(x.y);
+        dov[it][2] = __uint_as_float(x.z);
+        dov[it][3] = __uint_as_float(x.w);
+      }
+    } else {
+      load_dO_T(dov, a.dO, false, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+    }
     for (int q = t; q < (int)(2 * TILE / 16); q += 256)  // W^T images for the reverse chain
       reinterpret_cast<uint4*>(img + TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
     // P^T hi | lo (over the dead TV) -> P's slot: the big-products kernel's operand image
@@ -1772,17 +1789,41 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   // ---- 6. L = dO^T Qt: A = dO^T (rows p, K = i) over the dead K rows and P, B = Qt^T (rows q,
   // K = i) over the dead W^T
   if (ok) {
+    if (dm.out_bf16) {  // dO rows image over the dead Q rows, transposed into dO^T; dO is exact
+      unsigned char* Dr = smq + OFF_A;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, c0;
+        kmajor_piece(t + it * 256, D, r, c0);
+        *reinterpret_cast<uint4*>(Dr + kmajor_off(r, c0, D)) =
+            make_uint4(__float_as_uint(dov[it][0]), __float_as_uint(dov[it][1]), __float_as_uint(dov[it][2]),
+                       __float_as_uint(dov[it][3]));
+      }
+      __syncthreads();
+      tc::transpose_image(Ki, Dr, D, C);
+    } else {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
+        split8(Ki, TKh, kmajor_off(r, k0, C), dov[it]);
+      }
+    }
     tc::transpose_image(KT, Qrh, D, C);
     tc::transpose_image(VT, Qrl, D, C);
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
-      split8(Ki, TKh, kmajor_off(r, k0, C), dov[it]);
-    }
     sync_for_mma();
     if (t == 0) {
       fence_after_sync();
-      mma_terms(tb + COL_L, smem_u32(Ki), smem_u32(TKh), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
+      if (dm.out_bf16) {  // dO^T (Qt_hi + Qt_lo): the split's A_lo term would add exact zeros
+        const uint32_t sbo = (C / 8) * 128;
+        for (int term = 0; term < 2; ++term) {
+          const uint32_t bb = smem_u32(term == 0 ? KT : VT);
+          for (int kk = 0; kk < C / 16; ++kk)
+            mma_bf16(tb + COL_L, make_desc(smem_u32(Ki) + kk * 256, 128, sbo), make_desc(bb + kk * 256, 128, sbo),
+                     idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
+        }
+      } else {
+        mma_terms(tb + COL_L, smem_u32(Ki), smem_u32(TKh), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
+      }
       mma_commit(bar);
     }
     wait_mma();
