@@ -1208,6 +1208,28 @@ __device__ __forceinline__ void mma_terms(uint32_t d, uint32_t ahi, uint32_t alo
   }
 }
 
+// D (+)= A (B_hi + B_lo) = A_hi B_hi + A_hi B_lo: the split product when A is exact in bf16
+// (bf16 dO): its lo image would be all zeros, and the term A_lo B_hi adds exact zeros.
+__device__ __forceinline__ void mma_a_exact(uint32_t d, uint32_t a, uint32_t bhi, uint32_t blo, int K,
+                                            uint32_t idesc) {
+  const uint32_t sbo = (uint32_t)(K / 8) * 128;
+  for (int term = 0; term < 2; ++term) {
+    const uint32_t bb = term == 0 ? bhi : blo;
+    for (int kk = 0; kk < K / 16; ++kk)
+      tc::mma_bf16(d, tc::make_desc(a + kk * 256, 128, sbo), tc::make_desc(bb + kk * 256, 128, sbo), idesc,
+                   (term > 0 || kk > 0) ? 1u : 0u);
+  }
+}
+// 8 values exact in bf16 (widened bf16 inputs) as one 16-byte piece of a bf16 image
+__device__ __forceinline__ void store_bf16x8(unsigned char* img, uint32_t off, const float* v) {
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    w[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e])) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * e + 1])) << 16);
+  *reinterpret_cast<uint4*>(img + off) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   using namespace tcg;
   using namespace tc;
@@ -1369,17 +1391,24 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
         bulk_g2s(Bh, a.b.P + ch * C * C, C * C * 4, &bar[1]);
         cpending = true;
       }
+      const bool exact = dm.out_bf16;  // bf16 dO: no lo image, no A_lo term
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         int r, k0;
         kmajor_piece(t + it * 256, D, r, k0);
-        split8(Ah + 2 * IMGB, Ah + 3 * IMGB, kmajor_off(r, k0, D), v[it]);  // rows hi | lo
+        if (exact)
+          store_bf16x8(Ah + 2 * IMGB, kmajor_off(r, k0, D), v[it]);
+        else
+          split8(Ah + 2 * IMGB, Ah + 3 * IMGB, kmajor_off(r, k0, D), v[it]);  // rows hi | lo
       }
       __syncthreads();
       transpose_image(Ah, Ah + 2 * IMGB, D, C);
-      transpose_image(Ah + IMGB, Ah + 3 * IMGB, D, C);
+      if (!exact) transpose_image(Ah + IMGB, Ah + 3 * IMGB, D, C);
       issue_copies([&] {
-        mma_terms(tb + COL_1, sa_h, sa_h + IMGB, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C), 3);
+        if (exact)
+          mma_a_exact(tb + COL_1, sa_h, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C));
+        else
+          mma_terms(tb + COL_1, sa_h, sa_h + IMGB, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C), 3);
       });
     }
   }
@@ -1419,16 +1448,21 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     float v[4][8];
     load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
     build_dd<false>(Ah, Al, S0);
+    const bool exact = dm.out_bf16;  // bf16 dO: no lo image, no B_lo term
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
       int r, k0;
       kmajor_piece(t + it * 256, D, r, k0);
-      split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
+      if (exact)
+        store_bf16x8(Bh, kmajor_off(r, k0, D), v[it]);
+      else
+        split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
     }
     __syncthreads();
     transpose_image_inplace(Ah, D);
     transpose_image_inplace(Al, D);
-    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+    // A_hi B_hi (+ A_hi B_lo) + A_lo B_hi: with exact B the middle term adds exact zeros
+    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), exact ? 2 : 3); });
   }
   if (ok) {
     SplitTile<false, C, D> dut;  // dU rows, loaded while the first product runs
@@ -1813,14 +1847,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     sync_for_mma();
     if (t == 0) {
       fence_after_sync();
-      if (dm.out_bf16) {  // dO^T (Qt_hi + Qt_lo): the split's A_lo term would add exact zeros
-        const uint32_t sbo = (C / 8) * 128;
-        for (int term = 0; term < 2; ++term) {
-          const uint32_t bb = smem_u32(term == 0 ? KT : VT);
-          for (int kk = 0; kk < C / 16; ++kk)
-            mma_bf16(tb + COL_L, make_desc(smem_u32(Ki) + kk * 256, 128, sbo), make_desc(bb + kk * 256, 128, sbo),
-                     idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
-        }
+      if (dm.out_bf16) {  // dO^T (Qt_hi + Qt_lo)
+        mma_a_exact(tb + COL_L, smem_u32(Ki), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D));
       } else {
         mma_terms(tb + COL_L, smem_u32(Ki), smem_u32(TKh), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
       }
@@ -1968,7 +1996,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       int r, k0;
       kmajor_piece(t + it * 256, D, r, k0);
       const uint32_t off = kmajor_off(r, k0, D);
-      split8(ar + 32 * KB, ar + 48 * KB, off, vo[it]);
+      if (dm.out_bf16)  // exact: no lo image
+        store_bf16x8(ar + 32 * KB, off, vo[it]);
+      else
+        split8(ar + 32 * KB, ar + 48 * KB, off, vo[it]);
       *reinterpret_cast<uint4*>(ar + off) = qr[it];
       *reinterpret_cast<uint4*>(ar + 16 * KB + off) = kr[it];
     }
@@ -2022,7 +2053,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   };
   // ---- products 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64
   if (t == 0) {
-    mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C), 3);
+    if (dm.out_bf16)
+      mma_a_exact(tb + 0, sa + 32 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C));
+    else
+      mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C), 3);
     mma_terms(tb + 64, sa, sa, sa + 16 * KB, sa + 16 * KB, D, idesc_bf16(128, C), 1);
     mma_commit(&bar[0]);
   }
