@@ -1264,6 +1264,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     fence_mbar_init();
+    mbar_expect_tx(&bar[1], RB);  // the prep kernel's W rows image (hi | lo) for phase 1
+    bulk_g2s(Bh, a.b.W + ch * CD, RB, &bar[1]);
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
   fence_before_sync();
@@ -1272,7 +1274,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   const uint32_t tb = *tslot;
   const uint32_t tl = tmem_lane_addr(tb, warp, 0);
   uint32_t phase = 0, cphase = 0;
-  bool ok = true, pending = false, cpending = false;
+  bool ok = true, pending = false, cpending = true;
   auto run = [&]() {  // all threads: wait for the committed MMAs
     const bool done = mbar_wait(&bar[0], phase);
     if (done) {
@@ -1318,8 +1320,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 
   // ---- phase 1: U^T = Ut^T - S0 W^T
   build_dd<false>(Ah, Al, S0);
-  build_split<false, C, D>(Bh, Bl, a.b.W + ch * CD, D, C);
-  issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+  issue_copies([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
   {
     float ut[32];  // Ut for the readout, loaded while the product runs
 #pragma unroll
@@ -1718,9 +1719,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 16) {
         float v[16];
         tmem_ld16(tmem_lane_addr(tb, warp, COL_W + c0), v);
-#pragma unroll
-        for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4*>(a.b.W + ch * CD + (int64_t)i * D + c0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         split8(Wr, Wr + TILE, kmajor_off(i, c0, D), v);
         split8(Wr, Wr + TILE, kmajor_off(i, c0 + 8, D), v + 8);
       }
@@ -1739,6 +1737,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   for (int q = t; q < (int)(TILE / 16); q += 256)  // K rows image for the reverse chain
     reinterpret_cast<uint4*>(img)[q] = reinterpret_cast<const uint4*>(Ki)[q];
   sync_for_mma();
+  // the W rows image (hi | lo, 32 KB) into W's slot: the d x d products and the second
+  // gradients kernel bring it in by one bulk copy each
+  for (int q = t; q < (int)(2 * TILE / 16); q += 256)
+    reinterpret_cast<uint4*>(a.b.W + ch * CD)[q] = reinterpret_cast<const uint4*>(Wr)[q];
   if (ok && t == 0) {
     fence_after_sync();
     const uint32_t qa = smem_u32(Qi), ka = smem_u32(Ki), sbo = (D / 8) * 128;
@@ -2314,20 +2316,18 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar[1], 3 * IMG);
+    mbar_expect_tx(&bar[1], 5 * IMG);
+    bulk_g2s(ar, a.b.W + ch * CD, 2 * IMG, &bar[1]);  // the prep kernel's W rows image (hi | lo)
     bulk_g2s(ar + 32 * KB, gY, 2 * IMG, &bar[1]);
     bulk_g2s(ar + 64 * KB, img, IMG, &bar[1]);
   }
   {
-    SplitTile<false, C, D> w;
-    w.load(a.b.W + ch * CD, D, C);
     float g0 = 0.f, b0 = 0.f, p0 = 0.f;
     if (t < C) {
       g0 = a.b.G[ch * C + t];
       b0 = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
     }
     p0 = img[C * D / 2 + t];  // t < 4 C
-    w.store(ar, ar + 16 * KB);
     if (t < C) {
       Gs[t] = g0;
       bs[t] = b0;
