@@ -1372,7 +1372,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       transpose_image_inplace(Ah, D);
       transpose_image_inplace(Al, D);
       ur.store(Bh, Bl);
-      issue([&] { mma_terms(tb + COL_2, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+      issue([&] {
+        mma_terms(tb + COL_2, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3);
+        // the U rows image (hi | lo) into U's slot, for the first gradients kernel
+        bulk_s2g(a.b.U + ch * CD, Bh, RB);
+        bulk_store_commit();
+      });
     }
   }
   for (int w2 = 128; w2 > 0; w2 >>= 1) {
@@ -1388,6 +1393,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     run();
     if (ok) {
       if (t == 0) {
+        bulk_wait_read();  // the U image store has read B
         mbar_expect_tx(&bar[1], C * C * 4);
         bulk_g2s(Bh, a.b.P + ch * C * C, C * C * 4, &bar[1]);
         cpending = true;
@@ -1495,6 +1501,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     if (pending) mbar_wait(&bar[0], phase);  // let this CTA's products and copies finish
     if (cpending) mbar_wait(&bar[1], cphase);
   }
+  if (t == 0) bulk_wait_all();  // the U image store is complete
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
@@ -1960,6 +1967,13 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const int half = warp >> 2;
   const int helper = half * 64 + ((warp & 3) - 2) * 32 + lane;  // 0..127 on warps 2, 3, 6, 7
   const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  if (t == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+    mbar_expect_tx(&bar[1], 2 * IMG);  // the d x d products kernel's U rows image (hi | lo)
+    bulk_g2s(ar + 64 * KB, a.b.U + ch * CD, 2 * IMG, &bar[1]);
+  }
   // arena: products 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U hi/lo @64/@80; then Pm hi/lo
   // @32/@40, Pm^T @48/@56, K^T @64, Q^T @80; then T^T @0/@8, dU^T @16/@32, dW^T @48/@64
   {
@@ -2006,12 +2020,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       *reinterpret_cast<uint4*>(ar + 16 * KB + off) = kr[it];
     }
   }
-  build_split<false, C, D>(ar + 64 * KB, ar + 80 * KB, a.b.U + ch * CD, D, C);
-  if (t == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbar_init();
-  }
   if (warp == 0) tmem_alloc(tslot, TMEM1);
   fence_proxy_async();
   fence_before_sync();
@@ -2022,7 +2030,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const uint32_t sa = smem_u32(ar);
   uint32_t phase = 0;
   uint32_t cphase = 0;
-  bool ok = true, pending = false, cpending = false;
+  bool ok = true, pending = false, cpending = true;
   auto wait_mma = [&]() {
     const bool done = mbar_wait(&bar[0], phase);
     if (done) {
@@ -2053,16 +2061,14 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       pending = true;
     }
   };
-  // ---- products 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64
-  if (t == 0) {
+  // ---- products 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64 (after the U image)
+  issue(true, [&] {
     if (dm.out_bf16)
       mma_a_exact(tb + 0, sa + 32 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C));
     else
       mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C), 3);
     mma_terms(tb + 64, sa, sa, sa + 16 * KB, sa + 16 * KB, D, idesc_bf16(128, C), 1);
-    mma_commit(&bar[0]);
-  }
-  pending = true;
+  });
   if (t < C) eG[t] = expf(Gs[t]);
   decay_table_lower(gam, Gs);  // while the products run
   wait_mma();

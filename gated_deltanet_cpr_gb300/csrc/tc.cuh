@@ -117,6 +117,20 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 // every copy this thread issued has landed (the CTA still needs a barrier to see the others')
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// shared -> global bulk copy (16-byte aligned addresses, size a multiple of 16) in the
+// issuing thread's bulk group; the generic-proxy writes that made the source must be fenced
+// (fence_proxy_async) and synchronised before it.  bulk_store_commit closes the group;
+// bulk_wait_read waits until the thread's committed stores have read their sources (so the
+// region can be written again), bulk_wait_all until they are complete.
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Hint: bring the 128-byte line holding p into L2 (no register result, no wait).  A CTA that
 // walks items issues these for its next item's operands, so that their loads hit L2.
 __device__ __forceinline__ void prefetch_l2(const void* p) {
