@@ -1741,13 +1741,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     }
   }
   // ---- 4. P = Gam (.) (Q K^T); meanwhile W^T hi | lo from the W rows (over the dead K^T, V^T)
-  for (int q = t; q < (int)(TILE / 16); q += 256)  // K rows image for the reverse chain
-    reinterpret_cast<uint4*>(img)[q] = reinterpret_cast<const uint4*>(Ki)[q];
   sync_for_mma();
-  // the W rows image (hi | lo, 32 KB) into W's slot: the d x d products and the second
-  // gradients kernel bring it in by one bulk copy each
-  for (int q = t; q < (int)(2 * TILE / 16); q += 256)
-    reinterpret_cast<uint4*>(a.b.W + ch * CD)[q] = reinterpret_cast<const uint4*>(Wr)[q];
   if (ok && t == 0) {
     fence_after_sync();
     const uint32_t qa = smem_u32(Qi), ka = smem_u32(Ki), sbo = (D / 8) * 128;
@@ -1756,8 +1750,15 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
                idesc_bf16(128, C), kk > 0 ? 1u : 0u);
     mma_commit(bar);
   }
+  if (t == 0) {  // asynchronous bulk stores: the K rows image for the reverse chain, and the W
+                 // rows image (hi | lo) into W's slot for the d x d products and gradients kernels
+    bulk_s2g(img, Ki, TILE);
+    bulk_s2g(a.b.W + ch * CD, Wr, 2 * TILE);
+    bulk_store_commit();
+  }
   tc::transpose_image(KT, Wr, D, C);
   tc::transpose_image(VT, Wr + TILE, D, C);
+  if (t == 0) bulk_wait_read();  // the P readout writes over the W rows image
   if (ok) wait_mma();
   if (ok && (warp & 3) < 2) {  // P rows -> global and as the split image (over the dead W rows)
     const int i = lrow;
@@ -1784,6 +1785,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       fence_after_sync();
       mma_terms(tb + COL_QT, smem_u32(TKh), smem_u32(TKl), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
       mma_commit(bar);
+      bulk_s2g(img + TILE, KT, 2 * TILE);  // W^T images (hi | lo) for the reverse chain
+      bulk_store_commit();
     }
     if (dm.out_bf16) {
       const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(a.dO) + (tok0 * dm.hv + h) * D;
@@ -1800,14 +1803,16 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     } else {
       load_dO_T(dov, a.dO, false, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
     }
-    for (int q = t; q < (int)(2 * TILE / 16); q += 256)  // W^T images for the reverse chain
-      reinterpret_cast<uint4*>(img + TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
     // P^T hi | lo (over the dead TV) -> P's slot: the big-products kernel's operand image
     tc::transpose_image(smq + OFF_TV, TKh, C, C);
     tc::transpose_image(smq + OFF_TV + C * C * 2, TKl, C, C);
+    fence_proxy_async();
     __syncthreads();
-    for (int q = t; q < C * C * 4 / 16; q += 256)
-      reinterpret_cast<uint4*>(a.b.P + ch * C * C)[q] = reinterpret_cast<const uint4*>(smq + OFF_TV)[q];
+    if (t == 0) {
+      bulk_s2g(a.b.P + ch * C * C, smq + OFF_TV, C * C * 4);
+      bulk_store_commit();
+      bulk_wait_read();  // the Qt readout writes over it, step 6 over K^T, V^T and the K rows
+    }
     wait_mma();
   }
   // Qt rows hi | lo over the dead TV and T regions
@@ -1879,6 +1884,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
     mbar_wait(bar, phase);
   }
+  if (t == 0) bulk_wait_all();  // the image stores are complete
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
