@@ -1841,16 +1841,29 @@ __global__ void k_tail_fill(Dims dm, TokenArrays in, const SeqRec* __restrict__ 
   const int64_t base = (int64_t)rec.tok0 + rec.len - nt;
   const Tin* kin = static_cast<const Tin*>(in.k);
   const Tin* vin = static_cast<const Tin*>(in.v);
-  const int64_t nk = (int64_t)nt * dm.hqk * D, nv = (int64_t)nt * dm.hv * D, ng = (int64_t)nt * dm.hv;
-  for (int64_t e = (int64_t)k0 * dm.hqk * D + threadIdx.x; e < nk; e += blockDim.x)
-    tail_k[(int64_t)sl * C * dm.hqk * D + e] = kin[base * dm.hqk * D + e];
-  for (int64_t e = (int64_t)k0 * dm.hv * D + threadIdx.x; e < nv; e += blockDim.x)
-    tail_v[(int64_t)sl * C * dm.hv * D + e] = vin[base * dm.hv * D + e];
-  for (int64_t e = (int64_t)k0 * dm.hv + threadIdx.x; e < ng; e += blockDim.x) {
+  // rows k0 .. nt-1 of the last chunk: one contiguous range in the inputs and in the tail
+  // (a row of K or V is a multiple of 16 bytes), copied 16 bytes at a time by the
+  // gridDim.y CTAs of this sequence
+  const int64_t tid = (int64_t)blockIdx.y * blockDim.x + threadIdx.x, nth = (int64_t)gridDim.y * blockDim.x;
+  const int64_t rk = (int64_t)dm.hqk * D, rv = (int64_t)dm.hv * D;
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(kin + (base + k0) * rk);
+    uint4* dst = reinterpret_cast<uint4*>(tail_k + ((int64_t)sl * C + k0) * rk);
+    const int64_t n16 = (int64_t)(nt - k0) * rk * (int64_t)sizeof(Tin) / 16;
+    for (int64_t q = tid; q < n16; q += nth) dst[q] = src[q];
+  }
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(vin + (base + k0) * rv);
+    uint4* dst = reinterpret_cast<uint4*>(tail_v + ((int64_t)sl * C + k0) * rv);
+    const int64_t n16 = (int64_t)(nt - k0) * rv * (int64_t)sizeof(Tin) / 16;
+    for (int64_t q = tid; q < n16; q += nth) dst[q] = src[q];
+  }
+  const int64_t ng = (int64_t)nt * dm.hv;
+  for (int64_t e = (int64_t)k0 * dm.hv + tid; e < ng; e += nth) {
     tail_g[(int64_t)sl * C * dm.hv + e] = in.g[base * dm.hv + e];
     tail_beta[(int64_t)sl * C * dm.hv + e] = in.beta[base * dm.hv + e];
   }
-  if (threadIdx.x == 0) pos[sl] = (pos_base ? pos_base[n] : 0) + rec.len;
+  if (blockIdx.y == 0 && threadIdx.x == 0) pos[sl] = (pos_base ? pos_base[n] : 0) + rec.len;
 }
 
 void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, int N,
@@ -1858,13 +1871,14 @@ void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, 
                       float* tail_g, float* tail_beta, int32_t* pos, const int32_t* pos_base,
                       const int32_t* keep_rows, WsHeader* hdr, cudaStream_t st) {
   if (N <= 0) return;
+  const dim3 grid((unsigned)N, 16);  // 16 CTAs share each sequence's copy
   if (d.in_bf16)
-    k_tail_fill<__nv_bfloat16><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
+    k_tail_fill<__nv_bfloat16><<<grid, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
                                                   static_cast<__nv_bfloat16*>(tail_k),
                                                   static_cast<__nv_bfloat16*>(tail_v), tail_g,
                                                   tail_beta, pos, pos_base, keep_rows, hdr);
   else
-    k_tail_fill<float><<<N, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
+    k_tail_fill<float><<<grid, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
                                           static_cast<float*>(tail_k), static_cast<float*>(tail_v),
                                           tail_g, tail_beta, pos, pos_base, keep_rows, hdr);
 }
