@@ -574,11 +574,26 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
   // thread; a CTA with none exits before touching tensor memory.
   __shared__ int64_t s_list[128];
   __shared__ int s_cnt;
+  // Prefill: the CTAs (launched in order) take the (sequence, head) chains longest first, so
+  // that the longest chains do not start last; sequences ranked by chunk count, ties by index
+  // (up to 256 sequences; beyond that, in sequence order).
+  __shared__ int s_order[256];
+  const bool by_length = w.seqs && w.N <= 256;
+  if (by_length && t < w.N) {
+    const int mine = w.seqs[t].nchunks;
+    int r = 0;
+    for (int s2 = 0; s2 < w.N; ++s2) {
+      const int o = w.seqs[s2].nchunks;
+      r += (o > mine || (o == mine && s2 < t)) ? 1 : 0;
+    }
+    s_order[r] = t;
+  }
   if (t == 0) s_cnt = 0;
   __syncthreads();
   if (t < 128) {
-    const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
-    if (wi < total) {
+    const int64_t wc = blockIdx.x + (int64_t)t * gridDim.x;
+    const int64_t wi = (by_length && wc < total) ? (int64_t)s_order[wc / dm.hv] * dm.hv + wc % dm.hv : wc;
+    if (wc < total) {
       bool work = true;
       if (!w.seqs) {
         const int sl = w.slot[wi / dm.hv];
@@ -887,6 +902,8 @@ constexpr size_t SMEM = 3 * (size_t)TILE + 2 * (size_t)MAT + 5 * C * 4 + 64;
 constexpr uint32_t TMEM_COLS = 256, W_COL = 0, UT_COL = 128, GRAM_COL = 0;
 }  // namespace tcp
 
+constexpr int kPrepMaxItems = 1024;  // items one k_prep_tc CTA can hold (the launch sizes the grid)
+
 __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, PrepWork w,
                                                     float* __restrict__ Wout, float* __restrict__ Uout,
                                                     float* __restrict__ gamma_out, WsHeader* __restrict__ hdr) {
@@ -914,13 +931,13 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
   const int64_t total = w.n_items * dm.hv;
   // Which of this CTA's items (wi = blockIdx.x + j * gridDim.x) need the pre-pass: all
   // tested at once, one per thread; a CTA with none exits before touching tensor memory.
-  __shared__ int64_t s_list[256];
-  __shared__ int64_t s_tok0[256];
+  __shared__ int64_t s_list[kPrepMaxItems];
+  __shared__ int64_t s_tok0[kPrepMaxItems];
   __shared__ int s_cnt;
   if (t == 0) s_cnt = 0;
   __syncthreads();
-  {
-    const int64_t wi = blockIdx.x + (int64_t)t * gridDim.x;
+  for (int cand = t; cand < kPrepMaxItems; cand += 256) {
+    const int64_t wi = blockIdx.x + (int64_t)cand * gridDim.x;
     if (wi < total) {
       const int64_t item = wi / dm.hv;
       const int h = (int)(wi % dm.hv);
@@ -1898,7 +1915,7 @@ void launch_prep(const Dims& d, const TokenArrays& in, const PrepWork& w, float*
     ensure_smem(k_prep_tc, tcp::SMEM);
     const int64_t total = w.n_items * d.hv;
     int64_t cap = 2 * (int64_t)sm_count();  // persistent: two CTAs per SM walk the items
-    if ((total + cap - 1) / cap > 256) cap = (total + 255) / 256;  // at most 256 items per CTA
+    if ((total + cap - 1) / cap > kPrepMaxItems) cap = (total + kPrepMaxItems - 1) / kPrepMaxItems;
     k_prep_tc<<<(unsigned)(total < cap ? total : cap), 256, tcp::SMEM, st>>>(d, in, w, W, U, gamma, hdr);
   } else if (d.in_bf16) {
     GDN_DISPATCH_D(d.D, launch_prep_t<DD, __nv_bfloat16>(d, in, w, W, U, gamma, hdr, st))
