@@ -842,7 +842,24 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   // warp w reads TMEM lanes 32 (w % 4) .. + 31 (state rows) and column half w / 4
   const int t = threadIdx.x, warp = t >> 5, row = (warp & 3) * 32 + (t & 31), half = warp >> 2;
   const int cs0 = half * (D / 2), us0 = half * (C / 2);
-  const int n = blockIdx.x, h = blockIdx.y;
+  // CTA b = blockIdx.y * gridDim.x + blockIdx.x (launch order) takes the b-th (sequence, head)
+  // with the sequences longest first (ranked by chunk count, ties by index; up to 256
+  // sequences, beyond that in sequence order), so that the longest chains do not start last
+  __shared__ int s_order[256];
+  const bool by_length = a.N <= 256;
+  if (by_length && t < a.N) {
+    const int mine = a.seqs[t].nchunks;
+    int r = 0;
+    for (int s2 = 0; s2 < a.N; ++s2) {
+      const int o = a.seqs[s2].nchunks;
+      r += (o > mine || (o == mine && s2 < t)) ? 1 : 0;
+    }
+    s_order[r] = t;
+  }
+  __syncthreads();
+  const int lin = (int)(blockIdx.y * gridDim.x + blockIdx.x);
+  const int n = by_length ? s_order[lin / dm.hv] : (int)blockIdx.x;
+  const int h = by_length ? lin % dm.hv : (int)blockIdx.y;
   const SeqRec rec = a.seqs[n];
   if (!in_bounds(a.hdr, rec.chunk0 >= 0 && (int64_t)rec.chunk0 + rec.nchunks <= a.n_chunks && rec.tok0 >= 0 &&
                             (int64_t)rec.tok0 + rec.len <= a.T))
