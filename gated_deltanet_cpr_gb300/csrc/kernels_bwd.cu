@@ -843,17 +843,17 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   const int t = threadIdx.x, warp = t >> 5, row = (warp & 3) * 32 + (t & 31), half = warp >> 2;
   const int cs0 = half * (D / 2), us0 = half * (C / 2);
   // CTA b = blockIdx.y * gridDim.x + blockIdx.x (launch order) takes the b-th (sequence, head)
-  // with the sequences longest first (ranked by chunk count, ties by index; up to 256
+  // with the sequences longest first (ranked by chunk count, ties by index; up to 64
   // sequences, beyond that in sequence order), so that the longest chains do not start last
-  __shared__ int s_order[256];
-  const bool by_length = a.N <= 256;
+  constexpr int kRankSeqs = 64;
+  __shared__ int s_nch[kRankSeqs], s_order[kRankSeqs];
+  const bool by_length = a.N <= kRankSeqs;
+  if (by_length && t < a.N) s_nch[t] = a.seqs[t].nchunks;
+  __syncthreads();
   if (by_length && t < a.N) {
-    const int mine = a.seqs[t].nchunks;
+    const int mine = s_nch[t];
     int r = 0;
-    for (int s2 = 0; s2 < a.N; ++s2) {
-      const int o = a.seqs[s2].nchunks;
-      r += (o > mine || (o == mine && s2 < t)) ? 1 : 0;
-    }
+    for (int s2 = 0; s2 < a.N; ++s2) r += (s_nch[s2] > mine || (s_nch[s2] == mine && s2 < t)) ? 1 : 0;
     s_order[r] = t;
   }
   __syncthreads();

@@ -42,6 +42,8 @@ static void ensure_smem(F* fn, size_t bytes) {
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+constexpr int kRankSeqs = 64;  // batches the boundary chains order longest first (ranked per CTA)
+
 // Streaming multiprocessors of the current device (looked up once per device).
 static int sm_count() {
   static std::mutex mu;
@@ -576,19 +578,18 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
   __shared__ int s_cnt;
   // Prefill: the CTAs (launched in order) take the (sequence, head) chains longest first, so
   // that the longest chains do not start last; sequences ranked by chunk count, ties by index
-  // (up to 256 sequences; beyond that, in sequence order).
-  __shared__ int s_order[256];
-  const bool by_length = w.seqs && w.N <= 256;
+  // (up to kRankSeqs sequences, each CTA ranking them; beyond that, in sequence order).
+  __shared__ int s_nch[kRankSeqs], s_order[kRankSeqs];
+  const bool by_length = w.seqs && w.N <= kRankSeqs;
+  if (by_length && t < w.N) s_nch[t] = w.seqs[t].nchunks;
+  if (t == 0) s_cnt = 0;
+  __syncthreads();
   if (by_length && t < w.N) {
-    const int mine = w.seqs[t].nchunks;
+    const int mine = s_nch[t];
     int r = 0;
-    for (int s2 = 0; s2 < w.N; ++s2) {
-      const int o = w.seqs[s2].nchunks;
-      r += (o > mine || (o == mine && s2 < t)) ? 1 : 0;
-    }
+    for (int s2 = 0; s2 < w.N; ++s2) r += (s_nch[s2] > mine || (s_nch[s2] == mine && s2 < t)) ? 1 : 0;
     s_order[r] = t;
   }
-  if (t == 0) s_cnt = 0;
   __syncthreads();
   if (t < 128) {
     const int64_t wc = blockIdx.x + (int64_t)t * gridDim.x;
@@ -1888,7 +1889,9 @@ void launch_tail_fill(const Dims& d, const TokenArrays& in, const SeqRec* seqs, 
                       float* tail_g, float* tail_beta, int32_t* pos, const int32_t* pos_base,
                       const int32_t* keep_rows, WsHeader* hdr, cudaStream_t st) {
   if (N <= 0) return;
-  const dim3 grid((unsigned)N, 16);  // 16 CTAs share each sequence's copy
+  // CTAs per sequence sharing its copy: about two per SM in all, at most 16
+  const int64_t per = (2 * (int64_t)sm_count() + N - 1) / N;
+  const dim3 grid((unsigned)N, (unsigned)(per < 1 ? 1 : per > 16 ? 16 : per));
   if (d.in_bf16)
     k_tail_fill<__nv_bfloat16><<<grid, 256, 0, st>>>(d, in, seqs, slot_of_seq, slots,
                                                   static_cast<__nv_bfloat16*>(tail_k),
