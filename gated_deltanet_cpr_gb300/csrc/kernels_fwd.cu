@@ -1945,7 +1945,11 @@ void launch_chain(const Dims& d, const void* keys, const float* W, const float* 
   if (boundary_on_tensor_cores(d)) {
     const int64_t total = (int64_t)w.N * d.hv;
     ensure_smem(k_chain_tc, tcc::SMEM);
+    // one CTA per chain, scheduled by the hardware (longest first); for batches of short
+    // chains (fewer than two chunk records per sequence: continued prefill in small pieces)
+    // one wave of CTAs walking the items instead, since most CTAs would find nothing to do
     int64_t cap = total;
+    if (w.n_chunks < 2 * (int64_t)w.N && total > (int64_t)sm_count()) cap = sm_count();
     if ((total + cap - 1) / cap > 128) cap = (total + 127) / 128;  // at most 128 items per CTA
     k_chain_tc<<<(unsigned)(total < cap ? total : cap), 256, tcc::SMEM, st>>>(d, W, U, gamma, w, hdr);
   } else if (d.in_bf16) {
