@@ -791,19 +791,27 @@ __global__ void k_bwd_gqa(const float* __restrict__ dq_part, const float* __rest
 }
 
 // ============================================================  KB2 (tcgen05)  ===
-// Reverse boundary chain on tensor cores (bf16 inputs, d = 128, C = 64): one CTA of 128
-// threads per (sequence, head), thread i owns adjoint row i = TMEM lane i.  Per chunk j,
-// from the end adjoint dS = dS^(j+1):
+// Reverse boundary chain on tensor cores (bf16 inputs, d = 128, C = 64): one CTA of 256
+// threads per (sequence, head); adjoint row i is TMEM lane i, read by the two warps of its
+// lane quadrant, one half of the columns each.  Per chunk j, from the end adjoint
+// dS = dS^(j+1):
 //     D1 (128 x 64)  = dS K^T                     2 MMAs: dS_hi K + dS_lo K (K exact)
+//     D2 (128 x 128) = gamma_j dS + dO_j^T Qt_j    D2 preloaded; 2 MMAs (Qt = Qt_hi + Qt_lo,
+//                                                  bf16 dO exact; fp32 dO: 3)
 //     Xd[i][s]       = -dec_s D1[i][s]            (split to bf16 hi/lo)
-//     D2 (128 x 128) = (L_j + gamma_j dS) + Xd W   D2 preloaded, 3 MMAs with W = W_hi + W_lo
+//     D2            += Xd W                       3 MMAs with W = W_hi + W_lo
 // giving dS^(j).  Operands [K rows | W^T hi | W^T lo] come as one bulk copy per chunk,
-// prefetched a chunk ahead.
+// prefetched a chunk ahead; the dO^T and Qt^T images (the prep kernel's, in L's slot) as
+// another, issued as soon as the previous step's Xd W has consumed the region.
 namespace tcb {
 constexpr int D = 128, C = 64;
 constexpr uint32_t A1_BYTES = 128 * D * 2, A2_BYTES = 128 * C * 2, STAGE_BYTES = 3 * C * D * 2;
-constexpr size_t SMEM = 2 * (size_t)A1_BYTES + 2 * (size_t)A2_BYTES + 2 * (size_t)STAGE_BYTES + 64 * 4 + 64;
+// the L = dO^T Qt operands of a step, as the prep kernel left them in L's slot:
+// dO^T hi | Qt^T hi | Qt^T lo | dO^T lo (the last only for fp32 dO); Xd is built over them
+constexpr uint32_t IMG = C * D * 2, LA_BYTES = 4 * IMG;
+constexpr size_t SMEM = 2 * (size_t)A1_BYTES + 2 * (size_t)STAGE_BYTES + LA_BYTES + 64 * 4 + 64;
 constexpr uint32_t TMEM_COLS = 256, D1_COL = 0, D2_COL = 64;
+static_assert(2 * A2_BYTES <= LA_BYTES, "Xd hi | lo over the L operands");
 }  // namespace tcb
 
 __device__ __forceinline__ void split_store16(unsigned char* hi, unsigned char* lo, int row, int k0, int K,
@@ -831,12 +839,13 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smb[];
   unsigned char* A1h = smb;
   unsigned char* A1l = A1h + A1_BYTES;
-  unsigned char* A2h = A1l + A1_BYTES;
-  unsigned char* A2l = A2h + A2_BYTES;
-  unsigned char* stage0 = A2l + A2_BYTES;
-  float* decs = reinterpret_cast<float*>(stage0 + 2 * STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(decs + 64);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+  unsigned char* stage0 = A1l + A1_BYTES;
+  unsigned char* LA = stage0 + 2 * STAGE_BYTES;  // this step's dO^T, Qt^T images; then Xd
+  unsigned char* A2h = LA;
+  unsigned char* A2l = LA + A2_BYTES;
+  float* decs = reinterpret_cast<float*>(LA + LA_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(decs + 64);  // stage 0, stage 1, MMA, L operands
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
   // warp w reads TMEM lanes 32 (w % 4) .. + 31 (state rows) and column half w / 4
@@ -877,6 +886,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
     mbar_init(&bars[0], 1);
     mbar_init(&bars[1], 1);
     mbar_init(&bars[2], 1);
+    mbar_init(&bars[3], 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, TMEM_COLS);
@@ -887,15 +897,21 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   const uint32_t tlane = tmem_lane_addr(tbase, warp, 0);
   auto chead = [&](int j) { return ((int64_t)rec.chunk0 + j) * dm.hv + h; };
   auto gamma_of = [&](int j) { return expf(a.b.G[chead(j) * C + C - 1]); };
+  const bool dexact = dm.out_bf16;  // bf16 dO: no dO^T lo image
+  const uint32_t la_bytes = dexact ? 3 * IMG : 4 * IMG;
+  auto load_la = [&](int j) {  // thread 0: chunk j's dO^T and Qt^T images
+    mbar_expect_tx(&bars[3], la_bytes);
+    bulk_g2s(LA, a.b.L + chead(j) * SZ, la_bytes, &bars[3]);
+  };
   // prologue: dS^(nch) = dstate_out is the end adjoint of the last chunk
   {
     const int j = nch - 1;
     if (t == 0) {
       mbar_expect_tx(&bars[0], STAGE_BYTES);
       bulk_g2s(stage0, a.b.img + chead(j) * IW, STAGE_BYTES, &bars[0]);
+      load_la(j);
     }
     const float g = gamma_of(j);
-    const float* L = a.b.L + chead(j) * SZ + (int64_t)row * D;
     for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
       float v[16], w[16];
 #pragma unroll
@@ -906,7 +922,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
             make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
       split_store16(A1h, A1l, row, c0, D, v);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(L[c0 + e], __fmul_rn(g, v[e]));
+      for (int e = 0; e < 16; ++e) w[e] = __fmul_rn(g, v[e]);
       tmem_st16(tlane + D2_COL + c0, w);
     }
     tmem_st_wait();
@@ -914,9 +930,9 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   fence_proxy_async();
   fence_before_sync();
   __syncthreads();
-  uint32_t uses[2] = {0u, 0u}, mma_phase = 0;
+  uint32_t uses[2] = {0u, 0u}, la_uses = 0, mma_phase = 0;
   int pending = 0;
-  bool mma_pending = false, ok = true;
+  bool mma_pending = false, la_pending = true, ok = true;
   int q = 0;
   for (; q < nch; ++q) {
     const int j = nch - 1 - q;
@@ -927,22 +943,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
       bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, a.b.img + chead(j - 1) * IW, STAGE_BYTES, &bars[buf ^ 1]);
     }
     if (t < C) decs[t] = -expf(__fsub_rn(a.b.G[chead(j) * C + C - 1], a.b.G[chead(j) * C + t]));
-    float lpre[D / 2];  // next step's L half row, loaded while this step's MMAs run
-    float gpre = 0.f;
-    if (j > 0) {
-      const float4* L4 = reinterpret_cast<const float4*>(a.b.L + chead(j - 1) * SZ + (int64_t)row * D + cs0);
-#pragma unroll
-      for (int e = 0; e < D / 8; ++e) {
-        const float4 x = L4[e];
-        lpre[4 * e] = x.x; lpre[4 * e + 1] = x.y; lpre[4 * e + 2] = x.z; lpre[4 * e + 3] = x.w;
-      }
-      gpre = gamma_of(j - 1);
-    }
-    ok = __syncthreads_and(mbar_wait(&bars[buf], uses[buf] & 1u)) != 0;
+    const float gpre = j > 0 ? gamma_of(j - 1) : 0.f;
+    ok = __syncthreads_and(mbar_wait(&bars[buf], uses[buf] & 1u) && mbar_wait(&bars[3], la_uses & 1u)) != 0;
     if (!ok) break;
     ++uses[buf];
+    ++la_uses;
+    la_pending = false;
     pending = j > 0 ? (buf ^ 1) : -1;
-    if (t == 0) {  // D1 = dS K^T
+    if (t == 0) {  // D1 = dS K^T; D2 += dO^T Qt
       fence_after_sync();
       const uint32_t kimg = smem_u32(stg), sbo = (D / 8) * 128;
 #pragma unroll 1
@@ -951,6 +959,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
         for (int kk = 0; kk < D / 16; ++kk)
           mma_bf16(tbase + D1_COL, make_desc(aa + kk * 256, 128, sbo), make_desc(kimg + kk * 256, 128, sbo),
                    idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
+      }
+      const uint32_t dh = smem_u32(LA), qh = dh + IMG, ql = dh + 2 * IMG, dl = dh + 3 * IMG, lsbo = (C / 8) * 128;
+#pragma unroll 1
+      for (int term = 0; term < (dexact ? 2 : 3); ++term) {  // dO_hi Qt_hi + dO_hi Qt_lo (+ dO_lo Qt_hi)
+        const uint32_t aa = term == 2 ? dl : dh, bb = term == 1 ? ql : qh;
+        for (int kk = 0; kk < C / 16; ++kk)
+          mma_bf16(tbase + D2_COL, make_desc(aa + kk * 256, 128, lsbo), make_desc(bb + kk * 256, 128, lsbo),
+                   idesc_bf16(128, D), 1u);
       }
       mma_commit(&bars[2]);
     }
@@ -990,12 +1006,16 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
     mma_phase ^= 1u;
     mma_pending = false;
     fence_after_sync();
+    if (j > 0 && t == 0) {  // the next step's dO^T, Qt^T images over the consumed Xd
+      load_la(j - 1);
+      la_pending = true;
+    }
     {  // dS^(j): end adjoint of chunk j-1 (or dstate_in), next A operand, next D2 preload
       const bool more = j > 0;
       const float g = gpre;
-      // dS^(j) leaves through a per-warp staging tile in the (now free) Xd operand region,
-      // so that each store instruction writes 8 rows x 64 contiguous bytes
-      float* tile = reinterpret_cast<float*>(A2h) + warp * (32 * 20);
+      // dS^(j) leaves through a per-warp staging tile in this step's (now consumed) operand
+      // stage, so that each store instruction writes 8 rows x 64 contiguous bytes
+      float* tile = reinterpret_cast<float*>(stg) + warp * (32 * 20);
       const int lane = t & 31, rq = (warp & 3) * 32;
 #pragma unroll
       for (int c0 = cs0; c0 < cs0 + D / 2; c0 += 16) {
@@ -1016,7 +1036,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
           split_store16(A1h, A1l, row, c0, D, v);
           float w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) w[e] = __fadd_rn(lpre[c0 - cs0 + e], __fmul_rn(g, v[e]));
+          for (int e = 0; e < 16; ++e) w[e] = __fmul_rn(g, v[e]);
           tmem_st16(tlane + D2_COL + c0, w);
         } else if (a.dstate_in) {
 #pragma unroll
@@ -1033,6 +1053,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   if (!ok && t == 0) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
     if (pending >= 0) mbar_wait(&bars[pending], uses[pending] & 1u);
+    if (la_pending) mbar_wait(&bars[3], la_uses & 1u);
     if (mma_pending) mbar_wait(&bars[2], mma_phase);
   }
   fence_before_sync();
@@ -1530,10 +1551,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 //   Gram = K K^T, T = (I + A)^{-1} (SIMT), W = TK K, U^T = V^T TV^T    (as the forward pre-pass)
 //   P    = Gam (.) (Q K^T), lower with diagonal                       (exact bf16 inputs)
 //   Qt   = diag(e^G) Q - P W                                          (P, W split hi/lo)
-//   L    = dO^T Qt                                                    (dO, Qt split)
-// Outputs W, Ut, G, L, the reverse chain's images and two operand images: P^T for the
-// big-products kernel (in P's slot) and T^T for the gradients kernel (in T's slot).  W, P and Qt also leave their readouts as split images in
-// shared memory, where the transposed operands are built.
+//   dO^T, Qt^T                                                        (the operands of L = dO^T Qt)
+// Outputs: the W rows image (W's slot), Ut, G, the reverse chain's images [K rows | W^T hi |
+// W^T lo] and the operands of L (L's slot; the reverse chain forms L = dO^T Qt on its tensor
+// cores), and two more operand images: P^T for the big-products kernel (in P's slot) and T^T
+// for the gradients kernel (in T's slot).  W, P and Qt also leave their readouts as split
+// images in shared memory, where the transposed operands are built.
 namespace tcq {
 constexpr int D = 128, C = 64, QCP = C + 1, TCP = C;  // row strides of A (padded) and T
 constexpr uint32_t TILE = C * D * 2;  // 16 KB
@@ -1541,7 +1564,7 @@ constexpr uint32_t OFF_K = 0, OFF_KT = TILE, OFF_VT = 2 * TILE, OFF_TK = 3 * TIL
                    OFF_A = 5 * TILE, OFF_T = OFF_A + C * QCP * 4, OFF_VEC = OFF_T + C * TCP * 4;
 constexpr size_t SMEM = OFF_VEC + 2 * C * 4 + 64;  // fits two CTAs per SM
 constexpr uint32_t TMEM_COLS = 256;  // the products run one after another: W and U^T (192) at most
-constexpr uint32_t COL_G = 0, COL_W = 0, COL_UT = 128, COL_P = 0, COL_QT = 0, COL_L = 0;
+constexpr uint32_t COL_G = 0, COL_W = 0, COL_UT = 128, COL_P = 0, COL_QT = 0;
 }  // namespace tcq
 
 __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
@@ -1851,8 +1874,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   }
   fence_before_sync();
   __syncthreads();
-  // ---- 6. L = dO^T Qt: A = dO^T (rows p, K = i) over the dead K rows and P, B = Qt^T (rows q,
-  // K = i) over the dead W^T
+  // ---- 6. the operands of L = dO^T Qt, which the reverse chain forms on its tensor cores:
+  // dO^T (rows p, K = i) over the dead K rows (its lo image, fp32 dO only, over the dead P),
+  // Qt^T hi | lo (rows q, K = i) over the dead W^T; the four regions are contiguous and leave
+  // as one bulk store into L's slot: [dO^T hi | Qt^T hi | Qt^T lo (| dO^T lo)]
+  static_assert(OFF_KT == OFF_K + TILE && OFF_VT == OFF_KT + TILE && OFF_TK == OFF_VT + TILE,
+                "dO^T, Qt^T hi, Qt^T lo, dO^T lo contiguous");
   if (ok) {
     if (dm.out_bf16) {  // dO rows image over the dead Q rows, transposed into dO^T; dO is exact
       unsigned char* Dr = smq + OFF_A;
@@ -1875,27 +1902,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     }
     tc::transpose_image(KT, Qrh, D, C);
     tc::transpose_image(VT, Qrl, D, C);
-    sync_for_mma();
+    fence_proxy_async();
+    fence_before_sync();
+    __syncthreads();
     if (t == 0) {
-      fence_after_sync();
-      if (dm.out_bf16) {  // dO^T (Qt_hi + Qt_lo)
-        mma_a_exact(tb + COL_L, smem_u32(Ki), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D));
-      } else {
-        mma_terms(tb + COL_L, smem_u32(Ki), smem_u32(TKh), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
-      }
-      mma_commit(bar);
-    }
-    wait_mma();
-  }
-  if (ok) {
-    const int p = lrow;
-    for (int c0 = chalf * 64; c0 < chalf * 64 + 64; c0 += 16) {
-      float v[16];
-      tmem_ld16(tmem_lane_addr(tb, warp, COL_L + c0), v);
-#pragma unroll
-      for (int e = 0; e < 16; e += 4)
-        *reinterpret_cast<float4*>(a.b.L + ch * (int64_t)D * D + (int64_t)p * D + c0 + e) =
-            make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      bulk_s2g(a.b.L + ch * (int64_t)D * D, smq + OFF_K, dm.out_bf16 ? 3 * TILE : 4 * TILE);
+      bulk_store_commit();
     }
   } else if (t == 0) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
