@@ -1078,7 +1078,9 @@ namespace tcg {
 constexpr int D = 128, C = 64;
 constexpr uint32_t RA = 2 * 128 * D * 2;       // A operand hi | lo (64 KB)
 constexpr uint32_t RB = 2 * C * D * 2;         // B operand hi | lo (32 KB)
-constexpr size_t SMEM = (size_t)RA + (size_t)RB + C * 4 + 256 * 4 + 64;  // two CTAs per SM
+constexpr uint32_t RX = C * D * 2;             // one more 64 x 128 image (16 KB)
+constexpr size_t SMEM = (size_t)RA + RB + RX + C * 4 + 128 * 4 + 64;
+static_assert(SMEM <= 115712, "two CTAs per SM");
 constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t COL_0 = 0, COL_1 = 64, COL_2 = 128;  // 128 x 64 results
 }  // namespace tcg
@@ -1276,9 +1278,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   unsigned char* Al = Ah + RA / 2;
   unsigned char* Bh = smg + RA;       // B operand: 64 x 128 or 64 x 64 (P^T)
   unsigned char* Bl = Bh + RB / 2;
-  float* dec = reinterpret_cast<float*>(Bh + RB);
-  float* red = dec + C;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 256);  // [0] MMA, [1] bulk copies
+  unsigned char* Xh = Bh + RB;        // a third 64 x 128 image
+  float* dec = reinterpret_cast<float*>(Xh + RX);
+  float* red = dec + C;                                    // 128 partial sums
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 128);  // [0] MMA, [1] bulk copies
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
@@ -1354,7 +1357,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     }
     pending = ok;
   };
-  const uint32_t sa_h = smem_u32(Ah), sa_l = smem_u32(Al), sb_h = smem_u32(Bh), sb_l = smem_u32(Bl);
+  const uint32_t sa_h = smem_u32(Ah), sa_l = smem_u32(Al), sb_h = smem_u32(Bh), sb_l = smem_u32(Bl),
+                 sx = smem_u32(Xh);
 
   // ---- phase 1: U^T = Ut^T - S0 W^T
   build_dd<false>(Ah, Al, S0);
@@ -1364,14 +1368,16 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 #pragma unroll
     for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
     run();
-    if (ok) {  // U = Ut - (U^T)^T
+    if (ok) {  // U = Ut - (U^T)^T, kept as the U^T image (rows d, K = s): hi in X, lo in B's
+      // second half (phase 2a's K image takes the first)
 #pragma unroll
       for (int s1 = 0; s1 < 2; ++s1) {
         float v[16];
         tmem_ld16(tl + COL_0 + cbase + 16 * s1, v);
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          a.b.U[ch * CD + (int64_t)(cbase + 16 * s1 + e) * D + lane_row] = __fsub_rn(ut[16 * s1 + e], v[e]);
+        for (int e = 0; e < 16; ++e) v[e] = __fsub_rn(ut[16 * s1 + e], v[e]);
+        split8(Xh, Bl, kmajor_off(lane_row, cbase + 16 * s1, C), v);
+        split8(Xh, Bl, kmajor_off(lane_row, cbase + 16 * s1 + 8, C), v + 8);
       }
     }
   }
@@ -1380,13 +1386,13 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 
   // ---- phase 2a: E K^T (K rows: the prep kernel's image, one bulk copy); <E, S0> from the
   // E build
+  float part = 0.f;
   if (ok) {
     if (t == 0) {
       mbar_expect_tx(&bar[1], IMGB);
       bulk_g2s(Bh, a.b.img + ch * (int64_t)prep_w_floats(C, D), IMGB, &bar[1]);
       cpending = true;
     }
-    float part = 0.f;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {  // E image by halves, with S0 at the same positions
       SplitTile<false, 64, D> et, st;
@@ -1398,31 +1404,44 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
         for (int e = 0; e < 8; ++e) part = __fmaf_rn(et.v[it][e], st.v[it][e], part);
       et.store(Ah + hh * 16384, Al + hh * 16384);
     }
-    red[t] = part;
     issue_copies([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_h, D, idesc_bf16(128, C), 2); });
   }
-  // ---- phase 3: (U E)^T = E^T U^T, E^T by transposing the E image in place
+  // ---- phase 3: (U E)^T = E^T U^T, E^T by transposing the E image in place, U rows by
+  // transposing the U^T image (hi into B's first half, then lo into X)
   if (ok) {
-    SplitTile<false, C, D> ur;  // U rows, loaded while E K^T runs
-    ur.load(a.b.U + ch * CD, D, C);
     run();
     if (ok) {
       transpose_image_inplace(Ah, D);
       transpose_image_inplace(Al, D);
-      ur.store(Bh, Bl);
+      transpose_image(Bh, Xh, C, D);
+      __syncthreads();
+      transpose_image(Xh, Bl, C, D);
       issue([&] {
-        mma_terms(tb + COL_2, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3);
+        mma_terms(tb + COL_2, sa_h, sa_l, sb_h, sx, D, idesc_bf16(128, C), 3);
         // the U rows image (hi | lo) into U's slot, for the first gradients kernel
-        bulk_s2g(a.b.U + ch * CD, Bh, RB);
+        bulk_s2g(a.b.U + ch * CD, Bh, IMGB);
+        bulk_s2g(a.b.U + ch * CD + IMGB / 4, Xh, IMGB);
         bulk_store_commit();
       });
     }
   }
-  for (int w2 = 128; w2 > 0; w2 >>= 1) {
-    if (t < w2) red[t] = __fadd_rn(red[t], red[t + w2]);
-    __syncthreads();
+  // <E, S0>: the 256 partial sums added pairwise at strides 128, 64, ..., 1
+  if (t >= 128) red[t - 128] = part;
+  __syncthreads();
+  if (t < 128) part = __fadd_rn(part, red[t]);
+  __syncthreads();
+  if (t >= 64 && t < 128) red[t - 64] = part;
+  __syncthreads();
+  if (t < 64) part = __fadd_rn(part, red[t]);
+  __syncthreads();
+  if (t >= 32 && t < 64) red[t - 32] = part;
+  __syncthreads();
+  if (t < 32) {
+    part = __fadd_rn(part, red[t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_down_sync(0xffffffffu, part, o));
+    if (t == 0) a.b.sdot[ch] = part;
   }
-  if (t == 0) a.b.sdot[ch] = red[0];
   // ---- phase 2b: dO^T P: dO^T from the dO rows image (transposed in shared memory), P^T the
   // prep kernel's image (one bulk copy)
   if (ok) {
@@ -1467,55 +1486,64 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     }
     run();
   }
-  if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec): fp32 dU rows, and the dU^T operand image
-    // (rows d, K = s; hi | lo) for the gradients kernel in this chunk-head's adjoint L slot
-    unsigned char* uimg = reinterpret_cast<unsigned char*>(a.b.L + ch * SZ);
+  if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec) as the dU^T operand image (rows d, K = s;
+    // hi | lo) in A: one bulk copy into this chunk-head's adjoint L slot for the gradients
+    // kernel, and transposed into the dU rows image (B) for dW^T
 #pragma unroll
     for (int s1 = 0; s1 < 2; ++s1) {
       float e1[16], p1[16];
       tmem_ld16(tl + COL_0 + cbase + 16 * s1, e1);
       tmem_ld16(tl + COL_1 + cbase + 16 * s1, p1);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int s = cbase + 16 * s1 + e;
-        p1[e] = __fmaf_rn(dec[s], e1[e], p1[e]);
-        a.b.dU[ch * CD + (int64_t)s * D + lane_row] = p1[e];
-      }
-      split8(uimg, uimg + C * D * 2, kmajor_off(lane_row, cbase + 16 * s1, C), p1);
-      split8(uimg, uimg + C * D * 2, kmajor_off(lane_row, cbase + 16 * s1 + 8, C), p1 + 8);
+      for (int e = 0; e < 16; ++e) p1[e] = __fmaf_rn(dec[cbase + 16 * s1 + e], e1[e], p1[e]);
+      split8(Ah, Ah + IMGB, kmajor_off(lane_row, cbase + 16 * s1, C), p1);
+      split8(Ah, Ah + IMGB, kmajor_off(lane_row, cbase + 16 * s1 + 8, C), p1 + 8);
     }
+    fence_proxy_async();
+    __syncthreads();
+    if (t == 0) {
+      bulk_s2g(a.b.L + ch * SZ, Ah, 2 * IMGB);
+      bulk_store_commit();
+    }
+    transpose_image(Bh, Ah, C, D);
+    transpose_image(Bl, Ah + IMGB, C, D);
   }
-  fence_before_sync();
-  __syncthreads();
-  // ---- phase 4: (dO S0)^T = S0^T dO^T, then dW^T = -S0^T dU^T (the B region is reused);
-  // S0^T by transposing the S0 image in place
+  // ---- phase 4: dW^T = -S0^T dU^T and (dO S0)^T = S0^T dO^T, S0^T by transposing the S0
+  // image in place; bf16 dO (exact, hi only) waits in X and both products go together,
+  // fp32 dO (hi | lo) takes B once the first product is done
   if (ok) {
     float v[4][8];
     load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+    if (t == 0) bulk_wait_read();  // the dU^T image store has read A
+    fence_before_sync();
+    __syncthreads();
     build_dd<false>(Ah, Al, S0);
-    const bool exact = dm.out_bf16;  // bf16 dO: no lo image, no B_lo term
+    const bool exact = dm.out_bf16;
+    if (exact) {
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      int r, k0;
-      kmajor_piece(t + it * 256, D, r, k0);
-      if (exact)
-        store_bf16x8(Bh, kmajor_off(r, k0, D), v[it]);
-      else
-        split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(t + it * 256, D, r, k0);
+        store_bf16x8(Xh, kmajor_off(r, k0, D), v[it]);
+      }
     }
     __syncthreads();
     transpose_image_inplace(Ah, D);
     transpose_image_inplace(Al, D);
-    // A_hi B_hi (+ A_hi B_lo) + A_lo B_hi: with exact B the middle term adds exact zeros
-    issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), exact ? 2 : 3); });
-  }
-  if (ok) {
-    SplitTile<false, C, D> dut;  // dU rows, loaded while the first product runs
-    dut.load(a.b.dU + ch * CD, D, C);
+    issue([&] {
+      mma_terms(tb + COL_1, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3);
+      // A_hi B + A_lo B: with exact B the term A_hi B_lo adds exact zeros
+      if (exact) mma_terms(tb + COL_0, sa_h, sa_l, sx, sx, D, idesc_bf16(128, C), 2);
+    });
     run();
-    if (ok) {
-      dut.store(Bh, Bl);
-      issue([&] { mma_terms(tb + COL_1, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+    if (ok && !exact) {
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(t + it * 256, D, r, k0);
+        split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
+      }
+      issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
       run();
     }
   }
