@@ -1070,10 +1070,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
 //   phase 3  A = E^T    : (U E)^T  = E^T U^T
 //   phase 4  A = S0^T   : (dO S0)^T = S0^T dO^T,   dW^T = -S0^T dU^T
 // fp32 operands are split into bf16 hi + lo (three MMAs per product, lo x lo dropped);
-// bf16 inputs are exact.  Results go to the same global arrays as the SIMT kernel.  Sized
-// for two CTAs per SM (one A and one B operand image, 128 TMEM columns, 128 registers), so
-// that one CTA's loads and waits overlap the other's work: the two products of phase 2 and
-// of phase 4 run one after the other, and the 128 x 128 images are built in halves.
+// bf16 inputs are exact.  A transposed operand is the MN-major reading of an image already
+// in shared memory (E^T and S0^T of the E and S0 images, dO^T of the dO rows image, U and dU
+// rows of the U^T and dU^T images built from the TMEM readouts), so nothing is transposed.
+// The S0 image built in phase 1 leaves by bulk copy for two workspace slots that are free
+// here (the SIMT path's dU rows and the second half of the adjoint L slot) and comes back the
+// same way for phase 4.  Sized for two CTAs per SM (the A image pair, a 64 x 128 B image
+// pair and one more 64 x 128 image, 256 TMEM columns, 128 registers), so that one CTA's
+// loads and waits overlap the other's work.
 namespace tcg {
 constexpr int D = 128, C = 64;
 constexpr uint32_t RA = 2 * 128 * D * 2;       // A operand hi | lo (64 KB)
@@ -1248,18 +1252,6 @@ __device__ __forceinline__ void mma_terms(uint32_t d, uint32_t ahi, uint32_t alo
   }
 }
 
-// D (+)= A (B_hi + B_lo) = A_hi B_hi + A_hi B_lo: the split product when A is exact in bf16
-// (bf16 dO): its lo image would be all zeros, and the term A_lo B_hi adds exact zeros.
-__device__ __forceinline__ void mma_a_exact(uint32_t d, uint32_t a, uint32_t bhi, uint32_t blo, int K,
-                                            uint32_t idesc) {
-  const uint32_t sbo = (uint32_t)(K / 8) * 128;
-  for (int term = 0; term < 2; ++term) {
-    const uint32_t bb = term == 0 ? bhi : blo;
-    for (int kk = 0; kk < K / 16; ++kk)
-      tc::mma_bf16(d, tc::make_desc(a + kk * 256, 128, sbo), tc::make_desc(bb + kk * 256, 128, sbo), idesc,
-                   (term > 0 || kk > 0) ? 1u : 0u);
-  }
-}
 // 8 values exact in bf16 (widened bf16 inputs) as one 16-byte piece of a bf16 image
 __device__ __forceinline__ void store_bf16x8(unsigned char* img, uint32_t off, const float* v) {
   uint32_t w[4];
@@ -1274,15 +1266,15 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   using namespace tcg;
   using namespace tc;
   extern __shared__ __align__(128) unsigned char smg[];
-  unsigned char* Ah = smg;            // A operand: 128 x 128 (d x d) or 128 x 64 (dO^T)
+  unsigned char* Ah = smg;            // A: the S0 or E image pair (128 x 128)
   unsigned char* Al = Ah + RA / 2;
-  unsigned char* Bh = smg + RA;       // B operand: 64 x 128 or 64 x 64 (P^T)
+  unsigned char* Bh = smg + RA;       // B: 64 x 128 or 128 x 64 image pairs, P^T
   unsigned char* Bl = Bh + RB / 2;
   unsigned char* Xh = Bh + RB;        // a third 64 x 128 image
   float* dec = reinterpret_cast<float*>(Xh + RX);
   float* red = dec + C;                                    // 128 partial sums
-  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 128);  // [0] MMA, [1] bulk copies
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(red + 128);  // [0] MMA, [1] bulk copies, [2] S0 image back
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 3);
   if (!a.hdr->valid) return;
   const Dims dm = a.dm;
   const int t = threadIdx.x, warp = t >> 5;
@@ -1297,13 +1289,17 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   const int64_t SZ = (int64_t)D * D, CD = (int64_t)C * D;
   const float* S0 = a.saved_bnd + ch * SZ;
   const float* E = a.b.dSE + ch * SZ;
+  float* s0_hi = a.b.dU + ch * CD;           // where the S0 image waits for phase 4 (32 KB each)
+  float* s0_lo = a.b.L + ch * SZ + SZ / 2;
   const int lane_row = (warp & 3) * 32 + (t & 31);  // TMEM lane = row of the transposed result
   const int cbase = (warp >> 2) * 32;               // this warp's 32 result columns
   constexpr uint32_t IMGB = C * D * 2;  // one 64 x 128 (or 128 x 64) bf16 image
+  const bool exact = dm.out_bf16;       // bf16 dO: no lo image, no dO_lo term
   if (t < C) dec[t] = expf(__fsub_rn(a.b.G[ch * C + C - 1], a.b.G[ch * C + t]));
   if (t == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);
     fence_mbar_init();
     mbar_expect_tx(&bar[1], RB);  // the prep kernel's W rows image (hi | lo) for phase 1
     bulk_g2s(Bh, a.b.W + ch * CD, RB, &bar[1]);
@@ -1315,7 +1311,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   const uint32_t tb = *tslot;
   const uint32_t tl = tmem_lane_addr(tb, warp, 0);
   uint32_t phase = 0, cphase = 0;
-  bool ok = true, pending = false, cpending = true;
+  bool ok = true, pending = false, cpending = true, spending = false;
   auto run = [&]() {  // all threads: wait for the committed MMAs
     const bool done = mbar_wait(&bar[0], phase);
     if (done) {
@@ -1336,17 +1332,17 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     }
     pending = true;
   };
-  // the same after thread 0 has waited for the bulk copies in flight; every thread learns
-  // whether they arrived
-  auto issue_copies = [&](auto&& mmas) {
+  // the same after thread 0 has waited for the bulk copies in flight on barrier `cb` (phase
+  // `cp`); every thread learns whether they arrived
+  auto issue_after = [&](uint64_t* cb, uint32_t& cp, bool& cpend, auto&& mmas) {
     fence_proxy_async();
     fence_before_sync();
     bool got = true;
     if (t == 0) {
-      got = mbar_wait(&bar[1], cphase);
+      got = mbar_wait(cb, cp);
       if (got) {
-        cphase ^= 1u;
-        cpending = false;
+        cp ^= 1u;
+        cpend = false;
       }
     }
     ok = __syncthreads_and(got) != 0;
@@ -1359,17 +1355,23 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   };
   const uint32_t sa_h = smem_u32(Ah), sa_l = smem_u32(Al), sb_h = smem_u32(Bh), sb_l = smem_u32(Bl),
                  sx = smem_u32(Xh);
+  const uint32_t I_KK = idesc_bf16(128, C);
 
-  // ---- phase 1: U^T = Ut^T - S0 W^T
+  // ---- phase 1: U^T = Ut^T - S0 W^T; the S0 image also leaves for phase 4
   build_dd<false>(Ah, Al, S0);
-  issue_copies([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+  issue_after(&bar[1], cphase, cpending, [&] {
+    mma_split(tb + COL_0, opnd_k(sa_h, sa_l, D), opnd_k(sb_h, sb_l, D), D, I_KK, 3);
+    bulk_s2g(s0_hi, Ah, RA / 2);
+    bulk_s2g(s0_lo, Al, RA / 2);
+    bulk_store_commit();
+  });
   {
     float ut[32];  // Ut for the readout, loaded while the product runs
 #pragma unroll
     for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
     run();
-    if (ok) {  // U = Ut - (U^T)^T, kept as the U^T image (rows d, K = s): hi in X, lo in B's
-      // second half (phase 2a's K image takes the first)
+    if (ok) {  // U = Ut - (U^T)^T as the U^T image (rows d, K = s): hi in X, lo in B's second
+      // half (phase 2a's K image takes the first)
 #pragma unroll
       for (int s1 = 0; s1 < 2; ++s1) {
         float v[16];
@@ -1385,7 +1387,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   __syncthreads();
 
   // ---- phase 2a: E K^T (K rows: the prep kernel's image, one bulk copy); <E, S0> from the
-  // E build
+  // E build; the U^T image leaves for the first gradients kernel
   float part = 0.f;
   if (ok) {
     if (t == 0) {
@@ -1402,26 +1404,31 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       for (int it = 0; it < SplitTile<false, 64, D>::ITER; ++it)
 #pragma unroll
         for (int e = 0; e < 8; ++e) part = __fmaf_rn(et.v[it][e], st.v[it][e], part);
+      if (hh == 0) {
+        if (t == 0) bulk_wait_read();  // the S0 image store has read A
+        __syncthreads();
+      }
       et.store(Ah + hh * 16384, Al + hh * 16384);
     }
-    issue_copies([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_h, D, idesc_bf16(128, C), 2); });
+    issue_after(&bar[1], cphase, cpending, [&] {
+      mma_split(tb + COL_0, opnd_k(sa_h, sa_l, D), opnd_k(sb_h, sb_h, D), D, I_KK, 2);
+      bulk_s2g(a.b.U + ch * CD, Xh, IMGB);  // U^T image: hi, then lo
+      bulk_s2g(a.b.U + ch * CD + IMGB / 4, Bl, IMGB);
+      bulk_store_commit();
+    });
   }
-  // ---- phase 3: (U E)^T = E^T U^T, E^T by transposing the E image in place, U rows by
-  // transposing the U^T image (hi into B's first half, then lo into X)
+  // ---- phase 3: (U E)^T = E^T U^T, both operands MN-major readings of the E and U^T images;
+  // P^T (the prep kernel's image) comes into B's first half meanwhile
   if (ok) {
     run();
     if (ok) {
-      transpose_image_inplace(Ah, D);
-      transpose_image_inplace(Al, D);
-      transpose_image(Bh, Xh, C, D);
-      __syncthreads();
-      transpose_image(Xh, Bl, C, D);
+      if (t == 0) {
+        mbar_expect_tx(&bar[1], C * C * 4);
+        bulk_g2s(Bh, a.b.P + ch * C * C, C * C * 4, &bar[1]);
+        cpending = true;
+      }
       issue([&] {
-        mma_terms(tb + COL_2, sa_h, sa_l, sb_h, sx, D, idesc_bf16(128, C), 3);
-        // the U rows image (hi | lo) into U's slot, for the first gradients kernel
-        bulk_s2g(a.b.U + ch * CD, Bh, IMGB);
-        bulk_s2g(a.b.U + ch * CD + IMGB / 4, Xh, IMGB);
-        bulk_store_commit();
+        mma_split(tb + COL_2, opnd_mn(sa_h, sa_l, D), opnd_mn(sx, sb_l, C), D, I_KK | IDESC_A_MN | IDESC_B_MN, 3);
       });
     }
   }
@@ -1442,37 +1449,33 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     for (int o = 16; o > 0; o >>= 1) part = __fadd_rn(part, __shfl_down_sync(0xffffffffu, part, o));
     if (t == 0) a.b.sdot[ch] = part;
   }
-  // ---- phase 2b: dO^T P: dO^T from the dO rows image (transposed in shared memory), P^T the
-  // prep kernel's image (one bulk copy)
+  // ---- phase 2b: dO^T P: dO^T the MN-major reading of the dO rows image (in X; fp32 dO: lo in
+  // B's second half), P^T in B's first half; the S0 image comes back into A meanwhile
   if (ok) {
     float v[4][8];  // dO rows, loaded while E^T U^T runs
     load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
     run();
     if (ok) {
       if (t == 0) {
-        bulk_wait_read();  // the U image store has read B
-        mbar_expect_tx(&bar[1], C * C * 4);
-        bulk_g2s(Bh, a.b.P + ch * C * C, C * C * 4, &bar[1]);
-        cpending = true;
+        bulk_wait_all();  // the S0 image is in the workspace; the U^T image store has read X, B
+        mbar_expect_tx(&bar[2], RA);
+        bulk_g2s(Ah, s0_hi, RA / 2, &bar[2]);
+        bulk_g2s(Al, s0_lo, RA / 2, &bar[2]);
+        spending = true;
       }
-      const bool exact = dm.out_bf16;  // bf16 dO: no lo image, no A_lo term
+      __syncthreads();
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         int r, k0;
         kmajor_piece(t + it * 256, D, r, k0);
         if (exact)
-          store_bf16x8(Ah + 2 * IMGB, kmajor_off(r, k0, D), v[it]);
+          store_bf16x8(Xh, kmajor_off(r, k0, D), v[it]);
         else
-          split8(Ah + 2 * IMGB, Ah + 3 * IMGB, kmajor_off(r, k0, D), v[it]);  // rows hi | lo
+          split8(Xh, Bl, kmajor_off(r, k0, D), v[it]);
       }
-      __syncthreads();
-      transpose_image(Ah, Ah + 2 * IMGB, D, C);
-      if (!exact) transpose_image(Ah + IMGB, Ah + 3 * IMGB, D, C);
-      issue_copies([&] {
-        if (exact)
-          mma_a_exact(tb + COL_1, sa_h, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C));
-        else
-          mma_terms(tb + COL_1, sa_h, sa_h + IMGB, sb_h, sb_h + C * C * 2, C, idesc_bf16(128, C), 3);
+      issue_after(&bar[1], cphase, cpending, [&] {
+        mma_split(tb + COL_1, opnd_mn(sx, sb_l, D), opnd_k(sb_h, sb_h + C * C * 2, C), C, I_KK | IDESC_A_MN,
+                  exact ? -2 : 3);
       });
     }
   }
@@ -1486,9 +1489,9 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     }
     run();
   }
-  if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec) as the dU^T operand image (rows d, K = s;
-    // hi | lo) in A: one bulk copy into this chunk-head's adjoint L slot for the gradients
-    // kernel, and transposed into the dU rows image (B) for dW^T
+  if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec) as the dU^T image (rows d, K = s; hi | lo) in
+    // B: one bulk copy into this chunk-head's adjoint L slot for the gradients kernel, and
+    // read MN-major as the dU rows operand of dW^T
 #pragma unroll
     for (int s1 = 0; s1 < 2; ++s1) {
       float e1[16], p1[16];
@@ -1496,54 +1499,37 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       tmem_ld16(tl + COL_1 + cbase + 16 * s1, p1);
 #pragma unroll
       for (int e = 0; e < 16; ++e) p1[e] = __fmaf_rn(dec[cbase + 16 * s1 + e], e1[e], p1[e]);
-      split8(Ah, Ah + IMGB, kmajor_off(lane_row, cbase + 16 * s1, C), p1);
-      split8(Ah, Ah + IMGB, kmajor_off(lane_row, cbase + 16 * s1 + 8, C), p1 + 8);
+      split8(Bh, Bl, kmajor_off(lane_row, cbase + 16 * s1, C), p1);
+      split8(Bh, Bl, kmajor_off(lane_row, cbase + 16 * s1 + 8, C), p1 + 8);
     }
-    fence_proxy_async();
-    __syncthreads();
-    if (t == 0) {
-      bulk_s2g(a.b.L + ch * SZ, Ah, 2 * IMGB);
-      bulk_store_commit();
-    }
-    transpose_image(Bh, Ah, C, D);
-    transpose_image(Bl, Ah + IMGB, C, D);
   }
-  // ---- phase 4: dW^T = -S0^T dU^T and (dO S0)^T = S0^T dO^T, S0^T by transposing the S0
-  // image in place; bf16 dO (exact, hi only) waits in X and both products go together,
-  // fp32 dO (hi | lo) takes B once the first product is done
+  // ---- phase 4: dW^T = -S0^T dU^T and (dO S0)^T = S0^T dO^T, S0^T the MN-major reading of the
+  // S0 image; bf16 dO rows (exact) are still in X and both products go together, fp32 dO
+  // (hi | lo) is split again into B once dW^T is done
   if (ok) {
     float v[4][8];
-    load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
-    if (t == 0) bulk_wait_read();  // the dU^T image store has read A
-    fence_before_sync();
-    __syncthreads();
-    build_dd<false>(Ah, Al, S0);
-    const bool exact = dm.out_bf16;
-    if (exact) {
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        int r, k0;
-        kmajor_piece(t + it * 256, D, r, k0);
-        store_bf16x8(Xh, kmajor_off(r, k0, D), v[it]);
-      }
-    }
-    __syncthreads();
-    transpose_image_inplace(Ah, D);
-    transpose_image_inplace(Al, D);
-    issue([&] {
-      mma_terms(tb + COL_1, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3);
-      // A_hi B + A_lo B: with exact B the term A_hi B_lo adds exact zeros
-      if (exact) mma_terms(tb + COL_0, sa_h, sa_l, sx, sx, D, idesc_bf16(128, C), 2);
+    if (!exact) load_dO_rows(v, a.dO, false, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+    uint32_t sph = 0;
+    issue_after(&bar[2], sph, spending, [&] {
+      const Opnd s0t = opnd_mn(sa_h, sa_l, D);
+      mma_split(tb + COL_1, s0t, opnd_mn(sb_h, sb_l, C), D, I_KK | IDESC_A_MN | IDESC_B_MN, 3);
+      if (exact) mma_split(tb + COL_0, s0t, opnd_k(sx, sx, D), D, I_KK | IDESC_A_MN, 2);
+      bulk_s2g(a.b.L + ch * SZ, Bh, RB);
+      bulk_store_commit();
     });
     run();
     if (ok && !exact) {
+      if (t == 0) bulk_wait_read();  // the dU^T image store has read B
+      __syncthreads();
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
         int r, k0;
         kmajor_piece(t + it * 256, D, r, k0);
         split8(Bh, Bl, kmajor_off(r, k0, D), v[it]);
       }
-      issue([&] { mma_terms(tb + COL_0, sa_h, sa_l, sb_h, sb_l, D, idesc_bf16(128, C), 3); });
+      issue([&] {
+        mma_split(tb + COL_0, opnd_mn(sa_h, sa_l, D), opnd_k(sb_h, sb_l, D), D, I_KK | IDESC_A_MN, 3);
+      });
       run();
     }
   }
@@ -1566,8 +1552,9 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     set_error(a.hdr, GDN_DEVERR_TIMEOUT);
     if (pending) mbar_wait(&bar[0], phase);  // let this CTA's products and copies finish
     if (cpending) mbar_wait(&bar[1], cphase);
+    if (spending) mbar_wait(&bar[2], 0);
   }
-  if (t == 0) bulk_wait_all();  // the U image store is complete
+  if (t == 0) bulk_wait_all();  // the image stores are complete
   fence_before_sync();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
@@ -2034,10 +2021,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar[1], 2 * IMG);  // the d x d products kernel's U rows image (hi | lo)
+    mbar_expect_tx(&bar[1], 2 * IMG);  // the d x d products kernel's U^T image (hi | lo)
     bulk_g2s(ar + 64 * KB, a.b.U + ch * CD, 2 * IMG, &bar[1]);
   }
-  // arena: products 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U hi/lo @64/@80; then Pm hi/lo
+  // arena: products 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U^T hi/lo @64/@80; then Pm hi/lo
   // @32/@40, Pm^T @48/@56, K^T @64, Q^T @80; then T^T @0/@8, dU^T @16/@32, dW^T @48/@64
   {
     float g0 = 0.f, b0 = 0.f;
@@ -2124,12 +2111,11 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       pending = true;
     }
   };
-  // ---- products 1: Pm (raw) = dO U^T -> TMEM 0, QK = Q K^T -> TMEM 64 (after the U image)
+  // ---- products 1: Pm (raw) = dO U^T -> TMEM 0 (U rows: the MN-major reading of the U^T
+  // image), QK = Q K^T -> TMEM 64 (after the U^T image)
   issue(true, [&] {
-    if (dm.out_bf16)
-      mma_a_exact(tb + 0, sa + 32 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C));
-    else
-      mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa + 64 * KB, sa + 80 * KB, D, idesc_bf16(128, C), 3);
+    mma_split(tb + 0, opnd_k(sa + 32 * KB, sa + 48 * KB, D), opnd_mn(sa + 64 * KB, sa + 80 * KB, C), D,
+              idesc_bf16(128, C) | IDESC_B_MN, dm.out_bf16 ? -2 : 3);
     mma_terms(tb + 64, sa, sa, sa + 16 * KB, sa + 16 * KB, D, idesc_bf16(128, C), 1);
   });
   if (t < C) eG[t] = expf(Gs[t]);

@@ -4,12 +4,14 @@
 // and mbarrier waits with an iteration limit (a wait that gives up reports it instead of
 // hanging).
 //
-// Operand layout used throughout: bf16, K-major, no swizzle.  A tile of R rows x K columns
-// is stored as 8x8 "core matrices" (8 rows x 16 bytes, 128 contiguous bytes); the K/8 core
-// matrices of one 8-row group are contiguous (leading-dimension offset 128 B), and 8-row
-// groups follow each other (stride-dimension offset K/8 * 128 B):
+// Image layout used throughout: bf16, no swizzle.  A tile of R rows x K columns is stored as
+// 8x8 "core matrices" (8 rows x 16 bytes, 128 contiguous bytes); the K/8 core matrices of one
+// 8-row group are contiguous, and 8-row groups follow each other:
 //     byte(r, k) = (r / 8) * (K / 8) * 128 + (k / 8) * 128 + (r % 8) * 16 + (k % 8) * 2.
-// An MMA step over 16 columns of K advances the descriptor start address by 256 bytes.
+// Read K-major it is an operand with M (or N) = R (leading-dimension offset 128 B, stride-
+// dimension offset K/8 * 128 B; a step over 16 of K advances the start address by 256 B);
+// read MN-major (the instruction descriptor's transpose bit) it is the transposed operand,
+// with M (or N) = K and K = R (see Opnd).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -52,6 +54,24 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, dense.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with the A (bit 15) and / or B (bit 16) operand read MN-major
+constexpr uint32_t IDESC_A_MN = 1u << 15, IDESC_B_MN = 1u << 16;
+
+// An MMA operand in shared memory: a split image pair (hi, lo; lo unused where the operand is
+// exact) and how the descriptor walks it.  K-major: the layout above, rows along M (or N),
+// K = the image's columns.  MN-major: the same bytes read as their transpose, so that an
+// image with R rows and W columns serves as an operand with M (or N) = W and K = R (core
+// matrices adjacent along M or N are 128 B apart, along K W/8 * 128 B); its descriptors
+// advance by two 8-row groups per 16 of K.
+struct Opnd {
+  uint32_t hi, lo, lbo, sbo, kstep;
+};
+__device__ __forceinline__ Opnd opnd_k(uint32_t hi, uint32_t lo, int K) {
+  return Opnd{hi, lo, 128u, (uint32_t)K * 16u, 256u};
+}
+__device__ __forceinline__ Opnd opnd_mn(uint32_t hi, uint32_t lo, int W) {
+  return Opnd{hi, lo, (uint32_t)W * 16u, 128u, (uint32_t)W * 32u};
 }
 
 // ---------------------------------------------------------------- mbarrier ----
@@ -168,6 +188,22 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// One thread: D (+)= A_x B_y^T over K for one pair of split parts (x, y: hi or lo)
+__device__ __forceinline__ void mma_part(uint32_t d, const Opnd& A, bool alo, const Opnd& B, bool blo, int K,
+                                         uint32_t idesc, bool accumulate) {
+  const uint32_t a = alo ? A.lo : A.hi, b = blo ? B.lo : B.hi;
+  for (int kk = 0; kk < K / 16; ++kk)
+    mma_bf16(d, make_desc(a + kk * A.kstep, A.lbo, A.sbo), make_desc(b + kk * B.kstep, B.lbo, B.sbo), idesc,
+             (accumulate || kk > 0) ? 1u : 0u);
+}
+// D = A B^T from split parts, in this order: terms 3: A_hi B_hi + A_hi B_lo + A_lo B_hi;
+// 2 (B exact): A_hi B + A_lo B; -2 (A exact): A B_hi + A B_lo; 1 (both exact): A B
+__device__ __forceinline__ void mma_split(uint32_t d, const Opnd& A, const Opnd& B, int K, uint32_t idesc,
+                                          int terms) {
+  mma_part(d, A, false, B, false, K, idesc, false);
+  if (terms == 3 || terms == -2) mma_part(d, A, false, B, true, K, idesc, true);
+  if (terms == 3 || terms == 2) mma_part(d, A, true, B, false, K, idesc, true);
 }
 // One thread: arrive on `bar` once all previously issued MMAs of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -289,53 +325,6 @@ __device__ __forceinline__ void transpose_image(unsigned char* dst, const unsign
 #pragma unroll
     for (int k = 0; k < 4; ++k)
       if (c0 + 32 * k + 4 * warp < ncore) stsm_x4(da[k], r[k]);
-  }
-}
-
-// In-place transpose of a square N x N K-major image (N = 64 or 128); 256 threads.  Core
-// matrices (a, b) and (b, a) trade places, each transposed, two pairs per warp instruction;
-// then the diagonal cores, four per instruction.  With nb = N / 8 cores a side, unordered
-// pair p < nb (nb/2 - 1) is (a, a + k mod nb), k = 1 + p / nb, a = p mod nb, and the others
-// are (a, a + nb/2).  A core is read and rewritten by one warp only, and each batch of a
-// warp's ldmatrix completes before its stmatrix (the registers carry the data).
-__device__ __forceinline__ void transpose_image_inplace(unsigned char* img, int N) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nb = N / 8, npair_ops = nb * (nb - 1) / 4, nops = npair_ops + nb / 4;
-  const int nfirst = nb * (nb / 2 - 1);
-  const uint32_t sbo = (uint32_t)nb * 128;
-  const uint32_t base = smem_u32(img) + (lane & 7) * 16;
-  const int slot = lane >> 3;
-  for (int o0 = warp; o0 < nops; o0 += 32) {  // batches of up to four ops per warp
-    uint32_t r[4][4], da[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int o = o0 + 8 * k;
-      if (o < nops) {
-        int y, x;  // core loaded by this lane's slot; the slot stores to core (x, y)
-        if (o < npair_ops) {
-          const int p = 2 * o + (slot >> 1);
-          int pa, pb;
-          if (p < nfirst) {
-            pa = p % nb;
-            pb = (pa + 1 + p / nb) % nb;
-          } else {
-            pa = p - nfirst;
-            pb = pa + nb / 2;
-          }
-          y = (slot & 1) ? pb : pa;
-          x = (slot & 1) ? pa : pb;
-        } else {
-          y = x = 4 * (o - npair_ops) + slot;
-        }
-        ldsm_x4_trans(base + y * sbo + x * 128, r[k]);
-        da[k] = base + x * sbo + y * 128;
-      }
-    }
-    // register i holds the transpose of slot i's core; slot i's lanes give the address it
-    // goes to
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (o0 + 8 * k < nops) stsm_x4(da[k], r[k]);
   }
 }
 
