@@ -2025,7 +2025,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     bulk_g2s(ar + 64 * KB, a.b.U + ch * CD, 2 * IMG, &bar[1]);
   }
   // arena: products 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U^T hi/lo @64/@80; then Pm hi/lo
-  // @32/@40, Pm^T @48/@56, K^T @64, Q^T @80; then T^T @0/@8, dU^T @16/@32, dW^T @48/@64
+  // @32/@40 (with Q, K rows); then T^T @0/@8, dU^T @16/@32, dW^T @48/@64, V rows @80
   {
     float g0 = 0.f, b0 = 0.f;
     if (t < C) {
@@ -2151,15 +2151,13 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   }
   fence_before_sync();
   __syncthreads();
-  // ---- products 2: dQ = Pm K -> TMEM 0, dK1 = Pm^T Q -> TMEM 128
+  // ---- products 2: dQ = Pm K -> TMEM 0, dK1 = Pm^T Q -> TMEM 128; K^T, Q^T and Pm^T are the
+  // MN-major readings of the K rows, Q rows and Pm images
   if (ok) {
-    tc::transpose_image(ar + 48 * KB, ar + 32 * KB, C, C);  // Pm^T hi
-    tc::transpose_image(ar + 56 * KB, ar + 40 * KB, C, C);  // Pm^T lo
-    tc::transpose_image(ar + 64 * KB, ar + 16 * KB, D, C);  // K^T
-    tc::transpose_image(ar + 80 * KB, ar, D, C);            // Q^T
     issue(false, [&] {
-      mma_terms(tb + 0, sa + 32 * KB, sa + 40 * KB, sa + 64 * KB, sa + 64 * KB, C, idesc_bf16(128, D), 2);
-      mma_terms(tb + 128, sa + 48 * KB, sa + 56 * KB, sa + 80 * KB, sa + 80 * KB, C, idesc_bf16(128, D), 2);
+      const Opnd pm_k = opnd_k(sa + 32 * KB, sa + 40 * KB, C), pm_t = opnd_mn(sa + 32 * KB, sa + 40 * KB, C);
+      mma_split(tb + 0, pm_k, opnd_mn(sa + 16 * KB, sa + 16 * KB, D), C, idesc_bf16(128, D) | IDESC_B_MN, 2);
+      mma_split(tb + 128, pm_t, opnd_mn(sa, sa, D), C, idesc_bf16(128, D) | IDESC_A_MN | IDESC_B_MN, 2);
     });
     if (ok) wait_mma();
   }
@@ -2172,7 +2170,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     bulk_g2s(ar + 48 * KB, a.b.dW + ch * CD, 2 * IMG, &bar[1]);
     cpending = true;
   }
-  // dQ readout (row warps) || V rows image for the dv readout over the dead Q^T (other warps)
+  // dQ readout (row warps) || V rows image for the dv readout over the dead U^T lo (other warps)
   if (ok) {
     if (rowlane) {
       const int i = row;
@@ -2366,7 +2364,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   const int row = (warp & 3) * 32 + lane;
   const int half = warp >> 2;
   // arena: products A W hi/lo @0/@16, Y hi|lo @32, K rows @64; products B Ut hi/lo @0/@16,
-  // X hi|lo @32, K^T @80; products C dAm hi/lo @0/@8, dAm^T hi/lo @16/@24
+  // X hi|lo @32; products C dAm hi/lo @0/@8 (with the K rows)
   if (t == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -2449,7 +2447,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
       cpending = true;
     }
     ut.store(ar, ar + 16 * KB);
-    transpose_image(ar + 80 * KB, ar + 64 * KB, D, C);  // K^T
     issue(true, [&] {
       mma_terms(tb + 0, sa + 32 * KB, sa + 48 * KB, sa, sa + 16 * KB, D, idesc_bf16(128, C), 3, true);
     });
@@ -2492,13 +2489,15 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   }
   fence_before_sync();
   __syncthreads();
-  // ---- products C: dK2 = dAm K + dAm^T K -> TMEM 0
+  // ---- products C: dK2 = dAm K + dAm^T K -> TMEM 0; dAm^T and K^T are the MN-major readings
+  // of the dAm and K rows images
   if (ok) {
-    transpose_image(ar + 16 * KB, ar, C, C);
-    transpose_image(ar + 24 * KB, ar + 8 * KB, C, C);
     issue(false, [&] {
-      mma_terms(tb + 0, sa, sa + 8 * KB, sa + 80 * KB, sa + 80 * KB, C, idesc_bf16(128, D), 2);
-      mma_terms(tb + 0, sa + 16 * KB, sa + 24 * KB, sa + 80 * KB, sa + 80 * KB, C, idesc_bf16(128, D), 2, true);
+      const Opnd kt = opnd_mn(sa + 64 * KB, sa + 64 * KB, D);
+      mma_split(tb + 0, opnd_k(sa, sa + 8 * KB, C), kt, C, idesc_bf16(128, D) | IDESC_B_MN, 2);
+      const Opnd dat = opnd_mn(sa, sa + 8 * KB, C);
+      mma_part(tb + 0, dat, false, kt, false, C, idesc_bf16(128, D) | IDESC_A_MN | IDESC_B_MN, true);
+      mma_part(tb + 0, dat, true, kt, false, C, idesc_bf16(128, D) | IDESC_A_MN | IDESC_B_MN, true);
     });
     if (ok) wait_mma();
   }
