@@ -1560,6 +1560,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   if (warp == 0) tmem_dealloc(tb, TMEM_COLS);
 }
 
+// e^{G_i - G_s} for s <= i, packed by rows at i (i + 1) / 2 + s; all 256 threads, C = 64
+__device__ __forceinline__ void decay_table_lower(float* tab, const float* Gs) {
+  const int i = threadIdx.x & 63;
+  for (int s = threadIdx.x >> 6; s <= i; s += 4) tab[i * (i + 1) / 2 + s] = expf(__fsub_rn(Gs[i], Gs[s]));
+}
+
 // ============================================================  KB1 (tcgen05)  ===
 // Backward prep on tensor cores (bf16 inputs, d = 128, C = 64), one CTA of 256 threads per
 // chunk-head, every chunk zero-padded to C:
@@ -1813,9 +1819,11 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   }
   tc::transpose_image(KT, Wr, D, C);
   tc::transpose_image(VT, Wr + TILE, D, C);
+  float* gam = Tm;  // e^{G_i - G_s} (s <= i) over the dead T, by all threads
+  decay_table_lower(gam, Gs);
   if (t == 0) bulk_wait_read();  // the P readout writes over the W rows image
   if (ok) wait_mma();
-  if (ok && (warp & 3) < 2) {  // P rows -> global and as the split image (over the dead W rows)
+  if (ok && (warp & 3) < 2) {  // P rows as the split image (over the dead W rows)
     const int i = lrow;
     for (int s0 = chalf * 32; s0 < chalf * 32 + 32; s0 += 16) {
       float v[16];
@@ -1823,7 +1831,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int s = s0 + e;
-        v[e] = (i >= s) ? __fmul_rn(expf(__fsub_rn(Gs[i], Gs[s])), v[e]) : 0.f;
+        v[e] = (i >= s) ? __fmul_rn(gam[i * (i + 1) / 2 + s], v[e]) : 0.f;
       }
       split8(TKh, TKl, kmajor_off(i, s0, C), v);
       split8(TKh, TKl, kmajor_off(i, s0 + 8, C), v + 8);
@@ -1963,12 +1971,6 @@ constexpr size_t SMEM1 = ARENA + (13 * C + TRI) * 4 + 64;
 constexpr size_t SMEM2 = ARENA + (18 * C + TRI) * 4 + 64;
 constexpr uint32_t TMEM1 = 256, TMEM2 = 128;
 }  // namespace tcd
-
-// e^{G_i - G_s} for s <= i, packed by rows at i (i + 1) / 2 + s; all 256 threads, C = 64
-__device__ __forceinline__ void decay_table_lower(float* tab, const float* Gs) {
-  const int i = threadIdx.x & 63;
-  for (int s = threadIdx.x >> 6; s <= i; s += 4) tab[i * (i + 1) / 2 + s] = expf(__fsub_rn(Gs[i], Gs[s]));
-}
 
 // fixed-order warp sum (xor tree); every lane gets the total
 __device__ __forceinline__ float warp_sum(float x) {
