@@ -203,7 +203,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* A, float* Tm, fl
 // Per chunk-head workspace (floats), chunk length padded to C.
 struct BwdBufs {
   float *W, *Ut, *T, *P, *G, *L, *dSE, *U, *dU, *dOS0, *UdSe, *dW, *sdot;
-  float* img;  // tensor-core shapes: per chunk-head [K rows | W^T hi | W^T lo] bf16 images
+  float* img;  // tensor-core shapes: per chunk-head the K rows bf16 image, then scratch
   float *dq_part, *dk_part;  // [T, Hv, D]
 };
 
@@ -800,14 +800,15 @@ __global__ void k_bwd_gqa(const float* __restrict__ dq_part, const float* __rest
 //                                                  bf16 dO exact; fp32 dO: 3)
 //     Xd[i][s]       = -dec_s D1[i][s]            (split to bf16 hi/lo)
 //     D2            += Xd W                       3 MMAs with W = W_hi + W_lo
-// giving dS^(j).  Operands [K rows | W^T hi | W^T lo] come as one bulk copy per chunk,
-// prefetched a chunk ahead; the dO^T and Qt^T images (the prep kernel's, in L's slot) as
-// another, issued as soon as the previous step's Xd W has consumed the region.
+// giving dS^(j).  The K rows and W rows (hi | lo) images come by bulk copy a chunk ahead;
+// the dO and Qt rows images (the prep kernel's, in L's slot) by another, issued as soon as
+// the previous step's Xd W has consumed the region.  W^T, dO^T and Qt^T are the MN-major
+// readings of the row images.
 namespace tcb {
 constexpr int D = 128, C = 64;
 constexpr uint32_t A1_BYTES = 128 * D * 2, A2_BYTES = 128 * C * 2, STAGE_BYTES = 3 * C * D * 2;
-// the L = dO^T Qt operands of a step, as the prep kernel left them in L's slot:
-// dO^T hi | Qt^T hi | Qt^T lo | dO^T lo (the last only for fp32 dO); Xd is built over them
+// the L = dO^T Qt operands of a step, as the prep kernel left them in L's slot (row images):
+// dO hi | Qt hi | Qt lo | dO lo (the last only for fp32 dO); Xd is built over them
 constexpr uint32_t IMG = C * D * 2, LA_BYTES = 4 * IMG;
 constexpr size_t SMEM = 2 * (size_t)A1_BYTES + 2 * (size_t)STAGE_BYTES + LA_BYTES + 64 * 4 + 64;
 constexpr uint32_t TMEM_COLS = 256, D1_COL = 0, D2_COL = 64;
@@ -840,7 +841,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   unsigned char* A1h = smb;
   unsigned char* A1l = A1h + A1_BYTES;
   unsigned char* stage0 = A1l + A1_BYTES;
-  unsigned char* LA = stage0 + 2 * STAGE_BYTES;  // this step's dO^T, Qt^T images; then Xd
+  unsigned char* LA = stage0 + 2 * STAGE_BYTES;  // this step's dO, Qt rows images; then Xd
   unsigned char* A2h = LA;
   unsigned char* A2l = LA + A2_BYTES;
   float* decs = reinterpret_cast<float*>(LA + LA_BYTES);
@@ -899,16 +900,21 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
   auto gamma_of = [&](int j) { return expf(a.b.G[chead(j) * C + C - 1]); };
   const bool dexact = dm.out_bf16;  // bf16 dO: no dO^T lo image
   const uint32_t la_bytes = dexact ? 3 * IMG : 4 * IMG;
-  auto load_la = [&](int j) {  // thread 0: chunk j's dO^T and Qt^T images
+  auto load_la = [&](int j) {  // thread 0: chunk j's dO and Qt rows images
     mbar_expect_tx(&bars[3], la_bytes);
     bulk_g2s(LA, a.b.L + chead(j) * SZ, la_bytes, &bars[3]);
+  };
+  auto load_stage = [&](int j, int b) {  // thread 0: chunk j's K rows and W rows (hi | lo) images
+    unsigned char* dst = stage0 + b * STAGE_BYTES;
+    mbar_expect_tx(&bars[b], STAGE_BYTES);
+    bulk_g2s(dst, a.b.img + chead(j) * IW, IMG, &bars[b]);
+    bulk_g2s(dst + IMG, a.b.W + chead(j) * C * D, 2 * IMG, &bars[b]);
   };
   // prologue: dS^(nch) = dstate_out is the end adjoint of the last chunk
   {
     const int j = nch - 1;
     if (t == 0) {
-      mbar_expect_tx(&bars[0], STAGE_BYTES);
-      bulk_g2s(stage0, a.b.img + chead(j) * IW, STAGE_BYTES, &bars[0]);
+      load_stage(j, 0);
       load_la(j);
     }
     const float g = gamma_of(j);
@@ -938,10 +944,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
     const int j = nch - 1 - q;
     const int buf = q & 1;
     unsigned char* stg = stage0 + buf * STAGE_BYTES;
-    if (j > 0 && t == 0) {
-      mbar_expect_tx(&bars[buf ^ 1], STAGE_BYTES);
-      bulk_g2s(stage0 + (buf ^ 1) * STAGE_BYTES, a.b.img + chead(j - 1) * IW, STAGE_BYTES, &bars[buf ^ 1]);
-    }
+    if (j > 0 && t == 0) load_stage(j - 1, buf ^ 1);
     if (t < C) decs[t] = -expf(__fsub_rn(a.b.G[chead(j) * C + C - 1], a.b.G[chead(j) * C + t]));
     const float gpre = j > 0 ? gamma_of(j - 1) : 0.f;
     ok = __syncthreads_and(mbar_wait(&bars[buf], uses[buf] & 1u) && mbar_wait(&bars[3], la_uses & 1u)) != 0;
@@ -960,14 +963,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
           mma_bf16(tbase + D1_COL, make_desc(aa + kk * 256, 128, sbo), make_desc(kimg + kk * 256, 128, sbo),
                    idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
       }
-      const uint32_t dh = smem_u32(LA), qh = dh + IMG, ql = dh + 2 * IMG, dl = dh + 3 * IMG, lsbo = (C / 8) * 128;
-#pragma unroll 1
-      for (int term = 0; term < (dexact ? 2 : 3); ++term) {  // dO_hi Qt_hi + dO_hi Qt_lo (+ dO_lo Qt_hi)
-        const uint32_t aa = term == 2 ? dl : dh, bb = term == 1 ? ql : qh;
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16(tbase + D2_COL, make_desc(aa + kk * 256, 128, lsbo), make_desc(bb + kk * 256, 128, lsbo),
-                   idesc_bf16(128, D), 1u);
-      }
+      // dO_hi Qt_hi + dO_hi Qt_lo (+ dO_lo Qt_hi), dO^T and Qt^T the MN-major readings of the
+      // row images
+      const uint32_t dh = smem_u32(LA);
+      const Opnd dOt = opnd_mn(dh, dh + 3 * IMG, D), Qtt = opnd_mn(dh + IMG, dh + 2 * IMG, D);
+      const uint32_t il = idesc_bf16(128, D) | IDESC_A_MN | IDESC_B_MN;
+      mma_part(tbase + D2_COL, dOt, false, Qtt, false, C, il, true);
+      mma_part(tbase + D2_COL, dOt, false, Qtt, true, C, il, true);
+      if (!dexact) mma_part(tbase + D2_COL, dOt, true, Qtt, false, C, il, true);
       mma_commit(&bars[2]);
     }
     mma_pending = true;
@@ -987,17 +990,14 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();
-    if (t == 0) {  // D2 += Xd W (three split terms)
+    if (t == 0) {  // D2 += Xd W (three split terms; W^T the MN-major reading of the W rows)
       fence_after_sync();
-      const uint32_t wh = smem_u32(stg) + C * D * 2, wl = wh + C * D * 2, sbo = (C / 8) * 128;
-#pragma unroll 1
-      for (int term = 0; term < 3; ++term) {
-        const uint32_t aa = smem_u32(term == 2 ? A2l : A2h);
-        const uint32_t bb = term == 1 ? wl : wh;
-        for (int kk = 0; kk < C / 16; ++kk)
-          mma_bf16(tbase + D2_COL, make_desc(aa + kk * 256, 128, sbo), make_desc(bb + kk * 256, 128, sbo),
-                   idesc_bf16(128, D), 1u);
-      }
+      const uint32_t wh = smem_u32(stg) + C * D * 2;
+      const Opnd xd = opnd_k(smem_u32(A2h), smem_u32(A2l), C), wt = opnd_mn(wh, wh + C * D * 2, D);
+      const uint32_t iw = idesc_bf16(128, D) | IDESC_B_MN;
+      mma_part(tbase + D2_COL, xd, false, wt, false, C, iw, true);
+      mma_part(tbase + D2_COL, xd, false, wt, true, C, iw, true);
+      mma_part(tbase + D2_COL, xd, true, wt, false, C, iw, true);
       mma_commit(&bars[2]);
     }
     mma_pending = true;
@@ -1006,7 +1006,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd_chain_tc(BwdArgs a) {
     mma_phase ^= 1u;
     mma_pending = false;
     fence_after_sync();
-    if (j > 0 && t == 0) {  // the next step's dO^T, Qt^T images over the consumed Xd
+    if (j > 0 && t == 0) {  // the next step's dO, Qt rows images over the consumed Xd
       load_la(j - 1);
       la_pending = true;
     }
@@ -1185,25 +1185,8 @@ __device__ __forceinline__ void unpack8(const uint4 u, float* o) {
 
 // dO pieces of 256 threads for d = 128, C = 64 (4 per thread), tokens >= n zero.  The
 // dtype branch is outside the loops, so that all of a thread's loads are in flight together.
-// load_dO_T: piece q = t + 256 it is value dim r = q % 128 of tokens (q / 128) * 8 .. + 7
-// (a K-major image of dO^T); load_dO_rows: piece q is 8 consecutive dims of one token, in
-// kmajor_piece order (a K-major image of dO), read as one 16-byte (bf16) or two (fp32) loads.
-template <typename T>
-__device__ __forceinline__ void load_dO_T_t(float (&v)[4][8], const T* p, int64_t tstride, int n) {
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int q = threadIdx.x + it * 256, r = q % 128, k0 = (q / 128) * 8;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[it][e] = (k0 + e < n) ? to_f32(p[(int64_t)(k0 + e) * tstride + r]) : 0.f;
-  }
-}
-__device__ __forceinline__ void load_dO_T(float (&v)[4][8], const void* dO, bool bf16, int64_t base,
-                                          int64_t tstride, int n) {
-  if (bf16)
-    load_dO_T_t(v, static_cast<const __nv_bfloat16*>(dO) + base, tstride, n);
-  else
-    load_dO_T_t(v, static_cast<const float*>(dO) + base, tstride, n);
-}
+// load_dO_rows: piece q = t + 256 it is 8 consecutive dims of one token, in kmajor_piece order
+// (a K-major image of dO), read as one 16-byte (bf16) or two (fp32) loads.
 template <typename T>
 __device__ __forceinline__ void load_dO_rows_t(float (&v)[4][8], const T* p, int64_t tstride, int n) {
 #pragma unroll
@@ -1268,7 +1251,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   extern __shared__ __align__(128) unsigned char smg[];
   unsigned char* Ah = smg;            // A: the S0 or E image pair (128 x 128)
   unsigned char* Al = Ah + RA / 2;
-  unsigned char* Bh = smg + RA;       // B: 64 x 128 or 128 x 64 image pairs, P^T
+  unsigned char* Bh = smg + RA;       // B: 64 x 128 or 128 x 64 image pairs, P rows
   unsigned char* Bl = Bh + RB / 2;
   unsigned char* Xh = Bh + RB;        // a third 64 x 128 image
   float* dec = reinterpret_cast<float*>(Xh + RX);
@@ -1418,7 +1401,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     });
   }
   // ---- phase 3: (U E)^T = E^T U^T, both operands MN-major readings of the E and U^T images;
-  // P^T (the prep kernel's image) comes into B's first half meanwhile
+  // P rows (the prep kernel's image) come into B's first half meanwhile
   if (ok) {
     run();
     if (ok) {
@@ -1450,7 +1433,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     if (t == 0) a.b.sdot[ch] = part;
   }
   // ---- phase 2b: dO^T P: dO^T the MN-major reading of the dO rows image (in X; fp32 dO: lo in
-  // B's second half), P^T in B's first half; the S0 image comes back into A meanwhile
+  // B's second half), P^T that of the P rows (B's first half); the S0 image comes back into A
+  // meanwhile
   if (ok) {
     float v[4][8];  // dO rows, loaded while E^T U^T runs
     load_dO_rows(v, a.dO, dm.out_bf16, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
@@ -1474,8 +1458,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
           split8(Xh, Bl, kmajor_off(r, k0, D), v[it]);
       }
       issue_after(&bar[1], cphase, cpending, [&] {
-        mma_split(tb + COL_1, opnd_mn(sx, sb_l, D), opnd_k(sb_h, sb_h + C * C * 2, C), C, I_KK | IDESC_A_MN,
-                  exact ? -2 : 3);
+        mma_split(tb + COL_1, opnd_mn(sx, sb_l, D), opnd_mn(sb_h, sb_h + C * C * 2, C), C,
+                  I_KK | IDESC_A_MN | IDESC_B_MN, exact ? -2 : 3);
       });
     }
   }
@@ -1572,12 +1556,13 @@ __device__ __forceinline__ void decay_table_lower(float* tab, const float* Gs) {
 //   Gram = K K^T, T = (I + A)^{-1} (SIMT), W = TK K, U^T = V^T TV^T    (as the forward pre-pass)
 //   P    = Gam (.) (Q K^T), lower with diagonal                       (exact bf16 inputs)
 //   Qt   = diag(e^G) Q - P W                                          (P, W split hi/lo)
-//   dO^T, Qt^T                                                        (the operands of L = dO^T Qt)
-// Outputs: the W rows image (W's slot), Ut, G, the reverse chain's images [K rows | W^T hi |
-// W^T lo] and the operands of L (L's slot; the reverse chain forms L = dO^T Qt on its tensor
-// cores), and two more operand images: P^T for the big-products kernel (in P's slot) and T^T
-// for the gradients kernel (in T's slot).  W, P and Qt also leave their readouts as split
-// images in shared memory, where the transposed operands are built.
+//   dO, Qt rows                                                       (the operands of L = dO^T Qt)
+// Outputs: the W rows image (W's slot), Ut, G, the K rows image (the reverse chain's, with
+// the W rows), the operands of L (L's slot; the reverse chain forms L = dO^T Qt on its tensor
+// cores, reading the row images MN-major), and two more operand images: P rows for the
+// big-products kernel (in P's slot) and T^T for the gradients kernel (in T's slot).  W, P
+// and Qt also leave their readouts as split images in shared memory, where the later
+// products read them (W^T as the MN-major reading of the W rows).
 namespace tcq {
 constexpr int D = 128, C = 64, QCP = C + 1, TCP = C;  // row strides of A (padded) and T
 constexpr uint32_t TILE = C * D * 2;  // 16 KB
@@ -1801,7 +1786,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       }
     }
   }
-  // ---- 4. P = Gam (.) (Q K^T); meanwhile W^T hi | lo from the W rows (over the dead K^T, V^T)
+  // ---- 4. P = Gam (.) (Q K^T); the W rows image stays for step 5 (its B operand is W^T, the
+  // MN-major reading of the W rows)
   sync_for_mma();
   if (ok && t == 0) {
     fence_after_sync();
@@ -1812,18 +1798,17 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     mma_commit(bar);
   }
   if (t == 0) {  // asynchronous bulk stores: the K rows image for the reverse chain, and the W
-                 // rows image (hi | lo) into W's slot for the d x d products and gradients kernels
+                 // rows image (hi | lo) into W's slot for the reverse chain, the d x d products
+                 // and gradients kernels
     bulk_s2g(img, Ki, TILE);
     bulk_s2g(a.b.W + ch * CD, Wr, 2 * TILE);
     bulk_store_commit();
   }
-  tc::transpose_image(KT, Wr, D, C);
-  tc::transpose_image(VT, Wr + TILE, D, C);
   float* gam = Tm;  // e^{G_i - G_s} (s <= i) over the dead T, by all threads
   decay_table_lower(gam, Gs);
-  if (t == 0) bulk_wait_read();  // the P readout writes over the W rows image
+  unsigned char* Ph = KT;  // P rows image, hi | lo (8 KB each), over the dead K^T
   if (ok) wait_mma();
-  if (ok && (warp & 3) < 2) {  // P rows as the split image (over the dead W rows)
+  if (ok && (warp & 3) < 2) {
     const int i = lrow;
     for (int s0 = chalf * 32; s0 < chalf * 32 + 32; s0 += 16) {
       float v[16];
@@ -1833,22 +1818,21 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
         const int s = s0 + e;
         v[e] = (i >= s) ? __fmul_rn(gam[i * (i + 1) / 2 + s], v[e]) : 0.f;
       }
-      split8(TKh, TKl, kmajor_off(i, s0, C), v);
-      split8(TKh, TKl, kmajor_off(i, s0 + 8, C), v + 8);
+      split8(Ph, Ph + C * C * 2, kmajor_off(i, s0, C), v);
+      split8(Ph, Ph + C * C * 2, kmajor_off(i, s0 + 8, C), v + 8);
     }
   }
-  // ---- 5. Qt = diag(e^G) Q - P W: A = P (rows i), B = W^T (rows c)
-  // dO for step 6, loaded while the product runs: bf16 dO as rows (four 16-byte pieces per
-  // thread, held bit for bit in dov[it][0..3]) for an image transposed in shared memory; fp32
-  // dO as dO^T pieces to split
+  // ---- 5. Qt = diag(e^G) Q - P W: A = P (rows i), B = W^T; dO rows for step 6, loaded while
+  // the product runs (bf16 dO held bit for bit in dov[it][0..3], fp32 dO as values)
   float dov[4][8];
   if (ok) {
     sync_for_mma();
     if (t == 0) {
       fence_after_sync();
-      mma_terms(tb + COL_QT, smem_u32(TKh), smem_u32(TKl), smem_u32(KT), smem_u32(VT), C, idesc_bf16(128, D), 3);
+      mma_split(tb + COL_QT, opnd_k(smem_u32(Ph), smem_u32(Ph) + C * C * 2, C),
+                opnd_mn(smem_u32(Wr), smem_u32(Wr) + TILE, D), C, idesc_bf16(128, D) | IDESC_B_MN, 3);
       mma_commit(bar);
-      bulk_s2g(img + TILE, KT, 2 * TILE);  // W^T images (hi | lo) for the reverse chain
+      bulk_s2g(a.b.P + ch * C * C, Ph, C * C * 4);  // the P rows image for the d x d products kernel
       bulk_store_commit();
     }
     if (dm.out_bf16) {
@@ -1864,23 +1848,14 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
         dov[it][3] = __uint_as_float(x.w);
       }
     } else {
-      load_dO_T(dov, a.dO, false, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
+      load_dO_rows(dov, a.dO, false, (tok0 * dm.hv + h) * D, (int64_t)dm.hv * D, n);
     }
-    // P^T hi | lo (over the dead TV) -> P's slot: the big-products kernel's operand image
-    tc::transpose_image(smq + OFF_TV, TKh, C, C);
-    tc::transpose_image(smq + OFF_TV + C * C * 2, TKl, C, C);
-    fence_proxy_async();
-    __syncthreads();
-    if (t == 0) {
-      bulk_s2g(a.b.P + ch * C * C, smq + OFF_TV, C * C * 4);
-      bulk_store_commit();
-      bulk_wait_read();  // the Qt readout writes over it, step 6 over K^T, V^T and the K rows
-    }
+    if (t == 0) bulk_wait_read();  // the Qt readout writes over P, step 6 over the K and W rows
     wait_mma();
   }
-  // Qt rows hi | lo over the dead TV and T regions
-  unsigned char* Qrh = smq + OFF_TV;
-  unsigned char* Qrl = smq + OFF_T;
+  // Qt rows hi | lo over the dead P (K^T) and V^T
+  unsigned char* Qrh = KT;
+  unsigned char* Qrl = VT;
   if (ok && (warp & 3) < 2) {
     const int i = lrow;
     const float egi = expf(Gs[i]);
@@ -1895,36 +1870,24 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       split8(Qrh, Qrl, kmajor_off(i, c0 + 8, D), v + 8);
     }
   }
-  fence_before_sync();
-  __syncthreads();
-  // ---- 6. the operands of L = dO^T Qt, which the reverse chain forms on its tensor cores:
-  // dO^T (rows p, K = i) over the dead K rows (its lo image, fp32 dO only, over the dead P),
-  // Qt^T hi | lo (rows q, K = i) over the dead W^T; the four regions are contiguous and leave
-  // as one bulk store into L's slot: [dO^T hi | Qt^T hi | Qt^T lo (| dO^T lo)]
+  // ---- 6. the operands of L = dO^T Qt, which the reverse chain forms on its tensor cores
+  // reading dO^T and Qt^T MN-major from the row images: dO rows over the dead K rows (its lo
+  // image, fp32 dO only, over the dead W rows hi), after the Qt rows; the four regions are
+  // contiguous and leave as one bulk store into L's slot: [dO hi | Qt hi | Qt lo (| dO lo)]
   static_assert(OFF_KT == OFF_K + TILE && OFF_VT == OFF_KT + TILE && OFF_TK == OFF_VT + TILE,
-                "dO^T, Qt^T hi, Qt^T lo, dO^T lo contiguous");
+                "dO, Qt hi, Qt lo, dO lo contiguous");
   if (ok) {
-    if (dm.out_bf16) {  // dO rows image over the dead Q rows, transposed into dO^T; dO is exact
-      unsigned char* Dr = smq + OFF_A;
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        int r, c0;
-        kmajor_piece(t + it * 256, D, r, c0);
-        *reinterpret_cast<uint4*>(Dr + kmajor_off(r, c0, D)) =
-            make_uint4(__float_as_uint(dov[it][0]), __float_as_uint(dov[it][1]), __float_as_uint(dov[it][2]),
-                       __float_as_uint(dov[it][3]));
-      }
-      __syncthreads();
-      tc::transpose_image(Ki, Dr, D, C);
-    } else {
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int q = t + it * 256, r = q % D, k0 = (q / D) * 8;
-        split8(Ki, TKh, kmajor_off(r, k0, C), dov[it]);
-      }
+    for (int it = 0; it < 4; ++it) {
+      int r, c0;
+      kmajor_piece(t + it * 256, D, r, c0);
+      const uint32_t off = kmajor_off(r, c0, D);
+      if (dm.out_bf16)
+        *reinterpret_cast<uint4*>(Ki + off) = make_uint4(__float_as_uint(dov[it][0]), __float_as_uint(dov[it][1]),
+                                                         __float_as_uint(dov[it][2]), __float_as_uint(dov[it][3]));
+      else
+        split8(Ki, TKh, off, dov[it]);
     }
-    tc::transpose_image(KT, Qrh, D, C);
-    tc::transpose_image(VT, Qrl, D, C);
     fence_proxy_async();
     fence_before_sync();
     __syncthreads();

@@ -108,23 +108,68 @@ extern "C" int transpose_selftest(const void* X, void* Y, int R, int Ks, cudaStr
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }
 
-// transpose_image_inplace: an N x N bf16 matrix X into its K-major image, transposed in place
-__global__ void __launch_bounds__(256) k_transpose_inplace_selftest(const uint16_t* X, uint16_t* Y, int N) {
+// MN-major operands (Opnd, mma_part): D (128 x N) = A B^T with A (128 x K) and / or B (N x K)
+// given to the tensor core as the image of its transpose (A^T: K rows x 128, B^T: K rows x N,
+// each K-major over its own columns) read MN-major; amode / bmode 0 = the K-major image of the
+// operand itself.  One term, no initial accumulator.
+__global__ void __launch_bounds__(128) k_mn_selftest(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D,
+                                                     int N, int K, int amode, int bmode, uint32_t ncols,
+                                                     int* status) {
   extern __shared__ __align__(128) unsigned char sm[];
-  for (int e = threadIdx.x; e < N * N; e += 256)
-    *reinterpret_cast<uint16_t*>(sm + kmajor_off(e / N, e % N, N)) = X[e];
+  unsigned char* As = sm;
+  unsigned char* Bs = sm + 128 * K * 2;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Bs + N * K * 2);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int t = threadIdx.x, warp = t / 32;
+  for (int e = t; e < 128 * K; e += 128) {
+    const int r = e / K, k = e % K;
+    *reinterpret_cast<__nv_bfloat16*>(As + (amode ? kmajor_off(k, r, 128) : kmajor_off(r, k, K))) = A[e];
+  }
+  for (int e = t; e < N * K; e += 128) {
+    const int r = e / K, k = e % K;
+    *reinterpret_cast<__nv_bfloat16*>(Bs + (bmode ? kmajor_off(k, r, N) : kmajor_off(r, k, K))) = B[e];
+  }
+  if (t == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, ncols);
+  fence_proxy_async();
+  fence_before_sync();
   __syncthreads();
-  transpose_image_inplace(sm, N);
+  fence_after_sync();
+  const uint32_t tbase = *tslot;
+  if (t == 0) {
+    const Opnd a = amode ? opnd_mn(smem_u32(As), 0u, 128) : opnd_k(smem_u32(As), 0u, K);
+    const Opnd b = bmode ? opnd_mn(smem_u32(Bs), 0u, N) : opnd_k(smem_u32(Bs), 0u, K);
+    const uint32_t idesc = idesc_bf16(128, N) | (amode ? IDESC_A_MN : 0u) | (bmode ? IDESC_B_MN : 0u);
+    mma_part(tbase, a, false, b, false, K, idesc, false);
+    mma_commit(bar);
+  }
+  const int ok = __syncthreads_and(mbar_wait(bar, 0) ? 1 : 0);
+  fence_after_sync();
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem_lane_addr(tbase, warp, c0), v);
+      for (int i = 0; i < 16; ++i) D[t * N + c0 + i] = v[i];
+    }
+  } else if (t == 0) {
+    atomicExch(status, 1);
+  }
+  fence_before_sync();
   __syncthreads();
-  for (int e = threadIdx.x; e < N * N; e += 256) Y[e] = *reinterpret_cast<const uint16_t*>(sm + kmajor_off(e / N, e % N, N));
+  if (warp == 0) tmem_dealloc(tbase, ncols);
 }
 
-extern "C" int transpose_inplace_selftest(const void* X, void* Y, int N, cudaStream_t st) {
-  if (N != 64 && N != 128) return 1;
-  const size_t smem = (size_t)N * N * 2;
-  if (cudaFuncSetAttribute(k_transpose_inplace_selftest, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
+extern "C" int mn_selftest(const void* A, const void* B, float* D, int N, int K, int amode, int bmode, int* status,
+                           cudaStream_t st) {
+  if ((N != 64 && N != 128) || (K != 64 && K != 128)) return 1;
+  const uint32_t ncols = (uint32_t)N;
+  const size_t smem = (size_t)(128 + N) * K * 2 + 16;
+  if (cudaFuncSetAttribute(k_mn_selftest, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return 2;
-  k_transpose_inplace_selftest<<<1, 256, smem, st>>>(static_cast<const uint16_t*>(X), static_cast<uint16_t*>(Y), N);
+  k_mn_selftest<<<1, 128, smem, st>>>(static_cast<const __nv_bfloat16*>(A), static_cast<const __nv_bfloat16*>(B), D,
+                                       N, K, amode, bmode, ncols, status);
   return cudaGetLastError() == cudaSuccess ? 0 : 3;
 }

@@ -29,8 +29,8 @@ def lib():
     L.transpose_selftest.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_void_p]
     L.transpose_selftest.restype = ctypes.c_int
-    L.transpose_inplace_selftest.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
-    L.transpose_inplace_selftest.restype = ctypes.c_int
+    L.mn_selftest.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 + [ctypes.c_void_p] * 2
+    L.mn_selftest.restype = ctypes.c_int
     return L
 
 
@@ -101,15 +101,31 @@ def test_unrolled_inverse_matches_generic_bits(inv_lib, seed, scale):
     assert resid.abs().max().item() <= 1e-4 * max(1.0, T.abs().max().item())
 
 
-@pytest.mark.parametrize("N", [64, 128])
-def test_transpose_image_inplace_is_exact(lib, N):
-    """The in-place square image transpose (core-matrix pairs swapped through ldmatrix .trans +
-    stmatrix) moves every bf16 bit pattern to its transposed place."""
-    g = torch.Generator().manual_seed(N)
-    X = torch.randint(0, 1 << 16, (N, N), generator=g, dtype=torch.int32).to(torch.int16)
-    dX = X.cuda()
-    Y = torch.zeros((N, N), dtype=torch.int16, device="cuda")
-    rc = lib.transpose_inplace_selftest(dX.data_ptr(), Y.data_ptr(), N, torch.cuda.current_stream().cuda_stream)
+def _mn_product(lib, A, B, amode, bmode):
+    N, K = B.shape
+    D = torch.full((128, N), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.mn_selftest(A.data_ptr(), B.data_ptr(), D.data_ptr(), N, K, amode, bmode, status.data_ptr(),
+                         torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     torch.cuda.synchronize()
-    assert torch.equal(Y.cpu(), X.T.contiguous())
+    assert int(status.item()) == 0, "bounded wait gave up"
+    return D.cpu()
+
+
+@pytest.mark.parametrize("N,K", [(64, 64), (64, 128), (128, 64), (128, 128)])
+def test_mn_major_operands_match_k_major_bits(lib, N, K):
+    """An operand read MN-major from the image of its transpose (the instruction descriptor's
+    transpose bit; leading offset between core matrices along K, stride offset 128 B along M or
+    N) gives the product of the K-major operand, bit for bit, and the fp64 reference to fp32
+    accumulation rounding."""
+    g = torch.Generator().manual_seed(N * 31 + K)
+    A = torch.randn((128, K), generator=g).to(torch.bfloat16)
+    B = torch.randn((N, K), generator=g).to(torch.bfloat16)
+    ref = A.double() @ B.double().T
+    dA, dB = A.cuda(), B.cuda()
+    base = _mn_product(lib, dA, dB, 0, 0)
+    err = (base.double() - ref).abs().max().item() / ref.abs().max().item()
+    assert err < 1e-5, err
+    for amode, bmode in ((1, 0), (0, 1), (1, 1)):
+        assert torch.equal(_mn_product(lib, dA, dB, amode, bmode), base), (amode, bmode)
