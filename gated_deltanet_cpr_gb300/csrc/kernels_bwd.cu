@@ -1610,9 +1610,10 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   unsigned char* img = reinterpret_cast<unsigned char*>(a.b.img + ch * (int64_t)prep_w_floats(C, D));
   const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
 
-  // ---- 1. images of K rows and V rows (V staged in the A region), g, beta (zero beyond
-  // the chunk's tokens); every load issued before the first store
-  unsigned char* Vi = smq + OFF_A;
+  // ---- 1. images of K rows and V rows (V in the V^T region: step 3 reads K^T and V^T as the
+  // MN-major readings of the row images), g, beta (zero beyond the chunk's tokens); every
+  // load issued before the first store
+  unsigned char* Vi = VT;
   {
     float g0 = 0.f, b0 = 0.f;
     if (t < n) {
@@ -1679,9 +1680,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
       Gs[i] = run;
     }
   }
-  // K^T and V^T from the row images while the Gram product runs
-  tc::transpose_image(KT, Ki, D, C);
-  tc::transpose_image(VT, Vi, D, C);
   __syncthreads();
   if (t < C) a.b.G[ch * C + t] = Gs[t];
   // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs (V^T is built), by all
@@ -1733,17 +1731,13 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   sync_for_mma();
   if (ok && t == 0) {
     fence_after_sync();
-    const uint32_t sbo = (C / 8) * 128;
-    for (int term = 0; term < 2; ++term) {
-      const uint32_t ta = smem_u32(term == 0 ? TKh : TKl);
-      const uint32_t tv = smem_u32(term == 0 ? TVh : TVl);
-      for (int kk = 0; kk < C / 16; ++kk) {
-        mma_bf16(tb + COL_W, make_desc(ta + kk * 256, 128, sbo), make_desc(smem_u32(KT) + kk * 256, 128, sbo),
-                 idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
-        mma_bf16(tb + COL_UT, make_desc(smem_u32(VT) + kk * 256, 128, sbo), make_desc(tv + kk * 256, 128, sbo),
-                 idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
-      }
-    }
+    const Opnd tk = opnd_k(smem_u32(TKh), smem_u32(TKl), C), tv = opnd_k(smem_u32(TVh), smem_u32(TVl), C);
+    const Opnd kt = opnd_mn(smem_u32(Ki), 0u, D), vt = opnd_mn(smem_u32(Vi), 0u, D);
+    const uint32_t iw = idesc_bf16(128, D) | IDESC_B_MN, iu = idesc_bf16(128, C) | IDESC_A_MN;
+    mma_part(tb + COL_W, tk, false, kt, false, C, iw, false);  // W = TK_hi K + TK_lo K
+    mma_part(tb + COL_UT, vt, false, tv, false, C, iu, false);  // U^T = V^T TV_hi^T + V^T TV_lo^T
+    mma_part(tb + COL_W, tk, true, kt, false, C, iw, true);
+    mma_part(tb + COL_UT, vt, false, tv, true, C, iu, true);
     mma_commit(bar);
   }
   unsigned char* Qi = smq + OFF_A;  // Q rows image over the dead A region, while the products run
@@ -1806,7 +1800,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
   }
   float* gam = Tm;  // e^{G_i - G_s} (s <= i) over the dead T, by all threads
   decay_table_lower(gam, Gs);
-  unsigned char* Ph = KT;  // P rows image, hi | lo (8 KB each), over the dead K^T
+  unsigned char* Ph = KT;  // P rows image, hi | lo (8 KB each), in the K^T region
   if (ok) wait_mma();
   if (ok && (warp & 3) < 2) {
     const int i = lrow;
@@ -1853,7 +1847,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
     if (t == 0) bulk_wait_read();  // the Qt readout writes over P, step 6 over the K and W rows
     wait_mma();
   }
-  // Qt rows hi | lo over the dead P (K^T) and V^T
+  // Qt rows hi | lo over the dead P and V rows
   unsigned char* Qrh = KT;
   unsigned char* Qrl = VT;
   if (ok && (warp & 3) < 2) {
