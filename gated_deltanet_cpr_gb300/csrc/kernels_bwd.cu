@@ -1474,8 +1474,9 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     run();
   }
   if (ok) {  // dU^T = dO^T P + (E K^T) diag(dec) as the dU^T image (rows d, K = s; hi | lo) in
-    // B: one bulk copy into this chunk-head's adjoint L slot for the gradients kernel, and
-    // read MN-major as the dU rows operand of dW^T
+    // B: one bulk copy into the second half of this chunk-head's adjoint L slot for the
+    // gradients kernel (the first half still holds the prep's dO rows image, which the
+    // gradients kernel reads too), and read MN-major as the dU rows operand of dW^T
 #pragma unroll
     for (int s1 = 0; s1 < 2; ++s1) {
       float e1[16], p1[16];
@@ -1498,7 +1499,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       const Opnd s0t = opnd_mn(sa_h, sa_l, D);
       mma_split(tb + COL_1, s0t, opnd_mn(sb_h, sb_l, C), D, I_KK | IDESC_A_MN | IDESC_B_MN, 3);
       if (exact) mma_split(tb + COL_0, s0t, opnd_k(sx, sx, D), D, I_KK | IDESC_A_MN, 2);
-      bulk_s2g(a.b.L + ch * SZ, Bh, RB);
+      bulk_s2g(a.b.L + ch * SZ + SZ / 2, Bh, RB);  // over the S0 lo image, back in A by now
       bulk_store_commit();
     });
     run();
@@ -1791,10 +1792,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
                idesc_bf16(128, C), kk > 0 ? 1u : 0u);
     mma_commit(bar);
   }
-  if (t == 0) {  // asynchronous bulk stores: the K rows image for the reverse chain, and the W
-                 // rows image (hi | lo) into W's slot for the reverse chain, the d x d products
-                 // and gradients kernels
+  if (t == 0) {  // asynchronous bulk stores: the K and Q rows images into the image slot (the
+                 // reverse chain's and the later kernels' operands), and the W rows image
+                 // (hi | lo) into W's slot for the reverse chain, the d x d products and
+                 // gradients kernels
     bulk_s2g(img, Ki, TILE);
+    bulk_s2g(img + TILE, Qi, TILE);
     bulk_s2g(a.b.W + ch * CD, Wr, 2 * TILE);
     bulk_store_commit();
   }
@@ -1965,7 +1968,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const int64_t ch = c * dm.hv + h;
   const int64_t CD = (int64_t)C * D;
   const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
-  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(a.in.k) + tok0 * kstride + (int64_t)hq * D;
   const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.in.q) + tok0 * kstride + (int64_t)hq * D;
   const int64_t orow0 = tok0 * vstride + (int64_t)h * D;  // token 0 of this head in [T, Hv, D]
   const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(a.in.v) + orow0;
@@ -1980,8 +1982,15 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar[1], 2 * IMG);  // the d x d products kernel's U^T image (hi | lo)
+    // the operands of products 1 by bulk copy: the d x d products kernel's U^T image (hi | lo),
+    // the prep's Q and K rows images (the image slot) and, for bf16 dO, its dO rows image (the
+    // start of L's slot); all of them zero beyond the chunk's tokens
+    const unsigned char* qk = reinterpret_cast<const unsigned char*>(a.b.img + ch * (int64_t)prep_w_floats(C, D));
+    mbar_expect_tx(&bar[1], (dm.out_bf16 ? 5 : 4) * IMG);
     bulk_g2s(ar + 64 * KB, a.b.U + ch * CD, 2 * IMG, &bar[1]);
+    bulk_g2s(ar, qk + IMG, IMG, &bar[1]);
+    bulk_g2s(ar + 16 * KB, qk, IMG, &bar[1]);
+    if (dm.out_bf16) bulk_g2s(ar + 32 * KB, a.b.L + ch * (int64_t)D * D, IMG, &bar[1]);
   }
   // arena: products 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U^T hi/lo @64/@80; then Pm hi/lo
   // @32/@40 (with Q, K rows); then T^T @0/@8, dU^T @16/@32, dW^T @48/@64, V rows @80
@@ -1991,42 +2000,29 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       g0 = a.b.G[ch * C + t];
       b0 = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
     }
-    float vo[4][8];
-    uint4 qr[4], kr[4];
+    if (!dm.out_bf16) {  // fp32 dO rows, split into hi | lo
+      float vo[4][8];
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      int r, k0;
-      kmajor_piece(t + it * 256, D, r, k0);
-      if (r < n) {
-        const int64_t o = orow0 + (int64_t)r * vstride + k0;
-        if (dm.out_bf16)
-          load8(static_cast<const __nv_bfloat16*>(a.dO) + o, vo[it]);
-        else
-          load8(static_cast<const float*>(a.dO) + o, vo[it]);
-        qr[it] = *reinterpret_cast<const uint4*>(qb + r * kstride + k0);
-        kr[it] = *reinterpret_cast<const uint4*>(kb + r * kstride + k0);
-      } else {
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(t + it * 256, D, r, k0);
+        if (r < n) {
+          load8(static_cast<const float*>(a.dO) + orow0 + (int64_t)r * vstride + k0, vo[it]);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) vo[it][e] = 0.f;
-        qr[it] = zero4;
-        kr[it] = zero4;
+          for (int e = 0; e < 8; ++e) vo[it][e] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(t + it * 256, D, r, k0);
+        split8(ar + 32 * KB, ar + 48 * KB, kmajor_off(r, k0, D), vo[it]);
       }
     }
     if (t < C) {
       Gs[t] = g0;
       bs[t] = b0;
-    }
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      int r, k0;
-      kmajor_piece(t + it * 256, D, r, k0);
-      const uint32_t off = kmajor_off(r, k0, D);
-      if (dm.out_bf16)  // exact: no lo image
-        store_bf16x8(ar + 32 * KB, off, vo[it]);
-      else
-        split8(ar + 32 * KB, ar + 48 * KB, off, vo[it]);
-      *reinterpret_cast<uint4*>(ar + off) = qr[it];
-      *reinterpret_cast<uint4*>(ar + 16 * KB + off) = kr[it];
     }
   }
   if (warp == 0) tmem_alloc(tslot, TMEM1);
@@ -2125,7 +2121,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   if (ok && t == 0) {
     mbar_expect_tx(&bar[1], 2 * C * C * 2 + 4 * IMG);
     bulk_g2s(ar, a.b.T + ch * C * C, 2 * C * C * 2, &bar[1]);
-    bulk_g2s(ar + 16 * KB, a.b.L + ch * (int64_t)D * D, 2 * IMG, &bar[1]);
+    bulk_g2s(ar + 16 * KB, a.b.L + ch * (int64_t)D * D + D * D / 2, 2 * IMG, &bar[1]);
     bulk_g2s(ar + 48 * KB, a.b.dW + ch * CD, 2 * IMG, &bar[1]);
     cpending = true;
   }
@@ -2267,7 +2263,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   fence_before_sync();
   __syncthreads();
   if (ok && t < C) {  // per-token partial sums for G2
-    float* gp = a.b.img + ch * (int64_t)prep_w_floats(C, D) + C * D / 2;  // after the K rows image
+    float* gp = a.b.img + ch * (int64_t)prep_w_floats(C, D) + C * D;  // after the K and Q rows images
     gp[t] = __fmul_rn(eG[t], __fadd_rn(dGa[t], dGa[C + t]));                                // e^G dO S0 . q
     gp[C + t] = __fsub_rn(__fadd_rn(rowp[t], rowp[C + t]), __fadd_rn(colp[t], colp[C + t]));  // dG_b
     gp[2 * C + t] = __fadd_rn(dba[t], dba[C + t]);                                          // v . X
@@ -2339,7 +2335,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
       g0 = a.b.G[ch * C + t];
       b0 = t < n ? a.in.beta[(tok0 + t) * dm.hv + h] : 0.f;
     }
-    p0 = img[C * D / 2 + t];  // t < 4 C
+    p0 = img[C * D + t];  // t < 4 C
     if (t < C) {
       Gs[t] = g0;
       bs[t] = b0;
