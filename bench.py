@@ -811,9 +811,12 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
     """Same step through the public API with host buffers: every step copies its inputs from
     pinned host memory and reads its results back, pipelined as a serving or training loop
     would run it: step i + 1's inputs (prefill / trainer tokens and the decode tokens) go up on
-    one copy stream (into the second of two input buffers, the decode steps replayed from one
-    CUDA graph per buffer) while step i computes, and every result comes back on another copy
-    stream as soon as its kernels finish; the prefill output and the gradients alternate
+    a copy stream (into the second of two input buffers, the decode steps replayed from one
+    CUDA graph per buffer) while step i computes, and every result comes back on the same copy
+    stream (or, with --e2e-copy-streams 2, on a second one) as soon as its kernels finish: one
+    stream keeps the two directions from contending for the host link (measured: the copies
+    of a step take the isolated copy rates' time on one stream, about 15% more on two on a
+    quiet box and 1.7 times as much on a busy one); the prefill output and the gradients alternate
     between two sets of buffers, so a step's compute never waits for the previous step's
     read-back of them; the timed region opens before the first input copy and closes after
     the last read-back."""
@@ -835,7 +838,8 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
         return {} if gr is None else {n: gr[n] for n in ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")}
 
     comp = torch.cuda.current_stream(dev)
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    up = torch.cuda.Stream(dev)
+    down = up if args.e2e_copy_streams == 1 else torch.cuda.Stream(dev)
     t0 = dict(t)
     bufs = [t0, {n: torch.empty_like(v) for n, v in t0.items()}]
     dq_bufs = [dq_in, {n: torch.empty_like(v) for n, v in dq_in.items()}]
@@ -955,8 +959,11 @@ def bench_e2e(api, torch, dev, w, host, xd, args, prefill_call, graph, capture_d
             "h2d_gbs": bw["h2d"], "d2h_gbs": bw["d2h"], "copy_ms_per_step_serial": copy_ms,
             "h2d_ms_per_step_during_run": up_ms, "d2h_ms_per_step_during_run": down_ms,
             "exposed_ms_per_step": ms - compute_ms,
+            "copy_streams": args.e2e_copy_streams,
             "pipelined": "inputs of step i+1 uploaded during step i (two input buffers); "
-                         "results read back on a second copy stream as each part finishes"}
+                         + ("results read back on a second copy stream as each part finishes"
+                            if args.e2e_copy_streams == 2 else
+                            "results read back on the same copy stream, after it, as each part finishes")}
 
 
 def run_ncu_case(args):
@@ -1018,6 +1025,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-copy-streams", type=int, choices=[1, 2], default=1,
+                    help="end-to-end run: uploads and read-backs on one copy stream (default) or "
+                         "on two (concurrent directions, which contend for the host link)")
     ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode256", "resync64", "bwd"], default=None,
                     help="run a small fixed case for an ncu capture and exit")
     args = ap.parse_args(argv)
