@@ -2319,7 +2319,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   const int row = (warp & 3) * 32 + lane;
   const int half = warp >> 2;
   // arena: products A W hi/lo @0/@16, Y hi|lo @32, K rows @64; products B Ut hi/lo @0/@16,
-  // X hi|lo @32; products C dAm hi/lo @0/@8 (with the K rows)
+  // X hi|lo @32; products C dAm hi/lo @0/@8 (with the K rows), U dS_end rows @16, the first
+  // gradients kernel's dk rows @48 and @80 (staged for the dk readout)
   if (t == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
@@ -2441,6 +2442,32 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
     }
     rowb[half * C + i] = rb;
     rowg[half * C + i] = rg;
+  } else if (ok) {
+    // meanwhile the other warps stage U dS_end and the first gradients kernel's dk rows for
+    // the dk readout in the free arena (@16..@64 after products B, @80..@96): row r's 16-byte
+    // piece j at r * 512 + ((j ^ (r & 7)) * 16), so that the readout's lanes (consecutive
+    // rows, one piece each) hit distinct banks; two batches of 8 + 8 pieces per thread
+    const int hl = (warp >> 2) * 64 + ((warp & 3) - 2) * 32 + lane;  // 0..127 on warps 2, 3, 6, 7
+    const float* ue_g = a.b.UdSe + ch * CD;
+    const float* pk_g = a.b.dk_part + orow0;
+#pragma unroll
+    for (int bt = 0; bt < 2; ++bt) {
+      float4 u[8], pk[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int q = hl + 128 * (8 * bt + x), r = q >> 5, j = q & 31;
+        u[x] = *reinterpret_cast<const float4*>(ue_g + r * D + 4 * j);
+        pk[x] = r < n ? *reinterpret_cast<const float4*>(pk_g + (int64_t)r * vstride + 4 * j)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int q = hl + 128 * (8 * bt + x), r = q >> 5, j = q & 31;
+        const uint32_t sw = (uint32_t)((j ^ (r & 7)) << 4);
+        *reinterpret_cast<float4*>(ar + 16 * KB + r * 512 + sw) = u[x];
+        *reinterpret_cast<float4*>((r < 32 ? ar + 48 * KB + r * 512 : ar + 80 * KB + (r - 32) * 512) + sw) = pk[x];
+      }
+    }
   }
   fence_before_sync();
   __syncthreads();
@@ -2459,7 +2486,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
   if (ok && rowlane) {  // dk = G1's part + dK2 + dec U dS_end; U dS_end . k
     const int s2 = row;
     const bool live = s2 < n;
-    const float* ue_row = a.b.UdSe + ch * CD + (int64_t)s2 * D;
+    const unsigned char* ue_s = ar + 16 * KB + s2 * 512;  // the staged rows (swizzled pieces)
+    const unsigned char* pk_s = (s2 < 32 ? ar + 48 * KB : ar + 80 * KB - 32 * 512) + s2 * 512;
     float* dk_row = a.b.dk_part + orow0 + (int64_t)s2 * vstride;
     const float ds = dec[s2];
     float pcs = 0.f;
@@ -2467,8 +2495,9 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad2_tc(BwdArgs a) {
       float4 ue4[4], pk4[4];
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        ue4[x] = *reinterpret_cast<const float4*>(ue_row + cb + 4 * x);
-        pk4[x] = live ? *reinterpret_cast<const float4*>(dk_row + cb + 4 * x) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const uint32_t sw = (uint32_t)((((cb >> 2) + x) ^ (s2 & 7)) << 4);
+        ue4[x] = *reinterpret_cast<const float4*>(ue_s + sw);
+        pk4[x] = live ? *reinterpret_cast<const float4*>(pk_s + sw) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       const uint4 k0 = *reinterpret_cast<const uint4*>(ar + 64 * KB + kmajor_off(s2, cb, D));
       const uint4 k1 = *reinterpret_cast<const uint4*>(ar + 64 * KB + kmajor_off(s2, cb + 8, D));
