@@ -1993,7 +1993,8 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     if (dm.out_bf16) bulk_g2s(ar + 32 * KB, a.b.L + ch * (int64_t)D * D, IMG, &bar[1]);
   }
   // arena: products 1 Q rows @0, K rows @16, dO hi/lo @32/@48, U^T hi/lo @64/@80; then Pm hi/lo
-  // @32/@40 (with Q, K rows); then T^T @0/@8, dU^T @16/@32, dW^T @48/@64, V rows @80
+  // @32/@40 (with Q, K rows), dO S0 rows @48 and V rows @80 (staged); then T^T @0/@8, dU^T
+  // @16/@32; then K rows @16, dW^T @48/@64
   {
     float g0 = 0.f, b0 = 0.f;
     if (t < C) {
@@ -2103,6 +2104,39 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
       }
     }
     rowp[half * C + i] = rp;
+  } else if (ok) {
+    // meanwhile the other warps stage, in the operands of products 1 that are dead now, the
+    // d x d products kernel's dO S0 rows for the dQ readout (@48..@80; row r's 16-byte piece j
+    // at r * 512 + ((j ^ (r & 7)) * 16), so that the readout's lanes, consecutive rows, hit
+    // distinct banks) and the V rows image for the dv readout (@80)
+    const float* dos_g = a.b.dOS0 + ch * CD;
+#pragma unroll
+    for (int bt = 0; bt < 2; ++bt) {
+      float4 u[8];
+      uint4 vr[4];
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int q = helper + 128 * (8 * bt + x), r = q >> 5, j = q & 31;
+        u[x] = *reinterpret_cast<const float4*>(dos_g + r * D + 4 * j);
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(helper + (4 * bt + it) * 128, D, r, k0);
+        vr[it] = r < n ? *reinterpret_cast<const uint4*>(vb + r * vstride + k0) : zero4;
+      }
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        const int q = helper + 128 * (8 * bt + x), r = q >> 5, j = q & 31;
+        *reinterpret_cast<float4*>(ar + 48 * KB + r * 512 + ((j ^ (r & 7)) << 4)) = u[x];
+      }
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        int r, k0;
+        kmajor_piece(helper + (4 * bt + it) * 128, D, r, k0);
+        *reinterpret_cast<uint4*>(ar + 80 * KB + kmajor_off(r, k0, D)) = vr[it];
+      }
+    }
   }
   fence_before_sync();
   __syncthreads();
@@ -2116,34 +2150,37 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     });
     if (ok) wait_mma();
   }
-  // products 3 and 4: operands T^T, dU^T, dW^T: ready-made images (the prep and big-products
-  // kernels wrote them), one bulk copy each into the dead operands of products 1 and 2
+  // products 3's operands T^T and dU^T: ready-made images (the prep and big-products kernels
+  // wrote them), one bulk copy each into the dead operands of products 1 and 2
   if (ok && t == 0) {
-    mbar_expect_tx(&bar[1], 2 * C * C * 2 + 4 * IMG);
+    mbar_expect_tx(&bar[1], 2 * C * C * 2 + 2 * IMG);
     bulk_g2s(ar, a.b.T + ch * C * C, 2 * C * C * 2, &bar[1]);
     bulk_g2s(ar + 16 * KB, a.b.L + ch * (int64_t)D * D + D * D / 2, 2 * IMG, &bar[1]);
-    bulk_g2s(ar + 48 * KB, a.b.dW + ch * CD, 2 * IMG, &bar[1]);
     cpending = true;
   }
-  // dQ readout (row warps) || V rows image for the dv readout over the dead U^T lo (other warps)
-  if (ok) {
-    if (rowlane) {
+  // dQ readout (row warps): dO S0 from the staged rows, q from global memory (all of a
+  // thread's q pieces in flight at once)
+  if (ok && rowlane) {
+    {
       const int i = row;
       const bool live = i < n;
       const float egi = eG[i];
-      const float* dos_row = a.b.dOS0 + ch * CD + (int64_t)i * D;
+      const unsigned char* dos_s = ar + 48 * KB + i * 512;
+      uint4 qall[8];
+#pragma unroll
+      for (int x = 0; x < 8; ++x)
+        qall[x] = live ? *reinterpret_cast<const uint4*>(qb + i * kstride + half * 64 + 8 * x) : zero4;
       float pga = 0.f;
+#pragma unroll
       for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
         float4 ds4[4];
-        uint4 qv[2];
 #pragma unroll
-        for (int x = 0; x < 4; ++x) ds4[x] = *reinterpret_cast<const float4*>(dos_row + c0 + 4 * x);
-#pragma unroll
-        for (int x = 0; x < 2; ++x) qv[x] = live ? *reinterpret_cast<const uint4*>(qb + i * kstride + c0 + 8 * x) : zero4;
+        for (int x = 0; x < 4; ++x)
+          ds4[x] = *reinterpret_cast<const float4*>(dos_s + ((((c0 >> 2) + x) ^ (i & 7)) << 4));
         float dq[16], qf[16], ds[16];
         tmem_ld16(tl + 0 + c0, dq);
-        unpack8(qv[0], qf);
-        unpack8(qv[1], qf + 8);
+        unpack8(qall[(c0 - half * 64) / 8], qf);
+        unpack8(qall[(c0 - half * 64) / 8 + 1], qf + 8);
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
           ds[4 * x] = ds4[x].x;
@@ -2163,20 +2200,6 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
         }
       }
       dGa[half * C + i] = pga;
-    } else {
-      uint4 vr[8];
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        int r, k0;
-        kmajor_piece(helper + it * 128, D, r, k0);
-        vr[it] = r < n ? *reinterpret_cast<const uint4*>(vb + r * vstride + k0) : zero4;
-      }
-#pragma unroll
-      for (int it = 0; it < 8; ++it) {
-        int r, k0;
-        kmajor_piece(helper + it * 128, D, r, k0);
-        *reinterpret_cast<uint4*>(ar + 80 * KB + kmajor_off(r, k0, D)) = vr[it];
-      }
     }
   }
   // ---- products 3: X = T^T dU -> TMEM 0
@@ -2184,10 +2207,12 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     issue(true, [&] { mma_terms(tb + 0, sa, sa + 8 * KB, sa + 16 * KB, sa + 32 * KB, C, idesc_bf16(128, D), 3); });
     if (ok) wait_mma();
   }
-  // K rows image (the prep kernel's) for the dk readout over the dead dU^T
+  // K rows image (the prep kernel's) for the dk readout over the dead dU^T, and products 4's
+  // dW^T image (the d x d products kernel's) over the consumed dO S0 rows
   if (ok && t == 0) {
-    mbar_expect_tx(&bar[1], IMG);
+    mbar_expect_tx(&bar[1], 3 * IMG);
     bulk_g2s(ar + 16 * KB, a.b.img + ch * (int64_t)prep_w_floats(C, D), IMG, &bar[1]);
+    bulk_g2s(ar + 48 * KB, a.b.dW + ch * CD, 2 * IMG, &bar[1]);
     cpending = true;
   }
   if (ok && rowlane) {  // dv, dbeta_a; X image -> workspace
