@@ -1209,16 +1209,19 @@ __device__ __forceinline__ void load_dO_rows(float (&v)[4][8], const void* dO, b
     load_dO_rows_t(v, static_cast<const float*>(dO) + base, tstride, n);
 }
 
-// 128 x 128 image pair of a row-major fp32 d x d matrix (TRANS: of its transpose), built in
-// two 64-row halves so that a thread holds 32 values at a time
-template <bool TRANS>
-__device__ __forceinline__ void build_dd(unsigned char* hi, unsigned char* lo, const float* src) {
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    SplitTile<TRANS, 64, 128> tile;
-    tile.load(TRANS ? src + hh * 64 : src + hh * 64 * 128, 128, TRANS ? 128 : 64);
-    tile.store(hi + hh * 16384, lo + hh * 16384);
-  }
+// 128 x 128 image pair of a row-major fp32 d x d matrix, built in four 32-row quarters with
+// two in flight (a thread holds 32 values at a time: one quarter's loads overlap the previous
+// quarter's wait)
+__device__ __forceinline__ void build_dd4(unsigned char* hi, unsigned char* lo, const float* src) {
+  SplitTile<false, 32, 128> a, b;
+  a.load(src, 128, 32);
+  b.load(src + 32 * 128, 128, 32);
+  a.store(hi, lo);
+  a.load(src + 64 * 128, 128, 32);
+  b.store(hi + 8192, lo + 8192);
+  b.load(src + 96 * 128, 128, 32);
+  a.store(hi + 16384, lo + 16384);
+  b.store(hi + 24576, lo + 24576);
 }
 
 // D = A B^T over K with split operands: terms = 3 gives A_hi B_hi + A_hi B_lo + A_lo B_hi;
@@ -1341,7 +1344,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
   const uint32_t I_KK = idesc_bf16(128, C);
 
   // ---- phase 1: U^T = Ut^T - S0 W^T; the S0 image also leaves for phase 4
-  build_dd<false>(Ah, Al, S0);
+  build_dd4(Ah, Al, S0);
   issue_after(&bar[1], cphase, cpending, [&] {
     mma_split(tb + COL_0, opnd_k(sa_h, sa_l, D), opnd_k(sb_h, sb_l, D), D, I_KK, 3);
     bulk_s2g(s0_hi, Ah, RA / 2);
