@@ -1918,11 +1918,14 @@ __global__ void __launch_bounds__(256, 2) k_bwd_prep_tc(BwdArgs a) {
 //       dAm = dA beta_i Gam,  dK2 = dAm K + dAm^T K                   -> dk += dK2 + diag(dec) U dS_end
 //       dG, reverse cumulative sum -> dg, dbeta
 // The row and column sums of the dG terms come straight from the TMEM readouts (per-thread
-// row sums, warp-shuffle column sums in a fixed tree).  G1's operands T^T, dU^T and dW^T
+// row sums, warp-shuffle column sums in a fixed tree).  G1's operands T^T, U^T, dU^T and dW^T
 // arrive as ready-made images by bulk copy (the prep and big-products kernels write them),
-// as do the K rows; X and Y travel through the workspace (the adjoint L, dead after the
-// reverse chain) as images that G2 brings in the same way; the per-token partial sums go
-// through the image workspace.
+// as do the Q, K and (bf16) dO rows; X and Y travel through the workspace (the adjoint L,
+// dead after the reverse chain) as images that G2 brings in the same way; the per-token
+// partial sums go through the image workspace.  Transposed operands are MN-major readings
+// of the row images.  A 64-row result is read out by the four warps that own TMEM lanes
+// 0..63; the other four meanwhile stage the next readout's global operands (dO S0 and the V
+// rows in G1, U dS_end and G1's dk rows in G2) in shared memory.
 // 64-row operands use 128-row MMAs whose extra rows read neighbouring arena bytes and are
 // never read back.
 namespace tcd {
