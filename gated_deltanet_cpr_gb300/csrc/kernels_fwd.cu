@@ -513,13 +513,14 @@ static void launch_chain_t(const Dims& d, const void* keys, const float* W, cons
 //     Vd^T[i][s]     = Ud[s][i] - D1[i][s]           (registers; then split to bf16 hi/lo)
 //     D2 (128 x 128) = gamma S + Vd^T K               D2 preloaded with gamma S, 2 MMAs: Vd_hi K + Vd_lo K
 // with fp32 operands split as x = hi + lo (bf16 each) and bf16 inputs exact.  The pre-pass
-// wrote Wd hi/lo and K^T as ready-made shared-memory images, so a step's operands arrive by
-// one bulk copy, issued a step ahead into the other of two stage buffers.
+// wrote Wd hi/lo and the K rows as ready-made shared-memory images (K^T is the MN-major
+// reading of the K rows), so a step's operands arrive by one bulk copy, issued a step ahead
+// into the other of two stage buffers.
 namespace tcc {
 constexpr int D = 128, C = 64;
 constexpr uint32_t A1_BYTES = 128 * D * 2;  // state operand, per hi / lo
 constexpr uint32_t A2_BYTES = 128 * C * 2;  // Vd^T operand, per hi / lo
-constexpr uint32_t STAGE_BYTES = 3 * C * D * 2;  // Wd hi | Wd lo | K^T
+constexpr uint32_t STAGE_BYTES = 3 * C * D * 2;  // Wd hi | Wd lo | K rows
 constexpr size_t SMEM = 2 * (size_t)A1_BYTES + 2 * (size_t)A2_BYTES + 2 * (size_t)STAGE_BYTES + 64;
 constexpr uint32_t TMEM_COLS = 256, D1_COL = 0, D2_COL = 64;
 constexpr uint32_t IDESC1 = tc::idesc_bf16(128, C);
@@ -818,17 +819,12 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
       fence_proxy_async();
       fence_before_sync();
       __syncthreads();
-      if (t == 0) {  // D2 += Vd^T K (two split terms)
+      if (t == 0) {  // D2 += Vd^T K (two split terms; K^T the MN-major reading of the K rows image)
         fence_after_sync();
         const uint32_t k_img = smem_u32(stg) + 2 * C * D * 2;
-        const uint32_t sbo = (C / 8) * 128;
-#pragma unroll 1
-        for (int term = 0; term < 2; ++term) {
-          const uint32_t a = smem_u32(term == 0 ? A2h : A2l);
-          for (int kk = 0; kk < C / 16; ++kk)
-            mma_bf16(tbase + D2_COL, make_desc(a + kk * 256, 128, sbo), make_desc(k_img + kk * 256, 128, sbo),
-                     IDESC2, 1u);
-        }
+        const Opnd vd = opnd_k(smem_u32(A2h), smem_u32(A2l), C), kr = opnd_mn(k_img, 0u, D);
+        mma_part(tbase + D2_COL, vd, false, kr, false, C, IDESC2 | IDESC_B_MN, true);
+        mma_part(tbase + D2_COL, vd, true, kr, false, C, IDESC2 | IDESC_B_MN, true);
         mma_commit(&bars[2]);
       }
       mma_pending = true;
@@ -889,10 +885,11 @@ __global__ void __launch_bounds__(256, 1) k_chain_tc(Dims dm, const float* __res
 // threads per (chunk, head) as k_prep:
 //   Gram = K K^T                        1 MMA chain (bf16 inputs exact, fp32 accumulation)
 //   A, T = (I + A)^{-1}                 fp32 SIMT (blocked forward substitution)
-//   W    = (T diag(beta e^G)) K         A = TK split hi/lo, B = K^T image
-//   U^T  = V^T (T diag(beta))^T         A = V^T image, B = TV split hi/lo
-// Outputs as k_prep's tensor-core variant: the chain's images [Wd hi | Wd lo | K^T]
-// (Wd = diag(dec) W) and Ud = diag(dec) U in fp32, plus gamma.  Gram and W use 128-row MMAs
+//   W    = (T diag(beta e^G)) K         A = TK split hi/lo, B = K^T (MN-major reading of the K rows)
+//   U^T  = V^T (T diag(beta))^T         A = V^T (MN-major reading of the V rows), B = TV split hi/lo
+// Outputs as k_prep's tensor-core variant: the chain's images [Wd hi | Wd lo | K rows]
+// (Wd = diag(dec) W; the K rows image leaves by bulk copy as soon as it lands) and
+// Ud = diag(dec) U in fp32, plus gamma.  Gram and W use 128-row MMAs
 // of which rows 0..63 are the chunk (the other rows read neighbouring shared memory and
 // are never read back).
 namespace tcp {
@@ -910,9 +907,9 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
                                                     float* __restrict__ gamma_out, WsHeader* __restrict__ hdr) {
   using namespace tcp;
   extern __shared__ __align__(128) unsigned char smp[];
-  unsigned char* R0 = smp;             // K image (C x D), then Xs, then TK hi | TK lo (C x C each)
-  unsigned char* KT = R0 + TILE;       // K^T image (D x C)
-  unsigned char* VT = KT + TILE;       // V^T image (D x C)
+  unsigned char* R0 = smp;             // K rows image (C x D); W's B operand K^T is its MN-major reading
+  unsigned char* KT = R0 + TILE;       // Xs, then TK hi | TK lo (C x C each)
+  unsigned char* VT = KT + TILE;       // V rows image (C x D); U^T's A operand V^T is its MN-major reading
   float* A = reinterpret_cast<float*>(VT + TILE);  // then TV hi | TV lo images
   float* Tm = A + C * CP;
   float* gs = Tm + C * CP;
@@ -922,9 +919,9 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
   float* dec = bk + C;
   uint64_t* bar = reinterpret_cast<uint64_t*>(dec + C);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
-  float* Xs = reinterpret_cast<float*>(R0);
-  unsigned char* TKh = R0;
-  unsigned char* TKl = R0 + C * C * 2;
+  float* Xs = reinterpret_cast<float*>(KT);
+  unsigned char* TKh = KT;
+  unsigned char* TKl = KT + C * C * 2;
   unsigned char* TVh = reinterpret_cast<unsigned char*>(A);
   unsigned char* TVl = TVh + C * C * 2;
   const int t = threadIdx.x, warp = t >> 5;
@@ -1002,7 +999,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
       int r, c0;
       tc::kmajor_piece(t + it * 256, D, r, c0);
       tc::cp_async16(R0 + tc::kmajor_off(r, c0, D), kbj + r * kstride + c0);
-      tc::cp_async16(reinterpret_cast<unsigned char*>(A) + tc::kmajor_off(r, c0, D), vbj + r * vstride + c0);
+      tc::cp_async16(VT + tc::kmajor_off(r, c0, D), vbj + r * vstride + c0);
     }
     if (t < C) {
       tc::cp_async4(gs + t, in.g + (tj + t) * dm.hv + hj);
@@ -1017,11 +1014,18 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     const int64_t item = wi / dm.hv;
     const int h = (int)(wi % dm.hv);
 
-    // 1. this item's K, V, g and beta in shared memory
+    // 1. this item's K, V, g and beta in shared memory; the K rows image leaves at once for
+    // the chain (its K^T operand is the MN-major reading of this image)
+    float* Wo = Wout + (item * dm.hv + h) * (int64_t)prep_w_floats(C, D);
+    unsigned char* img = reinterpret_cast<unsigned char*>(Wo);
     tc::cp_async_wait_all();
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
+    if (t == 0) {
+      tc::bulk_s2g(img + 2 * TILE, R0, TILE);
+      tc::bulk_store_commit();
+    }
     // 2. Gram on the tensor cores while one thread forms G
     if (t == 0) {
       tc::fence_after_sync();
@@ -1038,16 +1042,13 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
         Gs[i] = run;
       }
     }
-    // K^T and V^T images from the row images while the Gram product runs (it reads only R0)
-    tc::transpose_image(KT, R0, D, C);
-    tc::transpose_image(VT, reinterpret_cast<const unsigned char*>(A), D, C);
     __syncthreads();
     if (t < C) {
       bk[t] = __fmul_rn(bs[t], expf(Gs[t]));
       dec[t] = expf(__fsub_rn(Gs[C - 1], Gs[t]));
     }
-    // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs (the V rows staged
-    // there are transposed), by all threads; the readout multiplies in place
+    // beta_i e^{G_i - G_s} (i > s) into A while the Gram product runs, by all threads; the
+    // readout multiplies in place
     tc::decay_matrix64(A, CP, bs, Gs);
     {
       const bool done = tc::mbar_wait(bar, phase);
@@ -1110,20 +1111,17 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     // 5. W = TK K (rows 0..63 of a 128-row MMA) and U^T = V^T TV^T
     if (t == 0) {
       tc::fence_after_sync();
-      const uint32_t sbo = (C / 8) * 128;
-      const uint32_t kt = tc::smem_u32(KT), vt = tc::smem_u32(VT);
-      for (int term = 0; term < 2; ++term) {
-        const uint32_t a = tc::smem_u32(term == 0 ? TKh : TKl);
-        const uint32_t b = tc::smem_u32(term == 0 ? TVh : TVl);
-        for (int kk = 0; kk < C / 16; ++kk) {
-          tc::mma_bf16(tbase + W_COL, tc::make_desc(a + kk * 256, 128, sbo), tc::make_desc(kt + kk * 256, 128, sbo),
-                       tc::idesc_bf16(128, D), (term > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_bf16(tbase + UT_COL, tc::make_desc(vt + kk * 256, 128, sbo), tc::make_desc(b + kk * 256, 128, sbo),
-                       tc::idesc_bf16(128, C), (term > 0 || kk > 0) ? 1u : 0u);
-        }
-      }
+      const tc::Opnd tk = tc::opnd_k(tc::smem_u32(TKh), tc::smem_u32(TKl), C);
+      const tc::Opnd tv = tc::opnd_k(tc::smem_u32(TVh), tc::smem_u32(TVl), C);
+      const tc::Opnd kt = tc::opnd_mn(tc::smem_u32(R0), 0u, D), vt = tc::opnd_mn(tc::smem_u32(VT), 0u, D);
+      const uint32_t iw = tc::idesc_bf16(128, D) | tc::IDESC_B_MN, iu = tc::idesc_bf16(128, C) | tc::IDESC_A_MN;
+      tc::mma_part(tbase + W_COL, tk, false, kt, false, C, iw, false);  // W = TK_hi K + TK_lo K
+      tc::mma_part(tbase + UT_COL, vt, false, tv, false, C, iu, false);  // U^T = V^T (TV_hi + TV_lo)^T
+      tc::mma_part(tbase + W_COL, tk, true, kt, false, C, iw, true);
+      tc::mma_part(tbase + UT_COL, vt, false, tv, true, C, iu, true);
       tc::mma_commit(bar);
     }
+    if (t == 0) tc::bulk_wait_read();  // the K rows image store has read R0 (the next item's lands there)
     {
       const bool done = tc::mbar_wait(bar, phase);
       ok = __syncthreads_and(done) != 0;
@@ -1131,10 +1129,8 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
       phase ^= 1u;
     }
     tc::fence_after_sync();
-    if (li + 1 < count) load_item(li + 1);  // R0, the A region, g and beta are free now
-    float* Wo = Wout + (item * dm.hv + h) * (int64_t)prep_w_floats(C, D);
+    if (li + 1 < count) load_item(li + 1);  // R0, V rows, g and beta are free now
     float* Uo = Uout + ((item * dm.hv + h) * C) * (int64_t)D;
-    unsigned char* img = reinterpret_cast<unsigned char*>(Wo);
     if ((warp & 3) < 2) {  // Wd rows 0..63 -> split image
       const int i = (warp & 3) * 32 + (t & 31);
       const int cbase = (warp >> 2) * 64;
@@ -1159,10 +1155,6 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
           *reinterpret_cast<uint4*>(img + TILE + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
       }
-    } else {  // the other warps meanwhile: the K^T image
-      const int th = (warp >> 2) * 64 + ((warp & 3) - 2) * 32 + (t & 31);  // 0 .. 127
-      for (int q = th; q < (int)(TILE / 16); q += 128)
-        reinterpret_cast<uint4*>(img + 2 * TILE)[q] = reinterpret_cast<const uint4*>(KT)[q];
     }
     {  // Ud[i][e] = dec_i U^T[e][i]: lane e, columns i
       const int e = (warp & 3) * 32 + (t & 31);
@@ -1183,6 +1175,7 @@ __global__ void __launch_bounds__(256, 2) k_prep_tc(Dims dm, TokenArrays in, Pre
     set_error(hdr, GDN_DEVERR_TIMEOUT);
     tc::mbar_wait(bar, phase);  // let the MMA in flight finish before releasing its memory
   }
+  if (t == 0) tc::bulk_wait_all();  // the K rows image stores are complete
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, TMEM_COLS);
