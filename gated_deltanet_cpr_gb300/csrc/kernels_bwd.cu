@@ -1345,6 +1345,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
 
   // ---- phase 1: U^T = Ut^T - S0 W^T; the S0 image also leaves for phase 4
   build_dd4(Ah, Al, S0);
+  SplitTile<false, 64, D> e_first;  // E rows 0..63 for phase 2a
   issue_after(&bar[1], cphase, cpending, [&] {
     mma_split(tb + COL_0, opnd_k(sa_h, sa_l, D), opnd_k(sb_h, sb_l, D), D, I_KK, 3);
     bulk_s2g(s0_hi, Ah, RA / 2);
@@ -1355,6 +1356,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
     float ut[32];  // Ut for the readout, loaded while the product runs
 #pragma unroll
     for (int x = 0; x < 32; ++x) ut[x] = a.b.Ut[ch * CD + (int64_t)(cbase + x) * D + lane_row];
+    e_first.load(E, D, 64);  // phase 2a's first E half, also in flight meanwhile
     run();
     if (ok) {  // U = Ut - (U^T)^T as the U^T image (rows d, K = s): hi in X, lo in B's second
       // half (phase 2a's K image takes the first)
@@ -1382,19 +1384,21 @@ __global__ void __launch_bounds__(256, 2) k_bwd_big_tc(BwdArgs a) {
       cpending = true;
     }
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {  // E image by halves, with S0 at the same positions
+    for (int hh = 0; hh < 2; ++hh) {  // E image by halves, with S0 at the same positions (the
+      // first E half loaded during phase 1)
       SplitTile<false, 64, D> et, st;
-      et.load(E + hh * 64 * D, D, 64);
+      if (hh == 1) et.load(E + 64 * D, D, 64);
       st.load(S0 + hh * 64 * D, D, 64);
+      const SplitTile<false, 64, D>& eh = hh == 0 ? e_first : et;
 #pragma unroll
       for (int it = 0; it < SplitTile<false, 64, D>::ITER; ++it)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) part = __fmaf_rn(et.v[it][e], st.v[it][e], part);
+        for (int e = 0; e < 8; ++e) part = __fmaf_rn(eh.v[it][e], st.v[it][e], part);
       if (hh == 0) {
         if (t == 0) bulk_wait_read();  // the S0 image store has read A
         __syncthreads();
       }
-      et.store(Ah + hh * 16384, Al + hh * 16384);
+      eh.store(Ah + hh * 16384, Al + hh * 16384);
     }
     issue_after(&bar[1], cphase, cpending, [&] {
       mma_split(tb + COL_0, opnd_k(sa_h, sa_l, D), opnd_k(sb_h, sb_h, D), D, I_KK, 2);
