@@ -1969,7 +1969,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const Dims dm = a.dm;
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int64_t c = blockIdx.x;
-  const int h = blockIdx.y, hq = h / (dm.hv / dm.hqk);
+  const int h = blockIdx.y;
   const ChunkRec rec = a.chunks[c];
   if (!in_bounds(a.hdr, rec.tok0 >= 0 && rec.len >= 0 && rec.len <= a.dm.C && (int64_t)rec.tok0 + rec.len <= a.T))
     return;
@@ -1977,8 +1977,7 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   const int64_t tok0 = rec.tok0;
   const int64_t ch = c * dm.hv + h;
   const int64_t CD = (int64_t)C * D;
-  const int64_t kstride = (int64_t)dm.hqk * D, vstride = (int64_t)dm.hv * D;
-  const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.in.q) + tok0 * kstride + (int64_t)hq * D;
+  const int64_t vstride = (int64_t)dm.hv * D;
   const int64_t orow0 = tok0 * vstride + (int64_t)h * D;  // token 0 of this head in [T, Hv, D]
   const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(a.in.v) + orow0;
   unsigned char* gX = reinterpret_cast<unsigned char*>(a.b.L + ch * (int64_t)D * D);  // X hi | lo images
@@ -2151,13 +2150,19 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
   fence_before_sync();
   __syncthreads();
   // ---- products 2: dQ = Pm K -> TMEM 0, dK1 = Pm^T Q -> TMEM 128; K^T, Q^T and Pm^T are the
-  // MN-major readings of the K rows, Q rows and Pm images
+  // MN-major readings of the K rows, Q rows and Pm images.  Meanwhile the row warps take their
+  // q pieces for the dQ readout from the Q rows image (products 3's T^T comes in over it)
+  uint4 qall[8];
   if (ok) {
     issue(false, [&] {
       const Opnd pm_k = opnd_k(sa + 32 * KB, sa + 40 * KB, C), pm_t = opnd_mn(sa + 32 * KB, sa + 40 * KB, C);
       mma_split(tb + 0, pm_k, opnd_mn(sa + 16 * KB, sa + 16 * KB, D), C, idesc_bf16(128, D) | IDESC_B_MN, 2);
       mma_split(tb + 128, pm_t, opnd_mn(sa, sa, D), C, idesc_bf16(128, D) | IDESC_A_MN | IDESC_B_MN, 2);
     });
+    if (rowlane) {
+#pragma unroll
+      for (int x = 0; x < 8; ++x) qall[x] = *reinterpret_cast<const uint4*>(ar + kmajor_off(row, half * 64 + 8 * x, D));
+    }
     if (ok) wait_mma();
   }
   // products 3's operands T^T and dU^T: ready-made images (the prep and big-products kernels
@@ -2168,18 +2173,13 @@ __global__ void __launch_bounds__(256, 2) k_bwd_grad1_tc(BwdArgs a) {
     bulk_g2s(ar + 16 * KB, a.b.L + ch * (int64_t)D * D + D * D / 2, 2 * IMG, &bar[1]);
     cpending = true;
   }
-  // dQ readout (row warps): dO S0 from the staged rows, q from global memory (all of a
-  // thread's q pieces in flight at once)
+  // dQ readout (row warps): dO S0 from the staged rows, q from registers
   if (ok && rowlane) {
     {
       const int i = row;
       const bool live = i < n;
       const float egi = eG[i];
       const unsigned char* dos_s = ar + 48 * KB + i * 512;
-      uint4 qall[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x)
-        qall[x] = live ? *reinterpret_cast<const uint4*>(qb + i * kstride + half * 64 + 8 * x) : zero4;
       float pga = 0.f;
 #pragma unroll
       for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
